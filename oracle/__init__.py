@@ -1,0 +1,189 @@
+"""fp64 CPU oracle for the paged KV-cache path -- TEST INFRASTRUCTURE ONLY.
+
+Only tests/, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+leg of bench.py may import this package.  The CUDA library never loads it,
+and it shares no code with the CUDA library.
+
+``build()`` compiles ``pa_oracle.c`` with gcc into ``_build/libpa_oracle.so``
+next to this file; the ctypes wrappers below take numpy arrays (bf16 data as
+uint16 bit patterns) and return numpy results.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libpa_oracle.so")
+_lib = None
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, force: bool = False) -> str:
+    """Compile the oracle with plain gcc (no vectorisation flags)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= max(
+            os.path.getmtime(src), os.path.getmtime(os.path.join(_HERE, "pa_oracle.h"))):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+                           "-I", _HERE, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+_I32 = ctypes.POINTER(ctypes.c_int32)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+_U16 = ctypes.POINTER(ctypes.c_uint16)
+_F64 = ctypes.POINTER(ctypes.c_double)
+
+
+def _declare(lib):
+    lib.oracle_slot.restype = ctypes.c_int64
+    lib.oracle_slot.argtypes = [_I32, ctypes.c_int32, ctypes.c_int64]
+    lib.oracle_query_start_loc.restype = None
+    lib.oracle_query_start_loc.argtypes = [_I32, ctypes.c_int32, _I32]
+    lib.oracle_slot_mapping.restype = None
+    lib.oracle_slot_mapping.argtypes = [_I32, ctypes.c_int32, _I32, _I32, ctypes.c_int32,
+                                        ctypes.c_int32, _I64]
+    lib.oracle_reshape_and_cache.restype = None
+    lib.oracle_reshape_and_cache.argtypes = [_U16, _U16, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, _U16, _U16, ctypes.c_int32,
+                                             ctypes.c_int32, _I64]
+    lib.oracle_kv_bytes_per_token.restype = ctypes.c_int64
+    lib.oracle_kv_bytes_per_token.argtypes = [ctypes.c_int32] * 4
+    lib.oracle_decode.restype = ctypes.c_int
+    lib.oracle_decode.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
+    lib.oracle_prefill_varlen.restype = ctypes.c_int
+    lib.oracle_prefill_varlen.argtypes = [_F64, _U16, _U16, _U16, _I32, _I32, ctypes.c_int32,
+                                          _I32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
+    lib.oracle_online_softmax.restype = None
+    lib.oracle_online_softmax.argtypes = [_F64, _F64, ctypes.c_int32, ctypes.c_int32, _I32,
+                                          ctypes.c_int32, _F64, _F64, _F64]
+    lib.oracle_merge_partitions.restype = None
+    lib.oracle_merge_partitions.argtypes = [_F64, _F64, _F64, ctypes.c_int32, ctypes.c_int32,
+                                            _F64]
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _p(a: np.ndarray, ty):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ty)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        a = a.view(np.uint16) if a.dtype.itemsize == 2 else a
+    return a
+
+
+class Oracle:
+    """numpy front end of one loaded oracle library (default: the built one)."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    def slot(self, block_table_row, block_size: int, position: int) -> int:
+        row = np.ascontiguousarray(block_table_row, np.int32)
+        return int(self.lib.oracle_slot(_p(row, _I32), block_size, position))
+
+    def query_start_loc(self, q_lens) -> np.ndarray:
+        ql = np.ascontiguousarray(q_lens, np.int32)
+        out = np.zeros(ql.shape[0] + 1, np.int32)
+        self.lib.oracle_query_start_loc(_p(ql, _I32), ql.shape[0], _p(out, _I32))
+        return out
+
+    def slot_mapping(self, block_tables, query_start_loc, seq_lens, block_size: int) -> np.ndarray:
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        qsl = np.ascontiguousarray(query_start_loc, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        out = np.full(int(qsl[-1]), -7, np.int64)
+        self.lib.oracle_slot_mapping(_p(bt, _I32), bt.shape[1], _p(qsl, _I32), _p(sl, _I32),
+                                     sl.shape[0], block_size, _p(out, _I64))
+        return out
+
+    def reshape_and_cache(self, key, value, key_cache, value_cache, slot_mapping):
+        """Return updated copies of the two caches (inputs are not modified)."""
+        k, v = _u16(key), _u16(value)
+        kc, vc = _u16(key_cache).copy(), _u16(value_cache).copy()
+        sm = np.ascontiguousarray(slot_mapping, np.int64)
+        nb, bs, hkv, d = kc.shape
+        assert k.shape == (sm.shape[0], hkv, d)
+        self.lib.oracle_reshape_and_cache(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv, d,
+                                          _p(kc, _U16), _p(vc, _U16), nb, bs, _p(sm, _I64))
+        return kc, vc
+
+    def kv_bytes_per_token(self, num_layers, num_kv_heads, head_dim, elem_bytes) -> int:
+        return int(self.lib.oracle_kv_bytes_per_token(num_layers, num_kv_heads, head_dim,
+                                                      elem_bytes))
+
+    def decode(self, q, key_cache, value_cache, block_tables, seq_lens, scale) -> np.ndarray:
+        q, kc, vc = _u16(q), _u16(key_cache), _u16(value_cache)
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        s, hq, d = q.shape
+        nb, bs, hkv, d2 = kc.shape
+        assert d2 == d and bt.shape[0] == s and sl.shape[0] == s
+        out = np.zeros((s, hq, d), np.float64)
+        rc = self.lib.oracle_decode(_p(out, _F64), _p(q, _U16), _p(kc, _U16), _p(vc, _U16),
+                                    _p(bt, _I32), bt.shape[1], _p(sl, _I32), s, hq, hkv, d, bs,
+                                    float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_decode rejected its arguments ({rc})")
+        return out
+
+    def prefill_varlen(self, q, key_cache, value_cache, query_start_loc, seq_lens,
+                       block_tables, scale) -> np.ndarray:
+        q, kc, vc = _u16(q), _u16(key_cache), _u16(value_cache)
+        qsl = np.ascontiguousarray(query_start_loc, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        tq, hq, d = q.shape
+        nb, bs, hkv, d2 = kc.shape
+        assert d2 == d and int(qsl[-1]) <= tq
+        out = np.zeros((tq, hq, d), np.float64)
+        rc = self.lib.oracle_prefill_varlen(_p(out, _F64), _p(q, _U16), _p(kc, _U16),
+                                            _p(vc, _U16), _p(qsl, _I32), _p(sl, _I32),
+                                            sl.shape[0], _p(bt, _I32), bt.shape[1], hq, hkv, d,
+                                            bs, float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_prefill_varlen rejected its arguments ({rc})")
+        return out
+
+    def online_softmax(self, s, v, bounds):
+        s = np.ascontiguousarray(s, np.float64)
+        v = np.ascontiguousarray(v, np.float64)
+        b = np.ascontiguousarray(bounds, np.int32)
+        out = np.zeros(v.shape[1], np.float64)
+        m = ctypes.c_double()
+        l = ctypes.c_double()
+        self.lib.oracle_online_softmax(_p(s, _F64), _p(v, _F64), s.shape[0], v.shape[1],
+                                       _p(b, _I32), b.shape[0] - 1, _p(out, _F64),
+                                       ctypes.byref(m), ctypes.byref(l))
+        return out, m.value, l.value
+
+    def merge_partitions(self, m_parts, l_parts, o_parts) -> np.ndarray:
+        m = np.ascontiguousarray(m_parts, np.float64)
+        l = np.ascontiguousarray(l_parts, np.float64)
+        o = np.ascontiguousarray(o_parts, np.float64)
+        out = np.zeros(o.shape[1], np.float64)
+        self.lib.oracle_merge_partitions(_p(m, _F64), _p(l, _F64), _p(o, _F64), m.shape[0],
+                                         o.shape[1], _p(out, _F64))
+        return out

@@ -1,0 +1,244 @@
+/*
+ * pa_oracle.c -- plain fp64 CPU oracle for the paged KV-cache path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only tests/, the smoke check in __graft_entry__.py and the
+ * CPU-baseline leg of bench.py use it.  It shares no code, header, table or
+ * helper with the CUDA library; it reads the cache through its own index
+ * arithmetic.
+ *
+ * Every function computes the plain definition of its step, slowly and in
+ * the obvious order, in double precision.  bf16 inputs are widened exactly
+ * (a bf16 value is the top 16 bits of an IEEE binary32).
+ *
+ * Sources (vLLM PagedAttention pages):
+ *   - "vLLM 深度解析（二）：PagedAttention 核心机制", section 2.1 (exact
+ *     attention S = QK^T, P = softmax(S), O = PV), section 2.2 (online
+ *     softmax state (m, l, A)), section 3.1 (logical block, offset,
+ *     physical block, slot), section 3.2.4/3.2.8 (masking past seq_len,
+ *     zeroed V of out-of-context slots), section 3.2.9 (cross-partition
+ *     merge), section 5.2 (query_start_loc packing).
+ *   - "分块预填充与混合批处理", section 11.6 (varlen batch: cu_seqlens_q =
+ *     query_start_loc, seqused_k = seq_lens counts this step's tokens).
+ *   - "vllm 深度解析：一切从 PagedAttention 谈起", BlockTable walk-through
+ *     (slot_id = physical_block * block_size + block_offset) and
+ *     write_to_paged_cache / reshape_and_cache ([num_tokens, heads, dim]
+ *     scattered to [blocks, block_size, heads, dim]).
+ *   - "LLM 推理基础与 vLLM 内部机制", section 2 (KV bytes per token).
+ *
+ * Readings of points the pages leave open (each also listed in the design
+ * notes): cache layout [num_blocks, block_size, num_kv_heads, head_dim];
+ * q head h reads kv head h / (num_heads / num_kv_heads); no epsilon in the
+ * softmax denominator; a negative slot means "do not write"; query i of a
+ * request with q_len new tokens sits at position seq_len - q_len + i and
+ * sees keys 0 .. seq_len - q_len + i (bottom-right causal alignment).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "pa_oracle.h"
+
+/* bf16 -> double, exact: the bf16 bit pattern is the high half of a binary32. */
+static double bf16_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ---- Paged addressing (page 1 section 3.1; page 3 BlockTable walk-through) */
+
+int64_t oracle_slot(const int32_t* block_table_row, int32_t block_size, int64_t position) {
+    int64_t logical_block = position / block_size;
+    int64_t offset = position % block_size;
+    int64_t physical_block = block_table_row[logical_block];
+    return physical_block * block_size + offset;
+}
+
+void oracle_query_start_loc(const int32_t* q_lens, int32_t num_seqs, int32_t* query_start_loc) {
+    /* page 1 section 5.2: consecutive differences are the per-request q_len */
+    query_start_loc[0] = 0;
+    for (int32_t r = 0; r < num_seqs; ++r) query_start_loc[r + 1] = query_start_loc[r] + q_lens[r];
+}
+
+void oracle_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* query_start_loc, const int32_t* seq_lens,
+                         int32_t num_seqs, int32_t block_size, int64_t* slot_mapping) {
+    for (int32_t r = 0; r < num_seqs; ++r) {
+        int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
+        int64_t first_pos = (int64_t)seq_lens[r] - q_len;
+        const int32_t* row = block_tables + (int64_t)r * max_blocks_per_seq;
+        for (int32_t i = 0; i < q_len; ++i)
+            slot_mapping[query_start_loc[r] + i] = oracle_slot(row, block_size, first_pos + i);
+    }
+}
+
+/* ---- reshape_and_cache (page 3 write_to_paged_cache) ------------------- */
+
+void oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, int32_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim,
+                              uint16_t* key_cache, uint16_t* value_cache,
+                              int32_t num_blocks, int32_t block_size,
+                              const int64_t* slot_mapping) {
+    (void)num_blocks;
+    int64_t row = (int64_t)num_kv_heads * head_dim; /* one token's [heads, dim] */
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t x = 0; x < head_dim; ++x) {
+                int64_t dst = ((block * block_size + offset) * num_kv_heads + h) * head_dim + x;
+                int64_t src = i * row + (int64_t)h * head_dim + x;
+                key_cache[dst] = key[src];
+                value_cache[dst] = value[src];
+            }
+    }
+}
+
+/* ---- KV bytes per token (page 1 section 1; page 4 section 2) ----------- */
+
+int64_t oracle_kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t elem_bytes) {
+    return 2LL * num_layers * num_kv_heads * head_dim * elem_bytes;
+}
+
+/* ---- Exact attention for one query row (page 1 section 2.1) ------------
+ * Gathers keys 0 .. n_keys-1 of one request through its block-table row,
+ * scores s_t = scale * <q, k_t>, takes the direct softmax (shift by the
+ * max, exponentiate, sum, divide) and returns O = sum_t p_t v_t.        */
+static void attend_row(double* out, const uint16_t* q_row, const uint16_t* key_cache,
+                       const uint16_t* value_cache, const int32_t* table_row, int64_t n_keys,
+                       int32_t kv_head, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, double scale, double* s) {
+    for (int64_t t = 0; t < n_keys; ++t) {
+        int64_t phys = table_row[t / block_size];
+        int64_t off = t % block_size;
+        const uint16_t* k = key_cache + ((phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
+        double dot = 0.0;
+        for (int32_t x = 0; x < head_dim; ++x) dot += bf16_to_double(q_row[x]) * bf16_to_double(k[x]);
+        s[t] = scale * dot;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n_keys; ++t) if (s[t] > m) m = s[t];
+    double l = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+    for (int32_t x = 0; x < head_dim; ++x) out[x] = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        int64_t phys = table_row[t / block_size];
+        int64_t off = t % block_size;
+        const uint16_t* v = value_cache + ((phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
+        double p = s[t] / l;
+        for (int32_t x = 0; x < head_dim; ++x) out[x] += p * bf16_to_double(v[x]);
+    }
+}
+
+/* ---- Paged decode (page 1 section 3.2; page 3 kernel summary) ----------
+ * out[r][h][:] for the single query row of request r, over all seq_lens[r]
+ * keys.  q is [num_seqs, num_heads, head_dim].                           */
+int oracle_decode(double* out, const uint16_t* q, const uint16_t* key_cache,
+                  const uint16_t* value_cache, const int32_t* block_tables,
+                  int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, double scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+    int32_t group = num_heads / num_kv_heads;
+    int64_t max_len = 0;
+    for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
+    double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!s) return -2;
+    for (int32_t r = 0; r < num_seqs; ++r)
+        for (int32_t h = 0; h < num_heads; ++h)
+            attend_row(out + ((int64_t)r * num_heads + h) * head_dim,
+                       q + ((int64_t)r * num_heads + h) * head_dim, key_cache, value_cache,
+                       block_tables + (int64_t)r * max_blocks_per_seq, seq_lens[r],
+                       h / group, num_kv_heads, head_dim, block_size, scale, s);
+    free(s);
+    return 0;
+}
+
+/* ---- Varlen chunked prefill (page 2 section 11.6; page 1 section 5.2) ---
+ * Request r owns query rows query_start_loc[r] .. query_start_loc[r+1]-1.
+ * With q_len rows and K/V length seq_lens[r], row i sits at position
+ * seq_lens[r] - q_len + i and attends keys 0 .. that position.  A q_len of
+ * 1 is a decode row and sees all seq_lens[r] keys.                       */
+int oracle_prefill_varlen(double* out, const uint16_t* q, const uint16_t* key_cache,
+                          const uint16_t* value_cache, const int32_t* query_start_loc,
+                          const int32_t* seq_lens, int32_t num_seqs,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, double scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+    int32_t group = num_heads / num_kv_heads;
+    int64_t max_len = 0;
+    for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
+    double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!s) return -2;
+    for (int32_t r = 0; r < num_seqs; ++r) {
+        int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
+        int64_t context = (int64_t)seq_lens[r] - q_len;
+        for (int32_t i = 0; i < q_len; ++i) {
+            int64_t row = (int64_t)query_start_loc[r] + i;
+            for (int32_t h = 0; h < num_heads; ++h)
+                attend_row(out + (row * num_heads + h) * head_dim,
+                           q + (row * num_heads + h) * head_dim, key_cache, value_cache,
+                           block_tables + (int64_t)r * max_blocks_per_seq, context + i + 1,
+                           h / group, num_kv_heads, head_dim, block_size, scale, s);
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/* ---- Online softmax over tiles (page 1 section 2.2) --------------------
+ * Scores s[0..n) and values v[n][dv] arrive in tiles [bounds[j],
+ * bounds[j+1]).  State (m, l, A) starts at (-inf, 0, 0); each tile:
+ *   m' = max(m, max s_j); l' = e^{m-m'} l + sum e^{s_j - m'};
+ *   A' = e^{m-m'} A + sum e^{s_j - m'} v_j.
+ * Returns O = A / l and the final (m, l).                                */
+void oracle_online_softmax(const double* s, const double* v, int32_t n, int32_t dv,
+                           const int32_t* bounds, int32_t num_tiles,
+                           double* out, double* m_out, double* l_out) {
+    double m = -INFINITY, l = 0.0;
+    double* A = (double*)calloc((size_t)(dv > 0 ? dv : 1), sizeof(double));
+    for (int32_t j = 0; j < num_tiles; ++j) {
+        int32_t lo = bounds[j], hi = bounds[j + 1];
+        if (hi > n) hi = n;
+        if (lo >= hi) continue;
+        double tile_max = -INFINITY;
+        for (int32_t t = lo; t < hi; ++t) if (s[t] > tile_max) tile_max = s[t];
+        double m_new = m > tile_max ? m : tile_max;
+        double alpha = exp(m - m_new); /* exp(-inf) = 0 on the first tile */
+        l *= alpha;
+        for (int32_t x = 0; x < dv; ++x) A[x] *= alpha;
+        for (int32_t t = lo; t < hi; ++t) {
+            double p = exp(s[t] - m_new);
+            l += p;
+            for (int32_t x = 0; x < dv; ++x) A[x] += p * v[(int64_t)t * dv + x];
+        }
+        m = m_new;
+    }
+    for (int32_t x = 0; x < dv; ++x) out[x] = A[x] / l;
+    *m_out = m;
+    *l_out = l;
+    free(A);
+}
+
+/* ---- Cross-partition merge (page 1 section 3.2.9) ----------------------
+ * Partition p holds its max m_p, exp-sum l_p and normalised output O_p.
+ *   m = max_p m_p;  L = sum_p l_p e^{m_p - m};  O = sum_p O_p l_p e^{m_p - m} / L. */
+void oracle_merge_partitions(const double* m_parts, const double* l_parts, const double* o_parts,
+                             int32_t num_parts, int32_t dv, double* out) {
+    double m = -INFINITY;
+    for (int32_t p = 0; p < num_parts; ++p) if (m_parts[p] > m) m = m_parts[p];
+    double L = 0.0;
+    for (int32_t p = 0; p < num_parts; ++p) L += l_parts[p] * exp(m_parts[p] - m);
+    for (int32_t x = 0; x < dv; ++x) out[x] = 0.0;
+    for (int32_t p = 0; p < num_parts; ++p) {
+        double w = l_parts[p] * exp(m_parts[p] - m) / L;
+        for (int32_t x = 0; x < dv; ++x) out[x] += o_parts[(int64_t)p * dv + x] * w;
+    }
+}

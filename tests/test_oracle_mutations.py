@@ -1,0 +1,79 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case copies oracle/pa_oracle.c, plants one mistake (a dropped term, a
+wrong sign or index, an off-by-one, a swapped operand), compiles the copy
+with gcc into a temporary library, and runs the pin that should notice it.
+The planted copy never leaves the temporary directory and is CPU-only.
+"""
+import os
+
+import pytest
+
+import oracle as oracle_pkg
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "pa_oracle.c")
+
+# (name, original snippet, planted snippet, pins expected to fail)
+MUTATIONS = [
+    ("offset_uses_division", "int64_t offset = position % block_size;",
+     "int64_t offset = position / block_size;", ["slot_examples"]),
+    ("slot_subtracts_offset", "return physical_block * block_size + offset;",
+     "return physical_block * block_size - offset;", ["slot_examples"]),
+    ("qsl_drops_running_sum", "query_start_loc[r + 1] = query_start_loc[r] + q_lens[r];",
+     "query_start_loc[r + 1] = q_lens[r];", ["qsl"]),
+    ("positions_off_by_one", "int64_t first_pos = (int64_t)seq_lens[r] - q_len;",
+     "int64_t first_pos = (int64_t)seq_lens[r] - q_len + 1;", ["positions"]),
+    ("kv_bytes_drops_factor_two", "return 2LL * num_layers", "return 1LL * num_layers",
+     ["kv_bytes"]),
+    ("score_drops_scale", "s[t] = scale * dot;", "s[t] = dot;", ["sdpa_decode"]),
+    ("softmax_adds_epsilon", "double p = s[t] / l;", "double p = s[t] / (l + 1e-6);",
+     ["sdpa_decode"]),
+    ("gqa_wrong_kv_head", "h / group, num_kv_heads, head_dim, block_size, scale, s);\n    free(s);\n    return 0;\n}\n\n/* ---- Varlen",
+     "h % num_kv_heads, num_kv_heads, head_dim, block_size, scale, s);\n    free(s);\n    return 0;\n}\n\n/* ---- Varlen", ["sdpa_decode"]),
+    ("value_row_reversed_in_block",
+     "const uint16_t* v = value_cache + ((phys * block_size + off) * num_kv_heads",
+     "const uint16_t* v = value_cache + ((phys * block_size + (block_size - 1 - off)) * num_kv_heads",
+     ["sdpa_decode"]),
+    ("causal_limit_off_by_one", "context + i + 1,", "context + i,", ["sdpa_prefill"]),
+    ("online_forgets_to_rescale_l", "l *= alpha;", "/* l not rescaled */", ["online"]),
+    ("merge_drops_rescale", "L += l_parts[p] * exp(m_parts[p] - m);", "L += l_parts[p];",
+     ["merge"]),
+    ("writer_shifts_offset", "int64_t offset = slot % block_size;\n        for",
+     "int64_t offset = (slot + 1) % block_size;\n        for", ["writer"]),
+]
+
+PINS = {
+    "slot_examples": lambda o: pins.test_slot_examples_printed_on_pages(o),
+    "qsl": lambda o: pins.test_query_start_loc_printed_on_pages(o),
+    "positions": lambda o: pins.test_varlen_positions_of_mixed_batch(o),
+    "kv_bytes": lambda o: pins.test_kv_bytes_formula_printed_on_pages(o),
+    "sdpa_decode": lambda o: pins.test_decode_matches_torch_sdpa(o, 4, 2, 64, [25, 12, 37, 20]),
+    "sdpa_prefill": lambda o: pins.test_prefill_matches_torch_sdpa_bottom_right_causal(o),
+    "online": lambda o: pins.test_online_softmax_equals_direct(o, "block16"),
+    "merge": lambda o: pins.test_partition_merge_equals_global_softmax(o),
+    "writer": lambda o: pins.test_reshape_and_cache_scatter(o),
+}
+
+
+def test_unplanted_copy_passes_every_pin(tmp_path):
+    lib = oracle_pkg.build(src=SRC, out=str(tmp_path / "liboracle_copy.so"), force=True)
+    o = oracle_pkg.Oracle(oracle_pkg.load(lib))
+    for name, pin in PINS.items():
+        pin(o)
+
+
+@pytest.mark.parametrize("name,orig,planted,expect", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, orig, planted, expect):
+    with open(SRC, encoding="utf-8") as f:
+        text = f.read()
+    assert text.count(orig) == 1, f"snippet for {name} must occur exactly once"
+    src = tmp_path / "pa_oracle.c"
+    src.write_text(text.replace(orig, planted), encoding="utf-8")
+    hdr = os.path.join(os.path.dirname(SRC), "pa_oracle.h")
+    (tmp_path / "pa_oracle.h").write_text(open(hdr, encoding="utf-8").read(), encoding="utf-8")
+    lib = oracle_pkg.build(src=str(src), out=str(tmp_path / "libmutant.so"), force=True)
+    o = oracle_pkg.Oracle(oracle_pkg.load(lib))
+    for pin in expect:
+        with pytest.raises(AssertionError):
+            PINS[pin](o)

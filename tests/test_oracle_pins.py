@@ -1,0 +1,321 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here touches the CUDA library.  Each check compares the oracle with
+something other than itself: a value printed on the pages (tests/golden/),
+a library routine (scipy's softmax, torch's fp64 scaled_dot_product_attention
+on the CPU), a closed form, or an invariance the definition implies.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from conftest import read_golden
+from paged_kv_cache_74_gb300 import workloads as wl
+
+
+def _ints(s):
+    return [int(x) for x in s.split()]
+
+
+# --------------------------------------------------------------- addressing
+
+def test_slot_examples_printed_on_pages(oracle):
+    rows = read_golden("slot_examples.txt")
+    assert len(rows) >= 2
+    for bs, table, pos, slot, _src in rows:
+        assert oracle.slot(_ints(table), int(bs), int(pos)) == int(slot)
+
+
+def test_query_start_loc_printed_on_pages(oracle):
+    for q_lens, qsl, _src in read_golden("query_start_loc.txt"):
+        assert oracle.query_start_loc(_ints(q_lens)).tolist() == _ints(qsl)
+
+
+def test_varlen_positions_of_mixed_batch(oracle):
+    """With an identity block table a slot equals its token position, so the
+    slot mapping exposes which positions the oracle gives the new tokens."""
+    rows = read_golden("varlen_positions.txt")
+    q_lens = [int(r[1]) for r in rows]
+    seq_lens = np.array([int(r[2]) for r in rows], np.int32)
+    qsl = oracle.query_start_loc(q_lens)
+    B = 16
+    nb = -(-int(seq_lens.max()) // B)
+    table = np.tile(np.arange(nb, dtype=np.int32), (len(rows), 1))
+    slots = oracle.slot_mapping(table, qsl, seq_lens, B)
+    for r, row in enumerate(rows):
+        got = slots[qsl[r]:qsl[r + 1]]
+        assert got[0] == int(row[3]) and got[-1] == int(row[4])
+        assert np.all(np.diff(got) == 1)
+
+
+def test_slot_mapping_matches_printed_walkthrough(oracle):
+    """Req1 (25 tokens in P3, P7) and Req2 (12 tokens in P1), one new token
+    each: their slots are 7*16+8 and 1*16+11."""
+    table = np.array([[3, 7], [1, 0]], np.int32)
+    qsl = oracle.query_start_loc([1, 1])
+    slots = oracle.slot_mapping(table, qsl, np.array([25, 12], np.int32), 16)
+    assert slots.tolist() == [120, 27]
+
+
+def test_kv_bytes_formula_printed_on_pages(oracle):
+    for shape, per_tok, tokens, total, _src in read_golden("kv_bytes.txt"):
+        L, hkv, d, b = _ints(shape)
+        got = oracle.kv_bytes_per_token(L, hkv, d, b)
+        assert got == int(per_tok)
+        assert got * int(tokens) == int(total)
+
+
+# ----------------------------------------------------------- softmax algebra
+
+def _direct(s, v):
+    return scipy.special.softmax(s) @ v
+
+
+@pytest.mark.parametrize("split", ["one", "block16", "part512", "random", "whole"])
+def test_online_softmax_equals_direct(oracle, split):
+    rng = np.random.default_rng(11)
+    n, dv = 1500, 64
+    s = rng.standard_normal(n) * 3.0
+    s[700] = 40.0  # a late large score forces a rescale of the running state
+    v = rng.standard_normal((n, dv))
+    if split == "one":
+        bounds = np.arange(n + 1)
+    elif split == "block16":
+        bounds = np.append(np.arange(0, n, 16), n)
+    elif split == "part512":
+        bounds = np.append(np.arange(0, n, 512), n)
+    elif split == "random":
+        cuts = np.sort(rng.choice(np.arange(1, n), size=37, replace=False))
+        bounds = np.concatenate([[0], cuts, [n]])
+    else:
+        bounds = np.array([0, n])
+    out, m, l = oracle.online_softmax(s, v, bounds)
+    np.testing.assert_allclose(out, _direct(s, v), rtol=0, atol=1e-12)
+    assert m == s.max()
+    np.testing.assert_allclose(l, np.exp(s - s.max()).sum(), rtol=1e-13)
+
+
+def test_partition_merge_equals_global_softmax(oracle):
+    rng = np.random.default_rng(12)
+    n, dv, P = 2000, 32, 512
+    s = rng.standard_normal(n) * 4.0
+    v = rng.standard_normal((n, dv))
+    ms, ls, os_ = [], [], []
+    for lo in range(0, n, P):
+        sp, vp = s[lo:lo + P], v[lo:lo + P]
+        ms.append(sp.max())
+        ls.append(np.exp(sp - sp.max()).sum())
+        os_.append(_direct(sp, vp))
+    out = oracle.merge_partitions(np.array(ms), np.array(ls), np.array(os_))
+    np.testing.assert_allclose(out, _direct(s, v), rtol=0, atol=1e-12)
+
+
+def test_partition_merge_single_partition_is_identity(oracle):
+    o = np.arange(8.0)[None, :]
+    out = oracle.merge_partitions(np.array([3.0]), np.array([2.5]), o)
+    np.testing.assert_array_equal(out, o[0])
+
+
+# --------------------------------------------------------------- attention
+
+def _contiguous_workload(seq_lens, hq, hkv, d, seed, q_lens=None):
+    """Each request owns consecutive physical blocks, so its keys form one
+    contiguous range of the pool viewed as [slots, kv_heads, d]."""
+    B = 16
+    seq_lens = np.asarray(seq_lens, np.int32)
+    q_lens = np.ones_like(seq_lens) if q_lens is None else np.asarray(q_lens, np.int32)
+    need = -(-seq_lens // B)
+    tables = np.zeros((len(seq_lens), int(need.max())), np.int32)
+    starts = np.concatenate([[1], 1 + np.cumsum(need)[:-1]])
+    for r in range(len(seq_lens)):
+        tables[r, :need[r]] = np.arange(starts[r], starts[r] + need[r])
+    w = wl.build_workload("contig", seq_lens, q_lens, num_heads=hq, num_kv_heads=hkv,
+                          head_dim=d, block_size=B, num_blocks=1 + int(need.sum()), seed=seed)
+    w.block_tables = tables
+    return w, starts * B
+
+
+def _sdpa(q, k, v, scale, mask=None):
+    """torch fp64 CPU attention; q [Hq, n_q, d], k/v [Hkv, n_k, d] (GQA by
+    repeating each kv head for its group of consecutive q heads)."""
+    g = q.shape[0] // k.shape[0]
+    k = k.repeat_interleave(g, dim=0)
+    v = v.repeat_interleave(g, dim=0)
+    return torch.nn.functional.scaled_dot_product_attention(
+        q[None], k[None], v[None], attn_mask=mask, scale=scale)[0]
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens", [(4, 2, 64, [25, 12, 37, 20]),
+                                           (8, 1, 128, [1, 16, 17, 100]),
+                                           (6, 6, 64, [3, 48]),
+                                           (16, 2, 128, [129, 33])])
+def test_decode_matches_torch_sdpa(oracle, hq, hkv, d, lens):
+    w, first_slot = _contiguous_workload(lens, hq, hkv, d, seed=21)
+    t = wl.make_tensors(w)
+    out = oracle.decode(t.q.view(torch.int16).numpy(), t.key_cache.view(torch.int16).numpy(),
+                        t.value_cache.view(torch.int16).numpy(), w.block_tables, w.seq_lens,
+                        w.scale)
+    kf = t.key_cache.double().reshape(-1, hkv, d)
+    vf = t.value_cache.double().reshape(-1, hkv, d)
+    for r, L in enumerate(lens):
+        k = kf[first_slot[r]:first_slot[r] + L].permute(1, 0, 2)
+        v = vf[first_slot[r]:first_slot[r] + L].permute(1, 0, 2)
+        ref = _sdpa(t.q[r].double()[:, None, :], k, v, w.scale)[:, 0, :]
+        np.testing.assert_allclose(out[r], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_single_token_returns_its_value(oracle):
+    w, first = _contiguous_workload([1, 1], 4, 2, 64, seed=22)
+    t = wl.make_tensors(w)
+    out = oracle.decode(t.q.view(torch.int16).numpy(), t.key_cache.view(torch.int16).numpy(),
+                        t.value_cache.view(torch.int16).numpy(), w.block_tables, w.seq_lens,
+                        w.scale)
+    for r in range(2):
+        v0 = t.value_cache.double().reshape(-1, 2, 64)[first[r]]
+        np.testing.assert_array_equal(out[r], v0.repeat_interleave(2, dim=0).numpy())
+
+
+def test_decode_identical_keys_average_values(oracle):
+    w, first = _contiguous_workload([37], 2, 1, 64, seed=23)
+    t = wl.make_tensors(w)
+    kc = t.key_cache.clone()
+    kc[:] = kc[1, 0]  # every key equal -> uniform weights
+    out = oracle.decode(t.q.view(torch.int16).numpy(), kc.view(torch.int16).numpy(),
+                        t.value_cache.view(torch.int16).numpy(), w.block_tables, w.seq_lens,
+                        w.scale)
+    vals = t.value_cache.double().reshape(-1, 1, 64)[first[0]:first[0] + 37, 0]
+    np.testing.assert_allclose(out[0, 0], vals.mean(0).numpy(), rtol=0, atol=1e-13)
+
+
+def test_decode_relocation_invariance(oracle):
+    """Moving physical blocks (and their contents) leaves outputs unchanged."""
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w)
+    args = lambda kc, vc, bt: oracle.decode(t.q.view(torch.int16).numpy(),
+                                           kc.view(torch.int16).numpy(),
+                                           vc.view(torch.int16).numpy(), bt, w.seq_lens, w.scale)
+    base = args(t.key_cache, t.value_cache, w.block_tables)
+    perm = np.random.default_rng(5).permutation(w.num_blocks)  # new id of each block
+    kc2 = torch.empty_like(t.key_cache)
+    vc2 = torch.empty_like(t.value_cache)
+    kc2[torch.from_numpy(perm)] = t.key_cache
+    vc2[torch.from_numpy(perm)] = t.value_cache
+    moved = args(kc2, vc2, perm[w.block_tables].astype(np.int32))
+    np.testing.assert_array_equal(base, moved)
+
+
+def test_prefill_matches_torch_sdpa_bottom_right_causal(oracle):
+    lens, qls = [40, 33, 16, 70], [7, 1, 16, 70]
+    hq, hkv, d = 4, 2, 64
+    w, first = _contiguous_workload(lens, hq, hkv, d, seed=24, q_lens=qls)
+    t = wl.make_tensors(w)
+    out = oracle.prefill_varlen(t.q.view(torch.int16).numpy(),
+                                t.key_cache.view(torch.int16).numpy(),
+                                t.value_cache.view(torch.int16).numpy(), w.query_start_loc,
+                                w.seq_lens, w.block_tables, w.scale)
+    kf = t.key_cache.double().reshape(-1, hkv, d)
+    vf = t.value_cache.double().reshape(-1, hkv, d)
+    for r, (L, ql) in enumerate(zip(lens, qls)):
+        k = kf[first[r]:first[r] + L].permute(1, 0, 2)
+        v = vf[first[r]:first[r] + L].permute(1, 0, 2)
+        q = t.q[w.query_start_loc[r]:w.query_start_loc[r + 1]].double().permute(1, 0, 2)
+        # bottom-right causal: query i (of ql) may see keys j <= L - ql + i
+        i = torch.arange(ql)[:, None]
+        j = torch.arange(L)[None, :]
+        mask = j <= (L - ql) + i
+        ref = _sdpa(q, k, v, w.scale, mask=mask).permute(1, 0, 2)
+        np.testing.assert_allclose(out[w.query_start_loc[r]:w.query_start_loc[r + 1]],
+                                   ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_square_chunk_is_plain_causal(oracle):
+    """With no cached context (q_len == seq_len) the mask is the usual
+    top-left causal one, which torch builds itself with is_causal."""
+    w, first = _contiguous_workload([48], 2, 2, 64, seed=25, q_lens=[48])
+    t = wl.make_tensors(w)
+    out = oracle.prefill_varlen(t.q.view(torch.int16).numpy(),
+                                t.key_cache.view(torch.int16).numpy(),
+                                t.value_cache.view(torch.int16).numpy(), w.query_start_loc,
+                                w.seq_lens, w.block_tables, w.scale)
+    k = t.key_cache.double().reshape(-1, 2, 64)[first[0]:first[0] + 48].permute(1, 0, 2)
+    v = t.value_cache.double().reshape(-1, 2, 64)[first[0]:first[0] + 48].permute(1, 0, 2)
+    q = t.q.double().permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None],
+                                                           is_causal=True, scale=w.scale)[0]
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_decode_rows_equal_decode(oracle):
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w)
+    a = oracle.decode(t.q.view(torch.int16).numpy(), t.key_cache.view(torch.int16).numpy(),
+                      t.value_cache.view(torch.int16).numpy(), w.block_tables, w.seq_lens,
+                      w.scale)
+    b = oracle.prefill_varlen(t.q.view(torch.int16).numpy(),
+                              t.key_cache.view(torch.int16).numpy(),
+                              t.value_cache.view(torch.int16).numpy(), w.query_start_loc,
+                              w.seq_lens, w.block_tables, w.scale)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_decode_ignores_nan_outside_context(oracle):
+    """Out-of-context slots, the null block and free blocks may hold NaN."""
+    w = wl.tiny_decode()
+    clean = wl.make_tensors(w)
+    dirty = wl.make_tensors(w, poison=True)
+    assert torch.isnan(dirty.key_cache.float()).any()
+    run = lambda t: oracle.decode(t.q.view(torch.int16).numpy(),
+                                  t.key_cache.view(torch.int16).numpy(),
+                                  t.value_cache.view(torch.int16).numpy(), w.block_tables,
+                                  w.seq_lens, w.scale)
+    np.testing.assert_array_equal(run(clean), run(dirty))
+
+
+# ------------------------------------------------------------ slot writer
+
+def test_reshape_and_cache_scatter(oracle):
+    """Identity tables make slot == position, so token i must land in row
+    slot of the pool viewed as [num_blocks * block_size, kv_heads, d]; all
+    other rows, and tokens with a negative slot, leave the pool untouched."""
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w)
+    n = 6
+    gen = torch.Generator().manual_seed(3)
+    key = torch.randn((n, 2, 64), generator=gen).to(torch.bfloat16)
+    val = torch.randn((n, 2, 64), generator=gen).to(torch.bfloat16)
+    slots = np.array([5, 100, -1, 511, 17, -3], np.int64)
+    kc, vc = oracle.reshape_and_cache(key.view(torch.int16).numpy(), val.view(torch.int16).numpy(),
+                                      t.key_cache.view(torch.int16).numpy(),
+                                      t.value_cache.view(torch.int16).numpy(), slots)
+    kc0 = t.key_cache.view(torch.int16).numpy().view(np.uint16).reshape(-1, 2, 64)
+    vc0 = t.value_cache.view(torch.int16).numpy().view(np.uint16).reshape(-1, 2, 64)
+    kc, vc = kc.reshape(-1, 2, 64), vc.reshape(-1, 2, 64)
+    written = {int(s): i for i, s in enumerate(slots) if s >= 0}
+    for s in range(kc.shape[0]):
+        if s in written:
+            i = written[s]
+            np.testing.assert_array_equal(kc[s], key[i].view(torch.int16).numpy().view(np.uint16))
+            np.testing.assert_array_equal(vc[s], val[i].view(torch.int16).numpy().view(np.uint16))
+        else:
+            np.testing.assert_array_equal(kc[s], kc0[s])
+            np.testing.assert_array_equal(vc[s], vc0[s])
+
+
+def test_reshape_then_slot_mapping_places_token_where_decode_reads_it(oracle):
+    """Writing each request's last token through the slot mapping and then
+    decoding is the same as decoding a pool that already held those keys."""
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w)
+    slots = oracle.slot_mapping(w.block_tables, w.query_start_loc, w.seq_lens, w.block_size)
+    kc, vc = oracle.reshape_and_cache(t.key.view(torch.int16).numpy(),
+                                      t.value.view(torch.int16).numpy(),
+                                      t.key_cache.view(torch.int16).numpy(),
+                                      t.value_cache.view(torch.int16).numpy(), slots)
+    for r in range(w.num_seqs):
+        L = int(w.seq_lens[r])
+        phys = w.block_tables[r, (L - 1) // 16]
+        np.testing.assert_array_equal(kc[phys, (L - 1) % 16],
+                                      t.key[r].view(torch.int16).numpy().view(np.uint16))
