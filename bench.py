@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode step on one GB300 (or N independent replicas).
+
+One step = the whole hot path for one decode batch: the slot mapping of
+the batch's new tokens, their reshape_and_cache write, and paged decode
+attention (split-KV partitions + merge).  Inputs are seeded synthetic
+tensors of the named workload, resident in HBM; L2 is flushed (a 512 MiB
+write) before every step, outside the timed events.
+
+Prints ONE JSON line (rank 0).  `value` is KV GB/s: the step's algorithmic
+bytes (each distinct K/V token the attention must read once, plus q, out,
+the block-table entries, and the new tokens' K/V read and written) over
+the device time of the step.  `--impl reference` times the fp64 CPU oracle
+on the same workload instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_74_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s & µs/call vs 8 TB/s HBM roofline (1×GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one paged_decode_kernel
+# launch (full workload, from the committed ncu summary), valid only while
+# the kernel source is unchanged (sha256 of decode.cu at capture time).
+PROFILED_TRAFFIC: dict = {}
+
+
+# ----------------------------------------------------------------- helpers
+
+def decode_src_sha() -> str:
+    p = os.path.join(ROOT, "paged_kv_cache_74_gb300", "csrc", "decode.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w: wl.Workload) -> dict:
+    """Bytes the decode step must move at least once.
+
+    KV: every distinct (physical block, offset) token slot read by some
+    request, times 2 (K and V) * kv_heads * head_dim * 2 bytes; a prefix
+    shared by several requests counts once.  Plus q read, out written,
+    block-table entries and seq_lens read, and the write of the new tokens
+    (read K/V rows, write them, read the slots).
+    """
+    per_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    slots = set()
+    logical = 0
+    table_entries = 0
+    for r in range(w.num_seqs):
+        L = int(w.seq_lens[r])
+        logical += L
+        nb = -(-L // w.block_size)
+        table_entries += nb
+        for j in range(nb):
+            phys = int(w.block_tables[r, j])
+            n = min(w.block_size, L - j * w.block_size)
+            slots.add((phys, n))
+    # distinct tokens: per physical block the largest prefix any request reads
+    best = {}
+    for phys, n in slots:
+        best[phys] = max(best.get(phys, 0), n)
+    unique = sum(best.values())
+    kv = unique * per_tok
+    qo = 2 * w.total_q * w.num_heads * w.head_dim * 2
+    meta = table_entries * 4 + w.num_seqs * 4 * 2
+    write = w.total_q * (2 * per_tok + 8) + w.num_seqs * 4 * 2
+    return {"kv_unique_tokens": unique, "kv_logical_tokens": logical, "kv_bytes": kv,
+            "decode_bytes": kv + qo + meta, "step_bytes": kv + qo + meta + write,
+            "kv_bytes_per_token": per_tok}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1].split()[0]))
+                smax.append(float(r[2].split()[0]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if "Active" in v and "Not" not in v:
+                    reasons.add(name)
+        load = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate_over_ranks(local_seconds: float, local_bytes: float, world: int) -> tuple:
+    """Max of the per-rank times and sum of the per-rank bytes (whole job)."""
+    if world == 1:
+        return local_seconds, local_bytes
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_74_gb300 as pa
+    pa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.NAMED[args.workload]()
+    t = wl.make_tensors(w, device=dev)
+    ab = algorithmic_bytes(w)
+    stream = torch.cuda.current_stream(dev)
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
+                                                   w.head_dim, w.max_seq_len), dev)
+    out = torch.empty_like(t.q)
+    slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    max_blocks = -(-w.max_seq_len // w.block_size)
+    max_parts = -(-max_blocks // part_blocks_guess(w))
+
+    def step():
+        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, w.block_size,
+                                w.num_blocks, w.total_q, out=slots)
+        pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+
+    def attend():
+        pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens, w.max_seq_len,
+                  w.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.add_(1)
+        step()
+        attend()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.add_(1)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    local_s = sum(step_ms) / 1e3
+    tot_s, tot_bytes = aggregate_over_ranks(local_s, ab["step_bytes"] * K, world)
+    value = tot_bytes / tot_s / 1e9
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    n_launch = 3 + (1 if max_parts > 1 else 0)
+
+    # e2e through the public API with pinned host buffers (H2D inputs, D2H out)
+    e2e = run_e2e(pa, w, t, dev, stream, flush, args, ab, world)
+
+    peak, peak_src = measured_peaks()
+    achieved = ab["decode_bytes"] / dec_avg_s / 1e9
+    prof = PROFILED_TRAFFIC.get(w.name)
+    traffic = prof["bytes"] if prof and prof.get("src_sha") == decode_src_sha() else None
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(tot_s / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, seeded block permutations)",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "max_seq_len": w.max_seq_len, "kv_unique_tokens": ab["kv_unique_tokens"],
+                   "step": "slot_mapping + reshape_and_cache + decode",
+                   "l2": "flushed before every step (512 MiB write, outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": round(dec_avg_s * 1e6, 2),
+        "decode_kv_gbs": round(ab["kv_bytes"] / dec_avg_s / 1e9, 2),
+        "wall_ms_per_step": round(wall / K * 1e3, 4),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged_decode_kernel + merge)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab["decode_bytes"]},
+        "e2e": e2e,
+        "gpu_launches": n_launch * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, t, ab)
+    if args.extra and rank == 0:
+        res["extra"] = {name: extra_decode(pa, name, dev, flush) for name in args.extra}
+    return res, rank
+
+
+def part_blocks_guess(w):
+    """Partition size the library picks (mirrors choose_partition_blocks)."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    max_blocks = -(-w.max_seq_len // 16)
+    pb = 32
+    while pb > 8 and w.num_seqs * w.num_kv_heads * -(-max_blocks // pb) < 4 * sms:
+        pb //= 2
+    return pb
+
+
+def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):
+    pin = lambda x: x.cpu().pin_memory()
+    h = {"q": pin(t.q), "key": pin(t.key), "value": pin(t.value), "bt": pin(t.block_tables),
+         "sl": pin(t.seq_lens), "qsl": pin(t.query_start_loc)}
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    out_h = torch.empty(t.q.shape, dtype=torch.bfloat16).pin_memory()
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
+                                                   w.head_dim, w.max_seq_len), dev)
+    out = torch.empty_like(t.q)
+    slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def once():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        pa.compute_slot_mapping(d["bt"], d["qsl"], d["sl"], w.block_size, w.num_blocks,
+                                w.total_q, out=slots)
+        pa.reshape_and_cache(d["key"], d["value"], t.key_cache, t.value_cache, slots)
+        pa.decode(d["q"], t.key_cache, t.value_cache, d["bt"], d["sl"], w.max_seq_len, w.scale,
+                  out=out, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        flush.add_(1)
+        once()
+    torch.cuda.synchronize(dev)
+    K = max(1, args.steps // 2)
+    ts = []
+    for _ in range(K):
+        flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        once()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    tot_s, tot_bytes = aggregate_over_ranks(sum(ts), ab["step_bytes"] * K, world)
+    return {"value": round(tot_bytes / tot_s / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(tot_s / K * 1e3, 5), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def extra_decode(pa, name, dev, flush, reps=20):
+    """Decode-only timing of another named workload (context for the line)."""
+    w = wl.NAMED[name]()
+    t = wl.make_tensors(w, device=dev)
+    ab = algorithmic_bytes(w)
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
+                                                   w.head_dim, w.max_seq_len), dev)
+    out = torch.empty_like(t.q)
+    call = lambda: pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
+                             w.max_seq_len, w.scale, out=out, workspace=ws)
+    for _ in range(3):
+        flush.add_(1)
+        call()
+    ms = []
+    for _ in range(reps):
+        flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    s = statistics.median(ms) / 1e3
+    peak, _ = measured_peaks()
+    res = {"us_per_call": round(s * 1e6, 2), "kv_gbs": round(ab["kv_bytes"] / s / 1e9, 2),
+           "decode_gbs": round(ab["decode_bytes"] / s / 1e9, 2),
+           "frac_of_measured_peak": round(ab["decode_bytes"] / s / 1e9 / peak, 4),
+           "kv_unique_tokens": ab["kv_unique_tokens"], "kv_logical_tokens": ab["kv_logical_tokens"]}
+    del t
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def _oracle_sample(w, kc, vc, q, rows):
+    from oracle import Oracle
+    o = Oracle()
+    t0 = time.perf_counter()
+    o.decode(q[rows], kc, vc, w.block_tables[rows], w.seq_lens[rows], w.scale)
+    return time.perf_counter() - t0
+
+
+def _sample_bytes(w, rows):
+    sub = wl.Workload(w.name, w.seq_lens[rows], w.q_lens[rows],
+                      np.concatenate([[0], np.cumsum(w.q_lens[rows])]).astype(np.int32),
+                      w.block_tables[rows], w.num_heads, w.num_kv_heads, w.head_dim,
+                      w.block_size, w.num_blocks, w.scale, w.seed, w.shared_blocks)
+    return algorithmic_bytes(sub)["decode_bytes"]
+
+
+def cpu_baseline(w, t, ab, budget_rows=None):
+    """The oracle, as it stands, on one thread of the host: one decode of a
+    bounded sample: the whole batch once (a few seconds at these sizes)."""
+    bits = lambda x: x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    kc, vc, q = bits(t.key_cache), bits(t.value_cache), bits(t.q)
+    rows = budget_rows if budget_rows is not None else _rows_for_fraction(w, 1.0)
+    secs = _oracle_sample(w, kc, vc, q, rows)
+    b = _sample_bytes(w, rows)
+    return {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle decode of requests {rows[0]}..{rows[-1]} ({len(rows)} of "
+                      f"{w.num_seqs}) of {w.name}, fp64, single thread, {secs:.2f} s"}
+
+
+def _rows_for_fraction(w, frac):
+    lens = w.seq_lens.astype(np.int64)
+    c = np.cumsum(lens)
+    n = int(np.searchsorted(c, frac * c[-1])) + 1
+    return np.arange(min(max(n, 1), w.num_seqs))
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None, rank
+    w = wl.NAMED[args.workload]()
+    t = wl.make_tensors(w, device="cpu")
+    bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kc, vc, q = bits(t.key_cache), bits(t.value_cache), bits(t.q)
+    rows = _rows_for_fraction(w, 0.02)
+    b = _sample_bytes(w, rows)
+    for _ in range(args.warmup):
+        _oracle_sample(w, kc, vc, q, rows)
+    secs = [_oracle_sample(w, kc, vc, q, rows) for _ in range(args.steps)]
+    tot = sum(secs)
+    v = b * args.steps / tot / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_rows": len(rows), "num_seqs": w.num_seqs},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"oracle decode of the first {len(rows)} requests of "
+                                       f"{w.name} per step (fp64, single thread)"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}, rank
+
+
+# -------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_decode_b64", choices=sorted(wl.NAMED))
+    ap.add_argument("--extra", nargs="*", default=["long_ctx_decode_8x32k",
+                                                    "prefix_shared_decode_b256"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        res, rank = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+        res, rank = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

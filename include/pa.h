@@ -1,0 +1,214 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache attention library (libpa.so) for one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The library implements the hot path that the vLLM PagedAttention pages
+ * describe:
+ *   - pa_reshape_and_cache   write new K/V tokens into their cache slots
+ *                            ("vllm 深度解析：一切从 PagedAttention 谈起",
+ *                            write_to_paged_cache -> reshape_and_cache);
+ *   - pa_compute_slot_mapping  slot = block_table[r][pos / B] * B + pos % B
+ *                            ("vLLM 深度解析（二）：PagedAttention 核心机制",
+ *                            section 3.1, BlockTable.compute_slot_mapping);
+ *   - pa_decode              paged decode attention with online softmax and
+ *                            a split-KV partition + merge pass (same page,
+ *                            sections 2.2, 3.2 and 3.3);
+ *   - pa_prefill_varlen      mixed chunked-prefill + decode batch driven by
+ *                            query_start_loc / seq_lens ("分块预填充与混合批处理",
+ *                            section 11.6; first page, section 5.2).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pointers.  Every tensor pointer is a DEVICE pointer owned by the caller.
+ *   The library allocates no device memory and keeps no per-call state;
+ *   scratch space is a caller-provided `workspace` sized by the matching
+ *   *_workspace_size() call.  Tensor pointers must be 16-byte aligned.
+ * Element types.  q, key, value, out and the caches are bf16 (IEEE
+ *   binary16-brain, stored as 16-bit patterns); block tables, seq_lens and
+ *   query_start_loc are int32; slot mappings are int64.
+ * Cache layout (NHD).  key_cache and value_cache are each a contiguous
+ *   [num_blocks, block_size, num_kv_heads, head_dim] array, i.e. a
+ *   [num_blocks * block_size, num_kv_heads, head_dim] array indexed by slot
+ *   (the combined [2, num_blocks, block_size, num_kv_heads, head_size]
+ *   cache of the page "vllm 深度解析：一切从 PagedAttention 谈起", split
+ *   into its K and V halves).  Block 0 is conventionally the null block.
+ * GQA.  num_heads must be a multiple of num_kv_heads; q head h reads kv head
+ *   h / (num_heads / num_kv_heads).
+ * Supported sizes.  head_dim 64 or 128; block_size 16; num_heads /
+ *   num_kv_heads between 1 and 16.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *   default stream).  Calls only enqueue work; they never synchronise.
+ *   A write through pa_reshape_and_cache must be enqueued before the
+ *   attention call that reads it, on the same stream (or ordered by events).
+ * Errors.  Arguments are validated on the host before anything is
+ *   launched; an invalid call returns a non-zero pa_status and enqueues
+ *   nothing.  PA_ERR_CUDA means a launch was refused by the CUDA runtime.
+ *   Device data (block ids, slots, lengths) is range-checked inside the
+ *   kernels: an out-of-range value is never dereferenced, the affected
+ *   output is left unspecified, and an error code is recorded in the
+ *   device status word (see pa_device_status below) when one is supplied.
+ * Device status word.  The first 16 bytes of every workspace hold an
+ *   int32[4] status record: [0] error code (0 = none, else a pa_device_error),
+ *   [1] request index, [2] detail (the offending value), [3] reserved.  The
+ *   kernels write it only on error (first error wins); the caller zeroes
+ *   it (e.g. cudaMemsetAsync) whenever it wants a fresh record.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* null or misaligned pointer, bad size or stride */
+    PA_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, block_size, group size */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than *_workspace_size() */
+    PA_ERR_CUDA = 4          /* the CUDA runtime refused a launch or query */
+} pa_status;
+
+typedef enum pa_device_error {
+    PA_DEV_OK = 0,
+    PA_DEV_BAD_SLOT = 1,        /* slot >= num_blocks * block_size (write skipped) */
+    PA_DEV_BAD_BLOCK_ID = 2,    /* block id outside [0, num_blocks) (tile read as zeros) */
+    PA_DEV_BAD_SEQ_LEN = 3,     /* seq_len < 1, > max_seq_len or > max_blocks_per_seq * block_size */
+    PA_DEV_BAD_QUERY_LEN = 4,   /* q_len > seq_len, > max_query_len, or rows beyond total_q */
+    PA_DEV_WAIT_TIMEOUT = 5     /* a pipeline wait gave up (internal error); the CTA stopped */
+} pa_device_error;
+
+/* Human-readable name of a pa_status value (static string, never NULL). */
+const char* pa_status_string(int status);
+
+/* ABI version of this header; bumped on any incompatible change. */
+#define PA_ABI_VERSION 1
+int pa_abi_version(void);
+
+/*
+ * pa_reshape_and_cache -- scatter new K/V tokens into the paged cache.
+ * ("vllm 深度解析：一切从 PagedAttention 谈起": write_to_paged_cache calls
+ * reshape_and_cache, which turns [num_tokens, heads, dim] into
+ * [blocks, block_size, heads, dim]; "vLLM 深度解析（二）", section 3.1:
+ * slot_mapping decides where each new token's K/V is written.)
+ *
+ *   key, value    [num_tokens, num_kv_heads, head_dim] bf16; token i starts
+ *                 key_stride (value_stride) ELEMENTS after token i-1; the
+ *                 heads of one token are contiguous.  Strides must be
+ *                 multiples of 8 elements (16 bytes).
+ *   key_cache, value_cache   the cache (layout above); written in place.
+ *   slot_mapping  [num_tokens] int64: token i goes to slot s =
+ *                 slot_mapping[i], i.e. block s / block_size, offset
+ *                 s % block_size.  s < 0 skips the token (padding).
+ *                 s >= num_blocks * block_size is a device error: skipped
+ *                 and recorded in *device_status.
+ *   device_status optional int32[4] device status record (NULL = none).
+ * Bit-exact copy; num_tokens == 0 is a no-op.  Two tokens with the same
+ * slot race (the last writer is unspecified).
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               int64_t key_stride, int64_t value_stride,
+                               void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t num_blocks,
+                               int32_t* device_status, void* stream);
+
+/*
+ * pa_compute_slot_mapping -- slots of this step's new tokens.
+ * ("vLLM 深度解析（二）", section 3.1: logical_block = pos / B, offset =
+ * pos % B, slot = block_table[request][logical_block] * B + offset.)
+ * Request r owns flattened tokens query_start_loc[r] .. query_start_loc[r+1]-1;
+ * its i-th new token sits at position seq_lens[r] - q_len + i (seq_lens
+ * counts this step's tokens).  slot_mapping has total_tokens entries; a
+ * token whose position or block id is out of range gets slot -1 and a
+ * device error is recorded in *device_status (optional, may be NULL).
+ */
+pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* query_start_loc, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t block_size, int32_t num_blocks,
+                                  int32_t* device_status, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
+ * sizes (>= 256: the status record plus the split-KV partials).  The
+ * same partition_tokens must be passed to pa_decode.  Returns 0 for
+ * arguments pa_decode would reject.
+ */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_seq_len,
+                                int32_t partition_tokens);
+
+/*
+ * pa_decode -- paged decode attention, one query row per request.
+ * ("vLLM 深度解析（二）", section 2.2 online softmax state (m, l, A);
+ * section 3.2 block-table gather, masking of tokens >= seq_len and zeroed
+ * out-of-context V; sections 3.2.7, 3.2.9 and 3.3 split-KV partitions and
+ * their merge m = max m_j, L = sum l_j e^{m_j - m}, O = sum O_j l_j e^{m_j - m} / L.)
+ *
+ *   out           [num_seqs, num_heads, head_dim] bf16 (written)
+ *   q             [num_seqs, num_heads, head_dim] bf16
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32; entries past
+ *                 ceil(seq_len / block_size) are never read
+ *   seq_lens      [num_seqs] int32, each in [1, max_seq_len]
+ *   max_seq_len   host-side upper bound of seq_lens (sizes the grid; no
+ *                 device-to-host read happens)
+ *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim))
+ *   partition_tokens  tokens per split-KV partition: 0 lets the library
+ *                 choose; otherwise a positive multiple of block_size
+ *   workspace     >= pa_decode_workspace_size(...) bytes, 256-byte aligned
+ * out[r, h] = sum_t softmax_t(scale * q[r,h] . k_t) v_t over the
+ * seq_lens[r] keys of request r (exact attention, fp32 accumulation,
+ * rounded once to bf16).
+ */
+pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale,
+                    int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs
+ * (status record, decode-row partials).  Returns 0 for invalid arguments.
+ */
+size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len);
+
+/*
+ * pa_prefill_varlen -- attention for a mixed batch of chunked-prefill and
+ * decode requests packed by query_start_loc.
+ * ("分块预填充与混合批处理", section 11.6: cu_seqlens_q = query_start_loc,
+ * seqused_k = seq_lens, which includes this step's tokens, and the block
+ * table gives the physical blocks; "vLLM 深度解析（二）", section 5.2:
+ * rows with q_len > 1 are prefill, q_len == 1 decode.)
+ *
+ *   out, q          [total_q, num_heads, head_dim] bf16
+ *   query_start_loc [num_seqs + 1] int32, non-decreasing, [0] = 0,
+ *                   [num_seqs] = total_q
+ *   seq_lens        [num_seqs] int32 K/V lengths (>= q_len of the request)
+ *   max_query_len, max_seq_len  host-side upper bounds
+ * Query i (0 <= i < q_len) of request r sits at position
+ * seq_lens[r] - q_len + i and attends keys 0 .. that position (causal,
+ * aligned to the end of the context).  Rows with q_len > 1 run on the
+ * tcgen05 tensor-core prefill tile; rows with q_len == 1 run the decode
+ * kernel; requests with q_len == 0 produce no rows.  K/V of this step's
+ * tokens must already be in the cache (pa_reshape_and_cache first).
+ */
+pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
+                            const void* value_cache, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                            int32_t max_query_len, int32_t max_seq_len,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

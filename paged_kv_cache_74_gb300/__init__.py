@@ -1,0 +1,15 @@
+"""Paged KV-cache attention for one NVIDIA GB300 (sm_103a).
+
+The compute path is libpa.so (hand-written CUDA behind a C ABI, see
+include/pa.h); this package holds its build script, a thin ctypes binding
+with the same names, and the seeded synthetic workload generator used by
+the tests and the benchmark.
+"""
+from ._binding import (ABI_SYMBOLS, DEVICE_ERRORS, PAError, compute_slot_mapping, decode,
+                       decode_workspace_size, device_status, library_path, load_library,
+                       new_workspace, prefill_varlen, prefill_workspace_size, reshape_and_cache)
+from .builder import build
+
+__all__ = ["ABI_SYMBOLS", "DEVICE_ERRORS", "PAError", "build", "compute_slot_mapping", "decode",
+           "decode_workspace_size", "device_status", "library_path", "load_library",
+           "new_workspace", "prefill_varlen", "prefill_workspace_size", "reshape_and_cache"]

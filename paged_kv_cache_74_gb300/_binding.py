@@ -1,0 +1,216 @@
+"""ctypes binding of libpa.so -- argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; these wrappers
+only check tensor dtypes and shapes, turn torch tensors into device
+pointers, pass torch's current CUDA stream, and raise on a non-zero
+pa_status.  There is no fallback: if the library is missing, or a call is
+made on tensors that are not on a CUDA device, they raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import builder as _build
+
+_lock = threading.Lock()
+_lib = None
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+DEVICE_ERRORS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "bad seq_len",
+                 4: "bad query length", 5: "wait timeout"}
+ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
+               "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
+               "pa_prefill_workspace_size", "pa_prefill_varlen")
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed: {msg}")
+        self.status = status
+
+
+_i32, _i64, _sz, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+
+def _declare(lib):
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_abi_version.restype = ctypes.c_int
+    lib.pa_abi_version.argtypes = []
+    lib.pa_reshape_and_cache.restype = ctypes.c_int
+    lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _i32,
+                                         _i32, _i32, _vp, _vp]
+    lib.pa_compute_slot_mapping.restype = ctypes.c_int
+    lib.pa_compute_slot_mapping.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
+                                            _vp, _vp]
+    lib.pa_decode_workspace_size.restype = _sz
+    lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                              _i32, _i32, _f32, _i32, _vp, _sz, _vp]
+    lib.pa_prefill_workspace_size.restype = _sz
+    lib.pa_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    lib.pa_prefill_varlen.restype = ctypes.c_int
+    lib.pa_prefill_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
+                                      _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]
+    return lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: str | None = None):
+    """Load libpa.so (it must have been built; see build.py).  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or _build.LIB
+            if not os.path.exists(p):
+                raise RuntimeError(f"libpa.so not built at {p}; run paged_kv_cache_74_gb300.build()")
+            lib = _declare(ctypes.CDLL(p))
+            if path is not None:
+                return lib
+            _lib = lib
+        return _lib
+
+
+def _check(fn, status):
+    if status != PA_OK:
+        raise PAError(fn, status, load_library().pa_status_string(status).decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _cuda(name, t, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _contig(name, t, dtype):
+    _cuda(name, t, dtype)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None):
+    """Write key/value [T, Hkv, d] (token stride may exceed Hkv*d) into the
+    caches at slot_mapping[T] (int64; negative = skip)."""
+    _cuda("key", key, torch.bfloat16)
+    _cuda("value", value, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("slot_mapping", slot_mapping, torch.int64)
+    nb, bs, hkv, d = key_cache.shape
+    T = slot_mapping.shape[0]
+    for name, t in (("key", key), ("value", value)):
+        if tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, {hkv}, {d}] with contiguous heads")
+    lib = load_library()
+    _check("pa_reshape_and_cache", lib.pa_reshape_and_cache(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache),
+        _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, _ptr(status), _stream()))
+
+
+def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, num_blocks,
+                         total_tokens, out=None, status=None):
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("query_start_loc", query_start_loc, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    if out is None:
+        out = torch.empty(total_tokens, dtype=torch.int64, device=block_tables.device)
+    _contig("slot_mapping", out, torch.int64)
+    lib = load_library()
+    _check("pa_compute_slot_mapping", lib.pa_compute_slot_mapping(
+        _ptr(out), total_tokens, _ptr(block_tables), block_tables.shape[1], _ptr(query_start_loc),
+        _ptr(seq_lens), seq_lens.shape[0], block_size, num_blocks, _ptr(status), _stream()))
+    return out
+
+
+def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
+                          partition_tokens=0):
+    return int(load_library().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                       max_seq_len, partition_tokens))
+
+
+def new_workspace(nbytes, device):
+    """A zeroed workspace (the status record starts clean)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def decode(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale, out=None,
+           workspace=None, partition_tokens=0):
+    """Paged decode attention; q [S, Hq, d] -> out [S, Hq, d] (bf16)."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    S, hq, d = q.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    if d2 != d or value_cache.shape != key_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(S, hq, hkv, d, max_seq_len, partition_tokens),
+                                  q.device)
+    lib = load_library()
+    _check("pa_decode", lib.pa_decode(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
+        float(scale), int(partition_tokens), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def prefill_workspace_size(num_seqs, total_q, num_heads, num_kv_heads, head_dim, max_seq_len):
+    return int(load_library().pa_prefill_workspace_size(num_seqs, total_q, num_heads, num_kv_heads,
+                                                        head_dim, max_seq_len))
+
+
+def prefill_varlen(q, key_cache, value_cache, query_start_loc, seq_lens, block_tables,
+                   max_query_len, max_seq_len, scale, out=None, workspace=None):
+    """Mixed chunked-prefill + decode attention; q [total_q, Hq, d]."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("query_start_loc", query_start_loc, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    _contig("block_tables", block_tables, torch.int32)
+    tq, hq, d = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    S = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(prefill_workspace_size(S, tq, hq, hkv, d, max_seq_len), q.device)
+    lib = load_library()
+    _check("pa_prefill_varlen", lib.pa_prefill_varlen(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(query_start_loc),
+        _ptr(seq_lens), S, tq, int(max_query_len), int(max_seq_len), _ptr(block_tables),
+        block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), _ptr(workspace),
+        workspace.numel(), _stream()))
+    return out
+
+
+def device_status(workspace_or_status):
+    """Read the int32[4] device status record (synchronises the stream)."""
+    t = workspace_or_status
+    rec = t[:16].view(torch.int32) if t.dtype == torch.uint8 else t[:4]
+    return [int(x) for x in rec.cpu()]

@@ -1,0 +1,111 @@
+// cache_write.cu -- the two writes that precede attention in a step:
+//
+//  * slot mapping ("vLLM 深度解析（二）：PagedAttention 核心机制", section 3.1):
+//      logical block = pos / B, offset = pos % B,
+//      slot = block_table[r][logical block] * B + offset,
+//    for the new tokens of each request, which sit at positions
+//    seq_len - q_len .. seq_len - 1 ("分块预填充与混合批处理", section 11.6:
+//    seq_lens counts this step's tokens);
+//  * reshape_and_cache ("vllm 深度解析：一切从 PagedAttention 谈起",
+//    write_to_paged_cache): token i's [kv_heads, head_dim] K and V rows are
+//    copied to slot slot_mapping[i] of the [slots, kv_heads, head_dim] cache.
+//
+// Both are pure data movement.  The cache write gives each token one warp;
+// lanes move 16-byte chunks, so each token's K and V rows (2 KB each at 8 kv
+// heads x 128) are read and written with fully coalesced vector accesses.
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWriteWarps = 8;
+
+__global__ void __launch_bounds__(kWriteWarps * 32)
+reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                         int64_t key_stride_chunks, int64_t value_stride_chunks,
+                         uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                         const int64_t* __restrict__ slot_mapping, int num_tokens,
+                         int row_chunks, int64_t num_slots, int32_t* status) {
+  const int token = blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (token >= num_tokens) return;
+  const int64_t slot = slot_mapping[token];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (lane == 0) record_error(status, PA_DEV_BAD_SLOT, token, static_cast<int>(slot));
+    return;
+  }
+  const uint4* ks = key + token * key_stride_chunks;
+  const uint4* vs = value + token * value_stride_chunks;
+  uint4* kd = key_cache + slot * row_chunks;
+  uint4* vd = value_cache + slot * row_chunks;
+  for (int c = lane; c < row_chunks; c += 32) {
+    const uint4 kv = __ldg(ks + c);
+    const uint4 vv = __ldg(vs + c);
+    kd[c] = kv;
+    vd[c] = vv;
+  }
+}
+
+// One CTA per request; its threads cover the request's new tokens.
+__global__ void __launch_bounds__(128)
+slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
+                    const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
+                    const int32_t* __restrict__ query_start_loc,
+                    const int32_t* __restrict__ seq_lens, int block_size, int num_blocks,
+                    int32_t* status) {
+  const int r = blockIdx.x;
+  const int q0 = query_start_loc[r];
+  const int q1 = query_start_loc[r + 1];
+  const int seq_len = seq_lens[r];
+  const int q_len = q1 - q0;
+  const int64_t first_pos = static_cast<int64_t>(seq_len) - q_len;
+  const int32_t* row = block_tables + static_cast<int64_t>(r) * max_blocks_per_seq;
+  for (int i = threadIdx.x; i < q_len; i += blockDim.x) {
+    const int64_t flat = static_cast<int64_t>(q0) + i;
+    if (flat < 0 || flat >= total_tokens) {
+      if (i == 0) record_error(status, PA_DEV_BAD_QUERY_LEN, r, q1);
+      continue;
+    }
+    const int64_t pos = first_pos + i;
+    const int64_t logical = pos >= 0 ? pos / block_size : -1;
+    int64_t slot = -1;
+    if (logical < 0 || logical >= max_blocks_per_seq) {
+      record_error(status, PA_DEV_BAD_SEQ_LEN, r, seq_len);
+    } else {
+      const int32_t phys = row[logical];
+      if (phys < 0 || phys >= num_blocks)
+        record_error(status, PA_DEV_BAD_BLOCK_ID, r, phys);
+      else
+        slot = static_cast<int64_t>(phys) * block_size + (pos - logical * block_size);
+    }
+    slot_mapping[flat] = slot;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
+                                     int64_t value_stride, void* key_cache, void* value_cache,
+                                     const int64_t* slot_mapping, int num_tokens, int row_elems,
+                                     int64_t num_slots, int32_t* status, cudaStream_t stream) {
+  const int grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
+  reshape_and_cache_kernel<<<grid, kWriteWarps * 32, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), key_stride / 8,
+      value_stride / 8, static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
+      slot_mapping, num_tokens, row_elems / 8, num_slots, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, int num_seqs, int block_size,
+                                int num_blocks, int32_t* status, cudaStream_t stream) {
+  slot_mapping_kernel<<<num_seqs, 128, 0, stream>>>(slot_mapping, total_tokens, block_tables,
+                                                    max_blocks_per_seq, query_start_loc, seq_lens,
+                                                    block_size, num_blocks, status);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

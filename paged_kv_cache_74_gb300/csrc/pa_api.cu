@@ -1,0 +1,308 @@
+// pa_api.cu -- the extern "C" entry points declared in include/pa.h:
+// host-side validation, TMA tensor-map encoding, the split-KV partition
+// choice, workspace carving and kernel dispatch.  No entry point allocates
+// device memory or synchronises.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int sm_count_current_device() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Tokens per split-KV partition, in blocks.  The pages' kernel uses 512
+// tokens; smaller partitions are used only when the batch would otherwise
+// leave the GPU's SMs short of CTAs.
+int choose_partition_blocks(int num_seqs, int num_kv_heads, int max_seq_len, int partition_tokens) {
+  if (partition_tokens > 0) return partition_tokens / kBlockSize;
+  const int max_blocks = ceil_div(max_seq_len, kBlockSize);
+  int sms = sm_count_current_device();
+  if (sms <= 0) sms = 148;
+  const int64_t target = 4LL * sms;
+  int pb = 32;
+  while (pb > 8 && static_cast<int64_t>(num_seqs) * num_kv_heads * ceil_div(max_blocks, pb) < target)
+    pb /= 2;
+  return pb;
+}
+
+// The K or V cache as a 3-D tensor [slots][kv_heads][head_dim] (innermost
+// first for TMA: {head_dim, kv_heads, slots}); one box is one (block, kv head)
+// tile of 16 tokens x head_dim.
+bool make_cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                    int head_dim) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DecodeLayout {
+  int partition_blocks = 0;
+  int max_parts = 0;
+  size_t ml_offset = 0, o_offset = 0, total = 0;
+};
+
+DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                           int max_seq_len, int partition_tokens) {
+  DecodeLayout L;
+  L.partition_blocks = choose_partition_blocks(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
+  L.max_parts = ceil_div(ceil_div(max_seq_len, kBlockSize), L.partition_blocks);
+  L.ml_offset = kWorkspaceHeader;
+  size_t total = kWorkspaceHeader;
+  if (L.max_parts > 1) {
+    const size_t n = static_cast<size_t>(num_seqs) * num_heads * L.max_parts;
+    total = align_up(total + n * 2 * sizeof(float), 256);
+    L.o_offset = total;
+    total += n * head_dim * sizeof(float);
+  }
+  L.total = align_up(total, 256);
+  return L;
+}
+
+// Shared shape checks of the attention entry points.
+pa_status check_attention_shape(int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks) {
+  if (num_kv_heads < 1 || num_heads < 1 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+  if (num_blocks < 1 || static_cast<int64_t>(num_blocks) * kBlockSize > 0x7fffffffLL)
+    return PA_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (decode_gmax(num_heads / num_kv_heads) == 0) return PA_ERR_UNSUPPORTED;
+  if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+// Validation shared by pa_decode and the decode rows of pa_prefill_varlen.
+pa_status check_decode_args(const void* out, const void* q, const void* key_cache,
+                            const void* value_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale) {
+  pa_status st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size, num_blocks);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535) return num_seqs < 0 ? PA_ERR_INVALID : PA_ERR_UNSUPPORTED;
+  if (!out || !q || !key_cache || !value_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PA_ERR_INVALID;
+  if (max_blocks_per_seq < 1 || max_seq_len < 1 ||
+      static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return PA_ERR_INVALID;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID;
+  return PA_OK;
+}
+
+pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, const void* value_cache,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                             int32_t num_seqs, int32_t total_q, int32_t max_seq_len,
+                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t num_blocks, float scale, const DecodeLayout& L,
+                             void* workspace, cudaStream_t stream) {
+  CUtensorMap kmap, vmap;
+  if (!make_cache_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
+      !make_cache_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
+    return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.part_ml = L.max_parts > 1 ? reinterpret_cast<float*>(ws + L.ml_offset) : nullptr;
+  a.part_o = L.max_parts > 1 ? reinterpret_cast<float*>(ws + L.o_offset) : nullptr;
+  a.status = reinterpret_cast<int32_t*>(ws);
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_heads / num_kv_heads;
+  a.partition_blocks = L.partition_blocks;
+  a.max_parts = L.max_parts;
+  a.max_seq_len = max_seq_len;
+  a.num_blocks = num_blocks;
+  a.total_q = total_q;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_decode(a, kmap, vmap, head_dim, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape not supported by this build";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: the CUDA runtime refused the call";
+    default: return "unknown pa_status";
+  }
+}
+
+int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
+                               int64_t value_stride, void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID;
+  if (head_dim < 8 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (block_size < 1) return PA_ERR_INVALID;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(slot_mapping, 8) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+    return PA_ERR_INVALID;
+  const cudaError_t e = launch_reshape_and_cache(
+      key, value, key_stride, value_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      static_cast<int>(row), static_cast<int64_t>(num_blocks) * block_size, device_status,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* query_start_loc, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t block_size, int32_t num_blocks,
+                                  int32_t* device_status, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || block_size < 1 || num_blocks < 1 ||
+      max_blocks_per_seq < 1)
+    return PA_ERR_INVALID;
+  if (num_seqs == 0 || total_tokens == 0) return PA_OK;
+  if (!slot_mapping || !block_tables || !query_start_loc || !seq_lens) return PA_ERR_INVALID;
+  if (!aligned(slot_mapping, 8) || !aligned(block_tables, 4) || !aligned(query_start_loc, 4) ||
+      !aligned(seq_lens, 4) || (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (num_seqs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_slot_mapping(slot_mapping, total_tokens, block_tables,
+                                            max_blocks_per_seq, query_start_loc, seq_lens, num_seqs,
+                                            block_size, num_blocks, device_status,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
+  if (num_seqs < 0 || max_seq_len < 1 || num_kv_heads < 1 || num_heads < 1 ||
+      num_heads % num_kv_heads != 0 || (head_dim != 64 && head_dim != 128))
+    return 0;
+  if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return 0;
+  return decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
+      .total;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale,
+                    int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale);
+  if (st != PA_OK) return st;
+  if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
+                                       partition_tokens);
+  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
+                            num_kv_heads, head_dim, num_blocks, scale, L, workspace,
+                            static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len) {
+  if (total_q < 0) return 0;
+  return pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
+}
+
+pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
+                            const void* value_cache, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                            int32_t max_query_len, int32_t max_seq_len,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale);
+  if (st != PA_OK) return st;
+  if (!query_start_loc || !aligned(query_start_loc, 4) || total_q < 0 || max_query_len < 0 ||
+      max_query_len > max_seq_len)
+    return PA_ERR_INVALID;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  if (max_query_len > 1) return PA_ERR_UNSUPPORTED;  // tensor-core tile not built yet
+  const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
+  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, query_start_loc, num_seqs, total_q, max_seq_len, num_heads,
+                            num_kv_heads, head_dim, num_blocks, scale, L, workspace,
+                            static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// pa_internal.h -- launch parameters shared by the library's translation
+// units (host and device).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kBlockSize = 16;        // tokens per KV block (the pages' default)
+constexpr int kWorkspaceHeader = 256; // status record + padding at the start of a workspace
+
+// Decode work: one CTA per (partition, kv head, request).  A partition is a
+// run of `partition_blocks` consecutive logical blocks of one request.
+struct DecodeArgs {
+  __nv_bfloat16* out;               // [rows, num_heads, D]
+  const __nv_bfloat16* q;           // [rows, num_heads, D]
+  const int32_t* block_tables;      // [num_seqs, max_blocks_per_seq]
+  const int32_t* seq_lens;          // [num_seqs]
+  const int32_t* query_start_loc;   // nullptr: row r = request r; else only q_len == 1 rows
+  float* part_o;                    // [num_seqs, num_heads, max_parts, D] normalised partial O
+  float* part_ml;                   // [num_seqs, num_heads, max_parts, 2] (max in log2 units, sum)
+  int32_t* status;                  // device status record (may be null)
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int group;                        // num_heads / num_kv_heads
+  int partition_blocks;
+  int max_parts;
+  int max_seq_len;
+  int num_blocks;
+  int total_q;                      // rows of q / out
+  float scale_log2;                 // softmax scale * log2(e)
+};
+
+// Launchers (decode.cu).  Return a cudaError_t from the launch.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          int head_dim, cudaStream_t stream);
+// Smallest group size the decode kernel is instantiated for that covers g.
+int decode_gmax(int group);
+
+// Cache writes (cache_write.cu).
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
+                                     int64_t value_stride, void* key_cache, void* value_cache,
+                                     const int64_t* slot_mapping, int num_tokens, int row_elems,
+                                     int64_t num_slots, int32_t* status, cudaStream_t stream);
+cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, int num_seqs, int block_size,
+                                int num_blocks, int32_t* status, cudaStream_t stream);
+
+}  // namespace pa

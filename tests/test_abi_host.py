@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports
+every symbol include/pa.h declares, and invalid calls are rejected on the
+host before anything is launched (no GPU needed: every pointer below is a
+fake, and validation fails before any device access)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_74_gb300 as pa
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert set(declared_functions()) == set(pa.ABI_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define PA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.pa_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.pa_status_string(s).decode().startswith("PA_")
+    assert lib.pa_status_string(99) == b"unknown pa_status"
+
+
+A = 0x10000  # a 256-byte-aligned fake device address (never dereferenced)
+
+
+def decode_call(lib, **kw):
+    args = dict(out=A, q=A, kc=A, vc=A, bt=A, mb=4, sl=A, ns=2, msl=64, hq=8, hkv=2, d=128, bs=16,
+                nb=32, scale=0.125, pt=0, ws=A, wsb=1 << 20)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.pa_decode(vp(args["out"]), vp(args["q"]), vp(args["kc"]), vp(args["vc"]),
+                         vp(args["bt"]), args["mb"], vp(args["sl"]), args["ns"], args["msl"],
+                         args["hq"], args["hkv"], args["d"], args["bs"], args["nb"], args["scale"],
+                         args["pt"], vp(args["ws"]), args["wsb"], vp(0))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(out=0), 1), (dict(q=0), 1), (dict(kc=0), 1), (dict(bt=0), 1), (dict(sl=0), 1),
+    (dict(q=A + 8), 1), (dict(out=A + 2), 1), (dict(bt=A + 2), 1),
+    (dict(hq=6, hkv=4), 1), (dict(hkv=0), 1), (dict(ns=-1), 1), (dict(nb=0), 1),
+    (dict(msl=65), 1), (dict(mb=0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(pt=24), 1), (dict(pt=-16), 1),
+    (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=32, hkv=2), 2), (dict(ns=70000), 2),
+    (dict(ws=0), 3), (dict(wsb=16), 3),
+    (dict(ws=A + 16), 1),
+])
+def test_decode_rejects_invalid_arguments(lib, kw, expect):
+    assert decode_call(lib, **kw) == expect
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert decode_call(lib, ns=0) == 0
+
+
+def test_workspace_size(lib):
+    small = lib.pa_decode_workspace_size(4, 4, 2, 64, 37, 0)
+    assert small >= 256 and small % 256 == 0
+    # forced 16-token partitions over 32K tokens need partials for 2048 partitions
+    big = lib.pa_decode_workspace_size(8, 32, 8, 128, 32768, 16)
+    assert big >= 8 * 32 * 2048 * (128 + 2) * 4
+    assert lib.pa_decode_workspace_size(4, 6, 4, 64, 37, 0) == 0   # Hq % Hkv != 0
+    assert lib.pa_decode_workspace_size(4, 4, 2, 80, 37, 0) == 0   # head_dim
+    assert lib.pa_decode_workspace_size(4, 4, 2, 64, 37, 20) == 0  # not a block multiple
+
+
+def test_reshape_and_cache_validation(lib):
+    vp = ctypes.c_void_p
+    call = lambda **k: lib.pa_reshape_and_cache(
+        vp(k.get("key", A)), vp(k.get("value", A)), k.get("ks", 1024), k.get("vs", 1024),
+        vp(k.get("kc", A)), vp(k.get("vc", A)), vp(k.get("sm", A)), k.get("n", 4), 8, 128, 16, 64,
+        vp(0), vp(0))
+    assert call(n=0) == 0                       # nothing to do, nothing launched
+    assert call(key=0) == 1
+    assert call(key=A + 4) == 1
+    assert call(ks=1000) == 1                   # stride below one token row
+    assert call(ks=1028) == 1                   # not a multiple of 8 elements
+    assert call(sm=A + 4) == 1
+    assert call(n=-1) == 1
+
+
+def test_slot_mapping_validation(lib):
+    vp = ctypes.c_void_p
+    call = lambda **k: lib.pa_compute_slot_mapping(
+        vp(k.get("out", A)), k.get("n", 4), vp(k.get("bt", A)), 4, vp(k.get("qsl", A)),
+        vp(k.get("sl", A)), k.get("ns", 2), 16, 32, vp(0), vp(0))
+    assert call(ns=0) == 0
+    assert call(out=0) == 1
+    assert call(out=A + 4) == 1
+    assert call(qsl=A + 2) == 1
+    assert call(n=-3) == 1
+
+
+def test_prefill_validation(lib):
+    vp = ctypes.c_void_p
+    call = lambda **k: lib.pa_prefill_varlen(
+        vp(A), vp(A), vp(A), vp(A), vp(k.get("qsl", A)), vp(A), 2, k.get("tq", 9),
+        k.get("mql", 8), k.get("msl", 64), vp(A), 4, 8, 2, k.get("d", 128), 16, 32, 0.1, vp(A),
+        1 << 20, vp(0))
+    assert call(qsl=0) == 1
+    assert call(mql=65) == 1
+    assert call(d=80) == 2
+    assert call(tq=0) == 0
