@@ -38,76 +38,60 @@ namespace {
 constexpr float kNegBig = -1e30f;      // finite stand-in for -inf in running maxima
 constexpr float kRescaleSlack = 8.0f;  // log2 units
 
+// Work split of one warp over one 16-token block (see the file comment).
 template <int D, int GMAX>
 struct DecodeCfg {
-  static constexpr int T = (GMAX * D / 64 > 8) ? GMAX * D / 64 : 8;  // lanes per token
-  static constexpr int NG = 32 / T;                                   // token groups per warp
-  static constexpr int NT = kBlockSize / NG;                          // tokens per group per block
-  static constexpr int CPL = D / 8 / T;                               // 16-byte chunks per lane
-  static constexpr int EL = CPL * 8;                                  // head_dim elements per lane
-  static constexpr int V = NT * GMAX;                                 // scores per group per block
-  static constexpr int VPL = V >= T ? V / T : 1;                      // scores per lane after scatter
-  static constexpr int REP = V >= T ? 1 : T / V;                      // lanes holding the same score
-  static constexpr int LPH = T / GMAX;                                // lanes per head in a group
-  static constexpr int NC = 4;                                        // consumer warps
-  static constexpr int STAGES = 8;
-  static constexpr int TILE = kBlockSize * D * 2;                     // bytes of one tile
+  static constexpr int T = (D == 128 && GMAX >= 4) ? 16 : 8;  // lanes per token
+  static constexpr int NG = 32 / T;                            // token groups per warp
+  static constexpr int NT = kBlockSize / NG;                   // tokens per group per block
+  static constexpr int CPL = D / 8 / T;                        // 16-byte chunks per lane per row
+  static constexpr int EL = CPL * 8;                           // head_dim elements per lane
+  static constexpr int EP = EL / 2;                            // ... as float2 pairs
+  static constexpr int SB = (NT * GMAX > 32) ? 32 / GMAX : NT; // tokens per sub-batch
+  static constexpr int NSB = NT / SB;
+  static constexpr int V = SB * GMAX;                          // partial scores per lane per sub-batch
+  static constexpr int VPL = V >= T ? V / T : 1;               // whole scores per lane after the sum
+  static constexpr int REP = V >= T ? 1 : T / V;               // lanes holding the same score
+  static constexpr int LPH = T / GMAX;                         // lanes of a group per head
+  static constexpr int CH = V / 4 > 0 ? V / 4 : 1;              // 16-byte chunks per transpose row
+  static constexpr int NC = 4;                                 // consumer warps
+  static constexpr int MINB = GMAX * EL > 32 ? 2 : 3;          // CTAs per SM the registers allow
+  static constexpr int TILE = kBlockSize * D * 2;              // bytes of one (block, kv head) tile
+  // The partial-score transpose (32 rows of V floats) reuses the warp's own
+  // K tile once its q.k products are done, when it fits and no later
+  // sub-batch still needs K; otherwise each warp gets a dedicated buffer.
+  static constexpr bool XPOSE_IN_K = 32 * CH * 16 <= TILE && NSB == 1;
+  static constexpr int XPOSE = XPOSE_IN_K ? 0 : 32 * CH * 16;
+  static constexpr int STAGES = D == 128 ? 8 : 16;             // a multiple of NC (see below)
+  static constexpr int SCRATCH = XPOSE + NG * V * 4;           // per warp: transpose + weights
+  static constexpr int SCRATCH_AL = (SCRATCH + 127) / 128 * 128;
+  static constexpr int COMB = NC * GMAX * (D + 2) * 4;         // cross-warp merge (aliases the ring)
   static constexpr int SMEM_RING = STAGES * 2 * TILE;
-  static constexpr int SMEM_COMB = NC * GMAX * (D + 2) * 4;
-  static constexpr int SMEM = SMEM_RING + SMEM_COMB + 2 * STAGES * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int SMEM_SCR = NC * SCRATCH_AL;
+  static constexpr int SMEM = SMEM_RING + SMEM_SCR + 2 * STAGES * 8 + 16 + 1024;  // + align slack
   static constexpr int THREADS = (NC + 1) * 32;
-  static_assert(CPL >= 1 && GMAX <= T, "unsupported decode shape");
+  // Block i goes to stage i % STAGES and to warp i % NC.  With STAGES a
+  // multiple of NC a stage is only ever used by one warp, so when a warp
+  // waits on a stage the barrier is at most one phase behind and the
+  // parity wait is unambiguous.
+  static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
+  static_assert(COMB <= SMEM_RING, "merge buffer must fit in the ring");
+  static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
+                "shared memory must allow MINB CTAs per SM");
+  static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V <= 32, "unsupported decode shape");
 };
 
-// Butterfly reduce-scatter inside a group of T lanes: on entry x[0..V) are
-// this lane's partial sums; on exit x[0..VPL) are complete sums of entries
-// (li * V / T) .. + VPL - 1.  When V < T the last steps are all-reduces.
-template <int V, int T>
-__device__ __forceinline__ void group_reduce_scatter(float (&x)[V], int li) {
-#pragma unroll
-  for (int b = T / 2; b >= 1; b >>= 1) {
-    const int n = (V * 2 * b / T) >= 1 ? (V * 2 * b / T) : 1;  // entries held before this step
-    if (n >= 2) {
-      const bool up = (li & b) != 0;
-#pragma unroll
-      for (int j = 0; j < n / 2; ++j) {
-        const float send = up ? x[j] : x[j + n / 2];
-        const float keep = up ? x[j + n / 2] : x[j];
-        x[j] = keep + __shfl_xor_sync(0xffffffffu, send, b);
-      }
-    } else {
-      x[0] += __shfl_xor_sync(0xffffffffu, x[0], b);
-    }
-  }
-}
-
-// Inverse of the scatter steps: on entry x[0..VPL) hold this lane's entries;
-// on exit x[0..V) hold all V entries of the group, in order.
-template <int V, int T>
-__device__ __forceinline__ void group_all_gather(float (&x)[V], int li) {
-#pragma unroll
-  for (int b = 1; b < T; b <<= 1) {
-    if (V * b >= T) {
-      const int h = V * b / T;  // entries held before this step
-      const bool up = (li & b) != 0;
-#pragma unroll
-      for (int j = 0; j < h; ++j) {
-        const float mine = x[j];
-        const float other = __shfl_xor_sync(0xffffffffu, mine, b);
-        x[j] = up ? other : mine;
-        x[j + h] = up ? mine : other;
-      }
-    }
-  }
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 template <int D, int GMAX>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(DecodeCfg<D, GMAX>::THREADS, DecodeCfg<D, GMAX>::MINB)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using C = DecodeCfg<D, GMAX>;
-  const int part = blockIdx.x;
-  const int kvh = blockIdx.y;
+  const int kvh = blockIdx.x;
+  const int part = blockIdx.y;
   const int seq = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -138,9 +122,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // TMA destinations want an aligned base: round up inside the (padded) allocation.
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  float* comb_o = reinterpret_cast<float*>(smem + C::SMEM_RING);  // [NC][GMAX][D]
-  float* comb_ml = comb_o + C::NC * GMAX * D;                      // [NC][GMAX][2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_RING + C::SMEM_COMB);
+  uint8_t* scratch = smem + C::SMEM_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + C::SMEM_SCR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * C::STAGES);
   const uint32_t ring_s = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
@@ -208,43 +191,46 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int g = lane / C::T;
   const int li = lane % C::T;
   const int head0 = kvh * a.group;
+  uint8_t* my_scratch = scratch + warp * C::SCRATCH_AL;
+  float* pbuf = reinterpret_cast<float*>(my_scratch + C::XPOSE);  // [NG][V] weights
 
-  float qf[GMAX][C::EL];
+  // q of every head of the group over this lane's slice of head_dim, as
+  // float2 pairs, pre-scaled by scale * log2(e).
+  float2 q2[GMAX][C::EP];
   {
     const __nv_bfloat16* qrow = a.q + (static_cast<size_t>(row) * a.num_heads + head0) * D;
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
 #pragma unroll
       for (int j = 0; j < C::CPL; ++j) {
-        float f[8];
-        if (h < a.group) {
-          unpack8(__ldg(reinterpret_cast<const uint4*>(qrow + h * D + (li + C::T * j) * 8)), f);
-        } else {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (h < a.group) w = __ldg(reinterpret_cast<const uint4*>(qrow + h * D + (li + C::T * j) * 8));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2(ws[e]);
+          q2[h][j * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qf[h][j * 8 + e] = f[e] * a.scale_log2;
       }
     }
   }
 
-  float o[GMAX][C::EL];
+  float2 o2[GMAX][C::EP];
 #pragma unroll
   for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-    for (int e = 0; e < C::EL; ++e) o[h][e] = 0.f;
+    for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
   float my_m = kNegBig;  // running max (log2 units) of this lane's head, same on all its lanes
   float my_l = 0.f;      // this lane's share of the running exp-sum
   const int idx0 = (li * C::V) / C::T;
-  const int my_h = idx0 / C::NT;
-  const int my_k0 = idx0 % C::NT;
+  const int my_h = idx0 / C::SB;
+  const int my_k0 = idx0 % C::SB;
   const bool head_real = my_h < a.group;
   const bool l_owner = (li % C::REP) == 0;
 
   for (int i = warp; i < nblk; i += C::NC) {
     const int s = i % C::STAGES;
-    // Every branch below is taken by the whole warp (shuffles follow).
+    // Every branch below is taken by the whole warp.
     if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
     const int landed = mbar_wait(full0 + 8 * s, (i / C::STAGES) & 1) ? 1 : 0;
     if (!__all_sync(0xffffffffu, landed)) {
@@ -256,82 +242,139 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const uint32_t kt = ring_s + (2 * s) * C::TILE;
     const uint32_t vt = kt + C::TILE;
+    // Transpose rows: lane L's 16-byte chunk c sits at chunk c ^ (L % CH) of
+    // row L (bank-conflict-free 16-byte stores from 8 consecutive lanes).
+    float* xpose = C::XPOSE_IN_K ? reinterpret_cast<float*>(smem + (2 * s) * C::TILE)
+                                 : reinterpret_cast<float*>(my_scratch);
     const int tok0 = (b0 + i) * kBlockSize;
     const bool tail = tok0 + kBlockSize > seq_len;
 
-    // Partial q.k over this lane's slice of head_dim, for every head.
-    float x[C::V];
 #pragma unroll
-    for (int k = 0; k < C::NT; ++k) {
-      const int t = k * C::NG + g;
-      float kf[C::EL];
+    for (int sb = 0; sb < C::NSB; ++sb) {
+      // Partial q.k over this lane's head_dim slice, every head, SB tokens.
+      float x[C::V];
 #pragma unroll
-      for (int j = 0; j < C::CPL; ++j)
-        unpack8(ld_shared_v4(kt + t * (D * 2) + (li + C::T * j) * 16), kf + 8 * j);
+      for (int kk = 0; kk < C::SB; ++kk) {
+        const int t = (sb * C::SB + kk) * C::NG + g;
+        uint4 kw[C::CPL];
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        float acc = 0.f;
+        for (int j = 0; j < C::CPL; ++j) kw[j] = ld_shared_v4(kt + t * (D * 2) + (li + C::T * j) * 16);
 #pragma unroll
-        for (int e = 0; e < C::EL; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-        x[h * C::NT + k] = acc;
+        for (int h = 0; h < GMAX; ++h) {
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j) {
+            acc = __ffma2_rn(q2[h][j * 4 + 0], unpack2(kw[j].x), acc);
+            acc = __ffma2_rn(q2[h][j * 4 + 1], unpack2(kw[j].y), acc);
+            acc = __ffma2_rn(q2[h][j * 4 + 2], unpack2(kw[j].z), acc);
+            acc = __ffma2_rn(q2[h][j * 4 + 3], unpack2(kw[j].w), acc);
+          }
+          x[h * C::SB + kk] = acc.x + acc.y;
+        }
       }
-    }
-    group_reduce_scatter<C::V, C::T>(x, li);
-
-    // Mask tokens past seq_len (and padding heads), then the lazy max.
-    float smax = -INFINITY;
+      // Sum the partials of the T lanes of a group through shared memory:
+      // lane L writes row L; each lane then adds up its VPL columns.
+      __syncwarp();  // every lane is done reading K before the rows overwrite it
+      if constexpr (C::V >= 4) {
 #pragma unroll
-    for (int u = 0; u < C::VPL; ++u) {
-      const int t = (my_k0 + u) * C::NG + g;
-      const bool ok = head_real && (tok0 + t < seq_len);
-      x[u] = ok ? x[u] : -INFINITY;
-      smax = fmaxf(smax, x[u]);
-    }
-    if (__any_sync(0xffffffffu, smax > my_m + kRescaleSlack)) {
-      float bm = smax;
+        for (int c = 0; c < C::CH; ++c)
+          *reinterpret_cast<float4*>(xpose + lane * (C::CH * 4) + ((c ^ (lane % C::CH)) * 4)) =
+              make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+      } else {
 #pragma unroll
-      for (int b = 1; b < C::LPH; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
-#pragma unroll
-      for (int b = C::T; b < 32; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
-      const float m_new = fmaxf(my_m, bm);
-      const float alpha = fast_exp2(my_m - m_new);
-      my_l *= alpha;
-      my_m = m_new;
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        const float ah = __shfl_sync(0xffffffffu, alpha, h * C::LPH);
-#pragma unroll
-        for (int e = 0; e < C::EL; ++e) o[h][e] *= ah;
+        for (int v = 0; v < C::V; ++v) xpose[lane * 4 + v] = x[v];
       }
-    }
-    float psum = 0.f;
+      __syncwarp();
+      float sc[C::VPL];
 #pragma unroll
-    for (int u = 0; u < C::VPL; ++u) {
-      x[u] = fast_exp2(x[u] - my_m);
-      psum += x[u];
-    }
-    my_l += l_owner ? psum : 0.f;
-    group_all_gather<C::V, C::T>(x, li);
-
-    // A += p v over this group's tokens.
+      for (int u = 0; u < C::VPL; ++u) sc[u] = 0.f;
 #pragma unroll
-    for (int k = 0; k < C::NT; ++k) {
-      const int t = k * C::NG + g;
-      float vf[C::EL];
+      for (int l2 = 0; l2 < C::T; ++l2) {
+        const int r = g * C::T + l2;
+        const float* src = C::V >= 4
+            ? xpose + r * (C::CH * 4) + (((idx0 / 4) ^ (r % C::CH)) * 4) + (idx0 % 4)
+            : xpose + r * 4 + idx0;
+        if constexpr (C::VPL == 2) {
+          const float2 v2 = *reinterpret_cast<const float2*>(src);
+          sc[0] += v2.x;
+          sc[1] += v2.y;
+        } else {
 #pragma unroll
-      for (int j = 0; j < C::CPL; ++j)
-        unpack8(ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16), vf + 8 * j);
-      if (tail && tok0 + t >= seq_len) {
-#pragma unroll
-        for (int e = 0; e < C::EL; ++e) vf[e] = 0.f;  // out-of-context slots may hold NaN
+          for (int u = 0; u < C::VPL; ++u) sc[u] += src[u];
+        }
       }
+      // Mask tokens past seq_len (and padding heads), then the lazy max.
+      float smax = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        const float p = x[h * C::NT + k];
-#pragma unroll
-        for (int e = 0; e < C::EL; ++e) o[h][e] = fmaf(p, vf[e], o[h][e]);
+      for (int u = 0; u < C::VPL; ++u) {
+        const int t = (sb * C::SB + my_k0 + u) * C::NG + g;
+        const bool ok = head_real && (tok0 + t < seq_len);
+        sc[u] = ok ? sc[u] : -INFINITY;
+        smax = fmaxf(smax, sc[u]);
       }
+      if (__any_sync(0xffffffffu, smax > my_m + kRescaleSlack)) {
+        float bm = smax;
+#pragma unroll
+        for (int b = 1; b < C::LPH; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
+#pragma unroll
+        for (int b = C::T; b < 32; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
+        const float m_new = fmaxf(my_m, bm);
+        const float alpha = fast_exp2(my_m - m_new);
+        my_l *= alpha;
+        my_m = m_new;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          const float ah = __shfl_sync(0xffffffffu, alpha, h * C::LPH);
+          const float2 a2 = make_float2(ah, ah);
+#pragma unroll
+          for (int e = 0; e < C::EP; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
+        }
+      }
+      float psum = 0.f;
+#pragma unroll
+      for (int u = 0; u < C::VPL; ++u) {
+        sc[u] = fast_exp2(sc[u] - my_m);
+        psum += sc[u];
+      }
+      my_l += l_owner ? psum : 0.f;
+      // Hand the weights to every lane of the group.
+#pragma unroll
+      for (int u = 0; u < C::VPL; ++u) pbuf[g * C::V + idx0 + u] = sc[u];
+      __syncwarp();
+      float p[C::V];
+#pragma unroll
+      for (int v = 0; v < C::V; v += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(pbuf + g * C::V + v);
+        p[v] = f.x; p[v + 1] = f.y; p[v + 2] = f.z; p[v + 3] = f.w;
+      }
+      // A += p v over this sub-batch's tokens.
+#pragma unroll
+      for (int kk = 0; kk < C::SB; ++kk) {
+        const int t = (sb * C::SB + kk) * C::NG + g;
+        uint4 vw[C::CPL];
+#pragma unroll
+        for (int j = 0; j < C::CPL; ++j) vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
+        if (tail && tok0 + t >= seq_len) {
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);  // may hold NaN
+        }
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j) {
+            o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
+            o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
+            o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
+            o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+          }
+        }
+      }
+      __syncwarp();  // the next sub-batch rewrites the scratch rows
     }
+    // The stage is refilled by TMA (async proxy) after this release; order
+    // this warp's generic-proxy writes into it (the transpose) before that.
+    if (C::XPOSE_IN_K) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
@@ -339,24 +382,33 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // ------------------------------------------------- merge inside the warp
   float lsum = my_l;
 #pragma unroll
-  for (int b = 1; b < C::T; b <<= 1)
-    if (b < C::LPH) lsum += __shfl_xor_sync(0xffffffffu, lsum, b);
+  for (int b = 1; b < C::LPH; b <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, b);
 #pragma unroll
   for (int b = C::T; b < 32; b <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, b);
 #pragma unroll
   for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-    for (int e = 0; e < C::EL; ++e)
+    for (int e = 0; e < C::EP; ++e)
 #pragma unroll
-      for (int b = C::T; b < 32; b <<= 1) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], b);
+      for (int b = C::T; b < 32; b <<= 1) {
+        o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, b);
+        o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, b);
+      }
+  // The merge buffer aliases the ring: wait until every warp is done with
+  // it.  Every block was issued and consumed unless the CTA aborted (then
+  // copies may be in flight and nothing more is written).
+  named_barrier_sync(1, C::NC * 32);
+  if (*abort_flag) return;
+  float* comb_o = reinterpret_cast<float*>(smem);          // [NC][GMAX][D]
+  float* comb_ml = comb_o + C::NC * GMAX * D;               // [NC][GMAX][2]
   if (g == 0) {
 #pragma unroll
     for (int h = 0; h < GMAX; ++h)
 #pragma unroll
       for (int j = 0; j < C::CPL; ++j) {
         float4* dst = reinterpret_cast<float4*>(comb_o + (warp * GMAX + h) * D + (li + C::T * j) * 8);
-        dst[0] = make_float4(o[h][j * 8 + 0], o[h][j * 8 + 1], o[h][j * 8 + 2], o[h][j * 8 + 3]);
-        dst[1] = make_float4(o[h][j * 8 + 4], o[h][j * 8 + 5], o[h][j * 8 + 6], o[h][j * 8 + 7]);
+        dst[0] = make_float4(o2[h][j * 4 + 0].x, o2[h][j * 4 + 0].y, o2[h][j * 4 + 1].x, o2[h][j * 4 + 1].y);
+        dst[1] = make_float4(o2[h][j * 4 + 2].x, o2[h][j * 4 + 2].y, o2[h][j * 4 + 3].x, o2[h][j * 4 + 3].y);
       }
     if (li % C::LPH == 0) {
       comb_ml[(warp * GMAX + my_h) * 2 + 0] = my_m;
@@ -364,7 +416,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   }
   named_barrier_sync(1, C::NC * 32);
-  if (*abort_flag) return;
 
   // ------------------------------------------------ merge across the warps
   for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
@@ -437,7 +488,11 @@ cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
   cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  const dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+  err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (err != cudaSuccess) return err;
+  const dim3 grid(a.num_kv_heads, a.max_parts, a.num_seqs);
   paged_decode_kernel<D, GMAX><<<grid, C::THREADS, C::SMEM, stream>>>(kmap, vmap, a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
