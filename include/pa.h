@@ -173,6 +173,38 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
                     void* stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this call: it exists for
+ * callers such as plugins or backends that a host framework hands only
+ * their input and output tensors, programs whose device-memory budget is
+ * fixed in advance, and hot paths that must not call cudaMalloc (it can
+ * stall the device and is not allowed while a stream is being recorded).
+ *
+ * Same arguments and result as pa_decode, minus the workspace.  Scratch
+ * comes from one static device array of PA_DECODE_NOALLOC_SCRATCH_BYTES
+ * that the library holds on every GPU that loads it until the process
+ * exits.  The call allocates nothing and calls no allocating routine.
+ *   - Sizes whose pa_decode_workspace_size(...) exceeds the array return
+ *     PA_ERR_WORKSPACE without launching anything (a larger
+ *     partition_tokens needs less scratch).
+ *   - The first call on a device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the array and leaves its contents
+ *     behind; each call clears the part that must start at zero.  Calls
+ *     whose work overlaps on the GPU (other streams, other host threads)
+ *     race on the array and must be serialised by the caller.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
+                            const void* value_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, float scale, int32_t partition_tokens,
+                            void* stream);
+
+/*
  * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs
  * (status record, decode-row partials).  Returns 0 for invalid arguments.
  */

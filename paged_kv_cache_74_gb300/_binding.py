@@ -24,7 +24,7 @@ DEVICE_ERRORS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "bad seq_len",
                  4: "bad query length", 5: "wait timeout"}
 ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
-               "pa_prefill_workspace_size", "pa_prefill_varlen")
+               "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc")
 
 
 class PAError(RuntimeError):
@@ -52,6 +52,9 @@ def _declare(lib):
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                               _i32, _i32, _f32, _i32, _vp, _sz, _vp]
+    lib.pa_decode_noalloc.restype = ctypes.c_int
+    lib.pa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                      _i32, _i32, _i32, _f32, _i32, _vp]
     lib.pa_prefill_workspace_size.restype = _sz
     lib.pa_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     lib.pa_prefill_varlen.restype = ctypes.c_int
@@ -175,6 +178,29 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
         float(scale), int(partition_tokens), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def decode_noalloc(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale,
+                   out=None, partition_tokens=0):
+    """pa_decode without a workspace: for callers that cannot allocate device
+    memory.  Scratch comes from a fixed-size array inside the library (see
+    include/pa.h); calls that overlap on the GPU must be serialised."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    S, hq, d = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    lib = load_library()
+    _check("pa_decode_noalloc", lib.pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
+        float(scale), int(partition_tokens), _stream()))
     return out
 
 
