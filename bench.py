@@ -189,8 +189,6 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(t.q)
     slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    max_blocks = -(-w.max_seq_len // w.block_size)
-    max_parts = -(-max_blocks // part_blocks_guess(w))
 
     def step():
         pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, w.block_size,
@@ -232,7 +230,7 @@ def run_ours(args, world, rank, local):
     tot_s, tot_bytes = aggregate_over_ranks(local_s, ab["step_bytes"] * K, world)
     value = tot_bytes / tot_s / 1e9
     dec_avg_s = statistics.mean(dec_ms) / 1e3
-    n_launch = 3 + (1 if max_parts > 1 else 0)
+    n_launch = 3  # slot mapping, reshape_and_cache, decode (one persistent kernel)
 
     # e2e through the public API with pinned host buffers (H2D inputs, D2H out)
     e2e = run_e2e(pa, w, t, dev, stream, flush, args, ab, world)
@@ -256,7 +254,7 @@ def run_ours(args, world, rank, local):
         "us_per_call": round(dec_avg_s * 1e6, 2),
         "decode_kv_gbs": round(ab["kv_bytes"] / dec_avg_s / 1e9, 2),
         "wall_ms_per_step": round(wall / K * 1e3, 4),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged_decode_kernel + merge)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (pa_decode)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": ab["decode_bytes"]},
@@ -269,16 +267,6 @@ def run_ours(args, world, rank, local):
     if args.extra and rank == 0:
         res["extra"] = {name: extra_decode(pa, name, dev, flush) for name in args.extra}
     return res, rank
-
-
-def part_blocks_guess(w):
-    """Partition size the library picks (mirrors choose_partition_blocks)."""
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    max_blocks = -(-w.max_seq_len // 16)
-    pb = 32
-    while pb > 8 and w.num_seqs * w.num_kv_heads * -(-max_blocks // pb) < 4 * sms:
-        pb //= 2
-    return pb
 
 
 def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):

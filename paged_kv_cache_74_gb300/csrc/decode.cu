@@ -7,28 +7,38 @@
 //                tile by tile, O = A / l at the end;
 //   section 3.2  masked scores of tokens >= seq_len are excluded and the V
 //                of out-of-context slots is zeroed before it is used;
-//   sections 3.2.7, 3.2.9, 3.3  long contexts are cut into partitions whose
-//                (m_j, l_j, O_j) are merged by a second pass.
+//   sections 3.2.7, 3.2.9, 3.3  a long context is cut into pieces whose
+//                (m_j, l_j, O_j) are merged: m = max m_j,
+//                L = sum l_j e^{m_j - m}, O = sum O_j l_j e^{m_j - m} / L.
 //
-// GB300 design.  Decode is HBM-bound (about 2 FMAs per byte of KV at
-// 4 q heads per kv head), so the K/V stream runs on CUDA cores, not tensor
-// cores.  One CTA owns (partition, kv head, request) and serves every q head
-// of that kv head, so each K/V byte is read from HBM once.  A producer warp
-// reads the partition's block ids 32 at a time and issues one TMA tensor
-// load per (block, kv head) tile of K and of V (16 tokens x head_dim, 4 KB at
-// head_dim 128) into an 8-stage shared-memory ring guarded by mbarriers.
-// Four consumer warps take every 4th block.  Inside a warp, T lanes share
-// one token: each lane holds a 16-byte-chunk slice of head_dim for q (fp32,
-// pre-scaled by scale * log2 e) and for its output accumulator, computes
-// partial dot products for all q heads of the group, and a butterfly
-// reduce-scatter leaves each lane with whole scores of a few (token, head)
-// pairs; the exponentials are then computed once per score, not once per
-// lane, and an all-gather hands the weights back for the P.V update.
-// The running max is rescaled lazily: only when a new score exceeds the
-// current reference by more than 2^8 (the final O = A / l is exact for any
-// reference).  Partials are merged across the four warps in shared memory
-// and either written as the final bf16 output (single partition) or as a
-// normalised partial (m_j, l_j, O_j) for the merge kernel.
+// GB300 design.  Decode is HBM-bound (about 2 FMAs per byte of KV at 4 q
+// heads per kv head), so the K/V stream runs on CUDA cores, not tensor
+// cores, and the kernel is built around keeping HBM busy:
+//
+// * Balanced persistent grid.  Every (request, kv head, 16-token block)
+//   tile of the batch is numbered (request-major, then kv head, then block)
+//   and the W tiles are cut into equal contiguous ranges, one per CTA, with
+//   as many CTAs as fit on the GPU at once.  No CTA idles at the tail and
+//   the K/V stream of a CTA never drains between requests.  A range covers
+//   whole (request, kv head) pairs, written straight to `out`, and at most
+//   two pieces of pairs shared with the neighbouring ranges; those are
+//   written as partials (m_j, l_j, O_j) and merged by the contributor that
+//   finishes last (an epoch-tagged counter per pair decides which).
+// * One CTA serves every q head of a kv head, so each K/V byte is read from
+//   HBM once.  A producer warp reads block ids 32 at a time and issues one
+//   TMA tensor load per (block, kv head) tile of K and of V (16 tokens x
+//   head_dim, 4 KB at head_dim 128) into an 8-stage ring guarded by
+//   mbarriers, writes each stage's block index and flags next to it, and
+//   prefetches each segment's q with a bulk copy into a double buffer.
+// * Four consumer warps take every 4th stage.  T lanes share a token; each
+//   lane holds a 16-byte slice of head_dim of q (fp32, pre-scaled by
+//   scale * log2 e) and of the output accumulators, computes partial q.k
+//   for all q heads with packed fp32 FMAs (fma.rn.f32x2), and the partials
+//   are summed through a shared-memory transpose that reuses the warp's own
+//   K tile.  The running max is rescaled lazily, only when a new score
+//   exceeds the reference by more than 2^8 (O = A / l is exact for any
+//   reference).  Each segment is padded to a multiple of four stages, so all
+//   warps finish it together and merge their states in shared memory.
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -38,7 +48,16 @@ namespace {
 constexpr float kNegBig = -1e30f;      // finite stand-in for -inf in running maxima
 constexpr float kRescaleSlack = 8.0f;  // log2 units
 
-// Work split of one warp over one 16-token block (see the file comment).
+// Stage flags (written by the producer next to each ring stage).
+constexpr int kSkip = 1;     // padding stage: no data, nothing to compute
+constexpr int kLastRow = 2;  // the segment ends after this row of stages
+constexpr int kDone = 4;     // no more work for the warp that receives it
+
+// How a segment's result is written.
+constexpr int kWhole = 0;  // the whole (request, kv head): final bf16 output
+constexpr int kHead = 1;   // continues a pair begun by an earlier CTA: partial slot 0
+constexpr int kTail = 2;   // begins a pair finished by later CTAs: partial slot 1
+
 template <int D, int GMAX>
 struct DecodeCfg {
   static constexpr int T = (D == 128 && GMAX >= 4) ? 16 : 8;  // lanes per token
@@ -53,7 +72,7 @@ struct DecodeCfg {
   static constexpr int VPL = V >= T ? V / T : 1;               // whole scores per lane after the sum
   static constexpr int REP = V >= T ? 1 : T / V;               // lanes holding the same score
   static constexpr int LPH = T / GMAX;                         // lanes of a group per head
-  static constexpr int CH = V / 4 > 0 ? V / 4 : 1;              // 16-byte chunks per transpose row
+  static constexpr int CH = V / 4;                             // 16-byte chunks per transpose row
   static constexpr int NC = 4;                                 // consumer warps
   static constexpr int MINB = GMAX * EL > 32 ? 2 : 3;          // CTAs per SM the registers allow
   static constexpr int TILE = kBlockSize * D * 2;              // bytes of one (block, kv head) tile
@@ -61,25 +80,111 @@ struct DecodeCfg {
   // K tile once its q.k products are done, when it fits and no later
   // sub-batch still needs K; otherwise each warp gets a dedicated buffer.
   static constexpr bool XPOSE_IN_K = 32 * CH * 16 <= TILE && NSB == 1;
-  static constexpr int XPOSE = XPOSE_IN_K ? 0 : 32 * CH * 16;
   static constexpr int STAGES = D == 128 ? 8 : 16;             // a multiple of NC (see below)
-  static constexpr int SCRATCH = XPOSE + NG * V * 4;           // per warp: transpose + weights
-  static constexpr int SCRATCH_AL = (SCRATCH + 127) / 128 * 128;
-  static constexpr int COMB = NC * GMAX * (D + 2) * 4;         // cross-warp merge (aliases the ring)
-  static constexpr int SMEM_RING = STAGES * 2 * TILE;
-  static constexpr int SMEM_SCR = NC * SCRATCH_AL;
-  static constexpr int SMEM = SMEM_RING + SMEM_SCR + 2 * STAGES * 8 + 16 + 1024;  // + align slack
+  // shared memory carve-up (bytes)
+  static constexpr int RING = STAGES * 2 * TILE;
+  static constexpr int XPOSE = XPOSE_IN_K ? 0 : NC * 32 * CH * 16;
+  static constexpr int PBUF = NC * NG * V * 4;                 // per-warp weights
+  static constexpr int COMB = NC * GMAX * (D + 2) * 4;         // cross-warp merge
+  static constexpr int PC = PBUF > COMB ? PBUF : COMB;         // weights and merge alias
+  static constexpr int QBUF = 2 * GMAX * D * 2;                // q of two segments
+  static constexpr int OFF_XPOSE = RING;
+  static constexpr int OFF_PC = OFF_XPOSE + XPOSE;
+  static constexpr int OFF_Q = OFF_PC + PC;
+  static constexpr int OFF_META = OFF_Q + QBUF;                // int2 per stage
+  static constexpr int OFF_SEG = OFF_META + STAGES * 8;        // 2 segment records
+  static constexpr int OFF_BAR = OFF_SEG + 2 * 32;             // full, empty, qfull, qempty, sync
+  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 5) * 8;
+  static constexpr int SMEM = OFF_MISC + 32;
   static constexpr int THREADS = (NC + 1) * 32;
-  // Block i goes to stage i % STAGES and to warp i % NC.  With STAGES a
-  // multiple of NC a stage is only ever used by one warp, so when a warp
-  // waits on a stage the barrier is at most one phase behind and the
-  // parity wait is unambiguous.
+  // Stage i goes to consumer warp i % NC.  With STAGES a multiple of NC a
+  // stage is only ever used by one warp, so when a warp waits on a stage
+  // the barrier is at most one phase behind and the parity wait is exact.
   static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
-  static_assert(COMB <= SMEM_RING, "merge buffer must fit in the ring");
+  static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V >= 4 && V <= 32, "decode shape");
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
-  static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V <= 32, "unsupported decode shape");
 };
+
+// What the producer tells the consumers about a segment: the run of blocks
+// of one (request, kv head) pair inside this CTA's range.
+struct SegInfo {
+  int row;        // q / out row of the request
+  int seq_len;
+  int nblk;       // blocks of the request
+  int kind;       // kWhole, kHead or kTail
+  long long t0;   // number of the pair's first tile
+  int r;
+  int kvh;
+};
+static_assert(sizeof(SegInfo) <= 32, "segment record");
+
+// Blocks of request r that the decode kernel processes (0 for rows that are
+// not decode rows, and for invalid lengths); also its length and q row.
+__device__ __forceinline__ int request_blocks(const DecodeArgs& a, int r, int* seq_len, int* row) {
+  int rw = r;
+  if (a.query_start_loc != nullptr) {
+    const int q0 = a.query_start_loc[r];
+    if (a.query_start_loc[r + 1] - q0 != 1) return 0;  // not a decode row
+    rw = q0;
+    if (rw < 0 || rw >= a.total_q) return 0;
+  }
+  const int len = a.seq_lens[r];
+  if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize) return 0;
+  *seq_len = len;
+  *row = rw;
+  return (len + kBlockSize - 1) / kBlockSize;
+}
+
+// Reports the rows request_blocks() rejects (done once, by CTA 0).
+__device__ void report_bad_rows(const DecodeArgs& a, int lane) {
+  for (int r = lane; r < a.num_seqs; r += 32) {
+    int rw = r;
+    if (a.query_start_loc != nullptr) {
+      const int q0 = a.query_start_loc[r];
+      if (a.query_start_loc[r + 1] - q0 != 1) continue;
+      rw = q0;
+      if (rw < 0 || rw >= a.total_q) {
+        record_error(a.status, PA_DEV_BAD_QUERY_LEN, r, rw);
+        continue;
+      }
+    }
+    const int len = a.seq_lens[r];
+    if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize)
+      record_error(a.status, PA_DEV_BAD_SEQ_LEN, r, len);
+  }
+}
+
+// Equal split of W tiles over C CTAs: CTA c owns [range_lo(c), range_lo(c+1)).
+__device__ __forceinline__ long long range_lo(long long W, int C, int c) {
+  const long long q = W / C, rem = W % C;
+  return static_cast<long long>(c) * q + (c < rem ? c : rem);
+}
+
+// The CTA whose range holds tile t (0 <= t < W).
+__device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
+  const long long q = W / C, rem = W % C;
+  const long long big = rem * (q + 1);
+  if (t < big) return static_cast<int>(t / (q + 1));
+  return static_cast<int>(rem + (t - big) / q);
+}
+
+// Registers this CTA's partial for a pair; true if it was the last of n.
+__device__ bool contribute(unsigned long long* counter, unsigned epoch, int n, int32_t* status,
+                           int who) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+  unsigned long long now = 0;
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    now = (static_cast<unsigned>(old >> 32) == epoch)
+              ? old + 1
+              : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    const unsigned long long seen = atomicCAS(counter, old, now);
+    if (seen == old) return static_cast<int>(now & 0xffffffffu) == n;
+    old = seen;
+  }
+  record_error(status, PA_DEV_WAIT_TIMEOUT, who, 3);
+  return false;
+}
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -90,395 +195,535 @@ __global__ void __launch_bounds__(DecodeCfg<D, GMAX>::THREADS, DecodeCfg<D, GMAX
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using C = DecodeCfg<D, GMAX>;
-  const int kvh = blockIdx.x;
-  const int part = blockIdx.y;
-  const int seq = blockIdx.z;
+  const int cta = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool reporter = threadIdx.x == 0 && part == 0 && kvh == 0;
 
-  int row = seq;
-  if (a.query_start_loc != nullptr) {
-    const int q0 = a.query_start_loc[seq];
-    const int q1 = a.query_start_loc[seq + 1];
-    if (q1 - q0 != 1) return;  // not a decode row
-    row = q0;
-    if (row < 0 || row >= a.total_q) {
-      if (reporter) record_error(a.status, PA_DEV_BAD_QUERY_LEN, seq, row);
-      return;
-    }
-  }
-  const int seq_len = a.seq_lens[seq];
-  if (seq_len < 1 || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * kBlockSize) {
-    if (reporter) record_error(a.status, PA_DEV_BAD_SEQ_LEN, seq, seq_len);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  int2* meta = reinterpret_cast<int2*>(smem + C::OFF_META);
+  SegInfo* seginfo = reinterpret_cast<SegInfo*>(smem + C::OFF_SEG);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+  volatile int* last_flag = abort_flag + 1;
+  long long* total_tiles = reinterpret_cast<long long*>(smem + C::OFF_MISC + 8);
+  const uint32_t ring_s = smem_u32(smem);
+  const uint32_t full0 = smem_u32(smem + C::OFF_BAR);
+  const uint32_t empty0 = full0 + 8 * C::STAGES;
+  const uint32_t qfull0 = empty0 + 8 * C::STAGES;
+  const uint32_t qempty0 = qfull0 + 16;
+  const uint32_t csync_bar = qempty0 + 16;  // consumer-warp barrier (bounded waits)
+  const uint32_t qbuf_s = smem_u32(smem + C::OFF_Q);
+
+  // TMA destinations must be 128-byte aligned; the dynamic shared-memory base
+  // always is on this GPU, but never issue a copy if it were not.
+  if (ring_s & 127) {
+    if (threadIdx.x == 0) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 6);
     return;
   }
-  const int nblk_seq = (seq_len + kBlockSize - 1) / kBlockSize;
-  const int b0 = part * a.partition_blocks;
-  if (b0 >= nblk_seq) return;
-  const int nblk = min(a.partition_blocks, nblk_seq - b0);
-  const int nparts = (nblk_seq + a.partition_blocks - 1) / a.partition_blocks;
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // TMA destinations want an aligned base: round up inside the (padded) allocation.
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* scratch = smem + C::SMEM_RING;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + C::SMEM_SCR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * C::STAGES);
-  const uint32_t ring_s = smem_u32(smem);
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * C::STAGES;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(qfull0 + 8 * k, 1);
+      mbar_init(qempty0 + 8 * k, C::NC);
+    }
+    mbar_init(csync_bar, C::NC);
     *abort_flag = 0;
+    *last_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp == C::NC) {
-    // ------------------------------------------------------------ producer
-    const int32_t* bt = a.block_tables + static_cast<size_t>(seq) * a.max_blocks_per_seq + b0;
-    const uint64_t policy = l2_policy_evict_first();
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
+    // ================================================================ producer
+    if (cta == 0) report_bad_rows(a, lane);
+    // Total tiles W of the batch.
+    long long nb_sum = 0;
+    for (int r = lane; r < a.num_seqs; r += 32) {
+      int len, row;
+      nb_sum += request_blocks(a, r, &len, &row);
     }
-    int my_id = 0;
-    int issued = 0;
-    for (int i = 0; i < nblk; ++i) {
-      if ((i & 31) == 0) {
-        const int j = i + lane;
-        my_id = j < nblk ? __ldg(bt + j) : 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
+    const long long W = nb_sum * a.num_kv_heads;
+    const long long lo = W > 0 ? range_lo(W, a.num_ctas, cta) : 0;
+    const long long hi = W > 0 ? range_lo(W, a.num_ctas, cta + 1) : 0;
+    if (lane == 0) *total_tiles = W;
+
+    int pos = 0;  // stage sequence number
+    auto stage_begin = [&](int p) -> bool {  // lane 0: wait until stage p may be refilled
+      if (p >= C::STAGES && !mbar_wait(empty0 + 8 * (p % C::STAGES), ((p / C::STAGES) - 1) & 1)) {
+        record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 1);
+        *abort_flag = 1;
       }
-      const int phys = __shfl_sync(0xffffffffu, my_id, i & 31);
-      int stop = 0;
-      if (lane == 0) {
-        const int s = i % C::STAGES;
-        if (i >= C::STAGES && !mbar_wait(empty0 + 8 * s, ((i / C::STAGES) - 1) & 1)) {
-          record_error(a.status, PA_DEV_WAIT_TIMEOUT, seq, 1);
-          *abort_flag = 1;
+      return *abort_flag == 0;
+    };
+
+    if (lo < hi) {
+      // Request holding tile `lo`: scan the per-request tile counts 32 at a time.
+      long long base = 0;  // tiles before request r0
+      int r0 = -1;
+      for (int rc = 0; rc < a.num_seqs && r0 < 0; rc += 32) {
+        const int r = rc + lane;
+        int len, row;
+        const long long nt = r < a.num_seqs ? static_cast<long long>(request_blocks(a, r, &len, &row)) *
+                                                  a.num_kv_heads
+                                            : 0;
+        long long incl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
         }
-        if (*abort_flag) {
-          stop = 1;
+        const unsigned hit = __ballot_sync(0xffffffffu, r < a.num_seqs && base + incl > lo);
+        if (hit) {
+          const int first = __ffs(hit) - 1;
+          const long long excl = __shfl_sync(0xffffffffu, incl - nt, first);
+          r0 = rc + first;
+          base += excl;
         } else {
-          int row0 = phys * kBlockSize;
-          if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
-            record_error(a.status, PA_DEV_BAD_BLOCK_ID, seq, phys);
-            row0 = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
-          }
-          const uint32_t full = full0 + 8 * s;
-          mbar_arrive_expect_tx(full, 2 * C::TILE);
-          tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
-          tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
-          issued = i + 1;
+          base += __shfl_sync(0xffffffffu, incl, 31);
         }
       }
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      int r = r0, len = 0, row = 0;
+      int nb = request_blocks(a, r, &len, &row);
+      long long off = lo - base;
+      int kvh = static_cast<int>(off / nb);
+      int b = static_cast<int>(off % nb);
+      long long t = lo;
+      const uint64_t policy = l2_policy_evict_first();
+      if (lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+      }
+      int seg = 0;
+      bool ok = true;
+      while (t < hi && ok) {
+        const int seg_n = static_cast<int>(min(hi - t, static_cast<long long>(nb - b)));
+        const int kind = (b == 0 && seg_n == nb) ? kWhole : (b > 0 ? kHead : kTail);
+        const int slot = seg & 1;
+        if (lane == 0) {
+          // q and the segment record go to slot seg % 2 once every consumer
+          // warp has taken segment seg - 2 from it.
+          if (seg >= 2 && !mbar_wait(qempty0 + 8 * slot, ((seg >> 1) - 1) & 1)) {
+            record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 4);
+            *abort_flag = 1;
+          }
+          if (*abort_flag == 0) {
+            SegInfo si;
+            si.row = row;
+            si.seq_len = len;
+            si.nblk = nb;
+            si.kind = kind;
+            si.t0 = base + static_cast<long long>(kvh) * nb;
+            si.r = r;
+            si.kvh = kvh;
+            seginfo[slot] = si;
+            const uint32_t qbytes = a.group * D * 2;
+            mbar_arrive_expect_tx(qfull0 + 8 * slot, qbytes);
+            bulk_copy_g2s(qbuf_s + slot * (GMAX * D * 2),
+                          a.q + (static_cast<size_t>(row) * a.num_heads +
+                                 static_cast<size_t>(kvh) * a.group) * D,
+                          qbytes, qfull0 + 8 * slot);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        const int rows = (seg_n + C::NC - 1) / C::NC;
+        const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq + b;
+        int my_id = 0;
+        for (int j = 0; j < rows * C::NC && ok; ++j) {
+          if ((j & 31) == 0) {
+            const int jj = j + lane;
+            my_id = jj < seg_n ? __ldg(bt + jj) : 0;
+          }
+          const int phys = __shfl_sync(0xffffffffu, my_id, j & 31);
+          if (lane == 0 && stage_begin(pos)) {
+            const int s = pos % C::STAGES;
+            const bool real = j < seg_n;
+            const int flags = (real ? 0 : kSkip) | (j >= (rows - 1) * C::NC ? kLastRow : 0);
+            meta[s] = make_int2(b + j, flags);
+            const uint32_t full = full0 + 8 * s;
+            if (real) {
+              int row0 = phys * kBlockSize;
+              if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+                record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys);
+                row0 = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
+              }
+              mbar_arrive_expect_tx(full, 2 * C::TILE);
+              tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
+              tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+            } else {
+              mbar_arrive(full);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+          ++pos;
+        }
+        t += seg_n;
+        b += seg_n;
+        ++seg;
+        if (b == nb && t < hi) {  // next (request, kv head) pair
+          b = 0;
+          if (++kvh == a.num_kv_heads) {
+            kvh = 0;
+            base += static_cast<long long>(nb) * a.num_kv_heads;
+            nb = 0;
+            while (nb == 0 && ++r < a.num_seqs) nb = request_blocks(a, r, &len, &row);
+            if (nb == 0) ok = false;  // cannot happen while t < hi
+          }
+        }
+      }
+    }
+    // One "done" stage for each consumer warp.
+    for (int j = 0; j < C::NC; ++j) {
+      if (lane == 0 && stage_begin(pos)) {
+        const int s = pos % C::STAGES;
+        meta[s] = make_int2(0, kDone);
+        mbar_arrive(full0 + 8 * s);
+      }
+      ++pos;
     }
     if (lane == 0 && *abort_flag) {
-      // Let the copies already in flight land before the CTA can exit.
-      for (int i = max(0, issued - C::STAGES); i < issued; ++i)
+      // Let copies already in flight land before the CTA can exit.
+      for (int i = max(0, pos - C::STAGES); i < pos; ++i)
         (void)mbar_wait(full0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1);
+      for (int k = 0; k < 2; ++k) (void)mbar_wait(qfull0 + 8 * k, 0);
     }
     return;
   }
 
-  // -------------------------------------------------------------- consumer
+  // ================================================================ consumers
   const int g = lane / C::T;
   const int li = lane % C::T;
-  const int head0 = kvh * a.group;
-  uint8_t* my_scratch = scratch + warp * C::SCRATCH_AL;
-  float* pbuf = reinterpret_cast<float*>(my_scratch + C::XPOSE);  // [NG][V] weights
-
-  // q of every head of the group over this lane's slice of head_dim, as
-  // float2 pairs, pre-scaled by scale * log2(e).
-  float2 q2[GMAX][C::EP];
-  {
-    const __nv_bfloat16* qrow = a.q + (static_cast<size_t>(row) * a.num_heads + head0) * D;
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-#pragma unroll
-      for (int j = 0; j < C::CPL; ++j) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (h < a.group) w = __ldg(reinterpret_cast<const uint4*>(qrow + h * D + (li + C::T * j) * 8));
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack2(ws[e]);
-          q2[h][j * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
-        }
-      }
-    }
-  }
-
-  float2 o2[GMAX][C::EP];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-    for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
-  float my_m = kNegBig;  // running max (log2 units) of this lane's head, same on all its lanes
-  float my_l = 0.f;      // this lane's share of the running exp-sum
+  float* pbuf = reinterpret_cast<float*>(smem + C::OFF_PC) + warp * (C::NG * C::V);
+  float* comb_o = reinterpret_cast<float*>(smem + C::OFF_PC);  // [NC][GMAX][D] (merge time)
+  float* comb_ml = comb_o + C::NC * GMAX * D;                   // [NC][GMAX][2]
   const int idx0 = (li * C::V) / C::T;
   const int my_h = idx0 / C::SB;
   const int my_k0 = idx0 % C::SB;
-  const bool head_real = my_h < a.group;
   const bool l_owner = (li % C::REP) == 0;
 
-  for (int i = warp; i < nblk; i += C::NC) {
-    const int s = i % C::STAGES;
-    // Every branch below is taken by the whole warp.
-    if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-    const int landed = mbar_wait(full0 + 8 * s, (i / C::STAGES) & 1) ? 1 : 0;
+  float2 q2[GMAX][C::EP];
+  float2 o2[GMAX][C::EP];
+  float my_m = kNegBig;  // running max (log2 units) of this lane's head, same on all its lanes
+  float my_l = 0.f;      // this lane's share of the running exp-sum
+  SegInfo si{};
+  bool fresh = true;
+  int seg = 0;
+  // Barrier of the four consumer warps: lane 0 of each warp arrives, every
+  // lane waits (bounded); orders the warps' shared-memory writes before the
+  // reads after it.  Returns false (and flags an abort) on a timeout.
+  uint32_t cphase = 0;
+  auto csync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(csync_bar);
+    const int ok = mbar_wait(csync_bar, cphase & 1) ? 1 : 0;
+    ++cphase;
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (lane == 0) {
+      record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 7);
+      *abort_flag = 1;
+    }
+    return false;
+  };
+
+  for (int pos = warp;; pos += C::NC) {
+    const int s = pos % C::STAGES;
+    const int landed = mbar_wait(full0 + 8 * s, (pos / C::STAGES) & 1) ? 1 : 0;
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) {
-        record_error(a.status, PA_DEV_WAIT_TIMEOUT, seq, 2);
+        record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 2);
         *abort_flag = 1;
       }
       break;
     }
-    const uint32_t kt = ring_s + (2 * s) * C::TILE;
-    const uint32_t vt = kt + C::TILE;
-    // Transpose rows: lane L's 16-byte chunk c sits at chunk c ^ (L % CH) of
-    // row L (bank-conflict-free 16-byte stores from 8 consecutive lanes).
-    float* xpose = C::XPOSE_IN_K ? reinterpret_cast<float*>(smem + (2 * s) * C::TILE)
-                                 : reinterpret_cast<float*>(my_scratch);
-    const int tok0 = (b0 + i) * kBlockSize;
-    const bool tail = tok0 + kBlockSize > seq_len;
+    const int2 m = meta[s];
+    if (m.y & kDone) break;
 
+    if (fresh) {  // first stage of a segment: take its q and reset the state
+      const int slot = seg & 1;
+      const int qok = mbar_wait(qfull0 + 8 * slot, (seg >> 1) & 1) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, qok)) {
+        if (lane == 0) {
+          record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 5);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      si = seginfo[slot];
+      const uint32_t qs = qbuf_s + slot * (GMAX * D * 2);
 #pragma unroll
-    for (int sb = 0; sb < C::NSB; ++sb) {
-      // Partial q.k over this lane's head_dim slice, every head, SB tokens.
-      float x[C::V];
+      for (int h = 0; h < GMAX; ++h) {
 #pragma unroll
-      for (int kk = 0; kk < C::SB; ++kk) {
-        const int t = (sb * C::SB + kk) * C::NG + g;
-        uint4 kw[C::CPL];
+        for (int j = 0; j < C::CPL; ++j) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (h < a.group) w = ld_shared_v4(qs + (h * D + (li + C::T * j) * 8) * 2);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < C::CPL; ++j) kw[j] = ld_shared_v4(kt + t * (D * 2) + (li + C::T * j) * 16);
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < C::CPL; ++j) {
-            acc = __ffma2_rn(q2[h][j * 4 + 0], unpack2(kw[j].x), acc);
-            acc = __ffma2_rn(q2[h][j * 4 + 1], unpack2(kw[j].y), acc);
-            acc = __ffma2_rn(q2[h][j * 4 + 2], unpack2(kw[j].z), acc);
-            acc = __ffma2_rn(q2[h][j * 4 + 3], unpack2(kw[j].w), acc);
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack2(ws[e]);
+            q2[h][j * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
           }
-          x[h * C::SB + kk] = acc.x + acc.y;
         }
       }
-      // Sum the partials of the T lanes of a group through shared memory:
-      // lane L writes row L; each lane then adds up its VPL columns.
-      __syncwarp();  // every lane is done reading K before the rows overwrite it
-      if constexpr (C::V >= 4) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+        for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
+      my_m = kNegBig;
+      my_l = 0.f;
+      fresh = false;
+    }
+
+    if (!(m.y & kSkip)) {
+      const uint32_t kt = ring_s + (2 * s) * C::TILE;
+      const uint32_t vt = kt + C::TILE;
+      const int tok0 = m.x * kBlockSize;
+      const int seq_len = si.seq_len;
+      const bool tail = tok0 + kBlockSize > seq_len;
+      const bool head_real = my_h < a.group;
+      // Transpose rows: lane L's 16-byte chunk c sits at chunk c ^ (L % CH)
+      // of row L (bank-conflict-free 16-byte stores from 8 lanes).
+      float* xpose = C::XPOSE_IN_K
+                         ? reinterpret_cast<float*>(smem + (2 * s) * C::TILE)
+                         : reinterpret_cast<float*>(smem + C::OFF_XPOSE) + warp * (32 * C::CH * 4);
+#pragma unroll
+      for (int sb = 0; sb < C::NSB; ++sb) {
+        // Partial q.k over this lane's head_dim slice, every head, SB tokens.
+        float x[C::V];
+#pragma unroll
+        for (int kk = 0; kk < C::SB; ++kk) {
+          const int t = (sb * C::SB + kk) * C::NG + g;
+          uint4 kw[C::CPL];
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j)
+            kw[j] = ld_shared_v4(kt + t * (D * 2) + (li + C::T * j) * 16);
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j) {
+              acc = __ffma2_rn(q2[h][j * 4 + 0], unpack2(kw[j].x), acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 1], unpack2(kw[j].y), acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 2], unpack2(kw[j].z), acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 3], unpack2(kw[j].w), acc);
+            }
+            x[h * C::SB + kk] = acc.x + acc.y;
+          }
+        }
+        // Sum the partials of the T lanes of a group through shared memory:
+        // lane L writes row L; each lane then adds up its VPL columns.
+        __syncwarp();  // every lane is done reading K before rows overwrite it
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
           *reinterpret_cast<float4*>(xpose + lane * (C::CH * 4) + ((c ^ (lane % C::CH)) * 4)) =
               make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-      } else {
+        __syncwarp();
+        float sc[C::VPL];
 #pragma unroll
-        for (int v = 0; v < C::V; ++v) xpose[lane * 4 + v] = x[v];
-      }
-      __syncwarp();
-      float sc[C::VPL];
+        for (int u = 0; u < C::VPL; ++u) sc[u] = 0.f;
 #pragma unroll
-      for (int u = 0; u < C::VPL; ++u) sc[u] = 0.f;
+        for (int l2 = 0; l2 < C::T; ++l2) {
+          const int rr = g * C::T + l2;
+          const float* src =
+              xpose + rr * (C::CH * 4) + (((idx0 / 4) ^ (rr % C::CH)) * 4) + (idx0 % 4);
+          if constexpr (C::VPL == 2) {
+            const float2 v2 = *reinterpret_cast<const float2*>(src);
+            sc[0] += v2.x;
+            sc[1] += v2.y;
+          } else {
 #pragma unroll
-      for (int l2 = 0; l2 < C::T; ++l2) {
-        const int r = g * C::T + l2;
-        const float* src = C::V >= 4
-            ? xpose + r * (C::CH * 4) + (((idx0 / 4) ^ (r % C::CH)) * 4) + (idx0 % 4)
-            : xpose + r * 4 + idx0;
-        if constexpr (C::VPL == 2) {
-          const float2 v2 = *reinterpret_cast<const float2*>(src);
-          sc[0] += v2.x;
-          sc[1] += v2.y;
-        } else {
-#pragma unroll
-          for (int u = 0; u < C::VPL; ++u) sc[u] += src[u];
-        }
-      }
-      // Mask tokens past seq_len (and padding heads), then the lazy max.
-      float smax = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < C::VPL; ++u) {
-        const int t = (sb * C::SB + my_k0 + u) * C::NG + g;
-        const bool ok = head_real && (tok0 + t < seq_len);
-        sc[u] = ok ? sc[u] : -INFINITY;
-        smax = fmaxf(smax, sc[u]);
-      }
-      if (__any_sync(0xffffffffu, smax > my_m + kRescaleSlack)) {
-        float bm = smax;
-#pragma unroll
-        for (int b = 1; b < C::LPH; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
-#pragma unroll
-        for (int b = C::T; b < 32; b <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, b));
-        const float m_new = fmaxf(my_m, bm);
-        const float alpha = fast_exp2(my_m - m_new);
-        my_l *= alpha;
-        my_m = m_new;
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          const float ah = __shfl_sync(0xffffffffu, alpha, h * C::LPH);
-          const float2 a2 = make_float2(ah, ah);
-#pragma unroll
-          for (int e = 0; e < C::EP; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
-        }
-      }
-      float psum = 0.f;
-#pragma unroll
-      for (int u = 0; u < C::VPL; ++u) {
-        sc[u] = fast_exp2(sc[u] - my_m);
-        psum += sc[u];
-      }
-      my_l += l_owner ? psum : 0.f;
-      // Hand the weights to every lane of the group.
-#pragma unroll
-      for (int u = 0; u < C::VPL; ++u) pbuf[g * C::V + idx0 + u] = sc[u];
-      __syncwarp();
-      float p[C::V];
-#pragma unroll
-      for (int v = 0; v < C::V; v += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(pbuf + g * C::V + v);
-        p[v] = f.x; p[v + 1] = f.y; p[v + 2] = f.z; p[v + 3] = f.w;
-      }
-      // A += p v over this sub-batch's tokens.
-#pragma unroll
-      for (int kk = 0; kk < C::SB; ++kk) {
-        const int t = (sb * C::SB + kk) * C::NG + g;
-        uint4 vw[C::CPL];
-#pragma unroll
-        for (int j = 0; j < C::CPL; ++j) vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
-        if (tail && tok0 + t >= seq_len) {
-#pragma unroll
-          for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);  // may hold NaN
-        }
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
-#pragma unroll
-          for (int j = 0; j < C::CPL; ++j) {
-            o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
-            o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
-            o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
-            o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+            for (int u = 0; u < C::VPL; ++u) sc[u] += src[u];
           }
         }
+        // Mask tokens past seq_len (and padding heads), then the lazy max.
+        float smax = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < C::VPL; ++u) {
+          const int t = (sb * C::SB + my_k0 + u) * C::NG + g;
+          const bool ok = head_real && (tok0 + t < seq_len);
+          sc[u] = ok ? sc[u] : -INFINITY;
+          smax = fmaxf(smax, sc[u]);
+        }
+        if (__any_sync(0xffffffffu, smax > my_m + kRescaleSlack)) {
+          float bm = smax;
+#pragma unroll
+          for (int bb = 1; bb < C::LPH; bb <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, bb));
+#pragma unroll
+          for (int bb = C::T; bb < 32; bb <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, bb));
+          const float m_new = fmaxf(my_m, bm);
+          const float alpha = fast_exp2(my_m - m_new);
+          my_l *= alpha;
+          my_m = m_new;
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            const float ah = __shfl_sync(0xffffffffu, alpha, h * C::LPH);
+            const float2 a2 = make_float2(ah, ah);
+#pragma unroll
+            for (int e = 0; e < C::EP; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
+          }
+        }
+        float psum = 0.f;
+#pragma unroll
+        for (int u = 0; u < C::VPL; ++u) {
+          sc[u] = fast_exp2(sc[u] - my_m);
+          psum += sc[u];
+        }
+        my_l += l_owner ? psum : 0.f;
+        // Hand the weights to every lane of the group.
+#pragma unroll
+        for (int u = 0; u < C::VPL; ++u) pbuf[g * C::V + idx0 + u] = sc[u];
+        __syncwarp();
+        float p[C::V];
+#pragma unroll
+        for (int v = 0; v < C::V; v += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(pbuf + g * C::V + v);
+          p[v] = f.x;
+          p[v + 1] = f.y;
+          p[v + 2] = f.z;
+          p[v + 3] = f.w;
+        }
+        // A += p v over this sub-batch's tokens.
+#pragma unroll
+        for (int kk = 0; kk < C::SB; ++kk) {
+          const int t = (sb * C::SB + kk) * C::NG + g;
+          uint4 vw[C::CPL];
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j)
+            vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
+          if (tail && tok0 + t >= seq_len) {
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);  // may hold NaN
+          }
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j) {
+              o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
+              o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
+              o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
+              o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+            }
+          }
+        }
+        __syncwarp();  // the next sub-batch rewrites the scratch rows
       }
-      __syncwarp();  // the next sub-batch rewrites the scratch rows
+      // The stage is refilled by TMA (async proxy) after this release; order
+      // this warp's generic-proxy writes into it (the transpose) before that.
+      if (C::XPOSE_IN_K) fence_proxy_async_smem();
     }
-    // The stage is refilled by TMA (async proxy) after this release; order
-    // this warp's generic-proxy writes into it (the transpose) before that.
-    if (C::XPOSE_IN_K) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
-  }
+    if (!(m.y & kLastRow)) continue;
 
-  // ------------------------------------------------- merge inside the warp
-  float lsum = my_l;
+    // ============================================ end of segment: merge
+    float lsum = my_l;
 #pragma unroll
-  for (int b = 1; b < C::LPH; b <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, b);
+    for (int bb = 1; bb < C::LPH; bb <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, bb);
 #pragma unroll
-  for (int b = C::T; b < 32; b <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, b);
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-    for (int e = 0; e < C::EP; ++e)
-#pragma unroll
-      for (int b = C::T; b < 32; b <<= 1) {
-        o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, b);
-        o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, b);
-      }
-  // The merge buffer aliases the ring: wait until every warp is done with
-  // it.  Every block was issued and consumed unless the CTA aborted (then
-  // copies may be in flight and nothing more is written).
-  named_barrier_sync(1, C::NC * 32);
-  if (*abort_flag) return;
-  float* comb_o = reinterpret_cast<float*>(smem);          // [NC][GMAX][D]
-  float* comb_ml = comb_o + C::NC * GMAX * D;               // [NC][GMAX][2]
-  if (g == 0) {
+    for (int bb = C::T; bb < 32; bb <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, bb);
 #pragma unroll
     for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-      for (int j = 0; j < C::CPL; ++j) {
-        float4* dst = reinterpret_cast<float4*>(comb_o + (warp * GMAX + h) * D + (li + C::T * j) * 8);
-        dst[0] = make_float4(o2[h][j * 4 + 0].x, o2[h][j * 4 + 0].y, o2[h][j * 4 + 1].x, o2[h][j * 4 + 1].y);
-        dst[1] = make_float4(o2[h][j * 4 + 2].x, o2[h][j * 4 + 2].y, o2[h][j * 4 + 3].x, o2[h][j * 4 + 3].y);
+      for (int e = 0; e < C::EP; ++e)
+#pragma unroll
+        for (int bb = C::T; bb < 32; bb <<= 1) {
+          o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, bb);
+          o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, bb);
+        }
+    if (!csync()) break;  // all warps are done with the weight buffers
+    if (g == 0) {
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+        for (int j = 0; j < C::CPL; ++j) {
+          float4* dst = reinterpret_cast<float4*>(comb_o + (warp * GMAX + h) * D + (li + C::T * j) * 8);
+          dst[0] = make_float4(o2[h][j * 4 + 0].x, o2[h][j * 4 + 0].y, o2[h][j * 4 + 1].x,
+                               o2[h][j * 4 + 1].y);
+          dst[1] = make_float4(o2[h][j * 4 + 2].x, o2[h][j * 4 + 2].y, o2[h][j * 4 + 3].x,
+                               o2[h][j * 4 + 3].y);
+        }
+      if (li % C::LPH == 0) {
+        comb_ml[(warp * GMAX + my_h) * 2 + 0] = my_m;
+        comb_ml[(warp * GMAX + my_h) * 2 + 1] = lsum;
       }
-    if (li % C::LPH == 0) {
-      comb_ml[(warp * GMAX + my_h) * 2 + 0] = my_m;
-      comb_ml[(warp * GMAX + my_h) * 2 + 1] = lsum;
     }
-  }
-  named_barrier_sync(1, C::NC * 32);
-
-  // ------------------------------------------------ merge across the warps
-  for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
-    const int h = it / (D / 2);
-    const int d = (it % (D / 2)) * 2;
-    float M = kNegBig;
+    if (!csync()) break;
+    const int head0 = si.kvh * a.group;
+    const int pslot = si.kind == kTail ? 1 : 0;
+    for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
+      const int h = it / (D / 2);
+      const int d = (it % (D / 2)) * 2;
+      float M = kNegBig;
 #pragma unroll
-    for (int w = 0; w < C::NC; ++w) M = fmaxf(M, comb_ml[(w * GMAX + h) * 2]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
+      for (int w = 0; w < C::NC; ++w) M = fmaxf(M, comb_ml[(w * GMAX + h) * 2]);
+      float L = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
-    for (int w = 0; w < C::NC; ++w) {
-      const float wt = fast_exp2(comb_ml[(w * GMAX + h) * 2] - M);
-      L = fmaf(wt, comb_ml[(w * GMAX + h) * 2 + 1], L);
-      const float2 ov = *reinterpret_cast<const float2*>(comb_o + (w * GMAX + h) * D + d);
-      o0 = fmaf(wt, ov.x, o0);
-      o1 = fmaf(wt, ov.y, o1);
+      for (int w = 0; w < C::NC; ++w) {
+        const float wt = fast_exp2(comb_ml[(w * GMAX + h) * 2] - M);
+        L = fmaf(wt, comb_ml[(w * GMAX + h) * 2 + 1], L);
+        const float2 ov = *reinterpret_cast<const float2*>(comb_o + (w * GMAX + h) * D + d);
+        o0 = fmaf(wt, ov.x, o0);
+        o1 = fmaf(wt, ov.y, o1);
+      }
+      const float inv = 1.f / L;
+      if (si.kind == kWhole) {
+        *reinterpret_cast<__nv_bfloat162*>(
+            a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
+            __floats2bfloat162_rn(o0 * inv, o1 * inv);
+      } else {
+        const size_t rec = (static_cast<size_t>(cta) * 2 + pslot) * a.group + h;
+        *reinterpret_cast<float2*>(a.part_o + rec * D + d) = make_float2(o0 * inv, o1 * inv);
+        if (d == 0) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(M, L);
+      }
     }
-    const float inv = 1.f / L;
-    const int head = head0 + h;
-    if (nparts == 1) {
-      *reinterpret_cast<__nv_bfloat162*>(a.out + (static_cast<size_t>(row) * a.num_heads + head) * D + d) =
-          __floats2bfloat162_rn(o0 * inv, o1 * inv);
-    } else {
-      const size_t base = (static_cast<size_t>(seq) * a.num_heads + head) * a.max_parts + part;
-      *reinterpret_cast<float2*>(a.part_o + base * D + d) = make_float2(o0 * inv, o1 * inv);
-      if (d == 0) *reinterpret_cast<float2*>(a.part_ml + base * 2) = make_float2(M, L);
+    if (si.kind != kWhole) {
+      // Publish the partial; the last of the pair's contributors merges them.
+      __threadfence();
+      if (!csync()) break;
+      const long long W = *total_tiles;
+      const int c0 = cta_of_tile(W, a.num_ctas, si.t0);
+      const int c1 = cta_of_tile(W, a.num_ctas, si.t0 + si.nblk - 1);
+      if (threadIdx.x == 0)
+        *last_flag = contribute(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh,
+                                a.epoch, c1 - c0 + 1, a.status, si.r) ? 1 : 0;
+      if (!csync()) break;
+      if (*last_flag) {
+        __threadfence();
+        for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
+          const int h = it / (D / 2);
+          const int d = (it % (D / 2)) * 2;
+          float M = kNegBig;
+          for (int c = c0; c <= c1; ++c) {
+            const size_t rec = (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * a.group + h;
+            M = fmaxf(M, __ldcg(a.part_ml + rec * 2));
+          }
+          float L = 0.f, o0 = 0.f, o1 = 0.f;
+          for (int c = c0; c <= c1; ++c) {
+            const size_t rec = (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * a.group + h;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec * 2));
+            const float wt = ml.y * fast_exp2(ml.x - M);
+            const float2 ov = __ldcg(reinterpret_cast<const float2*>(a.part_o + rec * D + d));
+            L += wt;
+            o0 = fmaf(wt, ov.x, o0);
+            o1 = fmaf(wt, ov.y, o1);
+          }
+          const float inv = 1.f / L;
+          *reinterpret_cast<__nv_bfloat162*>(
+              a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
+              __floats2bfloat162_rn(o0 * inv, o1 * inv);
+        }
+      }
     }
+    if (!csync()) break;  // merge buffers are free again
+    fresh = true;
+    ++seg;
   }
-}
-
-// Second pass for requests split into several partitions:
-//   M = max_j m_j,  w_j = l_j 2^{m_j - M},  O = sum_j w_j O_j / sum_j w_j.
-template <int D>
-__global__ void __launch_bounds__(D) merge_partitions_kernel(const DecodeArgs a) {
-  const int head = blockIdx.x;
-  const int seq = blockIdx.y;
-  const int d = threadIdx.x;
-  int row = seq;
-  if (a.query_start_loc != nullptr) {
-    const int q0 = a.query_start_loc[seq];
-    if (a.query_start_loc[seq + 1] - q0 != 1) return;
-    row = q0;
-    if (row < 0 || row >= a.total_q) return;
-  }
-  const int seq_len = a.seq_lens[seq];
-  if (seq_len < 1 || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * kBlockSize) return;
-  const int nblk_seq = (seq_len + kBlockSize - 1) / kBlockSize;
-  const int nparts = (nblk_seq + a.partition_blocks - 1) / a.partition_blocks;
-  if (nparts <= 1) return;
-  const size_t base = (static_cast<size_t>(seq) * a.num_heads + head) * a.max_parts;
-  const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
-  const float* po = a.part_o + base * D + d;
-  float M = kNegBig;
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, ml[p].x);
-  float L = 0.f, acc = 0.f;
-#pragma unroll 4
-  for (int p = 0; p < nparts; ++p) {
-    const float2 v = ml[p];
-    const float w = v.y * fast_exp2(v.x - M);
-    L += w;
-    acc = fmaf(w, po[static_cast<size_t>(p) * D], acc);
-  }
-  a.out[(static_cast<size_t>(row) * a.num_heads + head) * D + d] = __float2bfloat16_rn(acc / L);
 }
 
 template <int D, int GMAX>
@@ -492,15 +737,8 @@ cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (err != cudaSuccess) return err;
-  const dim3 grid(a.num_kv_heads, a.max_parts, a.num_seqs);
-  paged_decode_kernel<D, GMAX><<<grid, C::THREADS, C::SMEM, stream>>>(kmap, vmap, a);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  if (a.max_parts > 1) {
-    merge_partitions_kernel<D><<<dim3(a.num_heads, a.num_seqs), D, 0, stream>>>(a);
-    err = cudaGetLastError();
-  }
-  return err;
+  paged_decode_kernel<D, GMAX><<<a.num_ctas, C::THREADS, C::SMEM, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -511,6 +749,16 @@ int decode_gmax(int group) {
   if (group <= 4) return 4;
   if (group <= 8) return 8;
   return 0;
+}
+
+int decode_ctas_per_sm(int head_dim, int group) {
+  const int gmax = decode_gmax(group);
+#define PA_DECODE_CASE(DD, GG) \
+  if (head_dim == DD && gmax == GG) return DecodeCfg<DD, GG>::MINB;
+  PA_DECODE_CASE(128, 1) PA_DECODE_CASE(128, 2) PA_DECODE_CASE(128, 4) PA_DECODE_CASE(128, 8)
+  PA_DECODE_CASE(64, 1) PA_DECODE_CASE(64, 2) PA_DECODE_CASE(64, 4) PA_DECODE_CASE(64, 8)
+#undef PA_DECODE_CASE
+  return 1;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

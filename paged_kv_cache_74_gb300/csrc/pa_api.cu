@@ -2,6 +2,8 @@
 // host-side validation, TMA tensor-map encoding, the split-KV partition
 // choice, workspace carving and kernel dispatch.  No entry point allocates
 // device memory or synchronises.
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -48,19 +50,23 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-// Tokens per split-KV partition, in blocks.  The pages' kernel uses 512
-// tokens; smaller partitions are used only when the batch would otherwise
-// leave the GPU's SMs short of CTAs.
-int choose_partition_blocks(int num_seqs, int num_kv_heads, int max_seq_len, int partition_tokens) {
-  if (partition_tokens > 0) return partition_tokens / kBlockSize;
-  const int max_blocks = ceil_div(max_seq_len, kBlockSize);
+// CTAs of the persistent decode grid.  By default as many as fit on the GPU
+// at once (never more than one per kMinTilesPerCta tiles of the batch's
+// upper bound); with partition_tokens > 0, one CTA per that many tokens of
+// the upper bound, resident or not (tests use this to force many splits).
+constexpr int64_t kMinTilesPerCta = 4;
+constexpr int64_t kMaxDecodeCtas = 1 << 22;
+
+int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group, int max_seq_len,
+                        int partition_tokens) {
+  const int64_t upper = static_cast<int64_t>(num_kv_heads) * num_seqs *
+                        ceil_div(max_seq_len, kBlockSize);  // tiles
+  if (partition_tokens > 0) return std::max<int64_t>(1, (upper + partition_tokens / kBlockSize - 1) /
+                                                               (partition_tokens / kBlockSize));
   int sms = sm_count_current_device();
   if (sms <= 0) sms = 148;
-  const int64_t target = 4LL * sms;
-  int pb = 32;
-  while (pb > 8 && static_cast<int64_t>(num_seqs) * num_kv_heads * ceil_div(max_blocks, pb) < target)
-    pb /= 2;
-  return pb;
+  const int64_t resident = static_cast<int64_t>(sms) * decode_ctas_per_sm(head_dim, group);
+  return std::max<int64_t>(1, std::min(resident, (upper + kMinTilesPerCta - 1) / kMinTilesPerCta));
 }
 
 // The K or V cache as a 3-D tensor [slots][kv_heads][head_dim] (innermost
@@ -84,26 +90,35 @@ bool make_cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num
 }
 
 struct DecodeLayout {
-  int partition_blocks = 0;
-  int max_parts = 0;
-  size_t ml_offset = 0, o_offset = 0, total = 0;
+  int64_t num_ctas = 0;
+  size_t counters_offset = 0, ml_offset = 0, o_offset = 0, total = 0;
 };
 
+// Workspace: status record | per-(request, kv head) counters |
+// per-CTA partial (m, l) | per-CTA partial O.
 DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                            int max_seq_len, int partition_tokens) {
   DecodeLayout L;
-  L.partition_blocks = choose_partition_blocks(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
-  L.max_parts = ceil_div(ceil_div(max_seq_len, kBlockSize), L.partition_blocks);
-  L.ml_offset = kWorkspaceHeader;
-  size_t total = kWorkspaceHeader;
-  if (L.max_parts > 1) {
-    const size_t n = static_cast<size_t>(num_seqs) * num_heads * L.max_parts;
-    total = align_up(total + n * 2 * sizeof(float), 256);
-    L.o_offset = total;
-    total += n * head_dim * sizeof(float);
-  }
-  L.total = align_up(total, 256);
+  const int group = num_heads / num_kv_heads;
+  L.num_ctas = decode_num_ctas(num_seqs, num_kv_heads, head_dim, group, max_seq_len,
+                               partition_tokens);
+  size_t off = kWorkspaceHeader;
+  L.counters_offset = off;
+  off = align_up(off + static_cast<size_t>(num_seqs) * num_kv_heads * 8, 256);
+  L.ml_offset = off;
+  off = align_up(off + static_cast<size_t>(L.num_ctas) * 2 * group * 2 * sizeof(float), 256);
+  L.o_offset = off;
+  off += static_cast<size_t>(L.num_ctas) * 2 * group * head_dim * sizeof(float);
+  L.total = align_up(off, 256);
   return L;
+}
+
+// A distinct non-zero tag per decode launch (see the pair counters).
+unsigned next_epoch() {
+  static std::atomic<unsigned> epoch{0};
+  unsigned e = ++epoch;
+  if (e == 0) e = ++epoch;
+  return e;
 }
 
 // Shared shape checks of the attention entry points.
@@ -157,19 +172,20 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
   a.query_start_loc = query_start_loc;
-  a.part_ml = L.max_parts > 1 ? reinterpret_cast<float*>(ws + L.ml_offset) : nullptr;
-  a.part_o = L.max_parts > 1 ? reinterpret_cast<float*>(ws + L.o_offset) : nullptr;
+  a.counters = reinterpret_cast<unsigned long long*>(ws + L.counters_offset);
+  a.part_ml = reinterpret_cast<float*>(ws + L.ml_offset);
+  a.part_o = reinterpret_cast<float*>(ws + L.o_offset);
   a.status = reinterpret_cast<int32_t*>(ws);
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_seqs = num_seqs;
   a.num_heads = num_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = num_heads / num_kv_heads;
-  a.partition_blocks = L.partition_blocks;
-  a.max_parts = L.max_parts;
+  a.num_ctas = static_cast<int>(L.num_ctas);
   a.max_seq_len = max_seq_len;
   a.num_blocks = num_blocks;
   a.total_q = total_q;
+  a.epoch = next_epoch();
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, kmap, vmap, head_dim, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -265,6 +281,7 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
   if (num_seqs == 0) return PA_OK;
   const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
                                        partition_tokens);
+  if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,

@@ -15,27 +15,32 @@ namespace pa {
 constexpr int kBlockSize = 16;        // tokens per KV block (the pages' default)
 constexpr int kWorkspaceHeader = 256; // status record + padding at the start of a workspace
 
-// Decode work: one CTA per (partition, kv head, request).  A partition is a
-// run of `partition_blocks` consecutive logical blocks of one request.
+// Decode work.  The tiles (request, kv head, block) of all decode rows are
+// numbered request-major, then kv head, then block; the W tiles are split
+// into num_ctas contiguous, equal ranges, one per CTA of a persistent grid.
+// A CTA's range covers whole (request, kv head) pairs, written straight to
+// `out`, and at most two pieces of pairs shared with its neighbours, written
+// as partials (m, l, O) and merged by whichever contributor finishes last.
 struct DecodeArgs {
   __nv_bfloat16* out;               // [rows, num_heads, D]
   const __nv_bfloat16* q;           // [rows, num_heads, D]
   const int32_t* block_tables;      // [num_seqs, max_blocks_per_seq]
   const int32_t* seq_lens;          // [num_seqs]
   const int32_t* query_start_loc;   // nullptr: row r = request r; else only q_len == 1 rows
-  float* part_o;                    // [num_seqs, num_heads, max_parts, D] normalised partial O
-  float* part_ml;                   // [num_seqs, num_heads, max_parts, 2] (max in log2 units, sum)
+  unsigned long long* counters;     // [num_seqs * num_kv_heads] (epoch << 32 | contributions)
+  float* part_ml;                   // [num_ctas][2][group][2]  (max in log2 units, exp-sum)
+  float* part_o;                    // [num_ctas][2][group][D]  normalised partial output
   int32_t* status;                  // device status record (may be null)
   int max_blocks_per_seq;
   int num_seqs;
   int num_heads;
   int num_kv_heads;
   int group;                        // num_heads / num_kv_heads
-  int partition_blocks;
-  int max_parts;
+  int num_ctas;
   int max_seq_len;
   int num_blocks;
   int total_q;                      // rows of q / out
+  unsigned epoch;                   // distinct per call (never 0)
   float scale_log2;                 // softmax scale * log2(e)
 };
 
@@ -44,6 +49,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
                           int head_dim, cudaStream_t stream);
 // Smallest group size the decode kernel is instantiated for that covers g.
 int decode_gmax(int group);
+// CTAs per SM the decode kernel for (head_dim, group) is built for.
+int decode_ctas_per_sm(int head_dim, int group);
 
 // Cache writes (cache_write.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
