@@ -89,6 +89,22 @@ bool make_cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tiled tensor map with a 128-byte-swizzled box of {64, 1, rows}: the
+// operand layout the tcgen05 MMAs read (64 bf16 = one 128-byte row).
+bool make_sw128_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {64u, 1u, box_rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DecodeLayout {
   int64_t num_ctas = 0;
   size_t counters_offset = 0, ml_offset = 0, o_offset = 0, total = 0;
@@ -312,14 +328,44 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
       max_query_len > max_seq_len)
     return PA_ERR_INVALID;
   if (num_seqs == 0 || total_q == 0) return PA_OK;
-  if (max_query_len > 1) return PA_ERR_UNSUPPORTED;  // tensor-core tile not built yet
   const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
+  if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (max_query_len > 1) {
+    // Rows with q_len > 1: tensor-core tiles.
+    CUtensorMap qmap, kmap, vmap;
+    const uint64_t slots = static_cast<uint64_t>(num_blocks) * kBlockSize;
+    const uint64_t kv_row = static_cast<uint64_t>(num_kv_heads) * head_dim * 2;
+    if (!make_sw128_map(&qmap, q, head_dim, num_heads, total_q, head_dim * 2,
+                        static_cast<uint64_t>(num_heads) * head_dim * 2, 128) ||
+        !make_sw128_map(&kmap, key_cache, head_dim, num_kv_heads, slots, head_dim * 2, kv_row, 16) ||
+        !make_sw128_map(&vmap, value_cache, head_dim, num_kv_heads, slots, head_dim * 2, kv_row, 16))
+      return PA_ERR_CUDA;
+    PrefillArgs p;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.query_start_loc = query_start_loc;
+    p.status = static_cast<int32_t*>(workspace);
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_heads / num_kv_heads;
+    p.max_seq_len = max_seq_len;
+    p.max_query_len = max_query_len;
+    p.num_blocks = num_blocks;
+    p.total_q = total_q;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (launch_prefill(p, qmap, kmap, vmap, head_dim, cs) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  // Rows with q_len == 1: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, query_start_loc, num_seqs, total_q, max_seq_len, num_heads,
-                            num_kv_heads, head_dim, num_blocks, scale, L, workspace,
-                            static_cast<cudaStream_t>(stream));
+                            num_kv_heads, head_dim, num_blocks, scale, L, workspace, cs);
 }
 
 }  // extern "C"

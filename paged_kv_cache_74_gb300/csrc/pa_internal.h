@@ -52,6 +52,29 @@ int decode_gmax(int group);
 // CTAs per SM the decode kernel for (head_dim, group) is built for.
 int decode_ctas_per_sm(int head_dim, int group);
 
+// Chunked-prefill tiles (prefill.cu): one CTA per (128-row query tile,
+// q head, request) of every request with q_len > 1.
+struct PrefillArgs {
+  __nv_bfloat16* out;               // [total_q, num_heads, D]
+  const __nv_bfloat16* q;           // [total_q, num_heads, D]
+  const int32_t* block_tables;      // [num_seqs, max_blocks_per_seq]
+  const int32_t* seq_lens;          // [num_seqs]
+  const int32_t* query_start_loc;   // [num_seqs + 1]
+  int32_t* status;                  // device status record (may be null)
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int max_seq_len;
+  int max_query_len;
+  int num_blocks;
+  int total_q;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
+
 // Cache writes (cache_write.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
                                      int64_t value_stride, void* key_cache, void* value_cache,
