@@ -39,7 +39,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_decode_kernel
 # launch (full workload, from the committed ncu summary), valid only while
 # the kernel source is unchanged (sha256 of decode.cu at capture time).
-PROFILED_TRAFFIC: dict = {}
+PROFILED_TRAFFIC: dict = {
+    # profiles/decode_llama8b_decode_b64.md: 636.352256 MB read + 3.657472 MB written
+    "llama8b_decode_b64": {"bytes": 640009728, "src_sha": "16eb598d2d91d940"},
+}
 
 
 # ----------------------------------------------------------------- helpers
@@ -313,8 +316,86 @@ def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):
             "d2h_bytes_per_step": d2h}
 
 
+def causal_pairs(w: wl.Workload) -> int:
+    """(query, key) pairs the prefill rows (q_len > 1) attend."""
+    n = 0
+    for r in range(w.num_seqs):
+        ql, L = int(w.q_lens[r]), int(w.seq_lens[r])
+        if ql > 1:
+            ctx = L - ql
+            n += ql * ctx + ql * (ql + 1) // 2
+    return n
+
+
+def _time(call, flush, reps):
+    for _ in range(3):
+        flush.add_(1)
+        call()
+    ms = []
+    for _ in range(reps):
+        flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.median(ms) / 1e3
+
+
+def extra_mixed(pa, name, dev, flush, reps=20):
+    """The mixed chunked-prefill batch: slot mapping + write of every new
+    token + pa_prefill_varlen, and the prefill tiles alone (the chunk's
+    request by itself) as tensor-core FLOP/s."""
+    w = wl.NAMED[name]()
+    t = wl.make_tensors(w, device=dev)
+    ab = algorithmic_bytes(w)
+    ws = pa.new_workspace(pa.prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads,
+                                                    w.num_kv_heads, w.head_dim, w.max_seq_len), dev)
+    out = torch.empty_like(t.q)
+    slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
+
+    def step():
+        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, w.block_size,
+                                w.num_blocks, w.total_q, out=slots)
+        pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+        pa.prefill_varlen(t.q, t.key_cache, t.value_cache, t.query_start_loc, t.seq_lens,
+                          t.block_tables, w.max_query_len, w.max_seq_len, w.scale, out=out,
+                          workspace=ws)
+    s_step = _time(step, flush, reps)
+    # prefill rows alone
+    pre = [r for r in range(w.num_seqs) if w.q_lens[r] > 1]
+    qsl = torch.tensor([0] + list(np.cumsum(w.q_lens[pre])), dtype=torch.int32, device=dev)
+    rows = torch.cat([torch.arange(int(w.query_start_loc[r]), int(w.query_start_loc[r + 1]))
+                      for r in pre]).to(dev)
+    q_p = t.q[rows].contiguous()
+    bt_p = t.block_tables[pre].contiguous()
+    sl_p = t.seq_lens[pre].contiguous()
+    out_p = torch.empty_like(q_p)
+    mql = int(w.q_lens[pre].max())
+    msl = int(w.seq_lens[pre].max())
+    ws_p = pa.new_workspace(pa.prefill_workspace_size(len(pre), q_p.shape[0], w.num_heads,
+                                                      w.num_kv_heads, w.head_dim, msl), dev)
+    pcall = lambda: pa.prefill_varlen(q_p, t.key_cache, t.value_cache, qsl, sl_p, bt_p, mql, msl,
+                                      w.scale, out=out_p, workspace=ws_p)
+    s_pre = _time(pcall, flush, reps)
+    flops = 4.0 * causal_pairs(w) * w.num_heads * w.head_dim
+    res = {"us_per_step": round(s_step * 1e6, 2),
+           "step": "slot_mapping + reshape_and_cache (all new tokens) + prefill_varlen",
+           "step_kv_gbs": round(ab["step_bytes"] / s_step / 1e9, 2),
+           "prefill_only_us": round(s_pre * 1e6, 2),
+           "prefill_tflops": round(flops / s_pre / 1e12, 2),
+           "prefill_gflop": round(flops / 1e9, 3)}
+    del t
+    torch.cuda.empty_cache()
+    return res
+
+
 def extra_decode(pa, name, dev, flush, reps=20):
     """Decode-only timing of another named workload (context for the line)."""
+    if wl.NAMED[name]().max_query_len > 1:
+        return extra_mixed(pa, name, dev, flush, reps)
     w = wl.NAMED[name]()
     t = wl.make_tensors(w, device=dev)
     ab = algorithmic_bytes(w)
@@ -424,7 +505,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode_b64", choices=sorted(wl.NAMED))
     ap.add_argument("--extra", nargs="*", default=["long_ctx_decode_8x32k",
-                                                    "prefix_shared_decode_b256"])
+                                                    "prefix_shared_decode_b256",
+                                                    "mixed_chunked_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

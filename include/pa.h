@@ -20,9 +20,10 @@
  * Conventions shared by every call
  * --------------------------------
  * Pointers.  Every tensor pointer is a DEVICE pointer owned by the caller.
- *   The library allocates no device memory and keeps no per-call state;
- *   scratch space is a caller-provided `workspace` sized by the matching
- *   *_workspace_size() call.  Tensor pointers must be 16-byte aligned.
+ *   No call allocates device memory; scratch space is a caller-provided
+ *   `workspace` sized by the matching *_workspace_size() call (the one
+ *   exception, pa_decode_noalloc, uses a fixed array inside the library).
+ *   Tensor pointers must be 16-byte aligned.
  * Element types.  q, key, value, out and the caches are bf16 (IEEE
  *   binary16-brain, stored as 16-bit patterns); block tables, seq_lens and
  *   query_start_loc are int32; slot mappings are int64.
@@ -35,7 +36,7 @@
  * GQA.  num_heads must be a multiple of num_kv_heads; q head h reads kv head
  *   h / (num_heads / num_kv_heads).
  * Supported sizes.  head_dim 64 or 128; block_size 16; num_heads /
- *   num_kv_heads between 1 and 16.
+ *   num_kv_heads between 1 and 8; num_seqs up to 65535.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy
  *   default stream).  Calls only enqueue work; they never synchronise.
  *   A write through pa_reshape_and_cache must be enqueued before the
@@ -134,8 +135,11 @@ pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
 
 /*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
- * sizes (>= 256: the status record plus the split-KV partials).  The
- * same partition_tokens must be passed to pa_decode.  Returns 0 for
+ * sizes: the status record, one 8-byte counter per (request, kv head) and
+ * two partial records (m, l, O) per CTA of the decode grid.  The same
+ * partition_tokens must be passed to pa_decode, on the same device (the
+ * default grid size depends on its SM count).  No part of the workspace
+ * needs initialising (the counters carry a per-call tag).  Returns 0 for
  * arguments pa_decode would reject.
  */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
@@ -157,9 +161,13 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
  *   max_seq_len   host-side upper bound of seq_lens (sizes the grid; no
  *                 device-to-host read happens)
  *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim))
- *   partition_tokens  tokens per split-KV partition: 0 lets the library
- *                 choose; otherwise a positive multiple of block_size
- *   workspace     >= pa_decode_workspace_size(...) bytes, 256-byte aligned
+ *   partition_tokens  split-KV granularity.  0 (the default) splits the
+ *                 batch's K/V evenly over as many CTAs as the GPU holds at
+ *                 once; a positive multiple of block_size instead uses one
+ *                 CTA per that many tokens of num_seqs * max_seq_len (more,
+ *                 smaller pieces; used to test the merge)
+ *   workspace     >= pa_decode_workspace_size(...) bytes, 256-byte aligned;
+ *                 calls that overlap on the GPU need separate workspaces
  * out[r, h] = sum_t softmax_t(scale * q[r,h] . k_t) v_t over the
  * seq_lens[r] keys of request r (exact attention, fp32 accumulation,
  * rounded once to bf16).
