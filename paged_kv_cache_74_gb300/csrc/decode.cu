@@ -121,19 +121,25 @@ static_assert(sizeof(SegInfo) <= 32, "segment record");
 
 // Blocks of request r that the decode kernel processes (0 for rows that are
 // not decode rows, and for invalid lengths); also its length and q row.
-__device__ __forceinline__ int request_blocks(const DecodeArgs& a, int r, int* seq_len, int* row) {
+// `len` = seq_lens[r]; q0, q1 = query_start_loc[r], [r + 1] (when present).
+__device__ __forceinline__ int blocks_from(const DecodeArgs& a, int r, int len, int q0, int q1,
+                                           int* seq_len, int* row) {
   int rw = r;
   if (a.query_start_loc != nullptr) {
-    const int q0 = a.query_start_loc[r];
-    if (a.query_start_loc[r + 1] - q0 != 1) return 0;  // not a decode row
+    if (q1 - q0 != 1) return 0;  // not a decode row
     rw = q0;
     if (rw < 0 || rw >= a.total_q) return 0;
   }
-  const int len = a.seq_lens[r];
   if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize) return 0;
   *seq_len = len;
   *row = rw;
   return (len + kBlockSize - 1) / kBlockSize;
+}
+
+__device__ __forceinline__ int request_blocks(const DecodeArgs& a, int r, int* seq_len, int* row) {
+  const int q0 = a.query_start_loc != nullptr ? a.query_start_loc[r] : 0;
+  const int q1 = a.query_start_loc != nullptr ? a.query_start_loc[r + 1] : 0;
+  return blocks_from(a, r, a.seq_lens[r], q0, q1, seq_len, row);
 }
 
 // Reports the rows request_blocks() rejects (done once, by CTA 0).
@@ -287,8 +293,37 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           base += __shfl_sync(0xffffffffu, incl, 31);
         }
       }
+      // Block ids: lane L keeps ids 32m + L (m < kRowCache) of the current
+      // request and of the next one in registers, so the kv heads of one
+      // request and the switch to the next request need no global load on
+      // the issue path; ids past the cached ones are fetched one 32-tile
+      // chunk ahead.  The next request's length and q range are read early.
+      constexpr int kRowCache = 4;
+      int cur_ids[kRowCache], nxt_ids[kRowCache];
+      int nxt_r = -1, nxt_len = 0, nxt_q0 = 0, nxt_q1 = 0;
+      auto load_row = [&](int rr, int (&ids)[kRowCache]) {
+        const int32_t* rp = a.block_tables + static_cast<size_t>(rr) * a.max_blocks_per_seq;
+#pragma unroll
+        for (int m = 0; m < kRowCache; ++m) {
+          const int gi = 32 * m + lane;
+          ids[m] = (rr < a.num_seqs && gi < a.max_blocks_per_seq) ? __ldg(rp + gi) : 0;
+        }
+      };
+      auto prefetch_next = [&](int rr) {
+        nxt_r = rr + 1;
+        if (nxt_r < a.num_seqs) {
+          nxt_len = __ldg(a.seq_lens + nxt_r);
+          if (a.query_start_loc != nullptr) {
+            nxt_q0 = __ldg(a.query_start_loc + nxt_r);
+            nxt_q1 = __ldg(a.query_start_loc + nxt_r + 1);
+          }
+        }
+        load_row(nxt_r, nxt_ids);
+      };
       int r = r0, len = 0, row = 0;
+      load_row(r, cur_ids);
       int nb = request_blocks(a, r, &len, &row);
+      prefetch_next(r);
       long long off = lo - base;
       int kvh = static_cast<int>(off / nb);
       int b = static_cast<int>(off % nb);
@@ -331,12 +366,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
         const int rows = (seg_n + C::NC - 1) / C::NC;
-        const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq + b;
-        int my_id = 0;
+        const int32_t* rowp = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
+        const int seg_end = b + seg_n;  // one past the segment's last block
+        int my_id = 0, far_next = 0;
         for (int j = 0; j < rows * C::NC && ok; ++j) {
           if ((j & 31) == 0) {
-            const int jj = j + lane;
-            my_id = jj < seg_n ? __ldg(bt + jj) : 0;
+            const int gi = b + j + lane;  // block of this lane's tile in the chunk
+            int cached = 0;
+#pragma unroll
+            for (int m = 0; m < kRowCache; ++m) {
+              const int v = __shfl_sync(0xffffffffu, cur_ids[m], gi & 31);
+              if ((gi >> 5) == m) cached = v;
+            }
+            if (gi < 32 * kRowCache)
+              my_id = cached;
+            else if (j == 0)
+              my_id = gi < seg_end ? __ldg(rowp + gi) : 0;
+            else
+              my_id = far_next;
+            const int gn = gi + 32;  // next chunk, fetched now
+            far_next = (gn >= 32 * kRowCache && gn < seg_end) ? __ldg(rowp + gn) : 0;
           }
           const int phys = __shfl_sync(0xffffffffu, my_id, j & 31);
           if (lane == 0 && stage_begin(pos)) {
@@ -370,8 +419,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             kvh = 0;
             base += static_cast<long long>(nb) * a.num_kv_heads;
             nb = 0;
-            while (nb == 0 && ++r < a.num_seqs) nb = request_blocks(a, r, &len, &row);
+            while (nb == 0 && ++r < a.num_seqs) {
+              if (r == nxt_r) {
+                nb = blocks_from(a, r, nxt_len, nxt_q0, nxt_q1, &len, &row);
+#pragma unroll
+                for (int m = 0; m < kRowCache; ++m) cur_ids[m] = nxt_ids[m];
+              } else {
+                nb = request_blocks(a, r, &len, &row);
+                load_row(r, cur_ids);
+              }
+            }
             if (nb == 0) ok = false;  // cannot happen while t < hi
+            else prefetch_next(r);
           }
         }
       }
@@ -429,6 +488,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     return false;
   };
 
+  // No abort check per stage: every wait below is bounded on its own.
   for (int pos = warp;; pos += C::NC) {
     const int s = pos % C::STAGES;
     const int landed = mbar_wait(full0 + 8 * s, (pos / C::STAGES) & 1) ? 1 : 0;
@@ -523,9 +583,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           *reinterpret_cast<float4*>(xpose + lane * (C::CH * 4) + ((c ^ (lane % C::CH)) * 4)) =
               make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
         __syncwarp();
-        float sc[C::VPL];
+        // Four independent partial sums keep the add chain short.
+        float sc4[4][C::VPL];
 #pragma unroll
-        for (int u = 0; u < C::VPL; ++u) sc[u] = 0.f;
+        for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+          for (int u = 0; u < C::VPL; ++u) sc4[k4][u] = 0.f;
 #pragma unroll
         for (int l2 = 0; l2 < C::T; ++l2) {
           const int rr = g * C::T + l2;
@@ -533,13 +596,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
               xpose + rr * (C::CH * 4) + (((idx0 / 4) ^ (rr % C::CH)) * 4) + (idx0 % 4);
           if constexpr (C::VPL == 2) {
             const float2 v2 = *reinterpret_cast<const float2*>(src);
-            sc[0] += v2.x;
-            sc[1] += v2.y;
+            sc4[l2 % 4][0] += v2.x;
+            sc4[l2 % 4][1] += v2.y;
           } else {
 #pragma unroll
-            for (int u = 0; u < C::VPL; ++u) sc[u] += src[u];
+            for (int u = 0; u < C::VPL; ++u) sc4[l2 % 4][u] += src[u];
           }
         }
+        float sc[C::VPL];
+#pragma unroll
+        for (int u = 0; u < C::VPL; ++u) sc[u] = (sc4[0][u] + sc4[1][u]) + (sc4[2][u] + sc4[3][u]);
         // Mask tokens past seq_len (and padding heads), then the lazy max.
         float smax = -INFINITY;
 #pragma unroll
@@ -587,30 +653,34 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           p[v + 2] = f.z;
           p[v + 3] = f.w;
         }
-        // A += p v over this sub-batch's tokens.
+        // A += p v over this sub-batch's tokens.  In the last block of a
+        // request the V rows past seq_len may hold NaN and are replaced by 0.
+        auto pv = [&](bool check) {
 #pragma unroll
-        for (int kk = 0; kk < C::SB; ++kk) {
-          const int t = (sb * C::SB + kk) * C::NG + g;
-          uint4 vw[C::CPL];
+          for (int kk = 0; kk < C::SB; ++kk) {
+            const int t = (sb * C::SB + kk) * C::NG + g;
+            uint4 vw[C::CPL];
 #pragma unroll
-          for (int j = 0; j < C::CPL; ++j)
-            vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
-          if (tail && tok0 + t >= seq_len) {
+            for (int j = 0; j < C::CPL; ++j)
+              vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
+            if (check && tok0 + t >= seq_len) {
 #pragma unroll
-            for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);  // may hold NaN
-          }
+              for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
+            for (int h = 0; h < GMAX; ++h) {
+              const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
 #pragma unroll
-            for (int j = 0; j < C::CPL; ++j) {
-              o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
-              o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
-              o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
-              o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+              for (int j = 0; j < C::CPL; ++j) {
+                o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
+                o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
+                o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
+                o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+              }
             }
           }
-        }
+        };
+        if (tail) pv(true); else pv(false);
         __syncwarp();  // the next sub-batch rewrites the scratch rows
       }
       // The stage is refilled by TMA (async proxy) after this release; order

@@ -9,19 +9,32 @@
 // O = softmax(scale * Q K^T) V is computed tile by tile with the online
 // softmax state (m, l) per row and never materialises S or P in HBM.
 //
-// GB300 design.  One CTA of four warps owns 128 query rows of one q head of
-// one request.  TMA with 128-byte swizzle loads the Q tile once and K/V
-// tiles of 128 keys (eight 16-token blocks gathered through the block
-// table) into a two-stage ring.  One thread issues the MMAs:
-//   S = Q K^T   M = N = 128, K = head_dim, both operands K-major, into TMEM;
-//   O_j = P V   M = 128, N = head_dim, K = 128 keys, P K-major from shared
-//               memory, V MN-major exactly as TMA stored it.
-// Each warp reads its 32 rows of S from TMEM (tcgen05.ld), applies the
-// causal and length masks, updates (m, l), and writes P as bf16 into the
-// swizzled layout the next MMA reads; the output accumulator stays in
-// registers (O = alpha O + O_j per tile).  V rows of keys that are out of
-// context or not loaded are zeroed first: they may hold NaN, and a zero
-// weight does not cancel a NaN inside the MMA.
+// GB300 design.  One CTA owns 128 query rows of one q head of one request
+// and is warp-specialised:
+//   warp 8      producer: TMA (128-byte swizzle) loads the Q tile once and
+//               K and V tiles of 128 keys (eight 16-token blocks gathered
+//               through the block table) into two-stage rings, refilling a
+//               K stage as soon as its S MMA is done and a V stage as soon
+//               as its P.V MMA is done;
+//   warp 9      MMA issuer (tcgen05, kind::f16, bf16 in, fp32 accumulate in
+//               TMEM), in the order S_0, S_1, PV_0, S_2, PV_1, ...:
+//                 S_j = Q K_j^T  M = N = 128, K = head_dim, both operands
+//                                K-major, into one of two TMEM S buffers;
+//                 O  += P_j V_j  M = 128, N = head_dim, K = 128 keys; P_j from
+//                                one of two shared-memory buffers (K-major),
+//                                V as an MN-major operand exactly as TMA
+//                                stored it; O accumulates in TMEM;
+//   warps 0-7   softmax: two warps share each 32-row quarter of TMEM and
+//               split the key columns (and the columns of O); each reads its
+//               half of S_j (tcgen05.ld), applies the causal and length
+//               masks, exchanges the row maximum with its partner, and
+//               writes P_j = exp2(S_j * scale * log2 e - m) as bf16 into the
+//               swizzled layout the P.V MMA reads.
+// The reference m of a row moves only when a tile's max exceeds it by more
+// than 2^8; then that row of O (in TMEM) and its sum l are rescaled first
+// (the final O / l is exact for any reference).  V rows of keys that are out
+// of context or were not loaded are zeroed first: they may hold NaN, and a
+// zero weight does not cancel a NaN inside the MMA.  Every wait is bounded.
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -29,6 +42,7 @@ namespace pa {
 namespace {
 
 constexpr float kNegBigP = -1e30f;
+constexpr float kRescaleSlackP = 8.0f;  // log2 units
 
 // Two floats rounded to bf16 (nearest even), packed low / high.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -45,21 +59,36 @@ struct PrefillCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + HALVES * CHUNK;         // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * HALVES * CHUNK;     // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * HALVES * CHUNK;     // 2 key halves
-  static constexpr int OFF_BAR = OFF_P + 2 * CHUNK;            // q, kv[2], s, o
-  static constexpr int OFF_MISC = OFF_BAR + 8 * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;            // + 1024-byte alignment slack
-  static constexpr int THREADS = 128;
-  static constexpr uint32_t TMEM_COLS = 256;                   // S at column 0, O_j at 128
+  static constexpr int OFF_P = OFF_V + 2 * HALVES * CHUNK;     // 2 buffers x 2 key halves
+  static constexpr int NBAR = 14;
+  static constexpr int OFF_BAR = OFF_P + 4 * CHUNK;
+  static constexpr int OFF_RED = OFF_BAR + NBAR * 8;           // [2 halves][128 rows] floats
+  static constexpr int OFF_MISC = OFF_RED + 2 * 128 * 4;
+  static constexpr int SMEM = OFF_MISC + 32 + 1024;            // + 1024-byte alignment slack
+  static constexpr int SOFTMAX_WARPS = 8;
+  static constexpr int THREADS = (SOFTMAX_WARPS + 2) * 32;     // + producer, MMA issuer
+  static constexpr int HC = BN / 2;                            // S columns per softmax thread
+  static constexpr int HD = D / 2;                             // O columns per softmax thread
+  static constexpr uint32_t TMEM_COLS = 512;                   // S0 0, S1 128, O 256
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
-  static constexpr uint32_t KV_BLOCK_BYTES = 2 * HALVES * 16 * 128;  // K and V of one block
+  static constexpr uint32_t BLOCK_BYTES = HALVES * 16 * 128;  // K (or V) of one block
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
+// mbarriers (index into the barrier array)
+constexpr int kQFull = 0;
+constexpr int kKFull = 1;    // [2] K tile landed
+constexpr int kVFull = 3;    // [2] V tile landed
+constexpr int kKFree = 5;    // [2] S MMA that read the K stage is done
+constexpr int kSFull = 7;    // [2] S MMA done
+constexpr int kPFull = 9;    // [2] softmax wrote P (and finished reading S)
+constexpr int kPVDone = 11;  // [2] P.V MMA done (V stage and P buffer free, O current)
+constexpr int kRed = 13;     // softmax-warp barrier (row-max exchange)
+
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -92,7 +121,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   const int n_tiles = (kv_end + C::BN - 1) / C::BN;
   const int nblk_need = (kv_end + kBlockSize - 1) / kBlockSize;
   const int kvh = head / a.group;
-  const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // swizzle atoms
@@ -101,18 +129,17 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint32_t k_s = sbase + C::OFF_K;
   const uint32_t v_s = sbase + C::OFF_V;
   const uint32_t p_s = sbase + C::OFF_P;
-  const uint32_t q_bar = sbase + C::OFF_BAR;
-  const uint32_t kv_bar0 = q_bar + 8;
-  const uint32_t s_bar = q_bar + 24;
-  const uint32_t o_bar = q_bar + 32;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int k) -> uint32_t { return bar0 + 8 * k; };
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [half][row]
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+  volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   if (tid == 0) {
-    mbar_init(q_bar, 1);
-    mbar_init(kv_bar0, 1);
-    mbar_init(kv_bar0 + 8, 1);
-    mbar_init(s_bar, 1);
-    mbar_init(o_bar, 1);
+    for (int k = 0; k < kRed; ++k)
+      mbar_init(bar(k), (k == kPFull || k == kPFull + 1) ? C::SOFTMAX_WARPS : 1);
+    mbar_init(bar(kRed), C::SOFTMAX_WARPS);
+    *fail_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -123,204 +150,264 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const uint64_t policy = l2_policy_evict_first();
-
-  // Block ids of K/V tile t: warp 0 lanes 0..7 each hold one.
-  auto load_ids = [&](int t) -> int {
-    const int b = t * 8 + lane;
-    return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + b) : -1;
+  auto give_up = [&](int where) {
+    record_error(a.status, PA_DEV_WAIT_TIMEOUT, r, where);
+    *fail_flag = 1;
   };
-  // Issue (thread 0) the TMA loads of K/V tile t into stage t % 2; `ids`
-  // holds lane b's block id (warp 0 must be converged: shuffles inside).
-  auto issue_kv = [&](int t, int ids) {
-    int phys[8];
+
+  if (warp == C::SOFTMAX_WARPS) {
+    // ============================================================ producer
+    const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
+    const uint64_t policy = l2_policy_evict_first();
+    auto load_ids = [&](int t) -> int {
+      const int b = t * 8 + lane;
+      return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + b) : -1;
+    };
+    // K or V of tile t into stage t % 2 (lane 0 issues; shuffles inside).
+    auto issue_tile = [&](bool is_v, int t, int ids) {
+      int phys[8];
 #pragma unroll
-    for (int b = 0; b < 8; ++b) phys[b] = __shfl_sync(0xffffffffu, ids, b);
-    if (lane == 0 && t < n_tiles) {
-      const int st = t & 1;
-      const int nb = min(8, nblk_need - t * 8);
-      const uint32_t bar = kv_bar0 + 8 * st;
-      mbar_arrive_expect_tx(bar, nb * C::KV_BLOCK_BYTES);
-      for (int b = 0; b < nb; ++b) {
-        int row_c = phys[b] * kBlockSize;
-        if (static_cast<unsigned>(phys[b]) >= static_cast<unsigned>(a.num_blocks)) {
-          record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys[b]);
-          row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
-        }
+      for (int b = 0; b < 8; ++b) phys[b] = __shfl_sync(0xffffffffu, ids, b);
+      if (lane == 0) {
+        const int st = t & 1;
+        const int nb = min(8, nblk_need - t * 8);
+        const uint32_t full = bar((is_v ? kVFull : kKFull) + st);
+        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK;
+        mbar_arrive_expect_tx(full, nb * C::BLOCK_BYTES);
+        for (int b = 0; b < nb; ++b) {
+          int row_c = phys[b] * kBlockSize;
+          if (static_cast<unsigned>(phys[b]) >= static_cast<unsigned>(a.num_blocks)) {
+            if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys[b]);
+            row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
+          }
 #pragma unroll
-        for (int h = 0; h < C::HALVES; ++h) {
-          tma_load_3d(k_s + (st * C::HALVES + h) * C::CHUNK + b * 2048, &kmap, bar, 64 * h, kvh,
-                      row_c, policy);
-          tma_load_3d(v_s + (st * C::HALVES + h) * C::CHUNK + b * 2048, &vmap, bar, 64 * h, kvh,
-                      row_c, policy);
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_3d(dst + h * C::CHUNK + b * 2048, is_v ? &vmap : &kmap, full, 64 * h, kvh,
+                        row_c, policy);
         }
       }
-    }
-  };
-
-  int ids_next = 0;
-  if (warp == 0) {
+    };
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(q_bar, C::HALVES * C::CHUNK);
+      mbar_arrive_expect_tx(bar(kQFull), C::HALVES * C::CHUNK);
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h)
-        tma_load_3d(q_s + h * C::CHUNK, &qmap, q_bar, 64 * h, head, q0 + row0, policy);
+        tma_load_3d(q_s + h * C::CHUNK, &qmap, bar(kQFull), 64 * h, head, q0 + row0, policy);
     }
-    issue_kv(0, load_ids(0));
-    issue_kv(1, load_ids(1));
-    ids_next = load_ids(2);
-  }
-
-  // Per-row online-softmax state; thread tid owns query row tid of the tile.
-  const int i_row = tid;
-  const int limit = min(ctx + row0 + i_row, kv_end - 1);  // last key this row may see
-  const float sl2 = a.scale_log2;
-  float m_run = kNegBigP, l_run = 0.f;
-  float o_acc[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) o_acc[d] = 0.f;
-  bool failed = false;
-
-  for (int j = 0; j < n_tiles; ++j) {
-    const int st = j & 1;
-    // ---- S = Q K^T
-    if (tid == 0) {
-      bool ok = (j > 0 || mbar_wait(q_bar, 0)) && mbar_wait(kv_bar0 + 8 * st, (j >> 1) & 1);
-      if (ok) {
+    int ids = load_ids(0);
+    int ids_next = load_ids(1);
+    for (int t = 0; t < n_tiles; ++t) {
+      int ok = 1;
+      // K stage t % 2 held K_{t-2}: free once S_{t-2} is done.
+      if (lane == 0 && t >= 2 && !mbar_wait(bar(kKFree + (t & 1)), ((t - 2) >> 1) & 1)) ok = 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_tile(false, t, ids);
+      // V stage t % 2 held V_{t-2}: free once P_{t-2} V_{t-2} is done.
+      if (lane == 0 && t >= 2 && !mbar_wait(bar(kPVDone + (t & 1)), ((t - 2) >> 1) & 1)) ok = 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_tile(true, t, ids);
+      ids = ids_next;
+      ids_next = load_ids(t + 2);
+    }
+  } else if (warp == C::SOFTMAX_WARPS + 1) {
+    // ========================================================== MMA issuer
+    if (lane == 0) {
+      auto issue_s = [&](int t) -> bool {  // S_t = Q K_t^T into S buffer t % 2
+        // S buffer t % 2 held S_{t-2}: its softmax must be done reading it.
+        if (t >= 2 && !mbar_wait(bar(kPFull + (t & 1)), ((t - 2) >> 1) & 1)) return false;
+        if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) return false;
         tc_fence_after();
+        const uint32_t kst = k_s + (t & 1) * C::HALVES * C::CHUNK;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * C::CHUNK + (ks % 4) * 32;
-          umma_bf16(tmem, sdesc_sw128(q_s + off, 16, 1024),
-                    sdesc_sw128(k_s + st * C::HALVES * C::CHUNK + off, 16, 1024), C::IDESC_S,
-                    ks > 0);
+          umma_bf16(tmem + (t & 1) * C::BN, sdesc_sw128(q_s + off, 16, 1024),
+                    sdesc_sw128(kst + off, 16, 1024), C::IDESC_S, ks > 0);
         }
-        umma_commit(s_bar);
-      } else {
-        record_error(a.status, PA_DEV_WAIT_TIMEOUT, r, 10);
-      }
-    }
-    const bool s_ok = mbar_wait(s_bar, j & 1);
-    if (__syncthreads_or(!s_ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-
-    // ---- masks, online softmax, P (bf16) into shared memory
-    const int key0 = j * C::BN;
-    const bool full_tile = key0 + C::BN - 1 <= ctx + row0 && key0 + C::BN <= seq_len;
-    float mx = -INFINITY;
+        umma_commit(bar(kSFull + (t & 1)));
+        umma_commit(bar(kKFree + (t & 1)));
+        return true;
+      };
+      bool ok = mbar_wait(bar(kQFull), 0) && issue_s(0) && (n_tiles < 2 || issue_s(1));
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int sb = j & 1;
+        ok = mbar_wait(bar(kPFull + sb), (j >> 1) & 1) && mbar_wait(bar(kVFull + sb), (j >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < C::BN / 32; ++c) {
-      float sv[32];
-      tmem_ld32(tmem_lane + c * 32, sv);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const bool ok = full_tile || key0 + c * 32 + e <= limit;
-        mx = fmaxf(mx, ok ? sv[e] : -INFINITY);
+        for (int ks = 0; ks < C::BN / 16; ++ks) {
+          umma_bf16(tmem + 256, sdesc_sw128(p_s + (sb * 2 + ks / 4) * C::CHUNK + (ks % 4) * 32, 16, 1024),
+                    sdesc_sw128(v_s + sb * C::HALVES * C::CHUNK + ks * 2048, C::CHUNK, 1024),
+                    C::IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(kPVDone + sb));
+        if (j + 2 < n_tiles) ok = issue_s(j + 2);
       }
+      if (!ok) give_up(12);
     }
-    const float m_new = fmaxf(m_run, mx * sl2);
-    const float alpha = fast_exp2(m_run - m_new);
-    l_run *= alpha;
-    m_run = m_new;
-    float psum = 0.f;
-#pragma unroll
-    for (int c = 0; c < C::BN / 32; ++c) {
-      float sv[32];
-      tmem_ld32(tmem_lane + c * 32, sv);
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const bool ok0 = full_tile || key0 + c * 32 + e <= limit;
-        const bool ok1 = full_tile || key0 + c * 32 + e + 1 <= limit;
-        const float p0 = ok0 ? fast_exp2(fmaf(sv[e], sl2, -m_new)) : 0.f;
-        const float p1 = ok1 ? fast_exp2(fmaf(sv[e + 1], sl2, -m_new)) : 0.f;
-        pk[e / 2] = pack_bf16x2(p0, p1);
-        psum += bf16_lo(pk[e / 2]) + bf16_hi(pk[e / 2]);  // the sum uses the rounded weights
-      }
-      // keys c*32 .. c*32+31 = 4 chunks of 8 in key half c / 2
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = (c % 2) * 4 + q;  // chunk within the 64-key half
-        const uint32_t addr = p_s + (c / 2) * C::CHUNK + i_row * 128 + ((chunk ^ (i_row & 7)) * 16);
-        st_shared_v4(addr, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
-      }
-    }
-    l_run += psum;
-    // V rows of keys past the context or never loaded may hold NaN: zero them.
-    const int kz = min(seq_len, kv_end) - key0;  // keys [kz, BN) of this tile are unused
-    if (kz < C::BN) {
-      const int nz = (C::BN - max(kz, 0)) * C::HALVES * 8;
-      for (int idx = tid; idx < nz; idx += C::THREADS) {
-        const int row = max(kz, 0) + idx / (C::HALVES * 8);
-        const int h = (idx / 8) % C::HALVES;
-        st_shared_v4(v_s + (st * C::HALVES + h) * C::CHUNK + row * 128 + (idx % 8) * 16,
-                     make_uint4(0u, 0u, 0u, 0u));
-      }
-    }
-    fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor core
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- O_j = P V
-    if (tid == 0) {
+  } else {
+    // ============================================================ softmax
+    // Warp w serves rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
+    // column half w / 4 of S and of O; thread row i = 32 (w % 4) + lane.
+    const int half = warp >> 2;
+    const int i_row = (warp & 3) * 32 + lane;
+    const uint32_t tmem_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tmem_o = 256;
+    const int limit = min(ctx + row0 + i_row, kv_end - 1);  // last key this row may see
+    const float sl2 = a.scale_log2;
+    float m_ref = kNegBigP, l_run = 0.f;  // both threads of a row keep the same m_ref
+    bool ok = true;
+    uint32_t red_phase = 0;
+    // Barrier of the eight softmax warps (bounded; orders the red[] writes).
+    auto red_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kRed));
+      const int done = mbar_wait(bar(kRed), red_phase & 1) ? 1 : 0;
+      ++red_phase;
+      return __all_sync(0xffffffffu, done) != 0;
+    };
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sb), (j >> 1) & 1) ? 1 : 0) != 0;
+      if (!ok) break;
       tc_fence_after();
+      uint32_t sraw[C::HC];
 #pragma unroll
-      for (int ks = 0; ks < C::BN / 16; ++ks) {
-        umma_bf16(tmem + C::BN,
-                  sdesc_sw128(p_s + (ks / 4) * C::CHUNK + (ks % 4) * 32, 16, 1024),
-                  sdesc_sw128(v_s + st * C::HALVES * C::CHUNK + ks * 2048, C::CHUNK, 1024),
-                  C::IDESC_O, ks > 0);
+      for (int c = 0; c < C::HC / 32; ++c)
+        tmem_ld32_async(tmem_row + sb * C::BN + half * C::HC + c * 32, sraw + 32 * c);
+      tmem_wait_ld();
+      const int key0 = j * C::BN + half * C::HC;  // key of this thread's first column
+      const bool full_tile = j * C::BN + C::BN - 1 <= ctx + row0 && j * C::BN + C::BN <= seq_len;
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+      if (full_tile) {
+#pragma unroll
+        for (int e = 0; e < C::HC; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], __uint_as_float(sraw[e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < C::HC; ++e)
+          mx8[e % 8] = fmaxf(mx8[e % 8], key0 + e <= limit ? __uint_as_float(sraw[e]) : -INFINITY);
       }
-      umma_commit(o_bar);
-    }
-    const bool o_ok = mbar_wait(o_bar, j & 1);
-    if (__syncthreads_or(!o_ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      red[half * 128 + i_row] = mx;
+      if (!(ok = red_sync())) break;
+      mx = fmaxf(mx, red[(half ^ 1) * 128 + i_row]);  // the partner's half of the row
+      const float m_tile = mx * sl2;
+      const bool need = m_tile > m_ref + kRescaleSlackP;
+      if (__any_sync(0xffffffffu, need)) {
+        // O (in TMEM) must hold P_{j-1} V_{j-1} before its rows are rescaled.
+        if (j > 0)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(kPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1) ? 1 : 0) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        const float m_new = need ? m_tile : m_ref;
+        const float alpha = fast_exp2(m_ref - m_new);
+        if (j > 0) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float ov[32];
-      tmem_ld32(tmem_lane + C::BN + c * 32, ov);
+          for (int c = 0; c < C::HD / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o_acc[c * 32 + e] = fmaf(o_acc[c * 32 + e], alpha, ov[e]);
+            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+            tmem_st32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
+          }
+        }
+        l_run *= alpha;
+        m_ref = m_new;
+      }
+      // P buffer sb was read by P_{j-2} V_{j-2}: it must be done.
+      if (j >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + sb), ((j - 2) >> 1) & 1) ? 1 : 0) != 0;
+      if (!ok) break;
+      float ps8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::HC / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int k = c * 32 + e;
+          float p0 = fast_exp2(fmaf(__uint_as_float(sraw[k]), sl2, -m_ref));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sraw[k + 1]), sl2, -m_ref));
+          if (!full_tile) {
+            p0 = key0 + k <= limit ? p0 : 0.f;
+            p1 = key0 + k + 1 <= limit ? p1 : 0.f;
+          }
+          pk[e / 2] = pack_bf16x2(p0, p1);
+          ps8[(e / 2) % 8] += bf16_lo(pk[e / 2]) + bf16_hi(pk[e / 2]);  // rounded weights
+        }
+        // keys half*64 + c*32 .. +31 = chunks 4c .. 4c+3 of key half `half`
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = c * 4 + q;
+          const uint32_t addr =
+              p_s + (sb * 2 + half) * C::CHUNK + i_row * 128 + ((chunk ^ (i_row & 7)) * 16);
+          st_shared_v4(addr, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+        }
+      }
+      l_run += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      // V rows of keys past the needed range or never loaded may hold NaN.
+      const int kz = kv_end - j * C::BN;  // keys [kz, BN) of this tile are unused
+      if (kz < C::BN) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + sb), (j >> 1) & 1) ? 1 : 0) != 0;
+        if (!ok) break;
+        const int nz = (C::BN - max(kz, 0)) * C::HALVES * 8;
+        for (int idx = tid; idx < nz; idx += C::SOFTMAX_WARPS * 32) {
+          const int row = max(kz, 0) + idx / (C::HALVES * 8);
+          const int h = (idx / 8) % C::HALVES;
+          st_shared_v4(v_s + (sb * C::HALVES + h) * C::CHUNK + row * 128 + (idx % 8) * 16,
+                       make_uint4(0u, 0u, 0u, 0u));
+        }
+      }
+      fence_proxy_async_smem();  // P_j and the zeroed rows are read by the tensor core
+      tc_fence_before();         // S_j reads and O rescales precede the next MMAs
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kPFull + sb));
     }
-    // Stage st is free (its MMAs are done): refill it with tile j + 2.
-    if (warp == 0) {
-      issue_kv(j + 2, ids_next);
-      ids_next = load_ids(j + 3);
+    // ---- epilogue: O / l
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + ((n_tiles - 1) & 1)),
+                                             ((n_tiles - 1) >> 1) & 1) ? 1 : 0) != 0;
+    if (ok) {
+      red[half * 128 + i_row] = l_run;
+      ok = red_sync();
     }
-    tc_fence_before();
-    __syncthreads();  // S and O_j in TMEM may be overwritten now
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / (l_run + red[(half ^ 1) * 128 + i_row]);
+      __nv_bfloat16* dst =
+          a.out + (static_cast<size_t>(q0 + row0 + i_row) * a.num_heads + head) * D + half * C::HD;
+#pragma unroll
+      for (int c = 0; c < C::HD / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
+        if (i_row < rows) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            const uint4 v = make_uint4(pack_bf16x2(ov[e] * inv, ov[e + 1] * inv),
+                                       pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv),
+                                       pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv),
+                                       pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv));
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      give_up(13);
+    }
   }
 
-  if (!failed && i_row < rows) {
-    const float inv = 1.f / l_run;
-    __nv_bfloat16* dst = a.out + (static_cast<size_t>(q0 + row0 + i_row) * a.num_heads + head) * D;
-#pragma unroll
-    for (int d = 0; d < D; d += 8) {
-      const uint4 v = make_uint4(pack_bf16x2(o_acc[d] * inv, o_acc[d + 1] * inv),
-                                 pack_bf16x2(o_acc[d + 2] * inv, o_acc[d + 3] * inv),
-                                 pack_bf16x2(o_acc[d + 4] * inv, o_acc[d + 5] * inv),
-                                 pack_bf16x2(o_acc[d + 6] * inv, o_acc[d + 7] * inv));
-      *reinterpret_cast<uint4*>(dst + d) = v;
-    }
-  }
-  if (failed && tid == 0) {
-    record_error(a.status, PA_DEV_WAIT_TIMEOUT, r, 11);
-    // Let issued copies and MMAs finish before the CTA leaves (bounded).
-    (void)mbar_wait(kv_bar0, 0);
-    (void)mbar_wait(kv_bar0 + 8, 0);
-    (void)mbar_wait(s_bar, 0);
-    (void)mbar_wait(o_bar, 0);
+  __syncthreads();
+  if (*fail_flag && tid == 0) {
+    // Let copies and MMAs still in flight finish before TMEM is released
+    // and the CTA leaves (bounded; some of these phases may never come).
+    for (int k = 0; k < kRed; ++k) (void)mbar_wait(bar(k), 0);
   }
   tc_fence_before();
   __syncthreads();
