@@ -129,6 +129,35 @@ DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int he
   return L;
 }
 
+// A side stream (and fork / join events) per device, created on first use
+// and kept for the life of the process: pa_prefill_varlen runs the prefill
+// tiles on it, concurrently with the decode rows on the caller's stream.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+const SideStream* side_stream_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& s = g_side[dev];
+  if (s.stream == nullptr) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    s.stream = st;
+    s.fork = f;
+    s.join = j;
+  }
+  return &s;
+}
+
 // A distinct non-zero tag per decode launch (see the pair counters).
 unsigned next_epoch() {
   static std::atomic<unsigned> epoch{0};
@@ -346,6 +375,8 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     PrefillArgs p;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.q = static_cast<const __nv_bfloat16*>(q);
+    p.key_cache = static_cast<const __nv_bfloat16*>(key_cache);
+    p.value_cache = static_cast<const __nv_bfloat16*>(value_cache);
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.query_start_loc = query_start_loc;
@@ -360,9 +391,25 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     p.num_blocks = num_blocks;
     p.total_q = total_q;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (launch_prefill(p, qmap, kmap, vmap, head_dim, cs) != cudaSuccess) return PA_ERR_CUDA;
+    // The tiles run on a side stream, forked from and joined back into the
+    // caller's stream, so they overlap the decode rows.
+    const SideStream* side = side_stream_current_device();
+    if (side == nullptr) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_side_mu);  // one fork / join at a time per process
+    if (cudaEventRecord(side->fork, cs) != cudaSuccess ||
+        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (launch_prefill(p, qmap, kmap, vmap, head_dim, side->stream) != cudaSuccess) return PA_ERR_CUDA;
+    const pa_status st = launch_decode_rows(out, q, key_cache, value_cache, block_tables,
+                                            max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                            total_q, max_seq_len, num_heads, num_kv_heads, head_dim,
+                                            num_blocks, scale, L, workspace, cs);
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    return st;
   }
-  // Rows with q_len == 1: the decode kernel.
+  // Only decode rows: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, query_start_loc, num_seqs, total_q, max_seq_len, num_heads,
                             num_kv_heads, head_dim, num_blocks, scale, L, workspace, cs);

@@ -57,6 +57,8 @@ int decode_ctas_per_sm(int head_dim, int group);
 struct PrefillArgs {
   __nv_bfloat16* out;               // [total_q, num_heads, D]
   const __nv_bfloat16* q;           // [total_q, num_heads, D]
+  const __nv_bfloat16* key_cache;   // [num_blocks * 16, num_kv_heads, D]
+  const __nv_bfloat16* value_cache; // same layout
   const int32_t* block_tables;      // [num_seqs, max_blocks_per_seq]
   const int32_t* seq_lens;          // [num_seqs]
   const int32_t* query_start_loc;   // [num_seqs + 1]

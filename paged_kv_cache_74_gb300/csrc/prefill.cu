@@ -163,29 +163,27 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       const int b = t * 8 + lane;
       return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + b) : -1;
     };
-    // K or V of tile t into stage t % 2 (lane 0 issues; shuffles inside).
+    // K or V of tile t into stage t % 2: lane 0 posts the byte count, then
+    // lanes 0..7 each issue the TMA copies of their own block (lane b holds
+    // the id of block b of the tile).
     auto issue_tile = [&](bool is_v, int t, int ids) {
-      int phys[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) phys[b] = __shfl_sync(0xffffffffu, ids, b);
-      if (lane == 0) {
-        const int st = t & 1;
-        const int nb = min(8, nblk_need - t * 8);
-        const uint32_t full = bar((is_v ? kVFull : kKFull) + st);
-        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK;
-        mbar_arrive_expect_tx(full, nb * C::BLOCK_BYTES);
-        for (int b = 0; b < nb; ++b) {
-          int row_c = phys[b] * kBlockSize;
-          if (static_cast<unsigned>(phys[b]) >= static_cast<unsigned>(a.num_blocks)) {
-            if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys[b]);
-            row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
-          }
-#pragma unroll
-          for (int h = 0; h < C::HALVES; ++h)
-            tma_load_3d(dst + h * C::CHUNK + b * 2048, is_v ? &vmap : &kmap, full, 64 * h, kvh,
-                        row_c, policy);
+      const int st = t & 1;
+      const int nb = min(8, nblk_need - t * 8);
+      const uint32_t full = bar((is_v ? kVFull : kKFull) + st);
+      if (lane == 0) mbar_arrive_expect_tx(full, nb * C::BLOCK_BYTES);
+      __syncwarp();
+      if (lane < nb) {
+        int row_c = ids * kBlockSize;
+        if (static_cast<unsigned>(ids) >= static_cast<unsigned>(a.num_blocks)) {
+          if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, ids);
+          row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
         }
+        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK + lane * 2048;
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_3d(dst + h * C::CHUNK, is_v ? &vmap : &kmap, full, 64 * h, kvh, row_c, policy);
       }
+      __syncwarp();
     };
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
