@@ -238,6 +238,11 @@ size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_
  * tcgen05 tensor-core prefill tile; rows with q_len == 1 run the decode
  * kernel; requests with q_len == 0 produce no rows.  K/V of this step's
  * tokens must already be in the cache (pa_reshape_and_cache first).
+ * When max_query_len > 1 the tensor-core tiles run on a side stream that
+ * the library creates once per device (with one fork and one join event)
+ * and keeps until exit; it is forked from `stream` and joined back into it
+ * inside this call, so ordering on `stream` is as for a single kernel.
+ * Make the first such call on a device before any stream capture.
  */
 pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
                             const void* value_cache, const int32_t* query_start_loc,

@@ -206,3 +206,30 @@ def test_seq_len_beyond_bound_is_reported(cuda_lib):
               workspace=ws)
     st = pa.device_status(ws)
     assert st[0] == 3 and st[1] == 2
+
+
+def test_decode_step_in_a_cuda_graph(cuda_lib):
+    """A decode step captured in a CUDA graph replays to the eager result."""
+    pa = cuda_lib
+    w = wl.random_workload(46, num_seqs=16, max_len=2000, num_heads=32, num_kv_heads=8,
+                           head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    ws = pa.new_workspace(pa.decode_workspace_size(16, 32, 8, 128, w.max_seq_len), "cuda")
+    out = torch.empty_like(t.q)
+    call = lambda: pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
+                             w.max_seq_len, w.scale, out=out, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)

@@ -130,3 +130,99 @@ def test_prefill_without_context_is_causal_self_attention(cuda_lib, oracle):
     ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
                                 w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
     assert_close_to_oracle(out, ref, what="prompt")
+
+
+def test_prefill_is_deterministic(cuda_lib):
+    pa = cuda_lib
+    w = wl.random_workload(208, num_seqs=5, max_len=600, num_heads=32, num_kv_heads=8,
+                           head_dim=128, max_q_len=300, prefill_fraction=0.6)
+    t = wl.make_tensors(w, device="cuda")
+    a, _ = run_prefill(pa, w, t)
+    b, _ = run_prefill(pa, w, t)
+    assert torch.equal(a, b)
+
+
+def test_prefill_zero_length_requests_produce_nothing(cuda_lib, oracle):
+    """Requests with q_len == 0 own no rows; the others are unaffected."""
+    pa = cuda_lib
+    lens, qls = [50, 90, 33, 200], [0, 40, 0, 1]
+    w = wl.build_workload("zero", lens, qls, num_heads=8, num_kv_heads=2, head_dim=64,
+                          block_size=16, num_blocks=40, seed=3)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    out, ws = run_prefill(pa, w, t)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    assert_close_to_oracle(out, ref, what="zero-length requests")
+
+
+def test_prefill_bad_block_id_is_reported_not_dereferenced(cuda_lib, oracle):
+    pa = cuda_lib
+    lens, qls = [300, 120, 77], [200, 1, 60]
+    w = wl.build_workload("badblk", lens, qls, num_heads=8, num_kv_heads=2, head_dim=128,
+                          block_size=16, num_blocks=40, seed=4)
+    t = wl.make_tensors(w, device="cuda")
+    bt = t.block_tables.clone()
+    bt[0, 3] = w.num_blocks + 77  # a block the chunk of request 0 reads
+    ws = pa.new_workspace(pa.prefill_workspace_size(3, w.total_q, 8, 2, 128, w.max_seq_len), "cuda")
+    out = pa.prefill_varlen(t.q, t.key_cache, t.value_cache, t.query_start_loc, t.seq_lens, bt,
+                            w.max_query_len, w.max_seq_len, w.scale, workspace=ws)
+    st = pa.device_status(ws)
+    assert st[0] == 2 and st[1] == 0 and st[2] == w.num_blocks + 77
+    ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    rows = slice(int(w.query_start_loc[1]), int(w.query_start_loc[3]))  # requests 1 and 2
+    assert_close_to_oracle(out[rows], ref[rows], what="other requests")
+
+
+def test_prefill_query_longer_than_context_is_reported(cuda_lib):
+    pa = cuda_lib
+    w = wl.build_workload("qlong", [64, 40], [30, 1], num_heads=4, num_kv_heads=2, head_dim=64,
+                          block_size=16, num_blocks=12, seed=5)
+    t = wl.make_tensors(w, device="cuda")
+    sl = t.seq_lens.clone()
+    sl[0] = 20  # fewer keys than the request's 30 new queries
+    ws = pa.new_workspace(pa.prefill_workspace_size(2, w.total_q, 4, 2, 64, w.max_seq_len), "cuda")
+    pa.prefill_varlen(t.q, t.key_cache, t.value_cache, t.query_start_loc, sl, t.block_tables,
+                      w.max_query_len, w.max_seq_len, w.scale, workspace=ws)
+    st = pa.device_status(ws)
+    assert st[0] == 4 and st[1] == 0
+
+
+def test_mixed_step_in_a_cuda_graph(cuda_lib):
+    """Slot mapping, cache write and pa_prefill_varlen captured in one CUDA
+    graph (after an eager warm-up) replay to the eager result."""
+    pa = cuda_lib
+    w = wl.random_workload(209, num_seqs=6, max_len=500, num_heads=32, num_kv_heads=8,
+                           head_dim=128, max_q_len=200, prefill_fraction=0.5)
+    t = wl.make_tensors(w, device="cuda")
+    kc0, vc0 = t.key_cache.clone(), t.value_cache.clone()
+    ws = pa.new_workspace(pa.prefill_workspace_size(w.num_seqs, w.total_q, 32, 8, 128,
+                                                    w.max_seq_len), "cuda")
+    out = torch.empty_like(t.q)
+    slots = torch.empty(w.total_q, dtype=torch.int64, device="cuda")
+
+    def step():
+        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16, w.num_blocks,
+                                w.total_q, out=slots)
+        pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+        pa.prefill_varlen(t.q, t.key_cache, t.value_cache, t.query_start_loc, t.seq_lens,
+                          t.block_tables, w.max_query_len, w.max_seq_len, w.scale, out=out,
+                          workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    t.key_cache.copy_(kc0)
+    t.value_cache.copy_(vc0)
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
