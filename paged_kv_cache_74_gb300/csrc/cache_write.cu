@@ -13,6 +13,9 @@
 // Both are pure data movement.  The cache write gives each token one warp;
 // lanes move 16-byte chunks, so each token's K and V rows (2 KB each at 8 kv
 // heads x 128) are read and written with fully coalesced vector accesses.
+// Both are launched so that they (and the attention launch after them) may
+// be scheduled while the previous kernel in the stream finishes; each waits
+// for that kernel before it touches global memory.
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -27,6 +30,8 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
                          const int64_t* __restrict__ slot_mapping, int num_tokens,
                          int row_chunks, int64_t num_slots, int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();  // slot_mapping may come from the previous kernel
   const int token = blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= num_tokens) return;
@@ -55,6 +60,8 @@ slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
                     const int32_t* __restrict__ query_start_loc,
                     const int32_t* __restrict__ seq_lens, int block_size, int num_blocks,
                     int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int r = blockIdx.x;
   const int q0 = query_start_loc[r];
   const int q1 = query_start_loc[r + 1];
@@ -91,21 +98,20 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      const int64_t* slot_mapping, int num_tokens, int row_elems,
                                      int64_t num_slots, int32_t* status, cudaStream_t stream) {
   const int grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
-  reshape_and_cache_kernel<<<grid, kWriteWarps * 32, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), key_stride / 8,
-      value_stride / 8, static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
-      slot_mapping, num_tokens, row_elems / 8, num_slots, status);
-  return cudaGetLastError();
+  return launch_overlapped(reshape_and_cache_kernel, dim3(grid), dim3(kWriteWarps * 32), 0, stream,
+                           static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                           key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
+                           static_cast<uint4*>(value_cache), slot_mapping, num_tokens,
+                           row_elems / 8, num_slots, status);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,
                                 int max_blocks_per_seq, const int32_t* query_start_loc,
                                 const int32_t* seq_lens, int num_seqs, int block_size,
                                 int num_blocks, int32_t* status, cudaStream_t stream) {
-  slot_mapping_kernel<<<num_seqs, 128, 0, stream>>>(slot_mapping, total_tokens, block_tables,
-                                                    max_blocks_per_seq, query_start_loc, seq_lens,
-                                                    block_size, num_blocks, status);
-  return cudaGetLastError();
+  return launch_overlapped(slot_mapping_kernel, dim3(num_seqs), dim3(128), 0, stream, slot_mapping,
+                           total_tokens, block_tables, max_blocks_per_seq, query_start_loc,
+                           seq_lens, block_size, num_blocks, status);
 }
 
 }  // namespace pa

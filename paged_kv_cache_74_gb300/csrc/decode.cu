@@ -222,6 +222,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // TMA destinations must be 128-byte aligned; the dynamic shared-memory base
   // always is on this GPU, but never issue a copy if it were not.
   if (ring_s & 127) {
+    griddep_wait();
     if (threadIdx.x == 0) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 6);
     return;
   }
@@ -241,6 +242,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_wait();  // the cache write before this launch may still be finishing
 
   if (warp == C::NC) {
     // ================================================================ producer
@@ -807,8 +809,8 @@ cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (err != cudaSuccess) return err;
-  paged_decode_kernel<D, GMAX><<<a.num_ctas, C::THREADS, C::SMEM, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  return launch_overlapped(paged_decode_kernel<D, GMAX>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
+                           stream, kmap, vmap, a);
 }
 
 }  // namespace

@@ -44,6 +44,27 @@ struct DecodeArgs {
   float scale_log2;                 // softmax scale * log2(e)
 };
 
+// Launch `kernel` on `stream` with programmatic stream serialization: the
+// launch may be scheduled while the previous kernel in the stream is still
+// running.  Every kernel launched this way calls griddep_wait() before its
+// first access to global memory, so only its prologue (shared-memory and
+// barrier set-up) overlaps the previous kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launchers (decode.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, cudaStream_t stream);

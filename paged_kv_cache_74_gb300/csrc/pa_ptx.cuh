@@ -37,6 +37,21 @@ __device__ __forceinline__ void record_error(int32_t* status, int code, int who,
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this launch depends on (the previous kernel in the
+// stream, when this one was launched with programmatic stream serialization)
+// has finished and its writes are visible.  Returns at once otherwise.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next launch in the stream, if it opted in, to be scheduled now;
+// it still waits in griddep_wait() for this grid to finish.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
