@@ -36,7 +36,7 @@
  * GQA.  num_heads must be a multiple of num_kv_heads; q head h reads kv head
  *   h / (num_heads / num_kv_heads).
  * Supported sizes.  head_dim 64 or 128; block_size 16; num_heads /
- *   num_kv_heads between 1 and 8; num_seqs up to 65535.
+ *   num_kv_heads between 1 and 16; num_seqs up to 65535.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy
  *   default stream).  Calls only enqueue work; they never synchronise.
  *   A write through pa_reshape_and_cache must be enqueued before the
@@ -170,7 +170,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
  *                 calls that overlap on the GPU need separate workspaces
  * out[r, h] = sum_t softmax_t(scale * q[r,h] . k_t) v_t over the
  * seq_lens[r] keys of request r (exact attention, fp32 accumulation,
- * rounded once to bf16).
+ * rounded once to bf16).  Up to 4 q heads per kv head the products run on
+ * CUDA cores; with 5 to 16 they run on the tensor cores, and the weights
+ * are rounded to bf16 before they multiply V.
  */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -1,0 +1,100 @@
+// decode_common.cuh -- the split of a decode batch into per-CTA tile ranges
+// and the merge of the pieces of a (request, kv head) pair that several
+// CTAs share.  Used by both decode kernels.
+//
+// Every (request, kv head, 16-token block) tile of the decode rows is
+// numbered request-major, then kv head, then block; the W tiles are cut into
+// num_ctas contiguous ranges of equal size.  A range covers whole pairs,
+// written straight to the output, and at most two pieces of pairs shared
+// with its neighbours; those are written as partials (m_j, l_j, O_j) and
+// merged ("vLLM 深度解析（二）：PagedAttention 核心机制", sections 3.2.7 and
+// 3.3: m = max m_j, L = sum l_j e^{m_j - m}, O = sum O_j l_j e^{m_j - m} / L)
+// by the contributor that finishes last.
+#pragma once
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace {
+
+// How a segment's result is written.
+constexpr int kWhole = 0;  // the whole (request, kv head): final bf16 output
+constexpr int kHead = 1;   // continues a pair begun by an earlier CTA: partial slot 0
+constexpr int kTail = 2;   // begins a pair finished by later CTAs: partial slot 1
+
+// Blocks of request r that the decode kernel processes (0 for rows that are
+// not decode rows, and for invalid lengths); also its length and q row.
+// `len` = seq_lens[r]; q0, q1 = query_start_loc[r], [r + 1] (when present).
+__device__ __forceinline__ int blocks_from(const DecodeArgs& a, int r, int len, int q0, int q1,
+                                           int* seq_len, int* row) {
+  int rw = r;
+  if (a.query_start_loc != nullptr) {
+    if (q1 - q0 != 1) return 0;  // not a decode row
+    rw = q0;
+    if (rw < 0 || rw >= a.total_q) return 0;
+  }
+  if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize) return 0;
+  *seq_len = len;
+  *row = rw;
+  return (len + kBlockSize - 1) / kBlockSize;
+}
+
+__device__ __forceinline__ int request_blocks(const DecodeArgs& a, int r, int* seq_len, int* row) {
+  const int q0 = a.query_start_loc != nullptr ? a.query_start_loc[r] : 0;
+  const int q1 = a.query_start_loc != nullptr ? a.query_start_loc[r + 1] : 0;
+  return blocks_from(a, r, a.seq_lens[r], q0, q1, seq_len, row);
+}
+
+// Reports the rows request_blocks() rejects (done once, by CTA 0).
+__device__ void report_bad_rows(const DecodeArgs& a, int lane) {
+  for (int r = lane; r < a.num_seqs; r += 32) {
+    int rw = r;
+    if (a.query_start_loc != nullptr) {
+      const int q0 = a.query_start_loc[r];
+      if (a.query_start_loc[r + 1] - q0 != 1) continue;
+      rw = q0;
+      if (rw < 0 || rw >= a.total_q) {
+        record_error(a.status, PA_DEV_BAD_QUERY_LEN, r, rw);
+        continue;
+      }
+    }
+    const int len = a.seq_lens[r];
+    if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize)
+      record_error(a.status, PA_DEV_BAD_SEQ_LEN, r, len);
+  }
+}
+
+// Equal split of W tiles over C CTAs: CTA c owns [range_lo(c), range_lo(c+1)).
+__device__ __forceinline__ long long range_lo(long long W, int C, int c) {
+  const long long q = W / C, rem = W % C;
+  return static_cast<long long>(c) * q + (c < rem ? c : rem);
+}
+
+// The CTA whose range holds tile t (0 <= t < W).
+__device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
+  const long long q = W / C, rem = W % C;
+  const long long big = rem * (q + 1);
+  if (t < big) return static_cast<int>(t / (q + 1));
+  return static_cast<int>(rem + (t - big) / q);
+}
+
+// Registers this CTA's partial for a pair; true if it was the last of n.
+__device__ bool contribute(unsigned long long* counter, unsigned epoch, int n, int32_t* status,
+                           int who) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+  unsigned long long now = 0;
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    now = (static_cast<unsigned>(old >> 32) == epoch)
+              ? old + 1
+              : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    const unsigned long long seen = atomicCAS(counter, old, now);
+    if (seen == old) return static_cast<int>(now & 0xffffffffu) == n;
+    old = seen;
+  }
+  record_error(status, PA_DEV_WAIT_TIMEOUT, who, 3);
+  return false;
+}
+
+}  // namespace
+}  // namespace pa

@@ -57,6 +57,16 @@ int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 constexpr int64_t kMinTilesPerCta = 4;
 constexpr int64_t kMaxDecodeCtas = 1 << 22;
 
+// Which decode kernel runs.  Up to 4 q heads per kv head the CUDA-core
+// kernel (3 CTAs per SM, 16-token stages) keeps more bytes in flight than
+// the tensor-core one and is faster; from 5 to 16 the q.k and p.v work per
+// byte outgrows the CUDA cores and the tensor-core kernel (one CTA per SM)
+// takes over.
+bool decode_uses_tc(int head_dim, int group) {
+  (void)head_dim;
+  return group > 4;
+}
+
 int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group, int max_seq_len,
                         int partition_tokens) {
   const int64_t upper = static_cast<int64_t>(num_kv_heads) * num_seqs *
@@ -65,7 +75,8 @@ int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group,
                                                                (partition_tokens / kBlockSize));
   int sms = sm_count_current_device();
   if (sms <= 0) sms = 148;
-  const int64_t resident = static_cast<int64_t>(sms) * decode_ctas_per_sm(head_dim, group);
+  const int64_t resident =
+      static_cast<int64_t>(sms) * (decode_uses_tc(head_dim, group) ? 1 : decode_ctas_per_sm(head_dim, group));
   return std::max<int64_t>(1, std::min(resident, (upper + kMinTilesPerCta - 1) / kMinTilesPerCta));
 }
 
@@ -101,6 +112,47 @@ bool make_sw128_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [rows][heads][head_dim] for the tensor-core decode: box {64, group, 1}
+// (one 128-byte row per q head of a kv head).
+bool make_q_group_map(CUtensorMap* map, const void* q, int rows, int num_heads, int head_dim,
+                      int group) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(num_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(group), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A K or V cache as a 5-D tensor {64, 8, head_dim / 64, slots / 8, kv heads}
+// (head_dim low part, token within a group of 8, head_dim half, group of 8
+// tokens, kv head) with a box of {64, 8, head_dim / 64, 2, 1}: one copy per
+// (block, kv head) lands as [token group][head_dim half][8 tokens][128 B],
+// 128-byte swizzled, so the 8-token groups of consecutive blocks sit at one
+// uniform stride: the operand layout of both MMAs of the tensor-core decode.
+bool make_kv_group_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                       int head_dim) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2;  // bytes per token
+  const cuuint64_t dims[5] = {64u, 8u, static_cast<cuuint64_t>(head_dim / 64),
+                              static_cast<cuuint64_t>(num_blocks) * (kBlockSize / 8),
+                              static_cast<cuuint64_t>(num_kv_heads)};
+  const cuuint64_t strides[4] = {row, 128u, 8 * row, static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[5] = {64u, 8u, static_cast<cuuint32_t>(head_dim / 64), kBlockSize / 8, 1u};
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -174,7 +226,7 @@ pa_status check_attention_shape(int num_heads, int num_kv_heads, int head_dim, i
     return PA_ERR_INVALID;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
-  if (decode_gmax(num_heads / num_kv_heads) == 0) return PA_ERR_UNSUPPORTED;
+  if (num_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -206,10 +258,17 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t num_blocks, float scale, const DecodeLayout& L,
                              void* workspace, cudaStream_t stream) {
-  CUtensorMap kmap, vmap;
-  if (!make_cache_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
-      !make_cache_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
+  const bool tc = decode_uses_tc(head_dim, num_heads / num_kv_heads);
+  CUtensorMap kmap, vmap, qmap;
+  if (tc) {
+    if (!make_q_group_map(&qmap, q, total_q, num_heads, head_dim, num_heads / num_kv_heads) ||
+        !make_kv_group_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
+        !make_kv_group_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
+      return PA_ERR_CUDA;
+  } else if (!make_cache_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
+             !make_cache_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim)) {
     return PA_ERR_CUDA;
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -232,7 +291,9 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.total_q = total_q;
   a.epoch = next_epoch();
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_decode(a, kmap, vmap, head_dim, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, stream)
+                            : launch_decode(a, kmap, vmap, head_dim, stream);
+  return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace

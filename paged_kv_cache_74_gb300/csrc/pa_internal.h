@@ -68,6 +68,12 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Launchers (decode.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, cudaStream_t stream);
+// Tensor-core decode (decode_tc.cu): qmap = q as {head_dim, heads, rows}
+// with a {64, group, 1} box; kmap, vmap = the caches as {64, 8, head_dim /
+// 64, slots / 8, kv heads} with a {64, 8, head_dim / 64, 2, 1} box (one
+// block of one kv head per copy); all 128-byte swizzled.
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
 // Smallest group size the decode kernel is instantiated for that covers g.
 int decode_gmax(int group);
 // CTAs per SM the decode kernel for (head_dim, group) is built for.

@@ -66,7 +66,7 @@ def decode_call(lib, **kw):
     (dict(hq=6, hkv=4), 1), (dict(hkv=0), 1), (dict(ns=-1), 1), (dict(nb=0), 1),
     (dict(msl=65), 1), (dict(mb=0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
     (dict(pt=24), 1), (dict(pt=-16), 1),
-    (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=32, hkv=2), 2), (dict(ns=70000), 2),
+    (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=34, hkv=2), 2), (dict(ns=70000), 2),
     (dict(ws=0), 3), (dict(wsb=16), 3),
     (dict(ws=A + 16), 1),
 ])

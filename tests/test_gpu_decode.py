@@ -41,6 +41,9 @@ SWEEP = [
     (64, 16, 4, 129, 7, 104), (128, 32, 8, 600, 6, 105), (128, 8, 8, 40, 11, 106),
     (128, 16, 2, 1100, 3, 107), (128, 7, 1, 257, 4, 108), (128, 6, 2, 513, 5, 109),
     (64, 3, 3, 33, 8, 110), (128, 64, 8, 700, 3, 111), (64, 1, 1, 17, 4, 112),
+    # 9 to 16 q heads per kv head (tensor-core decode only)
+    (128, 32, 2, 900, 5, 113), (64, 16, 1, 260, 6, 114), (128, 24, 2, 333, 4, 115),
+    (128, 80, 8, 150, 3, 116),
 ]
 
 

@@ -51,6 +51,7 @@ MIXES = [
     (204, 7, 520, 300, 128, 16, 16),
     (205, 3, 400, 400, 128, 8, 1),
     (206, 5, 290, 130, 64, 16, 2),
+    (209, 4, 400, 200, 128, 32, 2),
 ]
 
 
