@@ -426,12 +426,10 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
   if (max_query_len > 1) {
     // Rows with q_len > 1: tensor-core tiles.
     CUtensorMap qmap, kmap, vmap;
-    const uint64_t slots = static_cast<uint64_t>(num_blocks) * kBlockSize;
-    const uint64_t kv_row = static_cast<uint64_t>(num_kv_heads) * head_dim * 2;
     if (!make_sw128_map(&qmap, q, head_dim, num_heads, total_q, head_dim * 2,
                         static_cast<uint64_t>(num_heads) * head_dim * 2, 128) ||
-        !make_sw128_map(&kmap, key_cache, head_dim, num_kv_heads, slots, head_dim * 2, kv_row, 16) ||
-        !make_sw128_map(&vmap, value_cache, head_dim, num_kv_heads, slots, head_dim * 2, kv_row, 16))
+        !make_kv_group_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
+        !make_kv_group_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
     PrefillArgs p;
     p.out = static_cast<__nv_bfloat16*>(out);

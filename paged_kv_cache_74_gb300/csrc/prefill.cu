@@ -13,9 +13,11 @@
 // and is warp-specialised:
 //   warp 8      producer: TMA (128-byte swizzle) loads the Q tile once and
 //               K and V tiles of 128 keys (eight 16-token blocks gathered
-//               through the block table) into two-stage rings, refilling a
-//               K stage as soon as its S MMA is done and a V stage as soon
-//               as its P.V MMA is done;
+//               through the block table, one copy per block that lands as
+//               [8-key group][head_dim half][8 keys][128 B], a layout both
+//               MMAs read directly) into two-stage rings, refilling a K
+//               stage as soon as its S MMA is done and a V stage as soon as
+//               its P.V MMA is done;
 //   warp 9      MMA issuer (tcgen05, kind::f16, bf16 in, fp32 accumulate in
 //               TMEM), in the order S_0, S_1, PV_0, S_2, PV_1, ...:
 //                 S_j = Q K_j^T  M = N = 128, K = head_dim, both operands
@@ -73,6 +75,9 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
   static constexpr uint32_t BLOCK_BYTES = HALVES * 16 * 128;  // K (or V) of one block
+  // K and V blocks land as [8-key group][head_dim half][8 keys][128 B]: the
+  // 8-key groups of a tile are GSTRIDE apart, head_dim halves 1 KB apart.
+  static constexpr int GSTRIDE = HALVES * 1024;
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -178,10 +183,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
           if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, ids);
           row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
         }
-        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK + lane * 2048;
-#pragma unroll
-        for (int h = 0; h < C::HALVES; ++h)
-          tma_load_3d(dst + h * C::CHUNK, is_v ? &vmap : &kmap, full, 64 * h, kvh, row_c, policy);
+        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK + lane * C::BLOCK_BYTES;
+        tma_load_5d(dst, is_v ? &vmap : &kmap, full, 0, 0, 0, row_c / 8, kvh, policy);
       }
       __syncwarp();
     };
@@ -220,9 +223,10 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
         const uint32_t kst = k_s + (t & 1) * C::HALVES * C::CHUNK;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * C::CHUNK + (ks % 4) * 32;
-          umma_bf16(tmem + (t & 1) * C::BN, sdesc_sw128(q_s + off, 16, 1024),
-                    sdesc_sw128(kst + off, 16, 1024), C::IDESC_S, ks > 0);
+          const uint32_t qoff = (ks / 4) * C::CHUNK + (ks % 4) * 32;
+          const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
+          umma_bf16(tmem + (t & 1) * C::BN, sdesc_sw128(q_s + qoff, 16, 1024),
+                    sdesc_sw128(kst + koff, 16, C::GSTRIDE), C::IDESC_S, ks > 0);
         }
         umma_commit(bar(kSFull + (t & 1)));
         umma_commit(bar(kKFree + (t & 1)));
@@ -237,7 +241,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
         for (int ks = 0; ks < C::BN / 16; ++ks) {
           umma_bf16(tmem + 256, sdesc_sw128(p_s + (sb * 2 + ks / 4) * C::CHUNK + (ks % 4) * 32, 16, 1024),
-                    sdesc_sw128(v_s + sb * C::HALVES * C::CHUNK + ks * 2048, C::CHUNK, 1024),
+                    sdesc_sw128(v_s + sb * C::HALVES * C::CHUNK + ks * C::BLOCK_BYTES, 1024, C::GSTRIDE),
                     C::IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar(kPVDone + sb));
@@ -359,7 +363,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int idx = tid; idx < nz; idx += C::SOFTMAX_WARPS * 32) {
           const int row = max(kz, 0) + idx / (C::HALVES * 8);
           const int h = (idx / 8) % C::HALVES;
-          st_shared_v4(v_s + (sb * C::HALVES + h) * C::CHUNK + row * 128 + (idx % 8) * 16,
+          st_shared_v4(v_s + sb * C::HALVES * C::CHUNK + (row >> 4) * C::BLOCK_BYTES +
+                           ((row >> 3) & 1) * C::GSTRIDE + h * 1024 + (row & 7) * 128 + (idx % 8) * 16,
                        make_uint4(0u, 0u, 0u, 0u));
         }
       }
