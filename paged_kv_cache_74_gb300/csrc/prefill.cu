@@ -11,13 +11,13 @@
 //
 // GB300 design.  One CTA owns 128 query rows of one q head of one request
 // and is warp-specialised:
-//   warp 8      producer: TMA (128-byte swizzle) loads the Q tile once and
-//               K and V tiles of 128 keys (eight 16-token blocks gathered
-//               through the block table, one copy per block that lands as
-//               [8-key group][head_dim half][8 keys][128 B], a layout both
-//               MMAs read directly) into two-stage rings, refilling a K
-//               stage as soon as its S MMA is done and a V stage as soon as
-//               its P.V MMA is done;
+//   warps 8, 10 producers: TMA (128-byte swizzle) loads the Q tile once
+//               (warp 8) and K (warp 8) and V (warp 10) tiles of 128 keys:
+//               eight 16-token blocks gathered through the block table, one
+//               copy per block that lands as [8-key group][head_dim half]
+//               [8 keys][128 B], a layout both MMAs read directly.  Two-stage
+//               rings; a K stage is refilled as soon as its S MMA is done, a
+//               V stage as soon as its P.V MMA is done;
 //   warp 9      MMA issuer (tcgen05, kind::f16, bf16 in, fp32 accumulate in
 //               TMEM), in the order S_0, S_1, PV_0, S_2, PV_1, ...:
 //                 S_j = Q K_j^T  M = N = 128, K = head_dim, both operands
@@ -68,7 +68,7 @@ struct PrefillCfg {
   static constexpr int OFF_MISC = OFF_RED + 2 * 128 * 4;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;            // + 1024-byte alignment slack
   static constexpr int SOFTMAX_WARPS = 8;
-  static constexpr int THREADS = (SOFTMAX_WARPS + 2) * 32;     // + producer, MMA issuer
+  static constexpr int THREADS = (SOFTMAX_WARPS + 3) * 32;     // + K producer, MMA issuer, V producer
   static constexpr int HC = BN / 2;                            // S columns per softmax thread
   static constexpr int HD = D / 2;                             // O columns per softmax thread
   static constexpr uint32_t TMEM_COLS = 512;                   // S0 0, S1 128, O 256
@@ -160,8 +160,11 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     *fail_flag = 1;
   };
 
-  if (warp == C::SOFTMAX_WARPS) {
-    // ============================================================ producer
+  if (warp == C::SOFTMAX_WARPS || warp == C::SOFTMAX_WARPS + 2) {
+    // ===================================================== K and V producers
+    // Two warps, so that a K tile is never queued behind the V copy that
+    // waits for an earlier P.V MMA.
+    const bool is_v = warp != C::SOFTMAX_WARPS;
     const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
     const uint64_t policy = l2_policy_evict_first();
     auto load_ids = [&](int t) -> int {
@@ -188,10 +191,10 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       __syncwarp();
     };
-    if (lane == 0) {
+    if (lane == 0 && is_v) tma_prefetch_desc(&vmap);
+    if (lane == 0 && !is_v) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
       mbar_arrive_expect_tx(bar(kQFull), C::HALVES * C::CHUNK);
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h)
@@ -201,14 +204,13 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     int ids_next = load_ids(1);
     for (int t = 0; t < n_tiles; ++t) {
       int ok = 1;
-      // K stage t % 2 held K_{t-2}: free once S_{t-2} is done.
-      if (lane == 0 && t >= 2 && !mbar_wait(bar(kKFree + (t & 1)), ((t - 2) >> 1) & 1)) ok = 0;
+      // Stage t % 2 held tile t - 2: a K stage is free once S_{t-2} is done,
+      // a V stage once P_{t-2} V_{t-2} is done.
+      if (lane == 0 && t >= 2 &&
+          !mbar_wait(bar((is_v ? kPVDone : kKFree) + (t & 1)), ((t - 2) >> 1) & 1))
+        ok = 0;
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issue_tile(false, t, ids);
-      // V stage t % 2 held V_{t-2}: free once P_{t-2} V_{t-2} is done.
-      if (lane == 0 && t >= 2 && !mbar_wait(bar(kPVDone + (t & 1)), ((t - 2) >> 1) & 1)) ok = 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issue_tile(true, t, ids);
+      issue_tile(is_v, t, ids);
       ids = ids_next;
       ids_next = load_ids(t + 2);
     }
