@@ -35,8 +35,9 @@
  *   into its K and V halves).  Block 0 is conventionally the null block.
  * GQA.  num_heads must be a multiple of num_kv_heads; q head h reads kv head
  *   h / (num_heads / num_kv_heads).
- * Supported sizes.  head_dim 64 or 128; block_size 16; num_heads /
- *   num_kv_heads between 1 and 16; num_seqs up to 65535.
+ * Supported sizes.  head_dim 64 or 128; block_size 16, 32 or 64 for the
+ *   attention calls (any positive block_size for the slot helpers); num_heads
+ *   / num_kv_heads between 1 and 16; num_seqs up to 65535.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy
  *   default stream).  Calls only enqueue work; they never synchronise.
  *   A write through pa_reshape_and_cache must be enqueued before the
@@ -132,6 +133,31 @@ pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
                                   const int32_t* query_start_loc, const int32_t* seq_lens,
                                   int32_t num_seqs, int32_t block_size, int32_t num_blocks,
                                   int32_t* device_status, void* stream);
+
+/*
+ * pa_map_to_kernel_blocks -- block tables of KV-manager blocks expanded into
+ * block tables of kernel blocks ("vllm 深度解析：一切从 PagedAttention 谈起",
+ * BlockTable.map_to_kernel_blocks: when the manager's block holds
+ * blocks_per_kv_block kernel blocks, manager block b becomes kernel blocks
+ * b * k, b * k + 1, ..., b * k + k - 1 with k = blocks_per_kv_block).
+ *
+ *   kernel_tables  [num_rows, max_blocks_per_row * k] int32 (written)
+ *   block_tables   [num_rows, max_blocks_per_row] int32; an entry < 0
+ *                  (padding) becomes k entries of -1
+ *   device_status  optional int32[4] status record (NULL = none): an id
+ *                  whose kernel ids exceed INT32_MAX is recorded as
+ *                  PA_DEV_BAD_BLOCK_ID and written as -1
+ * A cache of num_blocks blocks of block_size tokens is the same memory as
+ * num_blocks * k blocks of block_size / k tokens, so the attention calls
+ * give bit-identical results for (cache viewed with block_size, tables)
+ * and (cache viewed with block_size / k, expanded tables).
+ * Errors: PA_ERR_INVALID for null or misaligned pointers, negative sizes or
+ * k < 1; num_rows == 0 or max_blocks_per_row == 0 is a no-op.
+ */
+pa_status pa_map_to_kernel_blocks(int32_t* kernel_tables, const int32_t* block_tables,
+                                  int32_t num_rows, int32_t max_blocks_per_row,
+                                  int32_t blocks_per_kv_block, int32_t* device_status,
+                                  void* stream);
 
 /*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these

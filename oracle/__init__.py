@@ -56,6 +56,8 @@ def _declare(lib):
     lib.oracle_kv_bytes_per_token.restype = ctypes.c_int64
     lib.oracle_kv_bytes_per_token.argtypes = [ctypes.c_int32] * 4
     lib.oracle_decode.restype = ctypes.c_int
+    lib.oracle_map_to_kernel_blocks.restype = None
+    lib.oracle_map_to_kernel_blocks.argtypes = [_I32, ctypes.c_int32, ctypes.c_int32, _I32]
     lib.oracle_decode.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
@@ -129,6 +131,13 @@ class Oracle:
         self.lib.oracle_reshape_and_cache(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv, d,
                                           _p(kc, _U16), _p(vc, _U16), nb, bs, _p(sm, _I64))
         return kc, vc
+
+    def map_to_kernel_blocks(self, ids, k: int) -> np.ndarray:
+        """Manager block ids (any shape; last axis = blocks) -> kernel block ids."""
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        out = np.empty(a.shape[:-1] + (a.shape[-1] * k,), dtype=np.int32)
+        self.lib.oracle_map_to_kernel_blocks(_p(a, _I32), a.size, k, _p(out, _I32))
+        return out
 
     def kv_bytes_per_token(self, num_layers, num_kv_heads, head_dim, elem_bytes) -> int:
         return int(self.lib.oracle_kv_bytes_per_token(num_layers, num_kv_heads, head_dim,

@@ -242,3 +242,15 @@ void oracle_merge_partitions(const double* m_parts, const double* l_parts, const
         for (int32_t x = 0; x < dv; ++x) out[x] += o_parts[(int64_t)p * dv + x] * w;
     }
 }
+
+/* map_to_kernel_blocks ("vllm 深度解析：一切从 PagedAttention 谈起",
+ * BlockTable.map_to_kernel_blocks): every KV-manager block id b becomes the
+ * kernel block ids b*k, b*k+1, ..., b*k+k-1, in order, for k kernel blocks
+ * per manager block; with k == 1 the list is unchanged.  Negative entries
+ * (table padding) become k entries of -1. */
+void oracle_map_to_kernel_blocks(const int32_t* ids, int32_t n, int32_t k, int32_t* out) {
+    int64_t w = 0;
+    for (int32_t i = 0; i < n; ++i)
+        for (int32_t j = 0; j < k; ++j)
+            out[w++] = ids[i] < 0 ? -1 : (int32_t)((int64_t)ids[i] * k + j);
+}

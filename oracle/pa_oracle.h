@@ -41,6 +41,7 @@ int oracle_prefill_varlen(double* out, const uint16_t* q, const uint16_t* key_ca
 void oracle_online_softmax(const double* s, const double* v, int32_t n, int32_t dv,
                            const int32_t* bounds, int32_t num_tiles,
                            double* out, double* m_out, double* l_out);
+void oracle_map_to_kernel_blocks(const int32_t* ids, int32_t n, int32_t k, int32_t* out);
 void oracle_merge_partitions(const double* m_parts, const double* l_parts,
                              const double* o_parts, int32_t num_parts, int32_t dv,
                              double* out);

@@ -8,9 +8,11 @@ the tests and the benchmark.
 from ._binding import (ABI_SYMBOLS, DEVICE_ERRORS, PAError, compute_slot_mapping, decode,
                        decode_noalloc,
                        decode_workspace_size, device_status, library_path, load_library,
-                       new_workspace, prefill_varlen, prefill_workspace_size, reshape_and_cache)
+                       map_to_kernel_blocks, new_workspace, prefill_varlen,
+                       prefill_workspace_size, reshape_and_cache)
 from .builder import build
 
 __all__ = ["ABI_SYMBOLS", "DEVICE_ERRORS", "PAError", "build", "compute_slot_mapping", "decode",
            "decode_noalloc", "decode_workspace_size", "device_status", "library_path", "load_library",
-           "new_workspace", "prefill_varlen", "prefill_workspace_size", "reshape_and_cache"]
+           "map_to_kernel_blocks", "new_workspace", "prefill_varlen", "prefill_workspace_size",
+           "reshape_and_cache"]

@@ -24,7 +24,8 @@ DEVICE_ERRORS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "bad seq_len",
                  4: "bad query length", 5: "wait timeout"}
 ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
-               "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc")
+               "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
+               "pa_map_to_kernel_blocks")
 
 
 class PAError(RuntimeError):
@@ -47,6 +48,8 @@ def _declare(lib):
     lib.pa_compute_slot_mapping.restype = ctypes.c_int
     lib.pa_compute_slot_mapping.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                             _vp, _vp]
+    lib.pa_map_to_kernel_blocks.restype = ctypes.c_int
+    lib.pa_map_to_kernel_blocks.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp]
     lib.pa_decode_workspace_size.restype = _sz
     lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     lib.pa_decode.restype = ctypes.c_int
@@ -141,6 +144,20 @@ def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, nu
     _check("pa_compute_slot_mapping", lib.pa_compute_slot_mapping(
         _ptr(out), total_tokens, _ptr(block_tables), block_tables.shape[1], _ptr(query_start_loc),
         _ptr(seq_lens), seq_lens.shape[0], block_size, num_blocks, _ptr(status), _stream()))
+    return out
+
+
+def map_to_kernel_blocks(block_tables, blocks_per_kv_block, out=None, status=None):
+    """Block tables of manager blocks -> tables of kernel blocks (k per manager block)."""
+    _contig("block_tables", block_tables, torch.int32)
+    rows, cols = block_tables.shape
+    k = int(blocks_per_kv_block)
+    if out is None:
+        out = torch.empty((rows, cols * k), dtype=torch.int32, device=block_tables.device)
+    _contig("kernel_tables", out, torch.int32)
+    lib = load_library()
+    _check("pa_map_to_kernel_blocks", lib.pa_map_to_kernel_blocks(
+        _ptr(out), _ptr(block_tables), rows, cols, k, _ptr(status), _stream()))
     return out
 
 

@@ -91,7 +91,31 @@ slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
   }
 }
 
+// One thread per manager-block entry writes its k kernel-block ids.
+__global__ void __launch_bounds__(256)
+map_kernel_blocks_kernel(int32_t* __restrict__ out, const int32_t* __restrict__ in, int64_t n,
+                         int k, int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int32_t b = in[i];
+  const int64_t first = static_cast<int64_t>(b) * k;
+  const bool bad = b >= 0 && first + k - 1 > 0x7fffffffLL;
+  if (bad) record_error(status, PA_DEV_BAD_BLOCK_ID, static_cast<int>(i), b);
+  for (int j = 0; j < k; ++j)
+    out[i * k + j] = (b < 0 || bad) ? -1 : static_cast<int32_t>(first + j);
+}
+
 }  // namespace
+
+cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
+                                     int32_t* status, cudaStream_t stream) {
+  const int64_t grid = (n + 255) / 256;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  return launch_overlapped(map_kernel_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                           stream, out, in, n, k, status);
+}
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
                                      int64_t value_stride, void* key_cache, void* value_cache,

@@ -231,8 +231,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const int32_t* rp = a.block_tables + static_cast<size_t>(rr) * a.max_blocks_per_seq;
 #pragma unroll
         for (int m = 0; m < kRowCache; ++m) {
-          const int gi = 32 * m + lane;
-          ids[m] = (rr < a.num_seqs && gi < a.max_blocks_per_seq) ? __ldg(rp + gi) : 0;
+          const int gi = 32 * m + lane;  // tile index
+          ids[m] = (rr < a.num_seqs && (gi >> a.tile_shift) < a.max_blocks_per_seq)
+                       ? __ldg(rp + (gi >> a.tile_shift))
+                       : 0;
         }
       };
       auto prefetch_next = [&](int rr) {
@@ -293,11 +295,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         ok = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
         const int rows = (seg_n + C::NC - 1) / C::NC;
         const int32_t* rowp = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
-        const int seg_end = b + seg_n;  // one past the segment's last block
+        const int seg_end = b + seg_n;  // one past the segment's last tile
         int my_id = 0, far_next = 0;
         for (int j = 0; j < rows * C::NC && ok; ++j) {
           if ((j & 31) == 0) {
-            const int gi = b + j + lane;  // block of this lane's tile in the chunk
+            const int gi = b + j + lane;  // this lane's tile in the chunk
             int cached = 0;
 #pragma unroll
             for (int m = 0; m < kRowCache; ++m) {
@@ -307,11 +309,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             if (gi < 32 * kRowCache)
               my_id = cached;
             else if (j == 0)
-              my_id = gi < seg_end ? __ldg(rowp + gi) : 0;
+              my_id = gi < seg_end ? __ldg(rowp + (gi >> a.tile_shift)) : 0;
             else
               my_id = far_next;
             const int gn = gi + 32;  // next chunk, fetched now
-            far_next = (gn >= 32 * kRowCache && gn < seg_end) ? __ldg(rowp + gn) : 0;
+            far_next = (gn >= 32 * kRowCache && gn < seg_end) ? __ldg(rowp + (gn >> a.tile_shift)) : 0;
           }
           const int phys = __shfl_sync(0xffffffffu, my_id, j & 31);
           if (lane == 0 && stage_begin(pos)) {
@@ -321,10 +323,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             meta[s] = make_int2(b + j, flags);
             const uint32_t full = full0 + 8 * s;
             if (real) {
-              int row0 = phys * kBlockSize;
+              int row0 = tile_row(a, phys, b + j);
               if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
                 record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys);
-                row0 = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
+                row0 = a.num_blocks * a.block_size;  // wholly out of bounds: TMA fills zeros
               }
               mbar_arrive_expect_tx(full, 2 * C::TILE);
               tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);

@@ -23,7 +23,7 @@ constexpr int kWhole = 0;  // the whole (request, kv head): final bf16 output
 constexpr int kHead = 1;   // continues a pair begun by an earlier CTA: partial slot 0
 constexpr int kTail = 2;   // begins a pair finished by later CTAs: partial slot 1
 
-// Blocks of request r that the decode kernel processes (0 for rows that are
+// 16-token tiles of request r that the decode kernel processes (0 for rows that are
 // not decode rows, and for invalid lengths); also its length and q row.
 // `len` = seq_lens[r]; q0, q1 = query_start_loc[r], [r + 1] (when present).
 __device__ __forceinline__ int blocks_from(const DecodeArgs& a, int r, int len, int q0, int q1,
@@ -34,7 +34,7 @@ __device__ __forceinline__ int blocks_from(const DecodeArgs& a, int r, int len, 
     rw = q0;
     if (rw < 0 || rw >= a.total_q) return 0;
   }
-  if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize) return 0;
+  if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * a.block_size) return 0;
   *seq_len = len;
   *row = rw;
   return (len + kBlockSize - 1) / kBlockSize;
@@ -60,9 +60,15 @@ __device__ void report_bad_rows(const DecodeArgs& a, int lane) {
       }
     }
     const int len = a.seq_lens[r];
-    if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * kBlockSize)
+    if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * a.block_size)
       record_error(a.status, PA_DEV_BAD_SEQ_LEN, r, len);
   }
+}
+
+// First cache row (slot) of 16-token tile `tile` of a request whose tile
+// lives in block `block_id`.
+__device__ __forceinline__ int tile_row(const DecodeArgs& a, int block_id, int tile) {
+  return block_id * a.block_size + (tile & ((1 << a.tile_shift) - 1)) * kBlockSize;
 }
 
 // Equal split of W tiles over C CTAs: CTA c owns [range_lo(c), range_lo(c+1)).

@@ -281,11 +281,11 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    // Block ids 0 .. 63 of a request (lane L: ids L and 32 + L).
+    // Block ids of tiles 0 .. 63 of a request (lane L: tiles L and 32 + L).
     auto load_head = [&](int r, int nb, int& h0, int& h1) {
       const int32_t* rp = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
-      h0 = (r < a.num_seqs && lane < nb) ? __ldg(rp + lane) : 0;
-      h1 = (r < a.num_seqs && 32 + lane < nb) ? __ldg(rp + 32 + lane) : 0;
+      h0 = (r < a.num_seqs && lane < nb) ? __ldg(rp + (lane >> a.tile_shift)) : 0;
+      h1 = (r < a.num_seqs && 32 + lane < nb) ? __ldg(rp + ((32 + lane) >> a.tile_shift)) : 0;
     };
     if (lo < hi) {
       // Request holding tile `lo`: scan the per-request tile counts 32 at a time.
@@ -357,14 +357,14 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                         kvh * a.group, row, policy);
           *n_segs_issued = seg + 1;
         }
-        // ---- block ids: a window [win_b, win_b + 64) of the request's row
+        // ---- block ids of tiles [win_b, win_b + 64) of the request
         const int32_t* rowp = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
         const int seg_end = b + seg_n;
         int cur32 = head0, nxt32 = head1, win_b = 0;
         if (b > 0) {  // only the first segment of a range can start mid-request
           win_b = b;
-          cur32 = b + lane < seg_end ? __ldg(rowp + b + lane) : 0;
-          nxt32 = b + 32 + lane < seg_end ? __ldg(rowp + b + 32 + lane) : 0;
+          cur32 = b + lane < seg_end ? __ldg(rowp + ((b + lane) >> a.tile_shift)) : 0;
+          nxt32 = b + 32 + lane < seg_end ? __ldg(rowp + ((b + 32 + lane) >> a.tile_shift)) : 0;
         }
         // ---- chunks of 8 blocks: lane L < 8 copies the K of block L.
         const int nch = (seg_n + C::CB - 1) / C::CB;
@@ -375,7 +375,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
             win_b += 32;
             off -= 32;
             const int gi = win_b + 32 + lane;
-            nxt32 = gi < seg_end ? __ldg(rowp + gi) : 0;
+            nxt32 = gi < seg_end ? __ldg(rowp + (gi >> a.tile_shift)) : 0;
           }
           const int nbc = min(C::CB, seg_n - C::CB * c);
           const int vphys = __shfl_sync(0xffffffffu, cur32, (off + lane) & 31);
@@ -384,8 +384,9 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           // bounds (TMA fills zeros).
           const bool kbad = static_cast<unsigned>(kphys) >= static_cast<unsigned>(a.num_blocks);
           const bool vbad = static_cast<unsigned>(vphys) >= static_cast<unsigned>(a.num_blocks);
-          const int krow = (kbad ? a.num_blocks : kphys) * kBlockSize;
-          const int vrow = (vbad ? a.num_blocks : vphys) * kBlockSize;
+          const int tile = b + C::CB * c + lane;  // this lane's tile
+          const int krow = kbad ? a.num_blocks * a.block_size : tile_row(a, kphys, tile);
+          const int vrow = vbad ? a.num_blocks * a.block_size : tile_row(a, vphys, tile);
           if (lane < nbc && vbad) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, vphys);
           const int st = chunk % C::NST;
           // K: refill once the S MMA of chunk - NST is done (that MMA also

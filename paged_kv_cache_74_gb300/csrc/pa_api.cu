@@ -218,14 +218,17 @@ unsigned next_epoch() {
   return e;
 }
 
+// log2(block_size / 16) for the supported block sizes 16, 32 and 64.
+int tile_shift_of(int block_size) { return block_size == 64 ? 2 : block_size == 32 ? 1 : 0; }
+
 // Shared shape checks of the attention entry points.
 pa_status check_attention_shape(int num_heads, int num_kv_heads, int head_dim, int block_size,
                                 int num_blocks) {
   if (num_kv_heads < 1 || num_heads < 1 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID;
-  if (num_blocks < 1 || static_cast<int64_t>(num_blocks) * kBlockSize > 0x7fffffffLL)
+  if (block_size != 16 && block_size != 32 && block_size != 64) return PA_ERR_UNSUPPORTED;
+  if (num_blocks < 1 || static_cast<int64_t>(num_blocks) * block_size > 0x7fffffffLL)
     return PA_ERR_INVALID;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
   if (num_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
@@ -256,17 +259,19 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
                              const int32_t* seq_lens, const int32_t* query_start_loc,
                              int32_t num_seqs, int32_t total_q, int32_t max_seq_len,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t num_blocks, float scale, const DecodeLayout& L,
-                             void* workspace, cudaStream_t stream) {
+                             int32_t num_blocks, int32_t block_size, float scale,
+                             const DecodeLayout& L, void* workspace, cudaStream_t stream) {
+  // The TMA views address the cache in 16-token tiles.
+  const int num_tiles16 = num_blocks * (block_size / kBlockSize);
   const bool tc = decode_uses_tc(head_dim, num_heads / num_kv_heads);
   CUtensorMap kmap, vmap, qmap;
   if (tc) {
     if (!make_q_group_map(&qmap, q, total_q, num_heads, head_dim, num_heads / num_kv_heads) ||
-        !make_kv_group_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
-        !make_kv_group_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
+        !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
+        !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
-  } else if (!make_cache_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
-             !make_cache_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim)) {
+  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
+             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim)) {
     return PA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -288,6 +293,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.num_ctas = static_cast<int>(L.num_ctas);
   a.max_seq_len = max_seq_len;
   a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.tile_shift = tile_shift_of(block_size);
   a.total_q = total_q;
   a.epoch = next_epoch();
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -362,6 +369,21 @@ pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_map_to_kernel_blocks(int32_t* kernel_tables, const int32_t* block_tables,
+                                  int32_t num_rows, int32_t max_blocks_per_row,
+                                  int32_t blocks_per_kv_block, int32_t* device_status,
+                                  void* stream) {
+  if (num_rows < 0 || max_blocks_per_row < 0 || blocks_per_kv_block < 1) return PA_ERR_INVALID;
+  if (num_rows == 0 || max_blocks_per_row == 0) return PA_OK;
+  if (!kernel_tables || !block_tables || !aligned(kernel_tables, 4) || !aligned(block_tables, 4) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  const int64_t n = static_cast<int64_t>(num_rows) * max_blocks_per_row;
+  const cudaError_t e = launch_map_kernel_blocks(kernel_tables, block_tables, n, blocks_per_kv_block,
+                                                 device_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
   if (num_seqs < 0 || max_seq_len < 1 || num_kv_heads < 1 || num_heads < 1 ||
@@ -392,7 +414,7 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
-                            num_kv_heads, head_dim, num_blocks, scale, L, workspace,
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -428,8 +450,10 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     CUtensorMap qmap, kmap, vmap;
     if (!make_sw128_map(&qmap, q, head_dim, num_heads, total_q, head_dim * 2,
                         static_cast<uint64_t>(num_heads) * head_dim * 2, 128) ||
-        !make_kv_group_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim) ||
-        !make_kv_group_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim))
+        !make_kv_group_map(&kmap, key_cache, num_blocks * (block_size / kBlockSize), num_kv_heads,
+                           head_dim) ||
+        !make_kv_group_map(&vmap, value_cache, num_blocks * (block_size / kBlockSize), num_kv_heads,
+                           head_dim))
       return PA_ERR_CUDA;
     PrefillArgs p;
     p.out = static_cast<__nv_bfloat16*>(out);
@@ -448,6 +472,8 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     p.max_seq_len = max_seq_len;
     p.max_query_len = max_query_len;
     p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.tile_shift = tile_shift_of(block_size);
     p.total_q = total_q;
     p.scale_log2 = scale * 1.4426950408889634f;
     // The tiles run on a side stream, forked from and joined back into the
@@ -462,7 +488,7 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     const pa_status st = launch_decode_rows(out, q, key_cache, value_cache, block_tables,
                                             max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                                             total_q, max_seq_len, num_heads, num_kv_heads, head_dim,
-                                            num_blocks, scale, L, workspace, cs);
+                                            num_blocks, block_size, scale, L, workspace, cs);
     if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
         cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess)
       return PA_ERR_CUDA;
@@ -471,7 +497,7 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
   // Only decode rows: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, query_start_loc, num_seqs, total_q, max_seq_len, num_heads,
-                            num_kv_heads, head_dim, num_blocks, scale, L, workspace, cs);
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace, cs);
 }
 
 }  // extern "C"

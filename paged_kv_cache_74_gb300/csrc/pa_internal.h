@@ -12,7 +12,11 @@
 
 namespace pa {
 
-constexpr int kBlockSize = 16;        // tokens per KV block (the pages' default)
+// The kernels move K/V in tiles of kBlockSize = 16 tokens (the pages'
+// default block size).  A cache block of block_size = 16 R tokens (R = 1, 2
+// or 4) holds R tiles: tile t of a request is rows 16 (t mod R) .. + 15 of
+// block block_table[t / R].
+constexpr int kBlockSize = 16;
 constexpr int kWorkspaceHeader = 256; // status record + padding at the start of a workspace
 
 // Decode work.  The tiles (request, kv head, block) of all decode rows are
@@ -39,6 +43,8 @@ struct DecodeArgs {
   int num_ctas;
   int max_seq_len;
   int num_blocks;
+  int block_size;                   // tokens per cache block: 16, 32 or 64
+  int tile_shift;                   // log2(block_size / 16)
   int total_q;                      // rows of q / out
   unsigned epoch;                   // distinct per call (never 0)
   float scale_log2;                 // softmax scale * log2(e)
@@ -98,6 +104,8 @@ struct PrefillArgs {
   int max_seq_len;
   int max_query_len;
   int num_blocks;
+  int block_size;                   // tokens per cache block: 16, 32 or 64
+  int tile_shift;                   // log2(block_size / 16)
   int total_q;
   float scale_log2;
 };
@@ -109,6 +117,8 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      int64_t value_stride, void* key_cache, void* value_cache,
                                      const int64_t* slot_mapping, int num_tokens, int row_elems,
                                      int64_t num_slots, int32_t* status, cudaStream_t stream);
+cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
+                                     int32_t* status, cudaStream_t stream);
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,
                                 int max_blocks_per_seq, const int32_t* query_start_loc,
                                 const int32_t* seq_lens, int num_seqs, int block_size,

@@ -109,7 +109,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   const int q_len = a.query_start_loc[r + 1] - q0;
   if (q_len <= 1 || qt * C::BM >= q_len) return;  // decode rows and empty tiles
   const int seq_len = a.seq_lens[r];
-  if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * kBlockSize ||
+  if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
       q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q) {
     if (tid == 0 && qt == 0 && head == 0)
       record_error(a.status, q_len > seq_len || q_len > a.max_query_len || q0 < 0 ||
@@ -169,7 +169,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint64_t policy = l2_policy_evict_first();
     auto load_ids = [&](int t) -> int {
       const int b = t * 8 + lane;
-      return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + b) : -1;
+      return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + (b >> a.tile_shift)) : -1;
     };
     // K or V of tile t into stage t % 2: lane 0 posts the byte count, then
     // lanes 0..7 each issue the TMA copies of their own block (lane b holds
@@ -181,10 +181,11 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       if (lane == 0) mbar_arrive_expect_tx(full, nb * C::BLOCK_BYTES);
       __syncwarp();
       if (lane < nb) {
-        int row_c = ids * kBlockSize;
+        // rows 16 (tile mod R) .. + 15 of the block holding tile t * 8 + lane
+        int row_c = ids * a.block_size + ((t * 8 + lane) & ((1 << a.tile_shift) - 1)) * kBlockSize;
         if (static_cast<unsigned>(ids) >= static_cast<unsigned>(a.num_blocks)) {
           if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, ids);
-          row_c = a.num_blocks * kBlockSize;  // wholly out of bounds: TMA fills zeros
+          row_c = a.num_blocks * a.block_size;  // wholly out of bounds: TMA fills zeros
         }
         const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK + lane * C::BLOCK_BYTES;
         tma_load_5d(dst, is_v ? &vmap : &kmap, full, 0, 0, 0, row_c / 8, kvh, policy);

@@ -66,7 +66,7 @@ def decode_call(lib, **kw):
     (dict(hq=6, hkv=4), 1), (dict(hkv=0), 1), (dict(ns=-1), 1), (dict(nb=0), 1),
     (dict(msl=65), 1), (dict(mb=0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
     (dict(pt=24), 1), (dict(pt=-16), 1),
-    (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=34, hkv=2), 2), (dict(ns=70000), 2),
+    (dict(d=96), 2), (dict(bs=48), 2), (dict(bs=128), 2), (dict(hq=34, hkv=2), 2), (dict(ns=70000), 2),
     (dict(ws=0), 3), (dict(wsb=16), 3),
     (dict(ws=A + 16), 1),
 ])
@@ -126,3 +126,13 @@ def test_prefill_validation(lib):
     assert call(mql=65) == 1
     assert call(d=80) == 2
     assert call(tq=0) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, A, 2, 4, 0), 1), ((0, A, 2, 4, 2), 1), ((A, 0, 2, 4, 2), 1), ((A + 2, A, 2, 4, 2), 1),
+    ((A, A, -1, 4, 2), 1), ((A, A, 2, -4, 2), 1), ((A, A, 0, 4, 2), 0), ((A, A, 2, 0, 2), 0),
+])
+def test_map_to_kernel_blocks_validation(lib, args, expect):
+    out, src, rows, cols, k = args
+    vp = ctypes.c_void_p
+    assert lib.pa_map_to_kernel_blocks(vp(out), vp(src), rows, cols, k, vp(0), vp(0)) == expect

@@ -101,3 +101,31 @@ def test_slot_mapping_reports_bad_block_id(cuda_lib):
     assert int(got[2]) == -1
     st = pa.device_status(status)
     assert st[0] == 2 and st[1] == 2 and st[2] == w.num_blocks + 5
+
+
+@pytest.mark.parametrize("k", [1, 2, 4])
+def test_map_to_kernel_blocks_bit_exact(cuda_lib, oracle, k):
+    pa = cuda_lib
+    rng = np.random.default_rng(70 + k)
+    tables = rng.integers(0, 5000, size=(37, 23)).astype(np.int32)
+    tables[rng.random(tables.shape) < 0.2] = -1  # padding
+    got = pa.map_to_kernel_blocks(torch.from_numpy(tables).cuda(), k)
+    np.testing.assert_array_equal(got.cpu().numpy(), oracle.map_to_kernel_blocks(tables, k))
+
+
+@pytest.mark.parametrize("B", [32, 64])
+def test_slot_write_with_larger_blocks(cuda_lib, oracle, B):
+    """Slot mapping and the cache write with 32- and 64-token blocks."""
+    pa = cuda_lib
+    w = wl.random_workload(80 + B, num_seqs=6, max_len=500, num_heads=8, num_kv_heads=2,
+                           head_dim=128, block_size=B, max_q_len=70, prefill_fraction=0.5)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, B,
+                                    w.num_blocks, w.total_q)
+    ref_slots = oracle.slot_mapping(w.block_tables, w.query_start_loc, w.seq_lens, B)
+    np.testing.assert_array_equal(slots.cpu().numpy(), ref_slots)
+    kc, vc = oracle.reshape_and_cache(bits(t.key), bits(t.value), bits(t.key_cache),
+                                      bits(t.value_cache), ref_slots)
+    pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+    np.testing.assert_array_equal(bits(t.key_cache), kc)
+    np.testing.assert_array_equal(bits(t.value_cache), vc)

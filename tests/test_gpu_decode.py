@@ -236,3 +236,33 @@ def test_decode_step_in_a_cuda_graph(cuda_lib):
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("B,hq,hkv,d", [(32, 32, 8, 128), (64, 16, 4, 64), (32, 64, 8, 128),
+                                        (64, 24, 2, 128)])
+def test_decode_larger_blocks(cuda_lib, oracle, B, hq, hkv, d):
+    """Cache blocks of 32 and 64 tokens, both decode kernels (4 and 8-12 q heads per kv head)."""
+    pa = cuda_lib
+    w = wl.random_workload(120 + B + hq, num_seqs=7, max_len=900, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, block_size=B)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    out = run_decode(pa, w, t)
+    ref = oracle.decode(bits(t.q), bits(t.key_cache), bits(t.value_cache), w.block_tables,
+                        w.seq_lens, w.scale)
+    assert_close_to_oracle(out, ref, what=f"block {B} hq{hq} hkv{hkv}")
+
+
+@pytest.mark.parametrize("B,k,hq", [(32, 2, 32), (64, 4, 64), (64, 2, 32)])
+def test_decode_through_kernel_blocks_is_bit_identical(cuda_lib, B, k, hq):
+    """Blocks of B tokens and the same memory as blocks of B / k tokens with
+    the tables expanded by pa_map_to_kernel_blocks give identical bits."""
+    pa = cuda_lib
+    w = wl.random_workload(130 + B + k, num_seqs=9, max_len=1200, num_heads=hq, num_kv_heads=8,
+                           head_dim=128, block_size=B)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    a = run_decode(pa, w, t)
+    small = (w.num_blocks * k, B // k, w.num_kv_heads, w.head_dim)
+    tables = pa.map_to_kernel_blocks(t.block_tables, k)
+    b = pa.decode(t.q, t.key_cache.view(small), t.value_cache.view(small), tables, t.seq_lens,
+                  w.max_seq_len, w.scale)
+    assert torch.equal(a, b)

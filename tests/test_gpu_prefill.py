@@ -227,3 +227,17 @@ def test_mixed_step_in_a_cuda_graph(cuda_lib):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("B,seed", [(32, 211), (64, 212)])
+def test_prefill_larger_blocks(cuda_lib, oracle, B, seed):
+    """Chunked prefill and decode rows over 32- and 64-token cache blocks."""
+    pa = cuda_lib
+    w = wl.random_workload(seed, num_seqs=6, max_len=700, num_heads=16, num_kv_heads=4,
+                           head_dim=128, block_size=B, max_q_len=300, prefill_fraction=0.6)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    out, ws = run_prefill(pa, w, t)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    assert_close_to_oracle(out, ref, what=f"prefill block {B}")

@@ -41,6 +41,9 @@ MUTATIONS = [
      ["merge"]),
     ("writer_shifts_offset", "int64_t offset = slot % block_size;\n        for",
      "int64_t offset = (slot + 1) % block_size;\n        for", ["writer"]),
+    ("kernel_ids_transposed", "(int32_t)((int64_t)ids[i] * k + j)", "(int32_t)((int64_t)ids[i] + j * k)",
+     ["kernel_blocks"]),
+    ("kernel_ids_padding_kept", "ids[i] < 0 ? -1 :", "ids[i] < -1 ? -1 :", ["kernel_blocks_padding"]),
 ]
 
 PINS = {
@@ -48,7 +51,10 @@ PINS = {
     "qsl": lambda o: pins.test_query_start_loc_printed_on_pages(o),
     "positions": lambda o: pins.test_varlen_positions_of_mixed_batch(o),
     "kv_bytes": lambda o: pins.test_kv_bytes_formula_printed_on_pages(o),
-    "sdpa_decode": lambda o: pins.test_decode_matches_torch_sdpa(o, 4, 2, 64, [25, 12, 37, 20]),
+    "sdpa_decode": lambda o: pins.test_decode_matches_torch_sdpa(o, 4, 2, 64, [25, 12, 37, 20], 16),
+    "sdpa_decode_b32": lambda o: pins.test_decode_matches_torch_sdpa(o, 8, 2, 64, [31, 64, 70], 32),
+    "kernel_blocks": lambda o: pins.test_kernel_blocks_printed_on_pages(o),
+    "kernel_blocks_padding": lambda o: pins.test_kernel_blocks_identity_and_padding(o),
     "sdpa_prefill": lambda o: pins.test_prefill_matches_torch_sdpa_bottom_right_causal(o),
     "online": lambda o: pins.test_online_softmax_equals_direct(o, "block16"),
     "merge": lambda o: pins.test_partition_merge_equals_global_softmax(o),

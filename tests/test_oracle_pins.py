@@ -121,10 +121,9 @@ def test_partition_merge_single_partition_is_identity(oracle):
 
 # --------------------------------------------------------------- attention
 
-def _contiguous_workload(seq_lens, hq, hkv, d, seed, q_lens=None):
+def _contiguous_workload(seq_lens, hq, hkv, d, seed, q_lens=None, B=16):
     """Each request owns consecutive physical blocks, so its keys form one
     contiguous range of the pool viewed as [slots, kv_heads, d]."""
-    B = 16
     seq_lens = np.asarray(seq_lens, np.int32)
     q_lens = np.ones_like(seq_lens) if q_lens is None else np.asarray(q_lens, np.int32)
     need = -(-seq_lens // B)
@@ -148,12 +147,14 @@ def _sdpa(q, k, v, scale, mask=None):
         q[None], k[None], v[None], attn_mask=mask, scale=scale)[0]
 
 
-@pytest.mark.parametrize("hq,hkv,d,lens", [(4, 2, 64, [25, 12, 37, 20]),
-                                           (8, 1, 128, [1, 16, 17, 100]),
-                                           (6, 6, 64, [3, 48]),
-                                           (16, 2, 128, [129, 33])])
-def test_decode_matches_torch_sdpa(oracle, hq, hkv, d, lens):
-    w, first_slot = _contiguous_workload(lens, hq, hkv, d, seed=21)
+@pytest.mark.parametrize("hq,hkv,d,lens,B", [(4, 2, 64, [25, 12, 37, 20], 16),
+                                             (8, 1, 128, [1, 16, 17, 100], 16),
+                                             (6, 6, 64, [3, 48], 16),
+                                             (16, 2, 128, [129, 33], 16),
+                                             (8, 2, 64, [31, 64, 70], 32),
+                                             (4, 4, 128, [1, 65, 200], 64)])
+def test_decode_matches_torch_sdpa(oracle, hq, hkv, d, lens, B):
+    w, first_slot = _contiguous_workload(lens, hq, hkv, d, seed=21, B=B)
     t = wl.make_tensors(w)
     out = oracle.decode(t.q.view(torch.int16).numpy(), t.key_cache.view(torch.int16).numpy(),
                         t.value_cache.view(torch.int16).numpy(), w.block_tables, w.seq_lens,
@@ -319,3 +320,45 @@ def test_reshape_then_slot_mapping_places_token_where_decode_reads_it(oracle):
         phys = w.block_tables[r, (L - 1) // 16]
         np.testing.assert_array_equal(kc[phys, (L - 1) % 16],
                                       t.key[r].view(torch.int16).numpy().view(np.uint16))
+
+
+# ------------------------------------------------------- kernel block ids
+
+def test_kernel_blocks_printed_on_pages(oracle):
+    for ids, k, expect, _src in read_golden("kernel_blocks.txt"):
+        got = oracle.map_to_kernel_blocks(np.array([int(x) for x in ids.split(",")]), int(k))
+        np.testing.assert_array_equal(got, [int(x) for x in expect.split(",")])
+
+
+def test_kernel_blocks_identity_and_padding(oracle):
+    ids = np.array([[7, 3, -1, -1], [0, 12, 5, -1]], np.int32)
+    np.testing.assert_array_equal(oracle.map_to_kernel_blocks(ids, 1), ids)
+    got = oracle.map_to_kernel_blocks(ids, 4)
+    assert got.shape == (2, 16)
+    np.testing.assert_array_equal(got[0, :8], [28, 29, 30, 31, 12, 13, 14, 15])
+    assert (got[0, 8:] == -1).all() and (got[1, 12:] == -1).all()
+    # each kernel id names a distinct 1/k of its manager block
+    np.testing.assert_array_equal(got[1, :12] // 4, np.repeat([0, 12, 5], 4))
+    np.testing.assert_array_equal(got[1, :12] % 4, np.tile(np.arange(4), 3))
+
+
+@pytest.mark.parametrize("B,k", [(32, 2), (64, 4), (64, 2)])
+def test_block_size_views_agree(oracle, B, k):
+    """A cache of nb blocks of B tokens is the memory of nb * k blocks of
+    B / k tokens; attention through the expanded tables must match exactly."""
+    w = wl.random_workload(31 + B + k, num_seqs=5, max_len=300, num_heads=8, num_kv_heads=2,
+                           head_dim=64, block_size=B, max_q_len=40, prefill_fraction=0.6)
+    t = wl.make_tensors(w)
+    q = t.q.view(torch.int16).numpy()
+    kc = t.key_cache.view(torch.int16).numpy()
+    vc = t.value_cache.view(torch.int16).numpy()
+    small = (w.num_blocks * k, B // k, w.num_kv_heads, w.head_dim)
+    tables_k = oracle.map_to_kernel_blocks(w.block_tables, k)
+    dec = oracle.decode(q[w.query_start_loc[1:] - 1], kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dec_k = oracle.decode(q[w.query_start_loc[1:] - 1], kc.reshape(small), vc.reshape(small),
+                          tables_k, w.seq_lens, w.scale)
+    np.testing.assert_array_equal(dec, dec_k)
+    pre = oracle.prefill_varlen(q, kc, vc, w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    pre_k = oracle.prefill_varlen(q, kc.reshape(small), vc.reshape(small), w.query_start_loc,
+                                  w.seq_lens, tables_k, w.scale)
+    np.testing.assert_array_equal(pre, pre_k)
