@@ -56,6 +56,21 @@ def _declare(lib):
     lib.oracle_kv_bytes_per_token.restype = ctypes.c_int64
     lib.oracle_kv_bytes_per_token.argtypes = [ctypes.c_int32] * 4
     lib.oracle_decode.restype = ctypes.c_int
+    _U8 = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_reshape_and_cache_fp8.restype = None
+    lib.oracle_reshape_and_cache_fp8.argtypes = [_U16, _U16, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, _U8, _U8, ctypes.c_int32,
+                                                 ctypes.c_int32, _I64, ctypes.c_float,
+                                                 ctypes.c_float]
+    lib.oracle_decode_fp8.restype = ctypes.c_int
+    lib.oracle_decode_fp8.argtypes = [_F64, _U16, _U8, _U8, _I32, ctypes.c_int32, _I32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                      ctypes.c_double, ctypes.c_double]
     lib.oracle_map_to_kernel_blocks.restype = None
     lib.oracle_map_to_kernel_blocks.argtypes = [_I32, ctypes.c_int32, ctypes.c_int32, _I32]
     lib.oracle_decode.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
@@ -131,6 +146,47 @@ class Oracle:
         self.lib.oracle_reshape_and_cache(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv, d,
                                           _p(kc, _U16), _p(vc, _U16), nb, bs, _p(sm, _I64))
         return kc, vc
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        c = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.oracle_e4m3_decode(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+    def e4m3_encode(self, values) -> np.ndarray:
+        v = np.asarray(values, dtype=np.float32)
+        return np.array([self.lib.oracle_e4m3_encode(float(x)) for x in v.ravel()],
+                        dtype=np.uint8).reshape(v.shape)
+
+    def reshape_and_cache_fp8(self, key, value, key_cache, value_cache, slot_mapping,
+                              k_scale: float, v_scale: float):
+        """bf16 key/value bits -> (new e4m3 key cache, new e4m3 value cache)."""
+        k, v = _u16(key), _u16(value)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8).copy()
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8).copy()
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        nb, bs, hkv, d = kc.shape
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        self.lib.oracle_reshape_and_cache_fp8(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv, d,
+                                              _p(kc, u8), _p(vc, u8), nb, bs, _p(sm, _I64),
+                                              k_scale, v_scale)
+        return kc, vc
+
+    def decode_fp8(self, q, key_cache, value_cache, block_tables, seq_lens, scale,
+                   k_scale: float, v_scale: float) -> np.ndarray:
+        q = _u16(q)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        S, hq, d = q.shape
+        nb, bs, hkv, _ = kc.shape
+        out = np.zeros((S, hq, d), dtype=np.float64)
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        rc = self.lib.oracle_decode_fp8(_p(out, _F64), _p(q, _U16), _p(kc, u8), _p(vc, u8),
+                                        _p(bt, _I32), bt.shape[1], _p(sl, _I32), S, hq, hkv, d, bs,
+                                        scale, k_scale, v_scale)
+        if rc != 0:
+            raise ValueError(f"oracle_decode_fp8 failed ({rc})")
+        return out
 
     def map_to_kernel_blocks(self, ids, k: int) -> np.ndarray:
         """Manager block ids (any shape; last axis = blocks) -> kernel block ids."""

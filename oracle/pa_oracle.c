@@ -254,3 +254,115 @@ void oracle_map_to_kernel_blocks(const int32_t* ids, int32_t n, int32_t k, int32
         for (int32_t j = 0; j < k; ++j)
             out[w++] = ids[i] < 0 ? -1 : (int32_t)((int64_t)ids[i] * k + j);
 }
+
+/* ---- FP8 (e4m3) KV cache ------------------------------------------------
+ * "vLLM 深度解析（二）：PagedAttention 核心机制", section 3.2 (an FP8 KV
+ * cache is loaded as quantized vectors and converted with the cache's
+ * scale: fp8::scaled_convert) and "LLM 推理基础与 vLLM 内部机制", section 2
+ * (FP8 halves the bytes per token).  The e4m3 format: 1 sign bit, 4
+ * exponent bits (bias 7), 3 mantissa bits; exponent field 0 encodes the
+ * subnormals m/8 * 2^-6; 0x7F / 0xFF are NaN; there is no infinity; the
+ * largest finite magnitude is 1.75 * 2^8 = 448.
+ * Readings: a cache value is e4m3(x / scale), the quotient taken in binary32
+ * and rounded to the nearest e4m3 value, ties to the even mantissa, with
+ * magnitudes beyond 448 saturated to 448 (NaN stays NaN); reading it back
+ * gives decoded(e4m3) * scale. */
+
+double oracle_e4m3_decode(uint8_t c) {
+    int sign = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a > 448.0) a = 448.0;
+    /* spacing of the e4m3 values around a */
+    double quantum;
+    if (a < ldexp(1.0, -6)) {
+        quantum = ldexp(1.0, -9);
+    } else {
+        int ex;
+        frexp(a, &ex);                 /* a = f * 2^ex, 0.5 <= f < 1 */
+        quantum = ldexp(1.0, ex - 1 - 3);
+    }
+    double n = a / quantum;            /* exact: a and quantum are dyadic */
+    double fl = floor(n);
+    double r = n - fl;
+    if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double v = fl * quantum;           /* <= 448: 448 is itself an e4m3 value */
+    if (v == 0.0) return sign;
+    if (v < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(v / ldexp(1.0, -9)));
+    int ex;
+    double f = frexp(v, &ex);          /* v = f * 2^ex, mantissa 2f - 1 in [0, 1) */
+    int e = ex - 1 + 7;
+    int m = (int)((2.0 * f - 1.0) * 8.0);
+    return (uint8_t)(sign | (uint8_t)(e << 3) | (uint8_t)m);
+}
+
+/* Quantizing cache write: like oracle_reshape_and_cache, the slot's row of
+ * every kv head receives e4m3(x / scale) of the token's bf16 values. */
+void oracle_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, int32_t num_tokens,
+                                  int32_t num_kv_heads, int32_t head_dim, uint8_t* key_cache,
+                                  uint8_t* value_cache, int32_t num_blocks, int32_t block_size,
+                                  const int64_t* slot_mapping, float k_scale, float v_scale) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+        for (int64_t x = 0; x < row; ++x) {
+            float kf = (float)bf16_to_double(key[(int64_t)i * row + x]);
+            float vf = (float)bf16_to_double(value[(int64_t)i * row + x]);
+            key_cache[slot * row + x] = oracle_e4m3_encode(kf / k_scale);
+            value_cache[slot * row + x] = oracle_e4m3_encode(vf / v_scale);
+        }
+    }
+}
+
+/* Paged decode over an e4m3 cache: the same exact attention as
+ * oracle_decode with k_t = decoded(K) * k_scale and v_t = decoded(V) * v_scale. */
+int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
+                      const uint8_t* value_cache, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, double scale, double k_scale, double v_scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+    int32_t heads_per_kv = num_heads / num_kv_heads;
+    for (int32_t r = 0; r < num_seqs; ++r) {
+        int64_t n = seq_lens[r];
+        double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        if (!w) return -2;
+        const int32_t* table = block_tables + (int64_t)r * max_blocks_per_seq;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const uint16_t* qh = q + ((int64_t)r * num_heads + h) * head_dim;
+            int32_t kvh = h / heads_per_kv;
+            double top = -INFINITY;
+            for (int64_t t = 0; t < n; ++t) {
+                const uint8_t* kr = key_cache +
+                    (((int64_t)table[t / block_size] * block_size + t % block_size) * num_kv_heads + kvh) * head_dim;
+                double acc = 0.0;
+                for (int32_t x = 0; x < head_dim; ++x)
+                    acc += bf16_to_double(qh[x]) * (oracle_e4m3_decode(kr[x]) * k_scale);
+                w[t] = acc * scale;
+                if (w[t] > top) top = w[t];
+            }
+            double total = 0.0;
+            for (int64_t t = 0; t < n; ++t) { w[t] = exp(w[t] - top); total += w[t]; }
+            double* o = out + ((int64_t)r * num_heads + h) * head_dim;
+            for (int32_t x = 0; x < head_dim; ++x) o[x] = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                const uint8_t* vr = value_cache +
+                    (((int64_t)table[t / block_size] * block_size + t % block_size) * num_kv_heads + kvh) * head_dim;
+                for (int32_t x = 0; x < head_dim; ++x)
+                    o[x] += (w[t] / total) * (oracle_e4m3_decode(vr[x]) * v_scale);
+            }
+        }
+        free(w);
+    }
+    return 0;
+}

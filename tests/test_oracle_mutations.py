@@ -44,6 +44,13 @@ MUTATIONS = [
     ("kernel_ids_transposed", "(int32_t)((int64_t)ids[i] * k + j)", "(int32_t)((int64_t)ids[i] + j * k)",
      ["kernel_blocks"]),
     ("kernel_ids_padding_kept", "ids[i] < 0 ? -1 :", "ids[i] < -1 ? -1 :", ["kernel_blocks_padding"]),
+    ("e4m3_ties_away_from_zero", "if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;",
+     "if (r >= 0.5) fl += 1.0;", ["e4m3_torch"]),
+    ("e4m3_no_saturation", "if (a > 448.0) a = 448.0;", "/* no clamp */", ["e4m3_saturate"]),
+    ("e4m3_subnormal_scale", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);",
+     ["e4m3_decode"]),
+    ("fp8_decode_ignores_v_scale", "(oracle_e4m3_decode(vr[x]) * v_scale)", "(oracle_e4m3_decode(vr[x]))",
+     ["fp8_decode"]),
 ]
 
 PINS = {
@@ -54,6 +61,10 @@ PINS = {
     "sdpa_decode": lambda o: pins.test_decode_matches_torch_sdpa(o, 4, 2, 64, [25, 12, 37, 20], 16),
     "sdpa_decode_b32": lambda o: pins.test_decode_matches_torch_sdpa(o, 8, 2, 64, [31, 64, 70], 32),
     "kernel_blocks": lambda o: pins.test_kernel_blocks_printed_on_pages(o),
+    "e4m3_torch": lambda o: pins.test_e4m3_encode_matches_torch_in_range(o),
+    "e4m3_saturate": lambda o: pins.test_e4m3_encode_saturates_and_keeps_nan(o),
+    "e4m3_decode": lambda o: pins.test_e4m3_codes_decode_like_torch(o),
+    "fp8_decode": lambda o: pins.test_decode_fp8_equals_decode_of_dequantized_cache(o, 0.25, 4.0),
     "kernel_blocks_padding": lambda o: pins.test_kernel_blocks_identity_and_padding(o),
     "sdpa_prefill": lambda o: pins.test_prefill_matches_torch_sdpa_bottom_right_causal(o),
     "online": lambda o: pins.test_online_softmax_equals_direct(o, "block16"),

@@ -362,3 +362,89 @@ def test_block_size_views_agree(oracle, B, k):
     pre_k = oracle.prefill_varlen(q, kc.reshape(small), vc.reshape(small), w.query_start_loc,
                                   w.seq_lens, tables_k, w.scale)
     np.testing.assert_array_equal(pre, pre_k)
+
+
+# ------------------------------------------------------------ FP8 (e4m3)
+
+def test_e4m3_codes_decode_like_torch(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(ref))
+    np.testing.assert_array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+    assert np.nanmax(mine) == 448.0 and mine[0x01] == 2.0 ** -9 and mine[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_in_range(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    finite = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = (finite[1:] + finite[:-1]) / 2  # every tie between neighbours
+    rng = np.random.default_rng(8)
+    probe = np.concatenate([finite, mids, rng.uniform(-463.9, 463.9, 4000),
+                            rng.standard_normal(2000) * 1e-2]).astype(np.float32)
+    probe = probe[np.abs(probe) < 464]
+    ref = torch.from_numpy(probe).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(probe), ref)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan(oracle):
+    got = oracle.e4m3_encode(np.array([464.0, 1e6, np.inf, -464.0, -3e38, np.nan], np.float32))
+    np.testing.assert_array_equal(got, [0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F])
+
+
+def test_e4m3_encode_inverts_decode(oracle):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes).astype(np.float32)),
+                                  codes)
+
+
+def _fp8_workload(seed):
+    w = wl.random_workload(seed, num_seqs=5, max_len=180, num_heads=8, num_kv_heads=2, head_dim=64)
+    t = wl.make_tensors(w)
+    rng = np.random.default_rng(seed)
+    kc8 = rng.integers(0, 256, size=t.key_cache.shape, dtype=np.uint8)
+    vc8 = rng.integers(0, 256, size=t.value_cache.shape, dtype=np.uint8)
+    for c in (kc8, vc8):  # no NaN codes
+        c[(c & 0x7F) == 0x7F] = 0x3C
+    return w, t, kc8, vc8
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.25, 4.0), (2.0 ** -7, 2.0 ** 5)])
+def test_decode_fp8_equals_decode_of_dequantized_cache(oracle, k_scale, v_scale):
+    """With power-of-two scales every dequantized value is a bf16 value, so
+    the FP8 decode must equal the (separately pinned) bf16 decode exactly."""
+    w, t, kc8, vc8 = _fp8_workload(61)
+    deq = lambda c, s: torch.from_numpy(oracle.e4m3_decode(c) * s).to(torch.bfloat16)
+    kb, vb = deq(kc8, k_scale), deq(vc8, v_scale)
+    assert torch.equal(kb.double(), torch.from_numpy(oracle.e4m3_decode(kc8) * k_scale))
+    q = t.q.view(torch.int16).numpy()
+    ref = oracle.decode(q, kb.view(torch.int16).numpy(), vb.view(torch.int16).numpy(),
+                        w.block_tables, w.seq_lens, w.scale)
+    got = oracle.decode_fp8(q, kc8, vc8, w.block_tables, w.seq_lens, w.scale, k_scale, v_scale)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_reshape_and_cache_fp8_scatter(oracle):
+    w, t, kc8, vc8 = _fp8_workload(62)
+    rng = np.random.default_rng(62)
+    n = 11
+    gen = torch.Generator().manual_seed(62)
+    shape = (n, w.num_kv_heads, w.head_dim)
+    key = (torch.randn(shape, generator=gen) * 20).to(torch.bfloat16).view(torch.int16).numpy()
+    value = torch.randn(shape, generator=gen).to(torch.bfloat16).view(torch.int16).numpy()
+    slots = rng.choice(w.num_blocks * w.block_size, size=n, replace=False).astype(np.int64)
+    slots[3] = -1
+    kn, vn = oracle.reshape_and_cache_fp8(key, value, kc8, vc8, slots, 0.5, 0.125)
+    flat = lambda c: c.reshape(-1, w.num_kv_heads, w.head_dim)
+    kf = torch.from_numpy(key).view(torch.bfloat16).float().numpy()
+    vf = torch.from_numpy(value).view(torch.bfloat16).float().numpy()
+    touched = np.zeros(w.num_blocks * w.block_size, bool)
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        touched[s] = True
+        np.testing.assert_array_equal(flat(kn)[s], oracle.e4m3_encode(kf[i] / np.float32(0.5)))
+        np.testing.assert_array_equal(flat(vn)[s], oracle.e4m3_encode(vf[i] / np.float32(0.125)))
+    np.testing.assert_array_equal(flat(kn)[~touched], flat(kc8)[~touched])
+    np.testing.assert_array_equal(flat(vn)[~touched], flat(vc8)[~touched])
