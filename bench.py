@@ -392,8 +392,52 @@ def extra_mixed(pa, name, dev, flush, reps=20):
     return res
 
 
+def extra_decode_fp8(pa, name, dev, flush, reps=20):
+    """Decode-only timing of a named workload over an e4m3 copy of its cache
+    (per-tensor scales amax / 448); bytes counted at 1 per element."""
+    w = wl.NAMED[name]()
+    t = wl.make_tensors(w, device=dev)
+    ab = algorithmic_bytes(w)
+    k_scale = float(t.key_cache.float().abs().max()) / 448.0
+    v_scale = float(t.value_cache.float().abs().max()) / 448.0
+    kc = (t.key_cache.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc = (t.value_cache.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    del t.key_cache, t.value_cache
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
+                                                   w.head_dim, w.max_seq_len), dev)
+    out = torch.empty_like(t.q)
+    call = lambda: pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                                 k_scale, v_scale, out=out, workspace=ws)
+    for _ in range(3):
+        flush.add_(1)
+        call()
+    ms = []
+    for _ in range(reps):
+        flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    s = statistics.median(ms) / 1e3
+    peak, _ = measured_peaks()
+    kv8 = ab["kv_bytes"] // 2
+    dec8 = ab["decode_bytes"] - ab["kv_bytes"] + kv8
+    res = {"kv_dtype": "e4m3", "us_per_call": round(s * 1e6, 2), "kv_gbs": round(kv8 / s / 1e9, 2),
+           "decode_gbs": round(dec8 / s / 1e9, 2),
+           "frac_of_measured_peak": round(dec8 / s / 1e9 / peak, 4),
+           "kv_tokens_per_us": round(ab["kv_unique_tokens"] / (s * 1e6), 1)}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
 def extra_decode(pa, name, dev, flush, reps=20):
     """Decode-only timing of another named workload (context for the line)."""
+    if name.endswith("_fp8"):
+        return extra_decode_fp8(pa, name[:-len("_fp8")], dev, flush, reps)
     if wl.NAMED[name]().max_query_len > 1:
         return extra_mixed(pa, name, dev, flush, reps)
     w = wl.NAMED[name]()
@@ -506,7 +550,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b_decode_b64", choices=sorted(wl.NAMED))
     ap.add_argument("--extra", nargs="*", default=["long_ctx_decode_8x32k",
                                                     "prefix_shared_decode_b256",
-                                                    "mixed_chunked_prefill"])
+                                                    "mixed_chunked_prefill",
+                                                    "llama8b_decode_b64_fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -119,6 +119,30 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
                                int32_t* device_status, void* stream);
 
 /*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into an FP8 (e4m3) cache.
+ * ("vLLM 深度解析（二）", section 3.2: an FP8 KV cache is stored quantized
+ * and converted back with the cache's scale, fp8::scaled_convert; "LLM 推理
+ * 基础与 vLLM 内部机制", section 2: FP8 halves the bytes per token.)
+ *
+ *   key_cache, value_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *                 e4m3 bytes (OCP FP8 E4M3: 1 sign, 4 exponent bits with
+ *                 bias 7, 3 mantissa bits, no infinity, 0x7F = NaN)
+ *   k_scale, v_scale  per-tensor scales, finite and > 0
+ * Each value x becomes e4m3(x / scale): the quotient in binary32, rounded to
+ * the nearest e4m3 value (ties to the even mantissa), magnitudes beyond 448
+ * saturated to 448, NaN kept.  Other arguments, slots and errors as
+ * pa_reshape_and_cache; head_dim a multiple of 16.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value,
+                                   int64_t key_stride, int64_t value_stride,
+                                   void* key_cache, void* value_cache,
+                                   const int64_t* slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks,
+                                   float k_scale, float v_scale,
+                                   int32_t* device_status, void* stream);
+
+/*
  * pa_compute_slot_mapping -- slots of this step's new tokens.
  * ("vLLM 深度解析（二）", section 3.1: logical_block = pos / B, offset =
  * pos % B, slot = block_table[request][logical_block] * B + offset.)
@@ -244,6 +268,23 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
  * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs
  * (status record, decode-row partials).  Returns 0 for invalid arguments.
  */
+/*
+ * pa_decode_fp8 -- pa_decode over an FP8 (e4m3) cache written by
+ * pa_reshape_and_cache_fp8: key t contributes decoded(K_t) * k_scale and
+ * value t decoded(V_t) * v_scale ("vLLM 深度解析（二）", section 3.2,
+ * fp8::scaled_convert inside the K/V load).  Same arguments, workspace
+ * (pa_decode_workspace_size) and results as pa_decode otherwise.
+ * Supported: 1 to 4 q heads per kv head (PA_ERR_UNSUPPORTED beyond);
+ * k_scale and v_scale finite and > 0 (else PA_ERR_INVALID).
+ */
+pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                        int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, float scale, float k_scale,
+                        float v_scale, int32_t partition_tokens, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len);
 

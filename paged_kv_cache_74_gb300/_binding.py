@@ -25,7 +25,7 @@ DEVICE_ERRORS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "bad seq_len",
 ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
                "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
-               "pa_map_to_kernel_blocks")
+               "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8")
 
 
 class PAError(RuntimeError):
@@ -48,6 +48,12 @@ def _declare(lib):
     lib.pa_compute_slot_mapping.restype = ctypes.c_int
     lib.pa_compute_slot_mapping.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                             _vp, _vp]
+    lib.pa_reshape_and_cache_fp8.restype = ctypes.c_int
+    lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _i32,
+                                             _i32, _i32, _i32, _f32, _f32, _vp, _vp]
+    lib.pa_decode_fp8.restype = ctypes.c_int
+    lib.pa_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                  _i32, _i32, _i32, _f32, _f32, _f32, _i32, _vp, _sz, _vp]
     lib.pa_map_to_kernel_blocks.restype = ctypes.c_int
     lib.pa_map_to_kernel_blocks.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp]
     lib.pa_decode_workspace_size.restype = _sz
@@ -132,6 +138,26 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=N
         _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, _ptr(status), _stream()))
 
 
+def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale,
+                          status=None):
+    """Quantizing write into e4m3 caches (uint8 [nb, bs, Hkv, d]): e4m3(x / scale)."""
+    _cuda("key", key, torch.bfloat16)
+    _cuda("value", value, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.uint8)
+    _contig("value_cache", value_cache, torch.uint8)
+    _contig("slot_mapping", slot_mapping, torch.int64)
+    nb, bs, hkv, d = key_cache.shape
+    T = slot_mapping.shape[0]
+    for name, t in (("key", key), ("value", value)):
+        if tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, {hkv}, {d}] with contiguous heads")
+    lib = load_library()
+    _check("pa_reshape_and_cache_fp8", lib.pa_reshape_and_cache_fp8(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache),
+        _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, float(k_scale), float(v_scale),
+        _ptr(status), _stream()))
+
+
 def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, num_blocks,
                          total_tokens, out=None, status=None):
     _contig("block_tables", block_tables, torch.int32)
@@ -195,6 +221,33 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
         float(scale), int(partition_tokens), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def decode_fp8(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale, k_scale,
+               v_scale, out=None, workspace=None, partition_tokens=0):
+    """Paged decode over e4m3 caches (uint8 [nb, bs, Hkv, d]); q, out bf16."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.uint8)
+    _contig("value_cache", value_cache, torch.uint8)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    S, hq, d = q.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    if d2 != d or value_cache.shape != key_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(S, hq, hkv, d, max_seq_len, partition_tokens),
+                                  q.device)
+    lib = load_library()
+    _check("pa_decode_fp8", lib.pa_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
+        float(scale), float(k_scale), float(v_scale), int(partition_tokens), _ptr(workspace),
+        workspace.numel(), _stream()))
     return out
 
 

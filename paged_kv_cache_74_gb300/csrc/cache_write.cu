@@ -53,6 +53,56 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
   }
 }
 
+// Two floats to two e4m3 codes (low byte = lo): nearest even, magnitudes
+// beyond 448 saturated, NaN kept.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The quantizing write of an e4m3 cache ("vLLM 深度解析（二）", section 3.2:
+// the FP8 cache is stored quantized with a per-tensor scale): each lane
+// turns 8 bf16 values x into e4m3(x / scale) and stores 8 bytes.
+__global__ void __launch_bounds__(kWriteWarps * 32)
+reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                             int64_t key_stride_chunks, int64_t value_stride_chunks,
+                             uint2* __restrict__ key_cache, uint2* __restrict__ value_cache,
+                             const int64_t* __restrict__ slot_mapping, int num_tokens,
+                             int row_chunks, int64_t num_slots, float k_scale, float v_scale,
+                             int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();  // slot_mapping may come from the previous kernel
+  const int token = blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (token >= num_tokens) return;
+  const int64_t slot = slot_mapping[token];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (lane == 0) record_error(status, PA_DEV_BAD_SLOT, token, static_cast<int>(slot));
+    return;
+  }
+  auto quantize = [](uint4 w, float scale) -> uint2 {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __fdiv_rn(__uint_as_float(ws[e] << 16), scale);
+      const float hi = __fdiv_rn(__uint_as_float(ws[e] & 0xffff0000u), scale);
+      out[e] = e4m3x2(lo, hi);
+    }
+    return make_uint2(out[0] | (out[1] << 16), out[2] | (out[3] << 16));
+  };
+  const uint4* ks = key + token * key_stride_chunks;
+  const uint4* vs = value + token * value_stride_chunks;
+  uint2* kd = key_cache + slot * row_chunks;
+  uint2* vd = value_cache + slot * row_chunks;
+  for (int c = lane; c < row_chunks; c += 32) {
+    kd[c] = quantize(__ldg(ks + c), k_scale);
+    vd[c] = quantize(__ldg(vs + c), v_scale);
+  }
+}
+
 // One CTA per request; its threads cover the request's new tokens.
 __global__ void __launch_bounds__(128)
 slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
@@ -127,6 +177,19 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                            key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
                            static_cast<uint4*>(value_cache), slot_mapping, num_tokens,
                            row_elems / 8, num_slots, status);
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_stride,
+                                         int64_t value_stride, void* key_cache, void* value_cache,
+                                         const int64_t* slot_mapping, int num_tokens, int row_elems,
+                                         int64_t num_slots, float k_scale, float v_scale,
+                                         int32_t* status, cudaStream_t stream) {
+  const int grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
+  return launch_overlapped(reshape_and_cache_fp8_kernel, dim3(grid), dim3(kWriteWarps * 32), 0,
+                           stream, static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                           key_stride / 8, value_stride / 8, static_cast<uint2*>(key_cache),
+                           static_cast<uint2*>(value_cache), slot_mapping, num_tokens,
+                           row_elems / 8, num_slots, k_scale, v_scale, status);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,

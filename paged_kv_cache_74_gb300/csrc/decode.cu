@@ -55,7 +55,7 @@ constexpr int kLastRow = 2;  // the segment ends after this row of stages
 constexpr int kDone = 4;     // no more work for the warp that receives it
 
 
-template <int D, int GMAX>
+template <int D, int GMAX, bool KV8 = false>
 struct DecodeCfg {
   static constexpr int T = (D == 128 && GMAX >= 4) ? 16 : 8;  // lanes per token
   static constexpr int NG = 32 / T;                            // token groups per warp
@@ -72,12 +72,15 @@ struct DecodeCfg {
   static constexpr int CH = V / 4;                             // 16-byte chunks per transpose row
   static constexpr int NC = 4;                                 // consumer warps
   static constexpr int MINB = GMAX * EL > 32 ? 2 : 3;          // CTAs per SM the registers allow
-  static constexpr int TILE = kBlockSize * D * 2;              // bytes of one (block, kv head) tile
+  static constexpr int ELT = KV8 ? 1 : 2;                      // bytes per K/V element (e4m3 / bf16)
+  static constexpr int TILE = kBlockSize * D * ELT;            // bytes of one (block, kv head) tile
   // The partial-score transpose (32 rows of V floats) reuses the warp's own
   // K tile once its q.k products are done, when it fits and no later
   // sub-batch still needs K; otherwise each warp gets a dedicated buffer.
   static constexpr bool XPOSE_IN_K = 32 * CH * 16 <= TILE && NSB == 1;
-  static constexpr int STAGES = D == 128 ? 8 : 16;             // a multiple of NC (see below)
+  // A multiple of NC (see below).  e4m3 tiles are half as large: more of
+  // them fit, and more tokens are in flight.
+  static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 ? (XPOSE_IN_K ? 4 : 3) : 2) / 2;
   // shared memory carve-up (bytes)
   static constexpr int RING = STAGES * 2 * TILE;
   static constexpr int XPOSE = XPOSE_IN_K ? 0 : NC * 32 * CH * 16;
@@ -120,11 +123,39 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-template <int D, int GMAX>
-__global__ void __launch_bounds__(DecodeCfg<D, GMAX>::THREADS, DecodeCfg<D, GMAX>::MINB)
+// Eight consecutive K or V elements of one row, as stored: bf16 (16 bytes)
+// or e4m3 (8 bytes).  pair(e) returns elements 2e, 2e + 1 as fp32; every
+// e4m3 value is exact in f16, so the conversion loses nothing.
+template <bool KV8>
+struct Row8 {
+  uint4 w;
+  __device__ __forceinline__ void load(uint32_t addr) { w = ld_shared_v4(addr); }
+  __device__ __forceinline__ void clear() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float2 pair(int e) const {
+    return unpack2(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+  }
+};
+template <>
+struct Row8<true> {
+  uint2 w;
+  __device__ __forceinline__ void load(uint32_t addr) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w.x), "=r"(w.y) : "r"(addr));
+  }
+  __device__ __forceinline__ void clear() { w = make_uint2(0u, 0u); }
+  __device__ __forceinline__ float2 pair(int e) const {
+    const uint32_t word = e < 2 ? w.x : w.y;
+    const uint16_t two = static_cast<uint16_t>(e & 1 ? word >> 16 : word & 0xffffu);
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  }
+};
+
+template <int D, int GMAX, bool KV8>
+__global__ void __launch_bounds__(DecodeCfg<D, GMAX, KV8>::THREADS, DecodeCfg<D, GMAX, KV8>::MINB)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using C = DecodeCfg<D, GMAX>;
+  using C = DecodeCfg<D, GMAX, KV8>;
   const int cta = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -486,19 +517,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int kk = 0; kk < C::SB; ++kk) {
           const int t = (sb * C::SB + kk) * C::NG + g;
-          uint4 kw[C::CPL];
+          Row8<KV8> kw[C::CPL];
+#pragma unroll
+          for (int j = 0; j < C::CPL; ++j) kw[j].load(kt + (t * D + (li + C::T * j) * 8) * C::ELT);
+          float2 kf[C::CPL][4];
 #pragma unroll
           for (int j = 0; j < C::CPL; ++j)
-            kw[j] = ld_shared_v4(kt + t * (D * 2) + (li + C::T * j) * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kf[j][e] = kw[j].pair(e);
 #pragma unroll
           for (int h = 0; h < GMAX; ++h) {
             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < C::CPL; ++j) {
-              acc = __ffma2_rn(q2[h][j * 4 + 0], unpack2(kw[j].x), acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 1], unpack2(kw[j].y), acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 2], unpack2(kw[j].z), acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 3], unpack2(kw[j].w), acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 0], kf[j][0], acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 1], kf[j][1], acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 2], kf[j][2], acc);
+              acc = __ffma2_rn(q2[h][j * 4 + 3], kf[j][3], acc);
             }
             x[h * C::SB + kk] = acc.x + acc.y;
           }
@@ -587,23 +622,27 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
           for (int kk = 0; kk < C::SB; ++kk) {
             const int t = (sb * C::SB + kk) * C::NG + g;
-            uint4 vw[C::CPL];
+            Row8<KV8> vw[C::CPL];
 #pragma unroll
-            for (int j = 0; j < C::CPL; ++j)
-              vw[j] = ld_shared_v4(vt + t * (D * 2) + (li + C::T * j) * 16);
+            for (int j = 0; j < C::CPL; ++j) vw[j].load(vt + (t * D + (li + C::T * j) * 8) * C::ELT);
             if (check && tok0 + t >= seq_len) {
 #pragma unroll
-              for (int j = 0; j < C::CPL; ++j) vw[j] = make_uint4(0u, 0u, 0u, 0u);
+              for (int j = 0; j < C::CPL; ++j) vw[j].clear();
             }
+            float2 vf[C::CPL][4];
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) vf[j][e] = vw[j].pair(e);
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
               const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
 #pragma unroll
               for (int j = 0; j < C::CPL; ++j) {
-                o2[h][j * 4 + 0] = __ffma2_rn(pp, unpack2(vw[j].x), o2[h][j * 4 + 0]);
-                o2[h][j * 4 + 1] = __ffma2_rn(pp, unpack2(vw[j].y), o2[h][j * 4 + 1]);
-                o2[h][j * 4 + 2] = __ffma2_rn(pp, unpack2(vw[j].z), o2[h][j * 4 + 2]);
-                o2[h][j * 4 + 3] = __ffma2_rn(pp, unpack2(vw[j].w), o2[h][j * 4 + 3]);
+                o2[h][j * 4 + 0] = __ffma2_rn(pp, vf[j][0], o2[h][j * 4 + 0]);
+                o2[h][j * 4 + 1] = __ffma2_rn(pp, vf[j][1], o2[h][j * 4 + 1]);
+                o2[h][j * 4 + 2] = __ffma2_rn(pp, vf[j][2], o2[h][j * 4 + 2]);
+                o2[h][j * 4 + 3] = __ffma2_rn(pp, vf[j][3], o2[h][j * 4 + 3]);
               }
             }
           }
@@ -669,7 +708,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         o0 = fmaf(wt, ov.x, o0);
         o1 = fmaf(wt, ov.y, o1);
       }
-      const float inv = 1.f / L;
+      const float inv = a.v_scale / L;  // v_scale: the e4m3 cache's V scale, else 1
       if (si.kind == kWhole) {
         *reinterpret_cast<__nv_bfloat162*>(
             a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
@@ -724,19 +763,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-template <int D, int GMAX>
+template <int D, int GMAX, bool KV8>
 cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t stream) {
-  using C = DecodeCfg<D, GMAX>;
-  cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX>,
+  using C = DecodeCfg<D, GMAX, KV8>;
+  cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX, KV8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX>,
+  err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX, KV8>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (err != cudaSuccess) return err;
-  return launch_overlapped(paged_decode_kernel<D, GMAX>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
-                           stream, kmap, vmap, a);
+  return launch_overlapped(paged_decode_kernel<D, GMAX, KV8>, dim3(a.num_ctas), dim3(C::THREADS),
+                           C::SMEM, stream, kmap, vmap, a);
 }
 
 }  // namespace
@@ -759,10 +798,12 @@ int decode_ctas_per_sm(int head_dim, int group) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          int head_dim, cudaStream_t stream) {
+                          int head_dim, bool kv8, cudaStream_t stream) {
   const int gmax = decode_gmax(a.group);
-#define PA_DECODE_CASE(DD, GG) \
-  if (head_dim == DD && gmax == GG) return launch_decode_impl<DD, GG>(a, kmap, vmap, stream);
+#define PA_DECODE_CASE(DD, GG)                                                      \
+  if (head_dim == DD && gmax == GG)                                                 \
+    return kv8 ? launch_decode_impl<DD, GG, true>(a, kmap, vmap, stream)            \
+               : launch_decode_impl<DD, GG, false>(a, kmap, vmap, stream);
   PA_DECODE_CASE(128, 1) PA_DECODE_CASE(128, 2) PA_DECODE_CASE(128, 4)
   PA_DECODE_CASE(64, 1) PA_DECODE_CASE(64, 2) PA_DECODE_CASE(64, 4)
 #undef PA_DECODE_CASE

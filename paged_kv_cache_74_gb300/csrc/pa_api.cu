@@ -84,18 +84,20 @@ int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group,
 // first for TMA: {head_dim, kv_heads, slots}); one box is one (block, kv head)
 // tile of 16 tokens x head_dim.
 bool make_cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
-                    int head_dim) {
+                    int head_dim, bool e4m3 = false) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
+  const cuuint64_t elt = e4m3 ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
                               static_cast<cuuint64_t>(num_kv_heads),
                               static_cast<cuuint64_t>(num_blocks) * kBlockSize};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elt,
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * elt};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(kBlockSize)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides,
+  return enc(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(cache), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -254,13 +256,20 @@ pa_status check_decode_args(const void* out, const void* q, const void* key_cach
   return PA_OK;
 }
 
+// Element type of the K/V cache and its scales.
+struct KvFormat {
+  bool e4m3 = false;
+  float k_scale = 1.f, v_scale = 1.f;
+};
+
 pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, const void* value_cache,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              const int32_t* seq_lens, const int32_t* query_start_loc,
                              int32_t num_seqs, int32_t total_q, int32_t max_seq_len,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t num_blocks, int32_t block_size, float scale,
-                             const DecodeLayout& L, void* workspace, cudaStream_t stream) {
+                             const DecodeLayout& L, void* workspace, cudaStream_t stream,
+                             const KvFormat& kv = KvFormat()) {
   // The TMA views address the cache in 16-token tiles.
   const int num_tiles16 = num_blocks * (block_size / kBlockSize);
   const bool tc = decode_uses_tc(head_dim, num_heads / num_kv_heads);
@@ -270,8 +279,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
         !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
-  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
-             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim)) {
+  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim, kv.e4m3) ||
+             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim, kv.e4m3)) {
     return PA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -297,9 +306,11 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.tile_shift = tile_shift_of(block_size);
   a.total_q = total_q;
   a.epoch = next_epoch();
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale_log2 = scale * 1.4426950408889634f * kv.k_scale;
+  a.v_scale = kv.v_scale;
+  if (tc && kv.e4m3) return PA_ERR_UNSUPPORTED;
   const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, stream)
-                            : launch_decode(a, kmap, vmap, head_dim, stream);
+                            : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, stream);
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -322,6 +333,33 @@ const char* pa_status_string(int status) {
 }
 
 int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_stride,
+                                   int64_t value_stride, void* key_cache, void* value_cache,
+                                   const int64_t* slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int32_t num_blocks, float k_scale, float v_scale,
+                                   int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1 || block_size < 1) return PA_ERR_INVALID;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID;
+  if (head_dim < 16 || head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(slot_mapping, 8) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+    return PA_ERR_INVALID;
+  const cudaError_t e = launch_reshape_and_cache_fp8(
+      key, value, key_stride, value_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      static_cast<int>(row), static_cast<int64_t>(num_blocks) * block_size, k_scale, v_scale,
+      device_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
                                int64_t value_stride, void* key_cache, void* value_cache,
@@ -416,6 +454,37 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
                             seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
                             num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,
                             static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                        int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, float scale, float k_scale,
+                        float v_scale, int32_t partition_tokens, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale);
+  if (st != PA_OK) return st;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID;
+  if (decode_uses_tc(head_dim, num_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
+  if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
+                                       partition_tokens);
+  if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  KvFormat kv;
+  kv.e4m3 = true;
+  kv.k_scale = k_scale;
+  kv.v_scale = v_scale;
+  return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,
+                            static_cast<cudaStream_t>(stream), kv);
 }
 
 size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,

@@ -47,7 +47,8 @@ struct DecodeArgs {
   int tile_shift;                   // log2(block_size / 16)
   int total_q;                      // rows of q / out
   unsigned epoch;                   // distinct per call (never 0)
-  float scale_log2;                 // softmax scale * log2(e)
+  float scale_log2;                 // softmax scale * log2(e) (* k_scale for an e4m3 cache)
+  float v_scale;                    // multiplies O: the e4m3 cache's V scale, else 1
 };
 
 // Launch `kernel` on `stream` with programmatic stream serialization: the
@@ -72,8 +73,10 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // Launchers (decode.cu).  Return a cudaError_t from the launch.
+// kv8: the caches hold e4m3 values (their scales folded into scale_log2
+// and v_scale) instead of bf16.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          int head_dim, cudaStream_t stream);
+                          int head_dim, bool kv8, cudaStream_t stream);
 // Tensor-core decode (decode_tc.cu): qmap = q as {head_dim, heads, rows}
 // with a {64, group, 1} box; kmap, vmap = the caches as {64, 8, head_dim /
 // 64, slots / 8, kv heads} with a {64, 8, head_dim / 64, 2, 1} box (one
@@ -117,6 +120,12 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      int64_t value_stride, void* key_cache, void* value_cache,
                                      const int64_t* slot_mapping, int num_tokens, int row_elems,
                                      int64_t num_slots, int32_t* status, cudaStream_t stream);
+// e4m3 cache write: cache = e4m3(x / scale), nearest even, saturated to 448.
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_stride,
+                                         int64_t value_stride, void* key_cache, void* value_cache,
+                                         const int64_t* slot_mapping, int num_tokens, int row_elems,
+                                         int64_t num_slots, float k_scale, float v_scale,
+                                         int32_t* status, cudaStream_t stream);
 cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
                                      int32_t* status, cudaStream_t stream);
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,

@@ -136,3 +136,33 @@ def test_map_to_kernel_blocks_validation(lib, args, expect):
     out, src, rows, cols, k = args
     vp = ctypes.c_void_p
     assert lib.pa_map_to_kernel_blocks(vp(out), vp(src), rows, cols, k, vp(0), vp(0)) == expect
+
+
+def decode_fp8_call(lib, **kw):
+    args = dict(out=A, q=A, kc=A, vc=A, bt=A, mb=4, sl=A, ns=2, msl=64, hq=8, hkv=2, d=128, bs=16,
+                nb=32, scale=0.125, ks=1.0, vs=1.0, pt=0, ws=A, wsb=1 << 20)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.pa_decode_fp8(vp(args["out"]), vp(args["q"]), vp(args["kc"]), vp(args["vc"]),
+                             vp(args["bt"]), args["mb"], vp(args["sl"]), args["ns"], args["msl"],
+                             args["hq"], args["hkv"], args["d"], args["bs"], args["nb"],
+                             args["scale"], args["ks"], args["vs"], args["pt"], vp(args["ws"]),
+                             args["wsb"], vp(0))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ks=0.0), 1), (dict(vs=-1.0), 1), (dict(ks=float("nan")), 1), (dict(vs=float("inf")), 1),
+    (dict(q=0), 1), (dict(hq=64, hkv=8), 2), (dict(d=96), 2), (dict(ws=0), 3),
+])
+def test_decode_fp8_rejects_invalid_arguments(lib, kw, expect):
+    assert decode_fp8_call(lib, **kw) == expect
+
+
+def test_reshape_and_cache_fp8_rejects_bad_scales(lib):
+    vp = ctypes.c_void_p
+    for ks, vs in ((0.0, 1.0), (1.0, float("nan")), (-2.0, 1.0)):
+        assert lib.pa_reshape_and_cache_fp8(vp(A), vp(A), 256, 256, vp(A), vp(A), vp(A), 4, 2, 128,
+                                            16, 32, ks, vs, vp(0), vp(0)) == 1
+    # num_tokens == 0 is a no-op even with null pointers
+    assert lib.pa_reshape_and_cache_fp8(vp(0), vp(0), 256, 256, vp(0), vp(0), vp(0), 0, 2, 128, 16,
+                                        32, 1.0, 1.0, vp(0), vp(0)) == 0

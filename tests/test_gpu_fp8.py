@@ -1,0 +1,133 @@
+"""GPU parity of the FP8 (e4m3) KV cache: the quantizing cache write is
+bit-exact against the oracle (round to nearest even, saturating, scales that
+are not powers of two included), and pa_decode_fp8 matches the fp64 oracle's
+FP8 decode within max abs 1e-2, mean abs 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close_to_oracle, bits
+from paged_kv_cache_74_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+NAN_E4M3 = 0x7F
+
+
+def fp8_caches(w, t, k_scale, v_scale, seed):
+    """e4m3 caches holding N(0, 1) values (codes of x / scale), NaN codes in
+    every slot outside a request's context."""
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    k = torch.randn(shape, generator=gen, device="cuda")
+    v = torch.randn(shape, generator=gen, device="cuda")
+    kc = (k / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc = (v / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    used = torch.zeros(w.num_blocks * w.block_size, dtype=torch.bool)
+    for r in range(w.num_seqs):
+        L = int(w.seq_lens[r])
+        for tok in range(L):
+            used[int(w.block_tables[r, tok // w.block_size]) * w.block_size + tok % w.block_size] = True
+    unused = (~used).cuda().view(w.num_blocks, w.block_size)
+    kc[unused] = NAN_E4M3
+    vc[unused] = NAN_E4M3
+    return kc.contiguous(), vc.contiguous()
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 0.125), (0.013, 7.7), (3e-4, 0.021)])
+def test_fp8_write_bit_exact(cuda_lib, oracle, k_scale, v_scale):
+    pa = cuda_lib
+    w = wl.random_workload(301, num_seqs=6, max_len=400, num_heads=8, num_kv_heads=2,
+                           head_dim=128, max_q_len=50, prefill_fraction=0.5)
+    t = wl.make_tensors(w, device="cuda")
+    key = (t.key.float() * 8).to(torch.bfloat16)  # some values saturate at the small scales
+    value = t.value
+    kc = torch.randint(0, 127, (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim),
+                       dtype=torch.uint8, device="cuda")
+    vc = kc.flip(0).contiguous()
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16,
+                                    w.num_blocks, w.total_q)
+    ref_k, ref_v = oracle.reshape_and_cache_fp8(bits(key), bits(value), kc.cpu().numpy(),
+                                                vc.cpu().numpy(), slots.cpu().numpy(), k_scale, v_scale)
+    pa.reshape_and_cache_fp8(key, value, kc, vc, slots, k_scale, v_scale)
+    np.testing.assert_array_equal(kc.cpu().numpy(), ref_k)
+    np.testing.assert_array_equal(vc.cpu().numpy(), ref_v)
+
+
+FP8_SWEEP = [
+    # (head_dim, q heads, kv heads, max_len, num_seqs, block size, seed)
+    (128, 32, 8, 900, 7, 16, 311), (128, 8, 8, 300, 9, 16, 312), (128, 16, 8, 1500, 4, 32, 313),
+    (64, 8, 2, 700, 6, 16, 314), (64, 4, 4, 120, 10, 64, 315), (64, 2, 2, 2000, 3, 16, 316),
+    (128, 4, 1, 257, 5, 16, 317),
+]
+
+
+@pytest.mark.parametrize("d,hq,hkv,max_len,ns,B,seed", FP8_SWEEP)
+def test_decode_fp8_matches_oracle(cuda_lib, oracle, d, hq, hkv, max_len, ns, B, seed):
+    pa = cuda_lib
+    w = wl.random_workload(seed, num_seqs=ns, max_len=max_len, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, block_size=B)
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 2.0 ** -5, 0.03
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, seed)
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                        k_scale, v_scale)
+    ref = oracle.decode_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(), w.block_tables,
+                            w.seq_lens, w.scale, k_scale, v_scale)
+    assert torch.isfinite(out.float()).all()
+    assert_close_to_oracle(out, ref, what=f"fp8 d{d} hq{hq} hkv{hkv} B{B}")
+
+
+def test_decode_fp8_forced_splits(cuda_lib, oracle):
+    """16-token partitions: many partial pieces merged in the kernel."""
+    pa = cuda_lib
+    w = wl.random_workload(318, num_seqs=5, max_len=600, num_heads=32, num_kv_heads=8, head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.05, 0.05, 318)
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale, 0.05,
+                        0.05, partition_tokens=16)
+    ref = oracle.decode_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(), w.block_tables,
+                            w.seq_lens, w.scale, 0.05, 0.05)
+    assert_close_to_oracle(out, ref, what="fp8 forced splits")
+
+
+def test_fp8_write_then_decode(cuda_lib, oracle):
+    """Slot mapping, quantizing write of each request's new token, decode."""
+    pa = cuda_lib
+    w = wl.random_workload(319, num_seqs=8, max_len=800, num_heads=32, num_kv_heads=8, head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 0.04, 0.06
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, 319)
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16,
+                                    w.num_blocks, w.total_q)
+    ref_k, ref_v = oracle.reshape_and_cache_fp8(bits(t.key), bits(t.value), kc.cpu().numpy(),
+                                                vc.cpu().numpy(), slots.cpu().numpy(), k_scale, v_scale)
+    pa.reshape_and_cache_fp8(t.key, t.value, kc, vc, slots, k_scale, v_scale)
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale, k_scale,
+                        v_scale)
+    ref = oracle.decode_fp8(bits(t.q), ref_k, ref_v, w.block_tables, w.seq_lens, w.scale,
+                            k_scale, v_scale)
+    assert_close_to_oracle(out, ref, what="fp8 write then decode")
+
+
+def test_decode_fp8_full_size_8b(cuda_lib, oracle):
+    """The 8B-shaped batch (64 requests, U[512, 4096]) in the benchmark's launch configuration."""
+    pa = cuda_lib
+    w = wl.llama8b_decode()
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 2.0 ** -5, 2.0 ** -5, 320)
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                        2.0 ** -5, 2.0 ** -5)
+    rows = np.sort(np.random.default_rng(320).choice(w.num_seqs, 16, replace=False))
+    ref = oracle.decode_fp8(bits(t.q)[rows], kc.cpu().numpy(), vc.cpu().numpy(),
+                            w.block_tables[rows], w.seq_lens[rows], w.scale, 2.0 ** -5, 2.0 ** -5)
+    assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, what="fp8 8B batch")
+
+
+def test_decode_fp8_rejects_large_groups(cuda_lib):
+    pa = cuda_lib
+    w = wl.random_workload(321, num_seqs=2, max_len=50, num_heads=64, num_kv_heads=8, head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    kc = torch.zeros(t.key_cache.shape, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PAError):
+        pa.decode_fp8(t.q, kc, kc.clone(), t.block_tables, t.seq_lens, w.max_seq_len, w.scale, 1.0, 1.0)
