@@ -122,18 +122,20 @@ struct TcBars {
   static constexpr int COUNT = CREC + NREC;
 };
 
-// A segment: the run of blocks [b0, b0 + nseg) of one (request, kv head)
-// pair inside this CTA's tile range.
+// A segment: the run of 16-token tiles [b0, b0 + nseg) of one (request, kv
+// head) pair inside this CTA's range.  This kernel splits the batch in
+// units of whole 128-token chunks (8 tiles), so a range boundary never cuts
+// a chunk: only the last chunk of a pair can be partial.
 struct TcSeg {
   int row;       // q / out row of the request
   int seq_len;
-  int nblk;      // blocks of the request
+  int npair;     // chunks of the (request, kv head) pair (the split's unit)
   int b0;
   int nseg;
   int kind;      // kWhole, kHead, kTail or kEndSeg
   int r;
   int kvh;
-  long long t0;  // number of the pair's first tile
+  long long t0;  // number of the pair's first chunk
 };
 static_assert(sizeof(TcSeg) <= 48, "segment record");
 
@@ -230,11 +232,11 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       if (r < a.num_seqs) c_nb[k] = request_blocks(a, r, &lv, &rv);
       c_len[k] = lv;
       c_row[k] = rv;
-      nb_sum += c_nb[k];
+      nb_sum += (c_nb[k] + C::CB - 1) / C::CB;  // chunks
     }
     for (int r = 32 * kReqCache + lane; r < a.num_seqs; r += 32) {
       int len, row;
-      nb_sum += request_blocks(a, r, &len, &row);
+      nb_sum += (request_blocks(a, r, &len, &row) + C::CB - 1) / C::CB;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
@@ -288,7 +290,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       h1 = (r < a.num_seqs && 32 + lane < nb) ? __ldg(rp + ((32 + lane) >> a.tile_shift)) : 0;
     };
     if (lo < hi) {
-      // Request holding tile `lo`: scan the per-request tile counts 32 at a time.
+      // Request holding chunk `lo`: scan the per-request chunk counts 32 at a time.
       long long base = 0;
       int r0 = -1;
       for (int rc = 0; rc < a.num_seqs && r0 < 0; rc += 32) {
@@ -301,7 +303,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         } else if (r < a.num_seqs) {
           nbv = request_blocks(a, r, &len, &row);
         }
-        const long long nt = static_cast<long long>(nbv) * a.num_kv_heads;
+        const long long nt = static_cast<long long>((nbv + C::CB - 1) / C::CB) * a.num_kv_heads;
         long long incl = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -318,10 +320,12 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         }
       }
       int r = r0, len = 0, row = 0;
-      int nb = req_info(r, &len, &row);
+      int nb = req_info(r, &len, &row);   // tiles of the request
+      int nc = (nb + C::CB - 1) / C::CB;  // chunks of each of its pairs
       const long long off0 = lo - base;
-      int kvh = static_cast<int>(off0 / nb);
-      int b = static_cast<int>(off0 % nb);
+      int kvh = static_cast<int>(off0 / nc);
+      int cc = static_cast<int>(off0 % nc);  // first chunk of the range in the pair
+      int b = cc * C::CB;
       long long t = lo;
       // Ids of the current request's blocks 0 .. 63 and of the next request's.
       int head0, head1, nhead0, nhead1;
@@ -330,8 +334,9 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       int nnb = req_info(r + 1, &nlen, &nrow);
       load_head(r + 1, nnb, nhead0, nhead1);
       while (t < hi && ok) {
-        const int seg_n = static_cast<int>(min(hi - t, static_cast<long long>(nb - b)));
-        const int kind = (b == 0 && seg_n == nb) ? kWhole : (b > 0 ? kHead : kTail);
+        const int seg_c = static_cast<int>(min(hi - t, static_cast<long long>(nc - cc)));  // chunks
+        const int seg_n = min(seg_c * C::CB, nb - b);                                       // tiles
+        const int kind = (cc == 0 && seg_c == nc) ? kWhole : (cc > 0 ? kHead : kTail);
         const int slot = seg % C::SLOTS;
         // ---- segment record and q (slot reused once its epilogue is done)
         if (seg >= C::SLOTS && !lane0_wait(bar(B::SEGFREE + slot), ((seg / C::SLOTS) - 1) & 1, 20)) {
@@ -342,13 +347,13 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           TcSeg si;
           si.row = row;
           si.seq_len = len;
-          si.nblk = nb;
+          si.npair = nc;
           si.b0 = b;
           si.nseg = seg_n;
           si.kind = kind;
           si.r = r;
           si.kvh = kvh;
-          si.t0 = base + static_cast<long long>(kvh) * nb;
+          si.t0 = base + static_cast<long long>(kvh) * nc;
           segs[slot] = si;
           mbar_arrive_expect_tx(bar(B::QFULL + slot), a.group * D * 2);
 #pragma unroll
@@ -414,14 +419,16 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           ++chunk;
           if (lane == 0) *n_chunks_issued = chunk;
         }
-        t += seg_n;
-        b += seg_n;
+        t += seg_c;
+        cc += seg_c;
+        b = cc * C::CB;
         ++seg;
-        if (b == nb && t < hi) {  // next (request, kv head) pair
+        if (cc == nc && t < hi) {  // next (request, kv head) pair
+          cc = 0;
           b = 0;
           if (++kvh == a.num_kv_heads) {
             kvh = 0;
-            base += static_cast<long long>(nb) * a.num_kv_heads;
+            base += static_cast<long long>(nc) * a.num_kv_heads;
             ++r;
             if (nnb > 0) {  // the prefetched next request
               nb = nnb;
@@ -437,6 +444,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
               }
               if (nb > 0) load_head(r, nb, head0, head1);
             }
+            nc = (nb + C::CB - 1) / C::CB;
             if (nb == 0) {
               ok = false;  // cannot happen while t < hi
             } else {
@@ -778,7 +786,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         if (!(ok = ered_sync())) break;
         const long long W = *total_tiles;
         const int c0 = cta_of_tile(W, a.num_ctas, si.t0);
-        const int c1 = cta_of_tile(W, a.num_ctas, si.t0 + si.nblk - 1);
+        const int c1 = cta_of_tile(W, a.num_ctas, si.t0 + si.npair - 1);
         if (tl == 0)
           *last_flag = contribute(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh,
                                   a.epoch, c1 - c0 + 1, a.status, si.r) ? 1 : 0;
