@@ -551,6 +551,7 @@ def main(argv=None):
     ap.add_argument("--extra", nargs="*", default=["long_ctx_decode_8x32k",
                                                     "prefix_shared_decode_b256",
                                                     "mixed_chunked_prefill",
+                                                    "multi_chunk_prefill",
                                                     "llama8b_decode_b64_fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

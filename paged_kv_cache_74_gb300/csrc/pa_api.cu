@@ -544,6 +544,15 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     p.block_size = block_size;
     p.tile_shift = tile_shift_of(block_size);
     p.total_q = total_q;
+    {
+      // At most one CTA per SM (the tile needs ~227 KB of shared memory) and
+      // never more than the batch can have tiles.
+      const int64_t upper = static_cast<int64_t>(num_seqs) * num_heads *
+                            ceil_div(max_query_len, 128);
+      int sms = sm_count_current_device();
+      if (sms <= 0) sms = 148;
+      p.num_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, upper)));
+    }
     p.scale_log2 = scale * 1.4426950408889634f;
     // The tiles run on a side stream, forked from and joined back into the
     // caller's stream, so they overlap the decode rows.

@@ -88,8 +88,8 @@ int decode_gmax(int group);
 // CTAs per SM the decode kernel for (head_dim, group) is built for.
 int decode_ctas_per_sm(int head_dim, int group);
 
-// Chunked-prefill tiles (prefill.cu): one CTA per (128-row query tile,
-// q head, request) of every request with q_len > 1.
+// Chunked-prefill tiles (prefill.cu): 128-row query tiles of one q head of
+// every request with q_len > 1, taken in turn by a persistent grid.
 struct PrefillArgs {
   __nv_bfloat16* out;               // [total_q, num_heads, D]
   const __nv_bfloat16* q;           // [total_q, num_heads, D]
@@ -110,6 +110,7 @@ struct PrefillArgs {
   int block_size;                   // tokens per cache block: 16, 32 or 64
   int tile_shift;                   // log2(block_size / 16)
   int total_q;
+  int num_ctas;                     // persistent grid (at most one CTA per SM)
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,

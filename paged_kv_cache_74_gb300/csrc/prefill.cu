@@ -92,40 +92,45 @@ constexpr int kPFull = 9;    // [2] softmax wrote P (and finished reading S)
 constexpr int kPVDone = 11;  // [2] P.V MMA done (V stage and P buffer free, O current)
 constexpr int kRed = 13;     // softmax-warp barrier (row-max exchange)
 
+// Query tiles of request r (0 for rows that are not prefill rows or whose
+// lengths are out of range); each tile is 128 rows of one q head.
+__device__ __forceinline__ int prefill_tiles(const PrefillArgs& a, int r) {
+  const int q0 = a.query_start_loc[r];
+  const int q_len = a.query_start_loc[r + 1] - q0;
+  if (q_len <= 1) return 0;
+  const int seq_len = a.seq_lens[r];
+  if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
+      q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q)
+    return 0;
+  return (q_len + PrefillCfg<64>::BM - 1) / PrefillCfg<64>::BM * a.num_heads;
+}
+
+// Reports the prefill rows prefill_tiles() rejects (done once, by CTA 0).
+__device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
+  for (int r = lane; r < a.num_seqs; r += 32) {
+    const int q0 = a.query_start_loc[r];
+    const int q_len = a.query_start_loc[r + 1] - q0;
+    if (q_len <= 1) continue;
+    const int seq_len = a.seq_lens[r];
+    if (q_len > seq_len || q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q)
+      record_error(a.status, PA_DEV_BAD_QUERY_LEN, r, q_len > seq_len ? q_len : seq_len);
+    else if (seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size)
+      record_error(a.status, PA_DEV_BAD_SEQ_LEN, r, seq_len);
+  }
+}
+
+// Persistent: CTA c takes tiles c, c + gridDim.x, ... of the batch's tile
+// list (requests in order; within a request the last query tile, which
+// sees the most keys, first; then the q heads).
 template <int D>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   using C = PrefillCfg<D>;
-  const int qt = blockIdx.x;
-  const int head = blockIdx.y;
-  const int r = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  const int q0 = a.query_start_loc[r];
-  const int q_len = a.query_start_loc[r + 1] - q0;
-  if (q_len <= 1 || qt * C::BM >= q_len) return;  // decode rows and empty tiles
-  const int seq_len = a.seq_lens[r];
-  if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
-      q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q) {
-    if (tid == 0 && qt == 0 && head == 0)
-      record_error(a.status, q_len > seq_len || q_len > a.max_query_len || q0 < 0 ||
-                                     q0 + q_len > a.total_q
-                                 ? PA_DEV_BAD_QUERY_LEN
-                                 : PA_DEV_BAD_SEQ_LEN,
-                   r, q_len > seq_len ? q_len : seq_len);
-    return;
-  }
-  const int ctx = seq_len - q_len;
-  const int row0 = qt * C::BM;                     // first query (within the request)
-  const int rows = min(C::BM, q_len - row0);       // valid query rows of this tile
-  const int kv_end = ctx + row0 + rows;            // keys [0, kv_end) are needed
-  const int n_tiles = (kv_end + C::BN - 1) / C::BN;
-  const int nblk_need = (kv_end + kBlockSize - 1) / kBlockSize;
-  const int kvh = head / a.group;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // swizzle atoms
@@ -139,22 +144,75 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [half][row]
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* tile_rec = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // r, local, found
 
-  if (tid == 0) {
-    for (int k = 0; k < kRed; ++k)
-      mbar_init(bar(k), (k == kPFull || k == kPFull + 1) ? C::SOFTMAX_WARPS : 1);
-    mbar_init(bar(kRed), C::SOFTMAX_WARPS);
-    *fail_flag = 0;
-    fence_mbar_init();
-  }
+  if (tid == 0) *fail_flag = 0;
   if (warp == 0) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (blockIdx.x == 0 && warp == 1) report_bad_prefill_rows(a, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int scan_r = 0;            // warp 0: first request not yet passed by the tile search
+  long long scan_base = 0;   // tiles of the requests before scan_r
+
+  for (long long tile = blockIdx.x;; tile += gridDim.x) {
+  // ---- locate the tile (warp 0) and set up this tile's barriers
+  if (warp == 0) {
+    int r_found = -1;
+    long long local = 0;
+    for (int rc = scan_r; rc < a.num_seqs && r_found < 0; rc += 32) {
+      const int rr = rc + lane;
+      const long long nt = rr < a.num_seqs ? prefill_tiles(a, rr) : 0;
+      long long incl = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, rr < a.num_seqs && scan_base + incl > tile);
+      if (hit) {
+        const int first = __ffs(hit) - 1;
+        const long long excl = __shfl_sync(0xffffffffu, incl - nt, first);
+        r_found = rc + first;
+        scan_base += excl;
+        scan_r = r_found;
+        local = tile - scan_base;
+      } else {
+        scan_base += __shfl_sync(0xffffffffu, incl, 31);
+        scan_r = rc + 32;
+      }
+    }
+    if (lane == 0) {
+      tile_rec[0] = r_found;
+      tile_rec[1] = static_cast<int>(local);
+      tile_rec[2] = r_found >= 0 ? 1 : 0;
+      for (int k = 0; k <= kRed; ++k) {
+        if (tile != blockIdx.x) mbar_inval(bar(k));
+        mbar_init(bar(k), (k == kPFull || k == kPFull + 1 || k == kRed) ? C::SOFTMAX_WARPS : 1);
+      }
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (!tile_rec[2]) break;
+  const int r = tile_rec[0];
+  const int q0 = a.query_start_loc[r];
+  const int q_len = a.query_start_loc[r + 1] - q0;
+  const int seq_len = a.seq_lens[r];
+  const int ntq = (q_len + C::BM - 1) / C::BM;
+  const int qt = ntq - 1 - tile_rec[1] / a.num_heads;
+  const int head = tile_rec[1] % a.num_heads;
+  const int ctx = seq_len - q_len;
+  const int row0 = qt * C::BM;                     // first query (within the request)
+  const int rows = min(C::BM, q_len - row0);       // valid query rows of this tile
+  const int kv_end = ctx + row0 + rows;            // keys [0, kv_end) are needed
+  const int n_tiles = (kv_end + C::BN - 1) / C::BN;
+  const int nblk_need = (kv_end + kBlockSize - 1) / kBlockSize;
+  const int kvh = head / a.group;
   auto give_up = [&](int where) {
     record_error(a.status, PA_DEV_WAIT_TIMEOUT, r, where);
     *fail_flag = 1;
@@ -409,12 +467,17 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     }
   }
 
-  __syncthreads();
-  if (*fail_flag && tid == 0) {
-    // Let copies and MMAs still in flight finish before TMEM is released
-    // and the CTA leaves (bounded; some of these phases may never come).
-    for (int k = 0; k < kRed; ++k) (void)mbar_wait(bar(k), 0);
+  __syncthreads();  // end of the tile: every copy and MMA of it has completed
+  if (*fail_flag) {
+    if (tid == 0) {
+      // Let copies and MMAs still in flight finish before TMEM is released
+      // and the CTA leaves (bounded; some of these phases may never come).
+      for (int k = 0; k < kRed; ++k) (void)mbar_wait(bar(k), 0);
+    }
+    break;
   }
+  }  // tiles
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -431,8 +494,7 @@ cudaError_t launch_prefill_impl(const PrefillArgs& a, const CUtensorMap& qmap,
   cudaError_t err = cudaFuncSetAttribute(prefill_tile_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  const dim3 grid((a.max_query_len + C::BM - 1) / C::BM, a.num_heads, a.num_seqs);
-  prefill_tile_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(qmap, kmap, vmap, a);
+  prefill_tile_kernel<D><<<a.num_ctas, C::THREADS, C::SMEM, stream>>>(qmap, kmap, vmap, a);
   return cudaGetLastError();
 }
 

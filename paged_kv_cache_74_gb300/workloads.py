@@ -200,12 +200,27 @@ def mixed_chunked_prefill() -> Workload:
                           head_dim=128, block_size=16, num_blocks=40000, seed=5, rng=rng)
 
 
+def multi_chunk_prefill() -> Workload:
+    """Four long query chunks (q_len, context) = (2048, 0), (1024, 3072),
+    (1536, 6656), (768, 12032) plus 28 single-token decode rows with K/V
+    lengths uniform in [256, 8192]; 32 q heads / 8 kv heads; d = 128;
+    12000-block pool.  1344 query tiles: several per SM."""
+    rng = np.random.default_rng(6)
+    chunks = [(2048, 0), (1024, 3072), (1536, 6656), (768, 12032)]
+    dec = rng.integers(256, 8192, size=28, endpoint=True)
+    lens = np.concatenate([[q + c for q, c in chunks], dec]).astype(np.int32)
+    qls = np.concatenate([[q for q, _ in chunks], np.ones(28, np.int64)]).astype(np.int32)
+    return build_workload("multi_chunk_prefill", lens, qls, num_heads=32, num_kv_heads=8,
+                          head_dim=128, block_size=16, num_blocks=12000, seed=6, rng=rng)
+
+
 NAMED = {
     "tiny_decode": tiny_decode,
     "llama8b_decode_b64": llama8b_decode,
     "long_ctx_decode_8x32k": long_context_decode,
     "prefix_shared_decode_b256": prefix_shared_decode,
     "mixed_chunked_prefill": mixed_chunked_prefill,
+    "multi_chunk_prefill": multi_chunk_prefill,
 }
 
 

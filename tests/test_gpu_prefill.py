@@ -241,3 +241,22 @@ def test_prefill_larger_blocks(cuda_lib, oracle, B, seed):
     ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
                                 w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
     assert_close_to_oracle(out, ref, what=f"prefill block {B}")
+
+
+def test_multi_chunk_prefill_full_size(cuda_lib, oracle):
+    """Four long chunks (1344 query tiles, several per CTA of the persistent
+    grid) plus decode rows; every decode row and a sample of each chunk's
+    rows against the oracle."""
+    pa = cuda_lib
+    w = wl.multi_chunk_prefill()
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    out, ws = run_prefill(pa, w, t)
+    assert pa.device_status(ws)[0] == 0
+    rows = {}
+    for r in range(w.num_seqs):
+        ql = int(w.q_lens[r])
+        rows[r] = sorted({0, 1, 127, 128, ql // 2, ql - 2, ql - 1}) if ql > 1 else [0]
+    ref = oracle_rows(oracle, w, t, rows)
+    flat = sorted(ref)
+    got = out[torch.tensor(flat, device="cuda")]
+    assert_close_to_oracle(got, np.stack([ref[k] for k in flat]), what="multi-chunk prefill")
