@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (full workload, from the committed ncu summary), valid only while
 # the kernel source is unchanged (sha256 of decode.cu at capture time).
 PROFILED_TRAFFIC: dict = {
-    # profiles/decode_llama8b_decode_b64.md: 636.355840 MB read + 4.298752 MB written
-    "llama8b_decode_b64": {"bytes": 640654592, "src_sha": "817d52796d0500f4"},
+    # profiles/decode_llama8b_decode_b64.md: 636.439808 MB read + 4.233984 MB written
+    "llama8b_decode_b64": {"bytes": 640673792, "src_sha": "8033d060cc1bf81d"},
 }
 
 
