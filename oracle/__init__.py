@@ -71,6 +71,14 @@ def _declare(lib):
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double]
+    lib.oracle_reshape_and_cache_xsplit.restype = None
+    lib.oracle_reshape_and_cache_xsplit.argtypes = [_U16, _U16, ctypes.c_int32, ctypes.c_int32,
+                                                    ctypes.c_int32, _U16, _U16, ctypes.c_int32,
+                                                    ctypes.c_int32, _I64]
+    lib.oracle_decode_xsplit.restype = ctypes.c_int
+    lib.oracle_decode_xsplit.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
     lib.oracle_map_to_kernel_blocks.restype = None
     lib.oracle_map_to_kernel_blocks.argtypes = [_I32, ctypes.c_int32, ctypes.c_int32, _I32]
     lib.oracle_decode.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
@@ -186,6 +194,35 @@ class Oracle:
                                         scale, k_scale, v_scale)
         if rc != 0:
             raise ValueError(f"oracle_decode_fp8 failed ({rc})")
+        return out
+
+    def reshape_and_cache_xsplit(self, key, value, key_cache, value_cache, slot_mapping):
+        """x-split caches: key [nb, hkv, d / 8, B, 8], value [nb, hkv, d, B] (bf16 bits).
+        Returns updated copies (inputs are not modified)."""
+        k, v = _u16(key), _u16(value)
+        kc, vc = _u16(key_cache).copy(), _u16(value_cache).copy()
+        sm = np.ascontiguousarray(slot_mapping, np.int64)
+        nb, hkv, dx, bs, x = kc.shape
+        d = dx * x
+        assert x == 8 and vc.shape == (nb, hkv, d, bs) and k.shape == (sm.shape[0], hkv, d)
+        self.lib.oracle_reshape_and_cache_xsplit(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv, d,
+                                                 _p(kc, _U16), _p(vc, _U16), nb, bs, _p(sm, _I64))
+        return kc, vc
+
+    def decode_xsplit(self, q, key_cache, value_cache, block_tables, seq_lens,
+                      scale) -> np.ndarray:
+        q, kc, vc = _u16(q), _u16(key_cache), _u16(value_cache)
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        s, hq, d = q.shape
+        nb, hkv, dx, bs, x = kc.shape
+        assert x == 8 and dx * x == d and vc.shape == (nb, hkv, d, bs)
+        out = np.zeros((s, hq, d), np.float64)
+        rc = self.lib.oracle_decode_xsplit(_p(out, _F64), _p(q, _U16), _p(kc, _U16),
+                                           _p(vc, _U16), _p(bt, _I32), bt.shape[1], _p(sl, _I32),
+                                           s, hq, hkv, d, bs, float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_decode_xsplit rejected its arguments ({rc})")
         return out
 
     def map_to_kernel_blocks(self, ids, k: int) -> np.ndarray:

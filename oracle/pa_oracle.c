@@ -15,7 +15,8 @@
  *   - "vLLM 深度解析（二）：PagedAttention 核心机制", section 2.1 (exact
  *     attention S = QK^T, P = softmax(S), O = PV), section 2.2 (online
  *     softmax state (m, l, A)), section 3.1 (logical block, offset,
- *     physical block, slot), section 3.2.4/3.2.8 (masking past seq_len,
+ *     physical block, slot), section 3.2.1 (the x-split K/V cache shapes),
+ *     section 3.2.4/3.2.8 (masking past seq_len,
  *     zeroed V of out-of-context slots), section 3.2.9 (cross-partition
  *     merge), section 5.2 (query_start_loc packing).
  *   - "分块预填充与混合批处理", section 11.6 (varlen batch: cu_seqlens_q =
@@ -360,6 +361,100 @@ int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
                     (((int64_t)table[t / block_size] * block_size + t % block_size) * num_kv_heads + kvh) * head_dim;
                 for (int32_t x = 0; x < head_dim; ++x)
                     o[x] += (w[t] / total) * (oracle_e4m3_decode(vr[x]) * v_scale);
+            }
+        }
+        free(w);
+    }
+    return 0;
+}
+
+/* ---- The x-split cache layout (page 1 section 3.2.1) --------------------
+ * K cache [num_blocks, num_kv_heads, head_dim / x, block_size, x] and
+ * V cache [num_blocks, num_kv_heads, head_dim, block_size], with x the
+ * number of cache elements in 16 bytes (8 for bf16).  Element d of kv head
+ * h of the token in slot s (block s / B, offset s % B) sits at
+ *   K: (((block * H + h) * (D / x) + d / x) * B + offset) * x + d % x
+ *   V: ((block * H + h) * D + d) * B + offset.                          */
+#define ORACLE_XSPLIT_X 8
+
+static int64_t xsplit_k_index(int64_t block, int64_t offset, int32_t h, int32_t d,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+    int64_t chunks = head_dim / ORACLE_XSPLIT_X;
+    return (((block * num_kv_heads + h) * chunks + d / ORACLE_XSPLIT_X) * block_size + offset)
+               * ORACLE_XSPLIT_X + d % ORACLE_XSPLIT_X;
+}
+
+static int64_t xsplit_v_index(int64_t block, int64_t offset, int32_t h, int32_t d,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+    return ((block * num_kv_heads + h) * head_dim + d) * block_size + offset;
+}
+
+/* reshape_and_cache into the x-split layout: the same tokens and slots as
+ * oracle_reshape_and_cache, each element stored at its x-split position. */
+void oracle_reshape_and_cache_xsplit(const uint16_t* key, const uint16_t* value,
+                                     int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                     uint16_t* key_cache, uint16_t* value_cache,
+                                     int32_t num_blocks, int32_t block_size,
+                                     const int64_t* slot_mapping) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+        int64_t block = slot / block_size;
+        int64_t in_block = slot % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t d = 0; d < head_dim; ++d) {
+                int64_t src = i * row + (int64_t)h * head_dim + d;
+                key_cache[xsplit_k_index(block, in_block, h, d, num_kv_heads, head_dim, block_size)] =
+                    key[src];
+                value_cache[xsplit_v_index(block, in_block, h, d, num_kv_heads, head_dim,
+                                           block_size)] = value[src];
+            }
+    }
+}
+
+/* Paged decode over x-split caches: exact attention (page 1 section 2.1)
+ * with key t of request r read from block block_tables[r][t / B], offset
+ * t % B, at the x-split positions above. */
+int oracle_decode_xsplit(double* out, const uint16_t* q, const uint16_t* key_cache,
+                         const uint16_t* value_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, double scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim % ORACLE_XSPLIT_X != 0)
+        return -1;
+    int32_t heads_per_kv = num_heads / num_kv_heads;
+    for (int32_t r = 0; r < num_seqs; ++r) {
+        int64_t n = seq_lens[r];
+        double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        if (!w) return -2;
+        const int32_t* table = block_tables + (int64_t)r * max_blocks_per_seq;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const uint16_t* qh = q + ((int64_t)r * num_heads + h) * head_dim;
+            int32_t kvh = h / heads_per_kv;
+            double top = -INFINITY;
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t block = table[t / block_size], offset = t % block_size;
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    acc += bf16_to_double(qh[d]) *
+                           bf16_to_double(key_cache[xsplit_k_index(block, offset, kvh, d,
+                                                                   num_kv_heads, head_dim,
+                                                                   block_size)]);
+                w[t] = scale * acc;
+                if (w[t] > top) top = w[t];
+            }
+            double total = 0.0;
+            for (int64_t t = 0; t < n; ++t) { w[t] = exp(w[t] - top); total += w[t]; }
+            double* o = out + ((int64_t)r * num_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t block = table[t / block_size], offset = t % block_size;
+                double p = w[t] / total;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] += p * bf16_to_double(value_cache[xsplit_v_index(block, offset, kvh, d,
+                                                                          num_kv_heads, head_dim,
+                                                                          block_size)]);
             }
         }
         free(w);

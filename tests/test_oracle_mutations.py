@@ -51,6 +51,13 @@ MUTATIONS = [
      ["e4m3_decode"]),
     ("fp8_decode_ignores_v_scale", "(oracle_e4m3_decode(vr[x]) * v_scale)", "(oracle_e4m3_decode(vr[x]))",
      ["fp8_decode"]),
+    ("xsplit_k_reverses_x", "* ORACLE_XSPLIT_X + d % ORACLE_XSPLIT_X;",
+     "* ORACLE_XSPLIT_X + (ORACLE_XSPLIT_X - 1 - d % ORACLE_XSPLIT_X);", ["xsplit_layout"]),
+    ("xsplit_v_reverses_offset", "* head_dim + d) * block_size + offset;",
+     "* head_dim + d) * block_size + (block_size - 1 - offset);", ["xsplit_layout"]),
+    ("xsplit_decode_drops_scale", "w[t] = scale * acc;", "w[t] = acc;", ["xsplit_decode"]),
+    ("xsplit_decode_unnormalised", "double p = w[t] / total;", "double p = w[t];",
+     ["xsplit_decode"]),
 ]
 
 PINS = {
@@ -70,6 +77,9 @@ PINS = {
     "online": lambda o: pins.test_online_softmax_equals_direct(o, "block16"),
     "merge": lambda o: pins.test_partition_merge_equals_global_softmax(o),
     "writer": lambda o: pins.test_reshape_and_cache_scatter(o),
+    "xsplit_layout": lambda o: pins.test_xsplit_writer_places_elements_at_the_pages_shape(o, 2, 64, 16),
+    "xsplit_decode": lambda o: pins.test_decode_xsplit_equals_decode_of_the_same_cache(
+        o, 4, 2, 64, [25, 12, 37, 20], 16),
 }
 
 

@@ -448,3 +448,83 @@ def test_reshape_and_cache_fp8_scatter(oracle):
         np.testing.assert_array_equal(flat(vn)[s], oracle.e4m3_encode(vf[i] / np.float32(0.125)))
     np.testing.assert_array_equal(flat(kn)[~touched], flat(kc8)[~touched])
     np.testing.assert_array_equal(flat(vn)[~touched], flat(vc8)[~touched])
+
+
+# ------------------------------------------------------ x-split cache layout
+
+def _to_xsplit(key_cache, value_cache):
+    """[nb, B, H, d] caches -> the x-split shapes of the pages (numpy's own
+    reshape and transpose: K [nb, H, d / 8, B, 8], V [nb, H, d, B])."""
+    nb, B, H, d = key_cache.shape
+    kx = np.ascontiguousarray(key_cache.reshape(nb, B, H, d // 8, 8).transpose(0, 2, 3, 1, 4))
+    vx = np.ascontiguousarray(value_cache.reshape(nb, B, H, d).transpose(0, 2, 3, 1))
+    return kx, vx
+
+
+@pytest.mark.parametrize("hkv,d,B", [(2, 64, 16), (8, 128, 32), (1, 128, 64)])
+def test_xsplit_writer_places_elements_at_the_pages_shape(oracle, hkv, d, B):
+    """Token i with slot s must appear at K[s // B, h, d // 8, s % B, d % 8]
+    and V[s // B, h, d, s % B] (x = 16 bytes / 2 bytes = 8); every other
+    element, and tokens with a negative slot, leave the pool untouched."""
+    nb, n = 6, 9
+    rng = np.random.default_rng(71 + B)
+    key = rng.integers(0, 1 << 16, size=(n, hkv, d), dtype=np.uint16)
+    val = rng.integers(0, 1 << 16, size=(n, hkv, d), dtype=np.uint16)
+    kx0 = rng.integers(0, 1 << 16, size=(nb, hkv, d // 8, B, 8), dtype=np.uint16)
+    vx0 = rng.integers(0, 1 << 16, size=(nb, hkv, d, B), dtype=np.uint16)
+    slots = rng.choice(nb * B, size=n, replace=False).astype(np.int64)
+    slots[4] = -1
+    kx, vx = oracle.reshape_and_cache_xsplit(key, val, kx0, vx0, slots)
+    k_seen, v_seen = kx0.copy(), vx0.copy()
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        blk, off = divmod(int(s), B)
+        for h in range(hkv):
+            for e in range(d):
+                assert kx[blk, h, e // 8, off, e % 8] == key[i, h, e]
+                assert vx[blk, h, e, off] == val[i, h, e]
+        k_seen[blk, :, :, off, :] = kx[blk, :, :, off, :]
+        v_seen[blk, :, :, off] = vx[blk, :, :, off]
+    np.testing.assert_array_equal(kx, k_seen)
+    np.testing.assert_array_equal(vx, v_seen)
+
+
+def test_xsplit_writer_is_a_permutation_of_the_token_major_writer(oracle):
+    """The same tokens written by both writers give caches that numpy's
+    reshape + transpose carries into one another."""
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w)
+    n = 12
+    gen = torch.Generator().manual_seed(72)
+    key = torch.randn((n, 2, 64), generator=gen).to(torch.bfloat16).view(torch.int16).numpy()
+    val = torch.randn((n, 2, 64), generator=gen).to(torch.bfloat16).view(torch.int16).numpy()
+    slots = np.random.default_rng(72).choice(w.num_blocks * 16, size=n, replace=False)
+    kc0 = t.key_cache.view(torch.int16).numpy()
+    vc0 = t.value_cache.view(torch.int16).numpy()
+    kn, vn = oracle.reshape_and_cache(key, val, kc0, vc0, slots.astype(np.int64))
+    kx0, vx0 = _to_xsplit(kc0.view(np.uint16), vc0.view(np.uint16))
+    kx, vx = oracle.reshape_and_cache_xsplit(key, val, kx0, vx0, slots.astype(np.int64))
+    kref, vref = _to_xsplit(kn, vn)
+    np.testing.assert_array_equal(kx, kref)
+    np.testing.assert_array_equal(vx, vref)
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens,B", [(4, 2, 64, [25, 12, 37, 20], 16),
+                                             (8, 2, 128, [1, 31, 64, 70], 32),
+                                             (16, 2, 128, [129, 33], 64)])
+def test_decode_xsplit_equals_decode_of_the_same_cache(oracle, hq, hkv, d, lens, B):
+    """Decoding the x-split form of a cache must give exactly the (pinned)
+    decode of the token-major form: same keys, same arithmetic."""
+    w, _ = _contiguous_workload(lens, hq, hkv, d, seed=73, B=B)
+    need = -(-np.asarray(lens) // B)
+    for r, n in enumerate(need):  # blocks in reverse order: table lookups matter
+        w.block_tables[r, :n] = w.block_tables[r, :n][::-1].copy()
+    t = wl.make_tensors(w)
+    kc = t.key_cache.view(torch.int16).numpy().view(np.uint16)
+    vc = t.value_cache.view(torch.int16).numpy().view(np.uint16)
+    q = t.q.view(torch.int16).numpy()
+    ref = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    kx, vx = _to_xsplit(kc, vc)
+    got = oracle.decode_xsplit(q, kx, vx, w.block_tables, w.seq_lens, w.scale)
+    np.testing.assert_array_equal(got, ref)
