@@ -38,17 +38,21 @@ FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_decode_kernel
 # launch (full workload, from the committed ncu summary), valid only while
-# the kernel source is unchanged (sha256 of decode.cu at capture time).
+# the kernel source is unchanged (sha256 of its .cu file at capture time).
 PROFILED_TRAFFIC: dict = {
     # profiles/decode_llama8b_decode_b64.md: 636.439808 MB read + 4.233984 MB written
-    "llama8b_decode_b64": {"bytes": 640673792, "src_sha": "8033d060cc1bf81d"},
+    "llama8b_decode_b64": {"bytes": 640673792, "src": "decode.cu",
+                           "src_sha": "8033d060cc1bf81d"},
+    # profiles/decode_tc_prefix_shared_decode_b256.md: 940.244224 MB read + 5.690112 MB written
+    "prefix_shared_decode_b256": {"bytes": 945934336, "src": "decode_tc.cu",
+                                  "src_sha": "1f68982a15d0aa46"},
 }
 
 
 # ----------------------------------------------------------------- helpers
 
-def decode_src_sha() -> str:
-    p = os.path.join(ROOT, "paged_kv_cache_74_gb300", "csrc", "decode.cu")
+def decode_src_sha(src: str = "decode.cu") -> str:
+    p = os.path.join(ROOT, "paged_kv_cache_74_gb300", "csrc", src)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
@@ -241,7 +245,8 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peaks()
     achieved = ab["decode_bytes"] / dec_avg_s / 1e9
     prof = PROFILED_TRAFFIC.get(w.name)
-    traffic = prof["bytes"] if prof and prof.get("src_sha") == decode_src_sha() else None
+    traffic = (prof["bytes"] if prof and prof.get("src_sha") == decode_src_sha(prof["src"])
+               else None)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(tot_s / K * 1e3, 5),
@@ -257,7 +262,10 @@ def run_ours(args, world, rank, local):
         "us_per_call": round(dec_avg_s * 1e6, 2),
         "decode_kv_gbs": round(ab["kv_bytes"] / dec_avg_s / 1e9, 2),
         "wall_ms_per_step": round(wall / K * 1e3, 4),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (pa_decode)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_decode_tc_kernel (pa_decode)"
+                                if w.num_heads // w.num_kv_heads > 4
+                                else "paged_decode_kernel (pa_decode)"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": ab["decode_bytes"]},
