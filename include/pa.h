@@ -265,10 +265,6 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
                             void* stream);
 
 /*
- * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs
- * (status record, decode-row partials).  Returns 0 for invalid arguments.
- */
-/*
  * pa_decode_fp8 -- pa_decode over an FP8 (e4m3) cache written by
  * pa_reshape_and_cache_fp8: key t contributes decoded(K_t) * k_scale and
  * value t decoded(V_t) * v_scale ("vLLM 深度解析（二）", section 3.2,
@@ -285,6 +281,50 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const v
                         float v_scale, int32_t partition_tokens, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/*
+ * The x-split cache layout ("vLLM 深度解析（二）", section 3.2.1: the
+ * layout of the pages' own CUDA-core decode kernel), for drop-in use of
+ * caches laid out that way:
+ *   key_cache    [num_blocks, num_kv_heads, head_dim / 8, block_size, 8] bf16
+ *                (x = 16 bytes / 2 = 8 consecutive head_dim elements
+ *                innermost)
+ *   value_cache  [num_blocks, num_kv_heads, head_dim, block_size] bf16
+ * Element d of kv head h of the token in slot s = b * block_size + o sits
+ * at key_cache[b][h][d / 8][o][d % 8] and value_cache[b][h][d][o].
+ * Only the two calls below read or write this layout; pa_prefill_varlen
+ * and the FP8 calls take the token-major layout.
+ *
+ * pa_reshape_and_cache_xsplit -- pa_reshape_and_cache into x-split caches.
+ * Same arguments, slots, errors and bit-exactness; head_dim a multiple of 8.
+ */
+pa_status pa_reshape_and_cache_xsplit(const void* key, const void* value,
+                                      int64_t key_stride, int64_t value_stride,
+                                      void* key_cache, void* value_cache,
+                                      const int64_t* slot_mapping, int32_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks,
+                                      int32_t* device_status, void* stream);
+
+/*
+ * pa_decode_xsplit -- pa_decode over x-split caches.  Same arguments,
+ * workspace (pa_decode_workspace_size covers both layouts), sizes (head_dim
+ * 64 or 128, block_size 16, 32 or 64, 1 to 16 q heads per kv head) and
+ * errors as pa_decode.  Always on CUDA cores with fp32 weights: groups of
+ * more than 4 q heads are cut into work units of at most 4 (the largest
+ * divisor of the group not above 4), each reading its kv head's K/V.
+ */
+pa_status pa_decode_xsplit(void* out, const void* q, const void* key_cache,
+                           const void* value_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int32_t num_blocks, float scale, int32_t partition_tokens,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs
+ * (status record, decode-row partials).  Returns 0 for invalid arguments.
+ */
 size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len);
 

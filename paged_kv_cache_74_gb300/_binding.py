@@ -25,7 +25,8 @@ DEVICE_ERRORS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "bad seq_len",
 ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
                "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
-               "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8")
+               "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+               "pa_reshape_and_cache_xsplit", "pa_decode_xsplit")
 
 
 class PAError(RuntimeError):
@@ -54,6 +55,12 @@ def _declare(lib):
     lib.pa_decode_fp8.restype = ctypes.c_int
     lib.pa_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _i32, _f32, _f32, _f32, _i32, _vp, _sz, _vp]
+    lib.pa_reshape_and_cache_xsplit.restype = ctypes.c_int
+    lib.pa_reshape_and_cache_xsplit.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _i32,
+                                                _i32, _i32, _i32, _vp, _vp]
+    lib.pa_decode_xsplit.restype = ctypes.c_int
+    lib.pa_decode_xsplit.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                     _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp]
     lib.pa_map_to_kernel_blocks.restype = ctypes.c_int
     lib.pa_map_to_kernel_blocks.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp]
     lib.pa_decode_workspace_size.restype = _sz
@@ -158,6 +165,37 @@ def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_sc
         _ptr(status), _stream()))
 
 
+def _xsplit_shape(key_cache, value_cache):
+    """(num_blocks, block_size, num_kv_heads, head_dim) of x-split caches:
+    key [nb, Hkv, d / 8, bs, 8], value [nb, Hkv, d, bs]."""
+    if key_cache.dim() != 5 or key_cache.shape[4] != 8:
+        raise ValueError("x-split key_cache must be [num_blocks, kv_heads, head_dim / 8, block, 8]")
+    nb, hkv, dx, bs, _ = key_cache.shape
+    d = dx * 8
+    if tuple(value_cache.shape) != (nb, hkv, d, bs):
+        raise ValueError("x-split value_cache must be [num_blocks, kv_heads, head_dim, block]")
+    return nb, bs, hkv, d
+
+
+def reshape_and_cache_xsplit(key, value, key_cache, value_cache, slot_mapping, status=None):
+    """reshape_and_cache into x-split caches (key [nb, Hkv, d / 8, bs, 8],
+    value [nb, Hkv, d, bs], bf16)."""
+    _cuda("key", key, torch.bfloat16)
+    _cuda("value", value, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("slot_mapping", slot_mapping, torch.int64)
+    nb, bs, hkv, d = _xsplit_shape(key_cache, value_cache)
+    T = slot_mapping.shape[0]
+    for name, t in (("key", key), ("value", value)):
+        if tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, {hkv}, {d}] with contiguous heads")
+    lib = load_library()
+    _check("pa_reshape_and_cache_xsplit", lib.pa_reshape_and_cache_xsplit(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache),
+        _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, _ptr(status), _stream()))
+
+
 def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, num_blocks,
                          total_tokens, out=None, status=None):
     _contig("block_tables", block_tables, torch.int32)
@@ -248,6 +286,32 @@ def decode_fp8(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, s
         block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
         float(scale), float(k_scale), float(v_scale), int(partition_tokens), _ptr(workspace),
         workspace.numel(), _stream()))
+    return out
+
+
+def decode_xsplit(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale,
+                  out=None, workspace=None, partition_tokens=0):
+    """Paged decode over x-split caches (see reshape_and_cache_xsplit)."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    S, hq, d = q.shape
+    nb, bs, hkv, d2 = _xsplit_shape(key_cache, value_cache)
+    if d2 != d:
+        raise ValueError("cache shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(S, hq, hkv, d, max_seq_len, partition_tokens),
+                                  q.device)
+    lib = load_library()
+    _check("pa_decode_xsplit", lib.pa_decode_xsplit(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
+        float(scale), int(partition_tokens), _ptr(workspace), workspace.numel(), _stream()))
     return out
 
 

@@ -8,7 +8,8 @@
 //    seq_lens counts this step's tokens);
 //  * reshape_and_cache ("vllm 深度解析：一切从 PagedAttention 谈起",
 //    write_to_paged_cache): token i's [kv_heads, head_dim] K and V rows are
-//    copied to slot slot_mapping[i] of the [slots, kv_heads, head_dim] cache.
+//    copied to slot slot_mapping[i] of the [slots, kv_heads, head_dim] cache
+//    (also: an e4m3-quantizing variant, and one for the x-split layout).
 //
 // Both are pure data movement.  The cache write gives each token one warp;
 // lanes move 16-byte chunks, so each token's K and V rows (2 KB each at 8 kv
@@ -103,6 +104,50 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
   }
 }
 
+// The cache write into the x-split layout ("vLLM 深度解析（二）：PagedAttention
+// 核心机制", section 3.2.1): chunk c (8 bf16 = 16 bytes) of kv head h of the
+// token in slot s goes to K[s / B][h][c][s % B][0..7]; V element d to
+// V[s / B][h][d][s % B].  One warp per token, lanes over 16-byte chunks: the
+// K chunks are 16-byte stores, the V elements land B elements apart.
+__global__ void __launch_bounds__(kWriteWarps * 32)
+reshape_and_cache_xsplit_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                int64_t key_stride_chunks, int64_t value_stride_chunks,
+                                uint4* __restrict__ key_cache, uint16_t* __restrict__ value_cache,
+                                const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                int num_kv_heads, int head_dim, int block_size, int64_t num_slots,
+                                int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();  // slot_mapping may come from the previous kernel
+  const int token = blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (token >= num_tokens) return;
+  const int64_t slot = slot_mapping[token];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (lane == 0) record_error(status, PA_DEV_BAD_SLOT, token, static_cast<int>(slot));
+    return;
+  }
+  const int64_t blk = slot / block_size;
+  const int off = static_cast<int>(slot % block_size);
+  const int cpr = head_dim / 8;  // 16-byte chunks per kv head
+  const uint4* ks = key + token * key_stride_chunks;
+  const uint4* vs = value + token * value_stride_chunks;
+  for (int c = lane; c < num_kv_heads * cpr; c += 32) {
+    const int h = c / cpr, cc = c % cpr;
+    const int64_t head_base = blk * num_kv_heads + h;
+    const uint4 kv = __ldg(ks + c);
+    const uint4 vv = __ldg(vs + c);
+    key_cache[(head_base * cpr + cc) * block_size + off] = kv;
+    uint16_t* vd = value_cache + (head_base * head_dim + cc * 8) * block_size + off;
+    const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      vd[(2 * e) * block_size] = static_cast<uint16_t>(w[e] & 0xffffu);
+      vd[(2 * e + 1) * block_size] = static_cast<uint16_t>(w[e] >> 16);
+    }
+  }
+}
+
 // One CTA per request; its threads cover the request's new tokens.
 __global__ void __launch_bounds__(128)
 slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
@@ -190,6 +235,20 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
                            key_stride / 8, value_stride / 8, static_cast<uint2*>(key_cache),
                            static_cast<uint2*>(value_cache), slot_mapping, num_tokens,
                            row_elems / 8, num_slots, k_scale, v_scale, status);
+}
+
+cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, int64_t key_stride,
+                                            int64_t value_stride, void* key_cache,
+                                            void* value_cache, const int64_t* slot_mapping,
+                                            int num_tokens, int num_kv_heads, int head_dim,
+                                            int block_size, int64_t num_slots, int32_t* status,
+                                            cudaStream_t stream) {
+  const int grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
+  return launch_overlapped(reshape_and_cache_xsplit_kernel, dim3(grid), dim3(kWriteWarps * 32), 0,
+                           stream, static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                           key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
+                           static_cast<uint16_t*>(value_cache), slot_mapping, num_tokens,
+                           num_kv_heads, head_dim, block_size, num_slots, status);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,

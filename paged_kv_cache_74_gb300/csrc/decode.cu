@@ -55,7 +55,7 @@ constexpr int kLastRow = 2;  // the segment ends after this row of stages
 constexpr int kDone = 4;     // no more work for the warp that receives it
 
 
-template <int D, int GMAX, bool KV8 = false>
+template <int D, int GMAX, bool KV8 = false, bool XS = false>
 struct DecodeCfg {
   static constexpr int T = (D == 128 && GMAX >= 4) ? 16 : 8;  // lanes per token
   static constexpr int NG = 32 / T;                            // token groups per warp
@@ -104,6 +104,9 @@ struct DecodeCfg {
   static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V >= 4 && V <= 32, "decode shape");
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
+  // The x-split layout re-lays V out in the K stage after the q.k products
+  // (see the consumer), so the K stage must be free by then.
+  static_assert(!XS || (!KV8 && XPOSE_IN_K && NSB == 1), "x-split decode shape");
 };
 
 // What the producer tells the consumers about a segment: the run of blocks
@@ -151,11 +154,60 @@ struct Row8<true> {
   }
 };
 
-template <int D, int GMAX, bool KV8>
-__global__ void __launch_bounds__(DecodeCfg<D, GMAX, KV8>::THREADS, DecodeCfg<D, GMAX, KV8>::MINB)
+// ---- x-split layout ("vLLM 深度解析（二）：PagedAttention 核心机制", section
+// 3.2.1): K [blocks, kv heads, head_dim / 8, block, 8] (8 bf16 = 16 bytes
+// innermost), V [blocks, kv heads, head_dim, block].
+//
+// A K stage holds one 16-token tile as [head_dim / 8 chunks][2 token groups]
+// [8 tokens x 16 bytes]: 128-byte rows r = 2 c + t / 8, the 16-byte unit of
+// token t at (t % 8) ^ (r % 8) (the copy's 128-byte swizzle).  Lanes reading
+// chunk c of one token then hit distinct bank groups.
+__device__ __forceinline__ uint32_t xs_k_offset(int t, int c) {
+  const int r = 2 * c + (t >> 3);
+  return static_cast<uint32_t>(r * 128 + (((t & 7) ^ (r & 7)) * 16));
+}
+
+// Token rows [16][head_dim] bf16 with the 16-byte unit c of row t stored at
+// c ^ (t % 8): V re-laid out by xs_transpose_v, read like a token-major tile.
+template <int D>
+__device__ __forceinline__ uint32_t xs_row_offset(int t, int c) {
+  return static_cast<uint32_t>(t * (D * 2) + ((c ^ (t & 7)) * 16));
+}
+
+// V stage [head_dim][16 tokens] (32-byte rows, 16-byte halves swapped on
+// rows with bit 2 set: the copy's 32-byte swizzle) -> token rows at `dst`.
+// The tile is cut into 8 x 8 matrices (8 head_dim rows x 8 tokens);
+// ldmatrix.trans hands each lane a pair of consecutive head_dim values of
+// one token and stmatrix writes the pairs back as token rows.  Four
+// matrices per instruction, all 32 lanes (warp-collective).
+template <int D>
+__device__ __forceinline__ void xs_transpose_v(uint32_t src, uint32_t dst, int lane) {
+  constexpr int kGroups = D / 8 * 2 / 4;
+  const int rr = lane & 7;
+#pragma unroll
+  for (int q4 = 0; q4 < kGroups; ++q4) {
+    const int mi = 4 * q4 + (lane >> 3);  // this lane addresses row rr of matrix mi
+    const int db = mi >> 1, tb = mi & 1;  // head_dim block, token block
+    const int d = 8 * db + rr;
+    const uint32_t from = src + d * 32 + ((tb ^ ((d >> 2) & 1)) * 16);
+    uint32_t f0, f1, f2, f3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(f0), "=r"(f1), "=r"(f2), "=r"(f3)
+                 : "r"(from)
+                 : "memory");
+    const uint32_t to = dst + xs_row_offset<D>(8 * tb + rr, db);
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(to),
+                 "r"(f0), "r"(f1), "r"(f2), "r"(f3)
+                 : "memory");
+  }
+}
+
+template <int D, int GMAX, bool KV8, bool XS>
+__global__ void __launch_bounds__(DecodeCfg<D, GMAX, KV8, XS>::THREADS,
+                                  DecodeCfg<D, GMAX, KV8, XS>::MINB)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using C = DecodeCfg<D, GMAX, KV8>;
+  using C = DecodeCfg<D, GMAX, KV8, XS>;
   const int cta = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -174,9 +226,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t csync_bar = qempty0 + 16;  // consumer-warp barrier (bounded waits)
   const uint32_t qbuf_s = smem_u32(smem + C::OFF_Q);
 
-  // TMA destinations must be 128-byte aligned; the dynamic shared-memory base
-  // always is on this GPU, but never issue a copy if it were not.
-  if (ring_s & 127) {
+  // TMA destinations must be 128-byte aligned (1024 for the 128-byte
+  // swizzle of the x-split K boxes); the dynamic shared-memory base always
+  // is on this GPU, but never issue a copy if it were not.
+  if (ring_s & (XS ? 1023 : 127)) {
     griddep_wait();
     if (threadIdx.x == 0) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 6);
     return;
@@ -354,14 +407,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             meta[s] = make_int2(b + j, flags);
             const uint32_t full = full0 + 8 * s;
             if (real) {
-              int row0 = tile_row(a, phys, b + j);
-              if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
-                record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys);
-                row0 = a.num_blocks * a.block_size;  // wholly out of bounds: TMA fills zeros
-              }
+              const bool bad = static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks);
+              if (bad) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, phys);
               mbar_arrive_expect_tx(full, 2 * C::TILE);
-              tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
-              tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+              if constexpr (XS) {
+                // Block coordinate num_blocks is wholly out of bounds: TMA fills zeros.
+                const int blk = bad ? a.num_blocks : phys;
+                const int sub = (b + j) & ((1 << a.tile_shift) - 1);  // 16-token tile of the block
+                const int kvc = kvh / a.kv_div;                        // kv head of the cache
+                tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 2 * sub, 0, kvc, blk, policy);
+                tma_load_4d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 16 * sub, 0, kvc, blk,
+                            policy);
+              } else {
+                // Row num_blocks * block_size is wholly out of bounds: TMA fills zeros.
+                const int row0 = bad ? a.num_blocks * a.block_size : tile_row(a, phys, b + j);
+                tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
+                tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+              }
             } else {
               mbar_arrive(full);
             }
@@ -519,7 +581,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           const int t = (sb * C::SB + kk) * C::NG + g;
           Row8<KV8> kw[C::CPL];
 #pragma unroll
-          for (int j = 0; j < C::CPL; ++j) kw[j].load(kt + (t * D + (li + C::T * j) * 8) * C::ELT);
+          for (int j = 0; j < C::CPL; ++j)
+            kw[j].load(kt + (XS ? xs_k_offset(t, li + C::T * j) : (t * D + (li + C::T * j) * 8) * C::ELT));
           float2 kf[C::CPL][4];
 #pragma unroll
           for (int j = 0; j < C::CPL; ++j)
@@ -616,6 +679,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           p[v + 2] = f.z;
           p[v + 3] = f.w;
         }
+        if constexpr (XS) {
+          // V arrived as V^T [head_dim][16 tokens]; turn it into token rows
+          // in the K stage (free now: the last transpose reads are behind
+          // the __syncwarp above), where the loop below reads it.
+          xs_transpose_v<D>(vt, kt, lane);
+          __syncwarp();
+        }
         // A += p v over this sub-batch's tokens.  In the last block of a
         // request the V rows past seq_len may hold NaN and are replaced by 0.
         auto pv = [&](bool check) {
@@ -624,7 +694,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             const int t = (sb * C::SB + kk) * C::NG + g;
             Row8<KV8> vw[C::CPL];
 #pragma unroll
-            for (int j = 0; j < C::CPL; ++j) vw[j].load(vt + (t * D + (li + C::T * j) * 8) * C::ELT);
+            for (int j = 0; j < C::CPL; ++j)
+              vw[j].load(XS ? kt + xs_row_offset<D>(t, li + C::T * j)
+                            : vt + (t * D + (li + C::T * j) * 8) * C::ELT);
             if (check && tok0 + t >= seq_len) {
 #pragma unroll
               for (int j = 0; j < C::CPL; ++j) vw[j].clear();
@@ -763,19 +835,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-template <int D, int GMAX, bool KV8>
+template <int D, int GMAX, bool KV8, bool XS>
 cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t stream) {
-  using C = DecodeCfg<D, GMAX, KV8>;
-  cudaError_t err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX, KV8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  using C = DecodeCfg<D, GMAX, KV8, XS>;
+  auto* kernel = paged_decode_kernel<D, GMAX, KV8, XS>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(paged_decode_kernel<D, GMAX, KV8>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (err != cudaSuccess) return err;
-  return launch_overlapped(paged_decode_kernel<D, GMAX, KV8>, dim3(a.num_ctas), dim3(C::THREADS),
-                           C::SMEM, stream, kmap, vmap, a);
+  return launch_overlapped(kernel, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM, stream, kmap,
+                           vmap, a);
 }
 
 }  // namespace
@@ -798,12 +870,14 @@ int decode_ctas_per_sm(int head_dim, int group) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          int head_dim, bool kv8, cudaStream_t stream) {
+                          int head_dim, bool kv8, bool xsplit, cudaStream_t stream) {
   const int gmax = decode_gmax(a.group);
+  if (kv8 && xsplit) return cudaErrorInvalidValue;
 #define PA_DECODE_CASE(DD, GG)                                                      \
   if (head_dim == DD && gmax == GG)                                                 \
-    return kv8 ? launch_decode_impl<DD, GG, true>(a, kmap, vmap, stream)            \
-               : launch_decode_impl<DD, GG, false>(a, kmap, vmap, stream);
+    return kv8      ? launch_decode_impl<DD, GG, true, false>(a, kmap, vmap, stream) \
+           : xsplit ? launch_decode_impl<DD, GG, false, true>(a, kmap, vmap, stream) \
+                    : launch_decode_impl<DD, GG, false, false>(a, kmap, vmap, stream);
   PA_DECODE_CASE(128, 1) PA_DECODE_CASE(128, 2) PA_DECODE_CASE(128, 4)
   PA_DECODE_CASE(64, 1) PA_DECODE_CASE(64, 2) PA_DECODE_CASE(64, 4)
 #undef PA_DECODE_CASE

@@ -159,6 +159,62 @@ bool make_kv_group_map(CUtensorMap* map, const void* cache, int num_blocks, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The x-split K cache [blocks, kv heads, head_dim / 8, block, 8] as a 5-D
+// tensor {64, block / 8, head_dim / 8, kv heads, blocks} (8 tokens x 8
+// elements, token group, 16-byte chunk, kv head, block) with a box of
+// {64, 2, head_dim / 8, 1, 1}: one 16-token tile per copy, 128-byte rows,
+// 128-byte swizzled.
+bool make_xsplit_k_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                       int head_dim, int block_size) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t head = static_cast<cuuint64_t>(head_dim) * block_size * 2;  // bytes
+  const cuuint64_t dims[5] = {64u, static_cast<cuuint64_t>(block_size / 8),
+                              static_cast<cuuint64_t>(head_dim / 8),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {128u, static_cast<cuuint64_t>(block_size) * 16, head,
+                                 head * num_kv_heads};
+  const cuuint32_t box[5] = {64u, 2u, static_cast<cuuint32_t>(head_dim / 8), 1u, 1u};
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The x-split V cache [blocks, kv heads, head_dim, block] as a 4-D tensor
+// {block, head_dim, kv heads, blocks} with a box of {16, head_dim, 1, 1}:
+// one 16-token tile per copy as [head_dim][16 tokens], 32-byte swizzled.
+bool make_xsplit_v_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                       int head_dim, int block_size) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(block_size) * 2;  // bytes per head_dim row
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(head_dim),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {row, row * head_dim, row * head_dim * num_kv_heads};
+  const cuuint32_t box[4] = {16u, static_cast<cuuint32_t>(head_dim), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Work units per request of the x-split decode: the CUDA-core kernel serves
+// up to 4 q heads per unit, so a group of g q heads is cut into g / g'
+// units of g' heads (g' the largest divisor of g not above 4), each reading
+// its kv head's tiles (the units of one kv head are neighbours in the tile
+// order, so the repeated reads mostly hit L2).
+int xsplit_heads_per_unit(int group) {
+  for (int g = 4; g > 1; --g)
+    if (group % g == 0) return g;
+  return 1;
+}
+
 struct DecodeLayout {
   int64_t num_ctas = 0;
   size_t counters_offset = 0, ml_offset = 0, o_offset = 0, total = 0;
@@ -256,9 +312,10 @@ pa_status check_decode_args(const void* out, const void* q, const void* key_cach
   return PA_OK;
 }
 
-// Element type of the K/V cache and its scales.
+// Element type and layout of the K/V cache, and its scales.
 struct KvFormat {
   bool e4m3 = false;
+  bool xsplit = false;  // K [blocks, kv heads, d / 8, block, 8], V [blocks, kv heads, d, block]
   float k_scale = 1.f, v_scale = 1.f;
 };
 
@@ -272,9 +329,17 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
                              const KvFormat& kv = KvFormat()) {
   // The TMA views address the cache in 16-token tiles.
   const int num_tiles16 = num_blocks * (block_size / kBlockSize);
-  const bool tc = decode_uses_tc(head_dim, num_heads / num_kv_heads);
+  const int group = num_heads / num_kv_heads;
+  const bool tc = !kv.xsplit && decode_uses_tc(head_dim, group);
+  // x-split: units of up to 4 q heads (see xsplit_heads_per_unit).
+  const int unit_heads = kv.xsplit ? xsplit_heads_per_unit(group) : group;
+  const int kv_div = group / unit_heads;
   CUtensorMap kmap, vmap, qmap;
-  if (tc) {
+  if (kv.xsplit) {
+    if (!make_xsplit_k_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim, block_size) ||
+        !make_xsplit_v_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim, block_size))
+      return PA_ERR_CUDA;
+  } else if (tc) {
     if (!make_q_group_map(&qmap, q, total_q, num_heads, head_dim, num_heads / num_kv_heads) ||
         !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
@@ -297,8 +362,9 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_seqs = num_seqs;
   a.num_heads = num_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.group = num_heads / num_kv_heads;
+  a.num_kv_heads = num_kv_heads * kv_div;
+  a.group = unit_heads;
+  a.kv_div = kv_div;
   a.num_ctas = static_cast<int>(L.num_ctas);
   a.max_seq_len = max_seq_len;
   a.num_blocks = num_blocks;
@@ -310,7 +376,7 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.v_scale = kv.v_scale;
   if (tc && kv.e4m3) return PA_ERR_UNSUPPORTED;
   const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, stream)
-                            : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, stream);
+                            : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, kv.xsplit, stream);
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -428,8 +494,14 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
       num_heads % num_kv_heads != 0 || (head_dim != 64 && head_dim != 128))
     return 0;
   if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return 0;
-  return decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
-      .total;
+  // Enough for either layout: the x-split decode may cut a kv head's q heads
+  // into several work units (more pair counters, smaller partials).
+  const int units = num_kv_heads * (num_heads / num_kv_heads /
+                                    xsplit_heads_per_unit(num_heads / num_kv_heads));
+  return std::max(
+      decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
+          .total,
+      decode_layout(num_seqs, num_heads, units, head_dim, max_seq_len, partition_tokens).total);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
@@ -481,6 +553,59 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const v
   kv.e4m3 = true;
   kv.k_scale = k_scale;
   kv.v_scale = v_scale;
+  return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,
+                            static_cast<cudaStream_t>(stream), kv);
+}
+
+pa_status pa_reshape_and_cache_xsplit(const void* key, const void* value, int64_t key_stride,
+                                      int64_t value_stride, void* key_cache, void* value_cache,
+                                      const int64_t* slot_mapping, int32_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int32_t num_blocks, int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1 || block_size < 1) return PA_ERR_INVALID;
+  if (head_dim < 8 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(slot_mapping, 8) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+    return PA_ERR_INVALID;
+  const cudaError_t e = launch_reshape_and_cache_xsplit(
+      key, value, key_stride, value_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      num_kv_heads, head_dim, block_size, static_cast<int64_t>(num_blocks) * block_size,
+      device_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_xsplit(void* out, const void* q, const void* key_cache, const void* value_cache,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                           int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale,
+                           int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale);
+  if (st != PA_OK) return st;
+  if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  const int group = num_heads / num_kv_heads;
+  const int units = num_kv_heads * (group / xsplit_heads_per_unit(group));
+  if (units > 65535) return PA_ERR_UNSUPPORTED;
+  const DecodeLayout L =
+      decode_layout(num_seqs, num_heads, units, head_dim, max_seq_len, partition_tokens);
+  if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  KvFormat kv;
+  kv.xsplit = true;
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
                             num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,

@@ -38,8 +38,9 @@ struct DecodeArgs {
   int max_blocks_per_seq;
   int num_seqs;
   int num_heads;
-  int num_kv_heads;
-  int group;                        // num_heads / num_kv_heads
+  int num_kv_heads;                 // work units per request (see kv_div)
+  int group;                        // q heads per unit: num_heads / num_kv_heads
+  int kv_div;                       // units per cache kv head: unit u reads kv head u / kv_div
   int num_ctas;
   int max_seq_len;
   int num_blocks;
@@ -74,9 +75,14 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Launchers (decode.cu).  Return a cudaError_t from the launch.
 // kv8: the caches hold e4m3 values (their scales folded into scale_log2
-// and v_scale) instead of bf16.
+// and v_scale) instead of bf16.  xsplit: bf16 caches in the x-split layout,
+// K [blocks, kv heads, head_dim / 8, block, 8] seen through a 5-D map
+// {64, block / 8, head_dim / 8, kv heads, blocks} with box {64, 2, head_dim
+// / 8, 1, 1}, 128-byte swizzled, and V [blocks, kv heads, head_dim, block]
+// through a 4-D map {block, head_dim, kv heads, blocks} with box {16,
+// head_dim, 1, 1}, 32-byte swizzled.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          int head_dim, bool kv8, cudaStream_t stream);
+                          int head_dim, bool kv8, bool xsplit, cudaStream_t stream);
 // Tensor-core decode (decode_tc.cu): qmap = q as {head_dim, heads, rows}
 // with a {64, group, 1} box; kmap, vmap = the caches as {64, 8, head_dim /
 // 64, slots / 8, kv heads} with a {64, 8, head_dim / 64, 2, 1} box (one
@@ -127,6 +133,14 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
                                          const int64_t* slot_mapping, int num_tokens, int row_elems,
                                          int64_t num_slots, float k_scale, float v_scale,
                                          int32_t* status, cudaStream_t stream);
+// x-split cache write: K [blocks, kv heads, head_dim / 8, block, 8],
+// V [blocks, kv heads, head_dim, block] (bf16).
+cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, int64_t key_stride,
+                                            int64_t value_stride, void* key_cache,
+                                            void* value_cache, const int64_t* slot_mapping,
+                                            int num_tokens, int num_kv_heads, int head_dim,
+                                            int block_size, int64_t num_slots, int32_t* status,
+                                            cudaStream_t stream);
 cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
                                      int32_t* status, cudaStream_t stream);
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,

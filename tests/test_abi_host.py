@@ -166,3 +166,54 @@ def test_reshape_and_cache_fp8_rejects_bad_scales(lib):
     # num_tokens == 0 is a no-op even with null pointers
     assert lib.pa_reshape_and_cache_fp8(vp(0), vp(0), 256, 256, vp(0), vp(0), vp(0), 0, 2, 128, 16,
                                         32, 1.0, 1.0, vp(0), vp(0)) == 0
+
+
+def decode_xsplit_call(lib, **kw):
+    args = dict(out=A, q=A, kc=A, vc=A, bt=A, mb=4, sl=A, ns=2, msl=64, hq=8, hkv=2, d=128, bs=16,
+                nb=32, scale=0.125, pt=0, ws=A, wsb=1 << 20)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.pa_decode_xsplit(vp(args["out"]), vp(args["q"]), vp(args["kc"]), vp(args["vc"]),
+                                vp(args["bt"]), args["mb"], vp(args["sl"]), args["ns"],
+                                args["msl"], args["hq"], args["hkv"], args["d"], args["bs"],
+                                args["nb"], args["scale"], args["pt"], vp(args["ws"]),
+                                args["wsb"], vp(0))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(out=0), 1), (dict(kc=A + 8), 1), (dict(hq=6, hkv=4), 1), (dict(msl=65), 1),
+    (dict(scale=float("nan")), 1), (dict(pt=24), 1), (dict(ws=A + 16), 1),
+    (dict(d=96), 2), (dict(bs=8), 2), (dict(hq=34, hkv=2), 2),
+    (dict(ws=0), 3), (dict(wsb=16), 3),
+])
+def test_decode_xsplit_rejects_invalid_arguments(lib, kw, expect):
+    assert decode_xsplit_call(lib, **kw) == expect
+
+
+def test_decode_xsplit_empty_batch_is_a_no_op(lib):
+    assert decode_xsplit_call(lib, ns=0) == 0
+
+
+def test_workspace_size_covers_the_xsplit_units(lib):
+    """Groups above 4 q heads run as several work units per kv head in the
+    x-split decode: the workspace must hold a pair counter per unit."""
+    for hq, hkv in ((64, 8), (40, 8), (16, 1)):
+        ws = lib.pa_decode_workspace_size(1000, hq, hkv, 128, 4096, 0)
+        g = hq // hkv
+        units = hkv * (g // max(x for x in (1, 2, 3, 4) if g % x == 0))
+        assert ws >= 1000 * units * 8
+
+
+def test_reshape_and_cache_xsplit_validation(lib):
+    vp = ctypes.c_void_p
+    call = lambda **k: lib.pa_reshape_and_cache_xsplit(
+        vp(k.get("key", A)), vp(k.get("value", A)), k.get("ks", 1024), k.get("vs", 1024),
+        vp(k.get("kc", A)), vp(k.get("vc", A)), vp(k.get("sm", A)), k.get("n", 4), 8,
+        k.get("d", 128), 16, 64, vp(0), vp(0))
+    assert call(n=0) == 0
+    assert call(key=0) == 1
+    assert call(vc=A + 2) == 1
+    assert call(ks=1000) == 1
+    assert call(vs=1028) == 1
+    assert call(n=-1) == 1
+    assert call(d=12) == 2
