@@ -443,9 +443,15 @@ def extra_decode_fp8(pa, name, dev, flush, reps=20):
 
 
 def extra_decode(pa, name, dev, flush, reps=20):
-    """Decode-only timing of another named workload (context for the line)."""
+    """Decode-only timing of another named workload (context for the line).
+    Suffix _fp8: over an e4m3 copy of the cache; _xsplit: over the x-split
+    layout (K [blocks, kv heads, d / 8, block, 8], V [blocks, kv heads, d,
+    block]) of the same cache."""
     if name.endswith("_fp8"):
         return extra_decode_fp8(pa, name[:-len("_fp8")], dev, flush, reps)
+    xsplit = name.endswith("_xsplit")
+    if xsplit:
+        name = name[:-len("_xsplit")]
     if wl.NAMED[name]().max_query_len > 1:
         return extra_mixed(pa, name, dev, flush, reps)
     w = wl.NAMED[name]()
@@ -454,8 +460,16 @@ def extra_decode(pa, name, dev, flush, reps=20):
     ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
                                                    w.head_dim, w.max_seq_len), dev)
     out = torch.empty_like(t.q)
-    call = lambda: pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
-                             w.max_seq_len, w.scale, out=out, workspace=ws)
+    if xsplit:
+        nb, B, H, d = t.key_cache.shape
+        kx = t.key_cache.view(nb, B, H, d // 8, 8).permute(0, 2, 3, 1, 4).contiguous()
+        vx = t.value_cache.view(nb, B, H, d).permute(0, 2, 3, 1).contiguous()
+        del t.key_cache, t.value_cache
+        call = lambda: pa.decode_xsplit(t.q, kx, vx, t.block_tables, t.seq_lens, w.max_seq_len,
+                                        w.scale, out=out, workspace=ws)
+    else:
+        call = lambda: pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
+                                 w.max_seq_len, w.scale, out=out, workspace=ws)
     for _ in range(3):
         flush.add_(1)
         call()
@@ -471,11 +485,12 @@ def extra_decode(pa, name, dev, flush, reps=20):
         ms.append(a.elapsed_time(b))
     s = statistics.median(ms) / 1e3
     peak, _ = measured_peaks()
-    res = {"us_per_call": round(s * 1e6, 2), "kv_gbs": round(ab["kv_bytes"] / s / 1e9, 2),
+    res = {"kv_layout": "x-split" if xsplit else "token-major",
+           "us_per_call": round(s * 1e6, 2), "kv_gbs": round(ab["kv_bytes"] / s / 1e9, 2),
            "decode_gbs": round(ab["decode_bytes"] / s / 1e9, 2),
            "frac_of_measured_peak": round(ab["decode_bytes"] / s / 1e9 / peak, 4),
            "kv_unique_tokens": ab["kv_unique_tokens"], "kv_logical_tokens": ab["kv_logical_tokens"]}
-    del t
+    del t, call
     torch.cuda.empty_cache()
     return res
 
@@ -560,7 +575,9 @@ def main(argv=None):
                                                     "prefix_shared_decode_b256",
                                                     "mixed_chunked_prefill",
                                                     "multi_chunk_prefill",
-                                                    "llama8b_decode_b64_fp8"])
+                                                    "llama8b_decode_b64_fp8",
+                                                    "llama8b_decode_b64_xsplit",
+                                                    "prefix_shared_decode_b256_xsplit"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

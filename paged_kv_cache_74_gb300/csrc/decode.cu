@@ -39,6 +39,10 @@
 //   exceeds the reference by more than 2^8 (O = A / l is exact for any
 //   reference).  Each segment is padded to a multiple of four stages, so all
 //   warps finish it together and merge their states in shared memory.
+// * Two more cache formats run through the same code: e4m3 values (KV8,
+//   dequantized on the fly, scales folded into the softmax scale and 1/L)
+//   and the x-split layout of section 3.2.1 (XS: other TMA views, and V
+//   turned from [head_dim][token] into token rows in shared memory).
 #include "decode_common.cuh"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
