@@ -11,9 +11,8 @@
 //                (m_j, l_j, O_j) are merged: m = max m_j,
 //                L = sum l_j e^{m_j - m}, O = sum O_j l_j e^{m_j - m} / L.
 //
-// GB300 design.  Decode is HBM-bound (about 2 FMAs per byte of KV at 4 q
-// heads per kv head), so the K/V stream runs on CUDA cores, not tensor
-// cores, and the kernel is built around keeping HBM busy:
+// GB300 design.  Decode is HBM-bound, so the kernel is built around keeping
+// HBM busy; the products are small and must not hold the K/V stages long:
 //
 // * Balanced persistent grid.  Every (request, kv head, 16-token block)
 //   tile of the batch is numbered (request-major, then kv head, then block)
@@ -30,19 +29,32 @@
 //   head_dim, 4 KB at head_dim 128) into an 8-stage ring guarded by
 //   mbarriers, writes each stage's block index and flags next to it, and
 //   prefetches each segment's q with a bulk copy into a double buffer.
-// * Four consumer warps take every 4th stage.  T lanes share a token; each
-//   lane holds a 16-byte slice of head_dim of q (fp32, pre-scaled by
-//   scale * log2 e) and of the output accumulators, computes partial q.k
+// * bf16 caches: two consumer warps take alternate stages.  A warp computes
+//   S^T = K q^T (16 tokens x 8 columns of q heads, padding heads zero) and
+//   O^T += V^T P^T with warp-level m16n8k16 tensor-core products: K and V
+//   fragments come straight from the stage with ldmatrix (the copies land
+//   128-byte swizzled, so those reads are conflict-free), the weights P go
+//   from the score fragments to the operand fragments with movmatrix.  A
+//   tile costs about 0.5 us, so the stage is released soon after it lands.
+//   P is rounded to bf16 for the product and l sums the rounded weights.
+//   At a segment end the two warps merge their states through shared
+//   memory and hand the result to an epilogue warp, which writes the output
+//   or the partial, bumps the pair counter and, as last contributor, merges
+//   the partials; the consumers go straight on to the next segment.
+// * e4m3 caches (KV8): four consumer warps on CUDA cores.  T lanes share a
+//   token; each lane holds a 16-byte slice of head_dim of q (fp32, pre-scaled
+//   by scale * log2 e) and of the output accumulators, computes partial q.k
 //   for all q heads with packed fp32 FMAs (fma.rn.f32x2), and the partials
 //   are summed through a shared-memory transpose that reuses the warp's own
-//   K tile.  The running max is rescaled lazily, only when a new score
+//   K tile; the warps merge their states in shared memory at segment ends.
+// * In both, the running max is rescaled lazily, only when a new score
 //   exceeds the reference by more than 2^8 (O = A / l is exact for any
-//   reference).  Each segment is padded to a multiple of four stages, so all
-//   warps finish it together and merge their states in shared memory.
-// * Two more cache formats run through the same code: e4m3 values (KV8,
-//   dequantized on the fly, scales folded into the softmax scale and 1/L)
-//   and the x-split layout of section 3.2.1 (XS: other TMA views, and V
-//   turned from [head_dim][token] into token rows in shared memory).
+//   reference), and each segment is padded to a multiple of the consumer
+//   count in stages, so all consumers finish it together.
+// * The x-split layout of section 3.2.1 (XS) runs through the bf16 path with
+//   other TMA views: K as 8-token x 16-byte rows (128-byte swizzled), V as
+//   V^T [head_dim][16 tokens] (32-byte swizzled), which is already the
+//   operand layout of O^T += V^T P^T.
 #include "decode_common.cuh"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -57,6 +69,7 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units
 constexpr int kSkip = 1;     // padding stage: no data, nothing to compute
 constexpr int kLastRow = 2;  // the segment ends after this row of stages
 constexpr int kDone = 4;     // no more work for the warp that receives it
+constexpr int kEndSeg = 3;   // segment kind handed to the epilogue warp: no more segments
 
 
 template <int D, int GMAX, bool KV8 = false, bool XS = false>
@@ -74,9 +87,15 @@ struct DecodeCfg {
   static constexpr int REP = V >= T ? 1 : T / V;               // lanes holding the same score
   static constexpr int LPH = T / GMAX;                         // lanes of a group per head
   static constexpr int CH = V / 4;                             // 16-byte chunks per transpose row
-  static constexpr int NC = 4;                                 // consumer warps
-  static constexpr int MINB = GMAX * EL > 32 ? 2 : 3;          // CTAs per SM the registers allow
+  // Consumer warps: two tensor-core consumers keep up with the K/V stream
+  // (one 16-token tile takes ~0.5 us), four fp32 ones.
+  static constexpr int NC = KV8 ? 4 : 2;
+  static constexpr int MINB = (!KV8 || GMAX * EL <= 32) ? 3 : 2;  // CTAs per SM
   static constexpr int ELT = KV8 ? 1 : 2;                      // bytes per K/V element (e4m3 / bf16)
+  // bf16 caches: q.k and p.v as warp-level m16n8k16 tensor-core products
+  // (tokens / head_dim x 8 padded q heads); e4m3 caches: fp32 FMAs.
+  static constexpr bool MMA = !KV8;
+  static constexpr int KS = D / 16;                            // 16-wide steps of head_dim
   static constexpr int TILE = kBlockSize * D * ELT;            // bytes of one (block, kv head) tile
   // The partial-score transpose (32 rows of V floats) reuses the warp's own
   // K tile once its q.k products are done, when it fits and no later
@@ -87,20 +106,28 @@ struct DecodeCfg {
   static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 ? (XPOSE_IN_K ? 4 : 3) : 2) / 2;
   // shared memory carve-up (bytes)
   static constexpr int RING = STAGES * 2 * TILE;
-  static constexpr int XPOSE = XPOSE_IN_K ? 0 : NC * 32 * CH * 16;
-  static constexpr int PBUF = NC * NG * V * 4;                 // per-warp weights
-  static constexpr int COMB = NC * GMAX * (D + 2) * 4;         // cross-warp merge
+  static constexpr int XPOSE = (MMA || XPOSE_IN_K) ? 0 : NC * 32 * CH * 16;
+  static constexpr int PBUF = MMA ? 0 : NC * NG * V * 4;       // per-warp weights
+  // The tensor-core consumers hand every finished segment to an epilogue
+  // warp (partial write, pair counter, last-contributor merge), so the
+  // global round trips of a segment end never stall the K/V stream.
+  static constexpr bool EPI = MMA;
+  static constexpr int WF = GMAX * D + 2 * GMAX;               // floats of one (O, m, l) record
+  static constexpr int HF = WF + 8;                            // ... plus the segment record
+  static constexpr int COMB = MMA ? 0 : NC * GMAX * (D + 2) * 4;  // cross-warp merge
   static constexpr int PC = PBUF > COMB ? PBUF : COMB;         // weights and merge alias
+  static constexpr int HAND = EPI ? (HF * 4 + 15) / 16 * 16 : 0;  // the segment handed over
   static constexpr int QBUF = 2 * GMAX * D * 2;                // q of two segments
   static constexpr int OFF_XPOSE = RING;
   static constexpr int OFF_PC = OFF_XPOSE + XPOSE;
-  static constexpr int OFF_Q = OFF_PC + PC;
+  static constexpr int OFF_HAND = OFF_PC + PC;
+  static constexpr int OFF_Q = OFF_HAND + HAND;
   static constexpr int OFF_META = OFF_Q + QBUF;                // int2 per stage
   static constexpr int OFF_SEG = OFF_META + STAGES * 8;        // 2 segment records
-  static constexpr int OFF_BAR = OFF_SEG + 2 * 32;             // full, empty, qfull, qempty, sync
-  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 5) * 8;
+  static constexpr int OFF_BAR = OFF_SEG + 2 * 32;  // full, empty, qfull, qempty, sync, hfull, hempty
+  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 7) * 8;
   static constexpr int SMEM = OFF_MISC + 32;
-  static constexpr int THREADS = (NC + 1) * 32;
+  static constexpr int THREADS = (NC + 1 + (EPI ? 1 : 0)) * 32;
   // Stage i goes to consumer warp i % NC.  With STAGES a multiple of NC a
   // stage is only ever used by one warp, so when a warp waits on a stage
   // the barrier is at most one phase behind and the parity wait is exact.
@@ -108,9 +135,14 @@ struct DecodeCfg {
   static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V >= 4 && V <= 32, "decode shape");
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
-  // The x-split layout re-lays V out in the K stage after the q.k products
-  // (see the consumer), so the K stage must be free by then.
-  static_assert(!XS || (!KV8 && XPOSE_IN_K && NSB == 1), "x-split decode shape");
+  static_assert(!XS || MMA, "the x-split layout is read by the tensor-core consumers");
+  static_assert(!MMA || (GMAX <= 8 && NC == 2), "an m16n8k16 product serves at most 8 q heads");
+  // Bulk-copy destinations (ring, q) 16-byte aligned; the segment records'
+  // 64-bit fields 8-byte aligned.
+  static_assert(RING % 1024 == 0 && OFF_HAND % 16 == 0 && OFF_Q % 16 == 0 && OFF_META % 8 == 0 &&
+                    OFF_SEG % 8 == 0 && OFF_BAR % 8 == 0 && OFF_MISC % 8 == 0 && (WF * 4) % 8 == 0,
+                "shared-memory carve-up alignment");
+  static_assert(GMAX * D / 2 % 32 == 0, "the epilogue lanes split the head_dim pairs evenly");
 };
 
 // What the producer tells the consumers about a segment: the run of blocks
@@ -171,39 +203,57 @@ __device__ __forceinline__ uint32_t xs_k_offset(int t, int c) {
   return static_cast<uint32_t>(r * 128 + (((t & 7) ^ (r & 7)) * 16));
 }
 
-// Token rows [16][head_dim] bf16 with the 16-byte unit c of row t stored at
-// c ^ (t % 8): V re-laid out by xs_transpose_v, read like a token-major tile.
-template <int D>
-__device__ __forceinline__ uint32_t xs_row_offset(int t, int c) {
-  return static_cast<uint32_t>(t * (D * 2) + ((c ^ (t & 7)) * 16));
+// A V stage of the x-split layout holds V^T of the tile as [head_dim][16
+// tokens]: 32-byte rows, the two 16-byte halves (tokens 0-7, 8-15) swapped
+// on rows with bit 2 set (the copy's 32-byte swizzle).  Offset of half tb
+// of row d:
+__device__ __forceinline__ uint32_t xs_v_offset(int d, int tb) {
+  return static_cast<uint32_t>(d * 32 + ((tb ^ ((d >> 2) & 1)) * 16));
 }
 
-// V stage [head_dim][16 tokens] (32-byte rows, 16-byte halves swapped on
-// rows with bit 2 set: the copy's 32-byte swizzle) -> token rows at `dst`.
-// The tile is cut into 8 x 8 matrices (8 head_dim rows x 8 tokens);
-// ldmatrix.trans hands each lane a pair of consecutive head_dim values of
-// one token and stmatrix writes the pairs back as token rows.  Four
-// matrices per instruction, all 32 lanes (warp-collective).
+// A token-major K or V stage (the grouped copy, 128-byte swizzled):
+// [8-token group][head_dim / 64][8 tokens][128 B], the 16-byte chunk c of
+// token t at unit (c % 8) ^ (t % 8) of its 128-byte row.
 template <int D>
-__device__ __forceinline__ void xs_transpose_v(uint32_t src, uint32_t dst, int lane) {
-  constexpr int kGroups = D / 8 * 2 / 4;
-  const int rr = lane & 7;
-#pragma unroll
-  for (int q4 = 0; q4 < kGroups; ++q4) {
-    const int mi = 4 * q4 + (lane >> 3);  // this lane addresses row rr of matrix mi
-    const int db = mi >> 1, tb = mi & 1;  // head_dim block, token block
-    const int d = 8 * db + rr;
-    const uint32_t from = src + d * 32 + ((tb ^ ((d >> 2) & 1)) * 16);
-    uint32_t f0, f1, f2, f3;
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(f0), "=r"(f1), "=r"(f2), "=r"(f3)
-                 : "r"(from)
-                 : "memory");
-    const uint32_t to = dst + xs_row_offset<D>(8 * tb + rr, db);
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(to),
-                 "r"(f0), "r"(f1), "r"(f2), "r"(f3)
-                 : "memory");
-  }
+__device__ __forceinline__ uint32_t grp_offset(int t, int c) {
+  return static_cast<uint32_t>((t >> 3) * (D / 64) * 1024 + (c >> 3) * 1024 + (t & 7) * 128 +
+                               (((c & 7) ^ (t & 7)) * 16));
+}
+
+// ---- warp-level tensor-core helpers (m16n8k16, bf16 in, fp32 accumulate)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += A (16 x 16, row-major fragments a) * B (16 x 8, column fragments b0, b1).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The transpose of an 8 x 8 bf16 matrix held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 template <int D, int GMAX, bool KV8, bool XS>
@@ -228,12 +278,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t qfull0 = empty0 + 8 * C::STAGES;
   const uint32_t qempty0 = qfull0 + 16;
   const uint32_t csync_bar = qempty0 + 16;  // consumer-warp barrier (bounded waits)
+  const uint32_t hfull0 = csync_bar + 8;     // segment handed to the epilogue warp
+  const uint32_t hempty0 = hfull0 + 8;       // ... and taken by it
   const uint32_t qbuf_s = smem_u32(smem + C::OFF_Q);
 
   // TMA destinations must be 128-byte aligned (1024 for the 128-byte
-  // swizzle of the x-split K boxes); the dynamic shared-memory base always
+  // swizzled boxes of the bf16 paths); the dynamic shared-memory base always
   // is on this GPU, but never issue a copy if it were not.
-  if (ring_s & (XS ? 1023 : 127)) {
+  if (ring_s & (C::MMA ? 1023 : 127)) {
     griddep_wait();
     if (threadIdx.x == 0) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 6);
     return;
@@ -249,6 +301,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(qempty0 + 8 * k, C::NC);
     }
     mbar_init(csync_bar, C::NC);
+    mbar_init(hfull0, 1);
+    mbar_init(hempty0, 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -425,8 +479,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
               } else {
                 // Row num_blocks * block_size is wholly out of bounds: TMA fills zeros.
                 const int row0 = bad ? a.num_blocks * a.block_size : tile_row(a, phys, b + j);
-                tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
-                tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+                if constexpr (C::MMA) {  // grouped view: 8-token groups, 128-byte swizzle
+                  tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 0, 0, row0 / 8, kvh, policy);
+                  tma_load_5d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, 0, 0, row0 / 8, kvh,
+                              policy);
+                } else {
+                  tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
+                  tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+                }
               }
             } else {
               mbar_arrive(full);
@@ -478,6 +538,141 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     return;
   }
 
+  if (C::EPI && warp == C::NC + 1) {
+    // ================================================================ epilogue
+    // Finishes each segment handed over by the consumers: the bf16 output of
+    // a whole (request, kv head) pair, or the partial of a shared pair, its
+    // pair counter and, for the last contributor, the merge of all partials.
+    const float* hr = reinterpret_cast<const float*>(smem + C::OFF_HAND);
+    for (int seg = 0;; ++seg) {
+      const int got = mbar_wait(hfull0, seg & 1) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 8);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const SegInfo e = *reinterpret_cast<const SegInfo*>(hr + C::WF);
+      if (e.kind == kEndSeg) break;
+      const int head0 = e.kvh * a.group;
+      if (e.kind == kWhole) {
+        for (int it = lane; it < a.group * (D / 2); it += 32) {
+          const int h = it / (D / 2);
+          const int d = (it % (D / 2)) * 2;
+          const float inv = a.v_scale / hr[GMAX * D + 2 * h + 1];
+          const float2 ov = *reinterpret_cast<const float2*>(hr + h * D + d);
+          *reinterpret_cast<__nv_bfloat162*>(
+              a.out + (static_cast<size_t>(e.row) * a.num_heads + head0 + h) * D + d) =
+              __floats2bfloat162_rn(ov.x * inv, ov.y * inv);
+        }
+      } else {
+        const int pslot = e.kind == kTail ? 1 : 0;
+        const long long W = *total_tiles;
+        const int c0 = cta_of_tile(W, a.num_ctas, e.t0);
+        const int c1 = cta_of_tile(W, a.num_ctas, e.t0 + e.nblk - 1);
+        unsigned long long* counter = a.counters + static_cast<size_t>(e.r) * a.num_kv_heads + e.kvh;
+        // If every other contributor has already counted (the usual case for
+        // the CTA whose range ends inside the pair, at the end of its work),
+        // merge now from this CTA's own record, without publishing it.
+        int last = 0;
+        if (lane == 0 && c1 > c0 &&
+            ld_acquire_u64(counter) == ((static_cast<unsigned long long>(a.epoch) << 32) |
+                                        static_cast<unsigned>(c1 - c0)))
+          last = 2;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last == 0) {
+          for (int it = lane; it < a.group * (D / 2); it += 32) {
+            const int h = it / (D / 2);
+            const int d = (it % (D / 2)) * 2;
+            const float M = hr[GMAX * D + 2 * h], L = hr[GMAX * D + 2 * h + 1];
+            const float inv = a.v_scale / L;
+            const float2 ov = *reinterpret_cast<const float2*>(hr + h * D + d);
+            const size_t rec = (static_cast<size_t>(cta) * 2 + pslot) * a.group + h;
+            *reinterpret_cast<float2*>(a.part_o + rec * D + d) = make_float2(ov.x * inv, ov.y * inv);
+            if (d == 0) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(M, L);
+          }
+          // Publish the partial; the last of the pair's contributors merges them.
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) last = contribute(counter, a.epoch, c1 - c0 + 1, a.status, e.r) ? 1 : 0;
+          last = __shfl_sync(0xffffffffu, last, 0);
+        }
+        if (last) {
+          __syncwarp();  // lane 0 saw the other contributors' counts
+          __threadfence();
+          // Lane L merges head_dim pairs L, L + 32, ... of every head.  The
+          // loads of one contributor are independent of each other, so each
+          // contributor costs one memory round trip.
+          constexpr int kPer = GMAX * D / 2 / 32;  // head_dim pairs per lane (all heads)
+          float M[GMAX], L[GMAX], o[kPer][2];
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            M[h] = kNegBig;
+            L[h] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) o[k][0] = o[k][1] = 0.f;
+          for (int c = c0; c <= c1; ++c) {
+            const size_t rec0 = (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * a.group;
+            float2 ml[GMAX], ov[kPer];
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) ml[h] = make_float2(kNegBig, 0.f);
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) ov[k] = make_float2(0.f, 0.f);
+            const bool own = last == 2 && c == cta;  // this CTA's record is still in shared memory
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h)
+              if (h < a.group)
+                ml[h] = own ? make_float2(hr[GMAX * D + 2 * h], hr[GMAX * D + 2 * h + 1])
+                            : __ldcg(reinterpret_cast<const float2*>(a.part_ml + (rec0 + h) * 2));
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+              const int h = (lane + 32 * k) / (D / 2), d = ((lane + 32 * k) % (D / 2)) * 2;
+              if (h >= a.group) continue;
+              if (own) {
+                const float2 u = *reinterpret_cast<const float2*>(hr + h * D + d);
+                const float inv = a.v_scale / ml[h].y;
+                ov[k] = make_float2(u.x * inv, u.y * inv);
+              } else {
+                ov[k] = __ldcg(reinterpret_cast<const float2*>(a.part_o + (rec0 + h) * D + d));
+              }
+            }
+            float wo[GMAX], wt[GMAX];
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+              if (h >= a.group) continue;
+              const float mx = fmaxf(M[h], ml[h].x);
+              wo[h] = fast_exp2(M[h] - mx);
+              wt[h] = ml[h].y * fast_exp2(ml[h].x - mx);
+              L[h] = L[h] * wo[h] + wt[h];
+              M[h] = mx;
+            }
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+              const int h = (lane + 32 * k) / (D / 2);
+              if (h >= a.group) continue;
+              o[k][0] = o[k][0] * wo[h] + wt[h] * ov[k].x;
+              o[k][1] = o[k][1] * wo[h] + wt[h] * ov[k].y;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int h = (lane + 32 * k) / (D / 2), d = ((lane + 32 * k) % (D / 2)) * 2;
+            if (h >= a.group) continue;
+            const float inv = 1.f / L[h];
+            *reinterpret_cast<__nv_bfloat162*>(
+                a.out + (static_cast<size_t>(e.row) * a.num_heads + head0 + h) * D + d) =
+                __floats2bfloat162_rn(o[k][0] * inv, o[k][1] * inv);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hempty0);
+    }
+    return;
+  }
+
   // ================================================================ consumers
   const int g = lane / C::T;
   const int li = lane % C::T;
@@ -493,6 +688,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   float2 o2[GMAX][C::EP];
   float my_m = kNegBig;  // running max (log2 units) of this lane's head, same on all its lanes
   float my_l = 0.f;      // this lane's share of the running exp-sum
+  // Tensor-core consumers: lane = 4 fg + ft in the m16n8k16 fragments; the
+  // 8 columns of every product are q heads (those >= group are zero).
+  const int fg = lane >> 2, ft = lane & 3;
+  uint32_t qf[C::KS][2];  // q^T fragments: head fg, head_dim 16 ks + 2 ft (+1, +8, +9)
+  float om[C::KS][4];     // O^T: head_dim 16 m + fg (+8) x heads 2 ft, 2 ft + 1
+  float mh[2] = {kNegBig, kNegBig};  // running max (log2 units) of heads 2 ft, 2 ft + 1
+  float lh[2] = {0.f, 0.f};          // this lane's share of their exp-sums
   SegInfo si{};
   bool fresh = true;
   int seg = 0;
@@ -525,7 +727,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       break;
     }
     const int2 m = meta[s];
-    if (m.y & kDone) break;
+    if (m.y & kDone) {
+      if (C::EPI && warp == 0) {  // tell the epilogue warp that no segment follows
+        const int ok = (seg < 1 || mbar_wait(hempty0, (seg - 1) & 1)) ? 1 : 0;
+        if (__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) {
+            SegInfo* rec = reinterpret_cast<SegInfo*>(reinterpret_cast<float*>(smem + C::OFF_HAND) +
+                                                      C::WF);
+            rec->kind = kEndSeg;
+            mbar_arrive(hfull0);
+          }
+        } else if (lane == 0) {
+          record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 10);
+          *abort_flag = 1;
+        }
+      }
+      break;
+    }
 
     if (fresh) {  // first stage of a segment: take its q and reset the state
       const int slot = seg & 1;
@@ -539,8 +757,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       si = seginfo[slot];
       const uint32_t qs = qbuf_s + slot * (GMAX * D * 2);
+      if constexpr (C::MMA) {
+        // q stays bf16 (the products are exact in fp32); the scale is
+        // applied to the fp32 scores.
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
+        for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            qf[ks][j] = fg < a.group ? ld_shared_u32(qs + (fg * D + 16 * ks + 8 * j + 2 * ft) * 2) : 0u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
+#pragma unroll
+        for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) om[mt][i] = 0.f;
+        mh[0] = mh[1] = kNegBig;
+        lh[0] = lh[1] = 0.f;
+        fresh = false;
+      }
+#pragma unroll
+      for (int h = 0; h < (C::MMA ? 0 : GMAX); ++h) {
 #pragma unroll
         for (int j = 0; j < C::CPL; ++j) {
           uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -553,18 +789,103 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
+      if constexpr (!C::MMA) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h)
+        for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-        for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
-      my_m = kNegBig;
-      my_l = 0.f;
-      fresh = false;
+          for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
+        my_m = kNegBig;
+        my_l = 0.f;
+        fresh = false;
+      }
     }
 
-    if (!(m.y & kSkip)) {
+    if (!(m.y & kSkip) && C::MMA) {
+      const uint32_t kt = ring_s + (2 * s) * C::TILE;
+      const uint32_t vt = kt + C::TILE;
+      const int tok0 = m.x * kBlockSize;
+      const int seq_len = si.seq_len;
+      // S^T (16 tokens x 8 heads) = K q^T.  Matrix mi = lane / 8 of each
+      // ldmatrix: tokens 8 (mi % 2) .. + 7, head_dim chunk 2 ks + mi / 2.
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int ka_t = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        uint32_t af[4];
+        const int c = 2 * ks + (lane >> 4);
+        ldsm_x4(kt + (XS ? xs_k_offset(ka_t, c) : grp_offset<D>(ka_t, c)), af);
+        mma_16816(sacc, af, qf[ks][0], qf[ks][1]);
+      }
+      // Scores in log2 units: (token fg (+8), head 2 ft (+1)); tokens past
+      // seq_len and padding heads get weight 0.
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool ok = tok0 + fg + (i >> 1) * 8 < seq_len && 2 * ft + (i & 1) < a.group;
+        p[i] = ok ? sacc[i] * a.scale_log2 : -INFINITY;
+      }
+      float tmax[2] = {fmaxf(p[0], p[2]), fmaxf(p[1], p[3])};
+#pragma unroll
+      for (int bb = 4; bb < 32; bb <<= 1) {
+        tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], bb));
+        tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], bb));
+      }
+      if (__any_sync(0xffffffffu,
+                     tmax[0] > mh[0] + kRescaleSlack || tmax[1] > mh[1] + kRescaleSlack)) {
+        float al[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float mn = fmaxf(mh[e], tmax[e]);
+          al[e] = fast_exp2(mh[e] - mn);
+          mh[e] = mn;
+          lh[e] *= al[e];
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::KS; ++mt) {
+          om[mt][0] *= al[0];
+          om[mt][1] *= al[1];
+          om[mt][2] *= al[0];
+          om[mt][3] *= al[1];
+        }
+      }
+      // Weights rounded to bf16 for the product; l sums the rounded values.
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = fast_exp2(p[i] - mh[i & 1]);
+      const uint32_t pk0 = pack_bf16x2(p[0], p[1]);  // token fg:     heads 2 ft, 2 ft + 1
+      const uint32_t pk1 = pack_bf16x2(p[2], p[3]);  // token fg + 8
+      lh[0] += bf16_lo(pk0) + bf16_lo(pk1);
+      lh[1] += bf16_hi(pk0) + bf16_hi(pk1);
+      const uint32_t pb0 = movmatrix_t(pk0);  // P^T: tokens 2 ft, 2 ft + 1 of head fg
+      const uint32_t pb1 = movmatrix_t(pk1);  // tokens 2 ft + 8, 2 ft + 9
+      // O^T (head_dim x 8 heads) += V^T P^T, 16 head_dim rows per product.
+      // In the last block of a request the V rows past seq_len may hold NaN
+      // (0 x NaN is NaN): their halves of the V^T fragments are cleared.
+      uint32_t vm01 = 0xffffffffu, vm89 = 0xffffffffu;
+      if (tok0 + kBlockSize > seq_len) {
+        const int t0 = tok0 + 2 * ft;
+        vm01 = (t0 < seq_len ? 0x0000ffffu : 0u) | (t0 + 1 < seq_len ? 0xffff0000u : 0u);
+        vm89 = (t0 + 8 < seq_len ? 0x0000ffffu : 0u) | (t0 + 9 < seq_len ? 0xffff0000u : 0u);
+      }
+      const int va_r = lane & 7, va_m = lane >> 3;
+#pragma unroll
+      for (int mt = 0; mt < C::KS; ++mt) {
+        uint32_t af[4];
+        if constexpr (XS) {
+          // V^T rows: matrix mi = head_dim 16 mt + 8 (mi % 2) .., tokens 8 (mi / 2) ..
+          ldsm_x4(vt + xs_v_offset(16 * mt + 8 * (va_m & 1) + va_r, va_m >> 1), af);
+        } else {
+          // token rows, transposed: matrix mi = tokens 8 (mi / 2) .., chunk 2 mt + mi % 2
+          ldsm_x4_t(vt + grp_offset<D>(8 * (va_m >> 1) + va_r, 2 * mt + (va_m & 1)), af);
+        }
+        af[0] &= vm01;
+        af[1] &= vm01;
+        af[2] &= vm89;
+        af[3] &= vm89;
+        mma_16816(om[mt], af, pb0, pb1);
+      }
+    } else if (!(m.y & kSkip)) {
       const uint32_t kt = ring_s + (2 * s) * C::TILE;
       const uint32_t vt = kt + C::TILE;
       const int tok0 = m.x * kBlockSize;
@@ -585,8 +906,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           const int t = (sb * C::SB + kk) * C::NG + g;
           Row8<KV8> kw[C::CPL];
 #pragma unroll
-          for (int j = 0; j < C::CPL; ++j)
-            kw[j].load(kt + (XS ? xs_k_offset(t, li + C::T * j) : (t * D + (li + C::T * j) * 8) * C::ELT));
+          for (int j = 0; j < C::CPL; ++j) kw[j].load(kt + (t * D + (li + C::T * j) * 8) * C::ELT);
           float2 kf[C::CPL][4];
 #pragma unroll
           for (int j = 0; j < C::CPL; ++j)
@@ -683,13 +1003,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           p[v + 2] = f.z;
           p[v + 3] = f.w;
         }
-        if constexpr (XS) {
-          // V arrived as V^T [head_dim][16 tokens]; turn it into token rows
-          // in the K stage (free now: the last transpose reads are behind
-          // the __syncwarp above), where the loop below reads it.
-          xs_transpose_v<D>(vt, kt, lane);
-          __syncwarp();
-        }
         // A += p v over this sub-batch's tokens.  In the last block of a
         // request the V rows past seq_len may hold NaN and are replaced by 0.
         auto pv = [&](bool check) {
@@ -698,9 +1011,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             const int t = (sb * C::SB + kk) * C::NG + g;
             Row8<KV8> vw[C::CPL];
 #pragma unroll
-            for (int j = 0; j < C::CPL; ++j)
-              vw[j].load(XS ? kt + xs_row_offset<D>(t, li + C::T * j)
-                            : vt + (t * D + (li + C::T * j) * 8) * C::ELT);
+            for (int j = 0; j < C::CPL; ++j) vw[j].load(vt + (t * D + (li + C::T * j) * 8) * C::ELT);
             if (check && tok0 + t >= seq_len) {
 #pragma unroll
               for (int j = 0; j < C::CPL; ++j) vw[j].clear();
@@ -733,6 +1044,81 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     if (!(m.y & kLastRow)) continue;
+
+    if constexpr (C::EPI) {
+      // ======================== end of segment: merge the two warps' states
+      // and hand the result to the epilogue warp.  Record: O^T accumulators
+      // [GMAX][D], (m, l) per head, the segment record; each lane writes and
+      // reads only its own (head, d) places.
+      float ls[2] = {lh[0], lh[1]};
+#pragma unroll
+      for (int bb = 4; bb < 32; bb <<= 1) {
+        ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], bb);
+        ls[1] += __shfl_xor_sync(0xffffffffu, ls[1], bb);
+      }
+      float* hrec = reinterpret_cast<float*>(smem + C::OFF_HAND);
+      auto put = [&]() {
+#pragma unroll
+        for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = 2 * ft + (i & 1);
+            if (h < a.group) hrec[h * D + 16 * mt + fg + 8 * (i >> 1)] = om[mt][i];
+          }
+        if (fg == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = 2 * ft + e;
+            if (h < a.group) {
+              hrec[GMAX * D + 2 * h] = mh[e];
+              hrec[GMAX * D + 2 * h + 1] = ls[e];
+            }
+          }
+        }
+      };
+      if (warp == 1) {
+        // The record was last handed over one segment ago.
+        const int ok = (seg < 1 || mbar_wait(hempty0, (seg - 1) & 1)) ? 1 : 0;
+        if (__all_sync(0xffffffffu, ok)) {
+          put();
+        } else if (lane == 0) {
+          record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 9);
+          *abort_flag = 1;
+        }
+      }
+      if (!csync() || *abort_flag) break;
+      if (warp == 0) {
+        // Merge warp 1's state into this warp's, then hand the segment over.
+        float wa[2], wb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * ft + e;
+          const float mo = h < a.group ? hrec[GMAX * D + 2 * h] : kNegBig;
+          const float lo = h < a.group ? hrec[GMAX * D + 2 * h + 1] : 0.f;
+          const float mx = fmaxf(mh[e], mo);
+          wa[e] = fast_exp2(mh[e] - mx);
+          wb[e] = fast_exp2(mo - mx);
+          mh[e] = mx;
+          ls[e] = ls[e] * wa[e] + lo * wb[e];
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = 2 * ft + (i & 1);
+            const float ov = h < a.group ? hrec[h * D + 16 * mt + fg + 8 * (i >> 1)] : 0.f;
+            om[mt][i] = om[mt][i] * wa[i & 1] + ov * wb[i & 1];
+          }
+        __syncwarp();  // every lane has read the (m, l) entries before they change
+        put();
+        if (lane == 0) *reinterpret_cast<SegInfo*>(hrec + C::WF) = si;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hfull0);
+      }
+      fresh = true;
+      ++seg;
+      continue;
+    }
 
     // ============================================ end of segment: merge
     float lsum = my_l;

@@ -86,9 +86,12 @@ __device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
 }
 
 // Registers this CTA's partial for a pair; true if it was the last of n.
+// The first exchange assumes the other n - 1 have already counted (no read
+// before it): the contributor that finishes a pair pays one round trip.
 __device__ bool contribute(unsigned long long* counter, unsigned epoch, int n, int32_t* status,
                            int who) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+  unsigned long long old = (static_cast<unsigned long long>(epoch) << 32) |
+                           static_cast<unsigned>(n > 1 ? n - 1 : 0);
   unsigned long long now = 0;
   for (int tries = 0; tries < (1 << 20); ++tries) {
     now = (static_cast<unsigned>(old >> 32) == epoch)

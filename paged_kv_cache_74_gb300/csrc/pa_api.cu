@@ -204,11 +204,13 @@ bool make_xsplit_v_map(CUtensorMap* map, const void* cache, int num_blocks, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Work units per request of the x-split decode: the CUDA-core kernel serves
-// up to 4 q heads per unit, so a group of g q heads is cut into g / g'
-// units of g' heads (g' the largest divisor of g not above 4), each reading
-// its kv head's tiles (the units of one kv head are neighbours in the tile
-// order, so the repeated reads mostly hit L2).
+// Work units per request of the x-split decode: its kernel serves up to 4
+// q heads per unit, so a group of g q heads is cut into g / g' units of g'
+// heads (g' the largest divisor of g not above 4), each reading its kv
+// head's tiles (the units of one kv head are neighbours in the tile order,
+// so the repeated reads mostly hit L2).  Units of 8 heads (the 8 columns of
+// the kernel's products) measured slower on a batch of many short requests:
+// the per-segment hand-off work doubles while the K/V reads mostly hit L2.
 int xsplit_heads_per_unit(int group) {
   for (int g = 4; g > 1; --g)
     if (group % g == 0) return g;
@@ -339,13 +341,15 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
     if (!make_xsplit_k_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim, block_size) ||
         !make_xsplit_v_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim, block_size))
       return PA_ERR_CUDA;
-  } else if (tc) {
-    if (!make_q_group_map(&qmap, q, total_q, num_heads, head_dim, num_heads / num_kv_heads) ||
+  } else if (!kv.e4m3) {
+    // bf16: the grouped view (both decode kernels read tiles with ldmatrix
+    // or as tcgen05 operands).
+    if ((tc && !make_q_group_map(&qmap, q, total_q, num_heads, head_dim, group)) ||
         !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
-  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim, kv.e4m3) ||
-             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim, kv.e4m3)) {
+  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim, true) ||
+             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim, true)) {
     return PA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
