@@ -220,9 +220,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
  *                 calls that overlap on the GPU need separate workspaces
  * out[r, h] = sum_t softmax_t(scale * q[r,h] . k_t) v_t over the
  * seq_lens[r] keys of request r (exact attention, fp32 accumulation,
- * rounded once to bf16).  Up to 4 q heads per kv head the products run on
- * CUDA cores; with 5 to 16 they run on the tensor cores, and the weights
- * are rounded to bf16 before they multiply V.
+ * rounded once to bf16).  The products run on the tensor cores (warp-level
+ * products up to 4 q heads per kv head, tcgen05 from 5 to 16), and the
+ * softmax weights are rounded to bf16 before they multiply V.
  */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -309,9 +309,10 @@ pa_status pa_reshape_and_cache_xsplit(const void* key, const void* value,
  * pa_decode_xsplit -- pa_decode over x-split caches.  Same arguments,
  * workspace (pa_decode_workspace_size covers both layouts), sizes (head_dim
  * 64 or 128, block_size 16, 32 or 64, 1 to 16 q heads per kv head) and
- * errors as pa_decode.  Always on CUDA cores with fp32 weights: groups of
- * more than 4 q heads are cut into work units of at most 4 (the largest
- * divisor of the group not above 4), each reading its kv head's K/V.
+ * errors as pa_decode.  Always the warp-level tensor-core decode (weights
+ * rounded to bf16): groups of more than 4 q heads are cut into work units of
+ * at most 4 (the largest divisor of the group not above 4), each reading its
+ * kv head's K/V.
  */
 pa_status pa_decode_xsplit(void* out, const void* q, const void* key_cache,
                            const void* value_cache, const int32_t* block_tables,
