@@ -19,19 +19,24 @@
 //               rings; a K stage is refilled as soon as its S MMA is done, a
 //               V stage as soon as its P.V MMA is done;
 //   warp 9      MMA issuer (tcgen05, kind::f16, bf16 in, fp32 accumulate in
-//               TMEM), in the order S_0, S_1, PV_0, S_2, PV_1, ...:
+//               TMEM):
 //                 S_j = Q K_j^T  M = N = 128, K = head_dim, both operands
 //                                K-major, into one of two TMEM S buffers;
 //                 O  += P_j V_j  M = 128, N = head_dim, K = 128 keys; P_j from
 //                                one of two shared-memory buffers (K-major),
 //                                V as an MN-major operand exactly as TMA
-//                                stored it; O accumulates in TMEM;
+//                                stored it; O accumulates in TMEM.
+//               S_{j+2} is issued as soon as softmax j has S_j in registers
+//               and K_{j+2} has landed (before P_j V_j), so the softmax warps
+//               find S waiting and run tile after tile without a gap;
 //   warps 0-7   softmax: two warps share each 32-row quarter of TMEM and
 //               split the key columns (and the columns of O); each reads its
-//               half of S_j (tcgen05.ld), applies the causal and length
-//               masks, exchanges the row maximum with its partner, and
-//               writes P_j = exp2(S_j * scale * log2 e - m) as bf16 into the
-//               swizzled layout the P.V MMA reads.
+//               part of S_j (tcgen05.ld), applies the causal and length
+//               masks, exchanges the row maximum with its partner through two
+//               TMEM columns, and writes P_j = exp2(S_j * scale * log2 e - m)
+//               as bf16 into the swizzled layout the P.V MMA reads (the
+//               scale-and-shift and the row sums two values at a time with
+//               packed fp32 instructions; l sums the fp32 weights).
 // The reference m of a row moves only when a tile's max exceeds it by more
 // than 2^8; then that row of O (in TMEM) and its sum l are rescaled first
 // (the final O / l is exact for any reference).  V rows of keys that are out
@@ -45,6 +50,13 @@ namespace {
 
 constexpr float kNegBigP = -1e30f;
 constexpr float kRescaleSlackP = 8.0f;  // log2 units
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // Two floats rounded to bf16 (nearest even), packed low / high.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -62,15 +74,22 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + HALVES * CHUNK;         // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * HALVES * CHUNK;     // 2 stages
   static constexpr int OFF_P = OFF_V + 2 * HALVES * CHUNK;     // 2 buffers x 2 key halves
-  static constexpr int NBAR = 14;
+  static constexpr int NBAR = 16;
   static constexpr int OFF_BAR = OFF_P + 4 * CHUNK;
-  static constexpr int OFF_RED = OFF_BAR + NBAR * 8;           // [2 halves][128 rows] floats
-  static constexpr int OFF_MISC = OFF_RED + 2 * 128 * 4;
+  // Softmax: NSPLIT warps per 32-row TMEM lane quarter, each with 1/NSPLIT
+  // of the key columns of S and of the head_dim columns of O.  The parts of
+  // a row exchange their maxima (and, at the end, their sums) through TMEM
+  // columns XCOL.. (per tile parity) and LCOL.., after S and O.
+  static constexpr int NSPLIT = 2;
+  static constexpr uint32_t XCOL = 384;
+  static constexpr uint32_t LCOL = XCOL + 2 * NSPLIT;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;            // + 1024-byte alignment slack
-  static constexpr int SOFTMAX_WARPS = 8;
+  static constexpr int SOFTMAX_WARPS = 4 * NSPLIT;
   static constexpr int THREADS = (SOFTMAX_WARPS + 3) * 32;     // + K producer, MMA issuer, V producer
-  static constexpr int HC = BN / 2;                            // S columns per softmax thread
-  static constexpr int HD = D / 2;                             // O columns per softmax thread
+  static constexpr int HC = BN / NSPLIT;                       // S columns per softmax thread
+  static constexpr int HD = D / NSPLIT;                        // O columns per softmax thread
+  static_assert(HC % 32 == 0 && HD % 16 == 0 && NSPLIT <= 4, "softmax column split");
   static constexpr uint32_t TMEM_COLS = 512;                   // S0 0, S1 128, O 256
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
@@ -90,7 +109,8 @@ constexpr int kKFree = 5;    // [2] S MMA that read the K stage is done
 constexpr int kSFull = 7;    // [2] S MMA done
 constexpr int kPFull = 9;    // [2] softmax wrote P (and finished reading S)
 constexpr int kPVDone = 11;  // [2] P.V MMA done (V stage and P buffer free, O current)
-constexpr int kRed = 13;     // softmax-warp barrier (row-max exchange)
+constexpr int kSFree = 13;   // [2] softmax has S in registers (the S buffer may be refilled)
+constexpr int kRed = 15;     // softmax-warp barrier (row-max exchange)
 
 // Query tiles of request r (0 for rows that are not prefill rows or whose
 // lengths are out of range); each tile is 128 rows of one q head.
@@ -141,7 +161,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint32_t p_s = sbase + C::OFF_P;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int k) -> uint32_t { return bar0 + 8 * k; };
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [half][row]
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* tile_rec = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // r, local, found
@@ -192,7 +211,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       tile_rec[2] = r_found >= 0 ? 1 : 0;
       for (int k = 0; k <= kRed; ++k) {
         if (tile != blockIdx.x) mbar_inval(bar(k));
-        mbar_init(bar(k), (k == kPFull || k == kPFull + 1 || k == kRed) ? C::SOFTMAX_WARPS : 1);
+        const bool by_softmax = k == kPFull || k == kPFull + 1 || k == kSFree || k == kSFree + 1 ||
+                                k == kRed;
+        mbar_init(bar(k), by_softmax ? C::SOFTMAX_WARPS : 1);
       }
       fence_mbar_init();
     }
@@ -277,8 +298,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     // ========================================================== MMA issuer
     if (lane == 0) {
       auto issue_s = [&](int t) -> bool {  // S_t = Q K_t^T into S buffer t % 2
-        // S buffer t % 2 held S_{t-2}: its softmax must be done reading it.
-        if (t >= 2 && !mbar_wait(bar(kPFull + (t & 1)), ((t - 2) >> 1) & 1)) return false;
+        // S buffer t % 2 held S_{t-2}: its softmax must have read it.
+        if (t >= 2 && !mbar_wait(bar(kSFree + (t & 1)), ((t - 2) >> 1) & 1)) return false;
         if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t kst = k_s + (t & 1) * C::HALVES * C::CHUNK;
@@ -296,7 +317,16 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       bool ok = mbar_wait(bar(kQFull), 0) && issue_s(0) && (n_tiles < 2 || issue_s(1));
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int sb = j & 1;
-        ok = mbar_wait(bar(kPFull + sb), (j >> 1) & 1) && mbar_wait(bar(kVFull + sb), (j >> 1) & 1);
+        // S_{j+2} goes first when its K tile has landed (its S buffer is freed
+        // early in softmax j), so the tensor core works while softmax j runs;
+        // otherwise P_j V_j goes first and S_{j+2} waits for its K tile.
+        bool s_next = j + 2 < n_tiles;
+        if (s_next && mbar_wait(bar(kSFree + sb), (j >> 1) & 1) &&
+            mbar_try_wait(bar(kKFull + sb), ((j + 2) >> 1) & 1)) {
+          ok = issue_s(j + 2);
+          s_next = false;
+        }
+        ok = ok && mbar_wait(bar(kPFull + sb), (j >> 1) & 1) && mbar_wait(bar(kVFull + sb), (j >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -306,15 +336,15 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                     C::IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar(kPVDone + sb));
-        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        if (s_next) ok = issue_s(j + 2);
       }
       if (!ok) give_up(12);
     }
   } else {
     // ============================================================ softmax
     // Warp w serves rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-    // column half w / 4 of S and of O; thread row i = 32 (w % 4) + lane.
-    const int half = warp >> 2;
+    // column part w / 4 of S and of O; thread row i = 32 (w % 4) + lane.
+    const int part = warp >> 2;
     const int i_row = (warp & 3) * 32 + lane;
     const uint32_t tmem_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t tmem_o = 256;
@@ -323,7 +353,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     float m_ref = kNegBigP, l_run = 0.f;  // both threads of a row keep the same m_ref
     bool ok = true;
     uint32_t red_phase = 0;
-    // Barrier of the eight softmax warps (bounded; orders the red[] writes).
+    // Barrier of the softmax warps (bounded; orders the exchange writes).
     auto red_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kRed));
@@ -339,26 +369,41 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       uint32_t sraw[C::HC];
 #pragma unroll
       for (int c = 0; c < C::HC / 32; ++c)
-        tmem_ld32_async(tmem_row + sb * C::BN + half * C::HC + c * 32, sraw + 32 * c);
+        tmem_ld32_async(tmem_row + sb * C::BN + part * C::HC + c * 32, sraw + 32 * c);
       tmem_wait_ld();
-      const int key0 = j * C::BN + half * C::HC;  // key of this thread's first column
+      tc_fence_before();  // S_j is in registers: the S MMA of tile j + 2 may overwrite it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSFree + sb));
+      const int key0 = j * C::BN + part * C::HC;  // key of this thread's first column
       const bool full_tile = j * C::BN + C::BN - 1 <= ctx + row0 && j * C::BN + C::BN <= seq_len;
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
       if (full_tile) {
 #pragma unroll
-        for (int e = 0; e < C::HC; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], __uint_as_float(sraw[e]));
+        for (int e = 0; e < C::HC; e += 2)
+          mx8[(e / 2) % 8] = fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
       } else {
 #pragma unroll
-        for (int e = 0; e < C::HC; ++e)
-          mx8[e % 8] = fmaxf(mx8[e % 8], key0 + e <= limit ? __uint_as_float(sraw[e]) : -INFINITY);
+        for (int e = 0; e < C::HC; e += 2)
+          mx8[(e / 2) % 8] = fmax3(mx8[(e / 2) % 8],
+                                   key0 + e <= limit ? __uint_as_float(sraw[e]) : -INFINITY,
+                                   key0 + e + 1 <= limit ? __uint_as_float(sraw[e + 1]) : -INFINITY);
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      red[half * 128 + i_row] = mx;
+      // The row's maximum over all parts (TMEM columns of this tile parity).
+      const uint32_t xcol = tmem_row + C::XCOL + sb * C::NSPLIT;
+      tmem_st1(xcol + part, mx);
+      tc_fence_before();
       if (!(ok = red_sync())) break;
-      mx = fmaxf(mx, red[(half ^ 1) * 128 + i_row]);  // the partner's half of the row
+      tc_fence_after();
+      {
+        float xv[4];
+        tmem_ld4(xcol, xv);
+#pragma unroll
+        for (int p2 = 0; p2 < C::NSPLIT; ++p2) mx = fmaxf(mx, xv[p2]);
+      }
       const float m_tile = mx * sl2;
       const bool need = m_tile > m_ref + kRescaleSlackP;
       if (__any_sync(0xffffffffu, need)) {
@@ -372,12 +417,12 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
         const float alpha = fast_exp2(m_ref - m_new);
         if (j > 0) {
 #pragma unroll
-          for (int c = 0; c < C::HD / 32; ++c) {
-            float ov[32];
-            tmem_ld32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
+          for (int c = 0; c < C::HD / 16; ++c) {
+            float ov[16];
+            tmem_ld16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-            tmem_st32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
+            for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+            tmem_st16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
           }
         }
         l_run *= alpha;
@@ -387,34 +432,43 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       if (j >= 2)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + sb), ((j - 2) >> 1) & 1) ? 1 : 0) != 0;
       if (!ok) break;
-      float ps8[8];
+      // Weights: scale and shift two at a time (packed fp32), exponentiate,
+      // round to bf16 for the P.V product; l sums the fp32 weights.
+      float2 ps4[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+      for (int u = 0; u < 4; ++u) ps4[u] = make_float2(0.f, 0.f);
+      const float2 sl2v = make_float2(sl2, sl2), mneg = make_float2(-m_ref, -m_ref);
 #pragma unroll
       for (int c = 0; c < C::HC / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int k = c * 32 + e;
-          float p0 = fast_exp2(fmaf(__uint_as_float(sraw[k]), sl2, -m_ref));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sraw[k + 1]), sl2, -m_ref));
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sraw[k]), __uint_as_float(sraw[k + 1])),
+                                      sl2v, mneg);
+          float p0 = fast_exp2(x.x);
+          float p1 = fast_exp2(x.y);
           if (!full_tile) {
             p0 = key0 + k <= limit ? p0 : 0.f;
             p1 = key0 + k + 1 <= limit ? p1 : 0.f;
           }
           pk[e / 2] = pack_bf16x2(p0, p1);
-          ps8[(e / 2) % 8] += bf16_lo(pk[e / 2]) + bf16_hi(pk[e / 2]);  // rounded weights
+          ps4[(e / 2) % 4] = __fadd2_rn(ps4[(e / 2) % 4], make_float2(p0, p1));
         }
-        // keys half*64 + c*32 .. +31 = chunks 4c .. 4c+3 of key half `half`
+        // keys part*HC + c*32 .. +31: 16-byte chunks cb .. cb + 3 of key half kh
+        const int kfirst = part * C::HC + c * 32;
+        const int kh = kfirst >> 6, cb = (kfirst & 63) >> 3;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int chunk = c * 4 + q;
+          const int chunk = cb + q;
           const uint32_t addr =
-              p_s + (sb * 2 + half) * C::CHUNK + i_row * 128 + ((chunk ^ (i_row & 7)) * 16);
+              p_s + (sb * 2 + kh) * C::CHUNK + i_row * 128 + ((chunk ^ (i_row & 7)) * 16);
           st_shared_v4(addr, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
         }
       }
-      l_run += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      const float2 ps01 = __fadd2_rn(ps4[0], ps4[1]), ps23 = __fadd2_rn(ps4[2], ps4[3]);
+      const float2 ps = __fadd2_rn(ps01, ps23);
+      l_run += ps.x + ps.y;
       // V rows of keys past the needed range or never loaded may hold NaN.
       const int kz = kv_end - j * C::BN;  // keys [kz, BN) of this tile are unused
       if (kz < C::BN) {
@@ -439,26 +493,33 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + ((n_tiles - 1) & 1)),
                                              ((n_tiles - 1) >> 1) & 1) ? 1 : 0) != 0;
     if (ok) {
-      red[half * 128 + i_row] = l_run;
+      tc_fence_after();
+      tmem_st1(tmem_row + C::LCOL + part, l_run);
+      tc_fence_before();
       ok = red_sync();
     }
     if (ok) {
       tc_fence_after();
-      const float inv = 1.f / (l_run + red[(half ^ 1) * 128 + i_row]);
-      __nv_bfloat16* dst =
-          a.out + (static_cast<size_t>(q0 + row0 + i_row) * a.num_heads + head) * D + half * C::HD;
+      float lv[4];
+      tmem_ld4(tmem_row + C::LCOL, lv);
+      float lsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < C::HD / 32; ++c) {
-        float ov[32];
-        tmem_ld32(tmem_row + tmem_o + half * C::HD + c * 32, ov);
+      for (int p2 = 0; p2 < C::NSPLIT; ++p2) lsum += lv[p2];
+      const float inv = 1.f / lsum;
+      __nv_bfloat16* dst =
+          a.out + (static_cast<size_t>(q0 + row0 + i_row) * a.num_heads + head) * D + part * C::HD;
+#pragma unroll
+      for (int c = 0; c < C::HD / 16; ++c) {
+        float ov[16];
+        tmem_ld16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
         if (i_row < rows) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
+          for (int e = 0; e < 16; e += 8) {
             const uint4 v = make_uint4(pack_bf16x2(ov[e] * inv, ov[e + 1] * inv),
                                        pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv),
                                        pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv),
                                        pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv));
-            *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+            *reinterpret_cast<uint4*>(dst + c * 16 + e) = v;
           }
         }
       }
