@@ -189,8 +189,9 @@ pa_status pa_map_to_kernel_blocks(int32_t* kernel_tables, const int32_t* block_t
  * two partial records (m, l, O) per CTA of the decode grid.  The same
  * partition_tokens must be passed to pa_decode, on the same device (the
  * default grid size depends on its SM count).  No part of the workspace
- * needs initialising (the counters carry a per-call tag).  Returns 0 for
- * arguments pa_decode would reject.
+ * needs initialising (the counters carry a per-call tag), and a call leaves
+ * its counters at zero, so a call captured in a CUDA graph replays correctly
+ * with new inputs.  Returns 0 for arguments pa_decode would reject.
  */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t max_seq_len,

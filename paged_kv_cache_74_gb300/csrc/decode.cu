@@ -665,6 +665,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 a.out + (static_cast<size_t>(e.row) * a.num_heads + head0 + h) * D + d) =
                 __floats2bfloat162_rn(o[k][0] * inv, o[k][1] * inv);
           }
+          if (lane == 0) release_pair(counter);
         }
       }
       __syncwarp();
@@ -1217,6 +1218,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
               a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
               __floats2bfloat162_rn(o0 * inv, o1 * inv);
         }
+        if (threadIdx.x == 0)
+          release_pair(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh);
       }
     }
     if (!csync()) break;  // merge buffers are free again

@@ -85,6 +85,13 @@ __device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
   return static_cast<int>(rem + (t - big) / q);
 }
 
+// The last contributor of a pair clears its counter once it has merged:
+// every launch then leaves the counters at zero, so a launch replayed with
+// the same epoch (a CUDA graph) starts from clean counters too.
+__device__ __forceinline__ void release_pair(unsigned long long* counter) {
+  atomicExch(counter, 0ull);
+}
+
 // Registers this CTA's partial for a pair; true if it was the last of n.
 // The first exchange assumes the other n - 1 have already counted (no read
 // before it): the contributor that finishes a pair pays one round trip.

@@ -812,6 +812,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
             a.out[(static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d] =
                 __float2bfloat16_rn(acc / L);
           }
+          if (tl == 0)
+            release_pair(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh);
         }
       }
       if (!(ok = ered_sync())) break;  // the slot's m, l and last_flag are free again

@@ -211,6 +211,41 @@ def test_seq_len_beyond_bound_is_reported(cuda_lib):
     assert st[0] == 3 and st[1] == 2
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (64, 8)])
+def test_cuda_graph_replays_with_new_inputs(cuda_lib, hq, hkv):
+    """A captured decode replays correctly with new query values each time:
+    every replay equals an eager call on the same data (the pair counters of
+    the split requests start clean on every launch, also on a replay, which
+    reuses the launch's arguments)."""
+    pa = cuda_lib
+    w = wl.random_workload(47, num_seqs=16, max_len=3000, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    ws = pa.new_workspace(pa.decode_workspace_size(16, hq, hkv, 128, w.max_seq_len), "cuda")
+    out = torch.empty_like(t.q)
+    q = t.q.clone()
+    call = lambda: pa.decode(q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
+                             w.max_seq_len, w.scale, out=out, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    gen = torch.Generator(device="cuda").manual_seed(48)
+    for rep in range(3):
+        q.copy_(torch.randn(q.shape, generator=gen, device="cuda").to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = pa.decode(q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens, w.max_seq_len,
+                        w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"replay {rep}"
+
+
 def test_decode_step_in_a_cuda_graph(cuda_lib):
     """A decode step captured in a CUDA graph replays to the eager result."""
     pa = cuda_lib
