@@ -281,21 +281,33 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):
-    pin = lambda x: x.cpu().pin_memory()
-    h = {"q": pin(t.q), "key": pin(t.key), "value": pin(t.value), "bt": pin(t.block_tables),
-         "sl": pin(t.seq_lens), "qsl": pin(t.query_start_loc)}
-    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    """The step through the public API with host inputs: the step's inputs
+    (q, new K/V, block tables, seq_lens, query_start_loc) sit in one pinned
+    staging buffer, as a serving loop would assemble them, and reach the GPU
+    in one copy; the result comes back in one copy."""
+    src = {"q": t.q, "key": t.key, "value": t.value, "bt": t.block_tables,
+           "sl": t.seq_lens, "qsl": t.query_start_loc}
+    offs, total = {}, 0
+    for k, v in src.items():
+        offs[k] = total
+        total += -(-(v.numel() * v.element_size()) // 256) * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
+    d = {}
+    for k, v in src.items():
+        n = v.numel() * v.element_size()
+        stage_h[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
+        d[k] = stage_d[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
     out_h = torch.empty(t.q.shape, dtype=torch.bfloat16).pin_memory()
     ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
                                                    w.head_dim, w.max_seq_len), dev)
     out = torch.empty_like(t.q)
     slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
-    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    h2d = total
     d2h = out_h.numel() * out_h.element_size()
 
     def once():
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
+        stage_d.copy_(stage_h, non_blocking=True)
         pa.compute_slot_mapping(d["bt"], d["qsl"], d["sl"], w.block_size, w.num_blocks,
                                 w.total_q, out=slots)
         pa.reshape_and_cache(d["key"], d["value"], t.key_cache, t.value_cache, slots)
