@@ -197,10 +197,9 @@ def run_ours(args, world, rank, local):
     slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-    def step():
-        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, w.block_size,
-                                w.num_blocks, w.total_q, out=slots)
-        pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+    def step():  # slot mapping and cache write of the new tokens, one launch
+        pa.append_tokens(t.key, t.value, t.key_cache, t.value_cache, t.block_tables,
+                         t.query_start_loc, t.seq_lens, slot_mapping=slots)
 
     def attend():
         pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens, w.max_seq_len,
@@ -237,7 +236,7 @@ def run_ours(args, world, rank, local):
     tot_s, tot_bytes = aggregate_over_ranks(local_s, ab["step_bytes"] * K, world)
     value = tot_bytes / tot_s / 1e9
     dec_avg_s = statistics.mean(dec_ms) / 1e3
-    n_launch = 3  # slot mapping, reshape_and_cache, decode (one persistent kernel)
+    n_launch = 2  # append_tokens (slot mapping + cache write), decode (one persistent kernel)
 
     # e2e through the public API with pinned host buffers (H2D inputs, D2H out)
     e2e = run_e2e(pa, w, t, dev, stream, flush, args, ab, world)
@@ -256,7 +255,7 @@ def run_ours(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "num_blocks": w.num_blocks,
                    "max_seq_len": w.max_seq_len, "kv_unique_tokens": ab["kv_unique_tokens"],
-                   "step": "slot_mapping + reshape_and_cache + decode",
+                   "step": "append_tokens (slot mapping + cache write, one launch) + decode",
                    "l2": "flushed before every step (512 MiB write, outside the timed events)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(dec_avg_s * 1e6, 2),
@@ -308,9 +307,8 @@ def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):
 
     def once():
         stage_d.copy_(stage_h, non_blocking=True)
-        pa.compute_slot_mapping(d["bt"], d["qsl"], d["sl"], w.block_size, w.num_blocks,
-                                w.total_q, out=slots)
-        pa.reshape_and_cache(d["key"], d["value"], t.key_cache, t.value_cache, slots)
+        pa.append_tokens(d["key"], d["value"], t.key_cache, t.value_cache, d["bt"], d["qsl"],
+                         d["sl"], slot_mapping=slots)
         pa.decode(d["q"], t.key_cache, t.value_cache, d["bt"], d["sl"], w.max_seq_len, w.scale,
                   out=out, workspace=ws)
         out_h.copy_(out, non_blocking=True)
@@ -377,9 +375,8 @@ def extra_mixed(pa, name, dev, flush, reps=20):
     slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
 
     def step():
-        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, w.block_size,
-                                w.num_blocks, w.total_q, out=slots)
-        pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
+        pa.append_tokens(t.key, t.value, t.key_cache, t.value_cache, t.block_tables,
+                         t.query_start_loc, t.seq_lens, slot_mapping=slots)
         pa.prefill_varlen(t.q, t.key_cache, t.value_cache, t.query_start_loc, t.seq_lens,
                           t.block_tables, w.max_query_len, w.max_seq_len, w.scale, out=out,
                           workspace=ws)
@@ -402,7 +399,7 @@ def extra_mixed(pa, name, dev, flush, reps=20):
     s_pre = _time(pcall, flush, reps)
     flops = 4.0 * causal_pairs(w) * w.num_heads * w.head_dim
     res = {"us_per_step": round(s_step * 1e6, 2),
-           "step": "slot_mapping + reshape_and_cache (all new tokens) + prefill_varlen",
+           "step": "append_tokens (all new tokens) + prefill_varlen",
            "step_kv_gbs": round(ab["step_bytes"] / s_step / 1e9, 2),
            "prefill_only_us": round(s_pre * 1e6, 2),
            "prefill_tflops": round(flops / s_pre / 1e12, 2),

@@ -159,6 +159,31 @@ pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
                                   int32_t* device_status, void* stream);
 
 /*
+ * pa_append_tokens -- pa_compute_slot_mapping and pa_reshape_and_cache of
+ * this step's new tokens in one launch (the pages run them as two steps:
+ * slot_mapping, then write_to_paged_cache; fused, the cache write does not
+ * wait for a separate kernel's slots).
+ *
+ *   key, value     [total_tokens, num_kv_heads, head_dim] bf16, token rows
+ *                  key_stride / value_stride elements apart (multiples of 8)
+ *   key_cache, value_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables, query_start_loc, seq_lens  as pa_compute_slot_mapping
+ *   slot_mapping   optional [total_tokens] int64 output (NULL: not stored)
+ * Token i of request r goes to the slot pa_compute_slot_mapping gives it
+ * and its K and V rows are copied there bit for bit.  Tokens whose position
+ * or block id is out of range are skipped (slot -1) and a device error is
+ * recorded in *device_status (optional).  num_seqs == 0 or total_tokens == 0
+ * is a no-op.
+ */
+pa_status pa_append_tokens(const void* key, const void* value, int64_t key_stride,
+                           int64_t value_stride, void* key_cache, void* value_cache,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* query_start_loc, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t total_tokens, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                           int64_t* slot_mapping, int32_t* device_status, void* stream);
+
+/*
  * pa_map_to_kernel_blocks -- block tables of KV-manager blocks expanded into
  * block tables of kernel blocks ("vllm 深度解析：一切从 PagedAttention 谈起",
  * BlockTable.map_to_kernel_blocks: when the manager's block holds

@@ -26,7 +26,7 @@ ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
                "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
                "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-               "pa_reshape_and_cache_xsplit", "pa_decode_xsplit")
+               "pa_reshape_and_cache_xsplit", "pa_decode_xsplit", "pa_append_tokens")
 
 
 class PAError(RuntimeError):
@@ -61,6 +61,9 @@ def _declare(lib):
     lib.pa_decode_xsplit.restype = ctypes.c_int
     lib.pa_decode_xsplit.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                      _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp]
+    lib.pa_append_tokens.restype = ctypes.c_int
+    lib.pa_append_tokens.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _vp, _i32,
+                                     _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
     lib.pa_map_to_kernel_blocks.restype = ctypes.c_int
     lib.pa_map_to_kernel_blocks.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp]
     lib.pa_decode_workspace_size.restype = _sz
@@ -209,6 +212,33 @@ def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, nu
         _ptr(out), total_tokens, _ptr(block_tables), block_tables.shape[1], _ptr(query_start_loc),
         _ptr(seq_lens), seq_lens.shape[0], block_size, num_blocks, _ptr(status), _stream()))
     return out
+
+
+def append_tokens(key, value, key_cache, value_cache, block_tables, query_start_loc, seq_lens,
+                  slot_mapping=None, status=None):
+    """Slot mapping and cache write of the new tokens in one launch: token i of
+    request r goes to the slot compute_slot_mapping gives it (slots stored in
+    slot_mapping if given)."""
+    _cuda("key", key, torch.bfloat16)
+    _cuda("value", value, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.bfloat16)
+    _contig("value_cache", value_cache, torch.bfloat16)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("query_start_loc", query_start_loc, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    nb, bs, hkv, d = key_cache.shape
+    T = key.shape[0]
+    for name, t in (("key", key), ("value", value)):
+        if tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, {hkv}, {d}] with contiguous heads")
+    if slot_mapping is not None:
+        _contig("slot_mapping", slot_mapping, torch.int64)
+    lib = load_library()
+    _check("pa_append_tokens", lib.pa_append_tokens(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache), _ptr(value_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(query_start_loc), _ptr(seq_lens),
+        seq_lens.shape[0], T, hkv, d, bs, nb, _ptr(slot_mapping), _ptr(status), _stream()))
+    return slot_mapping
 
 
 def map_to_kernel_blocks(block_tables, blocks_per_kv_block, out=None, status=None):

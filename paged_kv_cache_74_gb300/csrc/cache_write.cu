@@ -186,6 +186,66 @@ slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
   }
 }
 
+// Slot mapping and cache write of this step's new tokens in one kernel (one
+// launch and one dependent memory round trip fewer than the two kernels
+// above in sequence): one CTA per request, its warps over the request's new
+// tokens; each warp computes its token's slot exactly as slot_mapping_kernel
+// does (optionally storing it) and copies the token's K and V rows as
+// reshape_and_cache_kernel does.
+__global__ void __launch_bounds__(kWriteWarps * 32)
+append_tokens_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                     int64_t key_stride_chunks, int64_t value_stride_chunks,
+                     uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                     const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
+                     const int32_t* __restrict__ query_start_loc,
+                     const int32_t* __restrict__ seq_lens, int total_tokens, int block_size,
+                     int num_blocks, int row_chunks, int64_t* __restrict__ slot_out,
+                     int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q0 = query_start_loc[r];
+  const int q1 = query_start_loc[r + 1];
+  const int seq_len = seq_lens[r];
+  const int q_len = q1 - q0;
+  const int64_t first_pos = static_cast<int64_t>(seq_len) - q_len;
+  const int32_t* row = block_tables + static_cast<int64_t>(r) * max_blocks_per_seq;
+  for (int i = warp; i < q_len; i += kWriteWarps) {
+    const int64_t flat = static_cast<int64_t>(q0) + i;
+    if (flat < 0 || flat >= total_tokens) {
+      if (i == 0 && lane == 0) record_error(status, PA_DEV_BAD_QUERY_LEN, r, q1);
+      continue;
+    }
+    const int64_t pos = first_pos + i;
+    const int64_t logical = pos >= 0 ? pos / block_size : -1;
+    int64_t slot = -1;
+    if (logical < 0 || logical >= max_blocks_per_seq) {
+      if (lane == 0) record_error(status, PA_DEV_BAD_SEQ_LEN, r, seq_len);
+    } else {
+      const int32_t phys = row[logical];
+      if (phys < 0 || phys >= num_blocks) {
+        if (lane == 0) record_error(status, PA_DEV_BAD_BLOCK_ID, r, phys);
+      } else {
+        slot = static_cast<int64_t>(phys) * block_size + (pos - logical * block_size);
+      }
+    }
+    if (slot_out != nullptr && lane == 0) slot_out[flat] = slot;
+    if (slot < 0) continue;
+    const uint4* ks = key + flat * key_stride_chunks;
+    const uint4* vs = value + flat * value_stride_chunks;
+    uint4* kd = key_cache + slot * row_chunks;
+    uint4* vd = value_cache + slot * row_chunks;
+    for (int c = lane; c < row_chunks; c += 32) {
+      const uint4 kv = __ldg(ks + c);
+      const uint4 vv = __ldg(vs + c);
+      kd[c] = kv;
+      vd[c] = vv;
+    }
+  }
+}
+
 // One thread per manager-block entry writes its k kernel-block ids.
 __global__ void __launch_bounds__(256)
 map_kernel_blocks_kernel(int32_t* __restrict__ out, const int32_t* __restrict__ in, int64_t n,
@@ -249,6 +309,21 @@ cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, 
                            key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
                            static_cast<uint16_t*>(value_cache), slot_mapping, num_tokens,
                            num_kv_heads, head_dim, block_size, num_slots, status);
+}
+
+cudaError_t launch_append_tokens(const void* key, const void* value, int64_t key_stride,
+                                 int64_t value_stride, void* key_cache, void* value_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* query_start_loc, const int32_t* seq_lens,
+                                 int num_seqs, int total_tokens, int block_size, int num_blocks,
+                                 int row_elems, int64_t* slot_mapping, int32_t* status,
+                                 cudaStream_t stream) {
+  return launch_overlapped(append_tokens_kernel, dim3(num_seqs), dim3(kWriteWarps * 32), 0, stream,
+                           static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                           key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
+                           static_cast<uint4*>(value_cache), block_tables, max_blocks_per_seq,
+                           query_start_loc, seq_lens, total_tokens, block_size, num_blocks,
+                           row_elems / 8, slot_mapping, status);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,

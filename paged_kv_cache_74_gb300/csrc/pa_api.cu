@@ -477,6 +477,39 @@ pa_status pa_compute_slot_mapping(int64_t* slot_mapping, int32_t total_tokens,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_append_tokens(const void* key, const void* value, int64_t key_stride,
+                           int64_t value_stride, void* key_cache, void* value_cache,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* query_start_loc, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t total_tokens, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                           int64_t* slot_mapping, int32_t* device_status, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || num_kv_heads < 1 || num_blocks < 1 ||
+      block_size < 1 || max_blocks_per_seq < 1)
+    return PA_ERR_INVALID;
+  if (head_dim < 8 || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_tokens == 0) return PA_OK;
+  if (num_seqs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+  if (!key || !value || !key_cache || !value_cache || !block_tables || !query_start_loc ||
+      !seq_lens)
+    return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(block_tables, 4) || !aligned(query_start_loc, 4) ||
+      !aligned(seq_lens, 4) || (slot_mapping && !aligned(slot_mapping, 8)) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+    return PA_ERR_INVALID;
+  const cudaError_t e = launch_append_tokens(
+      key, value, key_stride, value_stride, key_cache, value_cache, block_tables,
+      max_blocks_per_seq, query_start_loc, seq_lens, num_seqs, total_tokens, block_size,
+      num_blocks, static_cast<int>(row), slot_mapping, device_status,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_map_to_kernel_blocks(int32_t* kernel_tables, const int32_t* block_tables,
                                   int32_t num_rows, int32_t max_blocks_per_row,
                                   int32_t blocks_per_kv_block, int32_t* device_status,

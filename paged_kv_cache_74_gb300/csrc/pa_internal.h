@@ -143,6 +143,15 @@ cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, 
                                             cudaStream_t stream);
 cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
                                      int32_t* status, cudaStream_t stream);
+// Slot mapping and token-major cache write of the new tokens in one kernel
+// (slot_mapping may be null: the slots are not stored).
+cudaError_t launch_append_tokens(const void* key, const void* value, int64_t key_stride,
+                                 int64_t value_stride, void* key_cache, void* value_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* query_start_loc, const int32_t* seq_lens,
+                                 int num_seqs, int total_tokens, int block_size, int num_blocks,
+                                 int row_elems, int64_t* slot_mapping, int32_t* status,
+                                 cudaStream_t stream);
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, int total_tokens, const int32_t* block_tables,
                                 int max_blocks_per_seq, const int32_t* query_start_loc,
                                 const int32_t* seq_lens, int num_seqs, int block_size,

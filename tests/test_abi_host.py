@@ -217,3 +217,21 @@ def test_reshape_and_cache_xsplit_validation(lib):
     assert call(vs=1028) == 1
     assert call(n=-1) == 1
     assert call(d=12) == 2
+
+
+def test_append_tokens_validation(lib):
+    vp = ctypes.c_void_p
+    call = lambda **k: lib.pa_append_tokens(
+        vp(k.get("key", A)), vp(k.get("value", A)), k.get("ks", 1024), k.get("vs", 1024),
+        vp(k.get("kc", A)), vp(k.get("vc", A)), vp(k.get("bt", A)), k.get("mb", 4),
+        vp(k.get("qsl", A)), vp(k.get("sl", A)), k.get("ns", 4), k.get("n", 4), 8,
+        k.get("d", 128), 16, 64, vp(k.get("sm", 0)), vp(0), vp(0))
+    assert call(n=0) == 0 and call(ns=0) == 0      # nothing to do, nothing launched
+    assert call(key=0) == 1
+    assert call(bt=0) == 1
+    assert call(qsl=A + 2) == 1
+    assert call(sm=A + 4) == 1
+    assert call(ks=1000) == 1
+    assert call(ns=-1) == 1
+    assert call(mb=0) == 1
+    assert call(d=12) == 2

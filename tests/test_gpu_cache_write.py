@@ -129,3 +129,48 @@ def test_slot_write_with_larger_blocks(cuda_lib, oracle, B):
     pa.reshape_and_cache(t.key, t.value, t.key_cache, t.value_cache, slots)
     np.testing.assert_array_equal(bits(t.key_cache), kc)
     np.testing.assert_array_equal(bits(t.value_cache), vc)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "mixed_chunked_prefill", "random_varlen",
+                                  "llama8b_decode_b64"])
+def test_append_tokens_equals_slot_mapping_then_write(cuda_lib, oracle, name):
+    """The fused launch gives the oracle's slots and the oracle's whole pool
+    after its slot mapping and cache write, bit for bit."""
+    pa = cuda_lib
+    w = _slot_case(name)
+    t = wl.make_tensors(w, device="cuda")
+    ref_slots = oracle.slot_mapping(w.block_tables, w.query_start_loc, w.seq_lens, w.block_size)
+    kc, vc = oracle.reshape_and_cache(bits(t.key), bits(t.value), bits(t.key_cache),
+                                      bits(t.value_cache), ref_slots)
+    slots = torch.full((w.total_q,), -7, dtype=torch.int64, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pa.append_tokens(t.key, t.value, t.key_cache, t.value_cache, t.block_tables,
+                     t.query_start_loc, t.seq_lens, slot_mapping=slots, status=status)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy(), ref_slots)
+    np.testing.assert_array_equal(bits(t.key_cache), kc)
+    np.testing.assert_array_equal(bits(t.value_cache), vc)
+    assert pa.device_status(status)[0] == 0
+
+
+def test_append_tokens_without_slot_output_and_bad_block(cuda_lib, oracle):
+    """No slot output requested; a request whose block id is out of range is
+    reported and its token skipped, the others are written."""
+    pa = cuda_lib
+    w = wl.tiny_decode()
+    t = wl.make_tensors(w, device="cuda")
+    bt = t.block_tables.clone()
+    L = int(w.seq_lens[2])
+    bt[2, (L - 1) // 16] = w.num_blocks + 9  # the block of request 2's new token
+    good = w.block_tables.copy()
+    ref_slots = oracle.slot_mapping(good, w.query_start_loc, w.seq_lens, 16)
+    ref_slots[2] = -1
+    kc, vc = oracle.reshape_and_cache(bits(t.key), bits(t.value), bits(t.key_cache),
+                                      bits(t.value_cache), ref_slots)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pa.append_tokens(t.key, t.value, t.key_cache, t.value_cache, bt, t.query_start_loc,
+                     t.seq_lens, status=status)
+    st = pa.device_status(status)
+    assert st[0] == 2 and st[1] == 2 and st[2] == w.num_blocks + 9
+    np.testing.assert_array_equal(bits(t.key_cache), kc)
+    np.testing.assert_array_equal(bits(t.value_cache), vc)
