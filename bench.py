@@ -4,8 +4,11 @@
 One step = the whole hot path for one decode batch: the slot mapping of
 the batch's new tokens, their reshape_and_cache write, and paged decode
 attention (split-KV partitions + merge).  Inputs are seeded synthetic
-tensors of the named workload, resident in HBM; L2 is flushed (a 512 MiB
-write) before every step, outside the timed events.
+tensors of the named workload, resident in HBM; L2 is flushed before every
+step, outside the timed events: a 512 MiB write, then a 256 MiB read that
+writes the flush's dirty lines back to HBM, so that L2 holds clean,
+unrelated lines when the step starts (the decode's time with the dirty
+lines of the write alone is reported beside it).
 
 Prints ONE JSON line (rank 0).  `value` is KV GB/s: the step's algorithmic
 bytes (each distinct K/V token the attention must read once, plus q, out,
@@ -180,6 +183,27 @@ def barrier(world):
         dist.barrier()
 
 
+class L2Flush:
+    """Evicts the timed inputs from L2 between steps.
+
+    A 512 MiB write (four times the 129 MB L2), then a 256 MiB read of
+    another buffer.  The write alone leaves L2 full of dirty lines whose
+    write-back the next kernel would pay for inside its timed region; after
+    the read L2 holds clean lines of unrelated data.  `dirty=True` skips
+    the read (the write-only flush)."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self.dirty = False
+
+    def __call__(self):
+        self.w.add_(1)
+        if not self.dirty:
+            torch.sum(self.r, dim=0, out=self.sink)
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, world, rank, local):
@@ -195,7 +219,7 @@ def run_ours(args, world, rank, local):
                                                    w.head_dim, w.max_seq_len), dev)
     out = torch.empty_like(t.q)
     slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step():  # slot mapping and cache write of the new tokens, one launch
         pa.append_tokens(t.key, t.value, t.key_cache, t.value_cache, t.block_tables,
@@ -206,7 +230,7 @@ def run_ours(args, world, rank, local):
                   w.scale, out=out, workspace=ws)
 
     for _ in range(args.warmup):
-        flush.add_(1)
+        flush()
         step()
         attend()
     torch.cuda.synchronize(dev)
@@ -220,7 +244,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.add_(1)
+        flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -240,6 +264,10 @@ def run_ours(args, world, rank, local):
 
     # e2e through the public API with pinned host buffers (H2D inputs, D2H out)
     e2e = run_e2e(pa, w, t, dev, stream, flush, args, ab, world)
+    # The decode call after the write-only flush (L2 full of dirty lines).
+    flush.dirty = True
+    dirty_s = _time(attend, flush, min(K, 100))
+    flush.dirty = False
 
     peak, peak_src = measured_peaks()
     achieved = ab["decode_bytes"] / dec_avg_s / 1e9
@@ -256,9 +284,11 @@ def run_ours(args, world, rank, local):
                    "block_size": w.block_size, "num_blocks": w.num_blocks,
                    "max_seq_len": w.max_seq_len, "kv_unique_tokens": ab["kv_unique_tokens"],
                    "step": "append_tokens (slot mapping + cache write, one launch) + decode",
-                   "l2": "flushed before every step (512 MiB write, outside the timed events)",
+                   "l2": ("flushed before every step, outside the timed events: 512 MiB "
+                          "write, then a 256 MiB read that writes its dirty lines back"),
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(dec_avg_s * 1e6, 2),
+        "us_per_call_dirty_l2": round(dirty_s * 1e6, 2),
         "decode_kv_gbs": round(ab["kv_bytes"] / dec_avg_s / 1e9, 2),
         "wall_ms_per_step": round(wall / K * 1e3, 4),
         "roofline": {"bound": "hbm",
@@ -314,13 +344,13 @@ def run_e2e(pa, w, t, dev, stream, flush, args, ab, world):
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
-        flush.add_(1)
+        flush()
         once()
     torch.cuda.synchronize(dev)
     K = max(1, args.steps // 2)
     ts = []
     for _ in range(K):
-        flush.add_(1)
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -347,11 +377,11 @@ def causal_pairs(w: wl.Workload) -> int:
 
 def _time(call, flush, reps):
     for _ in range(3):
-        flush.add_(1)
+        flush()
         call()
     ms = []
     for _ in range(reps):
-        flush.add_(1)
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -426,11 +456,11 @@ def extra_decode_fp8(pa, name, dev, flush, reps=20):
     call = lambda: pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
                                  k_scale, v_scale, out=out, workspace=ws)
     for _ in range(3):
-        flush.add_(1)
+        flush()
         call()
     ms = []
     for _ in range(reps):
-        flush.add_(1)
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -480,11 +510,11 @@ def extra_decode(pa, name, dev, flush, reps=20):
         call = lambda: pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
                                  w.max_seq_len, w.scale, out=out, workspace=ws)
     for _ in range(3):
-        flush.add_(1)
+        flush()
         call()
     ms = []
     for _ in range(reps):
-        flush.add_(1)
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
