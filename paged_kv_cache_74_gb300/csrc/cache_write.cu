@@ -17,6 +17,8 @@
 // Both are launched so that they (and the attention launch after them) may
 // be scheduled while the previous kernel in the stream finishes; each waits
 // for that kernel before it touches global memory.
+#include <algorithm>
+
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -188,10 +190,16 @@ slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
 
 // Slot mapping and cache write of this step's new tokens in one kernel (one
 // launch and one dependent memory round trip fewer than the two kernels
-// above in sequence): one CTA per request, its warps over the request's new
-// tokens; each warp computes its token's slot exactly as slot_mapping_kernel
-// does (optionally storing it) and copies the token's K and V rows as
+// above in sequence).  CTA (r, y) serves request r; its warps take the
+// request's new tokens y * kWriteWarps + warp, then every gridDim.y *
+// kWriteWarps-th one after it, so a long chunk is spread over gridDim.y CTAs.
+// For each token a warp first loads the token's K and V rows (they depend
+// only on its row), then computes its slot exactly as slot_mapping_kernel
+// does (optionally storing it) and writes the rows there as
 // reshape_and_cache_kernel does.
+constexpr int kAppendChunksPerLane = 4;  // 16-byte chunks of a row held per lane per pass
+constexpr int kAppendMaxSplit = 16;      // CTAs per request, at most
+
 __global__ void __launch_bounds__(kWriteWarps * 32)
 append_tokens_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                      int64_t key_stride_chunks, int64_t value_stride_chunks,
@@ -208,15 +216,29 @@ append_tokens_kernel(const uint4* __restrict__ key, const uint4* __restrict__ va
   const int lane = threadIdx.x & 31;
   const int q0 = query_start_loc[r];
   const int q1 = query_start_loc[r + 1];
-  const int seq_len = seq_lens[r];
   const int q_len = q1 - q0;
+  const int first = static_cast<int>(blockIdx.y) * kWriteWarps + warp;
+  if (first >= q_len) return;
+  const int seq_len = seq_lens[r];
   const int64_t first_pos = static_cast<int64_t>(seq_len) - q_len;
   const int32_t* row = block_tables + static_cast<int64_t>(r) * max_blocks_per_seq;
-  for (int i = warp; i < q_len; i += kWriteWarps) {
+  for (int i = first; i < q_len; i += gridDim.y * kWriteWarps) {
     const int64_t flat = static_cast<int64_t>(q0) + i;
     if (flat < 0 || flat >= total_tokens) {
       if (i == 0 && lane == 0) record_error(status, PA_DEV_BAD_QUERY_LEN, r, q1);
       continue;
+    }
+    const uint4* ks = key + flat * key_stride_chunks;
+    const uint4* vs = value + flat * value_stride_chunks;
+    // The rows' first pass is loaded before the slot is known.
+    uint4 kb[kAppendChunksPerLane], vb[kAppendChunksPerLane];
+#pragma unroll
+    for (int k = 0; k < kAppendChunksPerLane; ++k) {
+      const int c = lane + 32 * k;
+      if (c < row_chunks) {
+        kb[k] = __ldg(ks + c);
+        vb[k] = __ldg(vs + c);
+      }
     }
     const int64_t pos = first_pos + i;
     const int64_t logical = pos >= 0 ? pos / block_size : -1;
@@ -233,11 +255,17 @@ append_tokens_kernel(const uint4* __restrict__ key, const uint4* __restrict__ va
     }
     if (slot_out != nullptr && lane == 0) slot_out[flat] = slot;
     if (slot < 0) continue;
-    const uint4* ks = key + flat * key_stride_chunks;
-    const uint4* vs = value + flat * value_stride_chunks;
     uint4* kd = key_cache + slot * row_chunks;
     uint4* vd = value_cache + slot * row_chunks;
-    for (int c = lane; c < row_chunks; c += 32) {
+#pragma unroll
+    for (int k = 0; k < kAppendChunksPerLane; ++k) {
+      const int c = lane + 32 * k;
+      if (c < row_chunks) {
+        kd[c] = kb[k];
+        vd[c] = vb[k];
+      }
+    }
+    for (int c = lane + 32 * kAppendChunksPerLane; c < row_chunks; c += 32) {  // longer rows
       const uint4 kv = __ldg(ks + c);
       const uint4 vv = __ldg(vs + c);
       kd[c] = kv;
@@ -318,7 +346,15 @@ cudaError_t launch_append_tokens(const void* key, const void* value, int64_t key
                                  int num_seqs, int total_tokens, int block_size, int num_blocks,
                                  int row_elems, int64_t* slot_mapping, int32_t* status,
                                  cudaStream_t stream) {
-  return launch_overlapped(append_tokens_kernel, dim3(num_seqs), dim3(kWriteWarps * 32), 0, stream,
+  // Every request has at least one new token in the usual step, so none has
+  // more than total_tokens - num_seqs + 1: that many tokens, kWriteWarps per
+  // CTA, set the split of a request over CTAs (a longer request is still
+  // served, its CTAs looping over it).
+  const int64_t longest = std::max<int64_t>(1, static_cast<int64_t>(total_tokens) - num_seqs + 1);
+  const int split = static_cast<int>(
+      std::min<int64_t>(kAppendMaxSplit, (longest + kWriteWarps - 1) / kWriteWarps));
+  return launch_overlapped(append_tokens_kernel, dim3(num_seqs, split), dim3(kWriteWarps * 32), 0,
+                           stream,
                            static_cast<const uint4*>(key), static_cast<const uint4*>(value),
                            key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
                            static_cast<uint4*>(value_cache), block_tables, max_blocks_per_seq,
