@@ -295,7 +295,10 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
  * pa_reshape_and_cache_fp8: key t contributes decoded(K_t) * k_scale and
  * value t decoded(V_t) * v_scale ("vLLM 深度解析（二）", section 3.2,
  * fp8::scaled_convert inside the K/V load).  Same arguments, workspace
- * (pa_decode_workspace_size) and results as pa_decode otherwise.
+ * (pa_decode_workspace_size) and results as pa_decode otherwise.  The
+ * products run on the tensor cores in f16: e4m3 K and V convert to f16
+ * exactly; q and the softmax weights are rounded to f16 (q saturates at
+ * +-65504).
  * Supported: 1 to 4 q heads per kv head (PA_ERR_UNSUPPORTED beyond);
  * k_scale and v_scale finite and > 0 (else PA_ERR_INVALID).
  */

@@ -26,31 +26,29 @@
 // * One CTA serves every q head of a kv head, so each K/V byte is read from
 //   HBM once.  A producer warp reads block ids 32 at a time and issues one
 //   TMA tensor load per (block, kv head) tile of K and of V (16 tokens x
-//   head_dim, 4 KB at head_dim 128) into an 8-stage ring guarded by
-//   mbarriers, writes each stage's block index and flags next to it, and
+//   head_dim, 4 KB at head_dim 128 in bf16) into an 8-stage ring (16
+//   stages of the half-size e4m3 tiles) guarded by mbarriers, writes each stage's block index and flags next to it, and
 //   prefetches each segment's q with a bulk copy into a double buffer.
-// * bf16 caches: two consumer warps take alternate stages.  A warp computes
-//   S^T = K q^T (16 tokens x 8 columns of q heads, padding heads zero) and
+// * Two consumer warps take alternate stages.  A warp computes S^T = K q^T
+//   (16 tokens x 8 columns of q heads, padding heads zero) and
 //   O^T += V^T P^T with warp-level m16n8k16 tensor-core products: K and V
 //   fragments come straight from the stage with ldmatrix (the copies land
-//   128-byte swizzled, so those reads are conflict-free), the weights P go
-//   from the score fragments to the operand fragments with movmatrix.  A
-//   tile costs about 0.5 us, so the stage is released soon after it lands.
-//   P is rounded to bf16 for the product and l sums the rounded weights.
-//   At a segment end the two warps merge their states through shared
-//   memory and hand the result to an epilogue warp, which writes the output
-//   or the partial, bumps the pair counter and, as last contributor, merges
-//   the partials; the consumers go straight on to the next segment.
-// * e4m3 caches (KV8): four consumer warps on CUDA cores.  T lanes share a
-//   token; each lane holds a 16-byte slice of head_dim of q (fp32, pre-scaled
-//   by scale * log2 e) and of the output accumulators, computes partial q.k
-//   for all q heads with packed fp32 FMAs (fma.rn.f32x2), and the partials
-//   are summed through a shared-memory transpose that reuses the warp's own
-//   K tile; the warps merge their states in shared memory at segment ends.
-// * In both, the running max is rescaled lazily, only when a new score
-//   exceeds the reference by more than 2^8 (O = A / l is exact for any
-//   reference), and each segment is padded to a multiple of the consumer
-//   count in stages, so all consumers finish it together.
+//   swizzled, so those reads are conflict-free), the weights P go from the
+//   score fragments to the operand fragments with movmatrix.  A tile costs
+//   about 0.5 us, so the stage is released soon after it lands.  bf16
+//   caches: bf16 products, P rounded to bf16.  e4m3 caches (KV8): the K
+//   and V bytes are converted to f16 in registers (exact: every e4m3 value
+//   is an f16 value), q and P are rounded to f16, and the head_dim order of
+//   the fragments follows the bytes ldmatrix delivers (see below).  l sums
+//   the rounded weights.  At a segment end the two warps merge their
+//   states through shared memory and hand the result to an epilogue warp,
+//   which writes the output or the partial, bumps the pair counter and, as
+//   last contributor, merges the partials; the consumers go straight on to
+//   the next segment.
+// * The running max is rescaled lazily, only when a new score exceeds the
+//   reference by more than 2^8 (O = A / l is exact for any reference), and
+//   each segment is padded to a multiple of the consumer count in stages,
+//   so both consumers finish it together.
 // * The x-split layout of section 3.2.1 (XS) runs through the bf16 path with
 //   other TMA views: K as 8-token x 16-byte rows (128-byte swizzled), V as
 //   V^T [head_dim][16 tokens] (32-byte swizzled), which is already the
@@ -74,69 +72,43 @@ constexpr int kEndSeg = 3;   // segment kind handed to the epilogue warp: no mor
 
 template <int D, int GMAX, bool KV8 = false, bool XS = false>
 struct DecodeCfg {
-  static constexpr int T = (D == 128 && GMAX >= 4) ? 16 : 8;  // lanes per token
-  static constexpr int NG = 32 / T;                            // token groups per warp
-  static constexpr int NT = kBlockSize / NG;                   // tokens per group per block
-  static constexpr int CPL = D / 8 / T;                        // 16-byte chunks per lane per row
-  static constexpr int EL = CPL * 8;                           // head_dim elements per lane
-  static constexpr int EP = EL / 2;                            // ... as float2 pairs
-  static constexpr int SB = (NT * GMAX > 32) ? 32 / GMAX : NT; // tokens per sub-batch
-  static constexpr int NSB = NT / SB;
-  static constexpr int V = SB * GMAX;                          // partial scores per lane per sub-batch
-  static constexpr int VPL = V >= T ? V / T : 1;               // whole scores per lane after the sum
-  static constexpr int REP = V >= T ? 1 : T / V;               // lanes holding the same score
-  static constexpr int LPH = T / GMAX;                         // lanes of a group per head
-  static constexpr int CH = V / 4;                             // 16-byte chunks per transpose row
-  // Consumer warps: two tensor-core consumers keep up with the K/V stream
-  // (one 16-token tile takes ~0.5 us), four fp32 ones.
-  static constexpr int NC = KV8 ? 4 : 2;
-  static constexpr int MINB = (!KV8 || GMAX * EL <= 32) ? 3 : 2;  // CTAs per SM
+  // Two consumer warps take alternate stages; each computes q.k and p.v of
+  // a 16-token tile as warp-level m16n8k16 tensor-core products (tokens /
+  // head_dim x 8 padded q heads), bf16 for bf16 caches, f16 for e4m3 ones.
+  // One 16-token tile takes ~0.5 us, so two warps keep up with the stream.
+  static constexpr int NC = 2;
+  static constexpr int MINB = 3;                               // CTAs per SM
   static constexpr int ELT = KV8 ? 1 : 2;                      // bytes per K/V element (e4m3 / bf16)
-  // bf16 caches: q.k and p.v as warp-level m16n8k16 tensor-core products
-  // (tokens / head_dim x 8 padded q heads); e4m3 caches: fp32 FMAs.
-  static constexpr bool MMA = !KV8;
   static constexpr int KS = D / 16;                            // 16-wide steps of head_dim
   static constexpr int TILE = kBlockSize * D * ELT;            // bytes of one (block, kv head) tile
-  // The partial-score transpose (32 rows of V floats) reuses the warp's own
-  // K tile once its q.k products are done, when it fits and no later
-  // sub-batch still needs K; otherwise each warp gets a dedicated buffer.
-  static constexpr bool XPOSE_IN_K = 32 * CH * 16 <= TILE && NSB == 1;
-  // A multiple of NC (see below).  e4m3 tiles are half as large: more of
-  // them fit, and more tokens are in flight.
-  static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 ? (XPOSE_IN_K ? 4 : 3) : 2) / 2;
+  // A multiple of NC (see below).  e4m3 tiles are half as large: twice as
+  // many fit, and the same bytes are in flight.
+  static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 ? 2 : 1);
   // shared memory carve-up (bytes)
   static constexpr int RING = STAGES * 2 * TILE;
-  static constexpr int XPOSE = (MMA || XPOSE_IN_K) ? 0 : NC * 32 * CH * 16;
-  static constexpr int PBUF = MMA ? 0 : NC * NG * V * 4;       // per-warp weights
-  // The tensor-core consumers hand every finished segment to an epilogue
-  // warp (partial write, pair counter, last-contributor merge), so the
-  // global round trips of a segment end never stall the K/V stream.
-  static constexpr bool EPI = MMA;
+  // The consumers hand every finished segment to an epilogue warp (partial
+  // write, pair counter, last-contributor merge), so the global round trips
+  // of a segment end never stall the K/V stream.
   static constexpr int WF = GMAX * D + 2 * GMAX;               // floats of one (O, m, l) record
   static constexpr int HF = WF + 8;                            // ... plus the segment record
-  static constexpr int COMB = MMA ? 0 : NC * GMAX * (D + 2) * 4;  // cross-warp merge
-  static constexpr int PC = PBUF > COMB ? PBUF : COMB;         // weights and merge alias
-  static constexpr int HAND = EPI ? (HF * 4 + 15) / 16 * 16 : 0;  // the segment handed over
+  static constexpr int HAND = (HF * 4 + 15) / 16 * 16;         // the segment handed over
   static constexpr int QBUF = 2 * GMAX * D * 2;                // q of two segments
-  static constexpr int OFF_XPOSE = RING;
-  static constexpr int OFF_PC = OFF_XPOSE + XPOSE;
-  static constexpr int OFF_HAND = OFF_PC + PC;
+  static constexpr int OFF_HAND = RING;
   static constexpr int OFF_Q = OFF_HAND + HAND;
   static constexpr int OFF_META = OFF_Q + QBUF;                // int2 per stage
   static constexpr int OFF_SEG = OFF_META + STAGES * 8;        // 2 segment records
   static constexpr int OFF_BAR = OFF_SEG + 2 * 32;  // full, empty, qfull, qempty, sync, hfull, hempty
   static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 7) * 8;
   static constexpr int SMEM = OFF_MISC + 32;
-  static constexpr int THREADS = (NC + 1 + (EPI ? 1 : 0)) * 32;
+  static constexpr int THREADS = (NC + 2) * 32;                // + producer and epilogue warps
   // Stage i goes to consumer warp i % NC.  With STAGES a multiple of NC a
   // stage is only ever used by one warp, so when a warp waits on a stage
   // the barrier is at most one phase behind and the parity wait is exact.
   static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
-  static_assert(CPL >= 1 && GMAX <= T && NT % SB == 0 && V >= 4 && V <= 32, "decode shape");
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
-  static_assert(!XS || MMA, "the x-split layout is read by the tensor-core consumers");
-  static_assert(!MMA || (GMAX <= 8 && NC == 2), "an m16n8k16 product serves at most 8 q heads");
+  static_assert(!XS || !KV8, "the x-split layout holds bf16");
+  static_assert(GMAX <= 8 && NC == 2, "an m16n8k16 product serves at most 8 q heads");
   // Bulk-copy destinations (ring, q) 16-byte aligned; the segment records'
   // 64-bit fields 8-byte aligned.
   static_assert(RING % 1024 == 0 && OFF_HAND % 16 == 0 && OFF_Q % 16 == 0 && OFF_META % 8 == 0 &&
@@ -157,38 +129,6 @@ struct SegInfo {
   int kvh;
 };
 static_assert(sizeof(SegInfo) <= 32, "segment record");
-
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Eight consecutive K or V elements of one row, as stored: bf16 (16 bytes)
-// or e4m3 (8 bytes).  pair(e) returns elements 2e, 2e + 1 as fp32; every
-// e4m3 value is exact in f16, so the conversion loses nothing.
-template <bool KV8>
-struct Row8 {
-  uint4 w;
-  __device__ __forceinline__ void load(uint32_t addr) { w = ld_shared_v4(addr); }
-  __device__ __forceinline__ void clear() { w = make_uint4(0u, 0u, 0u, 0u); }
-  __device__ __forceinline__ float2 pair(int e) const {
-    return unpack2(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
-  }
-};
-template <>
-struct Row8<true> {
-  uint2 w;
-  __device__ __forceinline__ void load(uint32_t addr) {
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w.x), "=r"(w.y) : "r"(addr));
-  }
-  __device__ __forceinline__ void clear() { w = make_uint2(0u, 0u); }
-  __device__ __forceinline__ float2 pair(int e) const {
-    const uint32_t word = e < 2 ? w.x : w.y;
-    const uint16_t two = static_cast<uint16_t>(e & 1 ? word >> 16 : word & 0xffffu);
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  }
-};
 
 // ---- x-split layout ("vLLM 深度解析（二）：PagedAttention 核心机制", section
 // 3.2.1): K [blocks, kv heads, head_dim / 8, block, 8] (8 bf16 = 16 bytes
@@ -256,6 +196,50 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// ---- e4m3 caches on the tensor cores (f16 products, fp32 accumulate).
+// Every e4m3 value is exact in f16, so K and V lose nothing in the
+// conversion; q and the weights are rounded to f16 (|q| saturates at 65504).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two e4m3 values (low byte first) as f16x2 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+  return h2;
+}
+// Bytes (b0, b2, b1, b3) of x.
+__device__ __forceinline__ uint32_t bytes_0213(uint32_t x) {
+  uint32_t y;
+  asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t h2;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(hi), "f"(lo));
+  return h2;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+// A K or V stage of an e4m3 cache: [16 tokens][head_dim bytes] through a
+// swizzled copy (128-byte rows: 16-byte chunk c of token t at c ^ (t % 8);
+// 64-byte rows: at c ^ ((t / 2) % 4)), so ldmatrix rows of 8 tokens hit 8
+// distinct bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t e8_offset(int t, int c) {
+  const int sw = D == 128 ? (t & 7) : ((t >> 1) & 3);
+  return static_cast<uint32_t>(t * D + ((c ^ sw) * 16));
+}
+
 template <int D, int GMAX, bool KV8, bool XS>
 __global__ void __launch_bounds__(DecodeCfg<D, GMAX, KV8, XS>::THREADS,
                                   DecodeCfg<D, GMAX, KV8, XS>::MINB)
@@ -270,7 +254,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   int2* meta = reinterpret_cast<int2*>(smem + C::OFF_META);
   SegInfo* seginfo = reinterpret_cast<SegInfo*>(smem + C::OFF_SEG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
-  volatile int* last_flag = abort_flag + 1;
   long long* total_tiles = reinterpret_cast<long long*>(smem + C::OFF_MISC + 8);
   const uint32_t ring_s = smem_u32(smem);
   const uint32_t full0 = smem_u32(smem + C::OFF_BAR);
@@ -285,7 +268,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // TMA destinations must be 128-byte aligned (1024 for the 128-byte
   // swizzled boxes of the bf16 paths); the dynamic shared-memory base always
   // is on this GPU, but never issue a copy if it were not.
-  if (ring_s & (C::MMA ? 1023 : 127)) {
+  if (ring_s & 1023) {
     griddep_wait();
     if (threadIdx.x == 0) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 6);
     return;
@@ -304,7 +287,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     mbar_init(hfull0, 1);
     mbar_init(hempty0, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -479,11 +461,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
               } else {
                 // Row num_blocks * block_size is wholly out of bounds: TMA fills zeros.
                 const int row0 = bad ? a.num_blocks * a.block_size : tile_row(a, phys, b + j);
-                if constexpr (C::MMA) {  // grouped view: 8-token groups, 128-byte swizzle
+                if constexpr (!KV8) {  // grouped view: 8-token groups, 128-byte swizzle
                   tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 0, 0, row0 / 8, kvh, policy);
                   tma_load_5d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, 0, 0, row0 / 8, kvh,
                               policy);
-                } else {
+                } else {  // e4m3: swizzled 3-D view, one tile per copy
                   tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
                   tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
                 }
@@ -538,7 +520,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     return;
   }
 
-  if (C::EPI && warp == C::NC + 1) {
+  if (warp == C::NC + 1) {
     // ================================================================ epilogue
     // Finishes each segment handed over by the consumers: the bf16 output of
     // a whole (request, kv head) pair, or the partial of a shared pair, its
@@ -675,31 +657,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   // ================================================================ consumers
-  const int g = lane / C::T;
-  const int li = lane % C::T;
-  float* pbuf = reinterpret_cast<float*>(smem + C::OFF_PC) + warp * (C::NG * C::V);
-  float* comb_o = reinterpret_cast<float*>(smem + C::OFF_PC);  // [NC][GMAX][D] (merge time)
-  float* comb_ml = comb_o + C::NC * GMAX * D;                   // [NC][GMAX][2]
-  const int idx0 = (li * C::V) / C::T;
-  const int my_h = idx0 / C::SB;
-  const int my_k0 = idx0 % C::SB;
-  const bool l_owner = (li % C::REP) == 0;
-
-  float2 q2[GMAX][C::EP];
-  float2 o2[GMAX][C::EP];
-  float my_m = kNegBig;  // running max (log2 units) of this lane's head, same on all its lanes
-  float my_l = 0.f;      // this lane's share of the running exp-sum
-  // Tensor-core consumers: lane = 4 fg + ft in the m16n8k16 fragments; the
-  // 8 columns of every product are q heads (those >= group are zero).
+  // lane = 4 fg + ft in the m16n8k16 fragments; the 8 columns of every
+  // product are q heads (those >= group are zero).
   const int fg = lane >> 2, ft = lane & 3;
   uint32_t qf[C::KS][2];  // q^T fragments: head fg, head_dim 16 ks + 2 ft (+1, +8, +9)
-  float om[C::KS][4];     // O^T: head_dim 16 m + fg (+8) x heads 2 ft, 2 ft + 1
+  float om[C::KS][4];     // O^T: head_dim 16 m + fg (+8) (e4m3: 16 m + 2 fg (+1)) x heads 2 ft (+1)
   float mh[2] = {kNegBig, kNegBig};  // running max (log2 units) of heads 2 ft, 2 ft + 1
   float lh[2] = {0.f, 0.f};          // this lane's share of their exp-sums
   SegInfo si{};
   bool fresh = true;
   int seg = 0;
-  // Barrier of the four consumer warps: lane 0 of each warp arrives, every
+  // Barrier of the consumer warps: lane 0 of each warp arrives, every
   // lane waits (bounded); orders the warps' shared-memory writes before the
   // reads after it.  Returns false (and flags an abort) on a timeout.
   uint32_t cphase = 0;
@@ -729,7 +697,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const int2 m = meta[s];
     if (m.y & kDone) {
-      if (C::EPI && warp == 0) {  // tell the epilogue warp that no segment follows
+      if (warp == 0) {  // tell the epilogue warp that no segment follows
         const int ok = (seg < 1 || mbar_wait(hempty0, (seg - 1) & 1)) ? 1 : 0;
         if (__all_sync(0xffffffffu, ok)) {
           if (lane == 0) {
@@ -758,52 +726,36 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       si = seginfo[slot];
       const uint32_t qs = qbuf_s + slot * (GMAX * D * 2);
-      if constexpr (C::MMA) {
-        // q stays bf16 (the products are exact in fp32); the scale is
-        // applied to the fp32 scores.
+      // q stays bf16 (f16 for e4m3 caches; the products are exact in fp32);
+      // the scale is applied to the fp32 scores.
 #pragma unroll
-        for (int ks = 0; ks < C::KS; ++ks)
+      for (int ks = 0; ks < C::KS; ++ks)
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            qf[ks][j] = fg < a.group ? ld_shared_u32(qs + (fg * D + 16 * ks + 8 * j + 2 * ft) * 2) : 0u;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
-#pragma unroll
-        for (int mt = 0; mt < C::KS; ++mt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) om[mt][i] = 0.f;
-        mh[0] = mh[1] = kNegBig;
-        lh[0] = lh[1] = 0.f;
-        fresh = false;
-      }
-#pragma unroll
-      for (int h = 0; h < (C::MMA ? 0 : GMAX); ++h) {
-#pragma unroll
-        for (int j = 0; j < C::CPL; ++j) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (h < a.group) w = ld_shared_v4(qs + (h * D + (li + C::T * j) * 8) * 2);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack2(ws[e]);
-            q2[h][j * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+        for (int j = 0; j < 2; ++j) {
+          if constexpr (KV8) {
+            // head_dim in the order the e4m3 K fragments hold it: product
+            // index 2 ft (+1) is element 4 ft (+1) of the 16-wide step,
+            // 2 ft + 8 (+9) is element 4 ft + 2 (+3).
+            const uint32_t w =
+                fg < a.group ? ld_shared_u32(qs + (fg * D + 16 * ks + 4 * ft + 2 * j) * 2) : 0u;
+            qf[ks][j] = pack_f16x2_sat(bf16_lo(w), bf16_hi(w));
+          } else {
+            qf[ks][j] =
+                fg < a.group ? ld_shared_u32(qs + (fg * D + 16 * ks + 8 * j + 2 * ft) * 2) : 0u;
           }
         }
-      }
-      if constexpr (!C::MMA) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty0 + 8 * slot);
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h)
+      for (int mt = 0; mt < C::KS; ++mt)
 #pragma unroll
-          for (int e = 0; e < C::EP; ++e) o2[h][e] = make_float2(0.f, 0.f);
-        my_m = kNegBig;
-        my_l = 0.f;
-        fresh = false;
-      }
+        for (int i = 0; i < 4; ++i) om[mt][i] = 0.f;
+      mh[0] = mh[1] = kNegBig;
+      lh[0] = lh[1] = 0.f;
+      fresh = false;
     }
 
-    if (!(m.y & kSkip) && C::MMA) {
+    if (!(m.y & kSkip)) {
       const uint32_t kt = ring_s + (2 * s) * C::TILE;
       const uint32_t vt = kt + C::TILE;
       const int tok0 = m.x * kBlockSize;
@@ -812,12 +764,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       // ldmatrix: tokens 8 (mi % 2) .. + 7, head_dim chunk 2 ks + mi / 2.
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       const int ka_t = ((lane >> 3) & 1) * 8 + (lane & 7);
+      if constexpr (KV8) {
+        // One ldmatrix covers two 16-wide steps of e4m3 head_dim: matrix mi
+        // = tokens 8 (mi % 2) .., chunk 2 kp + mi / 2; a lane's register
+        // holds elements 4 ft .. 4 ft + 3 of its token's chunk.
 #pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        uint32_t af[4];
-        const int c = 2 * ks + (lane >> 4);
-        ldsm_x4(kt + (XS ? xs_k_offset(ka_t, c) : grp_offset<D>(ka_t, c)), af);
-        mma_16816(sacc, af, qf[ks][0], qf[ks][1]);
+        for (int kp = 0; kp < C::KS / 2; ++kp) {
+          uint32_t r8[4];
+          ldsm_x4(kt + e8_offset<D>(ka_t, 2 * kp + (lane >> 4)), r8);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t af[4] = {e4m3x2_f16x2(r8[2 * h]), e4m3x2_f16x2(r8[2 * h + 1]),
+                                    e4m3x2_f16x2(r8[2 * h] >> 16), e4m3x2_f16x2(r8[2 * h + 1] >> 16)};
+            mma_16816_f16(sacc, af, qf[2 * kp + h][0], qf[2 * kp + h][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+          uint32_t af[4];
+          const int c = 2 * ks + (lane >> 4);
+          ldsm_x4(kt + (XS ? xs_k_offset(ka_t, c) : grp_offset<D>(ka_t, c)), af);
+          mma_16816(sacc, af, qf[ks][0], qf[ks][1]);
+        }
       }
       // Scores in log2 units: (token fg (+8), head 2 ft (+1)); tokens past
       // seq_len and padding heads get weight 0.
@@ -851,13 +820,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           om[mt][3] *= al[1];
         }
       }
-      // Weights rounded to bf16 for the product; l sums the rounded values.
+      // Weights rounded to bf16 (f16 for e4m3 caches) for the product; l
+      // sums the rounded values.
 #pragma unroll
       for (int i = 0; i < 4; ++i) p[i] = fast_exp2(p[i] - mh[i & 1]);
-      const uint32_t pk0 = pack_bf16x2(p[0], p[1]);  // token fg:     heads 2 ft, 2 ft + 1
-      const uint32_t pk1 = pack_bf16x2(p[2], p[3]);  // token fg + 8
-      lh[0] += bf16_lo(pk0) + bf16_lo(pk1);
-      lh[1] += bf16_hi(pk0) + bf16_hi(pk1);
+      uint32_t pk0, pk1;
+      if constexpr (KV8) {
+        pk0 = pack_f16x2_sat(p[0], p[1]);  // token fg:     heads 2 ft, 2 ft + 1
+        pk1 = pack_f16x2_sat(p[2], p[3]);  // token fg + 8
+        lh[0] += f16_lo(pk0) + f16_lo(pk1);
+        lh[1] += f16_hi(pk0) + f16_hi(pk1);
+      } else {
+        pk0 = pack_bf16x2(p[0], p[1]);
+        pk1 = pack_bf16x2(p[2], p[3]);
+        lh[0] += bf16_lo(pk0) + bf16_lo(pk1);
+        lh[1] += bf16_hi(pk0) + bf16_hi(pk1);
+      }
       const uint32_t pb0 = movmatrix_t(pk0);  // P^T: tokens 2 ft, 2 ft + 1 of head fg
       const uint32_t pb1 = movmatrix_t(pk1);  // tokens 2 ft + 8, 2 ft + 9
       // O^T (head_dim x 8 heads) += V^T P^T, 16 head_dim rows per product.
@@ -870,6 +848,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         vm89 = (t0 + 8 < seq_len ? 0x0000ffffu : 0u) | (t0 + 9 < seq_len ? 0xffff0000u : 0u);
       }
       const int va_r = lane & 7, va_m = lane >> 3;
+      if constexpr (KV8) {
+        // e4m3 V^T: matrix mi = tokens 8 (mi % 2) .., chunk 2 mp + mi / 2,
+        // read transposed in 16-bit units; a lane's register holds (token
+        // 2 ft, 2 ft + 1) x (head_dim 2 fg, 2 fg + 1) of the chunk.  Byte
+        // permute + conversion give row fg (head_dim 2 fg) and row fg + 8
+        // (head_dim 2 fg + 1) of the 16-row product, tokens 2 ft, 2 ft + 1.
+#pragma unroll
+        for (int mp = 0; mp < C::KS / 2; ++mp) {
+          uint32_t r8[4];
+          ldsm_x4_t(vt + e8_offset<D>(8 * (va_m & 1) + va_r, 2 * mp + (va_m >> 1)), r8);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t lo = bytes_0213(r8[2 * h]), hi = bytes_0213(r8[2 * h + 1]);
+            uint32_t af[4] = {e4m3x2_f16x2(lo), e4m3x2_f16x2(lo >> 16), e4m3x2_f16x2(hi),
+                              e4m3x2_f16x2(hi >> 16)};
+            af[0] &= vm01;
+            af[1] &= vm01;
+            af[2] &= vm89;
+            af[3] &= vm89;
+            mma_16816_f16(om[2 * mp + h], af, pb0, pb1);
+          }
+        }
+      } else {
 #pragma unroll
       for (int mt = 0; mt < C::KS; ++mt) {
         uint32_t af[4];
@@ -886,343 +887,86 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         af[3] &= vm89;
         mma_16816(om[mt], af, pb0, pb1);
       }
-    } else if (!(m.y & kSkip)) {
-      const uint32_t kt = ring_s + (2 * s) * C::TILE;
-      const uint32_t vt = kt + C::TILE;
-      const int tok0 = m.x * kBlockSize;
-      const int seq_len = si.seq_len;
-      const bool tail = tok0 + kBlockSize > seq_len;
-      const bool head_real = my_h < a.group;
-      // Transpose rows: lane L's 16-byte chunk c sits at chunk c ^ (L % CH)
-      // of row L (bank-conflict-free 16-byte stores from 8 lanes).
-      float* xpose = C::XPOSE_IN_K
-                         ? reinterpret_cast<float*>(smem + (2 * s) * C::TILE)
-                         : reinterpret_cast<float*>(smem + C::OFF_XPOSE) + warp * (32 * C::CH * 4);
-#pragma unroll
-      for (int sb = 0; sb < C::NSB; ++sb) {
-        // Partial q.k over this lane's head_dim slice, every head, SB tokens.
-        float x[C::V];
-#pragma unroll
-        for (int kk = 0; kk < C::SB; ++kk) {
-          const int t = (sb * C::SB + kk) * C::NG + g;
-          Row8<KV8> kw[C::CPL];
-#pragma unroll
-          for (int j = 0; j < C::CPL; ++j) kw[j].load(kt + (t * D + (li + C::T * j) * 8) * C::ELT);
-          float2 kf[C::CPL][4];
-#pragma unroll
-          for (int j = 0; j < C::CPL; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) kf[j][e] = kw[j].pair(e);
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < C::CPL; ++j) {
-              acc = __ffma2_rn(q2[h][j * 4 + 0], kf[j][0], acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 1], kf[j][1], acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 2], kf[j][2], acc);
-              acc = __ffma2_rn(q2[h][j * 4 + 3], kf[j][3], acc);
-            }
-            x[h * C::SB + kk] = acc.x + acc.y;
-          }
-        }
-        // Sum the partials of the T lanes of a group through shared memory:
-        // lane L writes row L; each lane then adds up its VPL columns.
-        __syncwarp();  // every lane is done reading K before rows overwrite it
-#pragma unroll
-        for (int c = 0; c < C::CH; ++c)
-          *reinterpret_cast<float4*>(xpose + lane * (C::CH * 4) + ((c ^ (lane % C::CH)) * 4)) =
-              make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-        __syncwarp();
-        // Four independent partial sums keep the add chain short.
-        float sc4[4][C::VPL];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
-#pragma unroll
-          for (int u = 0; u < C::VPL; ++u) sc4[k4][u] = 0.f;
-#pragma unroll
-        for (int l2 = 0; l2 < C::T; ++l2) {
-          const int rr = g * C::T + l2;
-          const float* src =
-              xpose + rr * (C::CH * 4) + (((idx0 / 4) ^ (rr % C::CH)) * 4) + (idx0 % 4);
-          if constexpr (C::VPL == 2) {
-            const float2 v2 = *reinterpret_cast<const float2*>(src);
-            sc4[l2 % 4][0] += v2.x;
-            sc4[l2 % 4][1] += v2.y;
-          } else {
-#pragma unroll
-            for (int u = 0; u < C::VPL; ++u) sc4[l2 % 4][u] += src[u];
-          }
-        }
-        float sc[C::VPL];
-#pragma unroll
-        for (int u = 0; u < C::VPL; ++u) sc[u] = (sc4[0][u] + sc4[1][u]) + (sc4[2][u] + sc4[3][u]);
-        // Mask tokens past seq_len (and padding heads), then the lazy max.
-        float smax = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < C::VPL; ++u) {
-          const int t = (sb * C::SB + my_k0 + u) * C::NG + g;
-          const bool ok = head_real && (tok0 + t < seq_len);
-          sc[u] = ok ? sc[u] : -INFINITY;
-          smax = fmaxf(smax, sc[u]);
-        }
-        if (__any_sync(0xffffffffu, smax > my_m + kRescaleSlack)) {
-          float bm = smax;
-#pragma unroll
-          for (int bb = 1; bb < C::LPH; bb <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, bb));
-#pragma unroll
-          for (int bb = C::T; bb < 32; bb <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, bb));
-          const float m_new = fmaxf(my_m, bm);
-          const float alpha = fast_exp2(my_m - m_new);
-          my_l *= alpha;
-          my_m = m_new;
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            const float ah = __shfl_sync(0xffffffffu, alpha, h * C::LPH);
-            const float2 a2 = make_float2(ah, ah);
-#pragma unroll
-            for (int e = 0; e < C::EP; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
-          }
-        }
-        float psum = 0.f;
-#pragma unroll
-        for (int u = 0; u < C::VPL; ++u) {
-          sc[u] = fast_exp2(sc[u] - my_m);
-          psum += sc[u];
-        }
-        my_l += l_owner ? psum : 0.f;
-        // Hand the weights to every lane of the group.
-#pragma unroll
-        for (int u = 0; u < C::VPL; ++u) pbuf[g * C::V + idx0 + u] = sc[u];
-        __syncwarp();
-        float p[C::V];
-#pragma unroll
-        for (int v = 0; v < C::V; v += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(pbuf + g * C::V + v);
-          p[v] = f.x;
-          p[v + 1] = f.y;
-          p[v + 2] = f.z;
-          p[v + 3] = f.w;
-        }
-        // A += p v over this sub-batch's tokens.  In the last block of a
-        // request the V rows past seq_len may hold NaN and are replaced by 0.
-        auto pv = [&](bool check) {
-#pragma unroll
-          for (int kk = 0; kk < C::SB; ++kk) {
-            const int t = (sb * C::SB + kk) * C::NG + g;
-            Row8<KV8> vw[C::CPL];
-#pragma unroll
-            for (int j = 0; j < C::CPL; ++j) vw[j].load(vt + (t * D + (li + C::T * j) * 8) * C::ELT);
-            if (check && tok0 + t >= seq_len) {
-#pragma unroll
-              for (int j = 0; j < C::CPL; ++j) vw[j].clear();
-            }
-            float2 vf[C::CPL][4];
-#pragma unroll
-            for (int j = 0; j < C::CPL; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) vf[j][e] = vw[j].pair(e);
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-              const float2 pp = make_float2(p[h * C::SB + kk], p[h * C::SB + kk]);
-#pragma unroll
-              for (int j = 0; j < C::CPL; ++j) {
-                o2[h][j * 4 + 0] = __ffma2_rn(pp, vf[j][0], o2[h][j * 4 + 0]);
-                o2[h][j * 4 + 1] = __ffma2_rn(pp, vf[j][1], o2[h][j * 4 + 1]);
-                o2[h][j * 4 + 2] = __ffma2_rn(pp, vf[j][2], o2[h][j * 4 + 2]);
-                o2[h][j * 4 + 3] = __ffma2_rn(pp, vf[j][3], o2[h][j * 4 + 3]);
-              }
-            }
-          }
-        };
-        if (tail) pv(true); else pv(false);
-        __syncwarp();  // the next sub-batch rewrites the scratch rows
       }
-      // The stage is refilled by TMA (async proxy) after this release; order
-      // this warp's generic-proxy writes into it (the transpose) before that.
-      if (C::XPOSE_IN_K) fence_proxy_async_smem();
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     if (!(m.y & kLastRow)) continue;
 
-    if constexpr (C::EPI) {
-      // ======================== end of segment: merge the two warps' states
-      // and hand the result to the epilogue warp.  Record: O^T accumulators
-      // [GMAX][D], (m, l) per head, the segment record; each lane writes and
-      // reads only its own (head, d) places.
-      float ls[2] = {lh[0], lh[1]};
+    // ======================== end of segment: merge the two warps' states
+    // and hand the result to the epilogue warp.  Record: O^T accumulators
+    // [GMAX][D], (m, l) per head, the segment record; each lane writes and
+    // reads only its own (head, d) places.
+    float ls[2] = {lh[0], lh[1]};
 #pragma unroll
-      for (int bb = 4; bb < 32; bb <<= 1) {
-        ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], bb);
-        ls[1] += __shfl_xor_sync(0xffffffffu, ls[1], bb);
-      }
-      float* hrec = reinterpret_cast<float*>(smem + C::OFF_HAND);
-      auto put = [&]() {
+    for (int bb = 4; bb < 32; bb <<= 1) {
+      ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], bb);
+      ls[1] += __shfl_xor_sync(0xffffffffu, ls[1], bb);
+    }
+    float* hrec = reinterpret_cast<float*>(smem + C::OFF_HAND);
+    // head_dim row of accumulator om[mt][i] (the e4m3 V^T fragments
+    // interleave the rows: product row fg is 2 fg, row fg + 8 is 2 fg + 1).
+    auto orow = [&](int mt, int i) -> int {
+      return KV8 ? 16 * mt + 2 * fg + (i >> 1) : 16 * mt + fg + 8 * (i >> 1);
+    };
+    auto put = [&]() {
 #pragma unroll
-        for (int mt = 0; mt < C::KS; ++mt)
+      for (int mt = 0; mt < C::KS; ++mt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int h = 2 * ft + (i & 1);
-            if (h < a.group) hrec[h * D + 16 * mt + fg + 8 * (i >> 1)] = om[mt][i];
-          }
-        if (fg == 0) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = 2 * ft + e;
-            if (h < a.group) {
-              hrec[GMAX * D + 2 * h] = mh[e];
-              hrec[GMAX * D + 2 * h + 1] = ls[e];
-            }
-          }
+        for (int i = 0; i < 4; ++i) {
+          const int h = 2 * ft + (i & 1);
+          if (h < a.group) hrec[h * D + orow(mt, i)] = om[mt][i];
         }
-      };
-      if (warp == 1) {
-        // The record was last handed over one segment ago.
-        const int ok = (seg < 1 || mbar_wait(hempty0, (seg - 1) & 1)) ? 1 : 0;
-        if (__all_sync(0xffffffffu, ok)) {
-          put();
-        } else if (lane == 0) {
-          record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 9);
-          *abort_flag = 1;
-        }
-      }
-      if (!csync() || *abort_flag) break;
-      if (warp == 0) {
-        // Merge warp 1's state into this warp's, then hand the segment over.
-        float wa[2], wb[2];
+      if (fg == 0) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int h = 2 * ft + e;
-          const float mo = h < a.group ? hrec[GMAX * D + 2 * h] : kNegBig;
-          const float lo = h < a.group ? hrec[GMAX * D + 2 * h + 1] : 0.f;
-          const float mx = fmaxf(mh[e], mo);
-          wa[e] = fast_exp2(mh[e] - mx);
-          wb[e] = fast_exp2(mo - mx);
-          mh[e] = mx;
-          ls[e] = ls[e] * wa[e] + lo * wb[e];
-        }
-#pragma unroll
-        for (int mt = 0; mt < C::KS; ++mt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int h = 2 * ft + (i & 1);
-            const float ov = h < a.group ? hrec[h * D + 16 * mt + fg + 8 * (i >> 1)] : 0.f;
-            om[mt][i] = om[mt][i] * wa[i & 1] + ov * wb[i & 1];
+          if (h < a.group) {
+            hrec[GMAX * D + 2 * h] = mh[e];
+            hrec[GMAX * D + 2 * h + 1] = ls[e];
           }
-        __syncwarp();  // every lane has read the (m, l) entries before they change
+        }
+      }
+    };
+    if (warp == 1) {
+      // The record was last handed over one segment ago.
+      const int ok = (seg < 1 || mbar_wait(hempty0, (seg - 1) & 1)) ? 1 : 0;
+      if (__all_sync(0xffffffffu, ok)) {
         put();
-        if (lane == 0) *reinterpret_cast<SegInfo*>(hrec + C::WF) = si;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(hfull0);
+      } else if (lane == 0) {
+        record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 9);
+        *abort_flag = 1;
       }
-      fresh = true;
-      ++seg;
-      continue;
     }
-
-    // ============================================ end of segment: merge
-    float lsum = my_l;
+    if (!csync() || *abort_flag) break;
+    if (warp == 0) {
+      // Merge warp 1's state into this warp's, then hand the segment over.
+      float wa[2], wb[2];
 #pragma unroll
-    for (int bb = 1; bb < C::LPH; bb <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, bb);
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * ft + e;
+        const float mo = h < a.group ? hrec[GMAX * D + 2 * h] : kNegBig;
+        const float lo = h < a.group ? hrec[GMAX * D + 2 * h + 1] : 0.f;
+        const float mx = fmaxf(mh[e], mo);
+        wa[e] = fast_exp2(mh[e] - mx);
+        wb[e] = fast_exp2(mo - mx);
+        mh[e] = mx;
+        ls[e] = ls[e] * wa[e] + lo * wb[e];
+      }
 #pragma unroll
-    for (int bb = C::T; bb < 32; bb <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, bb);
+      for (int mt = 0; mt < C::KS; ++mt)
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-      for (int e = 0; e < C::EP; ++e)
-#pragma unroll
-        for (int bb = C::T; bb < 32; bb <<= 1) {
-          o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, bb);
-          o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, bb);
+        for (int i = 0; i < 4; ++i) {
+          const int h = 2 * ft + (i & 1);
+          const float ov = h < a.group ? hrec[h * D + orow(mt, i)] : 0.f;
+          om[mt][i] = om[mt][i] * wa[i & 1] + ov * wb[i & 1];
         }
-    if (!csync()) break;  // all warps are done with the weight buffers
-    if (g == 0) {
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-        for (int j = 0; j < C::CPL; ++j) {
-          float4* dst = reinterpret_cast<float4*>(comb_o + (warp * GMAX + h) * D + (li + C::T * j) * 8);
-          dst[0] = make_float4(o2[h][j * 4 + 0].x, o2[h][j * 4 + 0].y, o2[h][j * 4 + 1].x,
-                               o2[h][j * 4 + 1].y);
-          dst[1] = make_float4(o2[h][j * 4 + 2].x, o2[h][j * 4 + 2].y, o2[h][j * 4 + 3].x,
-                               o2[h][j * 4 + 3].y);
-        }
-      if (li % C::LPH == 0) {
-        comb_ml[(warp * GMAX + my_h) * 2 + 0] = my_m;
-        comb_ml[(warp * GMAX + my_h) * 2 + 1] = lsum;
-      }
+      __syncwarp();  // every lane has read the (m, l) entries before they change
+      put();
+      if (lane == 0) *reinterpret_cast<SegInfo*>(hrec + C::WF) = si;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hfull0);
     }
-    if (!csync()) break;
-    const int head0 = si.kvh * a.group;
-    const int pslot = si.kind == kTail ? 1 : 0;
-    for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
-      const int h = it / (D / 2);
-      const int d = (it % (D / 2)) * 2;
-      float M = kNegBig;
-#pragma unroll
-      for (int w = 0; w < C::NC; ++w) M = fmaxf(M, comb_ml[(w * GMAX + h) * 2]);
-      float L = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < C::NC; ++w) {
-        const float wt = fast_exp2(comb_ml[(w * GMAX + h) * 2] - M);
-        L = fmaf(wt, comb_ml[(w * GMAX + h) * 2 + 1], L);
-        const float2 ov = *reinterpret_cast<const float2*>(comb_o + (w * GMAX + h) * D + d);
-        o0 = fmaf(wt, ov.x, o0);
-        o1 = fmaf(wt, ov.y, o1);
-      }
-      const float inv = a.v_scale / L;  // v_scale: the e4m3 cache's V scale, else 1
-      if (si.kind == kWhole) {
-        *reinterpret_cast<__nv_bfloat162*>(
-            a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
-            __floats2bfloat162_rn(o0 * inv, o1 * inv);
-      } else {
-        const size_t rec = (static_cast<size_t>(cta) * 2 + pslot) * a.group + h;
-        *reinterpret_cast<float2*>(a.part_o + rec * D + d) = make_float2(o0 * inv, o1 * inv);
-        if (d == 0) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(M, L);
-      }
-    }
-    if (si.kind != kWhole) {
-      // Publish the partial; the last of the pair's contributors merges them.
-      __threadfence();
-      if (!csync()) break;
-      const long long W = *total_tiles;
-      const int c0 = cta_of_tile(W, a.num_ctas, si.t0);
-      const int c1 = cta_of_tile(W, a.num_ctas, si.t0 + si.nblk - 1);
-      if (threadIdx.x == 0)
-        *last_flag = contribute(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh,
-                                a.epoch, c1 - c0 + 1, a.status, si.r) ? 1 : 0;
-      if (!csync()) break;
-      if (*last_flag) {
-        __threadfence();
-        for (int it = threadIdx.x; it < a.group * (D / 2); it += C::NC * 32) {
-          const int h = it / (D / 2);
-          const int d = (it % (D / 2)) * 2;
-          float M = kNegBig;
-          for (int c = c0; c <= c1; ++c) {
-            const size_t rec = (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * a.group + h;
-            M = fmaxf(M, __ldcg(a.part_ml + rec * 2));
-          }
-          float L = 0.f, o0 = 0.f, o1 = 0.f;
-          for (int c = c0; c <= c1; ++c) {
-            const size_t rec = (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * a.group + h;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec * 2));
-            const float wt = ml.y * fast_exp2(ml.x - M);
-            const float2 ov = __ldcg(reinterpret_cast<const float2*>(a.part_o + rec * D + d));
-            L += wt;
-            o0 = fmaf(wt, ov.x, o0);
-            o1 = fmaf(wt, ov.y, o1);
-          }
-          const float inv = 1.f / L;
-          *reinterpret_cast<__nv_bfloat162*>(
-              a.out + (static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + d) =
-              __floats2bfloat162_rn(o0 * inv, o1 * inv);
-        }
-        if (threadIdx.x == 0)
-          release_pair(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh);
-      }
-    }
-    if (!csync()) break;  // merge buffers are free again
     fresh = true;
     ++seg;
   }

@@ -80,25 +80,26 @@ int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group,
   return std::max<int64_t>(1, std::min(resident, (upper + kMinTilesPerCta - 1) / kMinTilesPerCta));
 }
 
-// The K or V cache as a 3-D tensor [slots][kv_heads][head_dim] (innermost
-// first for TMA: {head_dim, kv_heads, slots}); one box is one (block, kv head)
-// tile of 16 tokens x head_dim.
-bool make_cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
-                    int head_dim, bool e4m3 = false) {
+// An e4m3 K or V cache as a 3-D tensor [slots][kv_heads][head_dim] (innermost
+// first for TMA: {head_dim, kv_heads, slots}); one box is one (block, kv
+// head) tile of 16 tokens x head_dim bytes, swizzled (128-byte rows at
+// head_dim 128, 64-byte rows at 64) so that the decode's ldmatrix reads of
+// 8 token rows are free of bank conflicts.
+bool make_cache_map_e4m3(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                         int head_dim) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t elt = e4m3 ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
                               static_cast<cuuint64_t>(num_kv_heads),
                               static_cast<cuuint64_t>(num_blocks) * kBlockSize};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elt,
-                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * elt};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim),
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(kBlockSize)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
-  return enc(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-             const_cast<void*>(cache), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -348,8 +349,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
         !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
-  } else if (!make_cache_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim, true) ||
-             !make_cache_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim, true)) {
+  } else if (!make_cache_map_e4m3(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
+             !make_cache_map_e4m3(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim)) {
     return PA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
