@@ -46,9 +46,9 @@ PROFILED_TRAFFIC: dict = {
     # profiles/decode_llama8b_decode_b64.md: 636.349440 MB read + 3.913472 MB written
     "llama8b_decode_b64": {"bytes": 640262912, "src": "decode.cu",
                            "src_sha": "46e05a512c7eb607"},
-    # profiles/decode_tc_prefix_shared_decode_b256.md: 940.124672 MB read + 5.124096 MB written
-    "prefix_shared_decode_b256": {"bytes": 945248768, "src": "decode_tc.cu",
-                                  "src_sha": "d6c3902b37680ecf"},
+    # profiles/decode_tc_prefix_shared_decode_b256.md: 939.966208 MB read + 5.458176 MB written
+    "prefix_shared_decode_b256": {"bytes": 945424384, "src": "decode_tc.cu",
+                                  "src_sha": "3987d8d08ae62a6a"},
 }
 
 

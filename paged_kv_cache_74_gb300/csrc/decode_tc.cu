@@ -30,7 +30,8 @@
 // S MMA is done, its V stage as soon as its P.V MMA is done.
 //
 // Warp roles (352 threads):
-//   warp 0      K producer: walks this CTA's tile range (decode_common.cuh),
+//   warp 0      K producer: walks this CTA's range of whole 128-token
+//               chunks (a split by cost: see kCostSeg),
 //               writes one record per segment (the run of one pair's blocks
 //               in the range), loads that segment's q and the K of every
 //               chunk of 8 blocks, and leaves a record per chunk (block rows,
@@ -136,8 +137,20 @@ struct TcSeg {
   int r;
   int kvh;
   long long t0;  // number of the pair's first chunk
+  long long c0;  // split cost at which the pair's first chunk starts (see kCostSeg)
 };
 static_assert(sizeof(TcSeg) <= 48, "segment record");
+
+// The batch's chunks are split over the CTAs by cost, not by count: every
+// chunk costs kCostChunk and every (request, kv head) segment another
+// kCostSeg.  A segment start (q load, first S before any softmax, partial
+// last chunk, hand-off) costs about two chunks: on the 70B-shaped
+// shared-prefix batch with equal chunk counts a CTA took 216 us + 1.84 us
+// per segment of its range (R^2 0.92, 3 to 42 segments per CTA), and the
+// decode took 286.8 / 268 / 256 / 254 / 261 us with kCostSeg = 0 / 8 / 13 /
+// 18 / 24.
+constexpr int kCostChunk = 8;
+constexpr int kCostSeg = 16;
 
 // Order-preserving map between fp32 and int32 (its own inverse): signed
 // integer comparison of the keys orders the floats (NaN excepted).
@@ -180,6 +193,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   volatile long long* total_tiles = reinterpret_cast<volatile long long*>(smem + C::OFF_MISC + 24);
   volatile int* n_segs_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 32);
   volatile int* n_v_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 36);
+  volatile long long* total_cost = reinterpret_cast<volatile long long*>(smem + C::OFF_MISC + 40);
+  volatile int* cost_chunk = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);
   int* recs = reinterpret_cast<int*>(smem + C::OFF_REC);  // [NREC][12]: V rows of 8 blocks, kv head, blocks
 
   if (tid == 0) {
@@ -197,6 +212,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     *n_segs_issued = 0;
     *n_v_issued = 0;
     *total_tiles = 0;
+    *total_cost = 0;
+    *cost_chunk = 1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -221,7 +238,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     // loads gives the batch's tile total.
     constexpr int kReqCache = 8;
     int c_nb[kReqCache], c_len[kReqCache], c_row[kReqCache];
-    long long nb_sum = 0;
+    long long nb_sum = 0, nreq = 0;  // chunks per kv head; requests with chunks
 #pragma unroll
     for (int k = 0; k < kReqCache; ++k) {
       const int r = 32 * k + lane;
@@ -233,17 +250,86 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       c_len[k] = lv;
       c_row[k] = rv;
       nb_sum += (c_nb[k] + C::CB - 1) / C::CB;  // chunks
+      nreq += c_nb[k] > 0 ? 1 : 0;
     }
     for (int r = 32 * kReqCache + lane; r < a.num_seqs; r += 32) {
       int len, row;
-      nb_sum += (request_blocks(a, r, &len, &row) + C::CB - 1) / C::CB;
+      const int nbv = request_blocks(a, r, &len, &row);
+      nb_sum += (nbv + C::CB - 1) / C::CB;
+      nreq += nbv > 0 ? 1 : 0;
     }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
+    for (int o = 16; o >= 1; o >>= 1) {
+      nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
+      nreq += __shfl_xor_sync(0xffffffffu, nreq, o);
+    }
     const long long W = nb_sum * a.num_kv_heads;
-    const long long lo = W > 0 ? range_lo(W, a.num_ctas, cta) : 0;
-    const long long hi = W > 0 ? range_lo(W, a.num_ctas, cta + 1) : 0;
-    if (lane == 0) *total_tiles = W;
+    // Split by cost when every CTA's share spans at least one whole gap
+    // between chunk starts (so no CTA's range is empty); else by chunks.
+    const long long Cw = a.num_kv_heads * (kCostChunk * nb_sum + kCostSeg * nreq);
+    const bool by_cost = W > 0 && Cw / a.num_ctas >= kCostChunk + kCostSeg;
+    const int cu_chunk = by_cost ? kCostChunk : 1;
+    const int cu_seg = by_cost ? kCostSeg : 0;
+    const long long Ctot = by_cost ? Cw : W;
+    // (blocks) -> chunks of a request (every lane); cached for the first
+    // 32 kReqCache requests.
+    auto req_nb = [&](int r) -> int {
+      int nbv = 0;
+      if (r < 32 * kReqCache) {
+#pragma unroll
+        for (int m = 0; m < kReqCache; ++m)
+          if (m == (r >> 5)) nbv = c_nb[m];
+        nbv = __shfl_sync(0xffffffffu, nbv, r & 31);
+      } else if (r < a.num_seqs) {
+        int lv, rv;
+        nbv = request_blocks(a, r, &lv, &rv);
+      }
+      return nbv;
+    };
+    // The first chunk whose cost start is >= x (whole warp): the chunk u of
+    // (request r, kv head h, chunk j) starts at cost_base(r) + h (cu_chunk
+    // nc_r + cu_seg) + cu_seg + cu_chunk j.
+    auto chunk_at_cost = [&](long long x) -> long long {
+      long long cb = 0, chb = 0;
+      for (int rc = 0; rc < a.num_seqs; rc += 32) {
+        const int r = rc + lane;
+        const int nc = (req_nb(r) + C::CB - 1) / C::CB;
+        const long long ct = nc > 0 ? a.num_kv_heads * (static_cast<long long>(cu_chunk) * nc + cu_seg) : 0;
+        const long long nt = static_cast<long long>(nc) * a.num_kv_heads;
+        long long ic = ct, in = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long vc = __shfl_up_sync(0xffffffffu, ic, o);
+          const long long vn = __shfl_up_sync(0xffffffffu, in, o);
+          if (lane >= o) {
+            ic += vc;
+            in += vn;
+          }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, r < a.num_seqs && cb + ic > x);
+        if (hit) {
+          const int first = __ffs(hit) - 1;
+          const long long cbr = cb + __shfl_sync(0xffffffffu, ic - ct, first);
+          const long long chr = chb + __shfl_sync(0xffffffffu, in - nt, first);
+          const int ncr = __shfl_sync(0xffffffffu, nc, first);
+          const long long segcost = static_cast<long long>(cu_chunk) * ncr + cu_seg;
+          const long long off = x - cbr;
+          const long long h = off / segcost, o = off % segcost;
+          const long long j = o <= cu_seg ? 0 : (o - cu_seg + cu_chunk - 1) / cu_chunk;
+          return chr + h * ncr + j;
+        }
+        cb += __shfl_sync(0xffffffffu, ic, 31);
+        chb += __shfl_sync(0xffffffffu, in, 31);
+      }
+      return W;
+    };
+    const long long lo = W > 0 ? chunk_at_cost(range_lo(Ctot, a.num_ctas, cta)) : 0;
+    const long long hi = W > 0 ? chunk_at_cost(range_lo(Ctot, a.num_ctas, cta + 1)) : 0;
+    if (lane == 0) {
+      *total_tiles = W;
+      *total_cost = Ctot;
+      *cost_chunk = cu_chunk;
+    }
     // (blocks, length, q row) of request r, for every lane.
     auto req_info = [&](int r, int* len, int* row) -> int {
       int nbv = 0, lv = 0, rv = 0;
@@ -290,33 +376,34 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       h1 = (r < a.num_seqs && 32 + lane < nb) ? __ldg(rp + ((32 + lane) >> a.tile_shift)) : 0;
     };
     if (lo < hi) {
-      // Request holding chunk `lo`: scan the per-request chunk counts 32 at a time.
-      long long base = 0;
+      // Request holding chunk `lo`: scan the per-request chunk counts (and
+      // split costs) 32 at a time.
+      long long base = 0, cbase = 0;  // chunks and cost before request r0
       int r0 = -1;
       for (int rc = 0; rc < a.num_seqs && r0 < 0; rc += 32) {
         const int r = rc + lane;
-        int len, row, nbv = 0;
-        if (rc < 32 * kReqCache) {
-#pragma unroll
-          for (int m = 0; m < kReqCache; ++m)
-            if (m == (rc >> 5)) nbv = c_nb[m];
-        } else if (r < a.num_seqs) {
-          nbv = request_blocks(a, r, &len, &row);
-        }
-        const long long nt = static_cast<long long>((nbv + C::CB - 1) / C::CB) * a.num_kv_heads;
-        long long incl = nt;
+        const int nc = (req_nb(r) + C::CB - 1) / C::CB;
+        const long long nt = static_cast<long long>(nc) * a.num_kv_heads;
+        const long long ct = nc > 0 ? a.num_kv_heads * (static_cast<long long>(cu_chunk) * nc + cu_seg) : 0;
+        long long incl = nt, icl = ct;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
+          const long long vc = __shfl_up_sync(0xffffffffu, icl, o);
+          if (lane >= o) {
+            incl += v;
+            icl += vc;
+          }
         }
         const unsigned hit = __ballot_sync(0xffffffffu, r < a.num_seqs && base + incl > lo);
         if (hit) {
           const int first = __ffs(hit) - 1;
           base += __shfl_sync(0xffffffffu, incl - nt, first);
+          cbase += __shfl_sync(0xffffffffu, icl - ct, first);
           r0 = rc + first;
         } else {
           base += __shfl_sync(0xffffffffu, incl, 31);
+          cbase += __shfl_sync(0xffffffffu, icl, 31);
         }
       }
       int r = r0, len = 0, row = 0;
@@ -354,6 +441,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           si.r = r;
           si.kvh = kvh;
           si.t0 = base + static_cast<long long>(kvh) * nc;
+          si.c0 = cbase + static_cast<long long>(kvh) * (static_cast<long long>(cu_chunk) * nc + cu_seg) +
+                  cu_seg;
           segs[slot] = si;
           mbar_arrive_expect_tx(bar(B::QFULL + slot), a.group * D * 2);
 #pragma unroll
@@ -429,6 +518,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           if (++kvh == a.num_kv_heads) {
             kvh = 0;
             base += static_cast<long long>(nc) * a.num_kv_heads;
+            cbase += a.num_kv_heads * (static_cast<long long>(cu_chunk) * nc + cu_seg);
             ++r;
             if (nnb > 0) {  // the prefetched next request
               nb = nnb;
@@ -784,9 +874,10 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         // Publish the partial; the last of the pair's contributors merges them.
         __threadfence();
         if (!(ok = ered_sync())) break;
-        const long long W = *total_tiles;
-        const int c0 = cta_of_tile(W, a.num_ctas, si.t0);
-        const int c1 = cta_of_tile(W, a.num_ctas, si.t0 + si.npair - 1);
+        // The CTAs whose ranges hold the pair's first and last chunks.
+        const long long Ct = *total_cost;
+        const int c0 = cta_of_tile(Ct, a.num_ctas, si.c0);
+        const int c1 = cta_of_tile(Ct, a.num_ctas, si.c0 + static_cast<long long>(*cost_chunk) * (si.npair - 1));
         if (tl == 0)
           *last_flag = contribute(a.counters + static_cast<size_t>(si.r) * a.num_kv_heads + si.kvh,
                                   a.epoch, c1 - c0 + 1, a.status, si.r) ? 1 : 0;
