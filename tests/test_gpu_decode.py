@@ -163,7 +163,7 @@ def test_varlen_decode_rows_match_decode(cuda_lib):
 
 @pytest.mark.parametrize("name,sample", [("llama8b_decode_b64", None),
                                          ("long_ctx_decode_8x32k", None),
-                                         ("prefix_shared_decode_b256", 24)])
+                                         ("prefix_shared_decode_b256", None)])
 def test_full_size_workloads(cuda_lib, oracle, name, sample):
     """Full-size workloads in the benchmark's launch configuration; the
     oracle checks every request (or a seeded sample of them)."""
@@ -179,6 +179,23 @@ def test_full_size_workloads(cuda_lib, oracle, name, sample):
         rows = np.sort(np.random.default_rng(99).choice(w.num_seqs, sample, replace=False))
     ref = oracle_decode_rows(oracle, w, t, rows)
     assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, what=name)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 4, 128), (64, 4, 64)])
+def test_many_short_requests_tensor_core_decode(cuda_lib, oracle, hq, hkv, d):
+    """600 short requests of uneven length, 8 or 16 q heads per kv head: the
+    tensor-core decode splits its chunks over the CTAs by cost (segment
+    starts weigh as chunks do), so CTA ranges hold many segments and end
+    wherever the cost falls; every request is checked against the oracle."""
+    pa = cuda_lib
+    w = wl.random_workload(48 + hkv, num_seqs=600, max_len=300, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=d)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, hq, hkv, d, w.max_seq_len), "cuda")
+    out = run_decode(pa, w, t, workspace=ws)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle_decode_rows(oracle, w, t, np.arange(w.num_seqs))
+    assert_close_to_oracle(out, ref, what=f"600 short requests, {hq // hkv} q heads per kv head")
 
 
 def test_bad_block_id_is_reported_not_dereferenced(cuda_lib, oracle):
