@@ -79,6 +79,16 @@ def _declare(lib):
     lib.oracle_decode_xsplit.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
+    lib.oracle_reshape_and_cache_xsplit_fp8.restype = None
+    lib.oracle_reshape_and_cache_xsplit_fp8.argtypes = [_U16, _U16, ctypes.c_int32,
+                                                        ctypes.c_int32, ctypes.c_int32, _U8, _U8,
+                                                        ctypes.c_int32, ctypes.c_int32, _I64,
+                                                        ctypes.c_float, ctypes.c_float]
+    lib.oracle_decode_xsplit_fp8.restype = ctypes.c_int
+    lib.oracle_decode_xsplit_fp8.argtypes = [_F64, _U16, _U8, _U8, _I32, ctypes.c_int32, _I32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                             ctypes.c_double, ctypes.c_double]
     lib.oracle_map_to_kernel_blocks.restype = None
     lib.oracle_map_to_kernel_blocks.argtypes = [_I32, ctypes.c_int32, ctypes.c_int32, _I32]
     lib.oracle_decode.argtypes = [_F64, _U16, _U16, _U16, _I32, ctypes.c_int32, _I32,
@@ -223,6 +233,43 @@ class Oracle:
                                            s, hq, hkv, d, bs, float(scale))
         if rc != 0:
             raise ValueError(f"oracle_decode_xsplit rejected its arguments ({rc})")
+        return out
+
+    def reshape_and_cache_xsplit_fp8(self, key, value, key_cache, value_cache, slot_mapping,
+                                     k_scale: float, v_scale: float):
+        """e4m3 x-split caches: key [nb, hkv, d / 16, B, 16], value [nb, hkv, d, B] (bytes).
+        Returns updated copies (inputs are not modified)."""
+        k, v = _u16(key), _u16(value)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8).copy()
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8).copy()
+        sm = np.ascontiguousarray(slot_mapping, np.int64)
+        nb, hkv, dx, bs, x = kc.shape
+        d = dx * x
+        assert x == 16 and vc.shape == (nb, hkv, d, bs) and k.shape == (sm.shape[0], hkv, d)
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        self.lib.oracle_reshape_and_cache_xsplit_fp8(_p(k, _U16), _p(v, _U16), sm.shape[0], hkv,
+                                                     d, _p(kc, u8), _p(vc, u8), nb, bs,
+                                                     _p(sm, _I64), k_scale, v_scale)
+        return kc, vc
+
+    def decode_xsplit_fp8(self, q, key_cache, value_cache, block_tables, seq_lens, scale,
+                          k_scale: float, v_scale: float) -> np.ndarray:
+        q = _u16(q)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        s, hq, d = q.shape
+        nb, hkv, dx, bs, x = kc.shape
+        assert x == 16 and dx * x == d and vc.shape == (nb, hkv, d, bs)
+        out = np.zeros((s, hq, d), np.float64)
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        rc = self.lib.oracle_decode_xsplit_fp8(_p(out, _F64), _p(q, _U16), _p(kc, u8), _p(vc, u8),
+                                               _p(bt, _I32), bt.shape[1], _p(sl, _I32), s, hq,
+                                               hkv, d, bs, float(scale), float(k_scale),
+                                               float(v_scale))
+        if rc != 0:
+            raise ValueError(f"oracle_decode_xsplit_fp8 rejected its arguments ({rc})")
         return out
 
     def map_to_kernel_blocks(self, ids, k: int) -> np.ndarray:

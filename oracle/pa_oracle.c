@@ -461,3 +461,92 @@ int oracle_decode_xsplit(double* out, const uint16_t* q, const uint16_t* key_cac
     }
     return 0;
 }
+
+/* ---- The x-split layout with an e4m3 cache ------------------------------
+ * x is the number of cache elements in 16 bytes: 16 for one-byte e4m3.
+ * K cache [num_blocks, num_kv_heads, head_dim / 16, block_size, 16] and
+ * V cache [num_blocks, num_kv_heads, head_dim, block_size] of e4m3 bytes;
+ * the values are those of oracle_reshape_and_cache_fp8 at these places. */
+#define ORACLE_XSPLIT_X8 16
+
+static int64_t xsplit8_k_index(int64_t block, int64_t offset, int32_t h, int32_t d,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+    int64_t chunks = head_dim / ORACLE_XSPLIT_X8;
+    return (((block * num_kv_heads + h) * chunks + d / ORACLE_XSPLIT_X8) * block_size + offset)
+               * ORACLE_XSPLIT_X8 + d % ORACLE_XSPLIT_X8;
+}
+
+void oracle_reshape_and_cache_xsplit_fp8(const uint16_t* key, const uint16_t* value,
+                                         int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, uint8_t* key_cache,
+                                         uint8_t* value_cache, int32_t num_blocks,
+                                         int32_t block_size, const int64_t* slot_mapping,
+                                         float k_scale, float v_scale) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+        int64_t block = slot / block_size;
+        int64_t in_block = slot % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t d = 0; d < head_dim; ++d) {
+                int64_t src = i * row + (int64_t)h * head_dim + d;
+                float kf = (float)bf16_to_double(key[src]);
+                float vf = (float)bf16_to_double(value[src]);
+                key_cache[xsplit8_k_index(block, in_block, h, d, num_kv_heads, head_dim,
+                                          block_size)] = oracle_e4m3_encode(kf / k_scale);
+                value_cache[xsplit_v_index(block, in_block, h, d, num_kv_heads, head_dim,
+                                           block_size)] = oracle_e4m3_encode(vf / v_scale);
+            }
+    }
+}
+
+/* Paged decode over e4m3 x-split caches: exact attention with
+ * k_t = decoded(K) * k_scale and v_t = decoded(V) * v_scale read at the
+ * x-split positions above. */
+int oracle_decode_xsplit_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
+                             const uint8_t* value_cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                             int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, double scale,
+                             double k_scale, double v_scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim % ORACLE_XSPLIT_X8 != 0)
+        return -1;
+    int32_t heads_per_kv = num_heads / num_kv_heads;
+    for (int32_t r = 0; r < num_seqs; ++r) {
+        int64_t n = seq_lens[r];
+        double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        if (!w) return -2;
+        const int32_t* table = block_tables + (int64_t)r * max_blocks_per_seq;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const uint16_t* qh = q + ((int64_t)r * num_heads + h) * head_dim;
+            int32_t kvh = h / heads_per_kv;
+            double top = -INFINITY;
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t block = table[t / block_size], offset = t % block_size;
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    acc += bf16_to_double(qh[d]) *
+                           (oracle_e4m3_decode(key_cache[xsplit8_k_index(
+                                block, offset, kvh, d, num_kv_heads, head_dim, block_size)]) *
+                            k_scale);
+                w[t] = acc * scale;
+                if (w[t] > top) top = w[t];
+            }
+            double total = 0.0;
+            for (int64_t t = 0; t < n; ++t) { w[t] = exp(w[t] - top); total += w[t]; }
+            double* o = out + ((int64_t)r * num_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t block = table[t / block_size], offset = t % block_size;
+                double p = w[t] / total;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] += p * (oracle_e4m3_decode(value_cache[xsplit_v_index(
+                                     block, offset, kvh, d, num_kv_heads, head_dim, block_size)]) *
+                                 v_scale);
+            }
+        }
+        free(w);
+    }
+    return 0;
+}

@@ -62,6 +62,18 @@ int oracle_decode_xsplit(double* out, const uint16_t* q, const uint16_t* key_cac
                          int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
                          int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, double scale);
+void oracle_reshape_and_cache_xsplit_fp8(const uint16_t* key, const uint16_t* value,
+                                         int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, uint8_t* key_cache,
+                                         uint8_t* value_cache, int32_t num_blocks,
+                                         int32_t block_size, const int64_t* slot_mapping,
+                                         float k_scale, float v_scale);
+int oracle_decode_xsplit_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
+                             const uint8_t* value_cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                             int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, double scale,
+                             double k_scale, double v_scale);
 void oracle_map_to_kernel_blocks(const int32_t* ids, int32_t n, int32_t k, int32_t* out);
 void oracle_merge_partitions(const double* m_parts, const double* l_parts,
                              const double* o_parts, int32_t num_parts, int32_t dv,

@@ -528,3 +528,63 @@ def test_decode_xsplit_equals_decode_of_the_same_cache(oracle, hq, hkv, d, lens,
     kx, vx = _to_xsplit(kc, vc)
     got = oracle.decode_xsplit(q, kx, vx, w.block_tables, w.seq_lens, w.scale)
     np.testing.assert_array_equal(got, ref)
+
+
+def _to_xsplit8(key_cache, value_cache):
+    """e4m3 [nb, B, H, d] caches -> the x-split shapes with x = 16 one-byte
+    elements (numpy's own reshape and transpose: K [nb, H, d / 16, B, 16],
+    V [nb, H, d, B])."""
+    nb, B, H, d = key_cache.shape
+    kx = np.ascontiguousarray(key_cache.reshape(nb, B, H, d // 16, 16).transpose(0, 2, 3, 1, 4))
+    vx = np.ascontiguousarray(value_cache.reshape(nb, B, H, d).transpose(0, 2, 3, 1))
+    return kx, vx
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.013, 7.7)])
+def test_xsplit_fp8_writer_is_a_permutation_of_the_token_major_fp8_writer(oracle, k_scale,
+                                                                         v_scale):
+    """The e4m3 x-split writer stores exactly the bytes of the (pinned)
+    token-major e4m3 writer, at K[s // B, h, d // 16, s % B, d % 16] and
+    V[s // B, h, d, s % B]; tokens with a negative slot write nothing."""
+    nb, B, hkv, d, n = 7, 16, 2, 64, 11
+    rng = np.random.default_rng(74)
+    gen = torch.Generator().manual_seed(74)
+    key = torch.randn((n, hkv, d), generator=gen).to(torch.bfloat16).view(torch.int16).numpy()
+    val = torch.randn((n, hkv, d), generator=gen).to(torch.bfloat16).view(torch.int16).numpy()
+    kc0 = rng.integers(0, 256, size=(nb, B, hkv, d), dtype=np.uint8)
+    vc0 = rng.integers(0, 256, size=(nb, B, hkv, d), dtype=np.uint8)
+    slots = rng.choice(nb * B, size=n, replace=False).astype(np.int64)
+    slots[3] = -1
+    kn, vn = oracle.reshape_and_cache_fp8(key, val, kc0, vc0, slots, k_scale, v_scale)
+    kx0, vx0 = _to_xsplit8(kc0, vc0)
+    kx, vx = oracle.reshape_and_cache_xsplit_fp8(key, val, kx0, vx0, slots, k_scale, v_scale)
+    kref, vref = _to_xsplit8(kn, vn)
+    np.testing.assert_array_equal(kx, kref)
+    np.testing.assert_array_equal(vx, vref)
+    i = 5
+    blk, off = divmod(int(slots[i]), B)
+    for e in range(d):
+        assert kx[blk, 1, e // 16, off, e % 16] == kn[blk, off, 1, e]
+        assert vx[blk, 1, e, off] == vn[blk, off, 1, e]
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens,B", [(4, 2, 64, [25, 12, 37, 20], 16),
+                                             (8, 2, 128, [1, 31, 64, 70], 32)])
+def test_decode_xsplit_fp8_equals_decode_fp8_of_the_same_cache(oracle, hq, hkv, d, lens, B):
+    """Decoding the e4m3 x-split form of a cache gives exactly the (pinned)
+    e4m3 decode of the token-major form."""
+    w, _ = _contiguous_workload(lens, hq, hkv, d, seed=75, B=B)
+    need = -(-np.asarray(lens) // B)
+    for r, n in enumerate(need):
+        w.block_tables[r, :n] = w.block_tables[r, :n][::-1].copy()
+    t = wl.make_tensors(w)
+    rng = np.random.default_rng(75)
+    kc8 = rng.integers(0, 127, size=t.key_cache.shape, dtype=np.uint8)
+    vc8 = rng.integers(0, 127, size=t.value_cache.shape, dtype=np.uint8)
+    kc8[rng.random(kc8.shape) < 0.5] |= 0x80
+    vc8[rng.random(vc8.shape) < 0.5] |= 0x80
+    q = t.q.view(torch.int16).numpy()
+    ref = oracle.decode_fp8(q, kc8, vc8, w.block_tables, w.seq_lens, w.scale, 0.5, 0.125)
+    kx, vx = _to_xsplit8(kc8, vc8)
+    got = oracle.decode_xsplit_fp8(q, kx, vx, w.block_tables, w.seq_lens, w.scale, 0.5, 0.125)
+    np.testing.assert_array_equal(got, ref)
