@@ -539,9 +539,9 @@ int oracle_decode_xsplit_fp8(double* out, const uint16_t* q, const uint8_t* key_
             for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
             for (int64_t t = 0; t < n; ++t) {
                 int64_t block = table[t / block_size], offset = t % block_size;
-                double p = w[t] / total;
+                const double pw = w[t] / total;
                 for (int32_t d = 0; d < head_dim; ++d)
-                    o[d] += p * (oracle_e4m3_decode(value_cache[xsplit_v_index(
+                    o[d] += pw * (oracle_e4m3_decode(value_cache[xsplit_v_index(
                                      block, offset, kvh, d, num_kv_heads, head_dim, block_size)]) *
                                  v_scale);
             }

@@ -58,6 +58,12 @@ MUTATIONS = [
     ("xsplit_decode_drops_scale", "w[t] = scale * acc;", "w[t] = acc;", ["xsplit_decode"]),
     ("xsplit_decode_unnormalised", "double p = w[t] / total;", "double p = w[t];",
      ["xsplit_decode"]),
+    ("xsplit8_k_uses_bf16_x", "* ORACLE_XSPLIT_X8 + d % ORACLE_XSPLIT_X8;",
+     "* ORACLE_XSPLIT_X8 + d % ORACLE_XSPLIT_X;", ["xsplit8_writer"]),
+    ("xsplit8_writer_skips_v_scale", "oracle_e4m3_encode(vf / v_scale);\n            }\n    }\n}\n\n/* Paged decode over e4m3 x-split",
+     "oracle_e4m3_encode(vf);\n            }\n    }\n}\n\n/* Paged decode over e4m3 x-split", ["xsplit8_writer"]),
+    ("xsplit8_decode_unnormalised", "const double pw = w[t] / total;", "const double pw = w[t];",
+     ["xsplit8_decode"]),
 ]
 
 PINS = {
@@ -79,6 +85,10 @@ PINS = {
     "writer": lambda o: pins.test_reshape_and_cache_scatter(o),
     "xsplit_layout": lambda o: pins.test_xsplit_writer_places_elements_at_the_pages_shape(o, 2, 64, 16),
     "xsplit_decode": lambda o: pins.test_decode_xsplit_equals_decode_of_the_same_cache(
+        o, 4, 2, 64, [25, 12, 37, 20], 16),
+    "xsplit8_writer": lambda o: pins.test_xsplit_fp8_writer_is_a_permutation_of_the_token_major_fp8_writer(
+        o, 0.013, 7.7),
+    "xsplit8_decode": lambda o: pins.test_decode_xsplit_fp8_equals_decode_fp8_of_the_same_cache(
         o, 4, 2, 64, [25, 12, 37, 20], 16),
 }
 
