@@ -439,9 +439,11 @@ def extra_mixed(pa, name, dev, flush, reps=20):
     return res
 
 
-def extra_decode_fp8(pa, name, dev, flush, reps=20):
+def extra_decode_fp8(pa, name, dev, flush, reps=20, xsplit=False):
     """Decode-only timing of a named workload over an e4m3 copy of its cache
-    (per-tensor scales amax / 448); bytes counted at 1 per element."""
+    (per-tensor scales amax / 448), token-major or in the x-split layout
+    (K [blocks, kv heads, d / 16, block, 16], V [blocks, kv heads, d, block]);
+    bytes counted at 1 per element."""
     w = wl.NAMED[name]()
     t = wl.make_tensors(w, device=dev)
     ab = algorithmic_bytes(w)
@@ -453,8 +455,15 @@ def extra_decode_fp8(pa, name, dev, flush, reps=20):
     ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
                                                    w.head_dim, w.max_seq_len), dev)
     out = torch.empty_like(t.q)
-    call = lambda: pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
-                                 k_scale, v_scale, out=out, workspace=ws)
+    if xsplit:
+        nb, B, H, d = kc.shape
+        kc = kc.view(nb, B, H, d // 16, 16).permute(0, 2, 3, 1, 4).contiguous()
+        vc = vc.view(nb, B, H, d).permute(0, 2, 3, 1).contiguous()
+        call = lambda: pa.decode_xsplit_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len,
+                                            w.scale, k_scale, v_scale, out=out, workspace=ws)
+    else:
+        call = lambda: pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len,
+                                     w.scale, k_scale, v_scale, out=out, workspace=ws)
     for _ in range(3):
         flush()
         call()
@@ -472,7 +481,8 @@ def extra_decode_fp8(pa, name, dev, flush, reps=20):
     peak, _ = measured_peaks()
     kv8 = ab["kv_bytes"] // 2
     dec8 = ab["decode_bytes"] - ab["kv_bytes"] + kv8
-    res = {"kv_dtype": "e4m3", "us_per_call": round(s * 1e6, 2), "kv_gbs": round(kv8 / s / 1e9, 2),
+    res = {"kv_dtype": "e4m3", "kv_layout": "x-split" if xsplit else "token-major",
+           "us_per_call": round(s * 1e6, 2), "kv_gbs": round(kv8 / s / 1e9, 2),
            "decode_gbs": round(dec8 / s / 1e9, 2),
            "frac_of_measured_peak": round(dec8 / s / 1e9 / peak, 4),
            "kv_tokens_per_us": round(ab["kv_unique_tokens"] / (s * 1e6), 1)}
@@ -486,6 +496,8 @@ def extra_decode(pa, name, dev, flush, reps=20):
     Suffix _fp8: over an e4m3 copy of the cache; _xsplit: over the x-split
     layout (K [blocks, kv heads, d / 8, block, 8], V [blocks, kv heads, d,
     block]) of the same cache."""
+    if name.endswith("_fp8_xsplit"):
+        return extra_decode_fp8(pa, name[:-len("_fp8_xsplit")], dev, flush, reps, xsplit=True)
     if name.endswith("_fp8"):
         return extra_decode_fp8(pa, name[:-len("_fp8")], dev, flush, reps)
     xsplit = name.endswith("_xsplit")
@@ -615,6 +627,7 @@ def main(argv=None):
                                                     "mixed_chunked_prefill",
                                                     "multi_chunk_prefill",
                                                     "llama8b_decode_b64_fp8",
+                                                    "llama8b_decode_b64_fp8_xsplit",
                                                     "llama8b_decode_b64_xsplit",
                                                     "prefix_shared_decode_b256_xsplit"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

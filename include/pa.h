@@ -320,8 +320,9 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const v
  *   value_cache  [num_blocks, num_kv_heads, head_dim, block_size] bf16
  * Element d of kv head h of the token in slot s = b * block_size + o sits
  * at key_cache[b][h][d / 8][o][d % 8] and value_cache[b][h][d][o].
- * Only the two calls below read or write this layout; pa_prefill_varlen
- * and the FP8 calls take the token-major layout.
+ * Only the two calls below (and their FP8 forms after them) read or write
+ * this layout; pa_prefill_varlen and the other FP8 calls take the
+ * token-major layout.
  *
  * pa_reshape_and_cache_xsplit -- pa_reshape_and_cache into x-split caches.
  * Same arguments, slots, errors and bit-exactness; head_dim a multiple of 8.
@@ -350,6 +351,44 @@ pa_status pa_decode_xsplit(void* out, const void* q, const void* key_cache,
                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                            int32_t num_blocks, float scale, int32_t partition_tokens,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The x-split layout with an FP8 (e4m3) cache ("vLLM 深度解析（二）",
+ * section 3.2.1: x = 16 bytes / element size, 16 for one-byte elements):
+ *   key_cache    [num_blocks, num_kv_heads, head_dim / 16, block_size, 16]
+ *   value_cache  [num_blocks, num_kv_heads, head_dim, block_size]
+ * both e4m3 bytes.  Element d of kv head h of the token in slot
+ * s = b * block_size + o sits at key_cache[b][h][d / 16][o][d % 16] and
+ * value_cache[b][h][d][o].  At block_size 16 the K (or V) bytes of one
+ * (block, kv head) are one contiguous 2 KB run at head_dim 128.
+ *
+ * pa_reshape_and_cache_xsplit_fp8 -- pa_reshape_and_cache_fp8 into x-split
+ * e4m3 caches: the same values e4m3(x / scale) (binary32 quotient, nearest
+ * even, saturated to +-448, NaN kept), slots, skips and errors, at the
+ * x-split places; head_dim a multiple of 16.
+ */
+pa_status pa_reshape_and_cache_xsplit_fp8(const void* key, const void* value,
+                                          int64_t key_stride, int64_t value_stride,
+                                          void* key_cache, void* value_cache,
+                                          const int64_t* slot_mapping, int32_t num_tokens,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t block_size, int32_t num_blocks, float k_scale,
+                                          float v_scale, int32_t* device_status, void* stream);
+
+/*
+ * pa_decode_xsplit_fp8 -- pa_decode_fp8 over x-split e4m3 caches: key t
+ * contributes decoded(K_t) * k_scale and value t decoded(V_t) * v_scale.
+ * Same arguments, workspace, limits (1 to 4 q heads per kv head) and
+ * results as pa_decode_fp8; the products run on the tensor cores in f16.
+ */
+pa_status pa_decode_xsplit_fp8(void* out, const void* q, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, float scale, float k_scale, float v_scale,
+                               int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * pa_prefill_workspace_size -- bytes of workspace pa_prefill_varlen needs

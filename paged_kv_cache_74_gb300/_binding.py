@@ -26,7 +26,8 @@ ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_compute_slot_mapping", "pa_decode_workspace_size", "pa_decode",
                "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
                "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-               "pa_reshape_and_cache_xsplit", "pa_decode_xsplit", "pa_append_tokens")
+               "pa_reshape_and_cache_xsplit", "pa_decode_xsplit", "pa_append_tokens",
+               "pa_reshape_and_cache_xsplit_fp8", "pa_decode_xsplit_fp8")
 
 
 class PAError(RuntimeError):
@@ -61,6 +62,13 @@ def _declare(lib):
     lib.pa_decode_xsplit.restype = ctypes.c_int
     lib.pa_decode_xsplit.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                      _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp]
+    lib.pa_reshape_and_cache_xsplit_fp8.restype = ctypes.c_int
+    lib.pa_reshape_and_cache_xsplit_fp8.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _i32,
+                                                    _i32, _i32, _i32, _f32, _f32, _vp, _vp]
+    lib.pa_decode_xsplit_fp8.restype = ctypes.c_int
+    lib.pa_decode_xsplit_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                         _i32, _i32, _i32, _i32, _f32, _f32, _f32, _i32, _vp, _sz,
+                                         _vp]
     lib.pa_append_tokens.restype = ctypes.c_int
     lib.pa_append_tokens.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _vp, _i32,
                                      _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
@@ -197,6 +205,39 @@ def reshape_and_cache_xsplit(key, value, key_cache, value_cache, slot_mapping, s
     _check("pa_reshape_and_cache_xsplit", lib.pa_reshape_and_cache_xsplit(
         _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache),
         _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, _ptr(status), _stream()))
+
+
+def _xsplit8_shape(key_cache, value_cache):
+    """(num_blocks, block_size, num_kv_heads, head_dim) of e4m3 x-split caches:
+    key [nb, Hkv, d / 16, bs, 16], value [nb, Hkv, d, bs] (uint8)."""
+    if key_cache.dim() != 5 or key_cache.shape[4] != 16:
+        raise ValueError("e4m3 x-split key_cache must be [num_blocks, kv_heads, head_dim / 16, block, 16]")
+    nb, hkv, dx, bs, _ = key_cache.shape
+    d = dx * 16
+    if tuple(value_cache.shape) != (nb, hkv, d, bs):
+        raise ValueError("e4m3 x-split value_cache must be [num_blocks, kv_heads, head_dim, block]")
+    return nb, bs, hkv, d
+
+
+def reshape_and_cache_xsplit_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale,
+                                 v_scale, status=None):
+    """reshape_and_cache_fp8 into e4m3 x-split caches (key [nb, Hkv, d / 16,
+    bs, 16], value [nb, Hkv, d, bs], uint8)."""
+    _cuda("key", key, torch.bfloat16)
+    _cuda("value", value, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.uint8)
+    _contig("value_cache", value_cache, torch.uint8)
+    _contig("slot_mapping", slot_mapping, torch.int64)
+    nb, bs, hkv, d = _xsplit8_shape(key_cache, value_cache)
+    T = slot_mapping.shape[0]
+    for name, t in (("key", key), ("value", value)):
+        if tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, {hkv}, {d}] with contiguous heads")
+    lib = load_library()
+    _check("pa_reshape_and_cache_xsplit_fp8", lib.pa_reshape_and_cache_xsplit_fp8(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache),
+        _ptr(value_cache), _ptr(slot_mapping), T, hkv, d, bs, nb, float(k_scale), float(v_scale),
+        _ptr(status), _stream()))
 
 
 def compute_slot_mapping(block_tables, query_start_loc, seq_lens, block_size, num_blocks,
@@ -342,6 +383,33 @@ def decode_xsplit(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
         float(scale), int(partition_tokens), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def decode_xsplit_fp8(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale,
+                      k_scale, v_scale, out=None, workspace=None, partition_tokens=0):
+    """Paged decode over e4m3 x-split caches (see reshape_and_cache_xsplit_fp8)."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.uint8)
+    _contig("value_cache", value_cache, torch.uint8)
+    _contig("block_tables", block_tables, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    S, hq, d = q.shape
+    nb, bs, hkv, d2 = _xsplit8_shape(key_cache, value_cache)
+    if d2 != d:
+        raise ValueError("cache shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_size(S, hq, hkv, d, max_seq_len, partition_tokens),
+                                  q.device)
+    lib = load_library()
+    _check("pa_decode_xsplit_fp8", lib.pa_decode_xsplit_fp8(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
+        float(scale), float(k_scale), float(v_scale), int(partition_tokens), _ptr(workspace),
+        workspace.numel(), _stream()))
     return out
 
 

@@ -150,6 +150,64 @@ reshape_and_cache_xsplit_kernel(const uint4* __restrict__ key, const uint4* __re
   }
 }
 
+// The quantizing write into the x-split layout with an e4m3 cache (x = 16
+// one-byte elements): chunk c (16 values) of kv head h of the token in slot s
+// becomes e4m3(x / k_scale) at K[s / B][h][c][s % B][0..15], one 16-byte
+// store; V element d becomes e4m3(x / v_scale) at V[s / B][h][d][s % B].
+// One warp per token, lanes over 16-value chunks.
+__global__ void __launch_bounds__(kWriteWarps * 32)
+reshape_and_cache_xsplit_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                    int64_t key_stride_chunks, int64_t value_stride_chunks,
+                                    uint4* __restrict__ key_cache, uint8_t* __restrict__ value_cache,
+                                    const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int64_t num_slots, float k_scale, float v_scale,
+                                    int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();  // slot_mapping may come from the previous kernel
+  const int token = blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (token >= num_tokens) return;
+  const int64_t slot = slot_mapping[token];
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (lane == 0) record_error(status, PA_DEV_BAD_SLOT, token, static_cast<int>(slot));
+    return;
+  }
+  // 8 bf16 values -> 8 e4m3 bytes (in order, as two 32-bit words).
+  auto quantize8 = [](uint4 w, float scale, uint32_t* out) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __fdiv_rn(__uint_as_float(ws[e] << 16), scale);
+      const float hi = __fdiv_rn(__uint_as_float(ws[e] & 0xffff0000u), scale);
+      p[e] = e4m3x2(lo, hi);
+    }
+    out[0] = p[0] | (p[1] << 16);
+    out[1] = p[2] | (p[3] << 16);
+  };
+  const int64_t blk = slot / block_size;
+  const int off = static_cast<int>(slot % block_size);
+  const int cpr = head_dim / 16;  // 16-value chunks per kv head
+  const uint4* ks = key + token * key_stride_chunks;
+  const uint4* vs = value + token * value_stride_chunks;
+  for (int c = lane; c < num_kv_heads * cpr; c += 32) {
+    const int h = c / cpr, cc = c % cpr;
+    const int64_t head_base = blk * num_kv_heads + h;
+    uint32_t kq[4], vq[4];
+    quantize8(__ldg(ks + 2 * c), k_scale, kq);
+    quantize8(__ldg(ks + 2 * c + 1), k_scale, kq + 2);
+    quantize8(__ldg(vs + 2 * c), v_scale, vq);
+    quantize8(__ldg(vs + 2 * c + 1), v_scale, vq + 2);
+    key_cache[(head_base * cpr + cc) * block_size + off] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+    uint8_t* vd = value_cache + (head_base * head_dim + cc * 16) * block_size + off;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      vd[e * block_size] = static_cast<uint8_t>(vq[e >> 2] >> (8 * (e & 3)));
+  }
+}
+
 // One CTA per request; its threads cover the request's new tokens.
 __global__ void __launch_bounds__(128)
 slot_mapping_kernel(int64_t* __restrict__ slot_mapping, int total_tokens,
@@ -337,6 +395,22 @@ cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, 
                            key_stride / 8, value_stride / 8, static_cast<uint4*>(key_cache),
                            static_cast<uint16_t*>(value_cache), slot_mapping, num_tokens,
                            num_kv_heads, head_dim, block_size, num_slots, status);
+}
+
+cudaError_t launch_reshape_and_cache_xsplit_fp8(const void* key, const void* value,
+                                                int64_t key_stride, int64_t value_stride,
+                                                void* key_cache, void* value_cache,
+                                                const int64_t* slot_mapping, int num_tokens,
+                                                int num_kv_heads, int head_dim, int block_size,
+                                                int64_t num_slots, float k_scale, float v_scale,
+                                                int32_t* status, cudaStream_t stream) {
+  const int grid = (num_tokens + kWriteWarps - 1) / kWriteWarps;
+  return launch_overlapped(reshape_and_cache_xsplit_fp8_kernel, dim3(grid), dim3(kWriteWarps * 32),
+                           0, stream, static_cast<const uint4*>(key),
+                           static_cast<const uint4*>(value), key_stride / 8, value_stride / 8,
+                           static_cast<uint4*>(key_cache), static_cast<uint8_t*>(value_cache),
+                           slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_slots,
+                           k_scale, v_scale, status);
 }
 
 cudaError_t launch_append_tokens(const void* key, const void* value, int64_t key_stride,

@@ -107,7 +107,6 @@ struct DecodeCfg {
   static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
-  static_assert(!XS || !KV8, "the x-split layout holds bf16");
   static_assert(GMAX <= 8 && NC == 2, "an m16n8k16 product serves at most 8 q heads");
   // Bulk-copy destinations (ring, q) 16-byte aligned; the segment records'
   // 64-bit fields 8-byte aligned.
@@ -149,6 +148,17 @@ __device__ __forceinline__ uint32_t xs_k_offset(int t, int c) {
 // of row d:
 __device__ __forceinline__ uint32_t xs_v_offset(int d, int tb) {
   return static_cast<uint32_t>(d * 32 + ((tb ^ ((d >> 2) & 1)) * 16));
+}
+
+// e4m3 x-split stages: K as [head_dim / 16 chunks][16 tokens][16 B], V as
+// V^T [head_dim][16 tokens] (bytes, no swizzle: 8 consecutive 16-byte rows
+// are conflict-free).  A plain ldmatrix of V^T gives a lane tokens 4 ft ..
+// 4 ft + 3 of its head_dim row, so the products' token order is permuted:
+// product row r of S (and index r of the P.V reduction) is token xs8_token(r),
+// i.e. rows 2 t, 2 t + 1 are tokens 4 t, 4 t + 1 and rows 2 t + 8, 2 t + 9
+// are tokens 4 t + 2, 4 t + 3.  The K rows are read in that order.
+__device__ __forceinline__ int xs8_token(int r) {
+  return r < 8 ? 4 * (r >> 1) + (r & 1) : 4 * ((r - 8) >> 1) + 2 + (r & 1);
 }
 
 // A token-major K or V stage (the grouped copy, 128-byte swizzled):
@@ -455,7 +465,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int blk = bad ? a.num_blocks : phys;
                 const int sub = (b + j) & ((1 << a.tile_shift) - 1);  // 16-token tile of the block
                 const int kvc = kvh / a.kv_div;                        // kv head of the cache
-                tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 2 * sub, 0, kvc, blk, policy);
+                if constexpr (KV8)  // one contiguous run per chunk: {B x 16 bytes, d / 16, ...}
+                  tma_load_4d(ring_s + (2 * s) * C::TILE, &kmap, full, 256 * sub, 0, kvc, blk, policy);
+                else
+                  tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 2 * sub, 0, kvc, blk, policy);
                 tma_load_4d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 16 * sub, 0, kvc, blk,
                             policy);
               } else {
@@ -771,7 +784,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int kp = 0; kp < C::KS / 2; ++kp) {
           uint32_t r8[4];
-          ldsm_x4(kt + e8_offset<D>(ka_t, 2 * kp + (lane >> 4)), r8);
+          const int c8 = 2 * kp + (lane >> 4);
+          ldsm_x4(kt + (XS ? static_cast<uint32_t>(c8 * 256 + xs8_token(ka_t) * 16)
+                           : e8_offset<D>(ka_t, c8)),
+                  r8);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t af[4] = {e4m3x2_f16x2(r8[2 * h]), e4m3x2_f16x2(r8[2 * h + 1]),
@@ -793,7 +809,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       float p[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const bool ok = tok0 + fg + (i >> 1) * 8 < seq_len && 2 * ft + (i & 1) < a.group;
+        const int srow = fg + (i >> 1) * 8;
+        const int stok = (KV8 && XS) ? xs8_token(srow) : srow;
+        const bool ok = tok0 + stok < seq_len && 2 * ft + (i & 1) < a.group;
         p[i] = ok ? sacc[i] * a.scale_log2 : -INFINITY;
       }
       float tmax[2] = {fmaxf(p[0], p[2]), fmaxf(p[1], p[3])};
@@ -843,12 +861,33 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       // (0 x NaN is NaN): their halves of the V^T fragments are cleared.
       uint32_t vm01 = 0xffffffffu, vm89 = 0xffffffffu;
       if (tok0 + kBlockSize > seq_len) {
-        const int t0 = tok0 + 2 * ft;
+        // The two token pairs a lane's V^T halves hold: (2 ft, 2 ft + 1) and
+        // (2 ft + 8, 2 ft + 9); e4m3 x-split: (4 ft, 4 ft + 1), (4 ft + 2, 4 ft + 3).
+        const int t0 = tok0 + ((KV8 && XS) ? 4 * ft : 2 * ft);
+        const int t8 = t0 + ((KV8 && XS) ? 2 : 8);
         vm01 = (t0 < seq_len ? 0x0000ffffu : 0u) | (t0 + 1 < seq_len ? 0xffff0000u : 0u);
-        vm89 = (t0 + 8 < seq_len ? 0x0000ffffu : 0u) | (t0 + 9 < seq_len ? 0xffff0000u : 0u);
+        vm89 = (t8 < seq_len ? 0x0000ffffu : 0u) | (t8 + 1 < seq_len ? 0xffff0000u : 0u);
       }
       const int va_r = lane & 7, va_m = lane >> 3;
-      if constexpr (KV8) {
+      if constexpr (KV8 && XS) {
+        // e4m3 x-split V^T: plain ldmatrix of 8 head_dim rows of 16 bytes;
+        // matrix mi = head_dim 16 (2 mp + mi / 2) + 8 (mi % 2) ..  A lane's
+        // register holds tokens 4 ft .. 4 ft + 3 of row fg: its low half is
+        // reduction index (2 ft, 2 ft + 1), its high half (2 ft + 8, 2 ft + 9).
+#pragma unroll
+        for (int mp = 0; mp < C::KS / 2; ++mp) {
+          uint32_t r8[4];
+          ldsm_x4(vt + static_cast<uint32_t>((16 * (2 * mp + (va_m >> 1)) + 8 * (va_m & 1) + va_r) * 16),
+                  r8);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t af[4] = {e4m3x2_f16x2(r8[2 * h]) & vm01, e4m3x2_f16x2(r8[2 * h + 1]) & vm01,
+                                    e4m3x2_f16x2(r8[2 * h] >> 16) & vm89,
+                                    e4m3x2_f16x2(r8[2 * h + 1] >> 16) & vm89};
+            mma_16816_f16(om[2 * mp + h], af, pb0, pb1);
+          }
+        }
+      } else if constexpr (KV8) {
         // e4m3 V^T: matrix mi = tokens 8 (mi % 2) .., chunk 2 mp + mi / 2,
         // read transposed in 16-bit units; a lane's register holds (token
         // 2 ft, 2 ft + 1) x (head_dim 2 fg, 2 fg + 1) of the chunk.  Byte
@@ -907,7 +946,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // head_dim row of accumulator om[mt][i] (the e4m3 V^T fragments
     // interleave the rows: product row fg is 2 fg, row fg + 8 is 2 fg + 1).
     auto orow = [&](int mt, int i) -> int {
-      return KV8 ? 16 * mt + 2 * fg + (i >> 1) : 16 * mt + fg + 8 * (i >> 1);
+      return (KV8 && !XS) ? 16 * mt + 2 * fg + (i >> 1) : 16 * mt + fg + 8 * (i >> 1);
     };
     auto put = [&]() {
 #pragma unroll
@@ -1009,12 +1048,12 @@ int decode_ctas_per_sm(int head_dim, int group) {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, bool kv8, bool xsplit, cudaStream_t stream) {
   const int gmax = decode_gmax(a.group);
-  if (kv8 && xsplit) return cudaErrorInvalidValue;
 #define PA_DECODE_CASE(DD, GG)                                                      \
   if (head_dim == DD && gmax == GG)                                                 \
-    return kv8      ? launch_decode_impl<DD, GG, true, false>(a, kmap, vmap, stream) \
-           : xsplit ? launch_decode_impl<DD, GG, false, true>(a, kmap, vmap, stream) \
-                    : launch_decode_impl<DD, GG, false, false>(a, kmap, vmap, stream);
+    return kv8 ? (xsplit ? launch_decode_impl<DD, GG, true, true>(a, kmap, vmap, stream)      \
+                         : launch_decode_impl<DD, GG, true, false>(a, kmap, vmap, stream))    \
+               : (xsplit ? launch_decode_impl<DD, GG, false, true>(a, kmap, vmap, stream)     \
+                         : launch_decode_impl<DD, GG, false, false>(a, kmap, vmap, stream));
   PA_DECODE_CASE(128, 1) PA_DECODE_CASE(128, 2) PA_DECODE_CASE(128, 4)
   PA_DECODE_CASE(64, 1) PA_DECODE_CASE(64, 2) PA_DECODE_CASE(64, 4)
 #undef PA_DECODE_CASE

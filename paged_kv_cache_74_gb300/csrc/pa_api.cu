@@ -211,6 +211,50 @@ bool make_xsplit_v_map(CUtensorMap* map, const void* cache, int num_blocks, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The e4m3 x-split K cache [blocks, kv heads, head_dim / 16, block, 16] as a
+// 4-D byte tensor {block * 16, head_dim / 16, kv heads, blocks} with a box of
+// {256, head_dim / 16, 1, 1}: one 16-token tile per copy, as head_dim / 16
+// runs of 256 contiguous bytes (one 2 KB run at block 16), unswizzled.
+bool make_xsplit8_k_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                        int head_dim, int block_size) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t run = static_cast<cuuint64_t>(block_size) * 16;  // bytes of one chunk
+  const cuuint64_t head = run * (head_dim / 16);
+  const cuuint64_t dims[4] = {run, static_cast<cuuint64_t>(head_dim / 16),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {run, head, head * num_kv_heads};
+  const cuuint32_t box[4] = {256u, static_cast<cuuint32_t>(head_dim / 16), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The e4m3 x-split V cache [blocks, kv heads, head_dim, block] as a 4-D byte
+// tensor {block, head_dim, kv heads, blocks} with a box of {16, head_dim, 1,
+// 1}: one 16-token tile per copy as V^T [head_dim][16 tokens] (one 2 KB run
+// at block 16), unswizzled.
+bool make_xsplit8_v_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+                        int head_dim, int block_size) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(block_size);  // bytes per head_dim row
+  const cuuint64_t dims[4] = {row, static_cast<cuuint64_t>(head_dim),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {row, row * head_dim, row * head_dim * num_kv_heads};
+  const cuuint32_t box[4] = {16u, static_cast<cuuint32_t>(head_dim), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             block_size == 16 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Work units per request of the x-split decode: its kernel serves up to 4
 // q heads per unit, so a group of g q heads is cut into g / g' units of g'
 // heads (g' the largest divisor of g not above 4), each reading its kv
@@ -344,7 +388,11 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   const int unit_heads = kv.xsplit ? xsplit_heads_per_unit(group) : group;
   const int kv_div = group / unit_heads;
   CUtensorMap kmap, vmap, qmap;
-  if (kv.xsplit) {
+  if (kv.xsplit && kv.e4m3) {
+    if (!make_xsplit8_k_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim, block_size) ||
+        !make_xsplit8_v_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim, block_size))
+      return PA_ERR_CUDA;
+  } else if (kv.xsplit) {
     if (!make_xsplit_k_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim, block_size) ||
         !make_xsplit_v_map(&vmap, value_cache, num_blocks, num_kv_heads, head_dim, block_size))
       return PA_ERR_CUDA;
@@ -650,6 +698,67 @@ pa_status pa_decode_xsplit(void* out, const void* q, const void* key_cache, cons
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
   KvFormat kv;
   kv.xsplit = true;
+  return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                            seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,
+                            static_cast<cudaStream_t>(stream), kv);
+}
+
+pa_status pa_reshape_and_cache_xsplit_fp8(const void* key, const void* value,
+                                          int64_t key_stride, int64_t value_stride,
+                                          void* key_cache, void* value_cache,
+                                          const int64_t* slot_mapping, int32_t num_tokens,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t block_size, int32_t num_blocks, float k_scale,
+                                          float v_scale, int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1 || block_size < 1) return PA_ERR_INVALID;
+  if (head_dim < 16 || head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(slot_mapping, 8) ||
+      (device_status && !aligned(device_status, 4)))
+    return PA_ERR_INVALID;
+  if (key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+    return PA_ERR_INVALID;
+  const cudaError_t e = launch_reshape_and_cache_xsplit_fp8(
+      key, value, key_stride, value_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      num_kv_heads, head_dim, block_size, static_cast<int64_t>(num_blocks) * block_size, k_scale,
+      v_scale, device_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_xsplit_fp8(void* out, const void* q, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, float scale, float k_scale, float v_scale,
+                               int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale);
+  if (st != PA_OK) return st;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID;
+  if (num_heads / num_kv_heads > 4) return PA_ERR_UNSUPPORTED;
+  if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
+                                       partition_tokens);
+  if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID;
+  KvFormat kv;
+  kv.e4m3 = true;
+  kv.xsplit = true;
+  kv.k_scale = k_scale;
+  kv.v_scale = v_scale;
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, nullptr, num_seqs, num_seqs, max_seq_len, num_heads,
                             num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace,

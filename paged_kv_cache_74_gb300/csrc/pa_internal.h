@@ -141,6 +141,15 @@ cudaError_t launch_reshape_and_cache_xsplit(const void* key, const void* value, 
                                             int num_tokens, int num_kv_heads, int head_dim,
                                             int block_size, int64_t num_slots, int32_t* status,
                                             cudaStream_t stream);
+// x-split e4m3 cache write: K [blocks, kv heads, head_dim / 16, block, 16],
+// V [blocks, kv heads, head_dim, block] (bytes), values e4m3(x / scale).
+cudaError_t launch_reshape_and_cache_xsplit_fp8(const void* key, const void* value,
+                                                int64_t key_stride, int64_t value_stride,
+                                                void* key_cache, void* value_cache,
+                                                const int64_t* slot_mapping, int num_tokens,
+                                                int num_kv_heads, int head_dim, int block_size,
+                                                int64_t num_slots, float k_scale, float v_scale,
+                                                int32_t* status, cudaStream_t stream);
 cudaError_t launch_map_kernel_blocks(int32_t* out, const int32_t* in, int64_t n, int k,
                                      int32_t* status, cudaStream_t stream);
 // Slot mapping and token-major cache write of the new tokens in one kernel

@@ -131,3 +131,109 @@ def test_decode_fp8_rejects_large_groups(cuda_lib):
     kc = torch.zeros(t.key_cache.shape, dtype=torch.uint8, device="cuda")
     with pytest.raises(pa.PAError):
         pa.decode_fp8(t.q, kc, kc.clone(), t.block_tables, t.seq_lens, w.max_seq_len, w.scale, 1.0, 1.0)
+
+
+# ---- the x-split layout with an e4m3 cache (x = 16 one-byte elements)
+
+def to_xsplit8(kc, vc):
+    """e4m3 [nb, B, H, d] caches -> K [nb, H, d / 16, B, 16], V [nb, H, d, B]."""
+    nb, B, H, d = kc.shape
+    kx = kc.view(nb, B, H, d // 16, 16).permute(0, 2, 3, 1, 4).contiguous()
+    vx = vc.view(nb, B, H, d).permute(0, 2, 3, 1).contiguous()
+    return kx, vx
+
+
+@pytest.mark.parametrize("k_scale,v_scale,d,B", [(0.013, 7.7, 128, 16), (1.0, 1.0, 64, 32),
+                                                 (2.0 ** -5, 0.03, 128, 64)])
+def test_xsplit_fp8_write_bit_exact(cuda_lib, oracle, k_scale, v_scale, d, B):
+    """The e4m3 x-split writer against the oracle's, over the whole pool."""
+    pa = cuda_lib
+    w = wl.random_workload(330 + B, num_seqs=9, max_len=300, num_heads=16, num_kv_heads=4,
+                           head_dim=d, block_size=B, max_q_len=40, prefill_fraction=0.5)
+    t = wl.make_tensors(w, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(330)
+    kx = torch.randint(0, 256, (w.num_blocks, 4, d // 16, B, 16), generator=gen, device="cuda",
+                       dtype=torch.uint8)
+    vx = torch.randint(0, 256, (w.num_blocks, 4, d, B), generator=gen, device="cuda",
+                       dtype=torch.uint8)
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, B,
+                                    w.num_blocks, w.total_q)
+    slots[3] = -1
+    ref_k, ref_v = oracle.reshape_and_cache_xsplit_fp8(bits(t.key), bits(t.value), kx.cpu().numpy(),
+                                                       vx.cpu().numpy(), slots.cpu().numpy(),
+                                                       k_scale, v_scale)
+    pa.reshape_and_cache_xsplit_fp8(t.key, t.value, kx, vx, slots, k_scale, v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(kx.cpu().numpy(), ref_k)
+    assert np.array_equal(vx.cpu().numpy(), ref_v)
+
+
+XS8_SWEEP = [
+    # (head_dim, q heads, kv heads, max_len, num_seqs, block size, seed)
+    (128, 32, 8, 900, 7, 16, 341), (128, 8, 8, 300, 9, 16, 342), (128, 16, 8, 1500, 4, 32, 343),
+    (64, 8, 2, 700, 6, 16, 344), (64, 4, 4, 120, 10, 64, 345), (64, 2, 2, 2000, 3, 16, 346),
+    (128, 12, 4, 257, 5, 16, 347),
+]
+
+
+@pytest.mark.parametrize("d,hq,hkv,max_len,ns,B,seed", XS8_SWEEP)
+def test_decode_xsplit_fp8_matches_oracle(cuda_lib, oracle, d, hq, hkv, max_len, ns, B, seed):
+    """Decode over e4m3 x-split caches (NaN codes in every unused slot)
+    against the oracle's x-split e4m3 decode."""
+    pa = cuda_lib
+    w = wl.random_workload(seed, num_seqs=ns, max_len=max_len, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, block_size=B)
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 2.0 ** -5, 0.03
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, seed)
+    kx, vx = to_xsplit8(kc, vc)
+    out = pa.decode_xsplit_fp8(t.q, kx, vx, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                               k_scale, v_scale)
+    ref = oracle.decode_xsplit_fp8(bits(t.q), kx.cpu().numpy(), vx.cpu().numpy(), w.block_tables,
+                                   w.seq_lens, w.scale, k_scale, v_scale)
+    assert torch.isfinite(out.float()).all()
+    assert_close_to_oracle(out, ref, what=f"x-split fp8 d{d} hq{hq} hkv{hkv} B{B}")
+
+
+def test_decode_xsplit_fp8_forced_splits_and_write(cuda_lib, oracle):
+    """Write each request's new token into e4m3 x-split caches, then decode
+    with 16-token partitions (many pieces merged in the kernel)."""
+    pa = cuda_lib
+    w = wl.random_workload(348, num_seqs=6, max_len=700, num_heads=32, num_kv_heads=8, head_dim=128)
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 0.04, 0.06
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, 348)
+    kx, vx = to_xsplit8(kc, vc)
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16,
+                                    w.num_blocks, w.total_q)
+    ref_k, ref_v = oracle.reshape_and_cache_xsplit_fp8(bits(t.key), bits(t.value), kx.cpu().numpy(),
+                                                       vx.cpu().numpy(), slots.cpu().numpy(),
+                                                       k_scale, v_scale)
+    pa.reshape_and_cache_xsplit_fp8(t.key, t.value, kx, vx, slots, k_scale, v_scale)
+    out = pa.decode_xsplit_fp8(t.q, kx, vx, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                               k_scale, v_scale, partition_tokens=16)
+    ref = oracle.decode_xsplit_fp8(bits(t.q), ref_k, ref_v, w.block_tables, w.seq_lens, w.scale,
+                                   k_scale, v_scale)
+    assert_close_to_oracle(out, ref, what="x-split fp8 write + forced splits")
+
+
+def test_decode_xsplit_fp8_full_size_8b(cuda_lib, oracle):
+    """The 8B-shaped batch over e4m3 x-split caches in the benchmark's launch
+    configuration, against the oracle on a seeded sample of requests and
+    against the token-major e4m3 decode of the same values on all of them."""
+    pa = cuda_lib
+    w = wl.llama8b_decode()
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 2.0 ** -5, 2.0 ** -5, 349)
+    kx, vx = to_xsplit8(kc, vc)
+    out = pa.decode_xsplit_fp8(t.q, kx, vx, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                               2.0 ** -5, 2.0 ** -5)
+    tm = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                       2.0 ** -5, 2.0 ** -5)
+    err = (out.float() - tm.float()).abs()
+    assert torch.isfinite(out.float()).all() and err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+    rows = np.sort(np.random.default_rng(349).choice(w.num_seqs, 12, replace=False))
+    ref = oracle.decode_xsplit_fp8(bits(t.q)[rows], kx.cpu().numpy(), vx.cpu().numpy(),
+                                   w.block_tables[rows], w.seq_lens[rows], w.scale, 2.0 ** -5,
+                                   2.0 ** -5)
+    assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, what="x-split fp8 8B batch")
