@@ -86,7 +86,7 @@ typedef enum pa_device_error {
 const char* pa_status_string(int status);
 
 /* ABI version of this header; bumped on any incompatible change. */
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 int pa_abi_version(void);
 
 /*
@@ -266,10 +266,16 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
  * fixed in advance, and hot paths that must not call cudaMalloc (it can
  * stall the device and is not allowed while a stream is being recorded).
  *
- * Same arguments and result as pa_decode, minus the workspace.  Scratch
- * comes from one static device array of PA_DECODE_NOALLOC_SCRATCH_BYTES
- * that the library holds on every GPU that loads it until the process
- * exits.  The call allocates nothing and calls no allocating routine.
+ * Same arguments and result as pa_decode, minus the workspace, plus
+ *   device_status  optional int32[4] device pointer (NULL = none).  After
+ *                  the call (in stream order) it holds this call's device
+ *                  status record: all zero, or the first error a kernel
+ *                  recorded (bad block id, bad seq_len, wait timeout; the
+ *                  layout of the record at the start of a workspace).
+ * Scratch comes from one static device array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES that the library holds on every GPU that
+ * loads it until the process exits.  The call allocates nothing and calls
+ * no allocating routine.
  *   - Sizes whose pa_decode_workspace_size(...) exceeds the array return
  *     PA_ERR_WORKSPACE without launching anything (a larger
  *     partition_tokens needs less scratch).
@@ -288,7 +294,7 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
                             int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int32_t num_blocks, float scale, int32_t partition_tokens,
-                            void* stream);
+                            int32_t* device_status, void* stream);
 
 /*
  * pa_decode_fp8 -- pa_decode over an FP8 (e4m3) cache written by
@@ -416,11 +422,13 @@ size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_
  * tcgen05 tensor-core prefill tile; rows with q_len == 1 run the decode
  * kernel; requests with q_len == 0 produce no rows.  K/V of this step's
  * tokens must already be in the cache (pa_reshape_and_cache first).
- * When max_query_len > 1 the tensor-core tiles run on a side stream that
- * the library creates once per device (with one fork and one join event)
- * and keeps until exit; it is forked from `stream` and joined back into it
- * inside this call, so ordering on `stream` is as for a single kernel.
- * Make the first such call on a device before any stream capture.
+ * Both kernels are enqueued on `stream` and nowhere else (the library
+ * creates no stream or event).  When max_query_len > 1 the tile kernel goes
+ * first; the decode kernel is a programmatic dependent launch that may start
+ * once every kernel enqueued before this call has completed, so its CTAs
+ * fill the SMs the tiles leave free, and it completes only after the tile
+ * kernel: work enqueued on `stream` after this call sees both results, as
+ * for a single kernel.
  */
 pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
                             const void* value_cache, const int32_t* query_start_loc,

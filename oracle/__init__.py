@@ -23,14 +23,18 @@ _lib = None
 
 
 def build(src: str = _SRC, out: str = _LIB_PATH, force: bool = False) -> str:
-    """Compile the oracle with plain gcc (no vectorisation flags)."""
+    """Compile the oracle with plain gcc (no vectorisation flags), with
+    OpenMP when the compiler has it (it only spreads independent output rows
+    over threads; without it the same code runs on one thread)."""
     if not force and os.path.exists(out) and os.path.getmtime(out) >= max(
             os.path.getmtime(src), os.path.getmtime(os.path.join(_HERE, "pa_oracle.h"))):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
-                           "-I", _HERE, src, "-o", tmp, "-lm"])
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", "-I", _HERE, src,
+            "-o", tmp, "-lm"]
+    if subprocess.run(base + ["-fopenmp"], capture_output=True).returncode != 0:
+        subprocess.check_call(base)
     os.replace(tmp, out)
     return out
 
@@ -42,6 +46,10 @@ _F64 = ctypes.POINTER(ctypes.c_double)
 
 
 def _declare(lib):
+    lib.oracle_set_threads.restype = None
+    lib.oracle_set_threads.argtypes = [ctypes.c_int32]
+    lib.oracle_max_threads.restype = ctypes.c_int32
+    lib.oracle_max_threads.argtypes = []
     lib.oracle_slot.restype = ctypes.c_int64
     lib.oracle_slot.argtypes = [_I32, ctypes.c_int32, ctypes.c_int64]
     lib.oracle_query_start_loc.restype = None
@@ -134,6 +142,14 @@ class Oracle:
 
     def __init__(self, lib=None):
         self.lib = lib if lib is not None else load()
+
+    def set_threads(self, n: int) -> None:
+        """Threads of the decode / prefill loops (1 by default); the results
+        are the same for any count."""
+        self.lib.oracle_set_threads(int(n))
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
 
     def slot(self, block_table_row, block_size: int, position: int) -> int:
         row = np.ascontiguousarray(block_table_row, np.int32)

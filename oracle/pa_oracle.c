@@ -27,19 +27,37 @@
  *     scattered to [blocks, block_size, heads, dim]).
  *   - "LLM 推理基础与 vLLM 内部机制", section 2 (KV bytes per token).
  *
- * Readings of points the pages leave open (each also listed in the design
- * notes): cache layout [num_blocks, block_size, num_kv_heads, head_dim];
+ * Readings of points the pages leave open: cache layout [num_blocks, block_size, num_kv_heads, head_dim];
  * q head h reads kv head h / (num_heads / num_kv_heads); no epsilon in the
  * softmax denominator; a negative slot means "do not write"; query i of a
  * request with q_len new tokens sits at position seq_len - q_len + i and
- * sees keys 0 .. seq_len - q_len + i (bottom-right causal alignment).
+ * sees keys 0 .. seq_len - q_len + i (bottom-right causal alignment); a slot
+ * at or past num_blocks * block_size is not written either.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #include "pa_oracle.h"
+
+/* Worker threads of the attention loops.  Every output row is computed by
+ * one thread in the same order as on one thread, so the results do not
+ * depend on the thread count (OpenMP only spreads independent rows). */
+static int g_threads = 1;
+
+void oracle_set_threads(int32_t n) { g_threads = n > 0 ? n : 1; }
+
+int32_t oracle_max_threads(void) {
+#ifdef _OPENMP
+    return (int32_t)omp_get_num_procs();
+#else
+    return 1;
+#endif
+}
 
 /* bf16 -> double, exact: the bf16 bit pattern is the high half of a binary32. */
 static double bf16_to_double(uint16_t h) {
@@ -83,11 +101,12 @@ void oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, int32_
                               uint16_t* key_cache, uint16_t* value_cache,
                               int32_t num_blocks, int32_t block_size,
                               const int64_t* slot_mapping) {
-    (void)num_blocks;
     int64_t row = (int64_t)num_kv_heads * head_dim; /* one token's [heads, dim] */
     for (int32_t i = 0; i < num_tokens; ++i) {
         int64_t slot = slot_mapping[i];
-        if (slot < 0) continue;
+        /* a negative slot is padding; a slot past the pool's last block has
+         * no place in the cache: neither is written */
+        if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
         int64_t block = slot / block_size;
         int64_t offset = slot % block_size;
         for (int32_t h = 0; h < num_kv_heads; ++h)
@@ -149,16 +168,26 @@ int oracle_decode(double* out, const uint16_t* q, const uint16_t* key_cache,
     int32_t group = num_heads / num_kv_heads;
     int64_t max_len = 0;
     for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
-    double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
-    if (!s) return -2;
-    for (int32_t r = 0; r < num_seqs; ++r)
-        for (int32_t h = 0; h < num_heads; ++h)
-            attend_row(out + ((int64_t)r * num_heads + h) * head_dim,
-                       q + ((int64_t)r * num_heads + h) * head_dim, key_cache, value_cache,
-                       block_tables + (int64_t)r * max_blocks_per_seq, seq_lens[r],
-                       h / group, num_kv_heads, head_dim, block_size, scale, s);
-    free(s);
-    return 0;
+    int failed = 0;
+    /* one (request, q head) row per iteration; each thread its own scores */
+#pragma omp parallel num_threads(g_threads) reduction(|| : failed)
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t rh = 0; rh < (int64_t)num_seqs * num_heads; ++rh) {
+                int32_t r = (int32_t)(rh / num_heads), h = (int32_t)(rh % num_heads);
+                attend_row(out + ((int64_t)r * num_heads + h) * head_dim,
+                           q + ((int64_t)r * num_heads + h) * head_dim, key_cache, value_cache,
+                           block_tables + (int64_t)r * max_blocks_per_seq, seq_lens[r],
+                           h / group, num_kv_heads, head_dim, block_size, scale, s);
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
 }
 
 /* ---- Varlen chunked prefill (page 2 section 11.6; page 1 section 5.2) ---
@@ -176,22 +205,31 @@ int oracle_prefill_varlen(double* out, const uint16_t* q, const uint16_t* key_ca
     int32_t group = num_heads / num_kv_heads;
     int64_t max_len = 0;
     for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
-    double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
-    if (!s) return -2;
-    for (int32_t r = 0; r < num_seqs; ++r) {
-        int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
-        int64_t context = (int64_t)seq_lens[r] - q_len;
-        for (int32_t i = 0; i < q_len; ++i) {
-            int64_t row = (int64_t)query_start_loc[r] + i;
-            for (int32_t h = 0; h < num_heads; ++h)
-                attend_row(out + (row * num_heads + h) * head_dim,
-                           q + (row * num_heads + h) * head_dim, key_cache, value_cache,
-                           block_tables + (int64_t)r * max_blocks_per_seq, context + i + 1,
-                           h / group, num_kv_heads, head_dim, block_size, scale, s);
+    int failed = 0;
+    /* one (request, q head) per iteration, its query rows in order */
+#pragma omp parallel num_threads(g_threads) reduction(|| : failed)
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t rh = 0; rh < (int64_t)num_seqs * num_heads; ++rh) {
+                int32_t r = (int32_t)(rh / num_heads), h = (int32_t)(rh % num_heads);
+                int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
+                int64_t context = (int64_t)seq_lens[r] - q_len;
+                for (int32_t i = 0; i < q_len; ++i) {
+                    int64_t row = (int64_t)query_start_loc[r] + i;
+                    attend_row(out + (row * num_heads + h) * head_dim,
+                               q + (row * num_heads + h) * head_dim, key_cache, value_cache,
+                               block_tables + (int64_t)r * max_blocks_per_seq, context + i + 1,
+                               h / group, num_kv_heads, head_dim, block_size, scale, s);
+                }
+            }
+            free(s);
         }
     }
-    free(s);
-    return 0;
+    return failed ? -2 : 0;
 }
 
 /* ---- Online softmax over tiles (page 1 section 2.2) --------------------

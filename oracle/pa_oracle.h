@@ -15,6 +15,10 @@
 extern "C" {
 #endif
 
+/* Threads of the attention loops (default 1); results do not depend on it. */
+void oracle_set_threads(int32_t n);
+/* Processors OpenMP sees (1 when built without OpenMP). */
+int32_t oracle_max_threads(void);
 int64_t oracle_slot(const int32_t* block_table_row, int32_t block_size, int64_t position);
 void oracle_query_start_loc(const int32_t* q_lens, int32_t num_seqs, int32_t* query_start_loc);
 void oracle_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,

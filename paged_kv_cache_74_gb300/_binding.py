@@ -81,7 +81,7 @@ def _declare(lib):
                               _i32, _i32, _f32, _i32, _vp, _sz, _vp]
     lib.pa_decode_noalloc.restype = ctypes.c_int
     lib.pa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
-                                      _i32, _i32, _i32, _f32, _i32, _vp]
+                                      _i32, _i32, _i32, _f32, _i32, _vp, _vp]
     lib.pa_prefill_workspace_size.restype = _sz
     lib.pa_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     lib.pa_prefill_varlen.restype = ctypes.c_int
@@ -95,7 +95,7 @@ def library_path() -> str:
 
 
 def load_library(path: str | None = None):
-    """Load libpa.so (it must have been built; see build.py).  Raises if absent."""
+    """Load libpa.so (built by paged_kv_cache_74_gb300.build()).  Raises if absent."""
     global _lib
     with _lock:
         if _lib is None or path is not None:
@@ -414,10 +414,12 @@ def decode_xsplit_fp8(q, key_cache, value_cache, block_tables, seq_lens, max_seq
 
 
 def decode_noalloc(q, key_cache, value_cache, block_tables, seq_lens, max_seq_len, scale,
-                   out=None, partition_tokens=0):
+                   out=None, partition_tokens=0, status=None):
     """pa_decode without a workspace: for callers that cannot allocate device
     memory.  Scratch comes from a fixed-size array inside the library (see
-    include/pa.h); calls that overlap on the GPU must be serialised."""
+    include/pa.h); calls that overlap on the GPU must be serialised.  status:
+    optional int32[4] CUDA tensor that receives the call's device status
+    record."""
     _contig("q", q, torch.bfloat16)
     _contig("key_cache", key_cache, torch.bfloat16)
     _contig("value_cache", value_cache, torch.bfloat16)
@@ -432,7 +434,7 @@ def decode_noalloc(q, key_cache, value_cache, block_tables, seq_lens, max_seq_le
     _check("pa_decode_noalloc", lib.pa_decode_noalloc(
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, int(max_seq_len), hq, hkv, d, bs, nb,
-        float(scale), int(partition_tokens), _stream()))
+        float(scale), int(partition_tokens), _ptr(status), _stream()))
     return out
 
 

@@ -300,7 +300,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     fence_mbar_init();
   }
   __syncthreads();
-  griddep_wait();  // the cache write before this launch may still be finishing
+  if (!a.defer_griddep) griddep_wait();  // the cache write before this launch may still be finishing
 
   if (warp == C::NC) {
     // ================================================================ producer
@@ -530,6 +530,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         (void)mbar_wait(full0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1);
       for (int k = 0; k < 2; ++k) (void)mbar_wait(qfull0 + 8 * k, 0);
     }
+    // Deferred dependency: the CTA completes only after the previous grid.
+    if (a.defer_griddep && lane == 0) griddep_wait();
     return;
   }
 

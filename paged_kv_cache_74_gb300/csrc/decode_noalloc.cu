@@ -50,7 +50,7 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* key
                                        int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                        int32_t num_blocks, float scale, int32_t partition_tokens,
-                                       void* stream) {
+                                       int32_t* device_status, void* stream) {
   // Argument checks only: with no workspace, pa_decode validates everything
   // else and then answers PA_ERR_WORKSPACE without launching anything.
   const pa_status check =
@@ -58,6 +58,8 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* key
                 num_seqs, max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                 scale, partition_tokens, nullptr, 0, stream);
   if (check != PA_ERR_WORKSPACE) return check;  // invalid arguments, or nothing to do
+  if (device_status != nullptr && reinterpret_cast<uintptr_t>(device_status) % 4 != 0)
+    return PA_ERR_INVALID;
   const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                                max_seq_len, partition_tokens);
   if (need == 0 || need > PA_DECODE_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
@@ -65,10 +67,16 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* key
   if (scratch == nullptr) return PA_ERR_CUDA;
   // The device status record at the start of the scratch must start at
   // zero; the split-KV partials are always written before they are read.
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, 16, st) != cudaSuccess) return PA_ERR_CUDA;
-  return pa_decode(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
-                   num_seqs, max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
-                   num_blocks, scale, partition_tokens, scratch, PA_DECODE_NOALLOC_SCRATCH_BYTES,
-                   stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, 16, cs) != cudaSuccess) return PA_ERR_CUDA;
+  const pa_status st =
+      pa_decode(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                num_seqs, max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                scale, partition_tokens, scratch, PA_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+  if (st != PA_OK || device_status == nullptr) return st;
+  // The record lives in the shared scratch, which the caller cannot see:
+  // hand this call's record over, in stream order.
+  return cudaMemcpyAsync(device_status, scratch, 16, cudaMemcpyDeviceToDevice, cs) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }

@@ -223,7 +223,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  griddep_wait();  // the cache write before this launch may still be finishing
+  if (!a.defer_griddep) griddep_wait();  // the cache write before this launch may still be finishing
   const uint32_t tmem = *tmem_slot;
   auto give_up = [&](int where) {
     record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, where);
@@ -936,6 +936,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Deferred dependency: the CTA completes only after the previous grid.
+  if (a.defer_griddep && tid == 0) griddep_wait();
 }
 
 template <int D, int GM>

@@ -6,7 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
-#include <mutex>
+#include <mutex>  // std::call_once
 
 #include "pa_internal.h"
 
@@ -292,35 +292,6 @@ DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int he
   return L;
 }
 
-// A side stream (and fork / join events) per device, created on first use
-// and kept for the life of the process: pa_prefill_varlen runs the prefill
-// tiles on it, concurrently with the decode rows on the caller's stream.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_side_mu;
-SideStream g_side[64];
-
-const SideStream* side_stream_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(g_side_mu);
-  SideStream& s = g_side[dev];
-  if (s.stream == nullptr) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t f = nullptr, j = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess)
-      return nullptr;
-    s.stream = st;
-    s.fork = f;
-    s.join = j;
-  }
-  return &s;
-}
-
 // A distinct non-zero tag per decode launch (see the pair counters).
 unsigned next_epoch() {
   static std::atomic<unsigned> epoch{0};
@@ -379,7 +350,7 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t num_blocks, int32_t block_size, float scale,
                              const DecodeLayout& L, void* workspace, cudaStream_t stream,
-                             const KvFormat& kv = KvFormat()) {
+                             const KvFormat& kv = KvFormat(), bool after_prefill = false) {
   // The TMA views address the cache in 16-token tiles.
   const int num_tiles16 = num_blocks * (block_size / kBlockSize);
   const int group = num_heads / num_kv_heads;
@@ -433,6 +404,7 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.epoch = next_epoch();
   a.scale_log2 = scale * 1.4426950408889634f * kv.k_scale;
   a.v_scale = kv.v_scale;
+  a.defer_griddep = after_prefill ? 1 : 0;
   if (tc && kv.e4m3) return PA_ERR_UNSUPPORTED;
   const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, stream)
                             : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, kv.xsplit, stream);
@@ -832,23 +804,15 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
       p.num_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, upper)));
     }
     p.scale_log2 = scale * 1.4426950408889634f;
-    // The tiles run on a side stream, forked from and joined back into the
-    // caller's stream, so they overlap the decode rows.
-    const SideStream* side = side_stream_current_device();
-    if (side == nullptr) return PA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_side_mu);  // one fork / join at a time per process
-    if (cudaEventRecord(side->fork, cs) != cudaSuccess ||
-        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-      return PA_ERR_CUDA;
-    if (launch_prefill(p, qmap, kmap, vmap, head_dim, side->stream) != cudaSuccess) return PA_ERR_CUDA;
-    const pa_status st = launch_decode_rows(out, q, key_cache, value_cache, block_tables,
-                                            max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
-                                            total_q, max_seq_len, num_heads, num_kv_heads, head_dim,
-                                            num_blocks, block_size, scale, L, workspace, cs);
-    if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
-        cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess)
-      return PA_ERR_CUDA;
-    return st;
+    // Both kernels go on the caller's stream.  The tile kernel lets the
+    // decode launch start once the kernels before this call are complete;
+    // the decode CTAs then take the SMs the tiles leave free, and the decode
+    // launch completes only after the tile kernel.
+    if (launch_prefill(p, qmap, kmap, vmap, head_dim, cs) != cudaSuccess) return PA_ERR_CUDA;
+    return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                              seq_lens, query_start_loc, num_seqs, total_q, max_seq_len,
+                              num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, L,
+                              workspace, cs, KvFormat(), true);
   }
   // Only decode rows: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,

@@ -50,6 +50,13 @@ struct DecodeArgs {
   unsigned epoch;                   // distinct per call (never 0)
   float scale_log2;                 // softmax scale * log2(e) (* k_scale for an e4m3 cache)
   float v_scale;                    // multiplies O: the e4m3 cache's V scale, else 1
+  // 0: wait for the previous kernel in the stream (griddep_wait) before the
+  // first global access.  1: this launch follows the prefill tile kernel of
+  // the same pa_prefill_varlen call, which only lets it start once the
+  // kernels before the call are complete; the decode rows do not read what
+  // the tiles write, so the wait moves to the end of the CTA (the launch
+  // then completes after the tile kernel, which keeps stream order).
+  int defer_griddep;
 };
 
 // Launch `kernel` on `stream` with programmatic stream serialization: the

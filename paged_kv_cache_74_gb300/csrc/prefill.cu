@@ -170,6 +170,11 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
     tmem_relinquish();
   }
+  // The kernels before this launch (the cache write of this step's tokens)
+  // must be complete before anything is read.  Only then may the decode
+  // rows of the same call start: they run on the SMs these tiles leave free.
+  griddep_wait();
+  griddep_launch_dependents();
   if (blockIdx.x == 0 && warp == 1) report_bad_prefill_rows(a, lane);
   tc_fence_before();
   __syncthreads();
@@ -555,8 +560,8 @@ cudaError_t launch_prefill_impl(const PrefillArgs& a, const CUtensorMap& qmap,
   cudaError_t err = cudaFuncSetAttribute(prefill_tile_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  prefill_tile_kernel<D><<<a.num_ctas, C::THREADS, C::SMEM, stream>>>(qmap, kmap, vmap, a);
-  return cudaGetLastError();
+  return launch_overlapped(prefill_tile_kernel<D>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
+                           stream, qmap, kmap, vmap, a);
 }
 
 }  // namespace

@@ -29,8 +29,12 @@ def read_golden(name):
 
 @pytest.fixture(scope="session")
 def oracle():
+    """The oracle on every host core (its threads only spread independent
+    output rows; the results equal the single-thread ones bit for bit)."""
     from oracle import Oracle
-    return Oracle()
+    o = Oracle()
+    o.set_threads(o.max_threads())
+    return o
 
 
 @pytest.fixture(scope="session")

@@ -40,6 +40,17 @@ def test_abi_version_matches_header(lib):
     assert lib.pa_abi_version() == int(m.group(1))
 
 
+def test_library_owns_no_stream_or_event():
+    """Every call enqueues on the caller's stream only: the library creates
+    no stream and no event (no hidden ordering between callers' streams, and
+    nothing to create before a stream capture)."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_74_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        for call in ("cudaStreamCreate", "cudaEventCreate", "cuStreamCreate", "cuEventCreate"):
+            assert call not in text, f"{name} calls {call}"
+
+
 def test_status_strings(lib):
     for s in range(5):
         assert lib.pa_status_string(s).decode().startswith("PA_")

@@ -29,8 +29,8 @@ MUTATIONS = [
     ("score_drops_scale", "s[t] = scale * dot;", "s[t] = dot;", ["sdpa_decode"]),
     ("softmax_adds_epsilon", "double p = s[t] / l;", "double p = s[t] / (l + 1e-6);",
      ["sdpa_decode"]),
-    ("gqa_wrong_kv_head", "h / group, num_kv_heads, head_dim, block_size, scale, s);\n    free(s);\n    return 0;\n}\n\n/* ---- Varlen",
-     "h % num_kv_heads, num_kv_heads, head_dim, block_size, scale, s);\n    free(s);\n    return 0;\n}\n\n/* ---- Varlen", ["sdpa_decode"]),
+    ("gqa_wrong_kv_head", "h / group, num_kv_heads, head_dim, block_size, scale, s);\n            }\n            free(s);\n        }\n    }\n    return failed ? -2 : 0;\n}\n\n/* ---- Varlen",
+     "h % num_kv_heads, num_kv_heads, head_dim, block_size, scale, s);\n            }\n            free(s);\n        }\n    }\n    return failed ? -2 : 0;\n}\n\n/* ---- Varlen", ["sdpa_decode"]),
     ("value_row_reversed_in_block",
      "const uint16_t* v = value_cache + ((phys * block_size + off) * num_kv_heads",
      "const uint16_t* v = value_cache + ((phys * block_size + (block_size - 1 - off)) * num_kv_heads",
@@ -39,6 +39,10 @@ MUTATIONS = [
     ("online_forgets_to_rescale_l", "l *= alpha;", "/* l not rescaled */", ["online"]),
     ("merge_drops_rescale", "L += l_parts[p] * exp(m_parts[p] - m);", "L += l_parts[p];",
      ["merge"]),
+    ("writer_writes_past_the_pool",
+     "if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;\n        int64_t block = slot / block_size;\n        int64_t offset",
+     "if (slot < 0) continue;\n        int64_t block = slot / block_size;\n        int64_t offset",
+     ["writer_pool_end"]),
     ("writer_shifts_offset", "int64_t offset = slot % block_size;\n        for",
      "int64_t offset = (slot + 1) % block_size;\n        for", ["writer"]),
     ("kernel_ids_transposed", "(int32_t)((int64_t)ids[i] * k + j)", "(int32_t)((int64_t)ids[i] + j * k)",
@@ -83,6 +87,7 @@ PINS = {
     "online": lambda o: pins.test_online_softmax_equals_direct(o, "block16"),
     "merge": lambda o: pins.test_partition_merge_equals_global_softmax(o),
     "writer": lambda o: pins.test_reshape_and_cache_scatter(o),
+    "writer_pool_end": lambda o: pins.test_reshape_and_cache_skips_slots_past_the_pool(o),
     "xsplit_layout": lambda o: pins.test_xsplit_writer_places_elements_at_the_pages_shape(o, 2, 64, 16),
     "xsplit_decode": lambda o: pins.test_decode_xsplit_equals_decode_of_the_same_cache(
         o, 4, 2, 64, [25, 12, 37, 20], 16),

@@ -305,6 +305,36 @@ def test_reshape_and_cache_scatter(oracle):
             np.testing.assert_array_equal(vc[s], vc0[s])
 
 
+def test_reshape_and_cache_skips_slots_past_the_pool(oracle):
+    """A slot at or past num_blocks * block_size names no cache row: the
+    writer must leave every byte alone, including memory just past the pool
+    (the C function is handed a larger buffer and told the pool is smaller,
+    so a missing check writes into the spare rows instead of out of bounds)."""
+    import ctypes
+    nb_real, nb_told, B, H, d = 6, 4, 16, 2, 8
+    gen = np.random.default_rng(11)
+    key = gen.integers(0, 1 << 16, (4, H, d), dtype=np.uint16)
+    val = gen.integers(0, 1 << 16, (4, H, d), dtype=np.uint16)
+    kc = gen.integers(0, 1 << 16, (nb_real, B, H, d), dtype=np.uint16)
+    vc = gen.integers(0, 1 << 16, (nb_real, B, H, d), dtype=np.uint16)
+    kc0, vc0 = kc.copy(), vc.copy()
+    slots = np.array([nb_told * B, nb_told * B + 17, 3, nb_told * B - 1], np.int64)
+    u16 = ctypes.POINTER(ctypes.c_uint16)
+    i64 = ctypes.POINTER(ctypes.c_int64)
+    oracle.lib.oracle_reshape_and_cache(key.ctypes.data_as(u16), val.ctypes.data_as(u16), 4, H, d,
+                                        kc.ctypes.data_as(u16), vc.ctypes.data_as(u16), nb_told, B,
+                                        slots.ctypes.data_as(i64))
+    kf, vf, kf0, vf0 = (a.reshape(-1, H, d) for a in (kc, vc, kc0, vc0))
+    for s in range(nb_real * B):
+        if s == 3 or s == nb_told * B - 1:
+            i = 2 if s == 3 else 3
+            np.testing.assert_array_equal(kf[s], key[i])
+            np.testing.assert_array_equal(vf[s], val[i])
+        else:
+            np.testing.assert_array_equal(kf[s], kf0[s])
+            np.testing.assert_array_equal(vf[s], vf0[s])
+
+
 def test_reshape_then_slot_mapping_places_token_where_decode_reads_it(oracle):
     """Writing each request's last token through the slot mapping and then
     decoding is the same as decoding a pool that already held those keys."""
@@ -588,3 +618,26 @@ def test_decode_xsplit_fp8_equals_decode_fp8_of_the_same_cache(oracle, hq, hkv, 
     kx, vx = _to_xsplit8(kc8, vc8)
     got = oracle.decode_xsplit_fp8(q, kx, vx, w.block_tables, w.seq_lens, w.scale, 0.5, 0.125)
     np.testing.assert_array_equal(got, ref)
+
+
+def test_thread_count_does_not_change_results(oracle):
+    """The OpenMP loops only spread independent output rows: decode and
+    varlen prefill on several threads give the single-thread doubles bit for
+    bit (the all-core CPU baseline times the same arithmetic)."""
+    w = wl.random_workload(21, num_seqs=5, max_len=300, min_len=20, num_heads=8, num_kv_heads=2,
+                           head_dim=64, max_q_len=40, prefill_fraction=0.6)
+    t = wl.make_tensors(w)
+    b = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    runs = []
+    for n in (1, 4):
+        oracle.set_threads(n)
+        try:
+            runs.append((oracle.decode(b(t.q)[:w.num_seqs], b(t.key_cache), b(t.value_cache),
+                                       w.block_tables, w.seq_lens, w.scale),
+                         oracle.prefill_varlen(b(t.q), b(t.key_cache), b(t.value_cache),
+                                               w.query_start_loc, w.seq_lens, w.block_tables,
+                                               w.scale)))
+        finally:
+            oracle.set_threads(1)
+    np.testing.assert_array_equal(runs[0][0], runs[1][0])
+    np.testing.assert_array_equal(runs[0][1], runs[1][1])

@@ -21,13 +21,15 @@ pytestmark = pytest.mark.gpu
 PA_ERR_WORKSPACE = 3
 
 
-def _noalloc(lib, w, t, out, partition_tokens):
+def _noalloc(lib, w, t, out, partition_tokens, status=None, block_tables=None):
     vp = ctypes.c_void_p
+    bt = t.block_tables if block_tables is None else block_tables
     return lib.pa_decode_noalloc(
         vp(out.data_ptr()), vp(t.q.data_ptr()), vp(t.key_cache.data_ptr()),
-        vp(t.value_cache.data_ptr()), vp(t.block_tables.data_ptr()), w.max_blocks_per_seq,
+        vp(t.value_cache.data_ptr()), vp(bt.data_ptr()), w.max_blocks_per_seq,
         vp(t.seq_lens.data_ptr()), w.num_seqs, w.max_seq_len, w.num_heads, w.num_kv_heads,
         w.head_dim, w.block_size, w.num_blocks, ctypes.c_float(w.scale), partition_tokens,
+        vp(status.data_ptr() if status is not None else 0),
         vp(torch.cuda.current_stream().cuda_stream))
 
 
@@ -47,8 +49,10 @@ def test_noalloc_matches_workspace_decode_on_consecutive_calls(cuda_lib):
         ref = pa.decode(t.q, t.key_cache, t.value_cache, t.block_tables, t.seq_lens,
                         w.max_seq_len, w.scale, partition_tokens=pt)
         out = torch.full_like(t.q, float("nan"))
-        assert _noalloc(lib, w, t, out, pt) == 0
+        status = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+        assert _noalloc(lib, w, t, out, pt, status) == 0
         torch.cuda.synchronize()
+        assert status.tolist() == [0, 0, 0, 0]  # this call's record: no device error
         err = (out.double() - ref.double()).abs()
         assert torch.isfinite(out.float()).all()
         assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
@@ -66,6 +70,29 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     rc = lib.pa_decode_noalloc(vp(t.q.data_ptr()), vp(t.q.data_ptr()), vp(t.key_cache.data_ptr()),
                                vp(t.value_cache.data_ptr()), vp(t.block_tables.data_ptr()),
                                32768 // 16, vp(t.seq_lens.data_ptr()), 64, 32768, 32,
-                               8, 128, 16, w.num_blocks, ctypes.c_float(0.1), 16,
+                               8, 128, 16, w.num_blocks, ctypes.c_float(0.1), 16, vp(0),
                                vp(torch.cuda.current_stream().cuda_stream))
     assert rc == PA_ERR_WORKSPACE
+
+
+def test_noalloc_reports_device_errors_through_device_status(cuda_lib):
+    """The kernels' status record lives in the library's scratch array; the
+    call hands it to the caller's device_status.  A block id outside the pool
+    is range-checked in the kernel (never dereferenced: the tile reads as
+    zeros) and must come back as PA_DEV_BAD_BLOCK_ID with its request and
+    value; the next clean call must report a clean record again."""
+    pa = cuda_lib
+    lib = pa.load_library()
+    w, t = _case(74, 900)
+    bad = t.block_tables.clone()
+    bad_row = 5
+    bad[bad_row, 0] = w.num_blocks + 3  # outside the pool
+    out = torch.empty_like(t.q)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    assert _noalloc(lib, w, t, out, 128, status, block_tables=bad) == 0
+    torch.cuda.synchronize()
+    rec = status.tolist()
+    assert rec[0] == 2 and rec[1] == bad_row and rec[2] == w.num_blocks + 3, rec
+    assert _noalloc(lib, w, t, out, 128, status) == 0
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0, 0]
