@@ -420,20 +420,24 @@ def causal_pairs(w: wl.Workload) -> int:
 
 
 def _time(call, flush, reps):
+    """Median device time of `call` over `reps` calls, each after an L2
+    flush, events on the launching stream.  The calls are enqueued back to
+    back (one synchronisation at the end), so a call's events measure the
+    GPU's work, not the host's time to enqueue it (the flush before each
+    call gives the host ample lead)."""
     for _ in range(3):
         flush()
         call()
-    ms = []
-    for _ in range(reps):
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
         flush()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         a.record()
         call()
         b.record()
-        b.synchronize()
-        ms.append(a.elapsed_time(b))
-    return statistics.median(ms) / 1e3
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
 
 
 def extra_mixed(pa, name, dev, flush, reps=20, cpu=True):

@@ -1018,12 +1018,18 @@ cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t stream) {
   using C = DecodeCfg<D, GMAX, KV8, XS>;
   auto* kernel = paged_decode_kernel<D, GMAX, KV8, XS>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-  if (err != cudaSuccess) return err;
+  static bool attr_set[64] = {false};  // per device: set once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
   return launch_overlapped(kernel, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM, stream, kmap,
                            vmap, a);
 }

@@ -944,9 +944,15 @@ template <int D, int GM>
 cudaError_t launch_decode_tc_impl(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, cudaStream_t stream) {
   using C = TcCfg<D, GM>;
-  cudaError_t err = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (err != cudaSuccess) return err;
+  static bool attr_set[64] = {false};  // per device: set once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    const cudaError_t err = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GM>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
   return launch_overlapped(paged_decode_tc_kernel<D, GM>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
                            stream, qmap, kmap, vmap, a);
 }

@@ -292,6 +292,37 @@ DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int he
   return L;
 }
 
+// The prefill kernel's part of a pa_prefill_varlen workspace, after the
+// decode rows' part: one counter per work unit (an upper bound on the units:
+// a request of q_len rows has ceil(q_len / 128) query tiles, each with one
+// unit per head pair), then the partial records of the persistent grid.
+struct PrefillLayout {
+  int num_ctas = 0;
+  long long max_units = 0;
+  size_t counters_offset = 0, ml_offset = 0, o_offset = 0, total = 0;
+};
+
+PrefillLayout prefill_layout(size_t base, int num_seqs, int total_q, int num_heads,
+                             int num_kv_heads, int head_dim) {
+  PrefillLayout P;
+  int sms = sm_count_current_device();
+  if (sms <= 0) sms = 148;
+  P.num_ctas = sms;
+  const int group = num_heads / num_kv_heads;
+  const long long pairs = static_cast<long long>(num_kv_heads) * ((group + 1) / 2);
+  P.max_units = (static_cast<long long>(total_q) / 128 + num_seqs) * pairs;
+  size_t off = align_up(base, 256);
+  P.counters_offset = off;
+  off = align_up(off + static_cast<size_t>(P.max_units) * 8, 256);
+  P.ml_offset = off;
+  off = align_up(off + static_cast<size_t>(P.num_ctas) * 2 * 2 * 128 * 2 * sizeof(float), 256);
+  P.o_offset = off;
+  off += prefill_partials_bytes(P.num_ctas, head_dim) -
+         static_cast<size_t>(P.num_ctas) * 2 * 2 * 128 * 2 * sizeof(float);
+  P.total = align_up(off, 256);
+  return P;
+}
+
 // A distinct non-zero tag per decode launch (see the pair counters).
 unsigned next_epoch() {
   static std::atomic<unsigned> epoch{0};
@@ -332,7 +363,7 @@ pa_status check_decode_args(const void* out, const void* q, const void* key_cach
   if (max_blocks_per_seq < 1 || max_seq_len < 1 ||
       static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PA_ERR_INVALID;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID;
   return PA_OK;
 }
 
@@ -740,7 +771,10 @@ pa_status pa_decode_xsplit_fp8(void* out, const void* q, const void* key_cache,
 size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len) {
   if (total_q < 0) return 0;
-  return pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
+  const size_t dec =
+      pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
+  if (dec == 0) return 0;
+  return prefill_layout(dec, num_seqs, total_q, num_heads, num_kv_heads, head_dim).total;
 }
 
 pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
@@ -761,7 +795,10 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
   if (num_seqs == 0 || total_q == 0) return PA_OK;
   const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, 0);
   if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  const PrefillLayout PL =
+      prefill_layout(L.total, num_seqs, total_q, num_heads, num_kv_heads, head_dim);
+  if (!workspace || workspace_bytes < (max_query_len > 1 ? PL.total : L.total))
+    return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (max_query_len > 1) {
@@ -774,11 +811,10 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
         !make_kv_group_map(&vmap, value_cache, num_blocks * (block_size / kBlockSize), num_kv_heads,
                            head_dim))
       return PA_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrefillArgs p;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.q = static_cast<const __nv_bfloat16*>(q);
-    p.key_cache = static_cast<const __nv_bfloat16*>(key_cache);
-    p.value_cache = static_cast<const __nv_bfloat16*>(value_cache);
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.query_start_loc = query_start_loc;
@@ -794,15 +830,12 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     p.block_size = block_size;
     p.tile_shift = tile_shift_of(block_size);
     p.total_q = total_q;
-    {
-      // At most one CTA per SM (the tile needs ~227 KB of shared memory) and
-      // never more than the batch can have tiles.
-      const int64_t upper = static_cast<int64_t>(num_seqs) * num_heads *
-                            ceil_div(max_query_len, 128);
-      int sms = sm_count_current_device();
-      if (sms <= 0) sms = 148;
-      p.num_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, upper)));
-    }
+    p.num_ctas = PL.num_ctas;  // one CTA per SM
+    p.max_units = PL.max_units;
+    p.counters = reinterpret_cast<unsigned long long*>(ws + PL.counters_offset);
+    p.part_ml = reinterpret_cast<float*>(ws + PL.ml_offset);
+    p.part_o = reinterpret_cast<float*>(ws + PL.o_offset);
+    p.epoch = next_epoch();
     p.scale_log2 = scale * 1.4426950408889634f;
     // Both kernels go on the caller's stream.  The tile kernel lets the
     // decode launch start once the kernels before this call are complete;

@@ -101,17 +101,24 @@ int decode_gmax(int group);
 // CTAs per SM the decode kernel for (head_dim, group) is built for.
 int decode_ctas_per_sm(int head_dim, int group);
 
-// Chunked-prefill tiles (prefill.cu): 128-row query tiles of one q head of
-// every request with q_len > 1, taken in turn by a persistent grid.
+// Chunked-prefill attention (prefill.cu).  Work unit: 128 query rows of one
+// request with q_len > 1 for two q heads of the same kv head (one head when
+// the group has no partner left), over all the keys those rows see, in
+// 128-key steps.  The steps of all units are numbered (request-major, then
+// query tile from the last, then head pair, then key step) and cut into
+// num_ctas equal contiguous ranges, one per CTA of a persistent grid; a unit
+// cut by a range boundary is finished by merging its pieces' (m, l, O)
+// partials, by the contributor that finishes last.
 struct PrefillArgs {
   __nv_bfloat16* out;               // [total_q, num_heads, D]
   const __nv_bfloat16* q;           // [total_q, num_heads, D]
-  const __nv_bfloat16* key_cache;   // [num_blocks * 16, num_kv_heads, D]
-  const __nv_bfloat16* value_cache; // same layout
   const int32_t* block_tables;      // [num_seqs, max_blocks_per_seq]
   const int32_t* seq_lens;          // [num_seqs]
   const int32_t* query_start_loc;   // [num_seqs + 1]
   int32_t* status;                  // device status record (may be null)
+  unsigned long long* counters;     // [max_units] (epoch << 32 | contributions)
+  float* part_ml;                   // [num_ctas][2][2 heads][128 rows][2]  (m in log2 units, l)
+  float* part_o;                    // [num_ctas][2][2 heads][D][128 rows]  normalised partial O
   int max_blocks_per_seq;
   int num_seqs;
   int num_heads;
@@ -123,9 +130,13 @@ struct PrefillArgs {
   int block_size;                   // tokens per cache block: 16, 32 or 64
   int tile_shift;                   // log2(block_size / 16)
   int total_q;
-  int num_ctas;                     // persistent grid (at most one CTA per SM)
-  float scale_log2;
+  int num_ctas;                     // persistent grid (one CTA per SM)
+  long long max_units;              // size of `counters`
+  unsigned epoch;                   // distinct per call (never 0)
+  float scale_log2;                 // softmax scale * log2(e)
 };
+// Bytes of the prefill partial records (part_ml and part_o) for num_ctas CTAs.
+size_t prefill_partials_bytes(int num_ctas, int head_dim);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
 

@@ -1,55 +1,63 @@
-// prefill.cu -- chunked-prefill attention tiles of a varlen batch on the
-// sm_103a tensor cores (tcgen05).
+// prefill.cu -- chunked-prefill attention of a varlen batch on the sm_103a
+// tensor cores (tcgen05).
 //
 // Method ("分块预填充与混合批处理", section 11.6; "vLLM 深度解析（二）：
-// PagedAttention 核心机制", sections 2.1, 2.2, 3.1 and 5.2): request r owns
-// query rows query_start_loc[r] .. query_start_loc[r+1] - 1; with q_len rows
-// and K/V length seq_len, row i sits at position ctx + i (ctx = seq_len -
-// q_len) and attends keys 0 .. ctx + i, read through the block table.
-// O = softmax(scale * Q K^T) V is computed tile by tile with the online
-// softmax state (m, l) per row and never materialises S or P in HBM.
+// PagedAttention 核心机制", sections 2.1, 2.2, 3.1, 3.2.9 and 5.2): request r
+// owns query rows query_start_loc[r] .. query_start_loc[r+1] - 1; with q_len
+// rows and K/V length seq_len, row i sits at position ctx + i (ctx = seq_len
+// - q_len) and attends keys 0 .. ctx + i, read through the block table.
+// O = softmax(scale * Q K^T) V is computed 128 keys at a time with the
+// online softmax state (m, l) per row; S and P never reach HBM.  Pieces of a
+// row's keys computed by different CTAs are merged through their (m_j, l_j,
+// O_j): m = max m_j, L = sum l_j 2^(m_j - m), O = sum O_j l_j 2^(m_j - m) / L.
 //
-// GB300 design.  One CTA owns 128 query rows of one q head of one request
-// and is warp-specialised:
-//   warps 8, 10 producers: TMA (128-byte swizzle) loads the Q tile once
-//               (warp 8) and K (warp 8) and V (warp 10) tiles of 128 keys:
-//               eight 16-token blocks gathered through the block table, one
-//               copy per block that lands as [8-key group][head_dim half]
-//               [8 keys][128 B], a layout both MMAs read directly.  Two-stage
-//               rings; a K stage is refilled as soon as its S MMA is done, a
-//               V stage as soon as its P.V MMA is done;
-//   warp 9      MMA issuer (tcgen05, kind::f16, bf16 in, fp32 accumulate in
-//               TMEM):
-//                 S_j = Q K_j^T  M = N = 128, K = head_dim, both operands
-//                                K-major, into one of two TMEM S buffers;
-//                 O  += P_j V_j  M = 128, N = head_dim, K = 128 keys; P_j from
-//                                one of two shared-memory buffers (K-major),
-//                                V as an MN-major operand exactly as TMA
-//                                stored it; O accumulates in TMEM.
-//               S_{j+2} is issued as soon as softmax j has S_j in registers
-//               and K_{j+2} has landed (before P_j V_j), so the softmax warps
-//               find S waiting and run tile after tile without a gap;
-//   warps 0-7   softmax: two warps share each 32-row quarter of TMEM and
-//               split the key columns (and the columns of O); each reads its
-//               part of S_j (tcgen05.ld), applies the causal and length
-//               masks, exchanges the row maximum with its partner through two
-//               TMEM columns, and writes P_j = exp2(S_j * scale * log2 e - m)
-//               as bf16 into the swizzled layout the P.V MMA reads (the
-//               scale-and-shift and the row sums two values at a time with
-//               packed fp32 instructions; l sums the fp32 weights).
-// The reference m of a row moves only when a tile's max exceeds it by more
-// than 2^8; then that row of O (in TMEM) and its sum l are rescaled first
-// (the final O / l is exact for any reference).  V rows of keys that are out
-// of context or were not loaded are zeroed first: they may hold NaN, and a
-// zero weight does not cancel a NaN inside the MMA.  Every wait is bounded.
+// GB300 design.
+// * Work unit: 128 query rows of one request for TWO q heads of the same kv
+//   head (slots 0 and 1; one head when the group has an odd head left).
+//   Every K/V tile is copied into shared memory once and serves both heads.
+// * Persistent grid, one CTA per SM.  The 128-key steps of all units are
+//   numbered (request-major; within a request the last query tile, which
+//   sees the most keys, first; then head pair; then key step) and cut into
+//   equal contiguous ranges, one per CTA, so every SM gets the same number
+//   of MMA steps whatever the mix of chunk lengths.  A unit cut by a range
+//   boundary is finished by whichever of its contributors counts last on
+//   an epoch-tagged counter: it merges the pieces' partials.
+// * Per step and slot b: S_b = Q_b K^T (M = N = 128, K = head_dim) into TMEM
+//   columns [128 b, 128 b + 128); the softmax warps of slot b read S_b, write
+//   P_b = 2^(S_b * scale * log2 e - m) as bf16 over the first 64 of those
+//   columns, and O_b += P_b V (A = P_b read from TMEM, B = V from shared
+//   memory, MN-major) accumulates in TMEM columns 256 + b * head_dim.  The
+//   MMA warp issues P_0 V, then S_0 of the next step, then P_1 V, then S_1
+//   of the next step: while the tensor core works for one slot the other
+//   slot's softmax runs (ping-pong).
+// * The reference m of a row moves only when a step's maximum exceeds it by
+//   more than 2^8; O (in TMEM) and l are rescaled then (S_b completing
+//   implies the P_b V before it has completed, so O_b is current).
+// * Warp roles (352 threads): warp 0 Q and K producer (TMA; each 16-token
+//   block of a 128-key tile is one copy that lands as [8-key group][head_dim
+//   half][8 keys][128 B], the layout both MMAs read) and the range walk;
+//   warp 10 V producer; warp 1 MMA issuer; warps 2-5 softmax of slot 0 and
+//   warps 6-9 of slot 1 (thread = query row, all 128 columns of S), which
+//   also write the output, the partials and the merge.
+// V rows of keys that are out of context or were not loaded are zeroed
+// before the P.V product (a zero weight does not cancel a NaN inside the
+// MMA).  Every wait is bounded; a timeout records PA_DEV_WAIT_TIMEOUT.
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
+#include "work_split.cuh"
 
 namespace pa {
 namespace {
 
 constexpr float kNegBigP = -1e30f;
 constexpr float kRescaleSlackP = 8.0f;  // log2 units
+constexpr int kSegWhole = 0;            // the whole unit: bf16 output
+constexpr int kSegHead = 1;             // continues a unit begun by an earlier CTA: partial slot 0
+constexpr int kSegTail = 2;             // begins a unit finished by later CTAs: partial slot 1
+constexpr int kSegEnd = 3;              // no more work
+// Split costs (see the producer): a key step, and the start of a unit.
+constexpr long long kCostStep = 4;
+constexpr long long kCostUnit = 10;
 
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -66,66 +74,107 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int D>
 struct PrefillCfg {
-  static constexpr int BM = 128;                    // query rows per CTA
-  static constexpr int BN = 128;                    // keys per K/V tile (8 blocks)
+  static constexpr int BM = 128;                    // query rows per unit
+  static constexpr int BN = 128;                    // keys per step (8 blocks of 16)
   static constexpr int HALVES = D / 64;             // 128-byte column chunks of head_dim
-  static constexpr int CHUNK = 128 * 128;           // one 128-row x 128-byte swizzled chunk
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + HALVES * CHUNK;         // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * HALVES * CHUNK;     // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * HALVES * CHUNK;     // 2 buffers x 2 key halves
-  static constexpr int NBAR = 16;
-  static constexpr int OFF_BAR = OFF_P + 4 * CHUNK;
-  // Softmax: NSPLIT warps per 32-row TMEM lane quarter, each with 1/NSPLIT
-  // of the key columns of S and of the head_dim columns of O.  The parts of
-  // a row exchange their maxima (and, at the end, their sums) through TMEM
-  // columns XCOL.. (per tile parity) and LCOL.., after S and O.
-  static constexpr int NSPLIT = 2;
-  static constexpr uint32_t XCOL = 384;
-  static constexpr uint32_t LCOL = XCOL + 2 * NSPLIT;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 32 + 1024;            // + 1024-byte alignment slack
-  static constexpr int SOFTMAX_WARPS = 4 * NSPLIT;
-  static constexpr int THREADS = (SOFTMAX_WARPS + 3) * 32;     // + K producer, MMA issuer, V producer
-  static constexpr int HC = BN / NSPLIT;                       // S columns per softmax thread
-  static constexpr int HD = D / NSPLIT;                        // O columns per softmax thread
-  static_assert(HC % 32 == 0 && HD % 16 == 0 && NSPLIT <= 4, "softmax column split");
-  static constexpr uint32_t TMEM_COLS = 512;                   // S0 0, S1 128, O 256
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
-  static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
-  static constexpr uint32_t BLOCK_BYTES = HALVES * 16 * 128;  // K (or V) of one block
+  static constexpr int CHUNK = 128 * 128;           // 128 rows x 128 bytes, swizzled
+  static constexpr int QBYTES = HALVES * CHUNK;     // Q of one head
+  static constexpr int TBYTES = HALVES * CHUNK;     // K (or V) of one step
+  static constexpr int BLOCK_BYTES = HALVES * 16 * 128;  // K (or V) of one 16-token block
   // K and V blocks land as [8-key group][head_dim half][8 keys][128 B]: the
   // 8-key groups of a tile are GSTRIDE apart, head_dim halves 1 KB apart.
   static constexpr int GSTRIDE = HALVES * 1024;
+  static constexpr int NST = D == 128 ? 2 : 4;      // K stages = V stages
+  static constexpr int SEGS = 4;                    // segment records in flight
+  static constexpr int SEG_INTS = 16;
+  static constexpr int OFF_Q = 0;                   // [2 slots]
+  static constexpr int OFF_K = OFF_Q + 2 * QBYTES;
+  static constexpr int OFF_V = OFF_K + NST * TBYTES;
+  static constexpr int OFF_SEG = OFF_V + NST * TBYTES;
+  static constexpr int OFF_BAR = OFF_SEG + SEGS * SEG_INTS * 4;
+  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + 1024-byte alignment slack
+  static constexpr int THREADS = 11 * 32;
+  static constexpr uint32_t TMEM_COLS = 512;         // S0 0, S1 128, O0 256, O1 256 + D
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
+  static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-// mbarriers (index into the barrier array)
-constexpr int kQFull = 0;
-constexpr int kKFull = 1;    // [2] K tile landed
-constexpr int kVFull = 3;    // [2] V tile landed
-constexpr int kKFree = 5;    // [2] S MMA that read the K stage is done
-constexpr int kSFull = 7;    // [2] S MMA done
-constexpr int kPFull = 9;    // [2] softmax wrote P (and finished reading S)
-constexpr int kPVDone = 11;  // [2] P.V MMA done (V stage and P buffer free, O current)
-constexpr int kSFree = 13;   // [2] softmax has S in registers (the S buffer may be refilled)
-constexpr int kRed = 15;     // softmax-warp barrier (row-max exchange)
+// Barrier indices.
+template <int NST, int SEGS>
+struct PBars {
+  static constexpr int KFULL = 0;                // [NST] K step landed
+  static constexpr int KFREE = KFULL + NST;      // [NST] both S MMAs that read it are done
+  static constexpr int VFULL = KFREE + NST;      // [NST]
+  static constexpr int VFREE = VFULL + NST;      // [NST] both P.V MMAs that read it are done
+  static constexpr int QFULL = VFREE + NST;      // [2] Q of a slot landed
+  static constexpr int QFREE = QFULL + 2;        // [2] last S MMA of a segment read it
+  static constexpr int SFULL = QFREE + 2;        // [2] S_b in TMEM
+  static constexpr int PFULL = SFULL + 2;        // [2] P_b in TMEM (4 softmax warps)
+  static constexpr int OFULL = PFULL + 2;        // [2] last P.V of a segment done
+  static constexpr int OFREE = OFULL + 2;        // [2] O_b read at a segment end (4 warps)
+  static constexpr int SEGFULL = OFREE + 2;      // [SEGS] segment record written
+  static constexpr int SEGFREE = SEGFULL + SEGS; // [SEGS] every role is done with it
+  static constexpr int SYNC = SEGFREE + SEGS;    // the 8 softmax warps
+  static constexpr int DRAIN = SYNC + 1;         // the MMA warp's last commit
+  static constexpr int COUNT = DRAIN + 1;
+};
 
-// Query tiles of request r (0 for rows that are not prefill rows or whose
-// lengths are out of range); each tile is 128 rows of one q head.
-__device__ __forceinline__ int prefill_tiles(const PrefillArgs& a, int r) {
+// A segment: steps [j0, j1) of one unit inside this CTA's range.
+struct PSeg {
+  int r, q0, row0, rows;
+  int ctx, kv_end, n_kv, j0;
+  int j1, h0, h1, kvh;
+  int kind, unit, c0, c1;
+};
+static_assert(sizeof(PSeg) == 64, "segment record");
+
+// A request's prefill rows (q_len > 1 and lengths in range), else ntq = 0.
+struct PReq {
+  int q0, q_len, seq_len, ctx, ntq;
+};
+
+__device__ __forceinline__ PReq prefill_req(const PrefillArgs& a, int r) {
+  PReq p{0, 0, 0, 0, 0};
+  if (r >= a.num_seqs) return p;
   const int q0 = a.query_start_loc[r];
   const int q_len = a.query_start_loc[r + 1] - q0;
-  if (q_len <= 1) return 0;
+  if (q_len <= 1) return p;
   const int seq_len = a.seq_lens[r];
   if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
       q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q)
-    return 0;
-  return (q_len + PrefillCfg<64>::BM - 1) / PrefillCfg<64>::BM * a.num_heads;
+    return p;
+  p.q0 = q0;
+  p.q_len = q_len;
+  p.seq_len = seq_len;
+  p.ctx = seq_len - q_len;
+  p.ntq = (q_len + 127) / 128;
+  return p;
 }
 
-// Reports the prefill rows prefill_tiles() rejects (done once, by CTA 0).
+// Key steps of query tile u (u = 0: the request's last tile) of a request.
+__device__ __forceinline__ int unit_steps(const PReq& p, int u, int* row0, int* rows, int* kv_end) {
+  const int qt = p.ntq - 1 - u;
+  *row0 = qt * 128;
+  *rows = min(128, p.q_len - *row0);
+  *kv_end = p.ctx + *row0 + *rows;
+  return (*kv_end + 127) / 128;
+}
+
+// Key steps of all query tiles of a request (one head pair).
+__device__ __forceinline__ long long req_steps(const PReq& p) {
+  long long n = 0;
+  for (int u = 0; u < p.ntq; ++u) {
+    int row0, rows, kv_end;
+    n += unit_steps(p, u, &row0, &rows, &kv_end);
+  }
+  return n;
+}
+
+// Reports the prefill rows prefill_req() rejects (done once, by CTA 0).
 __device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
   for (int r = lane; r < a.num_seqs; r += 32) {
     const int q0 = a.query_start_loc[r];
@@ -139,15 +188,13 @@ __device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
   }
 }
 
-// Persistent: CTA c takes tiles c, c + gridDim.x, ... of the batch's tile
-// list (requests in order; within a request the last query tile, which
-// sees the most keys, first; then the q heads).
 template <int D>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
-prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
-                    const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   using C = PrefillCfg<D>;
+  using B = PBars<C::NST, C::SEGS>;
+  const int cta = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -158,395 +205,649 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint32_t q_s = sbase + C::OFF_Q;
   const uint32_t k_s = sbase + C::OFF_K;
   const uint32_t v_s = sbase + C::OFF_V;
-  const uint32_t p_s = sbase + C::OFF_P;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int k) -> uint32_t { return bar0 + 8 * k; };
+  PSeg* segs = reinterpret_cast<PSeg*>(smem + C::OFF_SEG);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* tile_rec = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // r, local, found
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  volatile int* n_k_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 12);
+  volatile int* n_v_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  volatile int* n_q_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 20);  // [2]
 
-  if (tid == 0) *fail_flag = 0;
-  if (warp == 0) {
+  if (tid == 0) {
+    for (int k = 0; k < B::COUNT; ++k) {
+      int count = 1;
+      if ((k >= B::PFULL && k < B::PFULL + 2) || (k >= B::OFREE && k < B::OFREE + 2)) count = 4;
+      if (k >= B::SEGFREE && k < B::SEGFREE + C::SEGS) count = 10;  // MMA, 8 softmax, V producer
+      if (k == B::SYNC) count = 8;
+      mbar_init(bar(k), count);
+    }
+    *fail_flag = 0;
+    *last_flag = 0;
+    *n_k_issued = 0;
+    *n_v_issued = 0;
+    n_q_issued[0] = 0;
+    n_q_issued[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
     tmem_relinquish();
   }
-  // The kernels before this launch (the cache write of this step's tokens)
-  // must be complete before anything is read.  Only then may the decode
-  // rows of the same call start: they run on the SMs these tiles leave free.
-  griddep_wait();
-  griddep_launch_dependents();
-  if (blockIdx.x == 0 && warp == 1) report_bad_prefill_rows(a, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The kernels before this launch (the cache write of this step's tokens)
+  // must be complete before anything is read.  Only then may the decode
+  // rows of the same call start: they run on the SMs these CTAs leave free.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
-  int scan_r = 0;            // warp 0: first request not yet passed by the tile search
-  long long scan_base = 0;   // tiles of the requests before scan_r
-
-  for (long long tile = blockIdx.x;; tile += gridDim.x) {
-  // ---- locate the tile (warp 0) and set up this tile's barriers
-  if (warp == 0) {
-    int r_found = -1;
-    long long local = 0;
-    for (int rc = scan_r; rc < a.num_seqs && r_found < 0; rc += 32) {
-      const int rr = rc + lane;
-      const long long nt = rr < a.num_seqs ? prefill_tiles(a, rr) : 0;
-      long long incl = nt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const unsigned hit = __ballot_sync(0xffffffffu, rr < a.num_seqs && scan_base + incl > tile);
-      if (hit) {
-        const int first = __ffs(hit) - 1;
-        const long long excl = __shfl_sync(0xffffffffu, incl - nt, first);
-        r_found = rc + first;
-        scan_base += excl;
-        scan_r = r_found;
-        local = tile - scan_base;
-      } else {
-        scan_base += __shfl_sync(0xffffffffu, incl, 31);
-        scan_r = rc + 32;
-      }
-    }
-    if (lane == 0) {
-      tile_rec[0] = r_found;
-      tile_rec[1] = static_cast<int>(local);
-      tile_rec[2] = r_found >= 0 ? 1 : 0;
-      for (int k = 0; k <= kRed; ++k) {
-        if (tile != blockIdx.x) mbar_inval(bar(k));
-        const bool by_softmax = k == kPFull || k == kPFull + 1 || k == kSFree || k == kSFree + 1 ||
-                                k == kRed;
-        mbar_init(bar(k), by_softmax ? C::SOFTMAX_WARPS : 1);
-      }
-      fence_mbar_init();
-    }
-  }
-  __syncthreads();
-  if (!tile_rec[2]) break;
-  const int r = tile_rec[0];
-  const int q0 = a.query_start_loc[r];
-  const int q_len = a.query_start_loc[r + 1] - q0;
-  const int seq_len = a.seq_lens[r];
-  const int ntq = (q_len + C::BM - 1) / C::BM;
-  const int qt = ntq - 1 - tile_rec[1] / a.num_heads;
-  const int head = tile_rec[1] % a.num_heads;
-  const int ctx = seq_len - q_len;
-  const int row0 = qt * C::BM;                     // first query (within the request)
-  const int rows = min(C::BM, q_len - row0);       // valid query rows of this tile
-  const int kv_end = ctx + row0 + rows;            // keys [0, kv_end) are needed
-  const int n_tiles = (kv_end + C::BN - 1) / C::BN;
-  const int nblk_need = (kv_end + kBlockSize - 1) / kBlockSize;
-  const int kvh = head / a.group;
+  const int GP = (a.group + 1) / 2;        // head pairs per kv head
+  const int NP = a.num_kv_heads * GP;      // head pairs (units per query tile)
   auto give_up = [&](int where) {
-    record_error(a.status, PA_DEV_WAIT_TIMEOUT, r, where);
+    record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, where);
     *fail_flag = 1;
   };
+  // Cache row of 16-token tile t8 + lane (lane < 8) of request r in the
+  // grouped TMA view; an id outside the pool is reported (if `report`) and
+  // read as wholly out of bounds (TMA fills zeros).
+  auto tile_rows = [&](int r, int t8, int nblk, bool report) -> int {
+    const int t16 = t8 + lane;
+    if (lane >= 8 || t16 >= nblk) return 0;
+    const int id = __ldg(a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq + (t16 >> a.tile_shift));
+    if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+      if (report) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, id);
+      return a.num_blocks * a.block_size;
+    }
+    return id * a.block_size + (t16 & ((1 << a.tile_shift) - 1)) * kBlockSize;
+  };
 
-  if (warp == C::SOFTMAX_WARPS || warp == C::SOFTMAX_WARPS + 2) {
-    // ===================================================== K and V producers
-    // Two warps, so that a K tile is never queued behind the V copy that
-    // waits for an earlier P.V MMA.
-    const bool is_v = warp != C::SOFTMAX_WARPS;
-    const int32_t* bt = a.block_tables + static_cast<size_t>(r) * a.max_blocks_per_seq;
+  if (warp == 0) {
+    // ====================================================== Q / K producer
+    if (cta == 0) report_bad_prefill_rows(a, lane);
     const uint64_t policy = l2_policy_evict_first();
-    auto load_ids = [&](int t) -> int {
-      const int b = t * 8 + lane;
-      return (lane < 8 && t < n_tiles && b < nblk_need) ? __ldg(bt + (b >> a.tile_shift)) : -1;
-    };
-    // K or V of tile t into stage t % 2: lane 0 posts the byte count, then
-    // lanes 0..7 each issue the TMA copies of their own block (lane b holds
-    // the id of block b of the tile).
-    auto issue_tile = [&](bool is_v, int t, int ids) {
-      const int st = t & 1;
-      const int nb = min(8, nblk_need - t * 8);
-      const uint32_t full = bar((is_v ? kVFull : kKFull) + st);
-      if (lane == 0) mbar_arrive_expect_tx(full, nb * C::BLOCK_BYTES);
-      __syncwarp();
-      if (lane < nb) {
-        // rows 16 (tile mod R) .. + 15 of the block holding tile t * 8 + lane
-        int row_c = ids * a.block_size + ((t * 8 + lane) & ((1 << a.tile_shift) - 1)) * kBlockSize;
-        if (static_cast<unsigned>(ids) >= static_cast<unsigned>(a.num_blocks)) {
-          if (!is_v) record_error(a.status, PA_DEV_BAD_BLOCK_ID, r, ids);
-          row_c = a.num_blocks * a.block_size;  // wholly out of bounds: TMA fills zeros
-        }
-        const uint32_t dst = (is_v ? v_s : k_s) + st * C::HALVES * C::CHUNK + lane * C::BLOCK_BYTES;
-        tma_load_5d(dst, is_v ? &vmap : &kmap, full, 0, 0, 0, row_c / 8, kvh, policy);
-      }
-      __syncwarp();
-    };
-    if (lane == 0 && is_v) tma_prefetch_desc(&vmap);
-    if (lane == 0 && !is_v) {
+    if (lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
-      mbar_arrive_expect_tx(bar(kQFull), C::HALVES * C::CHUNK);
+    }
+    // The split is by cost: every key step costs kCostStep and every unit
+    // (a segment start: Q load, first S before any softmax, epilogue)
+    // another kCostUnit, when every CTA's share is at least one unit start
+    // plus one step wide (so that every CTA between a unit's first and last
+    // contributor holds one of its steps); else by steps alone.
+    long long nsum = 0, usum = 0;
+    for (int r = lane; r < a.num_seqs; r += 32) {
+      const PReq p = prefill_req(a, r);
+      nsum += req_steps(p);
+      usum += p.ntq;
+    }
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h)
-        tma_load_3d(q_s + h * C::CHUNK, &qmap, bar(kQFull), 64 * h, head, q0 + row0, policy);
+    for (int o = 16; o >= 1; o >>= 1) {
+      nsum += __shfl_xor_sync(0xffffffffu, nsum, o);
+      usum += __shfl_xor_sync(0xffffffffu, usum, o);
     }
-    int ids = load_ids(0);
-    int ids_next = load_ids(1);
-    for (int t = 0; t < n_tiles; ++t) {
-      int ok = 1;
-      // Stage t % 2 held tile t - 2: a K stage is free once S_{t-2} is done,
-      // a V stage once P_{t-2} V_{t-2} is done.
-      if (lane == 0 && t >= 2 &&
-          !mbar_wait(bar((is_v ? kPVDone : kKFree) + (t & 1)), ((t - 2) >> 1) & 1))
-        ok = 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issue_tile(is_v, t, ids);
-      ids = ids_next;
-      ids_next = load_ids(t + 2);
+    const long long Cw = (kCostStep * nsum + kCostUnit * usum) * NP;
+    const bool by_cost = Cw / a.num_ctas >= kCostStep + kCostUnit;
+    const long long CT = by_cost ? kCostStep : 1, CS = by_cost ? kCostUnit : 0;
+    const long long Ctot = by_cost ? Cw : nsum * NP;
+    const long long x0 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta) : 0;
+    const long long x1 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta + 1) : 0;
+    int seg = 0, g = 0;
+    int nq[2] = {0, 0};
+    bool ok = true;
+    auto lane0_wait = [&](uint32_t b, uint32_t parity, int where) -> bool {
+      int good = 1;
+      if (lane == 0) {
+        if (*fail_flag) good = 0;
+        else if (!mbar_wait(b, parity)) { give_up(where); good = 0; }
+      }
+      return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    auto seg_slot = [&](int s) -> bool {  // ring slot of segment s is free again
+      return s < C::SEGS || lane0_wait(bar(B::SEGFREE + s % C::SEGS), ((s / C::SEGS) - 1) & 1, 60);
+    };
+    // Steps [j, ..) of a unit whose cost starts at cb: step j starts at
+    // cb + CS + CT j.  The first step starting at or after x:
+    auto first_step_at = [&](long long cb, long long x) -> long long {
+      return x <= cb + CS ? 0 : (x - cb - CS + CT - 1) / CT;
+    };
+    if (x0 < x1) {
+      // The request holding cost position x0, with the cost and units before it.
+      long long base = 0, ubase = 0;
+      int r = -1;
+      for (int rc = 0; rc < a.num_seqs && r < 0; rc += 32) {
+        const PReq p = prefill_req(a, rc + lane);
+        const long long ct = (CT * req_steps(p) + CS * p.ntq) * NP;
+        const long long nu = static_cast<long long>(p.ntq) * NP;
+        long long it = ct, iu = nu;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long vt = __shfl_up_sync(0xffffffffu, it, o);
+          const long long vu = __shfl_up_sync(0xffffffffu, iu, o);
+          if (lane >= o) {
+            it += vt;
+            iu += vu;
+          }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, base + it > x0);
+        if (hit) {
+          const int first = __ffs(hit) - 1;
+          base += __shfl_sync(0xffffffffu, it - ct, first);
+          ubase += __shfl_sync(0xffffffffu, iu - nu, first);
+          r = rc + first;
+        } else {
+          base += __shfl_sync(0xffffffffu, it, 31);
+          ubase += __shfl_sync(0xffffffffu, iu, 31);
+        }
+      }
+      // Unit (query tile u, head pair hp) of request r holding x0.
+      PReq p = prefill_req(a, r);
+      int u = 0, hp = 0, row0 = 0, rows = 0, kv_end = 0;
+      int n_u = unit_steps(p, 0, &row0, &rows, &kv_end);
+      long long cb = base;   // cost before the current unit
+      long long ub = ubase;  // units before query tile u of request r
+      while (cb + NP * (CS + CT * n_u) <= x0) {
+        cb += NP * (CS + CT * n_u);
+        ++u;
+        ub += NP;
+        n_u = unit_steps(p, u, &row0, &rows, &kv_end);
+      }
+      hp = static_cast<int>((x0 - cb) / (CS + CT * n_u));
+      cb += hp * (CS + CT * n_u);
+      long long j = first_step_at(cb, x0);
+      while (ok) {
+        if (j >= n_u) {
+          // no step of this unit starts in the range: on to the next unit
+          cb += CS + CT * n_u;
+          j = 0;
+          if (++hp == NP) {
+            hp = 0;
+            ub += NP;
+            if (++u == p.ntq) {
+              u = 0;
+              do {
+                p = prefill_req(a, ++r);
+              } while (p.ntq == 0 && r < a.num_seqs);
+              if (p.ntq == 0) break;  // no more work
+            }
+          }
+          n_u = unit_steps(p, u, &row0, &rows, &kv_end);
+        }
+        if (cb + CS + CT * j >= x1) break;  // the next step starts past the range
+        const int j0 = static_cast<int>(j);
+        const int j1 = static_cast<int>(min(static_cast<long long>(n_u), first_step_at(cb, x1)));
+        const int kvh = hp / GP;
+        const int h0 = kvh * a.group + 2 * (hp % GP);
+        const int h1 = 2 * (hp % GP) + 1 < a.group ? h0 + 1 : -1;
+        if (!(ok = seg_slot(seg))) break;
+        if (lane == 0) {
+          PSeg sg;
+          sg.r = r;
+          sg.q0 = p.q0;
+          sg.row0 = row0;
+          sg.rows = rows;
+          sg.ctx = p.ctx;
+          sg.kv_end = kv_end;
+          sg.n_kv = n_u;
+          sg.j0 = j0;
+          sg.j1 = j1;
+          sg.h0 = h0;
+          sg.h1 = h1;
+          sg.kvh = kvh;
+          sg.kind = (j0 == 0 && j1 == n_u) ? kSegWhole : (j0 > 0 ? kSegHead : kSegTail);
+          sg.unit = static_cast<int>(ub + hp);
+          sg.c0 = cta_of_tile(Ctot, a.num_ctas, cb + CS);
+          sg.c1 = cta_of_tile(Ctot, a.num_ctas, cb + CS + CT * (n_u - 1));
+          segs[seg % C::SEGS] = sg;
+          mbar_arrive(bar(B::SEGFULL + seg % C::SEGS));
+        }
+        // Q of both heads (their buffers are free once the previous
+        // segment's last S MMA of that slot is done).
+        for (int b = 0; b < 2 && ok; ++b) {
+          if (b == 1 && h1 < 0) break;
+          if (nq[b] > 0 && !(ok = lane0_wait(bar(B::QFREE + b), (nq[b] - 1) & 1, 61))) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B::QFULL + b), C::QBYTES);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_3d(q_s + b * C::QBYTES + h * C::CHUNK, &qmap, bar(B::QFULL + b), 64 * h,
+                          b ? h1 : h0, p.q0 + row0, policy);
+            n_q_issued[b] = nq[b] + 1;
+          }
+          ++nq[b];
+        }
+        // K of every step: lane L < 8 copies block L of the step.
+        const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+        int rowc = tile_rows(r, j0 * 8, nblk, true);
+        for (int jj = j0; jj < j1 && ok; ++jj) {
+          const int st = g % C::NST;
+          if (g >= C::NST && !(ok = lane0_wait(bar(B::KFREE + st), ((g / C::NST) - 1) & 1, 62))) break;
+          const int nb = min(8, nblk - jj * 8);
+          if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + st), nb * C::BLOCK_BYTES);
+          __syncwarp();
+          if (lane < nb)
+            tma_load_5d(k_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &kmap, bar(B::KFULL + st), 0, 0,
+                        0, rowc / 8, kvh, policy);
+          ++g;
+          if (lane == 0) *n_k_issued = g;
+          if (jj + 1 < j1) rowc = tile_rows(r, (jj + 1) * 8, nblk, true);
+        }
+        ++seg;
+        if (j1 < n_u) break;  // the range ends inside this unit
+        j = n_u;              // next unit
+      }
     }
-  } else if (warp == C::SOFTMAX_WARPS + 1) {
+    // End record.
+    if (ok && (ok = seg_slot(seg)) && lane == 0) {
+      segs[seg % C::SEGS].kind = kSegEnd;
+      mbar_arrive(bar(B::SEGFULL + seg % C::SEGS));
+    }
+    if (!ok && lane == 0) *fail_flag = 1;
+  } else if (warp == 10) {
+    // =========================================================== V producer
+    const uint64_t policy = l2_policy_evict_first();
+    if (lane == 0) tma_prefetch_desc(&vmap);
+    auto warp_wait = [&](uint32_t b, uint32_t parity, int where) -> bool {
+      if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
+      const bool good = __all_sync(0xffffffffu, mbar_wait(b, parity) ? 1 : 0) != 0;
+      if (!good && lane == 0) give_up(where);
+      return good;
+    };
+    bool ok = true;
+    int g = 0;
+    for (int seg = 0; ok; ++seg) {
+      const int slot = seg % C::SEGS;
+      if (!(ok = warp_wait(bar(B::SEGFULL + slot), (seg / C::SEGS) & 1, 63))) break;
+      const PSeg sg = segs[slot];
+      if (sg.kind == kSegEnd) break;
+      const int nblk = (sg.kv_end + kBlockSize - 1) / kBlockSize;
+      for (int jj = sg.j0; jj < sg.j1 && ok; ++jj) {
+        const int st = g % C::NST;
+        const int rowc = tile_rows(sg.r, jj * 8, nblk, false);
+        if (g >= C::NST && !(ok = warp_wait(bar(B::VFREE + st), ((g / C::NST) - 1) & 1, 64))) break;
+        const int nb = min(8, nblk - jj * 8);
+        if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + st), nb * C::BLOCK_BYTES);
+        __syncwarp();
+        if (lane < nb)
+          tma_load_5d(v_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &vmap, bar(B::VFULL + st), 0, 0, 0,
+                      rowc / 8, sg.kvh, policy);
+        ++g;
+        if (lane == 0) *n_v_issued = g;
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(bar(B::SEGFREE + slot));
+    }
+    if (!ok && lane == 0) *fail_flag = 1;
+  } else if (warp == 1) {
     // ========================================================== MMA issuer
     if (lane == 0) {
-      auto issue_s = [&](int t) -> bool {  // S_t = Q K_t^T into S buffer t % 2
-        // S buffer t % 2 held S_{t-2}: its softmax must have read it.
-        if (t >= 2 && !mbar_wait(bar(kSFree + (t & 1)), ((t - 2) >> 1) & 1)) return false;
-        if (!mbar_wait(bar(kKFull + (t & 1)), (t >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kst = k_s + (t & 1) * C::HALVES * C::CHUNK;
+      bool ok = true;
+      int g = 0, pc[2] = {0, 0}, oc[2] = {0, 0}, qc[2] = {0, 0};
+      auto wait = [&](int k, uint32_t parity, int where) -> bool {
+        if (*fail_flag) return false;
+        if (!mbar_wait(bar(k), parity)) {
+          give_up(where);
+          return false;
+        }
+        return true;
+      };
+      // S_b = Q_b K^T of the K stage st, into TMEM columns 128 b.
+      auto issue_s = [&](int b, int st) {
+        const uint32_t kst = k_s + st * C::TBYTES;
+        const uint32_t qb = q_s + b * C::QBYTES;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t qoff = (ks / 4) * C::CHUNK + (ks % 4) * 32;
           const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
-          umma_bf16(tmem + (t & 1) * C::BN, sdesc_sw128(q_s + qoff, 16, 1024),
+          umma_bf16(tmem + b * C::BN, sdesc_sw128(qb + qoff, 16, 1024),
                     sdesc_sw128(kst + koff, 16, C::GSTRIDE), C::IDESC_S, ks > 0);
         }
-        umma_commit(bar(kSFull + (t & 1)));
-        umma_commit(bar(kKFree + (t & 1)));
-        return true;
       };
-      bool ok = mbar_wait(bar(kQFull), 0) && issue_s(0) && (n_tiles < 2 || issue_s(1));
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int sb = j & 1;
-        // S_{j+2} goes first when its K tile has landed (its S buffer is freed
-        // early in softmax j), so the tensor core works while softmax j runs;
-        // otherwise P_j V_j goes first and S_{j+2} waits for its K tile.
-        bool s_next = j + 2 < n_tiles;
-        if (s_next && mbar_wait(bar(kSFree + sb), (j >> 1) & 1) &&
-            mbar_try_wait(bar(kKFull + sb), ((j + 2) >> 1) & 1)) {
-          ok = issue_s(j + 2);
-          s_next = false;
-        }
-        ok = ok && mbar_wait(bar(kPFull + sb), (j >> 1) & 1) && mbar_wait(bar(kVFull + sb), (j >> 1) & 1);
+      // O_b += P_b V of the V stage st (P_b: bf16 in TMEM columns 128 b ..).
+      auto issue_pv = [&](int b, int st, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < C::BN / 16; ++ks)
+          umma_tmem_a(tmem + 256 + b * D, tmem + b * C::BN + ks * 8,
+                      sdesc_sw128(v_s + st * C::TBYTES + ks * C::BLOCK_BYTES, 1024, C::GSTRIDE),
+                      C::IDESC_O, (acc || ks > 0) ? 1u : 0u);
+      };
+      for (int seg = 0; ok; ++seg) {
+        const int slot = seg % C::SEGS;
+        if (!(ok = wait(B::SEGFULL + slot, (seg / C::SEGS) & 1, 70))) break;
+        const PSeg sg = segs[slot];
+        if (sg.kind == kSegEnd) break;
+        const int n = sg.j1 - sg.j0;
+        const int nsl = sg.h1 >= 0 ? 2 : 1;
+        for (int b = 0; b < nsl && ok; ++b) ok = wait(B::QFULL + b, qc[b]++ & 1, 71);
+        ok = ok && wait(B::KFULL + g % C::NST, (g / C::NST) & 1, 72);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks) {
-          umma_bf16(tmem + 256, sdesc_sw128(p_s + (sb * 2 + ks / 4) * C::CHUNK + (ks % 4) * 32, 16, 1024),
-                    sdesc_sw128(v_s + sb * C::HALVES * C::CHUNK + ks * C::BLOCK_BYTES, 1024, C::GSTRIDE),
-                    C::IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
+        for (int b = 0; b < nsl; ++b) {
+          issue_s(b, g % C::NST);
+          umma_commit(bar(B::SFULL + b));
+          if (n == 1) umma_commit(bar(B::QFREE + b));
         }
-        umma_commit(bar(kPVDone + sb));
-        if (s_next) ok = issue_s(j + 2);
+        umma_commit(bar(B::KFREE + g % C::NST));
+        for (int k = 0; k < n && ok; ++k) {
+          const int gk = g + k, st = gk % C::NST, st1 = (gk + 1) % C::NST;
+          ok = wait(B::VFULL + st, (gk / C::NST) & 1, 73);
+          for (int b = 0; b < nsl && ok; ++b) {
+            ok = wait(B::PFULL + b, pc[b]++ & 1, 75) &&
+                 (k > 0 || oc[b] == 0 || wait(B::OFREE + b, (oc[b] - 1) & 1, 76));
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(b, st, k > 0);
+            if (k + 1 == n) {
+              umma_commit(bar(B::OFULL + b));
+            } else {
+              // S_b of the next step (its K stage may still be landing).
+              if (b == 0 && !(ok = wait(B::KFULL + st1, ((gk + 1) / C::NST) & 1, 74))) break;
+              tc_fence_after();
+              issue_s(b, st1);
+              umma_commit(bar(B::SFULL + b));
+              if (k + 2 == n) umma_commit(bar(B::QFREE + b));
+            }
+          }
+          if (!ok) break;
+          umma_commit(bar(B::VFREE + st));
+          if (k + 1 < n) umma_commit(bar(B::KFREE + st1));
+        }
+        if (!ok) break;
+        g += n;
+        for (int b = 0; b < nsl; ++b) ++oc[b];
+        mbar_arrive(bar(B::SEGFREE + slot));
       }
-      if (!ok) give_up(12);
+      if (!ok) *fail_flag = 1;
+      // Every MMA issued has completed before TMEM can be released.
+      umma_commit(bar(B::DRAIN));
+      (void)mbar_wait(bar(B::DRAIN), 0);
     }
+    __syncwarp();
   } else {
     // ============================================================ softmax
-    // Warp w serves rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-    // column part w / 4 of S and of O; thread row i = 32 (w % 4) + lane.
-    const int part = warp >> 2;
+    // Warps 2-5 serve slot 0, warps 6-9 slot 1; warp w owns TMEM lanes
+    // 32 (w % 4) .. + 31, i.e. query row i = 32 (w % 4) + lane of the unit.
+    const int b = warp < 6 ? 0 : 1;
     const int i_row = (warp & 3) * 32 + lane;
-    const uint32_t tmem_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tmem_o = 256;
-    const int limit = min(ctx + row0 + i_row, kv_end - 1);  // last key this row may see
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tm_s = lane_base + b * C::BN;
+    const uint32_t tm_o = lane_base + 256 + b * D;
     const float sl2 = a.scale_log2;
-    float m_ref = kNegBigP, l_run = 0.f;  // both threads of a row keep the same m_ref
     bool ok = true;
-    uint32_t red_phase = 0;
-    // Barrier of the softmax warps (bounded; orders the exchange writes).
-    auto red_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kRed));
-      const int done = mbar_wait(bar(kRed), red_phase & 1) ? 1 : 0;
-      ++red_phase;
-      return __all_sync(0xffffffffu, done) != 0;
+    int sc = 0, oc = 0, g = 0;
+    uint32_t sync_phase = 0;
+    auto all_wait = [&](int k, uint32_t parity, int where) -> bool {
+      if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
+      const bool good = __all_sync(0xffffffffu, mbar_wait(bar(k), parity) ? 1 : 0) != 0;
+      if (!good && lane == 0) give_up(where);
+      return good;
     };
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sb), (j >> 1) & 1) ? 1 : 0) != 0;
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sraw[C::HC];
-#pragma unroll
-      for (int c = 0; c < C::HC / 32; ++c)
-        tmem_ld32_async(tmem_row + sb * C::BN + part * C::HC + c * 32, sraw + 32 * c);
-      tmem_wait_ld();
-      tc_fence_before();  // S_j is in registers: the S MMA of tile j + 2 may overwrite it
+    // Barrier of the 8 softmax warps (bounded).
+    auto sync8 = [&]() -> bool {
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + sb));
-      const int key0 = j * C::BN + part * C::HC;  // key of this thread's first column
-      const bool full_tile = j * C::BN + C::BN - 1 <= ctx + row0 && j * C::BN + C::BN <= seq_len;
-      float mx8[8];
+      if (lane == 0) mbar_arrive(bar(B::SYNC));
+      const bool good = all_wait(B::SYNC, sync_phase & 1, 80);
+      ++sync_phase;
+      return good;
+    };
+    for (int seg = 0; ok; ++seg) {
+      const int slot = seg % C::SEGS;
+      if (!(ok = all_wait(B::SEGFULL + slot, (seg / C::SEGS) & 1, 81))) break;
+      const volatile PSeg& sg = segs[slot];  // fields read where used (fewer registers)
+      if (sg.kind == kSegEnd) break;
+      const int n = sg.j1 - sg.j0;
+      const bool active = b == 0 || sg.h1 >= 0;
+      const int head = b ? sg.h1 : sg.h0;
+      const int pslot = sg.kind == kSegTail ? 1 : 0;
+      float m_ref = kNegBigP, l_run = 0.f;
+      if (active) {
+        const int limit = min(sg.ctx + sg.row0 + i_row, sg.kv_end - 1);  // last key this row sees
+        for (int k = 0; k < n && ok; ++k) {
+          const int key0 = (sg.j0 + k) * C::BN;
+          if (!(ok = all_wait(B::SFULL + b, sc++ & 1, 82))) break;
+          tc_fence_after();
+          const bool masked = key0 + C::BN - 1 > sg.ctx + sg.row0 || key0 + C::BN > sg.kv_end;
+          const int nv = limit - key0 + 1;  // visible keys of this row in this step
+          // S_b row into registers; keys past this row's limit get -inf (their
+          // weight 2^-inf = 0); only a step on the diagonal or at the end of
+          // the keys has any.
+          auto load_s = [&](uint32_t (&sr)[C::BN]) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (full_tile) {
+            for (int c = 0; c < C::BN / 32; ++c) tmem_ld32_async(tm_s + c * 32, sr + 32 * c);
+            tmem_wait_ld();
+            if (masked) {
 #pragma unroll
-        for (int e = 0; e < C::HC; e += 2)
-          mx8[(e / 2) % 8] = fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
-      } else {
+              for (int e = 0; e < C::BN; ++e) sr[e] = e < nv ? sr[e] : 0xff800000u;  // -inf
+            }
+          };
+          float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+          uint32_t pk[C::BN / 2];
+          // Weights of one pair of columns: scale and shift (packed fp32),
+          // exponentiate, round to bf16 for the P.V product; l sums the fp32
+          // weights.
+          auto weights = [&](uint32_t s0, uint32_t s1, float m, int e) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)),
+                                        make_float2(sl2, sl2), make_float2(-m, -m));
+            const float p0 = fast_exp2(x.x);  // 0 for the masked keys
+            const float p1 = fast_exp2(x.y);
+            pk[e / 2] = pack_bf16x2(p0, p1);
+            ps4[(e / 2) % 4] = __fadd2_rn(ps4[(e / 2) % 4], make_float2(p0, p1));
+          };
+          bool rescale = true;
+          float alpha = 1.f;
+          if (k > 0) {
+            // Speculative: weights against the current reference and the
+            // step's row maximum in one pass; kept unless some row's maximum
+            // exceeds its reference by more than 2^8 (rare after the first
+            // steps), in which case the step is redone below.
+            uint32_t sraw[C::BN];
+            load_s(sraw);
+            float mx8[8];
 #pragma unroll
-        for (int e = 0; e < C::HC; e += 2)
-          mx8[(e / 2) % 8] = fmax3(mx8[(e / 2) % 8],
-                                   key0 + e <= limit ? __uint_as_float(sraw[e]) : -INFINITY,
-                                   key0 + e + 1 <= limit ? __uint_as_float(sraw[e + 1]) : -INFINITY);
-      }
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // The row's maximum over all parts (TMEM columns of this tile parity).
-      const uint32_t xcol = tmem_row + C::XCOL + sb * C::NSPLIT;
-      tmem_st1(xcol + part, mx);
-      tc_fence_before();
-      if (!(ok = red_sync())) break;
-      tc_fence_after();
-      {
-        float xv[4];
-        tmem_ld4(xcol, xv);
+            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
-        for (int p2 = 0; p2 < C::NSPLIT; ++p2) mx = fmaxf(mx, xv[p2]);
-      }
-      const float m_tile = mx * sl2;
-      const bool need = m_tile > m_ref + kRescaleSlackP;
-      if (__any_sync(0xffffffffu, need)) {
-        // O (in TMEM) must hold P_{j-1} V_{j-1} before its rows are rescaled.
-        if (j > 0)
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar(kPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1) ? 1 : 0) != 0;
+            for (int e = 0; e < C::BN; e += 2) {
+              mx8[(e / 2) % 8] =
+                  fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
+              weights(sraw[e], sraw[e + 1], m_ref, e);
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            rescale = __any_sync(0xffffffffu, mx * sl2 > m_ref + kRescaleSlackP);
+          }
+          if (rescale) {
+            // The row maximum first, then the weights against the new reference.
+            uint32_t sraw[C::BN];
+            load_s(sraw);
+            float mx8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < C::BN; e += 2)
+              mx8[(e / 2) % 8] =
+                  fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_tile = mx * sl2;
+            if (m_tile > m_ref + kRescaleSlackP) {
+              alpha = fast_exp2(m_ref - m_tile);
+              l_run *= alpha;
+              m_ref = m_tile;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ps4[u] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < C::BN; e += 2) weights(sraw[e], sraw[e + 1], m_ref, e);
+          }
+          // P_b over the first half of the S_b columns.
+#pragma unroll
+          for (int c = 0; c < C::BN / 32; ++c) tmem_st16_async(tm_s + c * 16, pk + 16 * c);
+          const float2 ps = __fadd2_rn(__fadd2_rn(ps4[0], ps4[1]), __fadd2_rn(ps4[2], ps4[3]));
+          l_run += ps.x + ps.y;
+          if (rescale && k > 0) {  // (warp-uniform: the TMEM accesses are warp-wide)
+            // S_b of this step completing means the P_b V before it has
+            // completed too: O_b is current and may be rescaled.
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              float ov[16];
+              tmem_ld16(tm_o + c * 16, ov);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+              tmem_st16(tm_o + c * 16, ov);
+            }
+          }
+          // V rows of keys past the needed range (or never loaded) may hold
+          // NaN: slot 0's warps zero them before the first P.V reads them.
+          const int kz = sg.kv_end - key0;  // keys [kz, BN) of this step are unused
+          if (b == 0 && kz < C::BN) {
+            const int st = (g + k) % C::NST;
+            if (!(ok = all_wait(B::VFULL + st, ((g + k) / C::NST) & 1, 83))) break;
+            const int nz = (C::BN - kz) * C::HALVES * 8;
+            for (int idx = tid - 64; idx < nz; idx += 128) {
+              const int row = kz + idx / (C::HALVES * 8);
+              const int h = (idx / 8) % C::HALVES;
+              st_shared_v4(v_s + st * C::TBYTES + (row >> 4) * C::BLOCK_BYTES + ((row >> 3) & 1) * C::GSTRIDE +
+                               h * 1024 + (row & 7) * 128 + (idx % 8) * 16,
+                           make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_proxy_async_smem();  // the zeroed rows are read by the tensor core
+          }
+          tmem_wait_st();
+          tc_fence_before();  // P_b and O_b writes precede the next MMAs
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B::PFULL + b));
+        }
         if (!ok) break;
+        // ---- end of the segment: O_b / l, or the partial
+        if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
         tc_fence_after();
-        const float m_new = need ? m_tile : m_ref;
-        const float alpha = fast_exp2(m_ref - m_new);
-        if (j > 0) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        // O_b row, 64 columns per TMEM round trip.
+        const bool whole = sg.kind == kSegWhole;
+        const size_t rec = ((static_cast<size_t>(cta) * 2 + pslot) * 2 + b) * C::BM + i_row;
+        __nv_bfloat16* dst_o =
+            a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
+        // partial O is column-major ([D][128 rows]): a warp's stores of one
+        // column are 128 contiguous bytes
+        float* dst_p = a.part_o + (rec - i_row) * D + i_row;
+        if (!whole) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(m_ref, l_run);
 #pragma unroll
-          for (int c = 0; c < C::HD / 16; ++c) {
-            float ov[16];
-            tmem_ld16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t orow[64];
+          tmem_ld32_async(tm_o + h * 64, orow);
+          tmem_ld32_async(tm_o + h * 64 + 32, orow + 32);
+          tmem_wait_ld();
+          if (whole) {
+            if (i_row < sg.rows) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] *= alpha;
-            tmem_st16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
+              for (int e = 0; e < 64; e += 8)
+                *reinterpret_cast<uint4*>(dst_o + h * 64 + e) = make_uint4(
+                    pack_bf16x2(__uint_as_float(orow[e]) * inv, __uint_as_float(orow[e + 1]) * inv),
+                    pack_bf16x2(__uint_as_float(orow[e + 2]) * inv, __uint_as_float(orow[e + 3]) * inv),
+                    pack_bf16x2(__uint_as_float(orow[e + 4]) * inv, __uint_as_float(orow[e + 5]) * inv),
+                    pack_bf16x2(__uint_as_float(orow[e + 6]) * inv, __uint_as_float(orow[e + 7]) * inv));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) dst_p[(h * 64 + e) * C::BM] = __uint_as_float(orow[e]) * inv;
           }
         }
-        l_run *= alpha;
-        m_ref = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B::OFREE + b));
       }
-      // P buffer sb was read by P_{j-2} V_{j-2}: it must be done.
-      if (j >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + sb), ((j - 2) >> 1) & 1) ? 1 : 0) != 0;
-      if (!ok) break;
-      // Weights: scale and shift two at a time (packed fp32), exponentiate,
-      // round to bf16 for the P.V product; l sums the fp32 weights.
-      float2 ps4[4];
+      g += n;
+      if (sg.kind != kSegWhole) {
+        // Publish the partial; the last of the unit's contributors merges.
+        __threadfence();
+        if (!(ok = sync8())) break;
+        if (warp == 2 && lane == 0) {
+          const bool in_range = sg.unit < a.max_units;
+          if (!in_range) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 85);
+          *last_flag = in_range && contribute(a.counters + sg.unit, a.epoch, sg.c1 - sg.c0 + 1,
+                                              a.status, sg.r) ? 1 : 0;
+        }
+        if (!(ok = sync8())) break;
+        if (*last_flag && active && i_row < sg.rows) {
+          // Merge this row's pieces: contributor c's record is in partial
+          // slot 1 for the unit's first CTA (its tail piece), else slot 0.
+          // Loads are issued in batches so that a batch costs one round trip.
+          __threadfence();
+          const int c0 = sg.c0, c1 = sg.c1;
+          auto rec_of = [&](int c) -> size_t {
+            return ((static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b) * C::BM + i_row;
+          };
+          float M = kNegBigP;
+          for (int c = c0; c <= c1; c += 4) {
+            float m4[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) ps4[u] = make_float2(0.f, 0.f);
-      const float2 sl2v = make_float2(sl2, sl2), mneg = make_float2(-m_ref, -m_ref);
-#pragma unroll
-      for (int c = 0; c < C::HC / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int k = c * 32 + e;
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sraw[k]), __uint_as_float(sraw[k + 1])),
-                                      sl2v, mneg);
-          float p0 = fast_exp2(x.x);
-          float p1 = fast_exp2(x.y);
-          if (!full_tile) {
-            p0 = key0 + k <= limit ? p0 : 0.f;
-            p1 = key0 + k + 1 <= limit ? p1 : 0.f;
+            for (int u = 0; u < 4; ++u) m4[u] = c + u <= c1 ? __ldcg(a.part_ml + rec_of(c + u) * 2) : kNegBigP;
+            M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
           }
-          pk[e / 2] = pack_bf16x2(p0, p1);
-          ps4[(e / 2) % 4] = __fadd2_rn(ps4[(e / 2) % 4], make_float2(p0, p1));
-        }
-        // keys part*HC + c*32 .. +31: 16-byte chunks cb .. cb + 3 of key half kh
-        const int kfirst = part * C::HC + c * 32;
-        const int kh = kfirst >> 6, cb = (kfirst & 63) >> 3;
+          __nv_bfloat16* dst =
+              a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
+          float invL = 0.f;
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            float acc[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = cb + q;
-          const uint32_t addr =
-              p_s + (sb * 2 + kh) * C::CHUNK + i_row * 128 + ((chunk ^ (i_row & 7)) * 16);
-          st_shared_v4(addr, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            float L = 0.f;
+            for (int c = c0; c <= c1; c += 2) {
+              const bool two = c + 1 <= c1;
+              const size_t r0 = rec_of(c), r1 = rec_of(two ? c + 1 : c);
+              const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + r0 * 2));
+              const float2 ml1 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + r1 * 2));
+              // column-major records: one column of 32 rows is 128 contiguous bytes
+              const float* p0 = a.part_o + (r0 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
+              const float* p1 = a.part_o + (r1 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
+              float v0[32], v1[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                v0[e] = __ldcg(p0 + e * C::BM);
+                v1[e] = __ldcg(p1 + e * C::BM);
+              }
+              const float w0 = ml0.y * fast_exp2(ml0.x - M);
+              const float w1 = two ? ml1.y * fast_exp2(ml1.x - M) : 0.f;
+              L += w0 + w1;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[e] = fmaf(w0, v0[e], fmaf(w1, v1[e], acc[e]));
+            }
+            if (cc == 0) invL = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+              *reinterpret_cast<uint4*>(dst + cc + e) = make_uint4(
+                  pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
+                  pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
+          }
         }
+        if (!(ok = sync8())) break;  // last_flag may change again after this
+        if (warp == 2 && lane == 0 && *last_flag) release_pair(a.counters + sg.unit);
       }
-      const float2 ps01 = __fadd2_rn(ps4[0], ps4[1]), ps23 = __fadd2_rn(ps4[2], ps4[3]);
-      const float2 ps = __fadd2_rn(ps01, ps23);
-      l_run += ps.x + ps.y;
-      // V rows of keys past the needed range or never loaded may hold NaN.
-      const int kz = kv_end - j * C::BN;  // keys [kz, BN) of this tile are unused
-      if (kz < C::BN) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kVFull + sb), (j >> 1) & 1) ? 1 : 0) != 0;
-        if (!ok) break;
-        const int nz = (C::BN - max(kz, 0)) * C::HALVES * 8;
-        for (int idx = tid; idx < nz; idx += C::SOFTMAX_WARPS * 32) {
-          const int row = max(kz, 0) + idx / (C::HALVES * 8);
-          const int h = (idx / 8) % C::HALVES;
-          st_shared_v4(v_s + sb * C::HALVES * C::CHUNK + (row >> 4) * C::BLOCK_BYTES +
-                           ((row >> 3) & 1) * C::GSTRIDE + h * 1024 + (row & 7) * 128 + (idx % 8) * 16,
-                       make_uint4(0u, 0u, 0u, 0u));
-        }
-      }
-      fence_proxy_async_smem();  // P_j and the zeroed rows are read by the tensor core
-      tc_fence_before();         // S_j reads and O rescales precede the next MMAs
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kPFull + sb));
+      if (lane == 0) mbar_arrive(bar(B::SEGFREE + slot));
     }
-    // ---- epilogue: O / l
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + ((n_tiles - 1) & 1)),
-                                             ((n_tiles - 1) >> 1) & 1) ? 1 : 0) != 0;
-    if (ok) {
-      tc_fence_after();
-      tmem_st1(tmem_row + C::LCOL + part, l_run);
-      tc_fence_before();
-      ok = red_sync();
-    }
-    if (ok) {
-      tc_fence_after();
-      float lv[4];
-      tmem_ld4(tmem_row + C::LCOL, lv);
-      float lsum = 0.f;
-#pragma unroll
-      for (int p2 = 0; p2 < C::NSPLIT; ++p2) lsum += lv[p2];
-      const float inv = 1.f / lsum;
-      __nv_bfloat16* dst =
-          a.out + (static_cast<size_t>(q0 + row0 + i_row) * a.num_heads + head) * D + part * C::HD;
-#pragma unroll
-      for (int c = 0; c < C::HD / 16; ++c) {
-        float ov[16];
-        tmem_ld16(tmem_row + tmem_o + part * C::HD + c * 16, ov);
-        if (i_row < rows) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 8) {
-            const uint4 v = make_uint4(pack_bf16x2(ov[e] * inv, ov[e + 1] * inv),
-                                       pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv),
-                                       pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv),
-                                       pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv));
-            *reinterpret_cast<uint4*>(dst + c * 16 + e) = v;
-          }
-        }
-      }
-    } else if (lane == 0) {
-      give_up(13);
-    }
+    if (!ok && lane == 0) *fail_flag = 1;
   }
 
-  __syncthreads();  // end of the tile: every copy and MMA of it has completed
-  if (*fail_flag) {
-    if (tid == 0) {
-      // Let copies and MMAs still in flight finish before TMEM is released
-      // and the CTA leaves (bounded; some of these phases may never come).
-      for (int k = 0; k < kRed; ++k) (void)mbar_wait(bar(k), 0);
-    }
-    break;
+  __syncthreads();
+  if (*fail_flag && tid == 0) {
+    // Let copies still in flight land before TMEM is released and the CTA
+    // leaves (bounded).
+    const int nk = *n_k_issued, nv = *n_v_issued;
+    for (int i = max(0, nk - C::NST); i < nk; ++i)
+      (void)mbar_wait(bar(B::KFULL + i % C::NST), (i / C::NST) & 1);
+    for (int i = max(0, nv - C::NST); i < nv; ++i)
+      (void)mbar_wait(bar(B::VFULL + i % C::NST), (i / C::NST) & 1);
+    for (int b = 0; b < 2; ++b)
+      if (n_q_issued[b] > 0) (void)mbar_wait(bar(B::QFULL + b), (n_q_issued[b] - 1) & 1);
   }
-  }  // tiles
-
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -557,14 +858,24 @@ cudaError_t launch_prefill_impl(const PrefillArgs& a, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const CUtensorMap& vmap,
                                 cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  cudaError_t err = cudaFuncSetAttribute(prefill_tile_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (err != cudaSuccess) return err;
-  return launch_overlapped(prefill_tile_kernel<D>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
-                           stream, qmap, kmap, vmap, a);
+  static bool attr_set[64] = {false};  // per device: set once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    const cudaError_t err = cudaFuncSetAttribute(prefill_kernel<D>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  return launch_overlapped(prefill_kernel<D>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM, stream,
+                           qmap, kmap, vmap, a);
 }
 
 }  // namespace
+
+size_t prefill_partials_bytes(int num_ctas, int head_dim) {
+  return static_cast<size_t>(num_ctas) * 2 * 2 * 128 * (2 + head_dim) * sizeof(float);
+}
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int head_dim, cudaStream_t stream) {

@@ -269,11 +269,11 @@ def test_two_mixed_calls_run_concurrently_on_two_caller_streams(cuda_lib, oracle
 
 def test_batch_order_does_not_change_a_requests_rows(cuda_lib, oracle):
     """The same requests in another order (block tables, lengths and query
-    rows permuted together; the cache unchanged).  A prefill row's tiles
-    never look at other requests, so its output is bit-identical; a decode
-    row's keys are split over the CTAs by the position of its tiles in the
-    whole batch, so its output may round differently and is compared with
-    the oracle in both orders instead."""
+    rows permuted together; the cache unchanged) give every request the same
+    rows up to rounding.  Both kernels split the batch's work over the CTAs
+    by position in the whole batch, so where a request's keys are cut into
+    merged pieces moves with the order: each order is compared with the
+    oracle, and the two orders with each other, within the bf16 tolerance."""
     pa = cuda_lib
     w, t = _mixed_case(233)
     out_a, ws = run_prefill(pa, w, t)
@@ -296,9 +296,7 @@ def test_batch_order_does_not_change_a_requests_rows(cuda_lib, oracle):
     for k, r in enumerate(perm):
         a = out_a[int(w.query_start_loc[r]):int(w.query_start_loc[r + 1])]
         b = out_b[int(qsl[k]):int(qsl[k + 1])]
-        if int(w.q_lens[r]) > 1:
-            assert torch.equal(a, b), f"prefill request {r} changed with the batch order"
-        else:
-            rr = ref[int(w.query_start_loc[r]):int(w.query_start_loc[r + 1])]
-            assert_close_to_oracle(a, rr, what=f"decode row {r}, batch order")
-            assert_close_to_oracle(b, rr, what=f"decode row {r}, permuted order")
+        rr = ref[int(w.query_start_loc[r]):int(w.query_start_loc[r + 1])]
+        assert_close_to_oracle(a, rr, what=f"request {r}, batch order")
+        assert_close_to_oracle(b, rr, what=f"request {r}, permuted order")
+        assert_close_to_oracle(b, a.double().cpu().numpy(), what=f"request {r}, the two orders")
