@@ -521,8 +521,9 @@ def extra_decode_fp8(pa, name, dev, flush, reps=20, xsplit=False):
     s = _time(call, flush, reps)
     kv8 = ab["kv_bytes"] // 2
     dec8 = ab["decode_bytes"] - ab["kv_bytes"] + kv8
-    rl = hbm_roofline(("pa_decode_xsplit_fp8" if xsplit else "pa_decode_fp8") + " (e4m3 cache)",
-                      dec8, s)
+    rl = hbm_roofline(("pa_decode_xsplit_fp8" if xsplit else "pa_decode_fp8") + " (e4m3 cache, " +
+                      ("tcgen05 decode)" if w.num_heads // w.num_kv_heads > 4 and not xsplit
+                       else "warp-level products)"), dec8, s)
     res = {"kv_dtype": "e4m3", "kv_layout": "x-split" if xsplit else "token-major",
            "us_per_call": round(s * 1e6, 2), "kv_gbs": round(kv8 / s / 1e9, 2),
            "decode_gbs": round(dec8 / s / 1e9, 2),
@@ -710,6 +711,7 @@ def main(argv=None):
                                                     "mixed_chunked_prefill",
                                                     "multi_chunk_prefill",
                                                     "llama8b_decode_b64_fp8",
+                                                    "prefix_shared_decode_b256_fp8",
                                                     "llama8b_decode_b64_fp8_xsplit",
                                                     "llama8b_decode_b64_xsplit",
                                                     "prefix_shared_decode_b256_xsplit"])

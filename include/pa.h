@@ -236,7 +236,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
  *   seq_lens      [num_seqs] int32, each in [1, max_seq_len]
  *   max_seq_len   host-side upper bound of seq_lens (sizes the grid; no
  *                 device-to-host read happens)
- *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim))
+ *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim));
+ *                 finite and > 0 (else PA_ERR_INVALID)
  *   partition_tokens  split-KV granularity.  0 (the default) splits the
  *                 batch's K/V evenly over as many CTAs as the GPU holds at
  *                 once; a positive multiple of block_size instead uses one
@@ -301,11 +302,13 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
  * pa_reshape_and_cache_fp8: key t contributes decoded(K_t) * k_scale and
  * value t decoded(V_t) * v_scale ("vLLM 深度解析（二）", section 3.2,
  * fp8::scaled_convert inside the K/V load).  Same arguments, workspace
- * (pa_decode_workspace_size) and results as pa_decode otherwise.  The
- * products run on the tensor cores in f16: e4m3 K and V convert to f16
- * exactly; q and the softmax weights are rounded to f16 (q saturates at
- * +-65504).
- * Supported: 1 to 4 q heads per kv head (PA_ERR_UNSUPPORTED beyond);
+ * (pa_decode_workspace_size), sizes (1 to 16 q heads per kv head) and
+ * results as pa_decode otherwise.  The products run on the tensor cores in
+ * f16: e4m3 K and V convert to f16 exactly; q and the softmax weights are
+ * rounded to f16 (q saturates at +-65504).  Up to 4 q heads per kv head the
+ * warp-level products read the e4m3 bytes directly; from 5 to 16 the
+ * tcgen05 decode converts each landed 128-token chunk (K into tensor
+ * memory, V into shared memory) before its MMAs.
  * k_scale and v_scale finite and > 0 (else PA_ERR_INVALID).
  */
 pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,

@@ -372,12 +372,21 @@ int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
                       int32_t block_size, double scale, double k_scale, double v_scale) {
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
     int32_t heads_per_kv = num_heads / num_kv_heads;
-    for (int32_t r = 0; r < num_seqs; ++r) {
+    int64_t max_len = 1;
+    for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
+    int failed = 0;
+    /* one (request, q head) row per iteration; each thread its own weights */
+#pragma omp parallel num_threads(g_threads) reduction(|| : failed)
+    {
+    double* w = (double*)malloc(sizeof(double) * (size_t)max_len);
+    if (!w) failed = 1;
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t rh = 0; rh < (int64_t)num_seqs * num_heads; ++rh) {
+        if (!w) continue;
+        int32_t r = (int32_t)(rh / num_heads), h = (int32_t)(rh % num_heads);
         int64_t n = seq_lens[r];
-        double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-        if (!w) return -2;
         const int32_t* table = block_tables + (int64_t)r * max_blocks_per_seq;
-        for (int32_t h = 0; h < num_heads; ++h) {
+        {
             const uint16_t* qh = q + ((int64_t)r * num_heads + h) * head_dim;
             int32_t kvh = h / heads_per_kv;
             double top = -INFINITY;
@@ -401,9 +410,10 @@ int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
                     o[x] += (w[t] / total) * (oracle_e4m3_decode(vr[x]) * v_scale);
             }
         }
-        free(w);
     }
-    return 0;
+    free(w);
+    }
+    return failed ? -2 : 0;
 }
 
 /* ---- The x-split cache layout (page 1 section 3.2.1) --------------------

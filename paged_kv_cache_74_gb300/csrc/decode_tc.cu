@@ -63,24 +63,31 @@ constexpr float kNegBigTc = -1e30f;
 constexpr float kSlackTc = 8.0f;  // log2 units
 constexpr int kEndSeg = 7;        // segment record kind: no more work
 
-template <int D, int GM>
+template <int D, int GM, bool KV8 = false>
 struct TcCfg {
   static constexpr int HALVES = D / 64;             // 128-byte column chunks of head_dim
   static constexpr int CB = 8;                      // blocks per chunk
   static constexpr int CT = CB * kBlockSize;        // tokens per chunk (MMA M)
   static constexpr int N = 16;                      // MMA N: the group's q heads, padded
-  static constexpr int BLK = HALVES * kBlockSize * 128;  // K (or V) bytes of one block
-  // A block lands as [8-token group][head_dim half][8 tokens][128 B]: the
+  static constexpr int BLK = HALVES * kBlockSize * 128;  // 16-bit K (or V) bytes of one block
+  static constexpr int BLK8 = kBlockSize * D;       // e4m3 K (or V) bytes of one block
+  // A 16-bit block is [8-token group][head_dim half][8 tokens][128 B]: the
   // 8-token groups of a chunk are GSTRIDE apart, head_dim halves 1 KB apart.
   static constexpr int GSTRIDE = HALVES * 1024;
-  static constexpr int STAGE = CB * BLK;            // one chunk of K (or of V)
-  static constexpr int NST = D == 128 ? 3 : 6;      // K stages = V stages
+  static constexpr int STAGE = CB * BLK;            // one 16-bit chunk of K (or of V)
+  static constexpr int RSTAGE = KV8 ? CB * BLK8 : STAGE;  // one chunk as it lands
+  // K stages = V stages (as they land; an e4m3 stage is half as large).
+  static constexpr int NST = KV8 ? (D == 128 ? 4 : 8) : (D == 128 ? 3 : 6);
+  // e4m3: converted chunks, K (f16) in TMEM and V (f16) in shared memory.
+  static constexpr int NCK = KV8 ? 3 : 0;
+  static constexpr int NCV = KV8 ? 2 : 0;
   static constexpr int SLOTS = 4;                   // segment records / q buffers
   static constexpr int QSLOT = HALVES * N * 128;    // q of a segment: [half][16 rows][128 B]
   static constexpr int PBUF = 2 * N * 128;          // P^T: [token half][16 rows][128 B]
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + NST * STAGE;
-  static constexpr int OFF_Q = OFF_V + NST * STAGE;  // also absorbs the unused half of A at D = 64
+  static constexpr int OFF_V = OFF_K + NST * RSTAGE;
+  static constexpr int OFF_VC = OFF_V + NST * RSTAGE;  // converted V (e4m3 caches)
+  static constexpr int OFF_Q = OFF_VC + NCV * STAGE;  // also absorbs the unused half of A at D = 64
   static constexpr int OFF_P = OFF_Q + SLOTS * QSLOT;
   static constexpr int OFF_SEG = OFF_P + 2 * PBUF;
   static constexpr int SEG_BYTES = 48;
@@ -89,25 +96,28 @@ struct TcCfg {
   static constexpr int NREC = 2 * NST;              // chunk records (K producer -> V producer)
   static constexpr int OFF_REC = OFF_ML + SLOTS * 5 * GM * 4;  // [NREC][12] ints
   static constexpr int OFF_BAR = OFF_REC + NREC * 48;
-  static constexpr int NBAR = 4 * NST + 3 * SLOTS + 2 * 6 + 2 + NREC;
+  static constexpr int NBAR = 4 * NST + 3 * SLOTS + 2 * 6 + 2 + NREC + 2 * NCK + 2 * NCV + SLOTS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + 1024-byte alignment slack
-  static constexpr int THREADS = 11 * 32;
-  static constexpr uint32_t TMEM_COLS = 64;          // S0 0, S1 16, O0 32, O1 48
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(CT, N, 0, 0);
-  static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, N, 0, 1);
+  static constexpr int THREADS = (KV8 ? 15 : 11) * 32;  // + 4 converter warps for e4m3
+  // TMEM: S0 0, S1 16, O0 32, O1 48; e4m3: converted K chunks from KCOL.
+  static constexpr uint32_t KCOL = 64;
+  static constexpr uint32_t TMEM_COLS = KV8 ? 256 : 64;
+  static constexpr uint32_t IDESC_S = KV8 ? idesc_f16_f32(CT, N, 0, 0) : idesc_bf16_f32(CT, N, 0, 0);
+  static constexpr uint32_t IDESC_O = KV8 ? idesc_f16_f32(128, N, 0, 1) : idesc_bf16_f32(128, N, 0, 1);
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(GM == 4 || GM == 8 || GM == 16, "group bucket");
+  static_assert(KCOL + NCK * (D / 2) <= TMEM_COLS, "tensor memory");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Barrier indices.
-template <int NST, int SLOTS, int NREC>
+template <int NST, int SLOTS, int NREC, int NCK, int NCV>
 struct TcBars {
   static constexpr int KFULL = 0;                 // [NST] K chunk landed
-  static constexpr int KFREE = KFULL + NST;       // [NST] S MMA done reading it
+  static constexpr int KFREE = KFULL + NST;       // [NST] S MMA (e4m3: the converter) done with it
   static constexpr int VFULL = KFREE + NST;       // [NST]
-  static constexpr int VFREE = VFULL + NST;       // [NST] P.V MMA done reading it
+  static constexpr int VFREE = VFULL + NST;       // [NST] P.V MMA (e4m3: the converter) done with it
   static constexpr int QFULL = VFREE + NST;       // [SLOTS] segment record + q landed
   static constexpr int LREADY = QFULL + SLOTS;    // [SLOTS] softmax published m, l (4 warps)
   static constexpr int SEGFREE = LREADY + SLOTS;  // [SLOTS] epilogue done with the slot (4 warps)
@@ -120,7 +130,12 @@ struct TcBars {
   static constexpr int RED = OFREE + 2;           // softmax-warp barrier (4 warps)
   static constexpr int ERED = RED + 1;            // epilogue-warp barrier (4 warps)
   static constexpr int CREC = ERED + 1;           // [NREC] chunk record written
-  static constexpr int COUNT = CREC + NREC;
+  static constexpr int KCFULL = CREC + NREC;      // [NCK] converted K in TMEM (4 converter warps)
+  static constexpr int KCFREE = KCFULL + NCK;     // [NCK] S MMA done reading it
+  static constexpr int VCFULL = KCFREE + NCK;     // [NCV] converted V (4 converter warps)
+  static constexpr int VCFREE = VCFULL + NCV;     // [NCV] P.V MMA done reading it
+  static constexpr int QCONV = VCFREE + NCV;      // [SLOTS] q converted to f16 (4 converter warps)
+  static constexpr int COUNT = QCONV + SLOTS;
 };
 
 // A segment: the run of 16-token tiles [b0, b0 + nseg) of one (request, kv
@@ -160,13 +175,38 @@ __device__ __forceinline__ int f2key(float x) {
 }
 __device__ __forceinline__ float key2f(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff)); }
 
-template <int D, int GM>
-__global__ void __launch_bounds__(TcCfg<D, GM>::THREADS, 1)
+// ---- e4m3 caches: every e4m3 value is exact in f16, so the converter warps
+// turn the landed K and V bytes into f16 operands without rounding; q and
+// the weights are rounded to f16 (q saturates at +-65504).
+// Two e4m3 values (low byte first) as f16x2 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+  return h2;
+}
+// Two bf16 values (low half first) rounded to f16x2, saturated to +-65504.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+      : "=r"(h2)
+      : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+  return h2;
+}
+// 16-byte chunk c of token row t of a landed e4m3 block (16 rows of head_dim
+// bytes, 128-byte swizzle at head_dim 128, 64-byte at 64).
+template <int D>
+__device__ __forceinline__ uint32_t e8_chunk(int t, int c) {
+  const int sw = D == 128 ? (t & 7) : ((t >> 1) & 3);
+  return static_cast<uint32_t>(t * D + ((c ^ sw) * 16));
+}
+
+template <int D, int GM, bool KV8>
+__global__ void __launch_bounds__(TcCfg<D, GM, KV8>::THREADS, 1)
 paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using C = TcCfg<D, GM>;
-  using B = TcBars<C::NST, C::SLOTS, C::NREC>;
+  using C = TcCfg<D, GM, KV8>;
+  using B = TcBars<C::NST, C::SLOTS, C::NREC, C::NCK, C::NCV>;
   const int cta = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -177,6 +217,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint32_t sbase = smem_u32(smem);
   const uint32_t k_s = sbase + C::OFF_K;
   const uint32_t v_s = sbase + C::OFF_V;
+  const uint32_t vc_s = sbase + C::OFF_VC;  // e4m3 caches: V converted to f16
   const uint32_t q_s = sbase + C::OFF_Q;
   const uint32_t p_s = sbase + C::OFF_P;
   const uint32_t bar0 = sbase + C::OFF_BAR;
@@ -195,13 +236,21 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   volatile int* n_v_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 36);
   volatile long long* total_cost = reinterpret_cast<volatile long long*>(smem + C::OFF_MISC + 40);
   volatile int* cost_chunk = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 48);
-  int* recs = reinterpret_cast<int*>(smem + C::OFF_REC);  // [NREC][12]: V rows of 8 blocks, kv head, blocks
+  // [NREC][12]: V rows of 8 blocks, kv head, blocks, valid tokens, first chunk of segment slot + 1
+  int* recs = reinterpret_cast<int*>(smem + C::OFF_REC);
 
   if (tid == 0) {
     for (int k = 0; k < B::COUNT; ++k) {
       const bool four = (k >= B::LREADY && k < B::SEGFREE + C::SLOTS) ||
                         (k >= B::SFREE && k < B::SFREE + 2) || (k >= B::PFULL && k < B::PFULL + 2) ||
-                        (k >= B::OFREE && k < B::OFREE + 2) || k == B::RED || k == B::ERED;
+                        (k >= B::OFREE && k < B::OFREE + 2) || k == B::RED || k == B::ERED ||
+                        // e4m3: the converter warps free the landed stages and fill
+                        // the converted K, V and q
+                        (KV8 && ((k >= B::KFREE && k < B::KFREE + C::NST) ||
+                                 (k >= B::VFREE && k < B::VFREE + C::NST) ||
+                                 (k >= B::KCFULL && k < B::KCFULL + C::NCK) ||
+                                 (k >= B::VCFULL && k < B::VCFULL + C::NCV) ||
+                                 (k >= B::QCONV && k < B::QCONV + C::SLOTS)));
       mbar_init(bar(k), four ? 4 : 1);
     }
     *fail_flag = 0;
@@ -495,16 +544,23 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           if (lane == 0) {
             rec[8] = kvh;
             rec[9] = nbc;
+            rec[10] = min(nbc * kBlockSize, len - (b + C::CB * c) * kBlockSize);  // valid tokens
+            rec[11] = c == 0 ? slot + 1 : 0;  // first chunk of the segment in q slot `slot`
           }
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(bar(B::CREC + chunk % C::NREC));
-            mbar_arrive_expect_tx(bar(B::KFULL + st), nbc * C::BLK);
+            mbar_arrive_expect_tx(bar(B::KFULL + st), nbc * (KV8 ? C::BLK8 : C::BLK));
           }
           __syncwarp();
-          if (lane < nbc)
-            tma_load_5d(k_s + st * C::STAGE + lane * C::BLK, &kmap, bar(B::KFULL + st), 0, 0, 0,
-                        krow / 8, kvh, policy);
+          if (lane < nbc) {
+            if constexpr (KV8)  // e4m3: 16 token rows of head_dim bytes, swizzled
+              tma_load_3d(k_s + st * C::RSTAGE + lane * C::BLK8, &kmap, bar(B::KFULL + st), 0, kvh, krow,
+                          policy);
+            else
+              tma_load_5d(k_s + st * C::STAGE + lane * C::BLK, &kmap, bar(B::KFULL + st), 0, 0, 0,
+                          krow / 8, kvh, policy);
+          }
           ++chunk;
           if (lane == 0) *n_chunks_issued = chunk;
         }
@@ -587,11 +643,16 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       const int st = i % C::NST;
       // V: refill once the P.V MMA of chunk i - NST is done.
       if (i >= C::NST && !(ok = warp_wait(bar(B::VFREE + st), ((i / C::NST) - 1) & 1, 22))) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + st), nbc * C::BLK);
+      if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + st), nbc * (KV8 ? C::BLK8 : C::BLK));
       __syncwarp();
-      if (lane < nbc)
-        tma_load_5d(v_s + st * C::STAGE + lane * C::BLK, &vmap, bar(B::VFULL + st), 0, 0, 0, vrow / 8,
-                    kvh, policy);
+      if (lane < nbc) {
+        if constexpr (KV8)
+          tma_load_3d(v_s + st * C::RSTAGE + lane * C::BLK8, &vmap, bar(B::VFULL + st), 0, kvh, vrow,
+                      policy);
+        else
+          tma_load_5d(v_s + st * C::STAGE + lane * C::BLK, &vmap, bar(B::VFULL + st), 0, 0, 0, vrow / 8,
+                      kvh, policy);
+      }
       if (lane == 0) *n_v_issued = i + 1;
     }
     if (!ok && lane == 0) *fail_flag = 1;
@@ -608,9 +669,14 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         const int pb = pv_j & 1;
         const int st = pv_j % C::NST;
         const int ob = pv_seg & 1;
+        const int cv = KV8 ? pv_j % C::NCV : 0;
         if (*fail_flag) return false;
         if (!mbar_wait(bar(B::PFULL + pb), (pv_j >> 1) & 1)) { give_up(30); return false; }
-        if (!mbar_wait(bar(B::VFULL + st), (pv_j / C::NST) & 1)) { give_up(31); return false; }
+        if (!(KV8 ? mbar_wait(bar(B::VCFULL + cv), (pv_j / C::NCV) & 1)
+                  : mbar_wait(bar(B::VFULL + st), (pv_j / C::NST) & 1))) {
+          give_up(31);
+          return false;
+        }
         if (pv_first && pv_seg >= 2 && !mbar_wait(bar(B::OFREE + ob), ((pv_seg - 2) >> 1) & 1)) {
           give_up(32);
           return false;
@@ -620,12 +686,14 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int kk = 0; kk < C::CB; ++kk) {
           // A = V^T of block kk (MN-major: head_dim halves 1 KB apart, its two
           // 8-token groups GSTRIDE apart); B = P^T tokens 16 kk .. 16 kk + 15.
-          umma_bf16(tmem + 32 + ob * 16, sdesc_sw128(v_s + st * C::STAGE + kk * C::BLK, 1024, C::GSTRIDE),
+          // (e4m3: the f16 V the converter warps wrote in the same layout)
+          const uint32_t va = KV8 ? vc_s + cv * C::STAGE + kk * C::BLK : v_s + st * C::STAGE + kk * C::BLK;
+          umma_bf16(tmem + 32 + ob * 16, sdesc_sw128(va, 1024, C::GSTRIDE),
                     sdesc_sw128(p_s + pb * C::PBUF + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024),
                     C::IDESC_O, (pv_first && kk == 0) ? 0u : 1u);
         }
         umma_commit(bar(B::PVDONE + pb));
-        umma_commit(bar(B::VFREE + st));
+        umma_commit(bar(KV8 ? B::VCFREE + cv : B::VFREE + st));
         if (pv_last) umma_commit(bar(B::OFULL + ob));
         *n_pv_issued = pv_j + 1;
         return true;
@@ -639,24 +707,41 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         const TcSeg si = segs[slot];
         if (si.kind == kEndSeg) break;
+        // e4m3: q of the segment converted to f16 by the converter warps.
+        if (KV8 && !mbar_wait(bar(B::QCONV + slot), (seg / C::SLOTS) & 1)) {
+          give_up(35);
+          ok = false;
+          break;
+        }
         const int nch = (si.nseg + C::CB - 1) / C::CB;
         for (int c = 0; c < nch && ok; ++c, ++j) {
           const int st = j % C::NST;
+          const int ck = KV8 ? j % C::NCK : 0;
           const int sb = j & 1;
-          if (*fail_flag || !mbar_wait(bar(B::KFULL + st), (j / C::NST) & 1)) { ok = false; break; }
+          if (*fail_flag || !(KV8 ? mbar_wait(bar(B::KCFULL + ck), (j / C::NCK) & 1)
+                                  : mbar_wait(bar(B::KFULL + st), (j / C::NST) & 1))) {
+            ok = false;
+            break;
+          }
           if (j >= 2 && !mbar_wait(bar(B::SFREE + sb), ((j - 2) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            // A = K (128 tokens x head_dim, K-major: 8-token groups GSTRIDE
-            // apart, head_dim halves 1 KB apart), B = q (16 rows x head_dim).
-            const uint32_t ka = k_s + st * C::STAGE + (kk >> 2) * 1024 + (kk & 3) * 32;
+            // A = K (128 tokens x head_dim), B = q (16 rows x head_dim).  bf16:
+            // K-major in shared memory (8-token groups GSTRIDE apart, head_dim
+            // halves 1 KB apart); e4m3: converted to f16 in TMEM (token = lane).
             const uint32_t qb = q_s + slot * C::QSLOT + (kk >> 2) * (C::N * 128) + (kk & 3) * 32;
-            umma_bf16(tmem + sb * 16, sdesc_sw128(ka, 16, C::GSTRIDE), sdesc_sw128(qb, 16, 1024),
-                      C::IDESC_S, kk > 0 ? 1u : 0u);
+            if constexpr (KV8) {
+              umma_tmem_a(tmem + sb * 16, tmem + C::KCOL + ck * (D / 2) + kk * 8, sdesc_sw128(qb, 16, 1024),
+                          C::IDESC_S, kk > 0 ? 1u : 0u);
+            } else {
+              const uint32_t ka = k_s + st * C::STAGE + (kk >> 2) * 1024 + (kk & 3) * 32;
+              umma_bf16(tmem + sb * 16, sdesc_sw128(ka, 16, C::GSTRIDE), sdesc_sw128(qb, 16, 1024),
+                        C::IDESC_S, kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(bar(B::SFULL + sb));
-          umma_commit(bar(B::KFREE + st));
+          umma_commit(bar(KV8 ? B::KCFREE + ck : B::KFREE + st));
           *n_s_issued = j + 1;
           if (pv_j >= 0 && !(ok = issue_pv())) break;
           pv_j = j;
@@ -773,15 +858,23 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           const float p = (valid && h < G) ? fast_exp2(fmaf(s[h], sl2, -m_ref[h])) : 0.f;
-          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-          l_run[h] += __bfloat162float(pb);
+          uint16_t pbits;
+          if constexpr (KV8) {  // f16 products for e4m3 caches
+            const __half ph = __float2half_rn(p);
+            l_run[h] += __half2float(ph);
+            pbits = __half_as_ushort(ph);
+          } else {
+            const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+            l_run[h] += __bfloat162float(pb);
+            pbits = __bfloat16_as_ushort(pb);
+          }
           const uint32_t r8 = h & 7;
-          st_shared_u16(prow + (h >> 3) * 1024 + r8 * 128 + ((pchunk ^ r8) << 4) + (tl & 7) * 2,
-                        __bfloat16_as_ushort(pb));
+          st_shared_u16(prow + (h >> 3) * 1024 + r8 * 128 + ((pchunk ^ r8) << 4) + (tl & 7) * 2, pbits);
         }
         // V rows of tokens past the context (or of blocks not loaded) may
-        // hold NaN, which a zero weight does not cancel inside the MMA.
-        if (ntok < C::CT) {
+        // hold NaN, which a zero weight does not cancel inside the MMA (the
+        // converter warps write those rows as zeros for e4m3 caches).
+        if (!KV8 && ntok < C::CT) {
           if (!(ok = all_wait(B::VFULL + st, (j / C::NST) & 1))) break;
           if (!valid) {
             const uint32_t vrow =
@@ -859,7 +952,7 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int h = 0; h < GM; ++h) {
           if (h < G) {
             const float L = (ml[GM + h] + ml[2 * GM + h]) + (ml[3 * GM + h] + ml[4 * GM + h]);
-            const float v = o[h] / L;
+            const float v = o[h] * a.v_scale / L;  // v_scale: the e4m3 cache's V scale, else 1
             if (si.kind == kWhole) {
               a.out[(static_cast<size_t>(si.row) * a.num_heads + head0 + h) * D + tl] = __float2bfloat16_rn(v);
             } else {
@@ -912,6 +1005,113 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       ++seg;
     }
     if (!ok && lane == 0 && !*fail_flag) give_up(50);
+  } else if constexpr (KV8) {
+    // ===================================================== e4m3 converter
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31: token tl of every chunk.
+    // Per chunk: K row tl -> f16 into TMEM lane tl (the A operand of S^T =
+    // K Q^T, head_dim pairs along the columns); V row tl -> f16 into the
+    // swizzled [8-token group][head_dim half][8 tokens][128 B] layout the
+    // P.V product reads (rows of tokens past the context written as zeros);
+    // at a segment's first chunk, that segment's q -> f16 in place.
+    const int q4 = warp & 3;
+    const int tl = q4 * 32 + lane;
+    const int ct = tl;  // converter thread 0 .. 127
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    auto all_wait = [&](int k, uint32_t parity, int where) -> bool {
+      if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
+      const bool good = __all_sync(0xffffffffu, mbar_wait(bar(k), parity) ? 1 : 0) != 0;
+      if (!good && lane == 0) give_up(where);
+      return good;
+    };
+    bool ok = true;
+    int seg = 0;
+    int prev_ntok = 0;  // valid tokens of chunk i - 1 (its V is converted after K of chunk i)
+    // Chunk i's K is converted before chunk i - 1's V, so that an S MMA never
+    // waits behind the P.V products that free the converted V buffers.
+    for (int i = 0; ok; ++i) {
+      const int rs = i % C::NREC;
+      if (!(ok = all_wait(B::CREC + rs, (i / C::NREC) & 1, 90))) break;
+      const int* rec = recs + rs * 12;
+      const int nbc = rec[9];
+      const int ntok = rec[10];
+      const int first = rec[11];
+      if (nbc > 0) {
+        const int st = i % C::NST, ck = i % C::NCK;
+        if (first) {
+          const int slot = first - 1;
+          if (!(ok = all_wait(B::QFULL + slot, (seg / C::SLOTS) & 1, 91))) break;
+          for (int u = ct; u < C::QSLOT / 16; u += 128) {
+            const uint32_t addr = q_s + slot * C::QSLOT + u * 16;
+            const uint4 w = ld_shared_v4(addr);
+            st_shared_v4(addr, make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y),
+                                          bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w)));
+          }
+          fence_proxy_async_smem();  // read by the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B::QCONV + slot));
+          ++seg;
+        }
+        if (!(ok = all_wait(B::KFULL + st, (i / C::NST) & 1, 92))) break;
+        if (i >= C::NCK && !(ok = all_wait(B::KCFREE + ck, ((i / C::NCK) - 1) & 1, 93))) break;
+        const uint32_t krow = k_s + st * C::RSTAGE + (tl >> 4) * C::BLK8;
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          uint32_t kw[32];  // head_dim 64 h .. 64 h + 63 as 32 f16 pairs
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 w = ld_shared_v4(krow + e8_chunk<D>(tl & 15, 4 * h + c));
+            kw[8 * c + 0] = e4m3x2_to_f16x2(w.x);
+            kw[8 * c + 1] = e4m3x2_to_f16x2(w.x >> 16);
+            kw[8 * c + 2] = e4m3x2_to_f16x2(w.y);
+            kw[8 * c + 3] = e4m3x2_to_f16x2(w.y >> 16);
+            kw[8 * c + 4] = e4m3x2_to_f16x2(w.z);
+            kw[8 * c + 5] = e4m3x2_to_f16x2(w.z >> 16);
+            kw[8 * c + 6] = e4m3x2_to_f16x2(w.w);
+            kw[8 * c + 7] = e4m3x2_to_f16x2(w.w >> 16);
+          }
+          tmem_st32_async(lane_base + C::KCOL + ck * (D / 2) + 32 * h, kw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B::KCFULL + ck));
+          mbar_arrive(bar(B::KFREE + st));  // the landed K stage may be refilled
+        }
+      }
+      if (i > 0) {
+        // V of chunk i - 1.
+        const int j = i - 1, st = j % C::NST, cv = j % C::NCV;
+        if (!(ok = all_wait(B::VFULL + st, (j / C::NST) & 1, 94))) break;
+        if (j >= C::NCV && !(ok = all_wait(B::VCFREE + cv, ((j / C::NCV) - 1) & 1, 95))) break;
+        const uint32_t vrow = v_s + st * C::RSTAGE + (tl >> 4) * C::BLK8;
+        const uint32_t vdst = vc_s + cv * C::STAGE + (tl >> 4) * C::BLK + ((tl >> 3) & 1) * C::GSTRIDE +
+                              (tl & 7) * 128;
+        const bool valid = tl < prev_ntok;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) w = ld_shared_v4(vrow + e8_chunk<D>(tl & 15, c));
+          // dims 16 c .. 16 c + 15: 16-byte units 2 (c % 4) and + 1 of head_dim half c / 4
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16),
+                                      e4m3x2_to_f16x2(w.y), e4m3x2_to_f16x2(w.y >> 16));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16),
+                                      e4m3x2_to_f16x2(w.w), e4m3x2_to_f16x2(w.w >> 16));
+          const int u = 2 * (c & 3);
+          st_shared_v4(vdst + (c >> 2) * 1024 + ((u ^ (tl & 7)) * 16), lo);
+          st_shared_v4(vdst + (c >> 2) * 1024 + (((u + 1) ^ (tl & 7)) * 16), hi);
+        }
+        fence_proxy_async_smem();  // read by the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B::VCFULL + cv));
+          mbar_arrive(bar(B::VFREE + st));  // the landed V stage may be refilled
+        }
+      }
+      prev_ntok = ntok;
+      if (nbc == 0) break;  // end of the chunk records
+    }
+    if (!ok && lane == 0 && !*fail_flag) give_up(96);
   }
 
   __syncthreads();
@@ -940,38 +1140,42 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (a.defer_griddep && tid == 0) griddep_wait();
 }
 
-template <int D, int GM>
+template <int D, int GM, bool KV8>
 cudaError_t launch_decode_tc_impl(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, cudaStream_t stream) {
-  using C = TcCfg<D, GM>;
+  using C = TcCfg<D, GM, KV8>;
   static bool attr_set[64] = {false};  // per device: set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    const cudaError_t err = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GM>,
+    const cudaError_t err = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GM, KV8>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  return launch_overlapped(paged_decode_tc_kernel<D, GM>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
+  return launch_overlapped(paged_decode_tc_kernel<D, GM, KV8>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
                            stream, qmap, kmap, vmap, a);
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_decode_tc_d(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t stream) {
-  if (a.group <= 4) return launch_decode_tc_impl<D, 4>(a, qmap, kmap, vmap, stream);
-  if (a.group <= 8) return launch_decode_tc_impl<D, 8>(a, qmap, kmap, vmap, stream);
-  if (a.group <= 16) return launch_decode_tc_impl<D, 16>(a, qmap, kmap, vmap, stream);
+  if (a.group <= 4) return launch_decode_tc_impl<D, 4, KV8>(a, qmap, kmap, vmap, stream);
+  if (a.group <= 8) return launch_decode_tc_impl<D, 8, KV8>(a, qmap, kmap, vmap, stream);
+  if (a.group <= 16) return launch_decode_tc_impl<D, 16, KV8>(a, qmap, kmap, vmap, stream);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, int head_dim, cudaStream_t stream) {
-  if (head_dim == 128) return launch_decode_tc_d<128>(a, qmap, kmap, vmap, stream);
-  if (head_dim == 64) return launch_decode_tc_d<64>(a, qmap, kmap, vmap, stream);
+                             const CUtensorMap& vmap, int head_dim, bool kv8, cudaStream_t stream) {
+  if (head_dim == 128)
+    return kv8 ? launch_decode_tc_d<128, true>(a, qmap, kmap, vmap, stream)
+               : launch_decode_tc_d<128, false>(a, qmap, kmap, vmap, stream);
+  if (head_dim == 64)
+    return kv8 ? launch_decode_tc_d<64, true>(a, qmap, kmap, vmap, stream)
+               : launch_decode_tc_d<64, false>(a, qmap, kmap, vmap, stream);
   return cudaErrorInvalidValue;
 }
 

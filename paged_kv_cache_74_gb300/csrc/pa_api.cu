@@ -405,7 +405,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
         !make_kv_group_map(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
-  } else if (!make_cache_map_e4m3(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
+  } else if ((tc && !make_q_group_map(&qmap, q, total_q, num_heads, head_dim, group)) ||
+             !make_cache_map_e4m3(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
              !make_cache_map_e4m3(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim)) {
     return PA_ERR_CUDA;
   }
@@ -436,8 +437,7 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.scale_log2 = scale * 1.4426950408889634f * kv.k_scale;
   a.v_scale = kv.v_scale;
   a.defer_griddep = after_prefill ? 1 : 0;
-  if (tc && kv.e4m3) return PA_ERR_UNSUPPORTED;
-  const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, stream)
+  const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, kv.e4m3, stream)
                             : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, kv.xsplit, stream);
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -636,7 +636,6 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const v
   if (st != PA_OK) return st;
   if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
     return PA_ERR_INVALID;
-  if (decode_uses_tc(head_dim, num_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
   if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,

@@ -91,11 +91,13 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, bool kv8, bool xsplit, cudaStream_t stream);
 // Tensor-core decode (decode_tc.cu): qmap = q as {head_dim, heads, rows}
-// with a {64, group, 1} box; kmap, vmap = the caches as {64, 8, head_dim /
+// with a {64, group, 1} box; kmap, vmap = bf16 caches as {64, 8, head_dim /
 // 64, slots / 8, kv heads} with a {64, 8, head_dim / 64, 2, 1} box (one
-// block of one kv head per copy); all 128-byte swizzled.
+// block of one kv head per copy), all 128-byte swizzled; kv8: e4m3 caches
+// as {head_dim, kv heads, slots} bytes with a {head_dim, 1, 16} box
+// (128-byte swizzle at head_dim 128, 64-byte at 64).
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
+                             const CUtensorMap& vmap, int head_dim, bool kv8, cudaStream_t stream);
 // Smallest group size the decode kernel is instantiated for that covers g.
 int decode_gmax(int group);
 // CTAs per SM the decode kernel for (head_dim, group) is built for.

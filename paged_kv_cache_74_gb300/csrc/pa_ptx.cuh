@@ -204,6 +204,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn, in
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16 with f16 A and B (fp32 accumulator),
+// majors and shape as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn, int a_mn = 0) {
+  return idesc_bf16_f32(M, N, b_mn, a_mn) & ~((1u << 7) | (1u << 10));
+}
+
 // D (TMEM) = A * B (+ D if accumulate).
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {

@@ -214,6 +214,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   volatile int* n_k_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 12);
   volatile int* n_v_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
   volatile int* n_q_issued = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 20);  // [2]
+  volatile int* direct_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 28);
 
   if (tid == 0) {
     for (int k = 0; k < B::COUNT; ++k) {
@@ -225,6 +226,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     *fail_flag = 0;
     *last_flag = 0;
+    *direct_flag = 0;
     *n_k_issued = 0;
     *n_v_issued = 0;
     n_q_issued[0] = 0;
@@ -721,38 +723,141 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           if (lane == 0) mbar_arrive(bar(B::PFULL + b));
         }
         if (!ok) break;
-        // ---- end of the segment: O_b / l, or the partial
-        if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
-        tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        // O_b row, 64 columns per TMEM round trip.
-        const bool whole = sg.kind == kSegWhole;
-        const size_t rec = ((static_cast<size_t>(cta) * 2 + pslot) * 2 + b) * C::BM + i_row;
-        __nv_bfloat16* dst_o =
-            a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
-        // partial O is column-major ([D][128 rows]): a warp's stores of one
-        // column are 128 contiguous bytes
-        float* dst_p = a.part_o + (rec - i_row) * D + i_row;
-        if (!whole) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(m_ref, l_run);
+      }
+      if (!ok) break;
+      // ---- end of the segment: O_b / l, the partial, or the merge
+      const bool whole = sg.kind == kSegWhole;
+      const int c0 = sg.c0, c1 = sg.c1;
+      const int unit = sg.unit;
+      // Record of contributor c's piece: partial slot 1 for the unit's first
+      // CTA (its tail piece), else slot 0; O column-major ([D][128 rows]).
+      auto rec_of = [&](int c) -> size_t {
+        return ((static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b) * C::BM + i_row;
+      };
+      // Merge of the unit's pieces for this row: the published partials of
+      // the CTAs in [c0, c1] other than `skip`, plus (own = true) this CTA's
+      // piece straight from TMEM (unnormalised O, reference m_ref, sum
+      // l_run).  Loads are issued in batches, one round trip per batch.
+      auto merge = [&](bool own, int skip) {
+        float M = own ? m_ref : kNegBigP;
+        for (int c = c0; c <= c1; c += 4) {
+          float m4[4];
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          uint32_t orow[64];
-          tmem_ld32_async(tm_o + h * 64, orow);
-          tmem_ld32_async(tm_o + h * 64 + 32, orow + 32);
-          tmem_wait_ld();
-          if (whole) {
-            if (i_row < sg.rows) {
+          for (int u = 0; u < 4; ++u)
+            m4[u] = (c + u <= c1 && c + u != skip) ? __ldcg(a.part_ml + rec_of(c + u) * 2) : kNegBigP;
+          M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        }
+        const float w_own = own ? fast_exp2(m_ref - M) : 0.f;
+        float L = l_run * w_own;
+        for (int c = c0; c <= c1; c += 4) {
+          float2 ml4[4];
 #pragma unroll
-              for (int e = 0; e < 64; e += 8)
-                *reinterpret_cast<uint4*>(dst_o + h * 64 + e) = make_uint4(
-                    pack_bf16x2(__uint_as_float(orow[e]) * inv, __uint_as_float(orow[e + 1]) * inv),
-                    pack_bf16x2(__uint_as_float(orow[e + 2]) * inv, __uint_as_float(orow[e + 3]) * inv),
-                    pack_bf16x2(__uint_as_float(orow[e + 4]) * inv, __uint_as_float(orow[e + 5]) * inv),
-                    pack_bf16x2(__uint_as_float(orow[e + 6]) * inv, __uint_as_float(orow[e + 7]) * inv));
-            }
+          for (int u = 0; u < 4; ++u)
+            ml4[u] = (c + u <= c1 && c + u != skip)
+                         ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec_of(c + u) * 2))
+                         : make_float2(kNegBigP, 0.f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) L += ml4[u].y * fast_exp2(ml4[u].x - M);
+        }
+        const float invL = L > 0.f ? 1.f / L : 0.f;
+        __nv_bfloat16* dst =
+            a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + (b ? sg.h1 : sg.h0)) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 16) {
+          float acc[16];
+          if (own) {
+            float ov[16];
+            tmem_ld16(tm_o + cc, ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] = ov[e] * w_own;
           } else {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) dst_p[(h * 64 + e) * C::BM] = __uint_as_float(orow[e]) * inv;
+            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+          }
+          for (int c = c0; c <= c1; c += 2) {
+            const bool u0 = c != skip, u1 = c + 1 <= c1 && c + 1 != skip;
+            const size_t r0 = rec_of(c), r1 = rec_of(u1 ? c + 1 : c);
+            const float2 ml0 = u0 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + r0 * 2))
+                                  : make_float2(kNegBigP, 0.f);
+            const float2 ml1 = u1 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + r1 * 2))
+                                  : make_float2(kNegBigP, 0.f);
+            const float* p0 = a.part_o + (r0 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
+            const float* p1 = a.part_o + (r1 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
+            float v0[16], v1[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              v0[e] = u0 ? __ldcg(p0 + e * C::BM) : 0.f;
+              v1[e] = u1 ? __ldcg(p1 + e * C::BM) : 0.f;
+            }
+            const float w0 = ml0.y * fast_exp2(ml0.x - M);
+            const float w1 = ml1.y * fast_exp2(ml1.x - M);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] = fmaf(w0, v0[e], fmaf(w1, v1[e], acc[e]));
+          }
+          if (i_row < sg.rows) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 8)
+              *reinterpret_cast<uint4*>(dst + cc + e) = make_uint4(
+                  pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
+                  pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
+          }
+        }
+      };
+      bool direct = false;
+      if (!whole) {
+        // When every other piece of the unit has already counted, this one
+        // is the last: it merges straight from TMEM without publishing.
+        if (warp == 2 && lane == 0) {
+          int d = 0;
+          if (unit < a.max_units) {
+            const unsigned long long cnt = ld_acquire_u64(a.counters + unit);
+            d = static_cast<unsigned>(cnt >> 32) == a.epoch &&
+                        static_cast<int>(cnt & 0xffffffffu) == c1 - c0
+                    ? 1
+                    : 0;
+          } else {
+            record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 85);
+          }
+          *direct_flag = d;
+        }
+        if (!(ok = sync8())) break;
+        direct = *direct_flag != 0;
+      }
+      if (active) {
+        if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
+        tc_fence_after();
+        if (direct) {
+          merge(true, cta);
+        } else {
+          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+          const size_t rec = ((static_cast<size_t>(cta) * 2 + pslot) * 2 + b) * C::BM + i_row;
+          __nv_bfloat16* dst_o =
+              a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
+          // partial O is column-major: a warp's stores of one column are 128
+          // contiguous bytes
+          float* dst_p = a.part_o + (rec - i_row) * D + i_row;
+          if (!whole) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(m_ref, l_run);
+          // O_b row, 64 columns per TMEM round trip.
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            uint32_t orow[64];
+            tmem_ld32_async(tm_o + h * 64, orow);
+            tmem_ld32_async(tm_o + h * 64 + 32, orow + 32);
+            tmem_wait_ld();
+            if (whole) {
+              if (i_row < sg.rows) {
+#pragma unroll
+                for (int e = 0; e < 64; e += 8)
+                  *reinterpret_cast<uint4*>(dst_o + h * 64 + e) = make_uint4(
+                      pack_bf16x2(__uint_as_float(orow[e]) * inv, __uint_as_float(orow[e + 1]) * inv),
+                      pack_bf16x2(__uint_as_float(orow[e + 2]) * inv, __uint_as_float(orow[e + 3]) * inv),
+                      pack_bf16x2(__uint_as_float(orow[e + 4]) * inv, __uint_as_float(orow[e + 5]) * inv),
+                      pack_bf16x2(__uint_as_float(orow[e + 6]) * inv, __uint_as_float(orow[e + 7]) * inv));
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 64; ++e) dst_p[(h * 64 + e) * C::BM] = __uint_as_float(orow[e]) * inv;
+            }
           }
         }
         tc_fence_before();
@@ -760,72 +865,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (lane == 0) mbar_arrive(bar(B::OFREE + b));
       }
       g += n;
-      if (sg.kind != kSegWhole) {
+      if (!whole && direct) {
+        if (!(ok = sync8())) break;  // direct_flag is read by every warp before it changes
+        if (warp == 2 && lane == 0) release_pair(a.counters + unit);
+      } else if (!whole) {
         // Publish the partial; the last of the unit's contributors merges.
         __threadfence();
         if (!(ok = sync8())) break;
-        if (warp == 2 && lane == 0) {
-          const bool in_range = sg.unit < a.max_units;
-          if (!in_range) record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 85);
-          *last_flag = in_range && contribute(a.counters + sg.unit, a.epoch, sg.c1 - sg.c0 + 1,
-                                              a.status, sg.r) ? 1 : 0;
-        }
+        if (warp == 2 && lane == 0)
+          *last_flag = unit < a.max_units &&
+                               contribute(a.counters + unit, a.epoch, c1 - c0 + 1, a.status, sg.r)
+                           ? 1
+                           : 0;
         if (!(ok = sync8())) break;
-        if (*last_flag && active && i_row < sg.rows) {
-          // Merge this row's pieces: contributor c's record is in partial
-          // slot 1 for the unit's first CTA (its tail piece), else slot 0.
-          // Loads are issued in batches so that a batch costs one round trip.
+        if (*last_flag && active) {
           __threadfence();
-          const int c0 = sg.c0, c1 = sg.c1;
-          auto rec_of = [&](int c) -> size_t {
-            return ((static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b) * C::BM + i_row;
-          };
-          float M = kNegBigP;
-          for (int c = c0; c <= c1; c += 4) {
-            float m4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) m4[u] = c + u <= c1 ? __ldcg(a.part_ml + rec_of(c + u) * 2) : kNegBigP;
-            M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-          }
-          __nv_bfloat16* dst =
-              a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
-          float invL = 0.f;
-#pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            float acc[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            float L = 0.f;
-            for (int c = c0; c <= c1; c += 2) {
-              const bool two = c + 1 <= c1;
-              const size_t r0 = rec_of(c), r1 = rec_of(two ? c + 1 : c);
-              const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + r0 * 2));
-              const float2 ml1 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + r1 * 2));
-              // column-major records: one column of 32 rows is 128 contiguous bytes
-              const float* p0 = a.part_o + (r0 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
-              const float* p1 = a.part_o + (r1 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
-              float v0[32], v1[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                v0[e] = __ldcg(p0 + e * C::BM);
-                v1[e] = __ldcg(p1 + e * C::BM);
-              }
-              const float w0 = ml0.y * fast_exp2(ml0.x - M);
-              const float w1 = two ? ml1.y * fast_exp2(ml1.x - M) : 0.f;
-              L += w0 + w1;
-#pragma unroll
-              for (int e = 0; e < 32; ++e) acc[e] = fmaf(w0, v0[e], fmaf(w1, v1[e], acc[e]));
-            }
-            if (cc == 0) invL = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              *reinterpret_cast<uint4*>(dst + cc + e) = make_uint4(
-                  pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
-                  pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
-          }
+          merge(false, -1);
         }
         if (!(ok = sync8())) break;  // last_flag may change again after this
-        if (warp == 2 && lane == 0 && *last_flag) release_pair(a.counters + sg.unit);
+        if (warp == 2 && lane == 0 && *last_flag) release_pair(a.counters + unit);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B::SEGFREE + slot));

@@ -76,6 +76,7 @@ def decode_call(lib, **kw):
     (dict(q=A + 8), 1), (dict(out=A + 2), 1), (dict(bt=A + 2), 1),
     (dict(hq=6, hkv=4), 1), (dict(hkv=0), 1), (dict(ns=-1), 1), (dict(nb=0), 1),
     (dict(msl=65), 1), (dict(mb=0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(scale=0.0), 1), (dict(scale=-0.125), 1),
     (dict(pt=24), 1), (dict(pt=-16), 1),
     (dict(d=96), 2), (dict(bs=48), 2), (dict(bs=128), 2), (dict(hq=34, hkv=2), 2), (dict(ns=70000), 2),
     (dict(ws=0), 3), (dict(wsb=16), 3),
@@ -163,7 +164,7 @@ def decode_fp8_call(lib, **kw):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(ks=0.0), 1), (dict(vs=-1.0), 1), (dict(ks=float("nan")), 1), (dict(vs=float("inf")), 1),
-    (dict(q=0), 1), (dict(hq=64, hkv=8), 2), (dict(d=96), 2), (dict(ws=0), 3),
+    (dict(q=0), 1), (dict(hq=68, hkv=4), 2), (dict(d=96), 2), (dict(ws=0), 3),
 ])
 def test_decode_fp8_rejects_invalid_arguments(lib, kw, expect):
     assert decode_fp8_call(lib, **kw) == expect

@@ -59,6 +59,9 @@ FP8_SWEEP = [
     (128, 32, 8, 900, 7, 16, 311), (128, 8, 8, 300, 9, 16, 312), (128, 16, 8, 1500, 4, 32, 313),
     (64, 8, 2, 700, 6, 16, 314), (64, 4, 4, 120, 10, 64, 315), (64, 2, 2, 2000, 3, 16, 316),
     (128, 4, 1, 257, 5, 16, 317),
+    # 5 to 16 q heads per kv head: the tensor-core decode with converted K/V
+    (128, 64, 8, 1100, 6, 16, 340), (128, 16, 1, 700, 5, 32, 341), (64, 40, 8, 900, 4, 16, 342),
+    (128, 48, 4, 400, 9, 64, 343), (64, 16, 2, 130, 7, 16, 344),
 ]
 
 
@@ -124,13 +127,43 @@ def test_decode_fp8_full_size_8b(cuda_lib, oracle):
     assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, what="fp8 8B batch")
 
 
-def test_decode_fp8_rejects_large_groups(cuda_lib):
+@pytest.mark.parametrize("pt", [128, 256])
+def test_decode_fp8_large_group_forced_splits(cuda_lib, oracle, pt):
+    """8 q heads per kv head (the tensor-core decode) cut into pieces of one
+    or two 128-token chunks, merged in the kernel, over NaN-coded unused slots."""
     pa = cuda_lib
-    w = wl.random_workload(321, num_seqs=2, max_len=50, num_heads=64, num_kv_heads=8, head_dim=128)
+    w = wl.random_workload(321, num_seqs=5, max_len=1300, min_len=200, num_heads=64,
+                           num_kv_heads=8, head_dim=128)
     t = wl.make_tensors(w, device="cuda")
-    kc = torch.zeros(t.key_cache.shape, dtype=torch.uint8, device="cuda")
-    with pytest.raises(pa.PAError):
-        pa.decode_fp8(t.q, kc, kc.clone(), t.block_tables, t.seq_lens, w.max_seq_len, w.scale, 1.0, 1.0)
+    kc, vc = fp8_caches(w, t, 0.05, 0.02, 321)
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, 64, 8, 128, w.max_seq_len, pt), "cuda")
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale, 0.05,
+                        0.02, workspace=ws, partition_tokens=pt)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle.decode_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(), w.block_tables,
+                            w.seq_lens, w.scale, 0.05, 0.02)
+    assert_close_to_oracle(out, ref, what=f"fp8 group 8, {pt}-token pieces")
+
+
+def test_decode_fp8_full_size_70b_prefix_shared(cuda_lib, oracle):
+    """The 70B-shaped prefix-shared batch (256 requests, 64 q / 8 kv heads,
+    a shared 1024-token prefix) over an e4m3 copy of its cache, in the
+    benchmark's launch configuration; every row against the oracle."""
+    pa = cuda_lib
+    w = wl.prefix_shared_decode()
+    t = wl.make_tensors(w, device="cuda")
+    k_scale = float(t.key_cache.float().abs().max()) / 448.0
+    v_scale = float(t.value_cache.float().abs().max()) / 448.0
+    kc = (t.key_cache.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc = (t.value_cache.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    ws = pa.new_workspace(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads,
+                                                   w.head_dim, w.max_seq_len), "cuda")
+    out = pa.decode_fp8(t.q, kc, vc, t.block_tables, t.seq_lens, w.max_seq_len, w.scale,
+                        k_scale, v_scale, workspace=ws)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle.decode_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(), w.block_tables,
+                            w.seq_lens, w.scale, k_scale, v_scale)
+    assert_close_to_oracle(out, ref, what="fp8 70B prefix-shared batch (every row)")
 
 
 # ---- the x-split layout with an e4m3 cache (x = 16 one-byte elements)

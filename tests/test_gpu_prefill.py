@@ -300,3 +300,25 @@ def test_batch_order_does_not_change_a_requests_rows(cuda_lib, oracle):
         assert_close_to_oracle(a, rr, what=f"request {r}, batch order")
         assert_close_to_oracle(b, rr, what=f"request {r}, permuted order")
         assert_close_to_oracle(b, a.double().cpu().numpy(), what=f"request {r}, the two orders")
+
+
+@pytest.mark.parametrize("q_len,ctx,hq,hkv,d", [(256, 2000, 2, 1, 128), (200, 3000, 3, 1, 64),
+                                                (130, 700, 4, 2, 128), (2, 5000, 2, 2, 128)])
+def test_prefill_unit_split_over_many_ctas(cuda_lib, oracle, q_len, ctx, hq, hkv, d):
+    """A batch with few key steps against a grid of one CTA per SM: each
+    128-row unit is cut into pieces of one or two steps held by many CTAs,
+    whose partials the last contributor merges (directly from tensor memory
+    when every other piece has already counted, else from the published
+    partials); an odd group leaves a single-head unit."""
+    pa = cuda_lib
+    lens = [ctx + q_len, 90]
+    w = wl.build_workload("split", lens, [q_len, 1], num_heads=hq, num_kv_heads=hkv, head_dim=d,
+                          block_size=16, num_blocks=1 + sum(-(-x // 16) for x in lens) + 4,
+                          seed=q_len + ctx)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    for _ in range(2):  # the second call reuses the workspace (counters left at zero)
+        out, ws = run_prefill(pa, w, t)
+        assert pa.device_status(ws)[0] == 0
+    ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    assert_close_to_oracle(out, ref, what=f"split q_len {q_len} ctx {ctx} heads {hq}/{hkv}")

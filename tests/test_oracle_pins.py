@@ -621,9 +621,9 @@ def test_decode_xsplit_fp8_equals_decode_fp8_of_the_same_cache(oracle, hq, hkv, 
 
 
 def test_thread_count_does_not_change_results(oracle):
-    """The OpenMP loops only spread independent output rows: decode and
-    varlen prefill on several threads give the single-thread doubles bit for
-    bit (the all-core CPU baseline times the same arithmetic)."""
+    """The OpenMP loops only spread independent output rows: decode, e4m3
+    decode and varlen prefill on several threads give the single-thread
+    doubles bit for bit (the all-core CPU baseline times the same arithmetic)."""
     w = wl.random_workload(21, num_seqs=5, max_len=300, min_len=20, num_heads=8, num_kv_heads=2,
                            head_dim=64, max_q_len=40, prefill_fraction=0.6)
     t = wl.make_tensors(w)
@@ -641,3 +641,13 @@ def test_thread_count_does_not_change_results(oracle):
             oracle.set_threads(1)
     np.testing.assert_array_equal(runs[0][0], runs[1][0])
     np.testing.assert_array_equal(runs[0][1], runs[1][1])
+    codes = np.random.default_rng(22).integers(0, 127, t.key_cache.shape, dtype=np.uint8)
+    fp8 = []
+    for n in (1, 4):
+        oracle.set_threads(n)
+        try:
+            fp8.append(oracle.decode_fp8(b(t.q)[:w.num_seqs], codes, codes[::-1].copy(),
+                                         w.block_tables, w.seq_lens, w.scale, 0.03, 0.07))
+        finally:
+            oracle.set_threads(1)
+    np.testing.assert_array_equal(fp8[0], fp8[1])
