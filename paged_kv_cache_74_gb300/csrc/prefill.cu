@@ -91,7 +91,9 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + 2 * QBYTES;
   static constexpr int OFF_V = OFF_K + NST * TBYTES;
   static constexpr int OFF_SEG = OFF_V + NST * TBYTES;
-  static constexpr int OFF_BAR = OFF_SEG + SEGS * SEG_INTS * 4;
+  static constexpr int REQ_CACHE = 256;             // requests whose lengths are cached
+  static constexpr int OFF_REQ = OFF_SEG + SEGS * SEG_INTS * 4;  // [3][REQ_CACHE] ints
+  static constexpr int OFF_BAR = OFF_REQ + 3 * REQ_CACHE * 4;
   static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + 1024-byte alignment slack
@@ -137,13 +139,11 @@ struct PReq {
   int q0, q_len, seq_len, ctx, ntq;
 };
 
-__device__ __forceinline__ PReq prefill_req(const PrefillArgs& a, int r) {
+// From request r's query_start_loc[r], [r + 1] and seq_lens[r].
+__device__ __forceinline__ PReq make_req(const PrefillArgs& a, int q0, int q1, int seq_len) {
   PReq p{0, 0, 0, 0, 0};
-  if (r >= a.num_seqs) return p;
-  const int q0 = a.query_start_loc[r];
-  const int q_len = a.query_start_loc[r + 1] - q0;
+  const int q_len = q1 - q0;
   if (q_len <= 1) return p;
-  const int seq_len = a.seq_lens[r];
   if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
       q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q)
     return p;
@@ -153,6 +153,11 @@ __device__ __forceinline__ PReq prefill_req(const PrefillArgs& a, int r) {
   p.ctx = seq_len - q_len;
   p.ntq = (q_len + 127) / 128;
   return p;
+}
+
+__device__ __forceinline__ PReq prefill_req(const PrefillArgs& a, int r) {
+  if (r >= a.num_seqs) return PReq{0, 0, 0, 0, 0};
+  return make_req(a, __ldg(a.query_start_loc + r), __ldg(a.query_start_loc + r + 1), __ldg(a.seq_lens + r));
 }
 
 // Key steps of query tile u (u = 0: the request's last tile) of a request.
@@ -279,9 +284,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // another kCostUnit, when every CTA's share is at least one unit start
     // plus one step wide (so that every CTA between a unit's first and last
     // contributor holds one of its steps); else by steps alone.
+    // query_start_loc and seq_lens of requests 0 .. REQ_CACHE - 1, copied to
+    // shared memory in one round of independent loads.
+    int* rq = reinterpret_cast<int*>(smem + C::OFF_REQ);  // [q0 | q1 | seq_len][REQ_CACHE]
+    {
+      const int nc = min(a.num_seqs, C::REQ_CACHE);
+      int v0[C::REQ_CACHE / 32], v1[C::REQ_CACHE / 32], v2[C::REQ_CACHE / 32];
+#pragma unroll
+      for (int m = 0; m < C::REQ_CACHE / 32; ++m) {
+        const int r = 32 * m + lane;
+        v0[m] = r < nc ? __ldg(a.query_start_loc + r) : 0;
+        v1[m] = r < nc ? __ldg(a.query_start_loc + r + 1) : 0;
+        v2[m] = r < nc ? __ldg(a.seq_lens + r) : 0;
+      }
+#pragma unroll
+      for (int m = 0; m < C::REQ_CACHE / 32; ++m) {
+        rq[32 * m + lane] = v0[m];
+        rq[C::REQ_CACHE + 32 * m + lane] = v1[m];
+        rq[2 * C::REQ_CACHE + 32 * m + lane] = v2[m];
+      }
+      __syncwarp();
+    }
+    auto req_local = [&](int r) -> PReq {
+      if (r >= a.num_seqs) return PReq{0, 0, 0, 0, 0};
+      if (r >= C::REQ_CACHE) return prefill_req(a, r);
+      return make_req(a, rq[r], rq[C::REQ_CACHE + r], rq[2 * C::REQ_CACHE + r]);
+    };
+    auto req_uniform = req_local;  // every lane reads the same entry
     long long nsum = 0, usum = 0;
     for (int r = lane; r < a.num_seqs; r += 32) {
-      const PReq p = prefill_req(a, r);
+      const PReq p = req_local(r);
       nsum += req_steps(p);
       usum += p.ntq;
     }
@@ -291,7 +323,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       usum += __shfl_xor_sync(0xffffffffu, usum, o);
     }
     const long long Cw = (kCostStep * nsum + kCostUnit * usum) * NP;
-    const bool by_cost = Cw / a.num_ctas >= kCostStep + kCostUnit;
+    const bool by_cost = div_ll(Cw, a.num_ctas) >= kCostStep + kCostUnit;
     const long long CT = by_cost ? kCostStep : 1, CS = by_cost ? kCostUnit : 0;
     const long long Ctot = by_cost ? Cw : nsum * NP;
     const long long x0 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta) : 0;
@@ -313,14 +345,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // Steps [j, ..) of a unit whose cost starts at cb: step j starts at
     // cb + CS + CT j.  The first step starting at or after x:
     auto first_step_at = [&](long long cb, long long x) -> long long {
-      return x <= cb + CS ? 0 : (x - cb - CS + CT - 1) / CT;
+      return x <= cb + CS ? 0 : div_ll(x - cb - CS + CT - 1, CT);
     };
     if (x0 < x1) {
       // The request holding cost position x0, with the cost and units before it.
       long long base = 0, ubase = 0;
       int r = -1;
       for (int rc = 0; rc < a.num_seqs && r < 0; rc += 32) {
-        const PReq p = prefill_req(a, rc + lane);
+        const PReq p = req_local(rc + lane);
         const long long ct = (CT * req_steps(p) + CS * p.ntq) * NP;
         const long long nu = static_cast<long long>(p.ntq) * NP;
         long long it = ct, iu = nu;
@@ -345,7 +377,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
       }
       // Unit (query tile u, head pair hp) of request r holding x0.
-      PReq p = prefill_req(a, r);
+      PReq p = req_uniform(r);
       int u = 0, hp = 0, row0 = 0, rows = 0, kv_end = 0;
       int n_u = unit_steps(p, 0, &row0, &rows, &kv_end);
       long long cb = base;   // cost before the current unit
@@ -356,7 +388,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         ub += NP;
         n_u = unit_steps(p, u, &row0, &rows, &kv_end);
       }
-      hp = static_cast<int>((x0 - cb) / (CS + CT * n_u));
+      hp = static_cast<int>(div_ll(x0 - cb, CS + CT * n_u));
       cb += hp * (CS + CT * n_u);
       long long j = first_step_at(cb, x0);
       while (ok) {
@@ -370,7 +402,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (++u == p.ntq) {
               u = 0;
               do {
-                p = prefill_req(a, ++r);
+                p = req_uniform(++r);
               } while (p.ntq == 0 && r < a.num_seqs);
               if (p.ntq == 0) break;  // no more work
             }
@@ -734,28 +766,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       auto rec_of = [&](int c) -> size_t {
         return ((static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b) * C::BM + i_row;
       };
-      // Merge of the unit's pieces for this row: the published partials of
-      // the CTAs in [c0, c1] other than `skip`, plus (own = true) this CTA's
-      // piece straight from TMEM (unnormalised O, reference m_ref, sum
-      // l_run).  Loads are issued in batches, one round trip per batch.
-      auto merge = [&](bool own, int skip) {
-        float M = own ? m_ref : kNegBigP;
-        for (int c = c0; c <= c1; c += 4) {
-          float m4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            m4[u] = (c + u <= c1 && c + u != skip) ? __ldcg(a.part_ml + rec_of(c + u) * 2) : kNegBigP;
-          M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-        }
-        const float w_own = own ? fast_exp2(m_ref - M) : 0.f;
-        float L = l_run * w_own;
+      // Merge of the unit's pieces for this row, in contributor order c0 ..
+      // c1: contributor `own` (this CTA, when it merges without publishing)
+      // is taken from registers and TMEM, the others from their published
+      // partials.  The arithmetic is the same either way (the own piece
+      // enters as the same fp32 values it would have published), so the
+      // result does not depend on which contributor merges.  Loads are
+      // issued in batches, one round trip per batch.
+      auto merge = [&](int own) {
+        const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
+        auto ml_of = [&](int c) -> float2 {
+          return c == own ? make_float2(m_ref, l_run)
+                          : __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec_of(c) * 2));
+        };
+        float M = kNegBigP;
         for (int c = c0; c <= c1; c += 4) {
           float2 ml4[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            ml4[u] = (c + u <= c1 && c + u != skip)
-                         ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec_of(c + u) * 2))
-                         : make_float2(kNegBigP, 0.f);
+          for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) M = fmaxf(M, ml4[u].x);
+        }
+        float L = 0.f;
+        for (int c = c0; c <= c1; c += 4) {
+          float2 ml4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
 #pragma unroll
           for (int u = 0; u < 4; ++u) L += ml4[u].y * fast_exp2(ml4[u].x - M);
         }
@@ -764,30 +800,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + (b ? sg.h1 : sg.h0)) * D;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 16) {
-          float acc[16];
-          if (own) {
+          float mine[16];  // this CTA's normalised piece (used only when own >= 0)
+          if (own >= 0) {
             float ov[16];
             tmem_ld16(tm_o + cc, ov);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[e] = ov[e] * w_own;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+            for (int e = 0; e < 16; ++e) mine[e] = ov[e] * inv_own;
           }
+          float acc[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = 0.f;
           for (int c = c0; c <= c1; c += 2) {
-            const bool u0 = c != skip, u1 = c + 1 <= c1 && c + 1 != skip;
-            const size_t r0 = rec_of(c), r1 = rec_of(u1 ? c + 1 : c);
-            const float2 ml0 = u0 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + r0 * 2))
-                                  : make_float2(kNegBigP, 0.f);
-            const float2 ml1 = u1 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + r1 * 2))
-                                  : make_float2(kNegBigP, 0.f);
+            const bool two = c + 1 <= c1;
+            const bool m0 = c == own, m1 = two && c + 1 == own;
+            const size_t r0 = rec_of(c), r1 = rec_of(two ? c + 1 : c);
+            const float2 ml0 = ml_of(c);
+            const float2 ml1 = two ? ml_of(c + 1) : make_float2(kNegBigP, 0.f);
             const float* p0 = a.part_o + (r0 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
             const float* p1 = a.part_o + (r1 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
             float v0[16], v1[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              v0[e] = u0 ? __ldcg(p0 + e * C::BM) : 0.f;
-              v1[e] = u1 ? __ldcg(p1 + e * C::BM) : 0.f;
+              v0[e] = m0 ? mine[e] : __ldcg(p0 + e * C::BM);
+              v1[e] = m1 ? mine[e] : (two ? __ldcg(p1 + e * C::BM) : 0.f);
             }
             const float w0 = ml0.y * fast_exp2(ml0.x - M);
             const float w1 = ml1.y * fast_exp2(ml1.x - M);
@@ -827,7 +862,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
         tc_fence_after();
         if (direct) {
-          merge(true, cta);
+          merge(cta);
         } else {
           const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
           const size_t rec = ((static_cast<size_t>(cta) * 2 + pslot) * 2 + b) * C::BM + i_row;
@@ -880,7 +915,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (!(ok = sync8())) break;
         if (*last_flag && active) {
           __threadfence();
-          merge(false, -1);
+          merge(-1);
         }
         if (!(ok = sync8())) break;  // last_flag may change again after this
         if (warp == 2 && lane == 0 && *last_flag) release_pair(a.counters + unit);

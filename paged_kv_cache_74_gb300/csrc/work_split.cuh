@@ -11,18 +11,25 @@
 namespace pa {
 namespace {
 
+// 64-bit division, through 32-bit unsigned division when both operands fit
+// (a 64-bit division is a long instruction sequence).
+__device__ __forceinline__ long long div_ll(long long a, long long b) {
+  if (((a | b) >> 31) == 0) return static_cast<unsigned>(a) / static_cast<unsigned>(b);
+  return a / b;
+}
+
 // Equal split of W tiles over C CTAs: CTA c owns [range_lo(c), range_lo(c+1)).
 __device__ __forceinline__ long long range_lo(long long W, int C, int c) {
-  const long long q = W / C, rem = W % C;
+  const long long q = div_ll(W, C), rem = W - q * C;
   return static_cast<long long>(c) * q + (c < rem ? c : rem);
 }
 
 // The CTA whose range holds tile t (0 <= t < W).
 __device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
-  const long long q = W / C, rem = W % C;
+  const long long q = div_ll(W, C), rem = W - q * C;
   const long long big = rem * (q + 1);
-  if (t < big) return static_cast<int>(t / (q + 1));
-  return static_cast<int>(rem + (t - big) / q);
+  if (t < big) return static_cast<int>(div_ll(t, q + 1));
+  return static_cast<int>(rem + div_ll(t - big, q));
 }
 
 // The last contributor of a pair clears its counter once it has merged:
