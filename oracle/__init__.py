@@ -79,6 +79,11 @@ def _declare(lib):
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double]
+    lib.oracle_prefill_varlen_fp8.restype = ctypes.c_int
+    lib.oracle_prefill_varlen_fp8.argtypes = [_F64, _U16, _U8, _U8, _I32, _I32, ctypes.c_int32,
+                                              _I32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_double, ctypes.c_double, ctypes.c_double]
     lib.oracle_reshape_and_cache_xsplit.restype = None
     lib.oracle_reshape_and_cache_xsplit.argtypes = [_U16, _U16, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int32, _U16, _U16, ctypes.c_int32,
@@ -330,6 +335,28 @@ class Oracle:
                                             bs, float(scale))
         if rc != 0:
             raise ValueError(f"oracle_prefill_varlen rejected its arguments ({rc})")
+        return out
+
+    def prefill_varlen_fp8(self, q, key_cache, value_cache, query_start_loc, seq_lens,
+                           block_tables, scale, k_scale: float, v_scale: float) -> np.ndarray:
+        """prefill_varlen over e4m3 caches (uint8 codes) with their scales."""
+        q = _u16(q)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+        qsl = np.ascontiguousarray(query_start_loc, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        bt = np.ascontiguousarray(block_tables, np.int32)
+        tq, hq, d = q.shape
+        nb, bs, hkv, d2 = kc.shape
+        assert d2 == d and int(qsl[-1]) <= tq
+        out = np.zeros((tq, hq, d), np.float64)
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        rc = self.lib.oracle_prefill_varlen_fp8(_p(out, _F64), _p(q, _U16), _p(kc, u8), _p(vc, u8),
+                                                _p(qsl, _I32), _p(sl, _I32), sl.shape[0],
+                                                _p(bt, _I32), bt.shape[1], hq, hkv, d, bs,
+                                                float(scale), float(k_scale), float(v_scale))
+        if rc != 0:
+            raise ValueError(f"oracle_prefill_varlen_fp8 rejected its arguments ({rc})")
         return out
 
     def online_softmax(self, s, v, bounds):

@@ -416,6 +416,77 @@ int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
     return failed ? -2 : 0;
 }
 
+/* ---- Varlen prefill over an FP8 (e4m3) cache (page 1 section 3.2:
+ * fp8::scaled_convert inside the K/V load; "分块预填充与混合批处理" section
+ * 11.6 for the varlen batch).  The same rows as oracle_prefill_varlen, with
+ * key t read as e4m3_decode(K_t) * k_scale and value t as
+ * e4m3_decode(V_t) * v_scale.                                            */
+static void attend_row_fp8(double* out, const uint16_t* q_row, const uint8_t* key_cache,
+                           const uint8_t* value_cache, const int32_t* table_row, int64_t n_keys,
+                           int32_t kv_head, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, double scale, double k_scale, double v_scale,
+                           double* s) {
+    for (int64_t t = 0; t < n_keys; ++t) {
+        int64_t phys = table_row[t / block_size];
+        int64_t off = t % block_size;
+        const uint8_t* k = key_cache + ((phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
+        double dot = 0.0;
+        for (int32_t x = 0; x < head_dim; ++x)
+            dot += bf16_to_double(q_row[x]) * (oracle_e4m3_decode(k[x]) * k_scale);
+        s[t] = dot * scale;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n_keys; ++t) if (s[t] > m) m = s[t];
+    double l = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+    for (int32_t x = 0; x < head_dim; ++x) out[x] = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        int64_t phys = table_row[t / block_size];
+        int64_t off = t % block_size;
+        const uint8_t* v = value_cache + ((phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
+        const double pt = s[t] / l;
+        for (int32_t x = 0; x < head_dim; ++x) out[x] += pt * (oracle_e4m3_decode(v[x]) * v_scale);
+    }
+}
+
+int oracle_prefill_varlen_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
+                              const uint8_t* value_cache, const int32_t* query_start_loc,
+                              const int32_t* seq_lens, int32_t num_seqs,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, double scale, double k_scale, double v_scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+    int32_t group = num_heads / num_kv_heads;
+    int64_t max_len = 0;
+    for (int32_t r = 0; r < num_seqs; ++r) if (seq_lens[r] > max_len) max_len = seq_lens[r];
+    int failed = 0;
+    /* one (request, q head) per iteration, its query rows in order */
+#pragma omp parallel num_threads(g_threads) reduction(|| : failed)
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (!s) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t rh = 0; rh < (int64_t)num_seqs * num_heads; ++rh) {
+                int32_t r = (int32_t)(rh / num_heads), h = (int32_t)(rh % num_heads);
+                int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
+                int64_t context = (int64_t)seq_lens[r] - q_len;
+                for (int32_t i = 0; i < q_len; ++i) {
+                    int64_t row = (int64_t)query_start_loc[r] + i;
+                    attend_row_fp8(out + (row * num_heads + h) * head_dim,
+                                   q + (row * num_heads + h) * head_dim, key_cache, value_cache,
+                                   block_tables + (int64_t)r * max_blocks_per_seq, context + 1 + i,
+                                   h / group, num_kv_heads, head_dim, block_size, scale, k_scale,
+                                   v_scale, s);
+                }
+            }
+            free(s);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
 /* ---- The x-split cache layout (page 1 section 3.2.1) --------------------
  * K cache [num_blocks, num_kv_heads, head_dim / x, block_size, x] and
  * V cache [num_blocks, num_kv_heads, head_dim, block_size], with x the

@@ -56,6 +56,12 @@ int oracle_decode_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
                       int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
                       int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                       int32_t block_size, double scale, double k_scale, double v_scale);
+int oracle_prefill_varlen_fp8(double* out, const uint16_t* q, const uint8_t* key_cache,
+                              const uint8_t* value_cache, const int32_t* query_start_loc,
+                              const int32_t* seq_lens, int32_t num_seqs,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, double scale, double k_scale, double v_scale);
 void oracle_reshape_and_cache_xsplit(const uint16_t* key, const uint16_t* value,
                                      int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                                      uint16_t* key_cache, uint16_t* value_cache,

@@ -58,6 +58,9 @@ constexpr int kSegEnd = 3;              // no more work
 // Split costs (see the producer): a key step, and the start of a unit.
 constexpr long long kCostStep = 4;
 constexpr long long kCostUnit = 10;
+// How long a unit's first CTA waits for the unit's other pieces before it
+// publishes its own instead of merging them.
+constexpr unsigned long long kMergeWaitNs = 20000;
 
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -94,7 +97,15 @@ struct PrefillCfg {
   static constexpr int REQ_CACHE = 256;             // requests whose lengths are cached
   static constexpr int OFF_REQ = OFF_SEG + SEGS * SEG_INTS * 4;  // [3][REQ_CACHE] ints
   static constexpr int OFF_BAR = OFF_REQ + 3 * REQ_CACHE * 4;
-  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2;
+  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2 + 14;
+  // Merge staging at a CTA's last segment: slot b's Q buffer and one K/V
+  // ring (K for slot 0, V for slot 1) are free once O_b is final; they are
+  // cut into 16 KB buffers (32 columns of one partial record), the last one
+  // holding the (m, l) records of up to MREM contributors.
+  static constexpr int MBUF = 16384;
+  static constexpr int MQB = QBYTES / MBUF;                       // buffers in the Q buffer
+  static constexpr int MDATA = (QBYTES + NST * TBYTES) / MBUF - 1;  // partial O buffers
+  static constexpr int MREM = MBUF / (128 * 8);                   // (m, l) records that fit
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + 1024-byte alignment slack
   static constexpr int THREADS = 11 * 32;
@@ -103,6 +114,7 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(MDATA >= 2 && MDATA <= 5 && D % 32 == 0, "merge staging");
 };
 
 // Barrier indices.
@@ -122,7 +134,10 @@ struct PBars {
   static constexpr int SEGFREE = SEGFULL + SEGS; // [SEGS] every role is done with it
   static constexpr int SYNC = SEGFREE + SEGS;    // the 8 softmax warps
   static constexpr int DRAIN = SYNC + 1;         // the MMA warp's last commit
-  static constexpr int COUNT = DRAIN + 1;
+  static constexpr int MFULL = DRAIN + 1;        // [2][5] staged partial O chunk landed
+  static constexpr int MLFULL = MFULL + 10;      // [2] staged (m, l) records landed
+  static constexpr int MSYNC = MLFULL + 2;       // [2] the 4 warps of a slot
+  static constexpr int COUNT = MSYNC + 2;
 };
 
 // A segment: steps [j0, j1) of one unit inside this CTA's range.
@@ -169,14 +184,12 @@ __device__ __forceinline__ int unit_steps(const PReq& p, int u, int* row0, int* 
   return (*kv_end + 127) / 128;
 }
 
-// Key steps of all query tiles of a request (one head pair).
-__device__ __forceinline__ long long req_steps(const PReq& p) {
-  long long n = 0;
-  for (int u = 0; u < p.ntq; ++u) {
-    int row0, rows, kv_end;
-    n += unit_steps(p, u, &row0, &rows, &kv_end);
-  }
-  return n;
+// Key steps of all query tiles of a request (one head pair): the sum of
+// unit_steps() over its tiles in closed form (every tile but the last ends
+// 128 rows after the one before it; the last ends at seq_len).
+__device__ __forceinline__ int req_steps(const PReq& p) {
+  if (p.ntq == 0) return 0;
+  return (p.ntq - 1) * p.ntq / 2 + (p.ntq - 1) * ((p.ctx + 127) / 128) + (p.seq_len + 127) / 128;
 }
 
 // Reports the prefill rows prefill_req() rejects (done once, by CTA 0).
@@ -191,6 +204,237 @@ __device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
     else if (seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size)
       record_error(a.status, PA_DEV_BAD_SEQ_LEN, r, seq_len);
   }
+}
+
+// Partial records of the merge ("vLLM 深度解析（二）：PagedAttention 核心机制",
+// sections 3.2.7 and 3.3: m = max m_j, L = sum l_j e^{m_j - m},
+// O = sum O_j l_j e^{m_j - m} / L).  Record (cta, piece, slot) holds, for each
+// of the unit's 128 query rows, (m_j, l_j) and the normalised O_j row; O is
+// stored as [D / 4][128 rows][4 columns], so that a warp's 16-byte accesses
+// to one column group are 512 contiguous bytes and 32 columns of a record
+// are one contiguous 16 KB block.  Piece 1 is a unit's first CTA (its tail
+// piece), piece 0 any later one.
+__device__ __forceinline__ size_t prec(int c, int c0, int b) {
+  return (static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b;
+}
+
+// The merge of a unit's pieces for one query row (thread i_row of slot b),
+// in contributor order c0 .. c1, from the published partials.  Contributor
+// `own` (this CTA, merging without publishing) is taken from registers
+// (m_ref, l_run) and TMEM (its unnormalised O at tm_o) instead, as the same
+// fp32 values it would have published, so the result does not depend on
+// which contributor merges; weights and sums are taken in the same order as
+// in merge_staged().  Out of line: its registers stay apart from the softmax
+// loop's.  Called by every lane of the warp (the TMEM loads are warp-wide).
+template <int D>
+__device__ __noinline__ void merge_row(const float* __restrict__ part_ml,
+                                       const float* __restrict__ part_o, int c0, int c1, int own,
+                                       int b, int i_row, float m_ref, float l_run, uint32_t tm_o,
+                                       __nv_bfloat16* dst, bool write) {
+  const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
+  auto ml_of = [&](int c) -> float2 {
+    return c == own ? make_float2(m_ref, l_run)
+                    : __ldcg(reinterpret_cast<const float2*>(part_ml + (prec(c, c0, b) * 128 + i_row) * 2));
+  };
+  float M = kNegBigP;
+  for (int c = c0; c <= c1; c += 4) {
+    float2 ml4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) M = fmaxf(M, ml4[u].x);
+  }
+  float L = 0.f;
+  for (int c = c0; c <= c1; c += 4) {
+    float2 ml4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + u <= c1) L += ml4[u].y * fast_exp2(ml4[u].x - M);
+  }
+  const float invL = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 16) {
+    float mine[16];
+    if (own >= 0) {
+      tmem_ld16(tm_o + cc, mine);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) mine[e] *= inv_own;
+    }
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int c = c0; c <= c1; c += 2) {
+      const bool two = c + 1 <= c1;
+      float4 v[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int cu = two ? c + u : c;
+        const float4* src = reinterpret_cast<const float4*>(part_o + prec(cu, c0, b) * (D * 128)) +
+                            (cc / 4) * 128 + i_row;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[u][e] = cu == own ? make_float4(mine[4 * e], mine[4 * e + 1], mine[4 * e + 2], mine[4 * e + 3])
+                              : __ldcg(src + e * 128);
+      }
+      const float2 ml0 = ml_of(c);
+      const float2 ml1 = two ? ml_of(c + 1) : make_float2(kNegBigP, 0.f);
+      const float w0 = ml0.y * fast_exp2(ml0.x - M);
+      const float w1 = ml1.y * fast_exp2(ml1.x - M);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[4 * e] = fmaf(w0, v[0][e].x, acc[4 * e]);
+        acc[4 * e + 1] = fmaf(w0, v[0][e].y, acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(w0, v[0][e].z, acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(w0, v[0][e].w, acc[4 * e + 3]);
+      }
+      if (two) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[4 * e] = fmaf(w1, v[1][e].x, acc[4 * e]);
+          acc[4 * e + 1] = fmaf(w1, v[1][e].y, acc[4 * e + 1]);
+          acc[4 * e + 2] = fmaf(w1, v[1][e].z, acc[4 * e + 2]);
+          acc[4 * e + 3] = fmaf(w1, v[1][e].w, acc[4 * e + 3]);
+        }
+      }
+    }
+    if (write) {
+#pragma unroll
+      for (int e = 0; e < 16; e += 8)
+        *reinterpret_cast<uint4*>(dst + cc + e) = make_uint4(
+            pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
+            pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
+    }
+  }
+}
+
+// The same merge at a CTA's last segment, with the other contributors'
+// records staged in shared memory by bulk copies: their (m, l) records
+// first, then their O records 32 columns at a time, up to C::MDATA copies
+// in flight, instead of a register round trip per few columns.  Run by the
+// 4 warps of slot b (`issuer`: one thread of them issues the copies);
+// `area_q` / `area_r`: slot b's free Q buffer and K or V ring.  Returns false
+// (error recorded) if a wait ran out; copies already issued are then waited
+// for (bounded) before it returns.
+template <int D>
+__device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
+                                          const float* __restrict__ part_o, int c0, int c1, int own,
+                                          int b, int i_row, bool issuer, float m_ref, float l_run,
+                                          uint32_t tm_o, uint32_t area_q, uint32_t area_r,
+                                          uint32_t bar_full, uint32_t bar_ml, uint32_t bar_sync,
+                                          __nv_bfloat16* dst, bool write, int32_t* status, int cta) {
+  using C = PrefillCfg<D>;
+  constexpr int NCH = D / 32;  // 32-column chunks of a record
+  const int lane = threadIdx.x & 31;
+  const int n_rem = c1 - c0 + 1 - (own >= 0 ? 1 : 0);
+  const int total = NCH * n_rem;
+  auto buf = [&](int i) -> uint32_t {
+    return i < C::MQB ? area_q + i * C::MBUF : area_r + (i - C::MQB) * C::MBUF;
+  };
+  const uint32_t ml_buf = buf(C::MDATA);
+  auto remote = [&](int k) -> int { return c0 + k + (own >= 0 && c0 + k >= own ? 1 : 0); };
+  int issued = 0;
+  auto issue = [&](int s) {  // copy s: chunk s / n_rem of remote contributor s % n_rem
+    const int c = remote(s % n_rem), ch = s / n_rem;
+    const uint32_t fb = bar_full + 8 * (s % C::MDATA);
+    mbar_arrive_expect_tx(fb, C::MBUF);
+    bulk_copy_g2s(buf(s % C::MDATA), part_o + prec(c, c0, b) * (D * 128) + ch * (32 * 128), C::MBUF, fb);
+    issued = s + 1;
+  };
+  if (issuer) {
+    // The partials were published (plain stores, a fence, the counter)
+    // before the counter this CTA observed; the copies read them through
+    // the asynchronous proxy.
+    __threadfence();
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(bar_ml, n_rem * 1024);
+    for (int k = 0; k < n_rem; ++k)
+      bulk_copy_g2s(ml_buf + k * 1024, part_ml + prec(remote(k), c0, b) * 256, 1024, bar_ml);
+    for (int s = 0; s < min(C::MDATA, total); ++s) issue(s);
+  }
+  uint32_t sync_phase = 0;
+  auto wait_all = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+    const bool good = __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
+    if (!good && lane == 0) record_error(status, PA_DEV_WAIT_TIMEOUT, cta, where);
+    return good;
+  };
+  bool ok = wait_all(bar_ml, 0, 86);
+  int s = 0;
+  if (ok) {
+    auto ml_at = [&](int c, int k) -> float2 {
+      if (c == own) return make_float2(m_ref, l_run);
+      return ld_shared_f2(ml_buf + (k * 128 + i_row) * 8);
+    };
+    float M = kNegBigP;
+    for (int c = c0, k = 0; c <= c1; ++c) {
+      M = fmaxf(M, ml_at(c, k).x);
+      if (c != own) ++k;
+    }
+    float L = 0.f;
+    for (int c = c0, k = 0; c <= c1; ++c) {
+      const float2 ml = ml_at(c, k);
+      L += ml.y * fast_exp2(ml.x - M);
+      if (c != own) ++k;
+    }
+    const float invL = L > 0.f ? 1.f / L : 0.f;
+    const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < NCH && ok; ++ch) {
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      for (int c = c0, k = 0; c <= c1 && ok; ++c) {
+        const float2 ml = ml_at(c, k);
+        const float w = ml.y * fast_exp2(ml.x - M);
+        float v[32];
+        if (c == own) {
+          uint32_t r[32];
+          tmem_ld32_async(tm_o + ch * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * inv_own;
+        } else {
+          if (!(ok = wait_all(bar_full + 8 * (s % C::MDATA), (s / C::MDATA) & 1, 87))) break;
+          const uint32_t src = buf(s % C::MDATA) + i_row * 16;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint4 u = ld_shared_v4(src + g * 128 * 16);
+            v[4 * g] = __uint_as_float(u.x);
+            v[4 * g + 1] = __uint_as_float(u.y);
+            v[4 * g + 2] = __uint_as_float(u.z);
+            v[4 * g + 3] = __uint_as_float(u.w);
+          }
+          // Every warp of the slot has read buffer s: it takes copy s + MDATA.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sync);
+          if (!(ok = wait_all(bar_sync, sync_phase++ & 1, 88))) break;
+          if (issuer && s + C::MDATA < total) {
+            fence_proxy_async_smem();
+            issue(s + C::MDATA);
+          }
+          ++s;
+          ++k;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+      }
+      if (ok && write) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8)
+          *reinterpret_cast<uint4*>(dst + ch * 32 + e) = make_uint4(
+              pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
+              pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
+      }
+    }
+  }
+  if (!ok && issuer) {
+    // No copy may still be landing when the CTA leaves (bounded waits).
+    (void)mbar_wait(bar_ml, 0);
+    for (int t = max(s, issued - C::MDATA); t < issued; ++t)
+      (void)mbar_wait(bar_full + 8 * (t % C::MDATA), (t / C::MDATA) & 1);
+  }
+  return ok;
 }
 
 template <int D>
@@ -227,6 +471,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       if ((k >= B::PFULL && k < B::PFULL + 2) || (k >= B::OFREE && k < B::OFREE + 2)) count = 4;
       if (k >= B::SEGFREE && k < B::SEGFREE + C::SEGS) count = 10;  // MMA, 8 softmax, V producer
       if (k == B::SYNC) count = 8;
+      if (k >= B::MSYNC && k < B::MSYNC + 2) count = 4;
       mbar_init(bar(k), count);
     }
     *fail_flag = 0;
@@ -289,19 +534,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int* rq = reinterpret_cast<int*>(smem + C::OFF_REQ);  // [q0 | q1 | seq_len][REQ_CACHE]
     {
       const int nc = min(a.num_seqs, C::REQ_CACHE);
-      int v0[C::REQ_CACHE / 32], v1[C::REQ_CACHE / 32], v2[C::REQ_CACHE / 32];
-#pragma unroll
-      for (int m = 0; m < C::REQ_CACHE / 32; ++m) {
-        const int r = 32 * m + lane;
-        v0[m] = r < nc ? __ldg(a.query_start_loc + r) : 0;
-        v1[m] = r < nc ? __ldg(a.query_start_loc + r + 1) : 0;
-        v2[m] = r < nc ? __ldg(a.seq_lens + r) : 0;
-      }
-#pragma unroll
-      for (int m = 0; m < C::REQ_CACHE / 32; ++m) {
-        rq[32 * m + lane] = v0[m];
-        rq[C::REQ_CACHE + 32 * m + lane] = v1[m];
-        rq[2 * C::REQ_CACHE + 32 * m + lane] = v2[m];
+#pragma unroll 1
+      for (int r = lane; r < nc; r += 32) {
+        rq[r] = __ldg(a.query_start_loc + r);
+        rq[C::REQ_CACHE + r] = __ldg(a.query_start_loc + r + 1);
+        rq[2 * C::REQ_CACHE + r] = __ldg(a.seq_lens + r);
       }
       __syncwarp();
     }
@@ -311,21 +548,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       return make_req(a, rq[r], rq[C::REQ_CACHE + r], rq[2 * C::REQ_CACHE + r]);
     };
     auto req_uniform = req_local;  // every lane reads the same entry
-    long long nsum = 0, usum = 0;
+    // (Key steps and units of one head pair fit 32 bits; costs are 64-bit.)
+    int nsum = 0, usum = 0;
+#pragma unroll 1
     for (int r = lane; r < a.num_seqs; r += 32) {
       const PReq p = req_local(r);
       nsum += req_steps(p);
       usum += p.ntq;
     }
-#pragma unroll
+#pragma unroll 1
     for (int o = 16; o >= 1; o >>= 1) {
       nsum += __shfl_xor_sync(0xffffffffu, nsum, o);
       usum += __shfl_xor_sync(0xffffffffu, usum, o);
     }
-    const long long Cw = (kCostStep * nsum + kCostUnit * usum) * NP;
+    const long long Cw = (kCostStep * nsum + kCostUnit * static_cast<long long>(usum)) * NP;
     const bool by_cost = div_ll(Cw, a.num_ctas) >= kCostStep + kCostUnit;
     const long long CT = by_cost ? kCostStep : 1, CS = by_cost ? kCostUnit : 0;
-    const long long Ctot = by_cost ? Cw : nsum * NP;
+    const long long Ctot = by_cost ? Cw : static_cast<long long>(nsum) * NP;
     const long long x0 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta) : 0;
     const long long x1 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta + 1) : 0;
     int seg = 0, g = 0;
@@ -348,34 +587,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       return x <= cb + CS ? 0 : div_ll(x - cb - CS + CT - 1, CT);
     };
     if (x0 < x1) {
-      // The request holding cost position x0, with the cost and units before it.
-      long long base = 0, ubase = 0;
+      // The request holding cost position x0, with the key steps and units
+      // (of one head pair) of the requests before it.
+      int sbase = 0, ubase32 = 0;
       int r = -1;
+#pragma unroll 1
       for (int rc = 0; rc < a.num_seqs && r < 0; rc += 32) {
         const PReq p = req_local(rc + lane);
-        const long long ct = (CT * req_steps(p) + CS * p.ntq) * NP;
-        const long long nu = static_cast<long long>(p.ntq) * NP;
-        long long it = ct, iu = nu;
-#pragma unroll
+        const int st = req_steps(p), nt = p.ntq;
+        int is = st, iu = nt;
+#pragma unroll 1
         for (int o = 1; o < 32; o <<= 1) {
-          const long long vt = __shfl_up_sync(0xffffffffu, it, o);
-          const long long vu = __shfl_up_sync(0xffffffffu, iu, o);
+          const int vs = __shfl_up_sync(0xffffffffu, is, o);
+          const int vu = __shfl_up_sync(0xffffffffu, iu, o);
           if (lane >= o) {
-            it += vt;
+            is += vs;
             iu += vu;
           }
         }
-        const unsigned hit = __ballot_sync(0xffffffffu, base + it > x0);
+        // cost up to the end of request rc + lane
+        const long long end = (CT * (sbase + is) + CS * (ubase32 + iu)) * NP;
+        const unsigned hit = __ballot_sync(0xffffffffu, end > x0);
         if (hit) {
           const int first = __ffs(hit) - 1;
-          base += __shfl_sync(0xffffffffu, it - ct, first);
-          ubase += __shfl_sync(0xffffffffu, iu - nu, first);
+          sbase += __shfl_sync(0xffffffffu, is - st, first);
+          ubase32 += __shfl_sync(0xffffffffu, iu - nt, first);
           r = rc + first;
         } else {
-          base += __shfl_sync(0xffffffffu, it, 31);
-          ubase += __shfl_sync(0xffffffffu, iu, 31);
+          sbase += __shfl_sync(0xffffffffu, is, 31);
+          ubase32 += __shfl_sync(0xffffffffu, iu, 31);
         }
       }
+      const long long base = (CT * sbase + CS * ubase32) * NP;
+      const long long ubase = static_cast<long long>(ubase32) * NP;
       // Unit (query tile u, head pair hp) of request r holding x0.
       PReq p = req_uniform(r);
       int u = 0, hp = 0, row0 = 0, rows = 0, kv_end = 0;
@@ -761,95 +1005,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const bool whole = sg.kind == kSegWhole;
       const int c0 = sg.c0, c1 = sg.c1;
       const int unit = sg.unit;
-      // Record of contributor c's piece: partial slot 1 for the unit's first
-      // CTA (its tail piece), else slot 0; O column-major ([D][128 rows]).
-      auto rec_of = [&](int c) -> size_t {
-        return ((static_cast<size_t>(c) * 2 + (c == c0 ? 1 : 0)) * 2 + b) * C::BM + i_row;
-      };
-      // Merge of the unit's pieces for this row, in contributor order c0 ..
-      // c1: contributor `own` (this CTA, when it merges without publishing)
-      // is taken from registers and TMEM, the others from their published
-      // partials.  The arithmetic is the same either way (the own piece
-      // enters as the same fp32 values it would have published), so the
-      // result does not depend on which contributor merges.  Loads are
-      // issued in batches, one round trip per batch.
-      auto merge = [&](int own) {
-        const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
-        auto ml_of = [&](int c) -> float2 {
-          return c == own ? make_float2(m_ref, l_run)
-                          : __ldcg(reinterpret_cast<const float2*>(a.part_ml + rec_of(c) * 2));
-        };
-        float M = kNegBigP;
-        for (int c = c0; c <= c1; c += 4) {
-          float2 ml4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) M = fmaxf(M, ml4[u].x);
-        }
-        float L = 0.f;
-        for (int c = c0; c <= c1; c += 4) {
-          float2 ml4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) ml4[u] = c + u <= c1 ? ml_of(c + u) : make_float2(kNegBigP, 0.f);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) L += ml4[u].y * fast_exp2(ml4[u].x - M);
-        }
-        const float invL = L > 0.f ? 1.f / L : 0.f;
-        __nv_bfloat16* dst =
-            a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + (b ? sg.h1 : sg.h0)) * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 16) {
-          float mine[16];  // this CTA's normalised piece (used only when own >= 0)
-          if (own >= 0) {
-            float ov[16];
-            tmem_ld16(tm_o + cc, ov);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) mine[e] = ov[e] * inv_own;
-          }
-          float acc[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-          for (int c = c0; c <= c1; c += 2) {
-            const bool two = c + 1 <= c1;
-            const bool m0 = c == own, m1 = two && c + 1 == own;
-            const size_t r0 = rec_of(c), r1 = rec_of(two ? c + 1 : c);
-            const float2 ml0 = ml_of(c);
-            const float2 ml1 = two ? ml_of(c + 1) : make_float2(kNegBigP, 0.f);
-            const float* p0 = a.part_o + (r0 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
-            const float* p1 = a.part_o + (r1 - i_row) * D + static_cast<size_t>(cc) * C::BM + i_row;
-            float v0[16], v1[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              v0[e] = m0 ? mine[e] : __ldcg(p0 + e * C::BM);
-              v1[e] = m1 ? mine[e] : (two ? __ldcg(p1 + e * C::BM) : 0.f);
-            }
-            const float w0 = ml0.y * fast_exp2(ml0.x - M);
-            const float w1 = ml1.y * fast_exp2(ml1.x - M);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc[e] = fmaf(w0, v0[e], fmaf(w1, v1[e], acc[e]));
-          }
-          if (i_row < sg.rows) {
-#pragma unroll
-            for (int e = 0; e < 16; e += 8)
-              *reinterpret_cast<uint4*>(dst + cc + e) = make_uint4(
-                  pack_bf16x2(acc[e] * invL, acc[e + 1] * invL), pack_bf16x2(acc[e + 2] * invL, acc[e + 3] * invL),
-                  pack_bf16x2(acc[e + 4] * invL, acc[e + 5] * invL), pack_bf16x2(acc[e + 6] * invL, acc[e + 7] * invL));
-          }
-        }
-      };
       bool direct = false;
       if (!whole) {
         // When every other piece of the unit has already counted, this one
-        // is the last: it merges straight from TMEM without publishing.
+        // is the last: it merges straight from TMEM without publishing.  The
+        // unit's first CTA holds its first steps at the end of its range,
+        // while every other piece starts its CTA's range (or fills it) and
+        // waits for nothing: that CTA alone waits for them, a bounded time
+        // (then it publishes like the others).
         if (warp == 2 && lane == 0) {
           int d = 0;
           if (unit < a.max_units) {
-            const unsigned long long cnt = ld_acquire_u64(a.counters + unit);
-            d = static_cast<unsigned>(cnt >> 32) == a.epoch &&
-                        static_cast<int>(cnt & 0xffffffffu) == c1 - c0
-                    ? 1
-                    : 0;
+            const bool patient = sg.kind == kSegTail;
+            const unsigned long long t0 = patient ? global_timer_ns() : 0ull;
+            while (true) {
+              const unsigned long long cnt = ld_acquire_u64(a.counters + unit);
+              if (static_cast<unsigned>(cnt >> 32) == a.epoch &&
+                  static_cast<int>(cnt & 0xffffffffu) == c1 - c0) {
+                d = 1;
+                break;
+              }
+              if (!patient || global_timer_ns() - t0 > kMergeWaitNs) break;
+              __nanosleep(64);
+            }
           } else {
             record_error(a.status, PA_DEV_WAIT_TIMEOUT, cta, 85);
           }
@@ -861,17 +1039,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       if (active) {
         if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
         tc_fence_after();
-        if (direct) {
-          merge(cta);
-        } else {
+        if (!direct) {
           const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-          const size_t rec = ((static_cast<size_t>(cta) * 2 + pslot) * 2 + b) * C::BM + i_row;
+          const size_t rec = (static_cast<size_t>(cta) * 2 + pslot) * 2 + b;
           __nv_bfloat16* dst_o =
               a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
-          // partial O is column-major: a warp's stores of one column are 128
-          // contiguous bytes
-          float* dst_p = a.part_o + (rec - i_row) * D + i_row;
-          if (!whole) *reinterpret_cast<float2*>(a.part_ml + rec * 2) = make_float2(m_ref, l_run);
+          float4* dst_p = reinterpret_cast<float4*>(a.part_o + rec * (D * 128)) + i_row;
+          if (!whole) *reinterpret_cast<float2*>(a.part_ml + (rec * 128 + i_row) * 2) = make_float2(m_ref, l_run);
           // O_b row, 64 columns per TMEM round trip.
 #pragma unroll
           for (int h = 0; h < D / 64; ++h) {
@@ -891,20 +1065,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
               }
             } else {
 #pragma unroll
-              for (int e = 0; e < 64; ++e) dst_p[(h * 64 + e) * C::BM] = __uint_as_float(orow[e]) * inv;
+              for (int e = 0; e < 64; e += 4)
+                dst_p[((h * 64 + e) / 4) * C::BM] =
+                    make_float4(__uint_as_float(orow[e]) * inv, __uint_as_float(orow[e + 1]) * inv,
+                                __uint_as_float(orow[e + 2]) * inv, __uint_as_float(orow[e + 3]) * inv);
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B::OFREE + b));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B::OFREE + b));
       }
       g += n;
+      // Merge: directly (this piece from TMEM), or, after publishing, when
+      // this CTA's count completes the unit; one call site for both.
+      int own = -2;  // -2: no merge here
       if (!whole && direct) {
-        if (!(ok = sync8())) break;  // direct_flag is read by every warp before it changes
-        if (warp == 2 && lane == 0) release_pair(a.counters + unit);
+        own = cta;
       } else if (!whole) {
-        // Publish the partial; the last of the unit's contributors merges.
         __threadfence();
         if (!(ok = sync8())) break;
         if (warp == 2 && lane == 0)
@@ -913,12 +1091,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                            ? 1
                            : 0;
         if (!(ok = sync8())) break;
-        if (*last_flag && active) {
-          __threadfence();
-          merge(-1);
+        if (*last_flag) own = -1;
+      }
+      if (own != -2 && active) {
+        __nv_bfloat16* dst =
+            a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
+        if (sg.j1 < sg.n_kv && c1 - c0 + 1 - (own >= 0 ? 1 : 0) <= C::MREM) {
+          // The range ends inside this unit, so this is the CTA's last
+          // segment: slot b's Q buffer and a K/V ring are free.
+          ok = merge_staged<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, (warp & 3) == 0 && lane == 0,
+                               m_ref, l_run, tm_o, q_s + b * C::QBYTES, b ? v_s : k_s,
+                               bar(B::MFULL + 5 * b), bar(B::MLFULL + b), bar(B::MSYNC + b), dst,
+                               i_row < sg.rows, a.status, cta);
+          if (!ok) break;
+        } else {
+          if (own == -1) __threadfence();
+          merge_row<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, m_ref, l_run, tm_o, dst,
+                       i_row < sg.rows);
         }
-        if (!(ok = sync8())) break;  // last_flag may change again after this
-        if (warp == 2 && lane == 0 && *last_flag) release_pair(a.counters + unit);
+      }
+      if (active && direct) {  // O_b was read by the merge
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B::OFREE + b));
+      }
+      if (!whole) {
+        if (!(ok = sync8())) break;  // direct_flag and last_flag are read by every warp before they change
+        if (warp == 2 && lane == 0 && own != -2) release_pair(a.counters + unit);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B::SEGFREE + slot));

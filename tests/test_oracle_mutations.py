@@ -66,6 +66,11 @@ MUTATIONS = [
      "* ORACLE_XSPLIT_X8 + d % ORACLE_XSPLIT_X;", ["xsplit8_writer"]),
     ("xsplit8_writer_skips_v_scale", "oracle_e4m3_encode(vf / v_scale);\n            }\n    }\n}\n\n/* Paged decode over e4m3 x-split",
      "oracle_e4m3_encode(vf);\n            }\n    }\n}\n\n/* Paged decode over e4m3 x-split", ["xsplit8_writer"]),
+    ("fp8_prefill_ignores_k_scale", "(oracle_e4m3_decode(k[x]) * k_scale)", "(oracle_e4m3_decode(k[x]))",
+     ["fp8_prefill"]),
+    ("fp8_prefill_causal_off_by_one", "context + 1 + i,", "context + i,", ["fp8_prefill_rows"]),
+    ("fp8_prefill_reads_kv_head_of_q_head", "h / group, num_kv_heads, head_dim, block_size, scale, k_scale,",
+     "h % num_kv_heads, num_kv_heads, head_dim, block_size, scale, k_scale,", ["fp8_prefill"]),
     ("xsplit8_decode_unnormalised", "const double pw = w[t] / total;", "const double pw = w[t];",
      ["xsplit8_decode"]),
 ]
@@ -93,6 +98,8 @@ PINS = {
         o, 4, 2, 64, [25, 12, 37, 20], 16),
     "xsplit8_writer": lambda o: pins.test_xsplit_fp8_writer_is_a_permutation_of_the_token_major_fp8_writer(
         o, 0.013, 7.7),
+    "fp8_prefill": lambda o: pins.test_prefill_fp8_equals_prefill_of_dequantized_cache(o, 0.5, 8.0),
+    "fp8_prefill_rows": lambda o: pins.test_prefill_fp8_equals_prefill_of_dequantized_cache(o, 1.0, 1.0),
     "xsplit8_decode": lambda o: pins.test_decode_xsplit_fp8_equals_decode_fp8_of_the_same_cache(
         o, 4, 2, 64, [25, 12, 37, 20], 16),
 }

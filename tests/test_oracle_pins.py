@@ -455,6 +455,51 @@ def test_decode_fp8_equals_decode_of_dequantized_cache(oracle, k_scale, v_scale)
     np.testing.assert_array_equal(got, ref)
 
 
+def _fp8_prefill_workload(seed):
+    """A mixed varlen batch (prefill chunks with context, decode rows, an
+    empty request) over random e4m3 caches without NaN codes."""
+    w = wl.build_workload("fp8mix", [90, 33, 140, 20, 5], [30, 1, 140, 1, 0], num_heads=6,
+                          num_kv_heads=2, head_dim=64, block_size=16, num_blocks=40, seed=seed)
+    t = wl.make_tensors(w)
+    rng = np.random.default_rng(seed)
+    kc8 = rng.integers(0, 256, size=t.key_cache.shape, dtype=np.uint8)
+    vc8 = rng.integers(0, 256, size=t.value_cache.shape, dtype=np.uint8)
+    for c in (kc8, vc8):
+        c[(c & 0x7F) == 0x7F] = 0x3C
+    return w, t, kc8, vc8
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 8.0), (2.0 ** -6, 2.0 ** 4)])
+def test_prefill_fp8_equals_prefill_of_dequantized_cache(oracle, k_scale, v_scale):
+    """Power-of-two scales keep every dequantized value a bf16 value: the FP8
+    varlen prefill must equal the (separately pinned) bf16 one exactly, rows
+    of every kind included."""
+    w, t, kc8, vc8 = _fp8_prefill_workload(63)
+    deq = lambda c, s: torch.from_numpy(oracle.e4m3_decode(c) * s).to(torch.bfloat16)
+    kb, vb = deq(kc8, k_scale), deq(vc8, v_scale)
+    assert torch.equal(vb.double(), torch.from_numpy(oracle.e4m3_decode(vc8) * v_scale))
+    q = t.q.view(torch.int16).numpy()
+    ref = oracle.prefill_varlen(q, kb.view(torch.int16).numpy(), vb.view(torch.int16).numpy(),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    got = oracle.prefill_varlen_fp8(q, kc8, vc8, w.query_start_loc, w.seq_lens, w.block_tables,
+                                    w.scale, k_scale, v_scale)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_prefill_fp8_decode_rows_equal_decode_fp8(oracle):
+    """A q_len == 1 row of the FP8 varlen prefill is the FP8 decode of its
+    request (non-power-of-two scales)."""
+    w, t, kc8, vc8 = _fp8_prefill_workload(64)
+    got = oracle.prefill_varlen_fp8(t.q.view(torch.int16).numpy(), kc8, vc8, w.query_start_loc,
+                                    w.seq_lens, w.block_tables, w.scale, 0.37, 1.9)
+    for r in (1, 3):
+        row = int(w.query_start_loc[r])
+        q1 = t.q[row:row + 1].view(torch.int16).numpy()
+        ref = oracle.decode_fp8(q1, kc8, vc8, w.block_tables[r:r + 1], w.seq_lens[r:r + 1],
+                                w.scale, 0.37, 1.9)
+        np.testing.assert_array_equal(got[row], ref[0])
+
+
 def test_reshape_and_cache_fp8_scatter(oracle):
     w, t, kc8, vc8 = _fp8_workload(62)
     rng = np.random.default_rng(62)
