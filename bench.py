@@ -476,12 +476,23 @@ def extra_mixed(pa, name, dev, flush, reps=20, cpu=True):
                                       w.scale, out=out_p, workspace=ws_p)
     s_pre = _time(pcall, flush, reps)
     flops = 4.0 * causal_pairs(w) * w.num_heads * w.head_dim
+    # The same prefill rows over an e4m3 copy of the cache (per-tensor scales amax / 448).
+    k_scale = float(t.key_cache.float().abs().max()) / 448.0
+    v_scale = float(t.value_cache.float().abs().max()) / 448.0
+    kc8 = (t.key_cache.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc8 = (t.value_cache.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    pcall8 = lambda: pa.prefill_varlen_fp8(q_p, kc8, vc8, qsl, sl_p, bt_p, mql, msl, w.scale,
+                                           k_scale, v_scale, out=out_p, workspace=ws_p)
+    s_pre8 = _time(pcall8, flush, reps)
+    del kc8, vc8
     res = {"us_per_step": round(s_step * 1e6, 2),
            "step": "append_tokens (all new tokens) + prefill_varlen",
            "step_kv_gbs": round(ab["step_bytes"] / s_step / 1e9, 2),
            "prefill_only_us": round(s_pre * 1e6, 2),
            "prefill_tflops": round(flops / s_pre / 1e12, 2),
            "prefill_gflop": round(flops / 1e9, 3),
+           "prefill_fp8_only_us": round(s_pre8 * 1e6, 2),
+           "prefill_fp8_tflops": round(flops / s_pre8 / 1e12, 2),
            "roofline": tensor_roofline("prefill_tile_kernel (pa_prefill_varlen, prefill rows "
                                        "alone)", flops, s_pre),
            "roofline_step": hbm_roofline("append_tokens + pa_prefill_varlen (whole step)",

@@ -442,6 +442,29 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
                             int32_t block_size, int32_t num_blocks, float scale,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pa_prefill_varlen_fp8 -- pa_prefill_varlen over FP8 (e4m3) caches written
+ * by pa_reshape_and_cache_fp8: key t contributes decoded(K_t) * k_scale and
+ * value t decoded(V_t) * v_scale ("vLLM 深度解析（二）", section 3.2,
+ * fp8::scaled_convert inside the K/V load; "分块预填充与混合批处理",
+ * section 11.6, for the varlen batch).  Same arguments, layouts (one byte
+ * per cache element), workspace (pa_prefill_workspace_size), ordering on
+ * `stream` and results as pa_prefill_varlen otherwise.  The prefill rows'
+ * products run on the tensor cores in f16: each landed e4m3 K/V step is
+ * converted exactly to f16 in shared memory, q is rounded to f16 (saturating
+ * at +-65504) and the softmax weights to f16; the decode rows run as in
+ * pa_decode_fp8.  k_scale and v_scale finite and > 0 (else PA_ERR_INVALID).
+ */
+pa_status pa_prefill_varlen_fp8(void* out, const void* q, const void* key_cache,
+                                const void* value_cache, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                                int32_t max_query_len, int32_t max_seq_len,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t num_blocks, float scale,
+                                float k_scale, float v_scale, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,7 +8,7 @@ the tests and the benchmark.
 from ._binding import (ABI_SYMBOLS, DEVICE_ERRORS, PAError, append_tokens, compute_slot_mapping, decode,
                        decode_fp8, decode_noalloc, decode_workspace_size, decode_xsplit,
                        decode_xsplit_fp8, device_status, library_path, load_library, map_to_kernel_blocks,
-                       new_workspace, prefill_varlen, prefill_workspace_size, reshape_and_cache,
+                       new_workspace, prefill_varlen, prefill_varlen_fp8, prefill_workspace_size, reshape_and_cache,
                        reshape_and_cache_fp8, reshape_and_cache_xsplit,
                        reshape_and_cache_xsplit_fp8)
 from .builder import build
@@ -16,5 +16,5 @@ from .builder import build
 __all__ = ["ABI_SYMBOLS", "DEVICE_ERRORS", "PAError", "append_tokens", "build", "compute_slot_mapping", "decode",
            "decode_fp8", "decode_noalloc", "decode_workspace_size", "decode_xsplit",
            "decode_xsplit_fp8", "device_status", "library_path", "load_library", "map_to_kernel_blocks",
-           "new_workspace", "prefill_varlen", "prefill_workspace_size", "reshape_and_cache",
+           "new_workspace", "prefill_varlen", "prefill_varlen_fp8", "prefill_workspace_size", "reshape_and_cache",
            "reshape_and_cache_fp8", "reshape_and_cache_xsplit", "reshape_and_cache_xsplit_fp8"]

@@ -27,7 +27,7 @@ ABI_SYMBOLS = ("pa_status_string", "pa_abi_version", "pa_reshape_and_cache",
                "pa_prefill_workspace_size", "pa_prefill_varlen", "pa_decode_noalloc",
                "pa_map_to_kernel_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
                "pa_reshape_and_cache_xsplit", "pa_decode_xsplit", "pa_append_tokens",
-               "pa_reshape_and_cache_xsplit_fp8", "pa_decode_xsplit_fp8")
+               "pa_reshape_and_cache_xsplit_fp8", "pa_decode_xsplit_fp8", "pa_prefill_varlen_fp8")
 
 
 class PAError(RuntimeError):
@@ -87,6 +87,10 @@ def _declare(lib):
     lib.pa_prefill_varlen.restype = ctypes.c_int
     lib.pa_prefill_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
                                       _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]
+    lib.pa_prefill_varlen_fp8.restype = ctypes.c_int
+    lib.pa_prefill_varlen_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
+                                          _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _vp,
+                                          _sz, _vp]
     return lib
 
 
@@ -466,6 +470,34 @@ def prefill_varlen(q, key_cache, value_cache, query_start_loc, seq_lens, block_t
         _ptr(seq_lens), S, tq, int(max_query_len), int(max_seq_len), _ptr(block_tables),
         block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), _ptr(workspace),
         workspace.numel(), _stream()))
+    return out
+
+
+def prefill_varlen_fp8(q, key_cache, value_cache, query_start_loc, seq_lens, block_tables,
+                       max_query_len, max_seq_len, scale, k_scale, v_scale, out=None, workspace=None):
+    """prefill_varlen over e4m3 caches (uint8 [nb, bs, Hkv, d]) with their scales."""
+    _contig("q", q, torch.bfloat16)
+    _contig("key_cache", key_cache, torch.uint8)
+    _contig("value_cache", value_cache, torch.uint8)
+    _contig("query_start_loc", query_start_loc, torch.int32)
+    _contig("seq_lens", seq_lens, torch.int32)
+    _contig("block_tables", block_tables, torch.int32)
+    tq, hq, d = q.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    if d2 != d or value_cache.shape != key_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    S = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    _contig("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = new_workspace(prefill_workspace_size(S, tq, hq, hkv, d, max_seq_len), q.device)
+    lib = load_library()
+    _check("pa_prefill_varlen_fp8", lib.pa_prefill_varlen_fp8(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(query_start_loc),
+        _ptr(seq_lens), S, tq, int(max_query_len), int(max_seq_len), _ptr(block_tables),
+        block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), float(k_scale), float(v_scale),
+        _ptr(workspace), workspace.numel(), _stream()))
     return out
 
 

@@ -178,20 +178,6 @@ __device__ __forceinline__ float key2f(int k) { return __int_as_float(k >= 0 ? k
 // ---- e4m3 caches: every e4m3 value is exact in f16, so the converter warps
 // turn the landed K and V bytes into f16 operands without rounding; q and
 // the weights are rounded to f16 (q saturates at +-65504).
-// Two e4m3 values (low byte first) as f16x2 (low half first).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
-  return h2;
-}
-// Two bf16 values (low half first) rounded to f16x2, saturated to +-65504.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  uint32_t h2;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
-      : "=r"(h2)
-      : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
-  return h2;
-}
 // 16-byte chunk c of token row t of a landed e4m3 block (16 rows of head_dim
 // bytes, 128-byte swizzle at head_dim 128, 64-byte at 64).
 template <int D>

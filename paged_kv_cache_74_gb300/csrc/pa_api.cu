@@ -84,9 +84,10 @@ int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group,
 // first for TMA: {head_dim, kv_heads, slots}); one box is one (block, kv
 // head) tile of 16 tokens x head_dim bytes, swizzled (128-byte rows at
 // head_dim 128, 64-byte rows at 64) so that the decode's ldmatrix reads of
-// 8 token rows are free of bank conflicts.
+// 8 token rows are free of bank conflicts; `plain`: rows unswizzled (the
+// prefill's converter reads whole rows).
 bool make_cache_map_e4m3(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
-                         int head_dim) {
+                         int head_dim, bool plain = false) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
@@ -99,7 +100,8 @@ bool make_cache_map_e4m3(CUtensorMap* map, const void* cache, int num_blocks, in
   std::memset(map, 0, sizeof(*map));
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             plain ? CU_TENSOR_MAP_SWIZZLE_NONE
+                   : (head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
              // A row is head_dim bytes: a larger L2 promotion would fetch the
              // next kv head's row too (a third more DRAM traffic, measured).
              head_dim == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
@@ -776,14 +778,19 @@ size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_
   return prefill_layout(dec, num_seqs, total_q, num_heads, num_kv_heads, head_dim).total;
 }
 
-pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
-                            const void* value_cache, const int32_t* query_start_loc,
-                            const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
-                            int32_t max_query_len, int32_t max_seq_len,
-                            const int32_t* block_tables, int32_t max_blocks_per_seq,
-                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                            int32_t block_size, int32_t num_blocks, float scale,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status prefill_varlen_impl(void* out, const void* q, const void* key_cache,
+                              const void* value_cache, const int32_t* query_start_loc,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                              int32_t max_query_len, int32_t max_seq_len,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks, float scale,
+                              void* workspace, size_t workspace_bytes, void* stream,
+                              const KvFormat& kv) {
   pa_status st = check_decode_args(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                                    seq_lens, num_seqs, max_seq_len, num_heads, num_kv_heads,
                                    head_dim, block_size, num_blocks, scale);
@@ -803,13 +810,15 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
   if (max_query_len > 1) {
     // Rows with q_len > 1: tensor-core tiles.
     CUtensorMap qmap, kmap, vmap;
-    if (!make_sw128_map(&qmap, q, head_dim, num_heads, total_q, head_dim * 2,
-                        static_cast<uint64_t>(num_heads) * head_dim * 2, 128) ||
-        !make_kv_group_map(&kmap, key_cache, num_blocks * (block_size / kBlockSize), num_kv_heads,
-                           head_dim) ||
-        !make_kv_group_map(&vmap, value_cache, num_blocks * (block_size / kBlockSize), num_kv_heads,
-                           head_dim))
-      return PA_ERR_CUDA;
+    const int tiles = num_blocks * (block_size / kBlockSize);
+    const bool maps_ok =
+        make_sw128_map(&qmap, q, head_dim, num_heads, total_q, head_dim * 2,
+                       static_cast<uint64_t>(num_heads) * head_dim * 2, 128) &&
+        (kv.e4m3 ? make_cache_map_e4m3(&kmap, key_cache, tiles, num_kv_heads, head_dim, true) &&
+                       make_cache_map_e4m3(&vmap, value_cache, tiles, num_kv_heads, head_dim, true)
+                 : make_kv_group_map(&kmap, key_cache, tiles, num_kv_heads, head_dim) &&
+                       make_kv_group_map(&vmap, value_cache, tiles, num_kv_heads, head_dim));
+    if (!maps_ok) return PA_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrefillArgs p;
     p.out = static_cast<__nv_bfloat16*>(out);
@@ -835,21 +844,64 @@ pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
     p.part_ml = reinterpret_cast<float*>(ws + PL.ml_offset);
     p.part_o = reinterpret_cast<float*>(ws + PL.o_offset);
     p.epoch = next_epoch();
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = scale * kv.k_scale * 1.4426950408889634f;
+    p.o_scale = kv.v_scale;
     // Both kernels go on the caller's stream.  The tile kernel lets the
     // decode launch start once the kernels before this call are complete;
     // the decode CTAs then take the SMs the tiles leave free, and the decode
     // launch completes only after the tile kernel.
-    if (launch_prefill(p, qmap, kmap, vmap, head_dim, cs) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_prefill(p, qmap, kmap, vmap, head_dim, kv.e4m3, cs) != cudaSuccess)
+      return PA_ERR_CUDA;
     return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                               seq_lens, query_start_loc, num_seqs, total_q, max_seq_len,
                               num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, L,
-                              workspace, cs, KvFormat(), true);
+                              workspace, cs, kv, true);
   }
   // Only decode rows: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                             seq_lens, query_start_loc, num_seqs, total_q, max_seq_len, num_heads,
-                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace, cs);
+                            num_kv_heads, head_dim, num_blocks, block_size, scale, L, workspace, cs,
+                            kv);
 }
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
+                            const void* value_cache, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                            int32_t max_query_len, int32_t max_seq_len,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_varlen_impl(out, q, key_cache, value_cache, query_start_loc, seq_lens, num_seqs,
+                             total_q, max_query_len, max_seq_len, block_tables, max_blocks_per_seq,
+                             num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             workspace, workspace_bytes, stream, KvFormat());
+}
+
+pa_status pa_prefill_varlen_fp8(void* out, const void* q, const void* key_cache,
+                                const void* value_cache, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, int32_t num_seqs, int32_t total_q,
+                                int32_t max_query_len, int32_t max_seq_len,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t num_blocks, float scale,
+                                float k_scale, float v_scale, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID;
+  KvFormat kv;
+  kv.e4m3 = true;
+  kv.k_scale = k_scale;
+  kv.v_scale = v_scale;
+  return prefill_varlen_impl(out, q, key_cache, value_cache, query_start_loc, seq_lens, num_seqs,
+                             total_q, max_query_len, max_seq_len, block_tables, max_blocks_per_seq,
+                             num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             workspace, workspace_bytes, stream, kv);
+}
+
 
 }  // extern "C"

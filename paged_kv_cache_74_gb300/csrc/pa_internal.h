@@ -120,7 +120,7 @@ struct PrefillArgs {
   int32_t* status;                  // device status record (may be null)
   unsigned long long* counters;     // [max_units] (epoch << 32 | contributions)
   float* part_ml;                   // [num_ctas][2][2 heads][128 rows][2]  (m in log2 units, l)
-  float* part_o;                    // [num_ctas][2][2 heads][D][128 rows]  normalised partial O
+  float* part_o;                    // [num_ctas][2][2 heads][D / 4][128 rows][4]  normalised partial O
   int max_blocks_per_seq;
   int num_seqs;
   int num_heads;
@@ -135,12 +135,13 @@ struct PrefillArgs {
   int num_ctas;                     // persistent grid (one CTA per SM)
   long long max_units;              // size of `counters`
   unsigned epoch;                   // distinct per call (never 0)
-  float scale_log2;                 // softmax scale * log2(e)
+  float scale_log2;                 // softmax scale (* k_scale for e4m3) * log2(e)
+  float o_scale;                    // 1, or v_scale for e4m3
 };
 // Bytes of the prefill partial records (part_ml and part_o) for num_ctas CTAs.
 size_t prefill_partials_bytes(int num_ctas, int head_dim);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
+                           const CUtensorMap& vmap, int head_dim, bool kv8, cudaStream_t stream);
 
 // Cache writes (cache_write.cu).
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride,

@@ -418,6 +418,28 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Two e4m3 values (low byte first) as f16x2 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+  return h2;
+}
+// Two bf16 values (low half first) rounded to f16x2, saturated to +-65504.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+      : "=r"(h2)
+      : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+  return h2;
+}
+
+// Two floats rounded to f16 (nearest even), packed low / high.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(hi), "f"(lo));
+  return h2;
+}
+
 // Hardware base-2 exponential (PTX ex2.approx); ex2(-inf) = +0.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

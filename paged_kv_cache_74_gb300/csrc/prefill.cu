@@ -97,7 +97,11 @@ struct PrefillCfg {
   static constexpr int REQ_CACHE = 256;             // requests whose lengths are cached
   static constexpr int OFF_REQ = OFF_SEG + SEGS * SEG_INTS * 4;  // [3][REQ_CACHE] ints
   static constexpr int OFF_BAR = OFF_REQ + 3 * REQ_CACHE * 4;
-  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2 + 14;
+  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2 + 14 + 2 * NST + 2;
+  // e4m3 cache: a step's K (or V) bytes land as 16-token blocks of head_dim
+  // bytes in the upper half of the f16 stage they are converted into.
+  static constexpr int RAW_BLOCK = 16 * D;
+  static constexpr int RAW_OFF = TBYTES / 2;
   // Merge staging at a CTA's last segment: slot b's Q buffer and one K/V
   // ring (K for slot 0, V for slot 1) are free once O_b is final; they are
   // cut into 16 KB buffers (32 columns of one partial record), the last one
@@ -137,7 +141,10 @@ struct PBars {
   static constexpr int MFULL = DRAIN + 1;        // [2][5] staged partial O chunk landed
   static constexpr int MLFULL = MFULL + 10;      // [2] staged (m, l) records landed
   static constexpr int MSYNC = MLFULL + 2;       // [2] the 4 warps of a slot
-  static constexpr int COUNT = MSYNC + 2;
+  static constexpr int KRAW = MSYNC + 2;         // [NST] e4m3 K step landed (then converted)
+  static constexpr int VRAW = KRAW + NST;        // [NST] e4m3 V step landed
+  static constexpr int QCONV = VRAW + NST;       // [2] Q of a slot converted to f16 (4 warps)
+  static constexpr int COUNT = QCONV + 2;
 };
 
 // A segment: steps [j0, j1) of one unit inside this CTA's range.
@@ -206,6 +213,47 @@ __device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
   }
 }
 
+// An e4m3 step (nb landed 16-token blocks of head_dim bytes at RAW_OFF of
+// the stage) turned in place into the f16 operand layout the bf16 copies
+// produce ([8-key group][head_dim half][8 keys][128 B], 128-byte swizzle).
+// e4m3 values are exact in f16.  Run by one warp.  The 8-key groups go in
+// order: group g's output bytes [g GSTRIDE, (g + 1) GSTRIDE) only cover raw
+// rows of groups up to g itself (raw row t sits at RAW_OFF + t D, with
+// GSTRIDE = 16 D and RAW_OFF = 128 D: the rows below (g + 1) GSTRIDE are
+// t < 16 g - 112 <= 8 g + 8 for g < 16), and each group is read whole
+// before it is written.
+template <int D>
+__device__ __forceinline__ void convert_e4m3_step(uint32_t stage, int nb, int lane) {
+  using C = PrefillCfg<D>;
+  constexpr int CPR = D / 16;     // 16-byte raw chunks per key row
+  constexpr int KPI = 32 / CPR;   // key rows per warp-wide load
+  constexpr int NLD = 8 / KPI;    // loads per lane per 8-key group
+  static_assert(C::GSTRIDE == 16 * D && C::RAW_OFF == 128 * D, "in-place conversion order");
+  const int c = lane % CPR;       // raw chunk: dims 16c .. 16c + 15
+  const uint32_t half = (c / 4) * 1024;
+  const int cc = 2 * (c % 4);     // its two f16 chunks in the half
+#pragma unroll 1
+  for (int g8 = 0; g8 < 2 * nb; ++g8) {
+    uint4 w[NLD];
+#pragma unroll
+    for (int k = 0; k < NLD; ++k)
+      w[k] = ld_shared_v4(stage + C::RAW_OFF + (g8 * 8 + lane / CPR + KPI * k) * D + c * 16);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < NLD; ++k) {
+      const int r = lane / CPR + KPI * k;
+      const uint32_t row = stage + g8 * C::GSTRIDE + half + r * 128;
+      st_shared_v4(row + ((cc ^ r) * 16),
+                   make_uint4(e4m3x2_to_f16x2(w[k].x), e4m3x2_to_f16x2(w[k].x >> 16),
+                              e4m3x2_to_f16x2(w[k].y), e4m3x2_to_f16x2(w[k].y >> 16)));
+      st_shared_v4(row + (((cc + 1) ^ r) * 16),
+                   make_uint4(e4m3x2_to_f16x2(w[k].z), e4m3x2_to_f16x2(w[k].z >> 16),
+                              e4m3x2_to_f16x2(w[k].w), e4m3x2_to_f16x2(w[k].w >> 16)));
+    }
+    __syncwarp();
+  }
+}
+
 // Partial records of the merge ("vLLM 深度解析（二）：PagedAttention 核心机制",
 // sections 3.2.7 and 3.3: m = max m_j, L = sum l_j e^{m_j - m},
 // O = sum O_j l_j e^{m_j - m} / L).  Record (cta, piece, slot) holds, for each
@@ -222,7 +270,7 @@ __device__ __forceinline__ size_t prec(int c, int c0, int b) {
 // in contributor order c0 .. c1, from the published partials.  Contributor
 // `own` (this CTA, merging without publishing) is taken from registers
 // (m_ref, l_run) and TMEM (its unnormalised O at tm_o) instead, as the same
-// fp32 values it would have published, so the result does not depend on
+// fp32 values it would have published (O_j o_scale / l_j), so the result does not depend on
 // which contributor merges; weights and sums are taken in the same order as
 // in merge_staged().  Out of line: its registers stay apart from the softmax
 // loop's.  Called by every lane of the warp (the TMEM loads are warp-wide).
@@ -230,8 +278,8 @@ template <int D>
 __device__ __noinline__ void merge_row(const float* __restrict__ part_ml,
                                        const float* __restrict__ part_o, int c0, int c1, int own,
                                        int b, int i_row, float m_ref, float l_run, uint32_t tm_o,
-                                       __nv_bfloat16* dst, bool write) {
-  const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
+                                       float o_scale, __nv_bfloat16* dst, bool write) {
+  const float inv_own = l_run > 0.f ? o_scale / l_run : 0.f;
   auto ml_of = [&](int c) -> float2 {
     return c == own ? make_float2(m_ref, l_run)
                     : __ldcg(reinterpret_cast<const float2*>(part_ml + (prec(c, c0, b) * 128 + i_row) * 2));
@@ -323,7 +371,8 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
                                           int b, int i_row, bool issuer, float m_ref, float l_run,
                                           uint32_t tm_o, uint32_t area_q, uint32_t area_r,
                                           uint32_t bar_full, uint32_t bar_ml, uint32_t bar_sync,
-                                          __nv_bfloat16* dst, bool write, int32_t* status, int cta) {
+                                          float o_scale, __nv_bfloat16* dst, bool write,
+                                          int32_t* status, int cta) {
   using C = PrefillCfg<D>;
   constexpr int NCH = D / 32;  // 32-column chunks of a record
   const int lane = threadIdx.x & 31;
@@ -378,7 +427,7 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
       if (c != own) ++k;
     }
     const float invL = L > 0.f ? 1.f / L : 0.f;
-    const float inv_own = l_run > 0.f ? 1.f / l_run : 0.f;
+    const float inv_own = l_run > 0.f ? o_scale / l_run : 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < NCH && ok; ++ch) {
       float acc[32];
@@ -437,12 +486,18 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
   return ok;
 }
 
-template <int D>
+// KV8: e4m3 K/V cache (k_scale folded into scale_log2, v_scale = o_scale):
+// each landed step is converted in place to f16 by its producer warp, each
+// slot's Q is converted to f16 (saturating) by the slot's softmax warps, the
+// weights are rounded to f16, and the MMAs are f16 x f16 -> fp32.
+template <int D, bool KV8>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   using C = PrefillCfg<D>;
   using B = PBars<C::NST, C::SEGS>;
+  constexpr uint32_t IDESC_S = KV8 ? idesc_f16_f32(C::BM, C::BN, 0) : C::IDESC_S;
+  constexpr uint32_t IDESC_O = KV8 ? idesc_f16_f32(C::BM, D, 1) : C::IDESC_O;
   const int cta = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -472,6 +527,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       if (k >= B::SEGFREE && k < B::SEGFREE + C::SEGS) count = 10;  // MMA, 8 softmax, V producer
       if (k == B::SYNC) count = 8;
       if (k >= B::MSYNC && k < B::MSYNC + 2) count = 4;
+      if (k >= B::QCONV && k < B::QCONV + 2) count = 4;
       mbar_init(bar(k), count);
     }
     *fail_flag = 0;
@@ -699,18 +755,49 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // K of every step: lane L < 8 copies block L of the step.
         const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
         int rowc = tile_rows(r, j0 * 8, nblk, true);
-        for (int jj = j0; jj < j1 && ok; ++jj) {
-          const int st = g % C::NST;
-          if (g >= C::NST && !(ok = lane0_wait(bar(B::KFREE + st), ((g / C::NST) - 1) & 1, 62))) break;
-          const int nb = min(8, nblk - jj * 8);
-          if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + st), nb * C::BLOCK_BYTES);
-          __syncwarp();
-          if (lane < nb)
-            tma_load_5d(k_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &kmap, bar(B::KFULL + st), 0, 0,
-                        0, rowc / 8, kvh, policy);
-          ++g;
-          if (lane == 0) *n_k_issued = g;
-          if (jj + 1 < j1) rowc = tile_rows(r, (jj + 1) * 8, nblk, true);
+        if constexpr (KV8) {
+          // e4m3: the copy of the segment's next step is issued before this
+          // step is waited for and converted (two copies in flight).
+          auto issue_raw = [&](int jj, int gg, int row) -> bool {
+            const int st = gg % C::NST;
+            if (gg >= C::NST && !lane0_wait(bar(B::KFREE + st), ((gg / C::NST) - 1) & 1, 62)) return false;
+            const int nb = min(8, nblk - jj * 8);
+            if (lane == 0) mbar_arrive_expect_tx(bar(B::KRAW + st), nb * C::RAW_BLOCK);
+            __syncwarp();
+            if (lane < nb)
+              tma_load_3d(k_s + st * C::TBYTES + C::RAW_OFF + lane * C::RAW_BLOCK, &kmap,
+                          bar(B::KRAW + st), 0, kvh, row, policy);
+            if (lane == 0) *n_k_issued = gg + 1;
+            return true;
+          };
+          if (j0 < j1) ok = issue_raw(j0, g, rowc);
+          for (int jj = j0; jj < j1 && ok; ++jj) {
+            if (jj + 1 < j1) {
+              rowc = tile_rows(r, (jj + 1) * 8, nblk, true);
+              if (!(ok = issue_raw(jj + 1, g + 1, rowc))) break;
+            }
+            const int st = g % C::NST;
+            if (!(ok = lane0_wait(bar(B::KRAW + st), (g / C::NST) & 1, 65))) break;
+            convert_e4m3_step<D>(k_s + st * C::TBYTES, min(8, nblk - jj * 8), lane);
+            fence_proxy_async_smem();  // read by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B::KFULL + st));
+            ++g;
+          }
+        } else {
+          for (int jj = j0; jj < j1 && ok; ++jj) {
+            const int st = g % C::NST;
+            if (g >= C::NST && !(ok = lane0_wait(bar(B::KFREE + st), ((g / C::NST) - 1) & 1, 62))) break;
+            const int nb = min(8, nblk - jj * 8);
+            if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + st), nb * C::BLOCK_BYTES);
+            __syncwarp();
+            if (lane < nb)
+              tma_load_5d(k_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &kmap, bar(B::KFULL + st), 0,
+                          0, 0, rowc / 8, kvh, policy);
+            ++g;
+            if (lane == 0) *n_k_issued = g;
+            if (jj + 1 < j1) rowc = tile_rows(r, (jj + 1) * 8, nblk, true);
+          }
         }
         ++seg;
         if (j1 < n_u) break;  // the range ends inside this unit
@@ -741,18 +828,47 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const PSeg sg = segs[slot];
       if (sg.kind == kSegEnd) break;
       const int nblk = (sg.kv_end + kBlockSize - 1) / kBlockSize;
-      for (int jj = sg.j0; jj < sg.j1 && ok; ++jj) {
-        const int st = g % C::NST;
-        const int rowc = tile_rows(sg.r, jj * 8, nblk, false);
-        if (g >= C::NST && !(ok = warp_wait(bar(B::VFREE + st), ((g / C::NST) - 1) & 1, 64))) break;
-        const int nb = min(8, nblk - jj * 8);
-        if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + st), nb * C::BLOCK_BYTES);
-        __syncwarp();
-        if (lane < nb)
-          tma_load_5d(v_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &vmap, bar(B::VFULL + st), 0, 0, 0,
-                      rowc / 8, sg.kvh, policy);
-        ++g;
-        if (lane == 0) *n_v_issued = g;
+      if constexpr (KV8) {
+        // As for K: the segment's next step is in flight while this one is
+        // converted.
+        auto issue_raw = [&](int jj, int gg) -> bool {
+          const int st = gg % C::NST;
+          const int rowc = tile_rows(sg.r, jj * 8, nblk, false);
+          if (gg >= C::NST && !warp_wait(bar(B::VFREE + st), ((gg / C::NST) - 1) & 1, 64)) return false;
+          const int nb = min(8, nblk - jj * 8);
+          if (lane == 0) mbar_arrive_expect_tx(bar(B::VRAW + st), nb * C::RAW_BLOCK);
+          __syncwarp();
+          if (lane < nb)
+            tma_load_3d(v_s + st * C::TBYTES + C::RAW_OFF + lane * C::RAW_BLOCK, &vmap,
+                        bar(B::VRAW + st), 0, sg.kvh, rowc, policy);
+          if (lane == 0) *n_v_issued = gg + 1;
+          return true;
+        };
+        if (sg.j0 < sg.j1) ok = issue_raw(sg.j0, g);
+        for (int jj = sg.j0; jj < sg.j1 && ok; ++jj) {
+          if (jj + 1 < sg.j1 && !(ok = issue_raw(jj + 1, g + 1))) break;
+          const int st = g % C::NST;
+          if (!(ok = warp_wait(bar(B::VRAW + st), (g / C::NST) & 1, 66))) break;
+          convert_e4m3_step<D>(v_s + st * C::TBYTES, min(8, nblk - jj * 8), lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B::VFULL + st));
+          ++g;
+        }
+      } else {
+        for (int jj = sg.j0; jj < sg.j1 && ok; ++jj) {
+          const int st = g % C::NST;
+          const int rowc = tile_rows(sg.r, jj * 8, nblk, false);
+          if (g >= C::NST && !(ok = warp_wait(bar(B::VFREE + st), ((g / C::NST) - 1) & 1, 64))) break;
+          const int nb = min(8, nblk - jj * 8);
+          if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + st), nb * C::BLOCK_BYTES);
+          __syncwarp();
+          if (lane < nb)
+            tma_load_5d(v_s + st * C::TBYTES + lane * C::BLOCK_BYTES, &vmap, bar(B::VFULL + st), 0, 0,
+                        0, rowc / 8, sg.kvh, policy);
+          ++g;
+          if (lane == 0) *n_v_issued = g;
+        }
       }
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(bar(B::SEGFREE + slot));
@@ -780,7 +896,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           const uint32_t qoff = (ks / 4) * C::CHUNK + (ks % 4) * 32;
           const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
           umma_bf16(tmem + b * C::BN, sdesc_sw128(qb + qoff, 16, 1024),
-                    sdesc_sw128(kst + koff, 16, C::GSTRIDE), C::IDESC_S, ks > 0);
+                    sdesc_sw128(kst + koff, 16, C::GSTRIDE), IDESC_S, ks > 0);
         }
       };
       // O_b += P_b V of the V stage st (P_b: bf16 in TMEM columns 128 b ..).
@@ -789,7 +905,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int ks = 0; ks < C::BN / 16; ++ks)
           umma_tmem_a(tmem + 256 + b * D, tmem + b * C::BN + ks * 8,
                       sdesc_sw128(v_s + st * C::TBYTES + ks * C::BLOCK_BYTES, 1024, C::GSTRIDE),
-                      C::IDESC_O, (acc || ks > 0) ? 1u : 0u);
+                      IDESC_O, (acc || ks > 0) ? 1u : 0u);
       };
       for (int seg = 0; ok; ++seg) {
         const int slot = seg % C::SEGS;
@@ -798,7 +914,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (sg.kind == kSegEnd) break;
         const int n = sg.j1 - sg.j0;
         const int nsl = sg.h1 >= 0 ? 2 : 1;
-        for (int b = 0; b < nsl && ok; ++b) ok = wait(B::QFULL + b, qc[b]++ & 1, 71);
+        for (int b = 0; b < nsl && ok; ++b) ok = wait((KV8 ? B::QCONV : B::QFULL) + b, qc[b]++ & 1, 71);
         ok = ok && wait(B::KFULL + g % C::NST, (g / C::NST) & 1, 72);
         if (!ok) break;
         tc_fence_after();
@@ -854,7 +970,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint32_t tm_o = lane_base + 256 + b * D;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    int sc = 0, oc = 0, g = 0;
+    int sc = 0, oc = 0, g = 0, qn = 0;
     uint32_t sync_phase = 0;
     auto all_wait = [&](int k, uint32_t parity, int where) -> bool {
       if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
@@ -880,6 +996,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const int head = b ? sg.h1 : sg.h0;
       const int pslot = sg.kind == kSegTail ? 1 : 0;
       float m_ref = kNegBigP, l_run = 0.f;
+      if (KV8 && active) {
+        // This slot's Q to f16 in place (same layout), before its first S MMA.
+        if (!(ok = all_wait(B::QFULL + b, qn++ & 1, 79))) break;
+        const uint32_t qb = q_s + b * C::QBYTES;
+        for (int i = (warp & 3) * 32 + lane; i < C::QBYTES / 16; i += 128) {
+          const uint4 w = ld_shared_v4(qb + i * 16);
+          st_shared_v4(qb + i * 16, make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y),
+                                               bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w)));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B::QCONV + b));
+      }
       if (active) {
         const int limit = min(sg.ctx + sg.row0 + i_row, sg.kv_end - 1);  // last key this row sees
         for (int k = 0; k < n && ok; ++k) {
@@ -911,7 +1040,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                         make_float2(sl2, sl2), make_float2(-m, -m));
             const float p0 = fast_exp2(x.x);  // 0 for the masked keys
             const float p1 = fast_exp2(x.y);
-            pk[e / 2] = pack_bf16x2(p0, p1);
+            pk[e / 2] = KV8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             ps4[(e / 2) % 4] = __fadd2_rn(ps4[(e / 2) % 4], make_float2(p0, p1));
           };
           bool rescale = true;
@@ -1040,7 +1169,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (!(ok = all_wait(B::OFULL + b, oc++ & 1, 84))) break;
         tc_fence_after();
         if (!direct) {
-          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+          const float inv = l_run > 0.f ? a.o_scale / l_run : 0.f;
           const size_t rec = (static_cast<size_t>(cta) * 2 + pslot) * 2 + b;
           __nv_bfloat16* dst_o =
               a.out + (static_cast<size_t>(sg.q0 + sg.row0 + i_row) * a.num_heads + head) * D;
@@ -1101,13 +1230,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           // segment: slot b's Q buffer and a K/V ring are free.
           ok = merge_staged<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, (warp & 3) == 0 && lane == 0,
                                m_ref, l_run, tm_o, q_s + b * C::QBYTES, b ? v_s : k_s,
-                               bar(B::MFULL + 5 * b), bar(B::MLFULL + b), bar(B::MSYNC + b), dst,
-                               i_row < sg.rows, a.status, cta);
+                               bar(B::MFULL + 5 * b), bar(B::MLFULL + b), bar(B::MSYNC + b),
+                               a.o_scale, dst, i_row < sg.rows, a.status, cta);
           if (!ok) break;
         } else {
           if (own == -1) __threadfence();
-          merge_row<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, m_ref, l_run, tm_o, dst,
-                       i_row < sg.rows);
+          merge_row<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, m_ref, l_run, tm_o, a.o_scale,
+                       dst, i_row < sg.rows);
         }
       }
       if (active && direct) {  // O_b was read by the merge
@@ -1130,10 +1259,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // Let copies still in flight land before TMEM is released and the CTA
     // leaves (bounded).
     const int nk = *n_k_issued, nv = *n_v_issued;
+    const int kb = KV8 ? B::KRAW : B::KFULL, vb = KV8 ? B::VRAW : B::VFULL;
     for (int i = max(0, nk - C::NST); i < nk; ++i)
-      (void)mbar_wait(bar(B::KFULL + i % C::NST), (i / C::NST) & 1);
+      (void)mbar_wait(bar(kb + i % C::NST), (i / C::NST) & 1);
     for (int i = max(0, nv - C::NST); i < nv; ++i)
-      (void)mbar_wait(bar(B::VFULL + i % C::NST), (i / C::NST) & 1);
+      (void)mbar_wait(bar(vb + i % C::NST), (i / C::NST) & 1);
     for (int b = 0; b < 2; ++b)
       if (n_q_issued[b] > 0) (void)mbar_wait(bar(B::QFULL + b), (n_q_issued[b] - 1) & 1);
   }
@@ -1145,7 +1275,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_prefill_impl(const PrefillArgs& a, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const CUtensorMap& vmap,
                                 cudaStream_t stream) {
@@ -1154,13 +1284,13 @@ cudaError_t launch_prefill_impl(const PrefillArgs& a, const CUtensorMap& qmap,
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    const cudaError_t err = cudaFuncSetAttribute(prefill_kernel<D>,
+    const cudaError_t err = cudaFuncSetAttribute(prefill_kernel<D, KV8>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  return launch_overlapped(prefill_kernel<D>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM, stream,
-                           qmap, kmap, vmap, a);
+  return launch_overlapped(prefill_kernel<D, KV8>, dim3(a.num_ctas), dim3(C::THREADS), C::SMEM,
+                           stream, qmap, kmap, vmap, a);
 }
 
 }  // namespace
@@ -1170,9 +1300,13 @@ size_t prefill_partials_bytes(int num_ctas, int head_dim) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream) {
-  if (head_dim == 128) return launch_prefill_impl<128>(a, qmap, kmap, vmap, stream);
-  if (head_dim == 64) return launch_prefill_impl<64>(a, qmap, kmap, vmap, stream);
+                           const CUtensorMap& vmap, int head_dim, bool kv8, cudaStream_t stream) {
+  if (head_dim == 128)
+    return kv8 ? launch_prefill_impl<128, true>(a, qmap, kmap, vmap, stream)
+               : launch_prefill_impl<128, false>(a, qmap, kmap, vmap, stream);
+  if (head_dim == 64)
+    return kv8 ? launch_prefill_impl<64, true>(a, qmap, kmap, vmap, stream)
+               : launch_prefill_impl<64, false>(a, qmap, kmap, vmap, stream);
   return cudaErrorInvalidValue;
 }
 

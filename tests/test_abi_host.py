@@ -180,6 +180,28 @@ def test_reshape_and_cache_fp8_rejects_bad_scales(lib):
                                         32, 1.0, 1.0, vp(0), vp(0)) == 0
 
 
+def prefill_fp8_call(lib, **kw):
+    args = dict(out=A, q=A, kc=A, vc=A, qsl=A, sl=A, ns=2, tq=10, mql=9, msl=64, bt=A, mb=4, hq=8,
+                hkv=2, d=128, bs=16, nb=32, scale=0.125, ks=1.0, vs=1.0, ws=A, wsb=1 << 30)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.pa_prefill_varlen_fp8(vp(args["out"]), vp(args["q"]), vp(args["kc"]), vp(args["vc"]),
+                                     vp(args["qsl"]), vp(args["sl"]), args["ns"], args["tq"],
+                                     args["mql"], args["msl"], vp(args["bt"]), args["mb"],
+                                     args["hq"], args["hkv"], args["d"], args["bs"], args["nb"],
+                                     args["scale"], args["ks"], args["vs"], vp(args["ws"]),
+                                     args["wsb"], vp(0))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ks=0.0), 1), (dict(vs=-1.0), 1), (dict(ks=float("inf")), 1), (dict(vs=float("nan")), 1),
+    (dict(qsl=0), 1), (dict(mql=65), 1), (dict(scale=0.0), 1), (dict(d=96), 2), (dict(ws=0), 3),
+])
+def test_prefill_fp8_rejects_invalid_arguments(lib, kw, expect):
+    """Checked on the host before any launch (no GPU needed)."""
+    assert prefill_fp8_call(lib, **kw) == expect
+
+
 def decode_xsplit_call(lib, **kw):
     args = dict(out=A, q=A, kc=A, vc=A, bt=A, mb=4, sl=A, ns=2, msl=64, hq=8, hkv=2, d=128, bs=16,
                 nb=32, scale=0.125, pt=0, ws=A, wsb=1 << 20)

@@ -270,3 +270,121 @@ def test_decode_xsplit_fp8_full_size_8b(cuda_lib, oracle):
                                    w.block_tables[rows], w.seq_lens[rows], w.scale, 2.0 ** -5,
                                    2.0 ** -5)
     assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, what="x-split fp8 8B batch")
+
+
+# ---- pa_prefill_varlen_fp8: the prefill tiles over e4m3 caches (each landed
+# step converted to f16 in shared memory) plus the FP8 decode rows.
+
+def run_prefill_fp8(pa, w, t, kc, vc, k_scale, v_scale):
+    ws = pa.new_workspace(pa.prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads,
+                                                    w.num_kv_heads, w.head_dim, w.max_seq_len),
+                          "cuda")
+    out = pa.prefill_varlen_fp8(t.q, kc, vc, t.query_start_loc, t.seq_lens, t.block_tables,
+                                w.max_query_len, w.max_seq_len, w.scale, k_scale, v_scale,
+                                workspace=ws)
+    return out, ws
+
+
+def prefill_fp8_ref(oracle, w, t, kc, vc, k_scale, v_scale):
+    return oracle.prefill_varlen_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(),
+                                     w.query_start_loc, w.seq_lens, w.block_tables, w.scale,
+                                     k_scale, v_scale)
+
+
+FP8_PREFILL_MIXES = [
+    # (seed, num_seqs, max_len, max_q_len, head_dim, q heads, kv heads, block size)
+    (351, 5, 300, 200, 128, 8, 2, 16),
+    (352, 6, 700, 260, 128, 32, 8, 16),
+    (353, 4, 150, 150, 64, 4, 2, 16),
+    (354, 5, 520, 300, 128, 16, 16, 32),
+    (355, 3, 400, 400, 128, 8, 1, 64),
+    (356, 5, 290, 130, 64, 16, 2, 16),
+    (357, 4, 400, 200, 128, 64, 8, 16),
+]
+
+
+@pytest.mark.parametrize("seed,ns,max_len,max_q,d,hq,hkv,B", FP8_PREFILL_MIXES)
+def test_prefill_fp8_random_mixes(cuda_lib, oracle, seed, ns, max_len, max_q, d, hq, hkv, B):
+    """Random prefill chunks with context next to decode rows, NaN codes in
+    every slot outside a request's context, scales that are not powers of two."""
+    pa = cuda_lib
+    w = wl.random_workload(seed, num_seqs=ns, max_len=max_len, num_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, max_q_len=max_q, prefill_fraction=0.7, block_size=B)
+    assert w.max_query_len > 1
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 0.037, 0.0213
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, seed)
+    out, ws = run_prefill_fp8(pa, w, t, kc, vc, k_scale, v_scale)
+    assert pa.device_status(ws)[0] == 0
+    assert torch.isfinite(out.float()).all()
+    ref = prefill_fp8_ref(oracle, w, t, kc, vc, k_scale, v_scale)
+    assert_close_to_oracle(out, ref, what=f"fp8 prefill mix {seed}")
+
+
+@pytest.mark.parametrize("q_len,ctx,d", [(2, 0, 128), (2, 37, 64), (127, 0, 128), (128, 0, 64),
+                                         (129, 5, 128), (256, 16, 128), (300, 1000, 64),
+                                         (17, 2047, 128)])
+def test_prefill_fp8_tile_edges(cuda_lib, oracle, q_len, ctx, d):
+    """Chunks at and around the 128-row tile and 16-token block edges (steps
+    with fewer than 8 landed blocks), next to a decode row."""
+    pa = cuda_lib
+    lens = [ctx + q_len, 77]
+    w = wl.build_workload("edge8", lens, [q_len, 1], num_heads=8, num_kv_heads=2, head_dim=d,
+                          block_size=16, num_blocks=1 + sum(-(-x // 16) for x in lens) + 4,
+                          seed=q_len + 7)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.05, 0.04, q_len)
+    out, ws = run_prefill_fp8(pa, w, t, kc, vc, 0.05, 0.04)
+    assert pa.device_status(ws)[0] == 0
+    ref = prefill_fp8_ref(oracle, w, t, kc, vc, 0.05, 0.04)
+    assert_close_to_oracle(out, ref, what=f"fp8 q_len {q_len} ctx {ctx} d {d}")
+
+
+@pytest.mark.parametrize("q_len,ctx,hq,hkv", [(256, 2000, 2, 1), (130, 700, 4, 2), (2, 5000, 2, 2)])
+def test_prefill_fp8_unit_split_over_many_ctas(cuda_lib, oracle, q_len, ctx, hq, hkv):
+    """Few key steps over a grid of one CTA per SM: units cut into pieces that
+    are merged in the kernel (the v_scale of each piece included)."""
+    pa = cuda_lib
+    lens = [ctx + q_len, 90]
+    w = wl.build_workload("split8", lens, [q_len, 1], num_heads=hq, num_kv_heads=hkv, head_dim=128,
+                          block_size=16, num_blocks=1 + sum(-(-x // 16) for x in lens) + 4,
+                          seed=q_len + ctx)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.03, 0.3, q_len + ctx)
+    for _ in range(2):
+        out, ws = run_prefill_fp8(pa, w, t, kc, vc, 0.03, 0.3)
+        assert pa.device_status(ws)[0] == 0
+    ref = prefill_fp8_ref(oracle, w, t, kc, vc, 0.03, 0.3)
+    assert_close_to_oracle(out, ref, what=f"fp8 split q_len {q_len} ctx {ctx}")
+
+
+def test_prefill_fp8_write_then_attend_full_size(cuda_lib, oracle):
+    """The 512-token chunk at context 3584 plus 63 decode rows over e4m3
+    caches: quantize all 575 new tokens through the slot mapping, then
+    attend; every row and head compared with the oracle."""
+    pa = cuda_lib
+    w = wl.mixed_chunked_prefill()
+    t = wl.make_tensors(w, device="cuda")
+    k_scale, v_scale = 2.0 ** -5, 0.0371
+    kc, vc = fp8_caches(w, t, k_scale, v_scale, 358)
+    slots = pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16,
+                                    w.num_blocks, w.total_q)
+    pa.reshape_and_cache_fp8(t.key, t.value, kc, vc, slots, k_scale, v_scale)
+    out, ws = run_prefill_fp8(pa, w, t, kc, vc, k_scale, v_scale)
+    assert pa.device_status(ws)[0] == 0
+    ref = prefill_fp8_ref(oracle, w, t, kc, vc, k_scale, v_scale)
+    assert_close_to_oracle(out, ref, what="fp8 mixed chunked prefill (every row)")
+
+
+def test_prefill_fp8_is_deterministic_and_rejects_bad_scales(cuda_lib):
+    pa = cuda_lib
+    w = wl.random_workload(359, num_seqs=5, max_len=600, num_heads=32, num_kv_heads=8,
+                           head_dim=128, max_q_len=300, prefill_fraction=0.6)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.05, 0.05, 359)
+    a, _ = run_prefill_fp8(pa, w, t, kc, vc, 0.05, 0.05)
+    b, _ = run_prefill_fp8(pa, w, t, kc, vc, 0.05, 0.05)
+    assert torch.equal(a, b)
+    for ks, vs in ((0.0, 1.0), (1.0, float("nan")), (-1.0, 1.0)):
+        with pytest.raises(pa.PAError):
+            run_prefill_fp8(pa, w, t, kc, vc, ks, vs)
