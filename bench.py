@@ -45,12 +45,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # only while that kernel's source is unchanged (sha256 prefix of its .cu file
 # when the counters were taken), else reported as null.
 PROFILED_TRAFFIC: dict = {
-    # 636.344832 MB read + 3.848704 MB written
-    "llama8b_decode_b64": {"bytes": 640193536, "src": "decode.cu",
-                           "src_sha": "bfa268418f2dac4c"},
-    # 939.966208 MB read + 5.458176 MB written
-    "prefix_shared_decode_b256": {"bytes": 945424384, "src": "decode_tc.cu",
-                                  "src_sha": "3987d8d08ae62a6a"},
+    # 636.349952 MB read + 3.460608 MB written
+    "llama8b_decode_b64": {"bytes": 639810560, "src": "decode.cu",
+                           "src_sha": "7d4d6d792b1d13d1"},
+    # 940.533760 MB read + 5.472000 MB written
+    "prefix_shared_decode_b256": {"bytes": 946005760, "src": "decode_tc.cu",
+                                  "src_sha": "f7d9cc97eaee6522"},
+    # prefill rows of the four-chunk batch alone: 878.280448 MB read + 18.357504 MB written
+    "multi_chunk_prefill": {"bytes": 896637952, "src": "prefill.cu",
+                            "src_sha": "1cc03e00de6c63a1"},
 }
 
 
@@ -95,12 +98,12 @@ def hbm_roofline(kernel, algo_bytes, seconds, traffic=None):
             "us_per_launch": round(seconds * 1e6, 2)}
 
 
-def tensor_roofline(kernel, flops, seconds):
+def tensor_roofline(kernel, flops, seconds, traffic=None):
     peak, src = measured_bf16_tflops()
     achieved = flops / seconds / 1e12
     return {"bound": "tensor", "kernel": kernel, "achieved": round(achieved, 2), "peak": peak,
             "peak_source": src, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": None, "algorithmic_flops_per_launch": int(flops),
+            "traffic": traffic, "algorithmic_flops_per_launch": int(flops),
             "us_per_launch": round(seconds * 1e6, 2)}
 
 
@@ -493,8 +496,8 @@ def extra_mixed(pa, name, dev, flush, reps=20, cpu=True):
            "prefill_gflop": round(flops / 1e9, 3),
            "prefill_fp8_only_us": round(s_pre8 * 1e6, 2),
            "prefill_fp8_tflops": round(flops / s_pre8 / 1e12, 2),
-           "roofline": tensor_roofline("prefill_tile_kernel (pa_prefill_varlen, prefill rows "
-                                       "alone)", flops, s_pre),
+           "roofline": tensor_roofline("prefill_kernel (pa_prefill_varlen, prefill rows alone)",
+                                       flops, s_pre, profiled_traffic(w.name)),
            "roofline_step": hbm_roofline("append_tokens + pa_prefill_varlen (whole step)",
                                          ab["step_bytes"], s_step)}
     if cpu:
