@@ -97,7 +97,7 @@ struct PrefillCfg {
   static constexpr int REQ_CACHE = 256;             // requests whose lengths are cached
   static constexpr int OFF_REQ = OFF_SEG + SEGS * SEG_INTS * 4;  // [3][REQ_CACHE] ints
   static constexpr int OFF_BAR = OFF_REQ + 3 * REQ_CACHE * 4;
-  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2 + 14 + 2 * NST + 2;
+  static constexpr int NBAR = 4 * NST + 12 + 2 * SEGS + 2 + 22 + 2 * NST + 2;
   // e4m3 cache: a step's K (or V) bytes land as 16-token blocks of head_dim
   // bytes in the upper half of the f16 stage they are converted into.
   static constexpr int RAW_BLOCK = 16 * D;
@@ -140,8 +140,8 @@ struct PBars {
   static constexpr int DRAIN = SYNC + 1;         // the MMA warp's last commit
   static constexpr int MFULL = DRAIN + 1;        // [2][5] staged partial O chunk landed
   static constexpr int MLFULL = MFULL + 10;      // [2] staged (m, l) records landed
-  static constexpr int MSYNC = MLFULL + 2;       // [2] the 4 warps of a slot
-  static constexpr int KRAW = MSYNC + 2;         // [NST] e4m3 K step landed (then converted)
+  static constexpr int MEMPTY = MLFULL + 2;      // [2][5] the slot's 4 warps have read a staged chunk
+  static constexpr int KRAW = MEMPTY + 10;       // [NST] e4m3 K step landed (then converted)
   static constexpr int VRAW = KRAW + NST;        // [NST] e4m3 V step landed
   static constexpr int QCONV = VRAW + NST;       // [2] Q of a slot converted to f16 (4 warps)
   static constexpr int COUNT = QCONV + 2;
@@ -370,7 +370,7 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
                                           const float* __restrict__ part_o, int c0, int c1, int own,
                                           int b, int i_row, bool issuer, float m_ref, float l_run,
                                           uint32_t tm_o, uint32_t area_q, uint32_t area_r,
-                                          uint32_t bar_full, uint32_t bar_ml, uint32_t bar_sync,
+                                          uint32_t bar_full, uint32_t bar_ml, uint32_t bar_empty,
                                           float o_scale, __nv_bfloat16* dst, bool write,
                                           int32_t* status, int cta) {
   using C = PrefillCfg<D>;
@@ -402,7 +402,6 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
       bulk_copy_g2s(ml_buf + k * 1024, part_ml + prec(remote(k), c0, b) * 256, 1024, bar_ml);
     for (int s = 0; s < min(C::MDATA, total); ++s) issue(s);
   }
-  uint32_t sync_phase = 0;
   auto wait_all = [&](uint32_t bar, uint32_t parity, int where) -> bool {
     const bool good = __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
     if (!good && lane == 0) record_error(status, PA_DEV_WAIT_TIMEOUT, cta, where);
@@ -454,14 +453,21 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
             v[4 * g + 2] = __uint_as_float(u.z);
             v[4 * g + 3] = __uint_as_float(u.w);
           }
-          // Every warp of the slot has read buffer s: it takes copy s + MDATA.
+          // This warp is done with buffer s; once all four are, it takes copy
+          // s + MDATA (only the issuing thread waits for that).
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_sync);
-          if (!(ok = wait_all(bar_sync, sync_phase++ & 1, 88))) break;
+          if (lane == 0) mbar_arrive(bar_empty + 8 * (s % C::MDATA));
+          int good = 1;
           if (issuer && s + C::MDATA < total) {
-            fence_proxy_async_smem();
-            issue(s + C::MDATA);
+            if (mbar_wait(bar_empty + 8 * (s % C::MDATA), (s / C::MDATA) & 1)) {
+              fence_proxy_async_smem();
+              issue(s + C::MDATA);
+            } else {
+              good = 0;
+              record_error(status, PA_DEV_WAIT_TIMEOUT, cta, 88);
+            }
           }
+          if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0)) break;
           ++s;
           ++k;
         }
@@ -526,7 +532,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       if ((k >= B::PFULL && k < B::PFULL + 2) || (k >= B::OFREE && k < B::OFREE + 2)) count = 4;
       if (k >= B::SEGFREE && k < B::SEGFREE + C::SEGS) count = 10;  // MMA, 8 softmax, V producer
       if (k == B::SYNC) count = 8;
-      if (k >= B::MSYNC && k < B::MSYNC + 2) count = 4;
+      if (k >= B::MEMPTY && k < B::MEMPTY + 10) count = 4;
       if (k >= B::QCONV && k < B::QCONV + 2) count = 4;
       mbar_init(bar(k), count);
     }
@@ -1017,24 +1023,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           tc_fence_after();
           const bool masked = key0 + C::BN - 1 > sg.ctx + sg.row0 || key0 + C::BN > sg.kv_end;
           const int nv = limit - key0 + 1;  // visible keys of this row in this step
-          // S_b row into registers; keys past this row's limit get -inf (their
-          // weight 2^-inf = 0); only a step on the diagonal or at the end of
-          // the keys has any.
-          auto load_s = [&](uint32_t (&sr)[C::BN]) {
-#pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) tmem_ld32_async(tm_s + c * 32, sr + 32 * c);
+          // S_b row, half a row (64 columns) at a time; keys past this row's
+          // limit get -inf (their weight 2^-inf = 0); only a step on the
+          // diagonal or at the end of the keys has any.
+          auto load_half = [&](int hf, uint32_t (&sr)[C::BN / 2]) {
+            tmem_ld32_async(tm_s + hf * 64, sr);
+            tmem_ld32_async(tm_s + hf * 64 + 32, sr + 32);
             tmem_wait_ld();
             if (masked) {
 #pragma unroll
-              for (int e = 0; e < C::BN; ++e) sr[e] = e < nv ? sr[e] : 0xff800000u;  // -inf
+              for (int e = 0; e < C::BN / 2; ++e) sr[e] = hf * 64 + e < nv ? sr[e] : 0xff800000u;  // -inf
             }
           };
           float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
-          uint32_t pk[C::BN / 2];
+          uint32_t pk[C::BN / 4];
           // Weights of one pair of columns: scale and shift (packed fp32),
-          // exponentiate, round to bf16 for the P.V product; l sums the fp32
-          // weights.
+          // exponentiate, round to 16 bits for the P.V product; l sums the
+          // fp32 weights.
           auto weights = [&](uint32_t s0, uint32_t s1, float m, int e) {
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)),
                                         make_float2(sl2, sl2), make_float2(-m, -m));
@@ -1043,55 +1049,40 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             pk[e / 2] = KV8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             ps4[(e / 2) % 4] = __fadd2_rn(ps4[(e / 2) % 4], make_float2(p0, p1));
           };
-          bool rescale = true;
+          // Pass 1: the row maximum; the reference moves (lazily: only when
+          // the maximum exceeds it by more than 2^8) before any weight.
+          float mx8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t sr[C::BN / 2];
+            load_half(hf, sr);
+#pragma unroll
+            for (int e = 0; e < C::BN / 2; e += 2)
+              mx8[(e / 2) % 8] = fmax3(mx8[(e / 2) % 8], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          }
+          const float m_tile = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+          const bool moved = m_tile > m_ref + kRescaleSlackP;
           float alpha = 1.f;
-          if (k > 0) {
-            // Speculative: weights against the current reference and the
-            // step's row maximum in one pass; kept unless some row's maximum
-            // exceeds its reference by more than 2^8 (rare after the first
-            // steps), in which case the step is redone below.
-            uint32_t sraw[C::BN];
-            load_s(sraw);
-            float mx8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < C::BN; e += 2) {
-              mx8[(e / 2) % 8] =
-                  fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
-              weights(sraw[e], sraw[e + 1], m_ref, e);
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            rescale = __any_sync(0xffffffffu, mx * sl2 > m_ref + kRescaleSlackP);
+          if (moved) {
+            alpha = fast_exp2(m_ref - m_tile);
+            l_run *= alpha;
+            m_ref = m_tile;
           }
-          if (rescale) {
-            // The row maximum first, then the weights against the new reference.
-            uint32_t sraw[C::BN];
-            load_s(sraw);
-            float mx8[8];
+          const bool rescale = __any_sync(0xffffffffu, moved);
+          // Pass 2: the weights; P_b of each half goes over S_b columns that
+          // have already been read (P_b: the first half of the S_b columns).
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t sr[C::BN / 2];
+            load_half(hf, sr);
 #pragma unroll
-            for (int e = 0; e < C::BN; e += 2)
-              mx8[(e / 2) % 8] =
-                  fmax3(mx8[(e / 2) % 8], __uint_as_float(sraw[e]), __uint_as_float(sraw[e + 1]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_tile = mx * sl2;
-            if (m_tile > m_ref + kRescaleSlackP) {
-              alpha = fast_exp2(m_ref - m_tile);
-              l_run *= alpha;
-              m_ref = m_tile;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) ps4[u] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < C::BN; e += 2) weights(sraw[e], sraw[e + 1], m_ref, e);
+            for (int e = 0; e < C::BN / 2; e += 2) weights(sr[e], sr[e + 1], m_ref, e);
+            tmem_st16_async(tm_s + hf * 32, pk);
+            tmem_st16_async(tm_s + hf * 32 + 16, pk + 16);
           }
-          // P_b over the first half of the S_b columns.
-#pragma unroll
-          for (int c = 0; c < C::BN / 32; ++c) tmem_st16_async(tm_s + c * 16, pk + 16 * c);
           const float2 ps = __fadd2_rn(__fadd2_rn(ps4[0], ps4[1]), __fadd2_rn(ps4[2], ps4[3]));
           l_run += ps.x + ps.y;
           if (rescale && k > 0) {  // (warp-uniform: the TMEM accesses are warp-wide)
@@ -1230,7 +1221,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           // segment: slot b's Q buffer and a K/V ring are free.
           ok = merge_staged<D>(a.part_ml, a.part_o, c0, c1, own, b, i_row, (warp & 3) == 0 && lane == 0,
                                m_ref, l_run, tm_o, q_s + b * C::QBYTES, b ? v_s : k_s,
-                               bar(B::MFULL + 5 * b), bar(B::MLFULL + b), bar(B::MSYNC + b),
+                               bar(B::MFULL + 5 * b), bar(B::MLFULL + b), bar(B::MEMPTY + 5 * b),
                                a.o_scale, dst, i_row < sg.rows, a.status, cta);
           if (!ok) break;
         } else {
