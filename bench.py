@@ -51,9 +51,9 @@ PROFILED_TRAFFIC: dict = {
     # 940.533760 MB read + 5.472000 MB written
     "prefix_shared_decode_b256": {"bytes": 946005760, "src": "decode_tc.cu",
                                   "src_sha": "f7d9cc97eaee6522"},
-    # prefill rows of the four-chunk batch alone: 878.280448 MB read + 18.357504 MB written
-    "multi_chunk_prefill": {"bytes": 896637952, "src": "prefill.cu",
-                            "src_sha": "1cc03e00de6c63a1"},
+    # prefill rows of the four-chunk batch: 907.697920 MB read + 15.792384 MB written
+    "multi_chunk_prefill": {"bytes": 923490304, "src": "prefill.cu",
+                            "src_sha": "49d8ba5101726682"},
 }
 
 
