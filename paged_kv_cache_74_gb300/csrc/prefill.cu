@@ -467,7 +467,7 @@ __device__ __noinline__ bool merge_staged(const float* __restrict__ part_ml,
               record_error(status, PA_DEV_WAIT_TIMEOUT, cta, 88);
             }
           }
-          if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0)) break;
+          if (!(ok = __all_sync(0xffffffffu, good) != 0)) break;
           ++s;
           ++k;
         }
@@ -618,11 +618,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       nsum += req_steps(p);
       usum += p.ntq;
     }
-#pragma unroll 1
-    for (int o = 16; o >= 1; o >>= 1) {
-      nsum += __shfl_xor_sync(0xffffffffu, nsum, o);
-      usum += __shfl_xor_sync(0xffffffffu, usum, o);
-    }
+    nsum = __reduce_add_sync(0xffffffffu, nsum);
+    usum = __reduce_add_sync(0xffffffffu, usum);
     const long long Cw = (kCostStep * nsum + kCostUnit * static_cast<long long>(usum)) * NP;
     const bool by_cost = div_ll(Cw, a.num_ctas) >= kCostStep + kCostUnit;
     const long long CT = by_cost ? kCostStep : 1, CS = by_cost ? kCostUnit : 0;
@@ -638,7 +635,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (*fail_flag) good = 0;
         else if (!mbar_wait(b, parity)) { give_up(where); good = 0; }
       }
-      return __shfl_sync(0xffffffffu, good, 0) != 0;
+      return __all_sync(0xffffffffu, good) != 0;
     };
     auto seg_slot = [&](int s) -> bool {  // ring slot of segment s is free again
       return s < C::SEGS || lane0_wait(bar(B::SEGFREE + s % C::SEGS), ((s / C::SEGS) - 1) & 1, 60);
@@ -653,10 +650,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       // (of one head pair) of the requests before it.
       int sbase = 0, ubase32 = 0;
       int r = -1;
+      // A chunk of 32 requests that ends before x0 is skipped with two warp
+      // reductions; inside the one that holds it, inclusive prefixes.
 #pragma unroll 1
       for (int rc = 0; rc < a.num_seqs && r < 0; rc += 32) {
         const PReq p = req_local(rc + lane);
         const int st = req_steps(p), nt = p.ntq;
+        const int ts = __reduce_add_sync(0xffffffffu, st), tu = __reduce_add_sync(0xffffffffu, nt);
+        if ((CT * (sbase + ts) + CS * (ubase32 + tu)) * NP <= x0) {  // past these 32 requests
+          sbase += ts;
+          ubase32 += tu;
+          continue;
+        }
         int is = st, iu = nt;
 #pragma unroll 1
         for (int o = 1; o < 32; o <<= 1) {
@@ -669,16 +674,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         // cost up to the end of request rc + lane
         const long long end = (CT * (sbase + is) + CS * (ubase32 + iu)) * NP;
-        const unsigned hit = __ballot_sync(0xffffffffu, end > x0);
-        if (hit) {
-          const int first = __ffs(hit) - 1;
-          sbase += __shfl_sync(0xffffffffu, is - st, first);
-          ubase32 += __shfl_sync(0xffffffffu, iu - nt, first);
-          r = rc + first;
-        } else {
-          sbase += __shfl_sync(0xffffffffu, is, 31);
-          ubase32 += __shfl_sync(0xffffffffu, iu, 31);
-        }
+        const int first = __ffs(__ballot_sync(0xffffffffu, end > x0)) - 1;
+        sbase += __shfl_sync(0xffffffffu, is - st, first);
+        ubase32 += __shfl_sync(0xffffffffu, iu - nt, first);
+        r = rc + first;
       }
       const long long base = (CT * sbase + CS * ubase32) * NP;
       const long long ubase = static_cast<long long>(ubase32) * NP;
@@ -821,7 +820,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint64_t policy = l2_policy_evict_first();
     if (lane == 0) tma_prefetch_desc(&vmap);
     auto warp_wait = [&](uint32_t b, uint32_t parity, int where) -> bool {
-      if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
+      if (*fail_flag) return false;  // one load by the whole warp: the same value
       const bool good = __all_sync(0xffffffffu, mbar_wait(b, parity) ? 1 : 0) != 0;
       if (!good && lane == 0) give_up(where);
       return good;
@@ -979,7 +978,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int sc = 0, oc = 0, g = 0, qn = 0;
     uint32_t sync_phase = 0;
     auto all_wait = [&](int k, uint32_t parity, int where) -> bool {
-      if (__shfl_sync(0xffffffffu, *fail_flag, 0)) return false;
+      if (*fail_flag) return false;  // one load by the whole warp: the same value
       const bool good = __all_sync(0xffffffffu, mbar_wait(bar(k), parity) ? 1 : 0) != 0;
       if (!good && lane == 0) give_up(where);
       return good;
