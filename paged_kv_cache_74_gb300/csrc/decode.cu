@@ -311,9 +311,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       int len, row;
       nb_sum += request_blocks(a, r, &len, &row);
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
-    const long long W = nb_sum * a.num_kv_heads;
+    const long long W = warp_sum_ll(nb_sum) * a.num_kv_heads;
     const long long lo = W > 0 ? range_lo(W, a.num_ctas, cta) : 0;
     const long long hi = W > 0 ? range_lo(W, a.num_ctas, cta + 1) : 0;
     if (lane == 0) *total_tiles = W;
@@ -337,6 +335,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const long long nt = r < a.num_seqs ? static_cast<long long>(request_blocks(a, r, &len, &row)) *
                                                   a.num_kv_heads
                                             : 0;
+        const long long chunk = warp_sum_ll(nt);
+        if (base + chunk <= lo) {  // tile `lo` lies past these 32 requests
+          base += chunk;
+          continue;
+        }
         long long incl = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

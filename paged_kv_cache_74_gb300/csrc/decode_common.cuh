@@ -47,6 +47,15 @@ __device__ __forceinline__ int request_blocks(const DecodeArgs& a, int r, int* s
   return blocks_from(a, r, a.seq_lens[r], q0, q1, seq_len, row);
 }
 
+// Sum over the warp of a non-negative per-lane value below 2^31, by two
+// 32-bit warp reductions of its 16-bit halves (a reduction is an order of
+// magnitude faster than a chain of shuffles here).
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+  const unsigned lo = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v) & 0xffffu);
+  const unsigned hi = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v >> 16));
+  return (static_cast<long long>(hi) << 16) + lo;
+}
+
 // Reports the rows request_blocks() rejects (done once, by CTA 0).
 __device__ void report_bad_rows(const DecodeArgs& a, int lane) {
   for (int r = lane; r < a.num_seqs; r += 32) {
