@@ -45,15 +45,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # only while that kernel's source is unchanged (sha256 prefix of its .cu file
 # when the counters were taken), else reported as null.
 PROFILED_TRAFFIC: dict = {
-    # 636.349952 MB read + 3.460608 MB written
-    "llama8b_decode_b64": {"bytes": 639810560, "src": "decode.cu",
-                           "src_sha": "7d4d6d792b1d13d1"},
+    # 636.339712 MB read + 3.599872 MB written
+    "llama8b_decode_b64": {"bytes": 639939584, "src": "decode.cu",
+                           "src_sha": "2818727373b9ecb4"},
     # 940.533760 MB read + 5.472000 MB written
     "prefix_shared_decode_b256": {"bytes": 946005760, "src": "decode_tc.cu",
                                   "src_sha": "f7d9cc97eaee6522"},
-    # prefill rows of the four-chunk batch: 907.697920 MB read + 15.792384 MB written
-    "multi_chunk_prefill": {"bytes": 923490304, "src": "prefill.cu",
-                            "src_sha": "49d8ba5101726682"},
+    # prefill rows of the four-chunk batch: 869.394688 MB read + 15.212544 MB written
+    "multi_chunk_prefill": {"bytes": 884607232, "src": "prefill.cu",
+                            "src_sha": "2c9ff3990fce3122"},
 }
 
 

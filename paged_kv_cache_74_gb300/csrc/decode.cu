@@ -61,6 +61,15 @@ namespace pa {
 namespace {
 
 constexpr float kNegBig = -1e30f;      // finite stand-in for -inf in running maxima
+
+// Order-preserving unsigned keys of floats (no NaN): larger float, larger key.
+__device__ __forceinline__ unsigned float_to_max_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float max_key_to_float(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 constexpr float kRescaleSlack = 8.0f;  // log2 units
 
 // Stage flags (written by the producer next to each ring stage).
@@ -819,11 +828,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const bool ok = tok0 + stok < seq_len && 2 * ft + (i & 1) < a.group;
         p[i] = ok ? sacc[i] * a.scale_log2 : -INFINITY;
       }
+      // The tile maximum of each head over the 8 lanes that share ft.  bf16
+      // token-major: a warp reduction of order-preserving keys per group of
+      // lanes (faster than a chain of shuffles there: 115.3 -> 113.4 us on
+      // the 8B batch); e4m3 and x-split: shuffles (the reduction measured
+      // 90.9 -> 104.9 us on e4m3, 437 -> 491 us on the x-split 70B batch).
       float tmax[2] = {fmaxf(p[0], p[2]), fmaxf(p[1], p[3])};
+      if constexpr (KV8 || XS) {
 #pragma unroll
-      for (int bb = 4; bb < 32; bb <<= 1) {
-        tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], bb));
-        tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], bb));
+        for (int bb = 4; bb < 32; bb <<= 1) {
+          tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], bb));
+          tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], bb));
+        }
+      } else {
+        const unsigned ftmask = 0x11111111u << ft;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          tmax[i] = max_key_to_float(__reduce_max_sync(ftmask, float_to_max_key(tmax[i])));
       }
       if (__any_sync(0xffffffffu,
                      tmax[0] > mh[0] + kRescaleSlack || tmax[1] > mh[1] + kRescaleSlack)) {
