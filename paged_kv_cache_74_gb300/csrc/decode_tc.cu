@@ -293,11 +293,8 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       nb_sum += (nbv + C::CB - 1) / C::CB;
       nreq += nbv > 0 ? 1 : 0;
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      nb_sum += __shfl_xor_sync(0xffffffffu, nb_sum, o);
-      nreq += __shfl_xor_sync(0xffffffffu, nreq, o);
-    }
+    nb_sum = warp_sum_ll(nb_sum);  // warp reductions: far faster than shuffle chains here
+    nreq = warp_sum_ll(nreq);
     const long long W = nb_sum * a.num_kv_heads;
     // Split by cost when every CTA's share spans at least one whole gap
     // between chunk starts (so no CTA's range is empty); else by chunks.
@@ -331,6 +328,12 @@ paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         const int nc = (req_nb(r) + C::CB - 1) / C::CB;
         const long long ct = nc > 0 ? a.num_kv_heads * (static_cast<long long>(cu_chunk) * nc + cu_seg) : 0;
         const long long nt = static_cast<long long>(nc) * a.num_kv_heads;
+        const long long tct = warp_sum_ll(ct);
+        if (cb + tct <= x) {  // x lies past these 32 requests
+          cb += tct;
+          chb += warp_sum_ll(nt);
+          continue;
+        }
         long long ic = ct, in = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
