@@ -48,9 +48,9 @@ PROFILED_TRAFFIC: dict = {
     # 636.339712 MB read + 3.599872 MB written
     "llama8b_decode_b64": {"bytes": 639939584, "src": "decode.cu",
                            "src_sha": "2818727373b9ecb4"},
-    # 940.533760 MB read + 5.472000 MB written
-    "prefix_shared_decode_b256": {"bytes": 946005760, "src": "decode_tc.cu",
-                                  "src_sha": "f7d9cc97eaee6522"},
+    # 940.190720 MB read + 5.581824 MB written
+    "prefix_shared_decode_b256": {"bytes": 945772544, "src": "decode_tc.cu",
+                                  "src_sha": "77528aa33e5a5c65"},
     # prefill rows of the four-chunk batch: 869.394688 MB read + 15.212544 MB written
     "multi_chunk_prefill": {"bytes": 884607232, "src": "prefill.cu",
                             "src_sha": "2c9ff3990fce3122"},
