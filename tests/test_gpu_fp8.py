@@ -388,3 +388,66 @@ def test_prefill_fp8_is_deterministic_and_rejects_bad_scales(cuda_lib):
     for ks, vs in ((0.0, 1.0), (1.0, float("nan")), (-1.0, 1.0)):
         with pytest.raises(pa.PAError):
             run_prefill_fp8(pa, w, t, kc, vc, ks, vs)
+
+
+def test_prefill_fp8_mixed_step_in_a_cuda_graph(cuda_lib):
+    """Slot mapping, the quantizing cache write and pa_prefill_varlen_fp8
+    captured in one CUDA graph (after an eager warm-up) replay to the eager
+    result bit for bit."""
+    pa = cuda_lib
+    w = wl.random_workload(360, num_seqs=6, max_len=500, num_heads=32, num_kv_heads=8,
+                           head_dim=128, max_q_len=200, prefill_fraction=0.5)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.04, 0.05, 360)
+    kc0, vc0 = kc.clone(), vc.clone()
+    ws = pa.new_workspace(pa.prefill_workspace_size(w.num_seqs, w.total_q, 32, 8, 128,
+                                                    w.max_seq_len), "cuda")
+    out = torch.empty_like(t.q)
+    slots = torch.empty(w.total_q, dtype=torch.int64, device="cuda")
+
+    def step():
+        pa.compute_slot_mapping(t.block_tables, t.query_start_loc, t.seq_lens, 16, w.num_blocks,
+                                w.total_q, out=slots)
+        pa.reshape_and_cache_fp8(t.key, t.value, kc, vc, slots, 0.04, 0.05)
+        pa.prefill_varlen_fp8(t.q, kc, vc, t.query_start_loc, t.seq_lens, t.block_tables,
+                              w.max_query_len, w.max_seq_len, w.scale, 0.04, 0.05, out=out,
+                              workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    kc.copy_(kc0)
+    vc.copy_(vc0)
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
+def test_prefill_fp8_bad_block_id_is_reported_not_dereferenced(cuda_lib, oracle):
+    """An out-of-range block id of one prefill chunk is reported in the status
+    record and read as zeros; the other requests' rows stay exact."""
+    pa = cuda_lib
+    w = wl.build_workload("bad8", [300, 90, 40], [200, 1, 30], num_heads=8, num_kv_heads=2,
+                          head_dim=128, block_size=16, num_blocks=40, seed=361)
+    t = wl.make_tensors(w, device="cuda")
+    kc, vc = fp8_caches(w, t, 0.05, 0.05, 361)
+    bt = t.block_tables.clone()
+    bt[0, 3] = w.num_blocks + 77
+    ws = pa.new_workspace(pa.prefill_workspace_size(3, w.total_q, 8, 2, 128, w.max_seq_len), "cuda")
+    out = pa.prefill_varlen_fp8(t.q, kc, vc, t.query_start_loc, t.seq_lens, bt, w.max_query_len,
+                                w.max_seq_len, w.scale, 0.05, 0.05, workspace=ws)
+    st = pa.device_status(ws)
+    assert st[0] == 2 and st[2] == w.num_blocks + 77
+    ref = oracle.prefill_varlen_fp8(bits(t.q), kc.cpu().numpy(), vc.cpu().numpy(),
+                                    w.query_start_loc, w.seq_lens, w.block_tables, w.scale,
+                                    0.05, 0.05)
+    rows = slice(int(w.query_start_loc[1]), int(w.query_start_loc[3]))
+    assert_close_to_oracle(out[rows], ref[rows], what="fp8: other requests")
