@@ -487,13 +487,24 @@ def extra_mixed(pa, name, dev, flush, reps=20, cpu=True):
     pcall8 = lambda: pa.prefill_varlen_fp8(q_p, kc8, vc8, qsl, sl_p, bt_p, mql, msl, w.scale,
                                            k_scale, v_scale, out=out_p, workspace=ws_p)
     s_pre8 = _time(pcall8, flush, reps)
-    del kc8, vc8
+    # The whole step over the e4m3 copy: quantizing write of the new tokens
+    # (at the slots the bf16 step computed) + pa_prefill_varlen_fp8.
+    out8 = torch.empty_like(t.q)
+
+    def step8():
+        pa.reshape_and_cache_fp8(t.key, t.value, kc8, vc8, slots, k_scale, v_scale)
+        pa.prefill_varlen_fp8(t.q, kc8, vc8, t.query_start_loc, t.seq_lens, t.block_tables,
+                              w.max_query_len, w.max_seq_len, w.scale, k_scale, v_scale, out=out8,
+                              workspace=ws)
+    s_step8 = _time(step8, flush, reps)
+    del kc8, vc8, out8
     res = {"us_per_step": round(s_step * 1e6, 2),
            "step": "append_tokens (all new tokens) + prefill_varlen",
            "step_kv_gbs": round(ab["step_bytes"] / s_step / 1e9, 2),
            "prefill_only_us": round(s_pre * 1e6, 2),
            "prefill_tflops": round(flops / s_pre / 1e12, 2),
            "prefill_gflop": round(flops / 1e9, 3),
+           "us_per_step_fp8": round(s_step8 * 1e6, 2),
            "prefill_fp8_only_us": round(s_pre8 * 1e6, 2),
            "prefill_fp8_tflops": round(flops / s_pre8 / 1e12, 2),
            "roofline": tensor_roofline("prefill_kernel (pa_prefill_varlen, prefill rows alone)",

@@ -431,7 +431,14 @@ size_t pa_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_
  * once every kernel enqueued before this call has completed, so its CTAs
  * fill the SMs the tiles leave free, and it completes only after the tile
  * kernel: work enqueued on `stream` after this call sees both results, as
- * for a single kernel.
+ * for a single kernel.  When the tile work is small (up to about 150 us of
+ * one SM's time per SM) and the decode rows run in the streaming decode
+ * kernel (up to 4 q heads per kv head) on every SM, the two kernels split
+ * the SMs from the batch's own sums: only as many tile CTAs as the tile
+ * work's share of the estimated SM time work, the others exit at once, and
+ * the decode rows go to the decode CTAs that start on the freed SMs.  The
+ * split depends only on the batch, so results stay the same from call to
+ * call.
  */
 pa_status pa_prefill_varlen(void* out, const void* q, const void* key_cache,
                             const void* value_cache, const int32_t* query_start_loc,

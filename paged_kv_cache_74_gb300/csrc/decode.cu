@@ -22,7 +22,10 @@
 //   whole (request, kv head) pairs, written straight to `out`, and at most
 //   two pieces of pairs shared with the neighbouring ranges; those are
 //   written as partials (m_j, l_j, O_j) and merged by the contributor that
-//   finishes last (an epoch-tagged counter per pair decides which).
+//   finishes last (an epoch-tagged counter per pair decides which).  Behind
+//   a small prefill tile batch of the same pa_prefill_varlen call
+//   (`tile_sms`), the ranges go only to the CTAs that start on the SMs the
+//   tile kernel leaves (tile_kernel_sms()); the rest find no work.
 // * One CTA serves every q head of a kv head, so each K/V byte is read from
 //   HBM once.  A producer warp reads block ids 32 at a time and issues one
 //   TMA tensor load per (block, kv head) tile of K and of V (16 tokens x
@@ -259,7 +262,10 @@ __device__ __forceinline__ uint32_t e8_offset(int t, int c) {
   return static_cast<uint32_t>(t * D + ((c ^ sw) * 16));
 }
 
-template <int D, int GMAX, bool KV8, bool XS>
+// MIX: the decode rows of a pa_prefill_varlen call that may split the SMs
+// with its tile kernel (DecodeArgs::tile_sms); a separate instantiation, so
+// that the plain decode's start-up stays as short as it is.
+template <int D, int GMAX, bool KV8, bool XS, bool MIX>
 __global__ void __launch_bounds__(DecodeCfg<D, GMAX, KV8, XS>::THREADS,
                                   DecodeCfg<D, GMAX, KV8, XS>::MINB)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -274,6 +280,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   SegInfo* seginfo = reinterpret_cast<SegInfo*>(smem + C::OFF_SEG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
   long long* total_tiles = reinterpret_cast<long long*>(smem + C::OFF_MISC + 8);
+  int* split_ctas = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // CTAs the tiles are split over
   const uint32_t ring_s = smem_u32(smem);
   const uint32_t full0 = smem_u32(smem + C::OFF_BAR);
   const uint32_t empty0 = full0 + 8 * C::STAGES;
@@ -321,8 +328,25 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       nb_sum += request_blocks(a, r, &len, &row);
     }
     const long long W = warp_sum_ll(nb_sum) * a.num_kv_heads;
-    const long long lo = W > 0 ? range_lo(W, a.num_ctas, cta) : 0;
-    const long long hi = W > 0 ? range_lo(W, a.num_ctas, cta + 1) : 0;
+    long long lo, hi;
+    if constexpr (MIX) {
+      // The tile kernel's cost (the call's prefill rows) sets how many CTAs
+      // take the decode rows.
+      long long tc_sum = 0;
+      for (int r = lane; r < a.num_seqs; r += 32) {
+        const TileReq p = tile_req(a.query_start_loc[r], a.query_start_loc[r + 1], a.seq_lens[r], row_limits(a));
+        tc_sum += kCostStep * tile_req_steps(p) + kCostUnit * p.ntq;
+      }
+      const long long Ct = warp_sum_ll(tc_sum) * a.num_kv_heads * ((a.group + 1) / 2);
+      const int nct =
+          decode_split_ctas(tile_kernel_sms(Ct, W, a.tile_sms, KV8), a.tile_sms, a.num_ctas, a.ctas_per_sm);
+      lo = W > 0 && cta < nct ? range_lo(W, nct, cta) : 0;
+      hi = W > 0 && cta < nct ? range_lo(W, nct, cta + 1) : 0;
+      if (lane == 0) *split_ctas = nct;
+    } else {
+      lo = W > 0 ? range_lo(W, a.num_ctas, cta) : 0;
+      hi = W > 0 ? range_lo(W, a.num_ctas, cta + 1) : 0;
+    }
     if (lane == 0) *total_tiles = W;
 
     int pos = 0;  // stage sequence number
@@ -578,8 +602,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       } else {
         const int pslot = e.kind == kTail ? 1 : 0;
         const long long W = *total_tiles;
-        const int c0 = cta_of_tile(W, a.num_ctas, e.t0);
-        const int c1 = cta_of_tile(W, a.num_ctas, e.t0 + e.nblk - 1);
+        const int nsplit = MIX ? *split_ctas : a.num_ctas;
+        const int c0 = cta_of_tile(W, nsplit, e.t0);
+        const int c1 = cta_of_tile(W, nsplit, e.t0 + e.nblk - 1);
         unsigned long long* counter = a.counters + static_cast<size_t>(e.r) * a.num_kv_heads + e.kvh;
         // If every other contributor has already counted (the usual case for
         // the CTA whose range ends inside the pair, at the end of its work),
@@ -1037,11 +1062,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-template <int D, int GMAX, bool KV8, bool XS>
+template <int D, int GMAX, bool KV8, bool XS, bool MIX = false>
 cudaError_t launch_decode_impl(const DecodeArgs& a, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t stream) {
   using C = DecodeCfg<D, GMAX, KV8, XS>;
-  auto* kernel = paged_decode_kernel<D, GMAX, KV8, XS>;
+  auto* kernel = paged_decode_kernel<D, GMAX, KV8, XS, MIX>;
   static bool attr_set[64] = {false};  // per device: set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1080,12 +1105,15 @@ int decode_ctas_per_sm(int head_dim, int group) {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, bool kv8, bool xsplit, cudaStream_t stream) {
   const int gmax = decode_gmax(a.group);
+  const bool mix = a.tile_sms > 0;  // built for head_dim 128 (the host splits the SMs only there)
 #define PA_DECODE_CASE(DD, GG)                                                      \
   if (head_dim == DD && gmax == GG)                                                 \
     return kv8 ? (xsplit ? launch_decode_impl<DD, GG, true, true>(a, kmap, vmap, stream)      \
-                         : launch_decode_impl<DD, GG, true, false>(a, kmap, vmap, stream))    \
+                  : mix    ? launch_decode_impl<DD, GG, true, false, DD == 128>(a, kmap, vmap, stream) \
+                           : launch_decode_impl<DD, GG, true, false>(a, kmap, vmap, stream))    \
                : (xsplit ? launch_decode_impl<DD, GG, false, true>(a, kmap, vmap, stream)     \
-                         : launch_decode_impl<DD, GG, false, false>(a, kmap, vmap, stream));
+                  : mix    ? launch_decode_impl<DD, GG, false, false, DD == 128>(a, kmap, vmap, stream) \
+                           : launch_decode_impl<DD, GG, false, false>(a, kmap, vmap, stream));
   PA_DECODE_CASE(128, 1) PA_DECODE_CASE(128, 2) PA_DECODE_CASE(128, 4)
   PA_DECODE_CASE(64, 1) PA_DECODE_CASE(64, 2) PA_DECODE_CASE(64, 4)
 #undef PA_DECODE_CASE

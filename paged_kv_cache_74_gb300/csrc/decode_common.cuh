@@ -27,17 +27,23 @@ constexpr int kTail = 2;   // begins a pair finished by later CTAs: partial slot
 // 16-token tiles of request r that the decode kernel processes (0 for rows that are
 // not decode rows, and for invalid lengths); also its length and q row.
 // `len` = seq_lens[r]; q0, q1 = query_start_loc[r], [r + 1] (when present).
+__device__ __forceinline__ RowLimits row_limits(const DecodeArgs& a) {
+  return RowLimits{a.max_query_len, a.max_seq_len, a.max_blocks_per_seq * a.block_size, a.total_q};
+}
+
 __device__ __forceinline__ int blocks_from(const DecodeArgs& a, int r, int len, int q0, int q1,
                                            int* seq_len, int* row) {
-  int rw = r;
-  if (a.query_start_loc != nullptr) {
-    if (q1 - q0 != 1) return 0;  // not a decode row
-    rw = q0;
-    if (rw < 0 || rw >= a.total_q) return 0;
+  if (a.query_start_loc != nullptr) {  // only decode rows (q_len == 1), at row q0
+    const int n = decode_row_tiles(q0, q1, len, row_limits(a));
+    if (n > 0) {
+      *seq_len = len;
+      *row = q0;
+    }
+    return n;
   }
   if (len < 1 || len > a.max_seq_len || len > a.max_blocks_per_seq * a.block_size) return 0;
   *seq_len = len;
-  *row = rw;
+  *row = r;
   return (len + kBlockSize - 1) / kBlockSize;
 }
 

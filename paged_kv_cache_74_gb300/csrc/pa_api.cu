@@ -383,7 +383,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t num_blocks, int32_t block_size, float scale,
                              const DecodeLayout& L, void* workspace, cudaStream_t stream,
-                             const KvFormat& kv = KvFormat(), bool after_prefill = false) {
+                             const KvFormat& kv = KvFormat(), bool after_prefill = false,
+                             int tile_sms = 0, int max_query_len = 0) {
   // The TMA views address the cache in 16-token tiles.
   const int num_tiles16 = num_blocks * (block_size / kBlockSize);
   const int group = num_heads / num_kv_heads;
@@ -439,6 +440,9 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.scale_log2 = scale * 1.4426950408889634f * kv.k_scale;
   a.v_scale = kv.v_scale;
   a.defer_griddep = after_prefill ? 1 : 0;
+  a.tile_sms = tile_sms;
+  a.ctas_per_sm = tile_sms > 0 ? static_cast<int>(L.num_ctas / tile_sms) : 0;
+  a.max_query_len = max_query_len;
   const cudaError_t err = tc ? launch_decode_tc(a, qmap, kmap, vmap, head_dim, kv.e4m3, stream)
                             : launch_decode(a, kmap, vmap, head_dim, kv.e4m3, kv.xsplit, stream);
   return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -846,6 +850,15 @@ pa_status prefill_varlen_impl(void* out, const void* q, const void* key_cache,
     p.epoch = next_epoch();
     p.scale_log2 = scale * kv.k_scale * 1.4426950408889634f;
     p.o_scale = kv.v_scale;
+    // Decode rows in the streaming decode kernel (head_dim 128), its grid
+    // exactly ctas-per-SM CTAs on every SM: the two kernels split the SMs between
+    // them (tile_kernel_sms()), so that the decode rows start at once on the
+    // SMs the tiles leave instead of after the tile CTAs.
+    const int group = num_heads / num_kv_heads;
+    const bool split_sms =
+        head_dim == 128 && !decode_uses_tc(head_dim, group) &&
+        L.num_ctas == static_cast<int64_t>(PL.num_ctas) * decode_ctas_per_sm(head_dim, group);
+    p.partition = split_sms ? 1 : 0;
     // Both kernels go on the caller's stream.  The tile kernel lets the
     // decode launch start once the kernels before this call are complete;
     // the decode CTAs then take the SMs the tiles leave free, and the decode
@@ -855,7 +868,7 @@ pa_status prefill_varlen_impl(void* out, const void* q, const void* key_cache,
     return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
                               seq_lens, query_start_loc, num_seqs, total_q, max_seq_len,
                               num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, L,
-                              workspace, cs, kv, true);
+                              workspace, cs, kv, true, split_sms ? PL.num_ctas : 0, max_query_len);
   }
   // Only decode rows: the decode kernel.
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,

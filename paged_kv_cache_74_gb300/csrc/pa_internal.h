@@ -57,6 +57,13 @@ struct DecodeArgs {
   // the tiles write, so the wait moves to the end of the CTA (the launch
   // then completes after the tile kernel, which keeps stream order).
   int defer_griddep;
+  // The tile kernel of the same pa_prefill_varlen call works on
+  // tile_kernel_sms() of its tile_sms CTAs (one per SM); the decode rows then
+  // go to this grid's first num_ctas - ctas_per_sm * that many CTAs, which
+  // start on the SMs the tile kernel leaves.  0: no such split.
+  int tile_sms;
+  int ctas_per_sm;
+  int max_query_len;                // of the call (the tile kernel's row checks)
 };
 
 // Launch `kernel` on `stream` with programmatic stream serialization: the
@@ -137,6 +144,10 @@ struct PrefillArgs {
   unsigned epoch;                   // distinct per call (never 0)
   float scale_log2;                 // softmax scale (* k_scale for e4m3) * log2(e)
   float o_scale;                    // 1, or v_scale for e4m3
+  // 1: the decode rows of the same call follow in the streaming decode
+  // kernel, which takes the SMs this grid leaves (tile_kernel_sms()); only
+  // that many CTAs work.  0: every CTA works.
+  int partition;
 };
 // Bytes of the prefill partial records (part_ml and part_o) for num_ctas CTAs.
 size_t prefill_partials_bytes(int num_ctas, int head_dim);

@@ -22,6 +22,11 @@
 //   of MMA steps whatever the mix of chunk lengths.  A unit cut by a range
 //   boundary is finished by whichever of its contributors counts last on
 //   an epoch-tagged counter: it merges the pieces' partials.
+// * A small tile batch with decode rows behind it (`partition`) is cut over
+//   fewer CTAs, tile_kernel_sms() of them, the tile work's share of the
+//   batch's estimated SM time; the other CTAs exit at once and leave their
+//   SMs to the decode CTAs of the same call, which then stream next to the
+//   tiles instead of after them.
 // * Per step and slot b: S_b = Q_b K^T (M = N = 128, K = head_dim) into TMEM
 //   columns [128 b, 128 b + 128); the softmax warps of slot b read S_b, write
 //   P_b = 2^(S_b * scale * log2 e - m) as bf16 over the first 64 of those
@@ -55,9 +60,6 @@ constexpr int kSegWhole = 0;            // the whole unit: bf16 output
 constexpr int kSegHead = 1;             // continues a unit begun by an earlier CTA: partial slot 0
 constexpr int kSegTail = 2;             // begins a unit finished by later CTAs: partial slot 1
 constexpr int kSegEnd = 3;              // no more work
-// Split costs (see the producer): a key step, and the start of a unit.
-constexpr long long kCostStep = 4;
-constexpr long long kCostUnit = 10;
 // How long a unit's first CTA waits for the unit's other pieces before it
 // publishes its own instead of merging them.
 constexpr unsigned long long kMergeWaitNs = 20000;
@@ -156,25 +158,15 @@ struct PSeg {
 };
 static_assert(sizeof(PSeg) == 64, "segment record");
 
-// A request's prefill rows (q_len > 1 and lengths in range), else ntq = 0.
-struct PReq {
-  int q0, q_len, seq_len, ctx, ntq;
-};
+using PReq = TileReq;
+
+__device__ __forceinline__ RowLimits row_limits(const PrefillArgs& a) {
+  return RowLimits{a.max_query_len, a.max_seq_len, a.max_blocks_per_seq * a.block_size, a.total_q};
+}
 
 // From request r's query_start_loc[r], [r + 1] and seq_lens[r].
 __device__ __forceinline__ PReq make_req(const PrefillArgs& a, int q0, int q1, int seq_len) {
-  PReq p{0, 0, 0, 0, 0};
-  const int q_len = q1 - q0;
-  if (q_len <= 1) return p;
-  if (q_len > seq_len || seq_len > a.max_seq_len || seq_len > a.max_blocks_per_seq * a.block_size ||
-      q_len > a.max_query_len || q0 < 0 || q0 + q_len > a.total_q)
-    return p;
-  p.q0 = q0;
-  p.q_len = q_len;
-  p.seq_len = seq_len;
-  p.ctx = seq_len - q_len;
-  p.ntq = (q_len + 127) / 128;
-  return p;
+  return tile_req(q0, q1, seq_len, row_limits(a));
 }
 
 __device__ __forceinline__ PReq prefill_req(const PrefillArgs& a, int r) {
@@ -192,12 +184,8 @@ __device__ __forceinline__ int unit_steps(const PReq& p, int u, int* row0, int* 
 }
 
 // Key steps of all query tiles of a request (one head pair): the sum of
-// unit_steps() over its tiles in closed form (every tile but the last ends
-// 128 rows after the one before it; the last ends at seq_len).
-__device__ __forceinline__ int req_steps(const PReq& p) {
-  if (p.ntq == 0) return 0;
-  return (p.ntq - 1) * p.ntq / 2 + (p.ntq - 1) * ((p.ctx + 127) / 128) + (p.seq_len + 127) / 128;
-}
+// unit_steps() over its tiles in closed form.
+__device__ __forceinline__ int req_steps(const PReq& p) { return tile_req_steps(p); }
 
 // Reports the prefill rows prefill_req() rejects (done once, by CTA 0).
 __device__ void report_bad_prefill_rows(const PrefillArgs& a, int lane) {
@@ -611,21 +599,41 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     };
     auto req_uniform = req_local;  // every lane reads the same entry
     // (Key steps and units of one head pair fit 32 bits; costs are 64-bit.)
-    int nsum = 0, usum = 0;
+    // With `partition`, also the decode rows' 16-token tiles (per kv head).
+    int nsum = 0, usum = 0, dsum = 0;
+    const RowLimits lim = row_limits(a);
 #pragma unroll 1
     for (int r = lane; r < a.num_seqs; r += 32) {
-      const PReq p = req_local(r);
+      int q0, q1, len;
+      if (r < C::REQ_CACHE) {
+        q0 = rq[r];
+        q1 = rq[C::REQ_CACHE + r];
+        len = rq[2 * C::REQ_CACHE + r];
+      } else {
+        q0 = __ldg(a.query_start_loc + r);
+        q1 = __ldg(a.query_start_loc + r + 1);
+        len = __ldg(a.seq_lens + r);
+      }
+      const PReq p = tile_req(q0, q1, len, lim);
       nsum += req_steps(p);
       usum += p.ntq;
+      if (a.partition) dsum += decode_row_tiles(q0, q1, len, lim);
     }
     nsum = __reduce_add_sync(0xffffffffu, nsum);
     usum = __reduce_add_sync(0xffffffffu, usum);
     const long long Cw = (kCostStep * nsum + kCostUnit * static_cast<long long>(usum)) * NP;
-    const bool by_cost = div_ll(Cw, a.num_ctas) >= kCostStep + kCostUnit;
+    // The CTAs that work: all, or (mixed batch) the share of the SMs the
+    // decode rows leave; the others exit at once.
+    const int nct = a.partition
+                        ? tile_kernel_sms(Cw, static_cast<long long>(__reduce_add_sync(0xffffffffu, dsum)) *
+                                                  a.num_kv_heads,
+                                          a.num_ctas, KV8)
+                        : a.num_ctas;
+    const bool by_cost = nct > 0 && div_ll(Cw, nct) >= kCostStep + kCostUnit;
     const long long CT = by_cost ? kCostStep : 1, CS = by_cost ? kCostUnit : 0;
     const long long Ctot = by_cost ? Cw : static_cast<long long>(nsum) * NP;
-    const long long x0 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta) : 0;
-    const long long x1 = Ctot > 0 ? range_lo(Ctot, a.num_ctas, cta + 1) : 0;
+    const long long x0 = Ctot > 0 && cta < nct ? range_lo(Ctot, nct, cta) : 0;
+    const long long x1 = Ctot > 0 && cta < nct ? range_lo(Ctot, nct, cta + 1) : 0;
     int seg = 0, g = 0;
     int nq[2] = {0, 0};
     bool ok = true;
@@ -737,8 +745,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           sg.kvh = kvh;
           sg.kind = (j0 == 0 && j1 == n_u) ? kSegWhole : (j0 > 0 ? kSegHead : kSegTail);
           sg.unit = static_cast<int>(ub + hp);
-          sg.c0 = cta_of_tile(Ctot, a.num_ctas, cb + CS);
-          sg.c1 = cta_of_tile(Ctot, a.num_ctas, cb + CS + CT * (n_u - 1));
+          sg.c0 = cta_of_tile(Ctot, nct, cb + CS);
+          sg.c1 = cta_of_tile(Ctot, nct, cb + CS + CT * (n_u - 1));
           segs[seg % C::SEGS] = sg;
           mbar_arrive(bar(B::SEGFULL + seg % C::SEGS));
         }

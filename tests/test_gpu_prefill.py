@@ -66,6 +66,37 @@ def test_prefill_tile_edges(cuda_lib, oracle, q_len, ctx):
     assert_close_to_oracle(out, ref, what=f"q_len {q_len} ctx {ctx}")
 
 
+@pytest.mark.parametrize("seed,n_pref,n_dec,dec_len", [
+    (241, 1, 120, 3000),  # decode rows dominate: the tiles keep a few SMs
+    (242, 6, 2, 64),      # tiles dominate: the decode rows go to one CTA
+    (243, 3, 40, 1500),   # in between
+])
+def test_mixed_batches_split_the_sms(cuda_lib, oracle, seed, n_pref, n_dec, dec_len):
+    """Mixed batches large enough for the decode grid to fill every SM, so
+    that the tile and decode kernels split the SMs between them, at several
+    ratios of tile to decode work; prefill chunks and decode rows
+    interleaved; every row against the oracle."""
+    pa = cuda_lib
+    rng = np.random.default_rng(seed)
+    pq = [int(x) for x in rng.integers(130, 300, n_pref)]
+    lens = [int(c) + q for c, q in zip(rng.integers(0, 900, n_pref), pq)]
+    lens += [int(x) for x in rng.integers(dec_len // 2, dec_len, n_dec)]
+    q_lens = pq + [1] * n_dec
+    order = rng.permutation(len(lens))
+    lens = [lens[i] for i in order]
+    q_lens = [q_lens[i] for i in order]
+    w = wl.build_workload("split", lens, q_lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                          block_size=16, num_blocks=sum(-(-x // 16) for x in lens) + 8, seed=seed)
+    t = wl.make_tensors(w, device="cuda", poison=True)
+    out, ws = run_prefill(pa, w, t)
+    assert pa.device_status(ws)[0] == 0
+    ref = oracle.prefill_varlen(bits(t.q), bits(t.key_cache), bits(t.value_cache),
+                                w.query_start_loc, w.seq_lens, w.block_tables, w.scale)
+    assert_close_to_oracle(out, ref, what=f"split {seed}")
+    again, _ = run_prefill(pa, w, t)
+    assert torch.equal(out, again)
+
+
 def test_prefill_nan_poison_does_not_change_output(cuda_lib):
     pa = cuda_lib
     w = wl.random_workload(207, num_seqs=4, max_len=400, num_heads=8, num_kv_heads=2,
