@@ -45,15 +45,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # only while that kernel's source is unchanged (sha256 prefix of its .cu file
 # when the counters were taken), else reported as null.
 PROFILED_TRAFFIC: dict = {
-    # 636.339712 MB read + 3.599872 MB written
-    "llama8b_decode_b64": {"bytes": 639939584, "src": "decode.cu",
-                           "src_sha": "2818727373b9ecb4"},
+    # 636.343808 MB read + 3.252736 MB written
+    "llama8b_decode_b64": {"bytes": 639596544, "src": "decode.cu",
+                           "src_sha": "76be29f7ab50b924"},
     # 940.190720 MB read + 5.581824 MB written
     "prefix_shared_decode_b256": {"bytes": 945772544, "src": "decode_tc.cu",
                                   "src_sha": "77528aa33e5a5c65"},
-    # prefill rows of the four-chunk batch: 869.394688 MB read + 15.212544 MB written
-    "multi_chunk_prefill": {"bytes": 884607232, "src": "prefill.cu",
-                            "src_sha": "2c9ff3990fce3122"},
+    # prefill rows of the four-chunk batch: 877.759744 MB read + 14.742016 MB written
+    "multi_chunk_prefill": {"bytes": 892501760, "src": "prefill.cu",
+                            "src_sha": "02e57917f8ebd2f1"},
 }
 
 
