@@ -92,10 +92,13 @@ struct DecodeCfg {
   static constexpr int MINB = 3;                               // CTAs per SM
   static constexpr int ELT = KV8 ? 1 : 2;                      // bytes per K/V element (e4m3 / bf16)
   static constexpr int KS = D / 16;                            // 16-wide steps of head_dim
-  static constexpr int TILE = kBlockSize * D * ELT;            // bytes of one (block, kv head) tile
-  // A multiple of NC (see below).  e4m3 tiles are half as large: twice as
-  // many fit, and the same bytes are in flight.
-  static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 ? 2 : 1);
+  // e4m3 units of two kv heads (8 q heads: GMAX 8): a tile holds both
+  // heads' 16 tokens, [token][kv head][head_dim] bytes, one copy for both.
+  static constexpr bool PAIR = KV8 && !XS && GMAX == 8;
+  static constexpr int TILE = kBlockSize * D * ELT * (PAIR ? 2 : 1);  // bytes of one K (or V) tile
+  // A multiple of NC (see below).  Plain e4m3 tiles are half as large:
+  // twice as many fit, and the same bytes are in flight.
+  static constexpr int STAGES = (D == 128 ? 8 : 16) * (KV8 && !PAIR ? 2 : 1);
   // shared memory carve-up (bytes)
   static constexpr int RING = STAGES * 2 * TILE;
   // The consumers hand every finished segment to an epilogue warp (partial
@@ -120,6 +123,7 @@ struct DecodeCfg {
   static_assert(SMEM <= 227 * 1024 && MINB * (SMEM + 1024) <= 228 * 1024,
                 "shared memory must allow MINB CTAs per SM");
   static_assert(GMAX <= 8 && NC == 2, "an m16n8k16 product serves at most 8 q heads");
+  static_assert(!PAIR || D == 128, "two-head e4m3 tiles: head_dim 128 (128-byte rows)");
   // Bulk-copy destinations (ring, q) 16-byte aligned; the segment records'
   // 64-bit fields 8-byte aligned.
   static_assert(RING % 1024 == 0 && OFF_HAND % 16 == 0 && OFF_Q % 16 == 0 && OFF_META % 8 == 0 &&
@@ -260,6 +264,12 @@ template <int D>
 __device__ __forceinline__ uint32_t e8_offset(int t, int c) {
   const int sw = D == 128 ? (t & 7) : ((t >> 1) & 3);
   return static_cast<uint32_t>(t * D + ((c ^ sw) * 16));
+}
+
+// Byte offset of 16-byte chunk c of row r of a 128-byte-swizzled tile of
+// 128-byte rows (a two-head e4m3 tile: row 2 t + h is token t of head h).
+__device__ __forceinline__ uint32_t e8_row_offset(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) * 16));
 }
 
 // MIX: the decode rows of a pa_prefill_varlen call that may split the SMs
@@ -514,9 +524,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   tma_load_5d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, 0, 0, row0 / 8, kvh, policy);
                   tma_load_5d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, 0, 0, row0 / 8, kvh,
                               policy);
-                } else {  // e4m3: swizzled 3-D view, one tile per copy
-                  tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kvh, row0, policy);
-                  tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kvh, row0, policy);
+                } else {  // e4m3: swizzled 3-D view, one tile (PAIR: two kv heads) per copy
+                  const int kh = C::PAIR ? 2 * kvh : kvh;
+                  tma_load_3d(ring_s + (2 * s) * C::TILE, &kmap, full, 0, kh, row0, policy);
+                  tma_load_3d(ring_s + (2 * s + 1) * C::TILE, &vmap, full, 0, kh, row0, policy);
                 }
               }
             } else {
@@ -816,7 +827,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       // ldmatrix: tokens 8 (mi % 2) .. + 7, head_dim chunk 2 ks + mi / 2.
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       const int ka_t = ((lane >> 3) & 1) * 8 + (lane & 7);
-      if constexpr (KV8) {
+      if constexpr (C::PAIR) {
+        // Two kv heads: S^T of each against all 8 q heads; a lane keeps the
+        // one its heads 2 ft, 2 ft + 1 belong to (kv head ft / 2).
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int kp = 0; kp < C::KS / 2; ++kp) {
+            uint32_t r8[4];
+            ldsm_x4(kt + e8_row_offset(2 * ka_t + hh, 2 * kp + (lane >> 4)), r8);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t af[4] = {e4m3x2_f16x2(r8[2 * h]), e4m3x2_f16x2(r8[2 * h + 1]),
+                                      e4m3x2_f16x2(r8[2 * h] >> 16), e4m3x2_f16x2(r8[2 * h + 1] >> 16)};
+              mma_16816_f16(s2[hh], af, qf[2 * kp + h][0], qf[2 * kp + h][1]);
+            }
+          }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sacc[i] = ft < 2 ? s2[0][i] : s2[1][i];
+      } else if constexpr (KV8) {
         // One ldmatrix covers two 16-wide steps of e4m3 head_dim: matrix mi
         // = tokens 8 (mi % 2) .., chunk 2 kp + mi / 2; a lane's register
         // holds elements 4 ft .. 4 ft + 3 of its token's chunk.
@@ -938,6 +968,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
             mma_16816_f16(om[2 * mp + h], af, pb0, pb1);
           }
         }
+      } else if constexpr (C::PAIR) {
+        // Two kv heads: O^T += V_h^T P_h^T for each, P_h^T the weights of
+        // kv head h's q heads (B operand column fg = q head: fg / 4 = h).
+        const uint32_t pq0[2] = {fg < 4 ? pb0 : 0u, fg < 4 ? 0u : pb0};
+        const uint32_t pq1[2] = {fg < 4 ? pb1 : 0u, fg < 4 ? 0u : pb1};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int mp = 0; mp < C::KS / 2; ++mp) {
+            uint32_t r8[4];
+            ldsm_x4_t(vt + e8_row_offset(2 * (8 * (va_m & 1) + va_r) + hh, 2 * mp + (va_m >> 1)), r8);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t lo = bytes_0213(r8[2 * h]), hi = bytes_0213(r8[2 * h + 1]);
+              uint32_t af[4] = {e4m3x2_f16x2(lo), e4m3x2_f16x2(lo >> 16), e4m3x2_f16x2(hi),
+                                e4m3x2_f16x2(hi >> 16)};
+              af[0] &= vm01;
+              af[1] &= vm01;
+              af[2] &= vm89;
+              af[3] &= vm89;
+              mma_16816_f16(om[2 * mp + h], af, pq0[hh], pq1[hh]);
+            }
+          }
       } else if constexpr (KV8) {
         // e4m3 V^T: matrix mi = tokens 8 (mi % 2) .., chunk 2 mp + mi / 2,
         // read transposed in 16-bit units; a lane's register holds (token
@@ -1104,6 +1157,9 @@ int decode_ctas_per_sm(int head_dim, int group) {
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, bool kv8, bool xsplit, cudaStream_t stream) {
+  // e4m3 units of two kv heads (8 q heads, head_dim 128): one instantiation.
+  if (kv8 && !xsplit && a.group == 8 && head_dim == 128 && a.tile_sms == 0)
+    return launch_decode_impl<128, 8, true, false>(a, kmap, vmap, stream);
   const int gmax = decode_gmax(a.group);
   const bool mix = a.tile_sms > 0;  // built for head_dim 128 (the host splits the SMs only there)
 #define PA_DECODE_CASE(DD, GG)                                                      \

@@ -68,15 +68,18 @@ bool decode_uses_tc(int head_dim, int group) {
 }
 
 int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group, int max_seq_len,
-                        int partition_tokens) {
+                        int partition_tokens, bool pair = false) {
   const int64_t upper = static_cast<int64_t>(num_kv_heads) * num_seqs *
                         ceil_div(max_seq_len, kBlockSize);  // tiles
   if (partition_tokens > 0) return std::max<int64_t>(1, (upper + partition_tokens / kBlockSize - 1) /
                                                                (partition_tokens / kBlockSize));
   int sms = sm_count_current_device();
   if (sms <= 0) sms = 148;
+  // (pair: the streaming decode over units of two kv heads, group = 2 x 4)
   const int64_t resident =
-      static_cast<int64_t>(sms) * (decode_uses_tc(head_dim, group) ? 1 : decode_ctas_per_sm(head_dim, group));
+      static_cast<int64_t>(sms) * (pair ? decode_ctas_per_sm(head_dim, group / 2)
+                                        : decode_uses_tc(head_dim, group) ? 1
+                                                                          : decode_ctas_per_sm(head_dim, group));
   return std::max<int64_t>(1, std::min(resident, (upper + kMinTilesPerCta - 1) / kMinTilesPerCta));
 }
 
@@ -87,7 +90,7 @@ int64_t decode_num_ctas(int num_seqs, int num_kv_heads, int head_dim, int group,
 // 8 token rows are free of bank conflicts; `plain`: rows unswizzled (the
 // prefill's converter reads whole rows).
 bool make_cache_map_e4m3(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
-                         int head_dim, bool plain = false) {
+                         int head_dim, bool plain = false, int heads_per_box = 1) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
@@ -95,16 +98,20 @@ bool make_cache_map_e4m3(CUtensorMap* map, const void* cache, int num_blocks, in
                               static_cast<cuuint64_t>(num_blocks) * kBlockSize};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim),
                                  static_cast<cuuint64_t>(num_kv_heads) * head_dim};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), static_cast<cuuint32_t>(heads_per_box),
+                             static_cast<cuuint32_t>(kBlockSize)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
+  const int row_bytes = head_dim * heads_per_box;  // contiguous bytes of one token in the box
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              plain ? CU_TENSOR_MAP_SWIZZLE_NONE
                    : (head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
-             // A row is head_dim bytes: a larger L2 promotion would fetch the
-             // next kv head's row too (a third more DRAM traffic, measured).
-             head_dim == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
+             // A larger L2 promotion than the box's row would fetch the next
+             // kv head's row too (a third more DRAM traffic, measured).
+             row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : (row_bytes == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                  : CU_TENSOR_MAP_L2_PROMOTION_L2_64B),
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -278,11 +285,11 @@ struct DecodeLayout {
 // Workspace: status record | per-(request, kv head) counters |
 // per-CTA partial (m, l) | per-CTA partial O.
 DecodeLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                           int max_seq_len, int partition_tokens) {
+                           int max_seq_len, int partition_tokens, bool pair = false) {
   DecodeLayout L;
   const int group = num_heads / num_kv_heads;
   L.num_ctas = decode_num_ctas(num_seqs, num_kv_heads, head_dim, group, max_seq_len,
-                               partition_tokens);
+                               partition_tokens, pair);
   size_t off = kWorkspaceHeader;
   L.counters_offset = off;
   off = align_up(off + static_cast<size_t>(num_seqs) * num_kv_heads * 8, 256);
@@ -373,8 +380,17 @@ pa_status check_decode_args(const void* out, const void* q, const void* key_cach
 struct KvFormat {
   bool e4m3 = false;
   bool xsplit = false;  // K [blocks, kv heads, d / 8, block, 8], V [blocks, kv heads, d, block]
+  bool pair = false;    // e4m3 streaming decode: work units of two kv heads, one copy for both
   float k_scale = 1.f, v_scale = 1.f;
 };
+
+// The e4m3 decode reads two kv heads per copy (4 KB per 16-token tile at
+// head_dim 128 instead of 2 KB): a unit is then two kv heads and their 8 q
+// heads.  Copies of 2 KB stream at about half the bytes per second of 4 KB
+// ones at the same bytes in flight.
+bool decode_fp8_pairs(int head_dim, int num_heads, int num_kv_heads) {
+  return head_dim == 128 && num_kv_heads % 2 == 0 && num_heads == 4 * num_kv_heads;
+}
 
 pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, const void* value_cache,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -392,6 +408,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   // x-split: units of up to 4 q heads (see xsplit_heads_per_unit).
   const int unit_heads = kv.xsplit ? xsplit_heads_per_unit(group) : group;
   const int kv_div = group / unit_heads;
+  const bool pair = kv.pair && kv.e4m3 && !kv.xsplit && !tc && decode_fp8_pairs(head_dim, num_heads, num_kv_heads);
+  if (kv.pair && !pair) return PA_ERR_INVALID;
   CUtensorMap kmap, vmap, qmap;
   if (kv.xsplit && kv.e4m3) {
     if (!make_xsplit8_k_map(&kmap, key_cache, num_blocks, num_kv_heads, head_dim, block_size) ||
@@ -409,8 +427,10 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
         !make_kv_group_map(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim))
       return PA_ERR_CUDA;
   } else if ((tc && !make_q_group_map(&qmap, q, total_q, num_heads, head_dim, group)) ||
-             !make_cache_map_e4m3(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim) ||
-             !make_cache_map_e4m3(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim)) {
+             !make_cache_map_e4m3(&kmap, key_cache, num_tiles16, num_kv_heads, head_dim, false,
+                                  pair ? 2 : 1) ||
+             !make_cache_map_e4m3(&vmap, value_cache, num_tiles16, num_kv_heads, head_dim, false,
+                                  pair ? 2 : 1)) {
     return PA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -427,8 +447,8 @@ pa_status launch_decode_rows(void* out, const void* q, const void* key_cache, co
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_seqs = num_seqs;
   a.num_heads = num_heads;
-  a.num_kv_heads = num_kv_heads * kv_div;
-  a.group = unit_heads;
+  a.num_kv_heads = pair ? num_kv_heads / 2 : num_kv_heads * kv_div;
+  a.group = pair ? 2 * unit_heads : unit_heads;
   a.kv_div = kv_div;
   a.num_ctas = static_cast<int>(L.num_ctas);
   a.max_seq_len = max_seq_len;
@@ -599,10 +619,16 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
   // into several work units (more pair counters, smaller partials).
   const int units = num_kv_heads * (num_heads / num_kv_heads /
                                     xsplit_heads_per_unit(num_heads / num_kv_heads));
-  return std::max(
+  size_t total = std::max(
       decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
           .total,
       decode_layout(num_seqs, num_heads, units, head_dim, max_seq_len, partition_tokens).total);
+  // ... or the e4m3 decode's units of two kv heads (larger partials).
+  if (decode_fp8_pairs(head_dim, num_heads, num_kv_heads))
+    total = std::max(total, decode_layout(num_seqs, num_heads, num_kv_heads / 2, head_dim, max_seq_len,
+                                          partition_tokens, true)
+                                .total);
+  return total;
 }
 
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
@@ -644,13 +670,15 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const v
     return PA_ERR_INVALID;
   if (partition_tokens < 0 || partition_tokens % kBlockSize != 0) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
-  const DecodeLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len,
-                                       partition_tokens);
+  const bool pair = decode_fp8_pairs(head_dim, num_heads, num_kv_heads);
+  const DecodeLayout L = decode_layout(num_seqs, num_heads, pair ? num_kv_heads / 2 : num_kv_heads,
+                                       head_dim, max_seq_len, partition_tokens, pair);
   if (L.num_ctas > kMaxDecodeCtas) return PA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_INVALID;
   KvFormat kv;
   kv.e4m3 = true;
+  kv.pair = pair;
   kv.k_scale = k_scale;
   kv.v_scale = v_scale;
   return launch_decode_rows(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,

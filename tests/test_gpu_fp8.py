@@ -59,6 +59,8 @@ FP8_SWEEP = [
     (128, 32, 8, 900, 7, 16, 311), (128, 8, 8, 300, 9, 16, 312), (128, 16, 8, 1500, 4, 32, 313),
     (64, 8, 2, 700, 6, 16, 314), (64, 4, 4, 120, 10, 64, 315), (64, 2, 2, 2000, 3, 16, 316),
     (128, 4, 1, 257, 5, 16, 317),
+    # 4 q heads per kv head, an even number of kv heads: units of two kv heads
+    (128, 8, 2, 700, 5, 64, 319), (128, 16, 4, 450, 6, 32, 322),
     # 5 to 16 q heads per kv head: the tensor-core decode with converted K/V
     (128, 64, 8, 1100, 6, 16, 340), (128, 16, 1, 700, 5, 32, 341), (64, 40, 8, 900, 4, 16, 342),
     (128, 48, 4, 400, 9, 64, 343), (64, 16, 2, 130, 7, 16, 344),
