@@ -306,9 +306,11 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* key_cache,
  * results as pa_decode otherwise.  The products run on the tensor cores in
  * f16: e4m3 K and V convert to f16 exactly; q and the softmax weights are
  * rounded to f16 (q saturates at +-65504).  Up to 4 q heads per kv head the
- * warp-level products read the e4m3 bytes directly; from 5 to 16 the
- * tcgen05 decode converts each landed 128-token chunk (K into tensor
- * memory, V into shared memory) before its MMAs.
+ * warp-level products read the e4m3 bytes directly (at head_dim 128 with
+ * exactly 4 q heads per kv head and an even num_kv_heads, one work unit
+ * takes two kv heads, whose 16-token tiles arrive in one copy); from 5 to
+ * 16 the tcgen05 decode converts each landed 128-token chunk (K into
+ * tensor memory, V into shared memory) before its MMAs.
  * k_scale and v_scale finite and > 0 (else PA_ERR_INVALID).
  */
 pa_status pa_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,

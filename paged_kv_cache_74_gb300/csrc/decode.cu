@@ -30,7 +30,10 @@
 //   HBM once.  A producer warp reads block ids 32 at a time and issues one
 //   TMA tensor load per (block, kv head) tile of K and of V (16 tokens x
 //   head_dim, 4 KB at head_dim 128 in bf16) into an 8-stage ring (16
-//   stages of the half-size e4m3 tiles) guarded by mbarriers, writes each stage's block index and flags next to it, and
+//   stages of the half-size e4m3 tiles; at head_dim 128 with 4 q heads per
+//   kv head an e4m3 unit is two kv heads, 8 q heads, whose tiles come in
+//   one 4 KB copy: copies of 2 KB stream at about half the bytes per
+//   second of 4 KB ones at the same bytes in flight) guarded by mbarriers, writes each stage's block index and flags next to it, and
 //   prefetches each segment's q with a bulk copy into a double buffer.
 // * Two consumer warps take alternate stages.  A warp computes S^T = K q^T
 //   (16 tokens x 8 columns of q heads, padding heads zero) and
