@@ -13,19 +13,19 @@ namespace {
 
 // 64-bit division, through 32-bit unsigned division when both operands fit
 // (a 64-bit division is a long instruction sequence).
-__device__ __forceinline__ long long div_ll(long long a, long long b) {
+__host__ __device__ __forceinline__ long long div_ll(long long a, long long b) {
   if (((a | b) >> 31) == 0) return static_cast<unsigned>(a) / static_cast<unsigned>(b);
   return a / b;
 }
 
 // Equal split of W tiles over C CTAs: CTA c owns [range_lo(c), range_lo(c+1)).
-__device__ __forceinline__ long long range_lo(long long W, int C, int c) {
+__host__ __device__ __forceinline__ long long range_lo(long long W, int C, int c) {
   const long long q = div_ll(W, C), rem = W - q * C;
   return static_cast<long long>(c) * q + (c < rem ? c : rem);
 }
 
 // The CTA whose range holds tile t (0 <= t < W).
-__device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
+__host__ __device__ __forceinline__ int cta_of_tile(long long W, int C, long long t) {
   const long long q = div_ll(W, C), rem = W - q * C;
   const long long big = rem * (q + 1);
   if (t < big) return static_cast<int>(div_ll(t, q + 1));
@@ -44,7 +44,7 @@ struct TileReq {
 };
 
 // From query_start_loc[r], [r + 1] and seq_lens[r] of request r.
-__device__ __forceinline__ TileReq tile_req(int q0, int q1, int seq_len, const RowLimits& l) {
+__host__ __device__ __forceinline__ TileReq tile_req(int q0, int q1, int seq_len, const RowLimits& l) {
   TileReq p{0, 0, 0, 0, 0};
   const int q_len = q1 - q0;
   if (q_len <= 1) return p;
@@ -61,14 +61,14 @@ __device__ __forceinline__ TileReq tile_req(int q0, int q1, int seq_len, const R
 
 // 128-key steps of all 128-row query tiles of a request (one head pair): the
 // last tile ends at seq_len, every other one 128 rows before the next.
-__device__ __forceinline__ int tile_req_steps(const TileReq& p) {
+__host__ __device__ __forceinline__ int tile_req_steps(const TileReq& p) {
   if (p.ntq == 0) return 0;
   return (p.ntq - 1) * p.ntq / 2 + (p.ntq - 1) * ((p.ctx + 127) / 128) + (p.seq_len + 127) / 128;
 }
 
 // 16-token tiles (per kv head) of a decode row (q_len == 1, lengths in
 // range), else 0.
-__device__ __forceinline__ int decode_row_tiles(int q0, int q1, int seq_len, const RowLimits& l) {
+__host__ __device__ __forceinline__ int decode_row_tiles(int q0, int q1, int seq_len, const RowLimits& l) {
   if (q1 - q0 != 1 || q0 < 0 || q0 >= l.total_q) return 0;
   if (seq_len < 1 || seq_len > l.max_seq_len || seq_len > l.max_tokens) return 0;
   return (seq_len + kBlockSize - 1) / kBlockSize;
@@ -106,7 +106,7 @@ constexpr long long kSplitMaxTileNsPerSm = 150000;
 // work.  num_sms: no split (every tile CTA works, then the decode rows take
 // every SM); 0: no tile work.  Both kernels compute it from the same batch
 // sums.
-__device__ __forceinline__ int tile_kernel_sms(long long tile_cost, long long decode_tiles, int num_sms,
+__host__ __device__ __forceinline__ int tile_kernel_sms(long long tile_cost, long long decode_tiles, int num_sms,
                                                bool e4m3) {
   if (tile_cost <= 0) return 0;
   const long long t = tile_cost * (e4m3 ? kTileNsPerCost8 : kTileNsPerCost);
@@ -118,7 +118,7 @@ __device__ __forceinline__ int tile_kernel_sms(long long tile_cost, long long de
 
 // CTAs of a decode grid of num_ctas (ctas_per_sm on each of num_sms SMs)
 // that take the decode rows when the tile kernel keeps tile_sms SMs.
-__device__ __forceinline__ int decode_split_ctas(int tile_sms, int num_sms, int num_ctas, int ctas_per_sm) {
+__host__ __device__ __forceinline__ int decode_split_ctas(int tile_sms, int num_sms, int num_ctas, int ctas_per_sm) {
   if (tile_sms <= 0 || tile_sms >= num_sms) return num_ctas;
   return num_ctas - ctas_per_sm * tile_sms;
 }
