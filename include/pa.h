@@ -210,8 +210,10 @@ pa_status pa_map_to_kernel_blocks(int32_t* kernel_tables, const int32_t* block_t
 
 /*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
- * sizes: the status record, one 8-byte counter per (request, kv head) and
- * two partial records (m, l, O) per CTA of the decode grid.  The same
+ * sizes: the status record, one 8-byte counter per (request, work unit) and
+ * two partial records (m, l, O) per CTA of the decode grid; the size covers
+ * every unit layout the decode entry points use for these sizes (one kv
+ * head, a share of one for the x-split layout, two for the e4m3 decode).  The same
  * partition_tokens must be passed to pa_decode, on the same device (the
  * default grid size depends on its SM count).  No part of the workspace
  * needs initialising (the counters carry a per-call tag), and a call leaves
